@@ -1,0 +1,153 @@
+"""ctypes wrapper around the CPU oracle (qmm_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
+CPU-baseline leg of bench.py, never by the product package.  It shares no
+code with the CUDA library.
+
+Types follow the library numbering: 0 = Q8_0, 1 = Q4_K, 2 = Q6_K.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+Q8_0, Q4_K, Q6_K = 0, 1, 2
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210}
+BLOCK_WEIGHTS = {Q8_0: 32, Q4_K: 256, Q6_K: 256}
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        L.oracle_half_to_float.restype = ctypes.c_float
+        L.oracle_half_to_float.argtypes = [ctypes.c_uint16]
+        L.oracle_unpack_q8_0.argtypes = [P, P, P]
+        L.oracle_pack_q8_0.argtypes = [ctypes.c_uint16, P, P]
+        L.oracle_unpack_q4_k.argtypes = [P, P, P, P, P, P]
+        L.oracle_pack_q4_k.argtypes = [ctypes.c_uint16, ctypes.c_uint16, P, P, P, P]
+        L.oracle_unpack_q6_k.argtypes = [P, P, P, P]
+        L.oracle_pack_q6_k.argtypes = [ctypes.c_uint16, P, P, P]
+        L.oracle_dequant.argtypes = [ctypes.c_int, P, i64, P]
+        L.oracle_quantize_act.argtypes = [P, i64, i64, P, P, P]
+        L.oracle_qmm.argtypes = [ctypes.c_int, P, i64, i64, P, i64, P, P, ctypes.c_int]
+        L.oracle_max_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
+
+
+def half_to_float(bits: int) -> float:
+    return float(lib().oracle_half_to_float(int(bits) & 0xFFFF))
+
+
+# --- single-block pack / unpack --------------------------------------------
+
+def unpack_q8_0(blk):
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    d = np.zeros(1, np.uint16)
+    q = np.zeros(32, np.int8)
+    lib().oracle_unpack_q8_0(_p(blk), _p(d), _p(q))
+    return int(d[0]), q
+
+
+def pack_q8_0(d_bits, q):
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    out = np.zeros(34, np.uint8)
+    lib().oracle_pack_q8_0(int(d_bits), _p(q), _p(out))
+    return out
+
+
+def unpack_q4_k(blk):
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    d = np.zeros(1, np.uint16)
+    dm = np.zeros(1, np.uint16)
+    sc = np.zeros(8, np.uint8)
+    m = np.zeros(8, np.uint8)
+    q = np.zeros(256, np.uint8)
+    lib().oracle_unpack_q4_k(_p(blk), _p(d), _p(dm), _p(sc), _p(m), _p(q))
+    return int(d[0]), int(dm[0]), sc, m, q
+
+
+def pack_q4_k(d_bits, dmin_bits, sc, m, q):
+    sc = np.ascontiguousarray(sc, dtype=np.uint8)
+    m = np.ascontiguousarray(m, dtype=np.uint8)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    out = np.zeros(144, np.uint8)
+    lib().oracle_pack_q4_k(int(d_bits), int(dmin_bits), _p(sc), _p(m), _p(q), _p(out))
+    return out
+
+
+def unpack_q6_k(blk):
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    d = np.zeros(1, np.uint16)
+    sc = np.zeros(16, np.int8)
+    q = np.zeros(256, np.uint8)
+    lib().oracle_unpack_q6_k(_p(blk), _p(d), _p(sc), _p(q))
+    return int(d[0]), sc, q
+
+
+def pack_q6_k(d_bits, sc, q):
+    sc = np.ascontiguousarray(sc, dtype=np.int8)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    out = np.zeros(210, np.uint8)
+    lib().oracle_pack_q6_k(int(d_bits), _p(sc), _p(q), _p(out))
+    return out
+
+
+# --- whole-tensor operations -----------------------------------------------
+
+def dequant(qtype: int, blocks, n_elems: int) -> np.ndarray:
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)
+    out = np.empty(n_elems, np.float32)
+    rc = lib().oracle_dequant(int(qtype), _p(blocks), int(n_elems), _p(out))
+    if rc:
+        raise ValueError(f"oracle_dequant failed: {rc}")
+    return out
+
+
+def quantize_act(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None]
+    M, K = x.shape
+    q = np.empty((M, K), np.int8)
+    d = np.empty((M, K // 32), np.float32)
+    s = np.empty((M, K // 32), np.int32)
+    rc = lib().oracle_quantize_act(_p(x), M, K, _p(q), _p(d), _p(s))
+    if rc:
+        raise ValueError(f"oracle_quantize_act failed: {rc}")
+    return q, d, s
+
+
+def qmm(qtype: int, W, N: int, K: int, x, nthreads: int = 0):
+    """Return (y, A): y[M,N] in f64 and the bound scale A = sum_k |w x^|."""
+    W = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None]
+    M = x.shape[0]
+    assert x.shape[1] == K
+    need = N * (K // BLOCK_WEIGHTS[qtype]) * BLOCK_BYTES[qtype]
+    assert W.size >= need, (W.size, need)
+    y = np.empty((M, N), np.float64)
+    A = np.empty((M, N), np.float64)
+    nt = nthreads if nthreads > 0 else max(1, os.cpu_count() or 1)
+    rc = lib().oracle_qmm(int(qtype), _p(W), int(N), int(K), _p(x), int(M), _p(y), _p(A), int(nt))
+    if rc:
+        raise ValueError(f"oracle_qmm failed: {rc}")
+    return y, A

@@ -1,0 +1,337 @@
+"""Pins for the CPU oracle: checks against facts fixed outside the oracle
+(IEEE binary16 via numpy, hand-worked blocks, closed forms, brute-force f64
+dense products built from the fields), so a dropped term, a wrong sign or
+index, or a transposed operand in the oracle fails one of them."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_fixture(name):
+    rows = {}
+    ws = []
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "w":
+                ws.append((int(vals[0]), vals[1], vals[2] if len(vals) > 2 else None))
+            else:
+                rows[key] = vals
+    return rows, ws
+
+
+# ---------------------------------------------------------------- binary16
+
+def test_half_to_float_exhaustive():
+    lib = O.lib()
+    bits = np.arange(65536, dtype=np.uint32)
+    want = bits.astype(np.uint16).view(np.float16).astype(np.float32)
+    got = np.array([lib.oracle_half_to_float(int(b)) for b in bits], np.float32)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+# ---------------------------------------------------------- golden blocks
+
+def test_golden_q4_k_block():
+    rows, ws = _read_fixture("q4_k_block.txt")
+    blk = np.frombuffer(bytes.fromhex(rows["header"][0] + rows["qs"][0]), np.uint8)
+    assert blk.size == 144
+    d, dm, sc, m, q = O.unpack_q4_k(blk)
+    assert d == 0x3C00 and dm == 0x3800
+    assert list(sc) == [int(v) for v in rows["sc"]]
+    assert list(m) == [int(v) for v in rows["m"]]
+    w = O.dequant(O.Q4_K, blk, 256)
+    for p, qv, wv in ws:
+        assert q[p] == int(qv), p
+        assert w[p] == np.float32(float(wv)), (p, w[p], wv)
+
+
+def test_golden_q6_k_block():
+    rows, ws = _read_fixture("q6_k_block.txt")
+    ql = bytes.fromhex(rows["ql"][0])
+    qh = bytes([0xE4] * 64)
+    blk = np.frombuffer(ql + qh + bytes.fromhex(rows["scales"][0]) + bytes.fromhex(rows["d"][0]), np.uint8)
+    assert blk.size == 210
+    d, sc, q = O.unpack_q6_k(blk)
+    assert d == 0x3400
+    assert list(sc) == list(range(-8, 8))
+    w = O.dequant(O.Q6_K, blk, 256)
+    for p, qv, wv in ws:
+        assert q[p] == int(qv), p
+        want = np.float32(float(wv))
+        assert w[p] == want and np.signbit(w[p]) == np.signbit(want), (p, w[p], wv)
+
+
+def test_golden_q8_0_block():
+    rows, ws = _read_fixture("q8_0_block.txt")
+    qv = np.array([int(v) for v in rows["q"]], np.int8)
+    blk = np.frombuffer(bytes.fromhex(rows["d"][0]) + qv.tobytes(), np.uint8)
+    d, q = O.unpack_q8_0(blk)
+    assert d == 0x2E66 and np.array_equal(q, qv)
+    w = O.dequant(O.Q8_0, blk, 32)
+    for p, wv, _ in ws:
+        assert w[p] == np.float32(float(wv)), (p, w[p], wv)
+
+
+# ------------------------------------------------------------- round trips
+
+def test_roundtrip_q8_0():
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        db = int(rng.integers(0, 65536))
+        q = rng.integers(-128, 128, 32).astype(np.int8)
+        d2, q2 = O.unpack_q8_0(O.pack_q8_0(db, q))
+        assert d2 == db and np.array_equal(q2, q)
+
+
+def test_roundtrip_q4_k_all_scale_values():
+    rng = np.random.default_rng(2)
+    # every value 0..63 in every scale and min slot
+    for v in range(64):
+        sc = np.full(8, v, np.uint8)
+        m = np.full(8, 63 - v, np.uint8)
+        q = rng.integers(0, 16, 256).astype(np.uint8)
+        d, dm, sc2, m2, q2 = O.unpack_q4_k(O.pack_q4_k(0x1234, 0xABCD, sc, m, q))
+        assert (d, dm) == (0x1234, 0xABCD)
+        assert np.array_equal(sc2, sc) and np.array_equal(m2, m) and np.array_equal(q2, q)
+    for _ in range(100):
+        sc = rng.integers(0, 64, 8).astype(np.uint8)
+        m = rng.integers(0, 64, 8).astype(np.uint8)
+        q = rng.integers(0, 16, 256).astype(np.uint8)
+        _, _, sc2, m2, q2 = O.unpack_q4_k(O.pack_q4_k(0, 0, sc, m, q))
+        assert np.array_equal(sc2, sc) and np.array_equal(m2, m) and np.array_equal(q2, q)
+
+
+def test_roundtrip_q6_k():
+    rng = np.random.default_rng(3)
+    for _ in range(100):
+        sc = rng.integers(-128, 128, 16).astype(np.int8)
+        q = rng.integers(0, 64, 256).astype(np.uint8)
+        db = int(rng.integers(0, 65536))
+        d2, sc2, q2 = O.unpack_q6_k(O.pack_q6_k(db, sc, q))
+        assert d2 == db and np.array_equal(sc2, sc) and np.array_equal(q2, q)
+    for v in (0, 31, 32, 63):
+        q = np.full(256, v, np.uint8)
+        _, _, q2 = O.unpack_q6_k(O.pack_q6_k(0, np.zeros(16, np.int8), q))
+        assert np.array_equal(q2, q)
+
+
+def test_synth_bytes_unpack_to_uniform_fields():
+    """The generator's uniform bytes give fields over their whole ranges."""
+    blk = synth.weights(synth.Q4_K, 64, 256, seed=5).reshape(-1, 144)
+    scs, ms, qs = [], [], []
+    for b in blk:
+        _, _, sc, m, q = O.unpack_q4_k(b)
+        scs += list(sc); ms += list(m); qs += list(q)
+    assert min(scs) == 0 and max(scs) == 63 and min(ms) == 0 and max(ms) == 63
+    assert set(qs) == set(range(16))
+    blk = synth.weights(synth.Q6_K, 64, 256, seed=6).reshape(-1, 210)
+    allq, allsc = [], []
+    for b in blk:
+        _, sc, q = O.unpack_q6_k(b)
+        allq += list(q); allsc += list(sc)
+    assert set(allq) == set(range(64))
+    assert min(allsc) == -32 and max(allsc) == 31
+
+
+# -------------------------------------------------------- hand-worked cases
+
+def test_q4_k_zero_quants_give_minus_dmin_m():
+    sc = np.arange(8, dtype=np.uint8) * 7
+    m = np.array([0, 1, 2, 3, 60, 61, 62, 63], np.uint8)
+    blk = O.pack_q4_k(0x3C00, 0x2E66, sc, m, np.zeros(256, np.uint8))
+    w = O.dequant(O.Q4_K, blk, 256)
+    dmin = np.float32(np.uint16(0x2E66).view(np.float16))
+    for j in range(8):
+        want = np.float32(0.0) * np.float32(0) - dmin * np.float32(m[j])
+        assert np.all(w[32 * j:32 * j + 32] == want)
+
+
+def test_q4_k_unit_scale_is_identity():
+    rng = np.random.default_rng(4)
+    q = rng.integers(0, 16, 256).astype(np.uint8)
+    blk = O.pack_q4_k(0x3C00, 0x0000, np.ones(8, np.uint8), np.zeros(8, np.uint8), q)
+    assert np.array_equal(O.dequant(O.Q4_K, blk, 256), q.astype(np.float32))
+
+
+def test_q6_k_q32_is_zero():
+    sc = np.arange(-8, 8, dtype=np.int8)
+    blk = O.pack_q6_k(0x3C00, sc, np.full(256, 32, np.uint8))
+    assert np.all(O.dequant(O.Q6_K, blk, 256) == 0)
+    x = synth.activations(2, 256, seed=9)
+    y, A = O.qmm(O.Q6_K, blk, 1, 256, x)
+    assert np.all(y == 0) and np.all(A == 0)
+
+
+def test_q8_0_unit_scale_gives_exact_integer_dot():
+    rng = np.random.default_rng(7)
+    N, K, M = 5, 512, 3
+    qw = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    W = np.concatenate([O.pack_q8_0(0x3C00, qw[n, 32 * b:32 * b + 32])
+                        for n in range(N) for b in range(K // 32)])
+    xi = rng.integers(-127, 128, (M, K)).astype(np.int64)
+    xi[:, ::32] = 127  # amax = 127 in every block, so d = 1 and q = x exactly
+    y, _ = O.qmm(O.Q8_0, W, N, K, xi.astype(np.float32))
+    assert np.array_equal(y, (xi @ qw.astype(np.int64).T).astype(np.float64))
+
+
+def test_subnormal_and_signed_zero_scales():
+    q = np.arange(-16, 16, dtype=np.int8)
+    w = O.dequant(O.Q8_0, O.pack_q8_0(0x0001, q), 32)   # 2^-24
+    assert np.array_equal(w, q.astype(np.float32) * np.float32(2.0 ** -24))
+    w = O.dequant(O.Q8_0, O.pack_q8_0(0x8000, q), 32)   # -0
+    assert np.all(w == 0) and np.array_equal(np.signbit(w), q >= 0)   # -0 * 0 = -0
+
+
+# ------------------------------------------------------------- quantiser
+
+def test_quantizer_closed_forms():
+    amax = np.float32(3.0)
+    k = np.arange(-15, 17, dtype=np.int32)
+    k[0] = 127
+    d = np.float32(amax / np.float32(127.0))
+    x = (k.astype(np.float32) * d).astype(np.float32)
+    x[0] = amax
+    q, dd, s = O.quantize_act(x)
+    assert dd[0, 0] == d
+    # x = k*d rounds back to k (the relative error of k*d*(1/d) is far below 0.5/k)
+    assert np.array_equal(q[0].astype(np.int32), k)
+    assert s[0, 0] == k.sum()
+
+
+def test_quantizer_ties_round_away_from_zero():
+    x = np.zeros(32, np.float32)
+    x[0] = 127.0   # d = 1, inv = 1
+    x[1:6] = [2.5, -2.5, 0.5, -0.5, 126.5]
+    q, d, s = O.quantize_act(x)
+    assert d[0, 0] == 1.0
+    assert list(q[0, :6]) == [127, 3, -3, 1, -1, 127]
+    assert s[0, 0] == 127 + 3 - 3 + 1 - 1 + 127
+
+
+def test_quantizer_zero_block_and_bounds():
+    x = synth.activations(4, 256, seed=11, outlier_frac=0.05)
+    x[1, 32:64] = 0
+    q, d, s = O.quantize_act(x)
+    assert d[1, 1] == 0 and np.all(q[1, 32:64] == 0) and s[1, 1] == 0
+    assert np.all(np.abs(q.astype(np.int32)) <= 127)
+    blocks = np.abs(x).reshape(4, 8, 32)
+    am = blocks.argmax(axis=2)
+    qb = q.reshape(4, 8, 32)
+    for r in range(4):
+        for b in range(8):
+            if d[r, b] != 0:
+                assert abs(int(qb[r, b, am[r, b]])) == 127
+    assert np.array_equal(s, q.reshape(4, 8, 32).astype(np.int32).sum(axis=2))
+
+
+# ------------------------------------------- qmm against brute-force dense
+
+def _q4_k_fields(rng, N, K):
+    nb = K // 256
+    f = dict(d=rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16),
+             dm=rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16),
+             sc=rng.integers(0, 64, (N, nb, 8)).astype(np.uint8),
+             m=rng.integers(0, 64, (N, nb, 8)).astype(np.uint8),
+             q=rng.integers(0, 16, (N, nb, 256)).astype(np.uint8))
+    W = np.concatenate([O.pack_q4_k(f["d"][n, b], f["dm"][n, b], f["sc"][n, b], f["m"][n, b], f["q"][n, b])
+                        for n in range(N) for b in range(nb)])
+    d = f["d"].view(np.float16).astype(np.float64)
+    dm = f["dm"].view(np.float16).astype(np.float64)
+    Wd = (d[:, :, None] * np.repeat(f["sc"], 32, axis=2) * f["q"]
+          - dm[:, :, None] * np.repeat(f["m"], 32, axis=2)).reshape(N, K)
+    return W, Wd
+
+
+def _q6_k_fields(rng, N, K):
+    nb = K // 256
+    dbits = rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16)
+    sc = rng.integers(-128, 128, (N, nb, 16)).astype(np.int8)
+    q = rng.integers(0, 64, (N, nb, 256)).astype(np.uint8)
+    W = np.concatenate([O.pack_q6_k(dbits[n, b], sc[n, b], q[n, b]) for n in range(N) for b in range(nb)])
+    d = dbits.view(np.float16).astype(np.float64)
+    Wd = (d[:, :, None] * np.repeat(sc.astype(np.float64), 16, axis=2)
+          * (q.astype(np.float64) - 32)).reshape(N, K)
+    return W, Wd
+
+
+def _q8_0_fields(rng, N, K):
+    nb = K // 32
+    dbits = rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16)
+    q = rng.integers(-127, 128, (N, nb, 32)).astype(np.int8)
+    W = np.concatenate([O.pack_q8_0(dbits[n, b], q[n, b]) for n in range(N) for b in range(nb)])
+    Wd = (dbits.view(np.float16).astype(np.float64)[:, :, None] * q).reshape(N, K)
+    return W, Wd
+
+
+@pytest.mark.parametrize("qtype,make", [(O.Q4_K, _q4_k_fields), (O.Q6_K, _q6_k_fields),
+                                        (O.Q8_0, _q8_0_fields)])
+@pytest.mark.parametrize("K", [256, 512])
+def test_qmm_matches_dense_f64(qtype, make, K):
+    rng = np.random.default_rng(100 + qtype + K)
+    N, M = 7, 3
+    W, Wd = make(rng, N, K)
+    # integer activations with amax 127 per block quantise exactly (d = 1)
+    xi = rng.integers(-127, 128, (M, K)).astype(np.float64)
+    xi[:, 5::32] = -127
+    # a power-of-two scale per row keeps the quantisation exact: x = 2^e * int
+    scale = np.array([1.0, 0.25, 8.0])[:, None]
+    x = (xi * scale).astype(np.float32)
+    y, A = O.qmm(qtype, W, N, K, x)
+    yd = (xi * scale) @ Wd.T
+    Ad = np.abs(xi * scale) @ np.abs(Wd).T
+    np.testing.assert_allclose(y, yd, rtol=1e-12, atol=1e-12 * np.abs(yd).max())
+    # A uses the fp32-rounded weights: agreement to fp32 rounding of w
+    np.testing.assert_allclose(A, Ad, rtol=1e-6)
+    assert np.all(np.abs(y) <= A * (1 + 1e-9))
+
+
+def test_qmm_linear_in_weight_scale():
+    rng = np.random.default_rng(12)
+    N, K = 4, 256
+    q = rng.integers(-127, 128, (N, K // 32, 32)).astype(np.int8)
+    W1 = np.concatenate([O.pack_q8_0(0x2C00, q[n, b]) for n in range(N) for b in range(K // 32)])
+    W2 = np.concatenate([O.pack_q8_0(0x3000, q[n, b]) for n in range(N) for b in range(K // 32)])
+    x = synth.activations(2, K, seed=13)
+    y1, _ = O.qmm(O.Q8_0, W1, N, K, x)
+    y2, _ = O.qmm(O.Q8_0, W2, N, K, x)
+    np.testing.assert_array_equal(2 * y1, y2)   # 0x3000 = 2 * 0x2C00 exactly
+
+
+def test_q4_k_unit_scale_is_textbook_int_matmul():
+    rng = np.random.default_rng(14)
+    N, K, M = 3, 512, 2
+    q = rng.integers(0, 16, (N, K // 256, 256)).astype(np.uint8)
+    W = np.concatenate([O.pack_q4_k(0x3C00, 0x3C00, np.ones(8, np.uint8), np.zeros(8, np.uint8), q[n, b])
+                        for n in range(N) for b in range(K // 256)])
+    x = synth.activations(M, K, seed=15)
+    xq, xd, _ = O.quantize_act(x)
+    y, _ = O.qmm(O.Q4_K, W, N, K, x)
+    qk = q.reshape(N, K).astype(np.int64)
+    want = np.zeros((M, N))
+    for b in range(K // 32):
+        I = xq[:, 32 * b:32 * b + 32].astype(np.int64) @ qk[:, 32 * b:32 * b + 32].T
+        want += xd[:, b:b + 1].astype(np.float64) * I
+    np.testing.assert_allclose(y, want, rtol=1e-13)
+
+
+def test_planted_mistake_is_caught():
+    """A plausible oracle mistake (swapping the two Q4_K nibble halves) breaks
+    the golden-block pin: the pins are sensitive to layout errors."""
+    rows, ws = _read_fixture("q4_k_block.txt")
+    blk = np.frombuffer(bytes.fromhex(rows["header"][0] + rows["qs"][0]), np.uint8).copy()
+    qs = blk[16:]
+    blk[16:] = ((qs & 15) << 4) | (qs >> 4)   # the mistake, applied to the input
+    _, _, _, _, q = O.unpack_q4_k(blk)
+    assert any(q[p] != int(qv) for p, qv, _ in ws)
