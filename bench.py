@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized-weight matmul hot path on GB300.
+
+One step = one M=1 decode pass over every Q4_K/Q6_K GEMV workload:
+  * Llama-3.2-1B-shaped Q4_K projections (2048->2048, 2048->512, 2048->8192,
+    8192->2048),
+  * the Q6_K lm_head 2048->128256,
+  * a Qwen3-14B-shaped Q4_K_M layer (q, k, v[Q6_K], o, gate, up, down[Q6_K]),
+each call going through the public C ABI (`qmm`: activation quantiser +
+decode GEMV).  `value` is the step's weight bytes / device time (GB/s); the
+447 MB of weights per step exceed the 129 MB L2, so every matrix is re-read
+from HBM.  The same run also times:
+  * every matrix alone over rotating copies (>= 4x L2) -> per-matrix GB/s,
+  * the Q4_K prefill GEMM at M=512 (Mistral-7B MLP up and down) -> TOPS,
+  * the dominant kernel (the Q6_K lm_head GEMV) for the roofline object,
+  * the end-to-end step with host buffers (x copied in, y copied out),
+  * the CPU oracle on a bounded sample (cpu_baseline).
+
+--impl reference times the CPU oracle (plain C, f64 accumulation) on the host
+cores instead, on a bounded sample of the same workload.
+
+Weights and activations are seeded synthetic data with the value
+distributions of the workloads (synth.py); no model files are used.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def decode_workload():
+    mats = []
+    for cfg in (1, 2, 3):
+        for idx, (name, qtype, K, N) in enumerate(synth.CONFIGS[cfg]["mats"]):
+            mats.append(dict(cfg=cfg, idx=idx, name=f"cfg{cfg}:{name}", qtype=qtype, K=K, N=N,
+                             bytes=synth.matrix_bytes(qtype, N, K)))
+    return mats
+
+
+WORKLOAD_NAME = ("decode M=1: Llama-3.2-1B Q4_K projections + Q6_K lm_head 2048x128256 + "
+                 "Qwen3-14B Q4_K_M layer (q,k,v,o,gate,up,down)")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d.get("hbm_gbs", 6800.0), bf16=d.get("bf16_tflops", 1900.0),
+                    bf16_sust=d.get("bf16_tflops_sustained", 1700.0), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
+
+
+def load_traffic(kernel_file):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    import hashlib
+    summ = os.path.join(ROOT, "profiles", "gemv_q6k_lm_head_k2048_n128256.txt")
+    if not os.path.exists(summ):
+        return None
+    vals = {}
+    with open(summ) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    src = open(os.path.join(ROOT, "mat_mul_gb300", "csrc", kernel_file), "rb").read()
+    if vals.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def _oracle_pass(mats, frac, nthreads):
+    import oracle
+    nbytes, secs = 0, 0.0
+    for m in mats:
+        rows = max(1, int(m["N"] * frac))
+        W = synth.weights(m["qtype"], rows, m["K"], seed=m["cfg"] * 1000 + m["idx"])
+        x = synth.config_activations(m["cfg"], 1, m["K"])
+        t0 = time.perf_counter()
+        oracle.qmm(m["qtype"], W, rows, m["K"], x, nthreads=nthreads)
+        secs += time.perf_counter() - t0
+        nbytes += rows * synth.row_bytes(m["qtype"], m["K"])
+    return nbytes, secs
+
+
+def oracle_rate(mats, seconds, nthreads):
+    """Time the CPU oracle on row samples of every matrix, the sample grown
+    until it takes about `seconds`; return (GB/s, description of the sample)."""
+    import oracle
+    oracle.lib()
+    total = sum(m["bytes"] for m in mats)
+    frac = 1.0 / 8192
+    while True:
+        nbytes, secs = _oracle_pass(mats, frac, nthreads)
+        if secs >= seconds or frac >= 1.0:
+            break
+        grow = 4.0 if secs < seconds / 8 else seconds / max(secs, 1e-6) * 1.05
+        frac = min(1.0, frac * grow)
+    return nbytes / secs / 1e9, (f"{frac:.4%} of the rows of every matrix: {nbytes / 1e6:.1f} MB "
+                                 f"of weights in {secs:.1f} s, M=1")
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.lib()
+    cores = len(os.sched_getaffinity(0))
+    mats = decode_workload()
+    total = sum(m["bytes"] for m in mats)
+    # each step: the oracle over a fixed row sample of every matrix (~2 s)
+    rate_gbs, _ = oracle_rate(mats, 1.0, cores)
+    frac = min(1.0, 2.0 * rate_gbs * 1e9 / total)
+    samples = []
+    for m in mats:
+        rows = max(1, int(m["N"] * frac))
+        W = synth.weights(m["qtype"], rows, m["K"], seed=m["cfg"] * 1000 + m["idx"])
+        x = synth.config_activations(m["cfg"], 1, m["K"])
+        samples.append((m, rows, W, x))
+    step_bytes = sum(rows * synth.row_bytes(m["qtype"], m["K"]) for m, rows, _, _ in samples)
+
+    def step():
+        for m, rows, W, x in samples:
+            oracle.qmm(m["qtype"], W, rows, m["K"], x, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = step_bytes / dt / 1e9
+    sample = f"{frac:.4%} of the rows of every matrix per step ({step_bytes / 1e6:.2f} MB of weights)"
+    line = {
+        "impl": "reference", "metric": "Q4_K/Q6_K GEMV weight GB/s at M=1 (decode step)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "M": 1, "weight_bytes_per_full_step": total,
+                   "l2": "inputs larger than L2 (sampled rows on CPU)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+
+    import mat_mul_gb300 as q
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q.load()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream()
+
+    mats = decode_workload()
+    step_bytes = sum(m["bytes"] for m in mats)
+    for m in mats:
+        W = synth.config_weights(m["cfg"], m["idx"])
+        m["W"] = torch.from_numpy(W).to(dev)
+        m["x_host"] = torch.from_numpy(synth.config_activations(m["cfg"], 1, m["K"])).pin_memory()
+        m["x"] = m["x_host"].to(dev)
+        m["y"] = torch.empty((1, m["N"]), dtype=torch.float32, device=dev)
+        m["y_host"] = torch.empty((1, m["N"]), dtype=torch.float32).pin_memory()
+
+    def step():
+        for m in mats:
+            q.qmm(m["qtype"], m["W"], m["N"], m["K"], m["x"], y=m["y"], stream=stream)
+
+    def step_e2e():
+        for m in mats:
+            m["x"].copy_(m["x_host"], non_blocking=True)
+            q.qmm(m["qtype"], m["W"], m["N"], m["K"], m["x"], y=m["y"], stream=stream)
+            m["y_host"].copy_(m["y"], non_blocking=True)
+
+    def capture(fn):
+        with torch.cuda.stream(stream):
+            fn()  # allocates the workspace of this stream outside the capture
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def timed(graph, steps, warmup, sampler=None):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                graph.replay()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        ctx = sampler if sampler else _Null()
+        with ctx:
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(steps):
+                    graph.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        if dist:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    launches_per_step = 2 * len(mats)
+
+    # ---- headline: the decode step, weights resident
+    g_step = capture(step)
+    sampler = ClockSampler(dev.index)
+    ms = timed(g_step, args.steps, args.warmup, sampler)
+    clocks = sampler.summary()
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    status = q.qmm_device_status(stream)
+    assert status == 0, f"device status {status}"
+
+    # ---- end to end: x copied in and y copied out every call
+    g_e2e = capture(step_e2e)
+    ms_e2e = timed(g_e2e, args.steps, args.warmup)
+    h2d = sum(m["K"] * 4 for m in mats)
+    d2h = sum(m["N"] * 4 for m in mats)
+    e2e_value = world * step_bytes / (ms_e2e * 1e-3) / 1e9
+    del g_e2e, g_step
+
+    detail = []
+    roof = None
+    gemm = None
+    cpu = None
+    if rank == 0 and not args.quick:
+        # ---- every matrix alone, over rotating copies >= 4x L2
+        for m in mats:
+            ncopy = max(2, -(-4 * L2_BYTES // m["bytes"]))
+            ncopy = min(ncopy, 2048)
+            copies = [m["W"]] + [m["W"].clone() for _ in range(ncopy - 1)]
+            calls = max(ncopy, 64)
+
+            def one(copies=copies, m=m, calls=calls):
+                for i in range(calls):
+                    q.qmm(m["qtype"], copies[i % len(copies)], m["N"], m["K"], m["x"], y=m["y"],
+                          stream=stream)
+
+            g = capture(one)
+            reps = max(3, min(20, int(2e9 / (calls * m["bytes"]) + 1)))
+            t_ms = timed(g, reps, 2) / calls
+            gbs = m["bytes"] / (t_ms * 1e-3) / 1e9
+            detail.append({"matrix": m["name"], "type": synth.TYPE_NAMES[m["qtype"]], "K": m["K"],
+                           "N": m["N"], "MB": round(m["bytes"] / 1e6, 3), "us": round(t_ms * 1e3, 2),
+                           "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4)})
+            if m["name"] == "cfg2:lm_head":
+                traffic = load_traffic("gemv.cu")
+                roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
+                        "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
+                        "traffic": traffic, "kernel": "gemv_kernel<Q6_K,1> (qmm, lm_head 2048x128256)",
+                        "bytes_per_launch": m["bytes"], "us_per_launch": round(t_ms * 1e3, 2),
+                        "peak_source": peaks["source"] + " hbm_gbs (copy, burst)"}
+            del g, copies
+            torch.cuda.empty_cache()
+
+        # ---- prefill GEMM, M=512
+        gemm = []
+        for idx, (name, qtype, K, N) in enumerate(synth.CONFIGS[4]["mats"]):
+            W = torch.from_numpy(synth.config_weights(4, idx)).to(dev)
+            x = torch.from_numpy(synth.config_activations(4, 512, K)).to(dev)
+            y = torch.empty((512, N), dtype=torch.float32, device=dev)
+
+            def gcall(W=W, x=x, y=y, qtype=qtype, K=K, N=N):
+                for _ in range(5):
+                    q.qmm(qtype, W, N, K, x, y=y, stream=stream)
+
+            g = capture(gcall)
+            t_ms = timed(g, 4, 1) / 5
+            tops = 2 * 512 * N * K / (t_ms * 1e-3) / 1e12
+            gemm.append({"matrix": f"mistral_{name}", "M": 512, "K": K, "N": N,
+                         "us": round(t_ms * 1e3, 1), "TOPS": round(tops, 1)})
+            del g
+        int8_peak = None
+        try:
+            a = torch.randint(-127, 127, (8192, 8192), dtype=torch.int8, device=dev)
+            b = torch.randint(-127, 127, (8192, 8192), dtype=torch.int8, device=dev).t()
+            for _ in range(3):
+                torch._int_mm(a, b)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(10):
+                torch._int_mm(a, b)
+            e1.record()
+            torch.cuda.synchronize()
+            int8_peak = 2 * 8192 ** 3 / (e0.elapsed_time(e1) / 10 * 1e-3) / 1e12
+            del a, b
+        except Exception as exc:  # noqa: BLE001
+            int8_peak = None
+            print(f"int8 peak probe unavailable: {exc}", file=sys.stderr)
+        for gm in gemm:
+            gm["frac_f16_peak"] = round(gm["TOPS"] / peaks["bf16"], 4)
+            gm["frac_int8_peak"] = round(gm["TOPS"] / int8_peak, 4) if int8_peak else None
+        gemm = {"kernels": gemm, "int8_peak_tops_torch_int_mm": round(int8_peak, 1) if int8_peak else None,
+                "f16_peak_tflops": peaks["bf16"]}
+
+        # ---- CPU oracle on a bounded sample
+        cores = len(os.sched_getaffinity(0))
+        rate, sample = oracle_rate(mats, args.cpu_seconds, cores)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": "Q4_K/Q6_K GEMV weight GB/s at M=1 (decode step)",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, "M": 1, "matrices": len(mats),
+                       "weight_bytes_per_step": step_bytes, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (447 MB of weights per step)",
+                       "frac_hbm_step": round(value / world / peaks["hbm"], 4)},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
+                    "note": "weights resident (model state); x in and y out every call"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks, "per_matrix": detail, "prefill_gemm": gemm,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--quick", action="store_true", help="headline and e2e only")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

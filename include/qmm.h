@@ -1,0 +1,140 @@
+/*
+ * qmm.h -- C ABI of libqmm: the quantized-weight matrix product y = W.x on
+ * NVIDIA GB300 (sm_103a), with W stored in GGUF block formats.
+ *
+ * The operation is the one the LLM engines on the blazr README ("Model
+ * Formats > GGUF": dp4a CUDA kernels for Q4_K, Q6_K and Q8_0) and the infr
+ * landing page ("models": in-shader dequant with dp4a mmq; default quant
+ * Q4_K_M; "Per-op device profiling": GEMV and GEMM buckets) spend their
+ * decode time in.  Neither page fixes an interface; the calls below follow
+ * the problem statement of this library.
+ *
+ * Conventions shared by every entry point
+ *   - Every buffer pointer is a DEVICE pointer owned by the caller; the
+ *     library never frees or retains it beyond the call.
+ *   - W is row-major by output row: row n holds the K/QK consecutive blocks
+ *     of weights W[n, 0..K), QK = 32 (Q8_0) or 256 (Q4_K, Q6_K).  The base
+ *     of a weight or block buffer must be 16-byte aligned (GGUF aligns tensor
+ *     data to 32 bytes; torch allocations to 256).
+ *   - x is row-major [M, K] fp32, y row-major [M, N] fp32; both 4-byte
+ *     aligned.  y is overwritten, never accumulated into.
+ *   - Status: 0 on success, a negative QMM_E* code otherwise.  All checks
+ *     happen before any launch; on error nothing is launched and
+ *     qmm_last_error() holds a one-line reason (thread-local).  Nothing
+ *     aborts.  Kernels run asynchronously: device-side faults surface at the
+ *     caller's next synchronisation, and a bounded device wait that expired
+ *     is reported by qmm_device_status().
+ *   - Empty problems (M == 0, N == 0, n_elems == 0) are valid and launch
+ *     nothing.  K == 0 with M, N > 0 writes y = 0.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight block formats (this library's own numbering). */
+typedef enum {
+    QMM_Q8_0 = 0, /* fp16 d | int8 q[32]                         34 B / 32 w  */
+    QMM_Q4_K = 1, /* fp16 d | fp16 dmin | 12 B six-bit sc,m | 128 B nibbles
+                     w = d*sc*q - dmin*m                        144 B / 256 w */
+    QMM_Q6_K = 2  /* 128 B ql | 64 B qh | int8 sc[16] | fp16 d
+                     w = d*sc*(q-32)                            210 B / 256 w */
+} qmm_type;
+
+/* Status codes. */
+enum {
+    QMM_OK = 0,
+    QMM_EINVAL_TYPE = -1,  /* unknown qmm_type                                */
+    QMM_EINVAL_SHAPE = -2, /* negative size, K or n_elems not a block multiple */
+    QMM_EINVAL_PTR = -3,   /* null or misaligned pointer for a non-empty call  */
+    QMM_ENOMEM = -4,       /* workspace allocation failed                      */
+    QMM_ECUDA = -5,        /* CUDA runtime error (detail in qmm_last_error)    */
+    QMM_ETIMEOUT = -6      /* a bounded device wait expired (qmm_device_status)*/
+};
+
+/*
+ * qmm_dequant -- unpack n_elems weights from `blocks` into out_f32[n_elems].
+ *   type     : qmm_type of the blocks.
+ *   blocks   : device, n_elems/QK consecutive blocks, 16-byte aligned.
+ *   n_elems  : number of weights, a multiple of QK (32 or 256).
+ *   out_f32  : device, n_elems floats, 16-byte aligned.
+ * Each weight is computed with a fixed fp32 order and no FMA contraction:
+ *   Q8_0: d*q;  Q4_K: ((d*sc)*q) - (dmin*m);  Q6_K: (d*sc)*(q-32),
+ * so the result is bit-for-bit reproducible.  Runs asynchronously on the
+ * legacy default stream (the call has no stream argument).
+ */
+QMM_API int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *out_f32);
+
+/*
+ * qmm -- y[M,N] = W[N,K] . x[M,K]^T with the activations quantised to int8
+ * in blocks of 32 (Q8_1 style: fp32 scale max|x|/127, round half away from
+ * zero, block sum), exact int32 per-block dot products, fp32 scaling.
+ *   type     : qmm_type of W.
+ *   W_blocks : device, N*(K/QK) blocks, row-major by output row, 16-B aligned.
+ *   N, K     : output rows and reduction length; K a multiple of QK.
+ *   x        : device, M*K floats row-major (the activations).
+ *   M        : activation rows.  M <= 8 runs the decode GEMV (weights
+ *              streamed once through shared memory by bulk async copies,
+ *              dp4a dot products); M > 8 runs the prefill GEMM.
+ *   y        : device, M*N floats, overwritten.
+ *   stream   : cudaStream_t to run on (NULL = legacy default stream).
+ * Accuracy: |y - y_exact| <= 2e-3 * sum_k |w_k * xhat_k| + 1e-5, where
+ * y_exact is the f64 result of the same quantised arithmetic.
+ * The call uses a library-owned device workspace per (device, stream) for
+ * the quantised activations.  It is allocated, or grown, on the first call
+ * that needs it, so make one call of the largest M*K on a stream before
+ * capturing that stream into a CUDA graph.  Calls on one stream are ordered;
+ * calls on different streams use different workspaces.
+ */
+QMM_API int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, int64_t M,
+        float *y, void *stream);
+
+/*
+ * qmm_quantize_act -- the activation quantiser on its own (test hook and
+ * building block): for each row of x[M,K] and each block b of 32,
+ *   d[m,b] = max|x|/127, q = round_half_away(x * (1/d)) (0 when d == 0),
+ *   s[m,b] = sum of the 32 q as int32.
+ *   x : device [M,K] fp32; q : device [M,K] int8; d : device [M,K/32] fp32;
+ *   s : device [M,K/32] int32.  K must be a multiple of 32.
+ * Bit-for-bit reproducible (IEEE division, separately rounded multiply).
+ */
+QMM_API int qmm_quantize_act(const float *x, int64_t M, int64_t K, int8_t *q, float *d, int32_t *s,
+                     void *stream);
+
+/* Name of a status code. */
+QMM_API const char *qmm_strerror(int status);
+
+/* Detail of the last error raised on the calling thread ("" if none). */
+QMM_API const char *qmm_last_error(void);
+
+/*
+ * qmm_device_status -- synchronise `stream` and report whether any kernel of
+ * this library on the current device gave up on a bounded wait since the
+ * last call (QMM_ETIMEOUT; the flag is then cleared), or QMM_ECUDA if the
+ * synchronisation itself failed.
+ */
+QMM_API int qmm_device_status(void *stream);
+
+/* Free every workspace of the library on the current device (synchronises
+ * the device first).  Later calls allocate again. */
+QMM_API int qmm_release(void);
+
+/* Number of kernel launches this library issued on the calling process
+ * since it was loaded (for launch accounting in benchmarks). */
+QMM_API int64_t qmm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

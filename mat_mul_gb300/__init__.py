@@ -1,0 +1,144 @@
+"""Python binding of libqmm (include/qmm.h): argument marshalling only.
+
+Every step of the computation runs in the CUDA kernels of libqmm.so; torch is
+used for device memory and streams.  There is no CPU fallback: when the
+library is missing or no GPU is present the calls raise.
+
+    import mat_mul_gb300 as q
+    y = q.qmm(q.Q4_K, W_blocks, N, K, x)          # x: cuda f32 [M, K]
+    w = q.qmm_dequant(q.Q6_K, blocks, n_elems)    # cuda f32 [n_elems]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+Q8_0, Q4_K, Q6_K = 0, 1, 2
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210}
+BLOCK_WEIGHTS = {Q8_0: 32, Q4_K: 256, Q6_K: 256}
+
+QMM_OK = 0
+QMM_EINVAL_TYPE = -1
+QMM_EINVAL_SHAPE = -2
+QMM_EINVAL_PTR = -3
+QMM_ENOMEM = -4
+QMM_ECUDA = -5
+QMM_ETIMEOUT = -6
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqmm.so")
+
+_lib = None
+
+
+class QmmError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{_strerror(status)}: {detail}")
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def load():
+    """Load libqmm.so, (re)building it first when it is absent or older than
+    its sources."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    L = ctypes.CDLL(LIB_PATH)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.qmm_dequant.argtypes = [I, P, I64, P]
+    L.qmm.argtypes = [I, P, I64, I64, P, I64, P, P]
+    L.qmm_quantize_act.argtypes = [P, I64, I64, P, P, P, P]
+    L.qmm_strerror.argtypes = [I]
+    L.qmm_strerror.restype = ctypes.c_char_p
+    L.qmm_last_error.restype = ctypes.c_char_p
+    L.qmm_device_status.argtypes = [P]
+    L.qmm_launch_count.restype = I64
+    for f in ("qmm_dequant", "qmm", "qmm_quantize_act", "qmm_device_status", "qmm_release"):
+        getattr(L, f).restype = I
+    _lib = L
+    return L
+
+
+def _strerror(status: int) -> str:
+    return load().qmm_strerror(int(status)).decode()
+
+
+def _check(rc: int):
+    if rc != QMM_OK:
+        raise QmmError(rc, load().qmm_last_error().decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libqmm takes device tensors; got a tensor on " + str(t.device))
+
+
+def qmm_dequant(qtype: int, blocks, n_elems: int, out=None):
+    """Unpack n_elems weights of type qtype from a uint8 device tensor."""
+    import torch
+    _require_cuda(blocks, out)
+    if out is None:
+        out = torch.empty(n_elems, dtype=torch.float32, device=blocks.device)
+    _check(load().qmm_dequant(int(qtype), _ptr(blocks), int(n_elems), _ptr(out)))
+    return out
+
+
+def qmm(qtype: int, W, N: int, K: int, x, y=None, stream=None):
+    """y[M,N] = W . x^T for a uint8 device tensor W of packed blocks and a
+    device f32 tensor x of shape [M, K] (or [K])."""
+    import torch
+    _require_cuda(W, x, y)
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 tensor")
+    M = 1 if x.dim() == 1 else x.shape[0]
+    if x.shape[-1] != K:
+        raise ValueError(f"x has {x.shape[-1]} columns, K = {K}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(load().qmm(int(qtype), _ptr(W), int(N), int(K), _ptr(x), int(M), _ptr(y),
+                      _stream_handle(stream)))
+    return y
+
+
+def qmm_quantize_act(x, stream=None):
+    """Return (q int8 [M,K], d f32 [M,K/32], s int32 [M,K/32]) for device x."""
+    import torch
+    _require_cuda(x)
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    M, K = x2.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    d = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
+    s = torch.empty((M, K // 32), dtype=torch.int32, device=x.device)
+    _check(load().qmm_quantize_act(_ptr(x2), int(M), int(K), _ptr(q), _ptr(d), _ptr(s),
+                                   _stream_handle(stream)))
+    return q, d, s
+
+
+def qmm_device_status(stream=None) -> int:
+    return int(load().qmm_device_status(_stream_handle(stream)))
+
+
+def qmm_release() -> None:
+    _check(load().qmm_release())
+
+
+def qmm_launch_count() -> int:
+    return int(load().qmm_launch_count())

@@ -1,0 +1,283 @@
+// qmm_abi.cu -- the C ABI of libqmm (include/qmm.h): argument validation,
+// dispatch between the decode GEMV (M <= 8) and the prefill GEMM, the
+// per-(device, stream) activation workspace, status and error reporting.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/qmm.h"
+#include "qmm_device.cuh"
+
+namespace qk {
+cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, int8_t *q, int64_t q_ld, float *d,
+                            int32_t *s, int64_t ds_ld, cudaStream_t st, bool trigger_dependents,
+                            int num_sms);
+cudaError_t launch_dequant(int type, const void *blocks, int64_t n_elems, float *out,
+                           cudaStream_t st, int num_sms);
+cudaError_t launch_gemv(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
+                        const float *xd, const int32_t *xs, int xd_ld, int M, float *y,
+                        cudaStream_t st, bool pdl, int num_sms, int max_smem, int *status);
+bool gemv_fits(int type, int M, int64_t K, int xd_ld, int max_smem);
+cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
+                            const float *xd, const int32_t *xs, int xd_ld, int64_t M, float *y,
+                            cudaStream_t st);
+}  // namespace qk
+
+namespace {
+
+thread_local char g_err[512] = "";
+std::atomic<int64_t> g_launches{0};
+
+int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(QMM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+    int num_sms = 0;
+    int max_smem = 0;
+    int *status = nullptr;  // device word raised by bounded waits that expired
+};
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_dev;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+int device_info(int dev, DeviceInfo &out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(dev);
+    if (it != g_dev.end()) {
+        out = it->second;
+        return QMM_OK;
+    }
+    DeviceInfo di;
+    cudaError_t e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&di.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    e = cudaMalloc(&di.status, 256);
+    if (e != cudaSuccess) return fail(QMM_ENOMEM, "status word: %s", cudaGetErrorString(e));
+    e = cudaMemset(di.status, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "status word init");
+    g_dev[dev] = di;
+    out = di;
+    return QMM_OK;
+}
+
+// Workspace of at least `bytes` for (dev, stream).  Growing synchronises the
+// stream before the old buffer is released.
+int workspace(int dev, cudaStream_t st, size_t bytes, void **ptr) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = g_ws[{dev, st}];
+    if (w.bytes >= bytes) {
+        *ptr = w.ptr;
+        return QMM_OK;
+    }
+    size_t want = bytes + bytes / 2;
+    want = (want + (2u << 20) - 1) & ~size_t((2u << 20) - 1);
+    if (w.ptr) {
+        cudaError_t e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "workspace grow (sync)");
+        cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&w.ptr, want);
+    if (e != cudaSuccess) {
+        w.ptr = nullptr;
+        return fail(QMM_ENOMEM, "workspace of %zu bytes: %s", want, cudaGetErrorString(e));
+    }
+    w.bytes = want;
+    *ptr = w.ptr;
+    return QMM_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_type(int type) {
+    if (type != QMM_Q8_0 && type != QMM_Q4_K && type != QMM_Q6_K)
+        return fail(QMM_EINVAL_TYPE, "unknown block type %d", type);
+    return QMM_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char *qmm_strerror(int status) {
+    switch (status) {
+    case QMM_OK: return "QMM_OK";
+    case QMM_EINVAL_TYPE: return "QMM_EINVAL_TYPE";
+    case QMM_EINVAL_SHAPE: return "QMM_EINVAL_SHAPE";
+    case QMM_EINVAL_PTR: return "QMM_EINVAL_PTR";
+    case QMM_ENOMEM: return "QMM_ENOMEM";
+    case QMM_ECUDA: return "QMM_ECUDA";
+    case QMM_ETIMEOUT: return "QMM_ETIMEOUT";
+    default: return "QMM_UNKNOWN";
+    }
+}
+
+const char *qmm_last_error(void) { return g_err; }
+
+int64_t qmm_launch_count(void) { return g_launches.load(); }
+
+int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *out_f32) {
+    g_err[0] = 0;
+    if (int rc = check_type(type)) return rc;
+    const int qk_ = qk::block_weights(type);
+    if (n_elems < 0 || n_elems % qk_)
+        return fail(QMM_EINVAL_SHAPE, "n_elems=%lld is not a non-negative multiple of %d",
+                    static_cast<long long>(n_elems), qk_);
+    if (n_elems == 0) return QMM_OK;
+    if (!blocks || !out_f32) return fail(QMM_EINVAL_PTR, "null pointer");
+    if (!aligned(blocks, 16) || !aligned(out_f32, 16))
+        return fail(QMM_EINVAL_PTR, "blocks and out_f32 must be 16-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo di;
+    if (int rc = device_info(dev, di)) return rc;
+    e = qk::launch_dequant(type, blocks, n_elems, out_f32, 0, di.num_sms);
+    if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
+    g_launches.fetch_add(1);
+    return QMM_OK;
+}
+
+int qmm_quantize_act(const float *x, int64_t M, int64_t K, int8_t *q, float *d, int32_t *s,
+                     void *stream) {
+    g_err[0] = 0;
+    if (M < 0 || K < 0 || K % 32)
+        return fail(QMM_EINVAL_SHAPE, "M=%lld K=%lld: K must be a non-negative multiple of 32",
+                    static_cast<long long>(M), static_cast<long long>(K));
+    if (M == 0 || K == 0) return QMM_OK;
+    if (!x || !q || !d || !s) return fail(QMM_EINVAL_PTR, "null pointer");
+    if (!aligned(x, 4) || !aligned(d, 4) || !aligned(s, 4))
+        return fail(QMM_EINVAL_PTR, "x, d and s must be 4-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo di;
+    if (int rc = device_info(dev, di)) return rc;
+    e = qk::launch_quantize(x, M, K, q, K, d, s, K / 32, static_cast<cudaStream_t>(stream), false,
+                            di.num_sms);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    g_launches.fetch_add(1);
+    return QMM_OK;
+}
+
+int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+        void *stream) {
+    g_err[0] = 0;
+    if (int rc = check_type(type)) return rc;
+    const int qk_ = qk::block_weights(type);
+    if (N < 0 || M < 0 || K < 0 || K % qk_)
+        return fail(QMM_EINVAL_SHAPE, "N=%lld K=%lld M=%lld: sizes must be >= 0 and K a multiple of %d",
+                    static_cast<long long>(N), static_cast<long long>(K), static_cast<long long>(M), qk_);
+    if (K > (int64_t(1) << 24))
+        return fail(QMM_EINVAL_SHAPE, "K=%lld exceeds 2^24", static_cast<long long>(K));
+    if (M == 0 || N == 0) return QMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!y) return fail(QMM_EINVAL_PTR, "null y");
+    if (!aligned(y, 4)) return fail(QMM_EINVAL_PTR, "y must be 4-byte aligned");
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(M * N) * sizeof(float), st);
+        if (e != cudaSuccess) return cuda_fail(e, "zero fill");
+        return QMM_OK;
+    }
+    if (!W_blocks || !x) return fail(QMM_EINVAL_PTR, "null pointer");
+    if (!aligned(W_blocks, 16)) return fail(QMM_EINVAL_PTR, "W_blocks must be 16-byte aligned");
+    if (!aligned(x, 4)) return fail(QMM_EINVAL_PTR, "x must be 4-byte aligned");
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo di;
+    if (int rc = device_info(dev, di)) return rc;
+
+    // workspace: q int8 [M][K] | d fp32 [M][ld] | s int32 [M][ld], ld = K/32 rounded to 4
+    const int xd_ld = static_cast<int>(align_up(static_cast<size_t>(K / 32), 4));
+    const size_t q_bytes = align_up(static_cast<size_t>(M * K), 256);
+    const size_t d_bytes = align_up(static_cast<size_t>(M) * xd_ld * 4, 256);
+    void *ws = nullptr;
+    if (int rc = workspace(dev, st, q_bytes + 2 * d_bytes, &ws)) return rc;
+    auto *xq = static_cast<int8_t *>(ws);
+    auto *xd = reinterpret_cast<float *>(static_cast<char *>(ws) + q_bytes);
+    auto *xs = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + q_bytes + d_bytes);
+
+    const bool decode = M <= 8 && qk::gemv_fits(type, static_cast<int>(M), K, xd_ld, di.max_smem);
+    e = qk::launch_quantize(x, M, K, xq, K, xd, xs, xd_ld, st, decode, di.num_sms);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    g_launches.fetch_add(1);
+    if (decode) {
+        e = qk::launch_gemv(type, W_blocks, N, K, xq, xd, xs, xd_ld, static_cast<int>(M), y, st, true,
+                            di.num_sms, di.max_smem, di.status);
+        if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    } else {
+        e = qk::launch_gemm_mma(type, W_blocks, N, K, xq, xd, xs, xd_ld, M, y, st);
+        if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    }
+    g_launches.fetch_add(1);
+    return QMM_OK;
+}
+
+int qmm_device_status(void *stream) {
+    g_err[0] = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo di;
+    if (int rc = device_info(dev, di)) return rc;
+    e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, di.status, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (word) {
+        e = cudaMemset(di.status, 0, sizeof word);
+        if (e != cudaSuccess) return cuda_fail(e, "status clear");
+        return fail(QMM_ETIMEOUT, "a bounded device wait expired (status word 0x%x)", word);
+    }
+    return QMM_OK;
+}
+
+int qmm_release(void) {
+    g_err[0] = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (auto it = g_ws.begin(); it != g_ws.end();) {
+        if (it->first.first == dev) {
+            cudaFree(it->second.ptr);
+            it = g_ws.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    return QMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+// qmm_device.cuh -- device-side building blocks of libqmm for sm_103a:
+// block-format constants, inline-PTX wrappers for mbarriers, bulk async
+// copies and programmatic dependent launch, bounded waits, and small
+// shared-memory load helpers.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qmm.h"
+
+namespace qk {
+
+// ---------------------------------------------------------------------------
+// Block formats (GGUF): bytes per block and weights per block.
+// ---------------------------------------------------------------------------
+template <int T> struct Fmt;
+template <> struct Fmt<QMM_Q8_0> { static constexpr int BB = 34, QK = 32; };
+template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, QK = 256; };
+template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, QK = 256; };
+
+inline int block_bytes(int t) { return t == QMM_Q8_0 ? 34 : t == QMM_Q4_K ? 144 : 210; }
+inline int block_weights(int t) { return t == QMM_Q8_0 ? 32 : 256; }
+
+// Status bits a kernel may raise in the per-device status word.
+enum : int { STATUS_TIMEOUT = 1 };
+
+// Wall-clock limit of every bounded wait (nanoseconds of %globaltimer).
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, giving up after
+// `limit_ns`; on expiry the status word `status` (device memory owned by the
+// library) records a timeout and the function returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > limit_ns) {
+            atomicOr(status, STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// One-dimensional bulk async copy global -> shared, completing on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Programmatic dependent launch: wait for the preceding grid's results /
+// allow the next grid to start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns the OR of `pred` over all participants, so
+// every participant takes the same decision after it.
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.cta.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// Shared-memory loads by 32-bit shared address.
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds32(a)); }
+
+// Read n consecutive 32-bit words starting at a 2-byte-aligned shared
+// address: aligned words are loaded and shifted into place.
+template <int NWORDS>
+__device__ __forceinline__ void lds_words_u16aligned(uint32_t a, uint32_t (&w)[NWORDS]) {
+    const uint32_t base = a & ~3u;
+    const uint32_t sh = (a & 3u) * 8u;
+    uint32_t prev = lds32(base);
+#pragma unroll
+    for (int i = 0; i < NWORDS; ++i) {
+        uint32_t next = lds32(base + 4u * (i + 1));
+        w[i] = __funnelshift_r(prev, next, sh);
+        prev = next;
+    }
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits & 0xffffu)));
+}
+
+}  // namespace qk

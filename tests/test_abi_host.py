@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads
+and exports every entry point declared in include/qmm.h, and argument
+validation rejects bad calls before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import mat_mul_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"QMM_API\s+[\w\s\*]*?\b(qmm\w*)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_symbols()
+    for want in ("qmm", "qmm_dequant", "qmm_quantize_act", "qmm_strerror", "qmm_last_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    path = q.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in _declared_symbols() if n not in exported]
+    assert not missing, missing
+    L = q.load()
+    for n in _declared_symbols():
+        assert hasattr(L, n)
+
+
+def test_strerror_names():
+    assert q._strerror(q.QMM_OK) == "QMM_OK"
+    assert q._strerror(q.QMM_ETIMEOUT) == "QMM_ETIMEOUT"
+    assert q._strerror(-99) == "QMM_UNKNOWN"
+
+
+def test_validation_rejects_before_launch():
+    L = q.load()
+    null = ctypes.c_void_p(0)
+    # unknown type
+    assert L.qmm(7, null, 1, 256, null, 1, null, null) == q.QMM_EINVAL_TYPE
+    assert b"unknown block type" in L.qmm_last_error()
+    # K not a multiple of the block
+    assert L.qmm(q.Q4_K, null, 4, 300, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm(q.Q8_0, null, 4, 48, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+    # negative sizes
+    assert L.qmm(q.Q6_K, null, -1, 256, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm(q.Q6_K, null, 1, 256, null, -2, null, null) == q.QMM_EINVAL_SHAPE
+    # null pointers on a non-empty problem
+    assert L.qmm(q.Q6_K, null, 1, 256, null, 1, null, null) == q.QMM_EINVAL_PTR
+    # misaligned W
+    buf = ctypes.create_string_buffer(4096)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    assert L.qmm(q.Q4_K, ctypes.c_void_p(base + 2), 1, 256, ctypes.c_void_p(base),
+                 1, ctypes.c_void_p(base), null) == q.QMM_EINVAL_PTR
+    # dequant
+    assert L.qmm_dequant(3, null, 32, null) == q.QMM_EINVAL_TYPE
+    assert L.qmm_dequant(q.Q4_K, null, 100, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_dequant(q.Q4_K, null, 256, null) == q.QMM_EINVAL_PTR
+    assert L.qmm_quantize_act(null, 1, 33, null, null, null, null) == q.QMM_EINVAL_SHAPE
+
+
+def test_empty_problems_are_noops():
+    L = q.load()
+    null = ctypes.c_void_p(0)
+    before = L.qmm_launch_count()
+    assert L.qmm(q.Q4_K, null, 0, 256, null, 3, null, null) == q.QMM_OK
+    assert L.qmm(q.Q4_K, null, 5, 256, null, 0, null, null) == q.QMM_OK
+    assert L.qmm_dequant(q.Q6_K, null, 0, null) == q.QMM_OK
+    assert L.qmm_quantize_act(null, 0, 64, null, null, null, null) == q.QMM_OK
+    assert L.qmm_launch_count() == before
+
+
+def test_binding_refuses_host_tensors():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        q.qmm(q.Q4_K, torch.zeros(144, dtype=torch.uint8), 1, 256, torch.zeros(1, 256))

@@ -1,0 +1,205 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars: dequantisation and the activation quantiser bit-for-bit; qmm outputs
+within |y_gpu - y_oracle| <= 2e-3 * sum_k |w_k xhat_k| + 1e-5 element-wise
+(the library's stated accuracy), at small shapes spanning several tiles and
+ragged tails, and at the full workload sizes on sampled output rows."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 2e-3, 1e-5
+
+
+def _dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _assert_within_bound(y_gpu, y_or, A, what=""):
+    err = np.abs(y_gpu.astype(np.float64) - y_or)
+    bound = REL * A + ABS
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside the bound; worst "
+                           f"err {err[bad].max():.3e} vs bound {bound[bad].min():.3e}")
+
+
+def _run_qmm(q, qtype, W, N, K, x):
+    y = q.qmm(qtype, _dev(W), N, K, _dev(x))
+    assert q.qmm_device_status() == 0
+    return y.cpu().numpy()
+
+
+# ------------------------------------------------------------------ dequant
+
+@pytest.mark.parametrize("qtype", [synth.Q8_0, synth.Q4_K, synth.Q6_K])
+@pytest.mark.parametrize("nblocks", [1, 3, 8, 37, 1000])
+def test_dequant_bitwise(cuda_lib, qtype, nblocks):
+    W = synth.weights(qtype, nblocks, synth.BLOCK_WEIGHTS[qtype], seed=nblocks + 10 * qtype)
+    n = nblocks * synth.BLOCK_WEIGHTS[qtype]
+    got = cuda_lib.qmm_dequant(qtype, _dev(W), n).cpu().numpy()
+    want = O.dequant(qtype, W, n)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("cfg,idx", [(0, 0), (1, 0), (2, 0), (3, 2), (3, 6), (4, 0)])
+def test_dequant_bitwise_workload_weights(cuda_lib, cfg, idx):
+    name, qtype, K, N = synth.CONFIGS[cfg]["mats"][idx]
+    W = synth.config_weights(cfg, idx)
+    n = N * K
+    got = cuda_lib.qmm_dequant(qtype, _dev(W), n).cpu().numpy()
+    want = O.dequant(qtype, W, n)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), name
+
+
+def test_dequant_extreme_fields(cuda_lib):
+    """Extreme scale/min values and fp16 subnormals, packed by the oracle."""
+    blocks = []
+    for v in (0, 1, 31, 32, 63):
+        sc = np.full(8, v, np.uint8)
+        m = np.full(8, 63 - v, np.uint8)
+        qv = (np.arange(256) % 16).astype(np.uint8)
+        for db in (0x0001, 0x03FF, 0x3C00, 0x7BFF, 0x8000):
+            blocks.append(O.pack_q4_k(db, 0x0400 | v, sc, m, qv))
+    W = np.concatenate(blocks)
+    n = len(blocks) * 256
+    got = cuda_lib.qmm_dequant(synth.Q4_K, _dev(W), n).cpu().numpy()
+    want = O.dequant(synth.Q4_K, W, n)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    blocks = [O.pack_q6_k(db, np.array([-128, 127, 0, -1] * 4, np.int8),
+                          (np.arange(256) % 64).astype(np.uint8))
+              for db in (0x0001, 0x3C00, 0x7BFF, 0xFBFF)]
+    W = np.concatenate(blocks)
+    got = cuda_lib.qmm_dequant(synth.Q6_K, _dev(W), 1024).cpu().numpy()
+    want = O.dequant(synth.Q6_K, W, 1024)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+# ----------------------------------------------------------------- quantiser
+
+@pytest.mark.parametrize("M,K", [(1, 32), (1, 2048), (3, 5120), (8, 17408), (64, 4096)])
+def test_quantizer_bitwise(cuda_lib, M, K):
+    x = synth.activations(M, K, seed=M * 7 + K, outlier_frac=0.01)
+    x[0, :32] = 0.0                                  # all-zero block
+    x[-1, 32:64] = np.float32(127.0) * np.arange(-16, 16) / 16   # exact halves
+    q, d, s = cuda_lib.qmm_quantize_act(_dev(x))
+    qo, do, so = O.quantize_act(x)
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(d.cpu().numpy().view(np.uint32), do.view(np.uint32))
+    assert np.array_equal(s.cpu().numpy(), so)
+
+
+# ----------------------------------------------------------- qmm, small shapes
+
+SMALL = [
+    # (qtype, N, K, M)
+    (synth.Q4_K, 37, 256, 1), (synth.Q4_K, 300, 1280, 1), (synth.Q4_K, 129, 2048, 2),
+    (synth.Q4_K, 64, 5120, 3), (synth.Q4_K, 77, 768, 4), (synth.Q4_K, 50, 2304, 8),
+    (synth.Q6_K, 37, 256, 1), (synth.Q6_K, 301, 1280, 1), (synth.Q6_K, 65, 5120, 2),
+    (synth.Q6_K, 33, 768, 5), (synth.Q6_K, 40, 2048, 8), (synth.Q6_K, 8, 17408, 1),
+    (synth.Q8_0, 33, 32, 1), (synth.Q8_0, 256, 512, 1), (synth.Q8_0, 100, 1056, 2),
+    (synth.Q8_0, 17, 4096, 7), (synth.Q8_0, 1, 96, 8),
+]
+
+
+@pytest.mark.parametrize("qtype,N,K,M", SMALL)
+def test_qmm_decode_small(cuda_lib, qtype, N, K, M):
+    W = synth.weights(qtype, N, K, seed=N + K + M)
+    x = synth.activations(M, K, seed=N * K + M, outlier_frac=0.01)
+    y = _run_qmm(cuda_lib, qtype, W, N, K, x)
+    yo, A = O.qmm(qtype, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"type {qtype} N={N} K={K} M={M}")
+
+
+GEMM_SMALL = [
+    (synth.Q4_K, 70, 512, 9), (synth.Q4_K, 130, 768, 64), (synth.Q4_K, 64, 256, 100),
+    (synth.Q6_K, 70, 512, 9), (synth.Q6_K, 129, 1024, 65), (synth.Q8_0, 70, 544, 33),
+    (synth.Q8_0, 64, 256, 64), (synth.Q4_K, 200, 4096, 130),
+]
+
+
+@pytest.mark.parametrize("qtype,N,K,M", GEMM_SMALL)
+def test_qmm_prefill_small(cuda_lib, qtype, N, K, M):
+    W = synth.weights(qtype, N, K, seed=N + K + M + 1)
+    x = synth.activations(M, K, seed=N * K + M + 1, outlier_frac=0.01)
+    y = _run_qmm(cuda_lib, qtype, W, N, K, x)
+    yo, A = O.qmm(qtype, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"type {qtype} N={N} K={K} M={M}")
+
+
+def test_qmm_is_deterministic_and_overwrites_y(cuda_lib):
+    import torch
+    qtype, N, K = synth.Q6_K, 300, 5120
+    W = _dev(synth.weights(qtype, N, K, seed=3))
+    x = _dev(synth.activations(2, K, seed=4))
+    y1 = torch.full((2, N), float("nan"), device="cuda")
+    cuda_lib.qmm(qtype, W, N, K, x, y=y1)
+    y2 = cuda_lib.qmm(qtype, W, N, K, x)
+    assert torch.equal(y1, y2)
+
+
+def test_qmm_zero_k_and_empty(cuda_lib):
+    import torch
+    y = torch.full((3, 5), 7.0, device="cuda")
+    x = torch.zeros((3, 0), device="cuda")
+    W = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    cuda_lib.qmm(synth.Q4_K, W, 5, 0, x, y=y)
+    assert torch.all(y.cpu() == 0)
+
+
+def test_qmm_on_side_stream(cuda_lib):
+    import torch
+    qtype, N, K = synth.Q4_K, 256, 2048
+    W = synth.weights(qtype, N, K, seed=5)
+    x = synth.activations(1, K, seed=6)
+    s = torch.cuda.Stream()
+    Wd, xd = _dev(W), _dev(x)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        y = cuda_lib.qmm(qtype, Wd, N, K, xd, stream=s)
+    s.synchronize()
+    yo, A = O.qmm(qtype, W, N, K, x)
+    _assert_within_bound(y.cpu().numpy(), yo, A)
+
+
+# ------------------------------------------- the workloads at full size
+
+def _sample_rows(N, k=384, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(range(min(N, 64))) | set(range(max(0, N - 64), N))
+    rows |= set(rng.choice(N, size=min(N, k), replace=False).tolist())
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+def test_qmm_workloads_full_size(cuda_lib, cfg):
+    c = synth.CONFIGS[cfg]
+    for idx, (name, qtype, K, N) in enumerate(c["mats"]):
+        W = synth.config_weights(cfg, idx)
+        Wdev = _dev(W)
+        rb = synth.row_bytes(qtype, K)
+        for M in c["M"]:
+            x = synth.config_activations(cfg, M, K)
+            y = cuda_lib.qmm(qtype, Wdev, N, K, _dev(x)).cpu().numpy()
+            assert cuda_lib.qmm_device_status() == 0
+            rows = _sample_rows(N, seed=idx + M) if N * K > 4_000_000 else np.arange(N)
+            Wr = W.reshape(N, rb)[rows]
+            yo, A = O.qmm(qtype, Wr, len(rows), K, x)
+            _assert_within_bound(y[:, rows], yo, A, f"cfg {cfg} {name} M={M}")
+
+
+def test_qmm_prefill_workload_full_size(cuda_lib):
+    c = synth.CONFIGS[4]
+    for idx, (name, qtype, K, N) in enumerate(c["mats"]):
+        W = synth.config_weights(4, idx)
+        x = synth.config_activations(4, 512, K)
+        y = cuda_lib.qmm(qtype, _dev(W), N, K, _dev(x)).cpu().numpy()
+        assert cuda_lib.qmm_device_status() == 0
+        rows = _sample_rows(N, k=96, seed=idx)
+        rb = synth.row_bytes(qtype, K)
+        yo, A = O.qmm(qtype, W.reshape(N, rb)[rows], len(rows), K, x)
+        _assert_within_bound(y[:, rows], yo, A, f"prefill {name}")
