@@ -96,27 +96,50 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.rows = []
+        self.all_rows = []
+        self.window_open = False
         self.proc = None
 
-    def __enter__(self):
+    def start(self):
+        """Start sampling and wait (up to 5 s) for the first sample."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
             self.proc = None
+            return self
+        t0 = time.time()
+        while not self.all_rows and time.time() - t0 < 5:
+            time.sleep(0.01)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 8:
-                self.rows.append(parts)
+                self.all_rows.append((time.time(), parts))
+                if self.window_open:
+                    self.rows.append(parts)
+
+    def __enter__(self):
+        self.window_open = True
+        return self
+
+    def stop(self):
+        self.__exit__()
 
     def __exit__(self, *a):
+        self.window_open = False
+        if not self.rows and self.all_rows:
+            # the timed window was shorter than one sampling period: keep the
+            # sample closest to it
+            self.rows.append(self.all_rows[-1][1])
+
+    def close(self):
         if self.proc:
             self.proc.terminate()
             try:
@@ -300,9 +323,10 @@ def run_ours(args):
 
     # ---- headline: the decode step, weights resident
     g_step = capture(step)
-    sampler = ClockSampler(dev.index)
+    sampler = ClockSampler(dev.index).start()
     ms = timed(g_step, args.steps, args.warmup, sampler)
     clocks = sampler.summary()
+    sampler.close()
     value = world * step_bytes / (ms * 1e-3) / 1e9
     status = q.qmm_device_status(stream)
     assert status == 0, f"device status {status}"
@@ -430,7 +454,7 @@ class _Null:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

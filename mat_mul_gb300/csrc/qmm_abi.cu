@@ -16,14 +16,14 @@
 
 namespace qk {
 cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, int8_t *q, int64_t q_ld, float *d,
-                            int32_t *s, int64_t ds_ld, cudaStream_t st, bool trigger_dependents,
-                            int num_sms);
+                            int32_t *s, int64_t ds_ld, int64_t s_ld, bool sum16, cudaStream_t st,
+                            bool trigger_dependents, int num_sms);
 cudaError_t launch_dequant(int type, const void *blocks, int64_t n_elems, float *out,
                            cudaStream_t st, int num_sms);
 cudaError_t launch_gemv(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
-                        const float *xd, const int32_t *xs, int xd_ld, int M, float *y,
+                        const float *xd, const int32_t *xs, int xd_ld, int xs_ld, int M, float *y,
                         cudaStream_t st, bool pdl, int num_sms, int max_smem, int *status);
-bool gemv_fits(int type, int M, int64_t K, int xd_ld, int max_smem);
+bool gemv_fits(int type, int M, int64_t K, int xd_ld, int xs_ld, int max_smem);
 cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
                             const float *xd, const int32_t *xs, int xd_ld, int64_t M, float *y,
                             cudaStream_t st);
@@ -179,8 +179,8 @@ int qmm_quantize_act(const float *x, int64_t M, int64_t K, int8_t *q, float *d, 
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     DeviceInfo di;
     if (int rc = device_info(dev, di)) return rc;
-    e = qk::launch_quantize(x, M, K, q, K, d, s, K / 32, static_cast<cudaStream_t>(stream), false,
-                            di.num_sms);
+    e = qk::launch_quantize(x, M, K, q, K, d, s, K / 32, K / 32, false,
+                            static_cast<cudaStream_t>(stream), false, di.num_sms);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     g_launches.fetch_add(1);
     return QMM_OK;
@@ -215,23 +215,28 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     DeviceInfo di;
     if (int rc = device_info(dev, di)) return rc;
 
-    // workspace: q int8 [M][K] | d fp32 [M][ld] | s int32 [M][ld], ld = K/32 rounded to 4
+    // workspace: q int8 [M][K] | d fp32 [M][xd_ld] | s int32 [M][xs_ld]
+    // xd_ld = K/32 and xs_ld = K/16 (decode: sums per 16-element half block)
+    // or K/32 (prefill: sums per block), both rounded up to 4.
     const int xd_ld = static_cast<int>(align_up(static_cast<size_t>(K / 32), 4));
+    const int xs16_ld = static_cast<int>(align_up(static_cast<size_t>(K / 16), 4));
+    const bool decode = M <= 8 && qk::gemv_fits(type, static_cast<int>(M), K, xd_ld, xs16_ld, di.max_smem);
+    const int xs_ld = decode ? xs16_ld : xd_ld;
     const size_t q_bytes = align_up(static_cast<size_t>(M * K), 256);
     const size_t d_bytes = align_up(static_cast<size_t>(M) * xd_ld * 4, 256);
+    const size_t s_bytes = align_up(static_cast<size_t>(M) * xs_ld * 4, 256);
     void *ws = nullptr;
-    if (int rc = workspace(dev, st, q_bytes + 2 * d_bytes, &ws)) return rc;
+    if (int rc = workspace(dev, st, q_bytes + d_bytes + s_bytes, &ws)) return rc;
     auto *xq = static_cast<int8_t *>(ws);
     auto *xd = reinterpret_cast<float *>(static_cast<char *>(ws) + q_bytes);
     auto *xs = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + q_bytes + d_bytes);
 
-    const bool decode = M <= 8 && qk::gemv_fits(type, static_cast<int>(M), K, xd_ld, di.max_smem);
-    e = qk::launch_quantize(x, M, K, xq, K, xd, xs, xd_ld, st, decode, di.num_sms);
+    e = qk::launch_quantize(x, M, K, xq, K, xd, xs, xd_ld, xs_ld, decode, st, decode, di.num_sms);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     g_launches.fetch_add(1);
     if (decode) {
-        e = qk::launch_gemv(type, W_blocks, N, K, xq, xd, xs, xd_ld, static_cast<int>(M), y, st, true,
-                            di.num_sms, di.max_smem, di.status);
+        e = qk::launch_gemv(type, W_blocks, N, K, xq, xd, xs, xd_ld, xs_ld, static_cast<int>(M), y, st,
+                            true, di.num_sms, di.max_smem, di.status);
         if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
     } else {
         e = qk::launch_gemm_mma(type, W_blocks, N, K, xq, xd, xs, xd_ld, M, y, st);

@@ -1,0 +1,126 @@
+"""CPU model of the decode kernel's address arithmetic (gemv.cu), checked
+before any GPU run: every bulk copy starts 16-byte aligned, has a size that
+is a multiple of 16, stays inside the weight buffer and its shared-memory
+slot; every block a lane reads lies inside the bytes its stage copied; the
+stages of all CTAs cover the matrix exactly once; the activation copies are
+16-byte multiples.  The constants mirror gemv.cu (16 compute warps, ~20 KB
+stages, 2..8 stage ring, 64-byte slot slack, 512-byte header)."""
+import pytest
+
+import synth
+
+NW, SLOT_SLACK, HEAD = 16, 64, 512
+UPB = {synth.Q8_0: 1, synth.Q4_K: 8, synth.Q6_K: 4}
+SMEM_MAX = 232448        # GB300 opt-in shared memory per block
+SMS = 152
+OVERREAD = {synth.Q8_0: 38, synth.Q4_K: 144, synth.Q6_K: 214}  # last byte read + 1, per block
+
+
+def align(v, a):
+    return (v + a - 1) // a * a
+
+
+def plan(qtype, M, K):
+    BB = synth.BLOCK_BYTES[qtype]
+    rb = (32 // UPB[qtype]) * BB
+    MT = 1 if M <= 1 else 2 if M <= 2 else 4 if M <= 4 else 8
+    xd_ld = align(K // 32, 4)
+    xs_ld = align(K // 16, 4)
+    xq_b, xd_b, xs_b = align(MT * K, 16), align(MT * xd_ld * 4, 16), align(MT * xs_ld * 4, 16)
+    nr = max(NW, NW * ((20480 + NW * rb // 2) // (NW * rb)))
+    while nr >= NW // 2:
+        slot = align(nr * rb + SLOT_SLACK, 128)
+        for ns in range(8, 1, -1):
+            off = HEAD
+            off = align(off + ns * nr * MT * 4, 128)
+            off = align(off + xq_b, 128)
+            off = align(off + xd_b, 128)
+            off = align(off + xs_b, 128)
+            if off + ns * slot <= SMEM_MAX:
+                return dict(NR=nr, NS=ns, slot=slot, xd_ld=xd_ld, xs_ld=xs_ld, smem=off + ns * slot)
+        nr = nr - NW if nr > NW else nr - NW // 2
+    return None
+
+
+def check(qtype, N, K, M=1):
+    BB, QK = synth.BLOCK_BYTES[qtype], synth.BLOCK_WEIGHTS[qtype]
+    nb = K // QK
+    RB = nb * BB
+    UPR = nb * UPB[qtype]
+    RPR = (UPR + 31) // 32
+    total = N * RB
+    P = plan(qtype, M, K)
+    assert P is not None
+    assert P["NR"] % NW == 0 or P["NR"] == NW // 2
+    # activation copies
+    for nbytes in (M * K, M * P["xd_ld"] * 4, M * P["xs_ld"] * 4):
+        assert nbytes % 16 == 0
+
+    def rbeg(R):
+        row, rr = divmod(R, RPR)
+        return row * RB + (32 * rr // UPB[qtype]) * BB
+
+    def rend(R):
+        row, rr = divmod(R, RPR)
+        return row * RB + (min(32 * (rr + 1), UPR) // UPB[qtype]) * BB
+
+    grid = min(SMS, N)
+    covered = []
+    for c in range(grid):
+        r0, r1 = N * c // grid, N * (c + 1) // grid
+        cta_byte = r0 * RB
+        Wc = cta_byte & ~15
+        cta_off = cta_byte & 15
+        avail = total - Wc
+        nrounds = (r1 - r0) * RPR
+        nstages = -(-nrounds // P["NR"])
+        for s in range(nstages):
+            R0, R1 = s * P["NR"], min((s + 1) * P["NR"], nrounds)
+            a, b = cta_off + rbeg(R0), cta_off + rend(R1 - 1)
+            a16 = a & ~15
+            b16 = (b + 15) & ~15
+            tail = 0
+            if b16 > avail:
+                b16 = b & ~15
+                tail = b - b16
+            nbytes = b16 - a16
+            assert (Wc + a16) % 16 == 0 and nbytes % 16 == 0 and nbytes >= 0
+            assert Wc + b16 <= total and Wc + b16 + tail <= total
+            assert b - a16 <= P["slot"]
+            covered.append((Wc + a, Wc + b))
+            # every lane's block inside the stage's bytes, over-read inside the slot
+            for R in range(R0, R1):
+                row, rr = divmod(R, RPR)
+                nu = min(32, UPR - 32 * rr)
+                for lane in range(nu):
+                    kb = (32 * rr + lane) // UPB[qtype]
+                    blk = cta_off + row * RB + kb * BB - a16      # offset in the slot
+                    assert blk >= a - a16 and blk + BB <= b - a16
+                    assert blk + OVERREAD[qtype] <= P["slot"]
+                    assert blk % 2 == 0
+                    if qtype == synth.Q4_K:
+                        assert blk % 16 == 0
+    covered.sort()
+    assert covered[0][0] == 0 and covered[-1][1] == total
+    for (x0, x1), (y0, y1) in zip(covered, covered[1:]):
+        assert x1 == y0
+
+
+SHAPES = [(q, N, K) for (_, q, K, N) in
+          synth.LLAMA_1B + synth.QWEN3_14B_LAYER + synth.LM_HEAD + synth.Q8_SMALL]
+SHAPES += [(synth.Q4_K, 37, 256), (synth.Q4_K, 300, 1280), (synth.Q6_K, 37, 256),
+           (synth.Q6_K, 301, 1280), (synth.Q6_K, 65, 5120), (synth.Q6_K, 8, 17408),
+           (synth.Q8_0, 33, 32), (synth.Q8_0, 100, 1056), (synth.Q8_0, 17, 4096),
+           (synth.Q8_0, 1, 96), (synth.Q6_K, 1000, 768), (synth.Q6_K, 153, 256 * 7)]
+
+
+@pytest.mark.parametrize("qtype,N,K", SHAPES)
+def test_gemv_address_arithmetic(qtype, N, K):
+    check(qtype, N, K)
+
+
+@pytest.mark.parametrize("M", [2, 3, 4, 8])
+def test_gemv_plan_fits_multi_slot(M):
+    for (_, q, K, N) in synth.QWEN3_14B_LAYER:
+        assert plan(q, M, K) is not None
+        check(q, min(N, 400), K, M)
