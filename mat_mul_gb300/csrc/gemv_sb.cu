@@ -1,0 +1,593 @@
+// gemv_sb.cu -- decode product y[M,N] = W[N,K] . x[M,K]^T for small M with
+// one weight block per lane: a whole 256-weight super-block for Q4_K/Q6_K,
+// one 32-weight block for Q8_0.
+//
+// Design (sm_103a):
+//   * One CTA per SM owns a contiguous range of whole output rows.  Its
+//     blocks, in memory order, are split evenly (to one block) between
+//     twelve warps.
+//   * Every warp streams its own slice through a private ring of stages of
+//     32 blocks with 1-D bulk async copies (cp.async.bulk + mbarrier, issued
+//     by lane 0), so each SM keeps ~80-160 KB in flight.  Q6_K/Q8_0 blocks
+//     are only 2-byte aligned: a stage is copied from its start rounded down
+//     to 16 bytes and indexed from the remainder.
+//   * Lane i computes block i of the stage with exact int32 dp4a dot products
+//     against the quantised activations in shared memory; the per-block
+//     scale handling (six-bit scales and mins, 16-weight groups) is amortised
+//     over 256 weights.  The activations are stored with their 16-byte chunks
+//     XOR-swizzled per super-block so lanes reading consecutive super-blocks
+//     hit distinct banks.
+//   * A segmented shuffle scan sums the lanes of each row inside a stage;
+//     rows crossing stages carry in registers; rows cut by a warp boundary
+//     are parked in shared memory and added in warp order after a final CTA
+//     barrier.  Every y element is produced once, in a fixed order.
+//   * All waits are bounded mbarrier waits; the quantiser runs just before
+//     with programmatic dependent launch, so the weight stream starts first.
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace qk {
+
+namespace {
+
+constexpr int NWARP = 12;
+constexpr int NTHREADS = NWARP * 32;
+constexpr int SU = 32;           // blocks per stage (one per lane)
+constexpr int HEAD_BYTES = 2048; // mbarriers and warp-edge records
+constexpr int MAX_NSW = 6;
+
+struct SbParams {
+    const uint8_t *W;
+    int64_t total_bytes;  // N * RB
+    int64_t N;
+    int K, M;
+    int nb;  // blocks per row
+    int RB;  // bytes per row
+    int NSW, slot_bytes;
+    int64_t rows_q;  // N / gridDim.x
+    int rows_r;      // N % gridDim.x: the first rows_r CTAs take one row more
+    const float *x;  // [M][K] activations, fp32
+    int x_vec;       // x is 16-byte aligned: load four at a time
+    int q_ld, d_ld, s16_ld;
+    float *y;
+    int off_edge, off_xq, off_xd, off_xaux, off_ring;
+    int *status;
+};
+
+__device__ __forceinline__ uint4 ld16(const uint8_t *sm, int off) {
+    return *reinterpret_cast<const uint4 *>(sm + off);
+}
+
+// n consecutive 32-bit words at byte offset `off` of shared memory (any
+// alignment): aligned words loaded and funnel-shifted into place.
+template <int N>
+__device__ __forceinline__ void ld_words(const uint8_t *sm, int off, uint32_t (&w)[N]) {
+    const uint32_t *a = reinterpret_cast<const uint32_t *>(sm + (off & ~3));
+    const uint32_t sh = static_cast<uint32_t>(off & 3) * 8u;
+    uint32_t prev = a[0];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const uint32_t next = a[i + 1];
+        w[i] = __funnelshift_r(prev, next, sh);
+        prev = next;
+    }
+}
+
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+
+// a as four unsigned bytes, b as four signed bytes
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+struct XS {
+    const uint8_t *sm;
+    int xq, xd, xaux;
+    int q_ld, d_ld, s16_ld;
+};
+
+// Shared-memory byte offset of 16-byte chunk c of super-block kb, row m.
+__device__ __forceinline__ int xchunk(const XS &X, int m, int kb, int c) {
+    return X.xq + m * X.q_ld + kb * 256 + ((c ^ (kb & 7)) << 4);
+}
+
+// ---- Q4_K: w = d*sc*q - dmin*m over eight 32-weight sub-blocks ----------
+//   y += d * sum_j dx_j*sc_j*I_j  -  dmin * sum_j m_j*(dx_j*s_j)
+// I_j for odd j uses the high nibbles in place (x16), folded into d/16.
+template <int MT>
+__device__ __forceinline__ void sb_q4k(const XS &X, int blk, int kb, float (&v)[MT]) {
+    const uint8_t *sm = X.sm;
+    const uint4 hdr = ld16(sm, blk);
+    const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
+    const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, mn_lo = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t mn_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    int sc[8];
+    float mf[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t sw = j < 4 ? sc_lo : sc_hi, mw = j < 4 ? mn_lo : mn_hi;
+        sc[j] = static_cast<int>((sw >> (8 * (j & 3))) & 0xFF);
+        mf[j] = static_cast<float>((mw >> (8 * (j & 3))) & 0xFF);
+    }
+    uint4 q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = ld16(sm, blk + 16 + 16 * i);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const float *dx = reinterpret_cast<const float *>(sm + X.xd + 4 * (m * X.d_ld + kb * 8));
+        const float *ds = reinterpret_cast<const float *>(sm + X.xaux + 4 * (m * X.d_ld + kb * 8));
+        const float4 dx0 = *reinterpret_cast<const float4 *>(dx), dx1 = *reinterpret_cast<const float4 *>(dx + 4);
+        const float4 ds0 = *reinterpret_cast<const float4 *>(ds), ds1 = *reinterpret_cast<const float4 *>(ds + 4);
+        const float dxs[8] = {dx0.x, dx0.y, dx0.z, dx0.w, dx1.x, dx1.y, dx1.z, dx1.w};
+        float acc_min = mf[0] * ds0.x;
+        acc_min += mf[1] * ds0.y;
+        acc_min += mf[2] * ds0.z;
+        acc_min += mf[3] * ds0.w;
+        acc_min += mf[4] * ds1.x;
+        acc_min += mf[5] * ds1.y;
+        acc_min += mf[6] * ds1.z;
+        acc_min += mf[7] * ds1.w;
+        float acc_lo = 0.0f, acc_hi = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 qa = q[2 * c], qb = q[2 * c + 1];
+            const uint4 x0 = ld16(sm, xchunk(X, m, kb, 4 * c));
+            const uint4 x1 = ld16(sm, xchunk(X, m, kb, 4 * c + 1));
+            const uint4 x2 = ld16(sm, xchunk(X, m, kb, 4 * c + 2));
+            const uint4 x3 = ld16(sm, xchunk(X, m, kb, 4 * c + 3));
+            constexpr uint32_t LO = 0x0F0F0F0Fu, HI = 0xF0F0F0F0u;
+            int I0 = dp4a_ss(qa.x & LO, x0.x, 0);
+            I0 = dp4a_ss(qa.y & LO, x0.y, I0);
+            I0 = dp4a_ss(qa.z & LO, x0.z, I0);
+            I0 = dp4a_ss(qa.w & LO, x0.w, I0);
+            I0 = dp4a_ss(qb.x & LO, x1.x, I0);
+            I0 = dp4a_ss(qb.y & LO, x1.y, I0);
+            I0 = dp4a_ss(qb.z & LO, x1.z, I0);
+            I0 = dp4a_ss(qb.w & LO, x1.w, I0);
+            int I1 = dp4a_us(qa.x & HI, x2.x, 0);
+            I1 = dp4a_us(qa.y & HI, x2.y, I1);
+            I1 = dp4a_us(qa.z & HI, x2.z, I1);
+            I1 = dp4a_us(qa.w & HI, x2.w, I1);
+            I1 = dp4a_us(qb.x & HI, x3.x, I1);
+            I1 = dp4a_us(qb.y & HI, x3.y, I1);
+            I1 = dp4a_us(qb.z & HI, x3.z, I1);
+            I1 = dp4a_us(qb.w & HI, x3.w, I1);
+            acc_lo += dxs[2 * c] * static_cast<float>(sc[2 * c] * I0);
+            acc_hi += dxs[2 * c + 1] * static_cast<float>(sc[2 * c + 1] * I1);
+        }
+        v[m] += d * acc_lo + (d * 0.0625f) * acc_hi - dmin * acc_min;
+    }
+}
+
+// ---- Q6_K: w = d*sc*(q-32), sixteen 16-weight groups ---------------------
+//   y += d * sum_g dx_g * sc_g * (sum q*x - 32 * sum x)
+template <int MT>
+__device__ __forceinline__ void sb_q6k(const XS &X, int blk, int kb, float (&v)[MT]) {
+    const uint8_t *sm = X.sm;
+    uint32_t scw[4];
+    ld_words<4>(sm, blk + 192, scw);
+    const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(sm + blk + 208));
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t ql[16], qh[8];
+        ld_words<16>(sm, blk + 64 * h, ql);
+        ld_words<8>(sm, blk + 128 + 32 * h, qh);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            uint32_t q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t src = ql[(g & 1) * 8 + e];
+                const uint32_t lo = ((g & 2) ? (src >> 4) : src) & 0x0F0F0F0Fu;
+                uint32_t hi;
+                if (g == 0) hi = (qh[e] << 4) & 0x30303030u;
+                else if (g == 1) hi = (qh[e] << 2) & 0x30303030u;
+                else if (g == 2) hi = qh[e] & 0x30303030u;
+                else hi = (qh[e] >> 2) & 0x30303030u;
+                q[e] = lo | hi;
+            }
+            const int si = 8 * h + 2 * g;  // scales si, si+1
+            const int sa = static_cast<int>(static_cast<int8_t>((scw[si >> 2] >> (8 * (si & 3))) & 0xFF));
+            const int sb = static_cast<int>(static_cast<int8_t>((scw[si >> 2] >> (8 * ((si + 1) & 3))) & 0xFF));
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const uint4 xa = ld16(sm, xchunk(X, m, kb, 8 * h + 2 * g));
+                const uint4 xb = ld16(sm, xchunk(X, m, kb, 8 * h + 2 * g + 1));
+                const int2 s2 = *reinterpret_cast<const int2 *>(
+                    sm + X.xaux + 4 * (m * X.s16_ld + kb * 16 + 8 * h + 2 * g));
+                int Ia = dp4a_ss(q[0], xa.x, -32 * s2.x);
+                Ia = dp4a_ss(q[1], xa.y, Ia);
+                Ia = dp4a_ss(q[2], xa.z, Ia);
+                Ia = dp4a_ss(q[3], xa.w, Ia);
+                int Ib = dp4a_ss(q[4], xb.x, -32 * s2.y);
+                Ib = dp4a_ss(q[5], xb.y, Ib);
+                Ib = dp4a_ss(q[6], xb.z, Ib);
+                Ib = dp4a_ss(q[7], xb.w, Ib);
+                const float dxg = *reinterpret_cast<const float *>(
+                    sm + X.xd + 4 * (m * X.d_ld + kb * 8 + 4 * h + g));
+                acc[m] += dxg * static_cast<float>(sa * Ia + sb * Ib);
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) v[m] += d * acc[m];
+}
+
+// ---- Q8_0: w = d*q, one 32-weight block ----------------------------------
+template <int MT>
+__device__ __forceinline__ void sb_q80(const XS &X, int blk, int kb, float (&v)[MT]) {
+    const uint8_t *sm = X.sm;
+    uint32_t qw[8];
+    ld_words<8>(sm, blk + 2, qw);
+    const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(sm + blk));
+    const int sbk = kb >> 3, j = kb & 7;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const uint4 x0 = ld16(sm, xchunk(X, m, sbk, 2 * j));
+        const uint4 x1 = ld16(sm, xchunk(X, m, sbk, 2 * j + 1));
+        int I = dp4a_ss(qw[0], x0.x, 0);
+        I = dp4a_ss(qw[1], x0.y, I);
+        I = dp4a_ss(qw[2], x0.z, I);
+        I = dp4a_ss(qw[3], x0.w, I);
+        I = dp4a_ss(qw[4], x1.x, I);
+        I = dp4a_ss(qw[5], x1.y, I);
+        I = dp4a_ss(qw[6], x1.z, I);
+        I = dp4a_ss(qw[7], x1.w, I);
+        const float dx = *reinterpret_cast<const float *>(sm + X.xd + 4 * (m * X.d_ld + kb));
+        v[m] += dx * (d * static_cast<float>(I));
+    }
+}
+
+// ---- the activation quantiser, into shared memory --------------------------
+// Same arithmetic as the standalone quantiser (and the oracle): per block of
+// 32, amax = max|x|, d = amax/127, inv = 1/d (0 if d == 0; the correctly
+// rounded reciprocal equals the IEEE quotient 1/d), q = round half away from
+// zero of x*inv clamped to +-127.  One thread per block: its 128 bytes of x
+// are loaded by eight independent 16-byte loads.  Writes the swizzled q, the
+// scale d, and d*sum (Q4_K) or the two half-block sums (Q6_K).
+template <int T>
+__device__ __forceinline__ void quantize_to_smem(const SbParams &P, uint8_t *smem) {
+    const int nb32 = P.K / 32;
+    const int total = P.M * nb32;
+    for (int id = threadIdx.x; id < total; id += NTHREADS) {
+        const int m = id / nb32, b = id - m * nb32;
+        const float *src = P.x + static_cast<int64_t>(m) * P.K + 32 * b;
+        float a[32];
+        if (P.x_vec) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + i);
+                a[4 * i] = v.x; a[4 * i + 1] = v.y; a[4 * i + 2] = v.z; a[4 * i + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = __ldg(src + i);
+        }
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(a[i]));
+        const float db = __fdiv_rn(am, 127.0f);
+        const float inv = (db != 0.0f) ? __frcp_rn(db) : 0.0f;
+        uint32_t w[8];
+        int s_lo = 0, s_hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int q = static_cast<int>(fminf(fmaxf(roundf(__fmul_rn(a[4 * i + e], inv)), -127.0f), 127.0f));
+                if (i < 4) s_lo += q; else s_hi += q;
+                word |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * e);
+            }
+            w[i] = word;
+        }
+        // the two 16-byte chunks of this block, swizzled within its super-block
+        const int sb = b >> 3, c0 = (2 * (b & 7)) ^ (sb & 7), c1 = (2 * (b & 7) + 1) ^ (sb & 7);
+        uint8_t *row = smem + P.off_xq + m * P.q_ld + sb * 256;
+        *reinterpret_cast<uint4 *>(row + 16 * c0) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(row + 16 * c1) = make_uint4(w[4], w[5], w[6], w[7]);
+        reinterpret_cast<float *>(smem + P.off_xd)[m * P.d_ld + b] = db;
+        if (T == QMM_Q4_K)
+            reinterpret_cast<float *>(smem + P.off_xaux)[m * P.d_ld + b] = db * static_cast<float>(s_lo + s_hi);
+        if (T == QMM_Q6_K)
+            *reinterpret_cast<int2 *>(smem + P.off_xaux + 4 * (m * P.s16_ld + 2 * b)) = make_int2(s_lo, s_hi);
+    }
+}
+
+template <int T, int MT>
+__global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_kernel(const __grid_constant__ SbParams P) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int BB = Fmt<T>::BB;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int cta = blockIdx.x;
+    const int64_t r0 = P.rows_q * cta + min(cta, P.rows_r);
+    const int64_t r1 = r0 + P.rows_q + (cta < P.rows_r ? 1 : 0);
+    const int U = static_cast<int>(r1 - r0) * P.nb;  // blocks of this CTA
+    const int uw0 = static_cast<int>((static_cast<int64_t>(U) * warp) / NWARP);
+    const int uw1 = static_cast<int>((static_cast<int64_t>(U) * (warp + 1)) / NWARP);
+    const int nst = (uw1 - uw0 + SU - 1) / SU;
+
+    const uint32_t bar0 = smem_u32(smem);
+    int *edge_row = reinterpret_cast<int *>(smem + P.off_edge);
+    float *edge_val = reinterpret_cast<float *>(edge_row + 2 * NWARP);
+
+    // Each warp's lane 0 sets up its own barriers and starts its stream at
+    // once; warp 0 clears the edge records (read only after the CTA barrier
+    // that follows the activation quantiser).
+    const uint32_t my_bar = bar0 + 8u * warp * MAX_NSW;
+    if (lane == 0) {
+        for (int i = 0; i < P.NSW; ++i) mbar_init(my_bar + 8u * i, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane < 2 * NWARP) edge_row[lane] = -1;
+    __syncwarp();
+
+    // weights of this CTA, relative to its first byte rounded down to 16
+    const int64_t cta_byte = r0 * P.RB;
+    const uint8_t *Wc = P.W + (cta_byte & ~int64_t(15));
+    const int cta_off = static_cast<int>(cta_byte & 15);
+    const int64_t avail = P.total_bytes - (cta_byte & ~int64_t(15));
+    const int ring = P.off_ring + warp * P.NSW * P.slot_bytes;
+
+    // issue stage t of this warp into slot t % NSW (lane 0 only)
+    auto issue = [&](int t, uint64_t pol) {
+        const int slot = t % P.NSW;
+        const int u0 = uw0 + SU * t, u1 = min(u0 + SU, uw1);
+        const int a = cta_off + u0 * BB, b = cta_off + u1 * BB;
+        const int a16 = a & ~15;
+        int b16 = (b + 15) & ~15;
+        const int dst = ring + slot * P.slot_bytes;
+        if (b16 > avail) {  // the last bytes of the matrix: plain loads for the tail
+            b16 = b & ~15;
+            for (int i = b16; i < b; ++i) smem[dst + (i - a16)] = Wc[i];
+        }
+        const uint32_t nbytes = static_cast<uint32_t>(b16 - a16);
+        mbar_arrive_expect_tx(my_bar + 8u * slot, nbytes);
+        if (nbytes) bulk_g2s(smem_u32(smem + dst), Wc + a16, nbytes, my_bar + 8u * slot, pol);
+    };
+
+    uint64_t pol_w = 0;
+    int issued = 0;
+    if (lane == 0) {
+        pol_w = policy_evict_first();
+        for (; issued < min(P.NSW, nst); ++issued) issue(issued, pol_w);
+    }
+    // The weights are read-only here, so streaming them may begin before the
+    // preceding kernel on the stream has finished; the activations and y may
+    // not be touched before it has.  Let the next kernel start launching too.
+    pdl_trigger();
+    pdl_wait();
+    quantize_to_smem<T>(P, smem);
+    __syncthreads();
+
+    XS X;
+    X.sm = smem;
+    X.xq = P.off_xq;
+    X.xd = P.off_xd;
+    X.xaux = P.off_xaux;
+    X.q_ld = P.q_ld;
+    X.d_ld = P.d_ld;
+    X.s16_ld = P.s16_ld;
+
+    bool failed = false;
+    int carry_row = -1;
+    float carry[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) carry[m] = 0.0f;
+    int consumed = 0;
+    for (int t = 0; t < nst && !failed; ++t) {
+        const int slot = t % P.NSW;
+        if (!mbar_wait(my_bar + 8u * slot, static_cast<uint32_t>((t / P.NSW) & 1), P.status)) {
+            failed = true;
+            break;
+        }
+        consumed = t + 1;
+        const int u0 = uw0 + SU * t, u1 = min(u0 + SU, uw1), nv = u1 - u0;
+        const int a16 = (cta_off + u0 * BB) & ~15;
+        // shared-memory offset of CTA-relative block 0 for this stage
+        const int base = ring + slot * P.slot_bytes - a16 + cta_off;
+        const int u = u0 + lane;
+        const bool valid = lane < nv;
+        const int row = valid ? u / P.nb : -1;
+        float v[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) v[m] = 0.0f;
+        if (valid) {
+            const int kb = u - row * P.nb;
+            const int blk = base + u * BB;
+            if constexpr (T == QMM_Q4_K) sb_q4k<MT>(X, blk, kb, v);
+            else if constexpr (T == QMM_Q6_K) sb_q6k<MT>(X, blk, kb, v);
+            else sb_q80<MT>(X, blk, kb, v);
+        }
+        __syncwarp();
+        if (lane == 0 && issued < nst) {
+            // the slot just read is refilled: order the reads before the async write
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(issued, pol_w);
+            ++issued;
+        }
+        // segmented suffix sums: lane i gets the sum of its row over lanes i..seg_last
+        const int row_start = row * P.nb, row_end = row_start + P.nb;
+        const int seg_last = valid ? min(nv, row_end - u0) - 1 : -1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const float o = __shfl_down_sync(0xffffffffu, v[m], off);
+                if (lane + off <= seg_last) v[m] += o;
+            }
+        }
+        const bool head = valid && (lane == 0 || u == row_start);
+        if (head && lane == 0 && row == carry_row) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) v[m] += carry[m];
+        }
+        // the stage's last row continues into this warp's next stage?
+        const int row_last = (u1 - 1) / P.nb;
+        const int head_last = max(0, row_last * P.nb - u0);
+        const bool cont = (row_last + 1) * P.nb > u1 && u1 < uw1;
+        if (head && !(cont && row == row_last)) {
+            if (row_start < uw0 || row_end > uw1) {
+                const int e = 2 * warp + (row_start < uw0 ? 0 : 1);
+                edge_row[e] = row;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) edge_val[e * 8 + m] = v[m];
+            } else {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    if (m < P.M) P.y[static_cast<int64_t>(m) * P.N + r0 + row] = v[m];
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) carry[m] = __shfl_sync(0xffffffffu, v[m], head_last);
+        carry_row = cont ? row_last : -1;
+    }
+    // no bulk copy may still be in flight when the CTA exits
+    if (lane == 0)
+        for (int t = consumed; t < issued; ++t)
+            mbar_wait(my_bar + 8u * (t % P.NSW), static_cast<uint32_t>((t / P.NSW) & 1), P.status);
+    __syncthreads();
+    if (warp == 0) {
+        // Rows cut by warp boundaries: record e = 2w + {0, 1} holds warp w's
+        // partial of its first / last row.  Rows are nondecreasing in e; the
+        // first record of each row adds the others in record order.
+        const int e = lane;
+        const int r = e < 2 * NWARP ? edge_row[e] : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, r);
+        float acc[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+        for (int j = 0; j < 2 * NWARP; ++j) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const float vj = __shfl_sync(0xffffffffu, r >= 0 ? edge_val[(e < 2 * NWARP ? e : 0) * 8 + m] : 0.0f, j);
+                if ((same >> j) & 1u) acc[m] += vj;
+            }
+        }
+        if (r >= 0 && (__ffs(same) - 1) == lane) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < P.M) P.y[static_cast<int64_t>(m) * P.N + r0 + r] = acc[m];
+        }
+    }
+}
+
+int mt_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+int64_t align64(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+// Shared-memory plan: header | activations | NWARP rings of NSW stages.
+bool plan_sb(int type, int M, int64_t K, int max_smem, SbParams &P, int &smem) {
+    const int MT = mt_of(M);
+    const int BB = block_bytes(type);
+    const int64_t q_ld = align64(K, 256);
+    const int64_t d_ld = align64(K / 32, 4);
+    const int64_t s16_ld = align64(K / 16, 4);
+    int64_t off = HEAD_BYTES;
+    const int64_t o_xq = off;
+    off = align64(off + MT * q_ld, 128);
+    const int64_t o_xd = off;
+    off = align64(off + MT * d_ld * 4, 128);
+    const int64_t o_xaux = off;
+    if (type == QMM_Q4_K) off = align64(off + MT * d_ld * 4, 128);
+    if (type == QMM_Q6_K) off = align64(off + MT * s16_ld * 4, 128);
+    const int64_t o_ring = off;
+    const int64_t slot = align64(static_cast<int64_t>(SU) * BB + 32, 128);
+    int64_t nsw = (max_smem - o_ring) / (NWARP * slot);
+    if (nsw > MAX_NSW) nsw = MAX_NSW;
+    if (nsw < 2) return false;
+    P.NSW = static_cast<int>(nsw);
+    P.slot_bytes = static_cast<int>(slot);
+    P.off_edge = 8 * NWARP * MAX_NSW;
+    P.q_ld = static_cast<int>(q_ld);
+    P.d_ld = static_cast<int>(d_ld);
+    P.s16_ld = static_cast<int>(s16_ld);
+    P.off_xq = static_cast<int>(o_xq);
+    P.off_xd = static_cast<int>(o_xd);
+    P.off_xaux = static_cast<int>(o_xaux);
+    P.off_ring = static_cast<int>(o_ring);
+    smem = static_cast<int>(o_ring + NWARP * nsw * slot);
+    return true;
+}
+
+template <int T, int MT>
+cudaError_t launch_t(const SbParams &P, int grid, int smem, cudaStream_t st) {
+    auto kfn = gemv_sb_kernel<T, MT>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kfn, P);
+}
+
+template <int T>
+cudaError_t launch_m(const SbParams &P, int MT, int grid, int smem, cudaStream_t st) {
+    switch (MT) {
+    case 1: return launch_t<T, 1>(P, grid, smem, st);
+    case 2: return launch_t<T, 2>(P, grid, smem, st);
+    case 4: return launch_t<T, 4>(P, grid, smem, st);
+    default: return launch_t<T, 8>(P, grid, smem, st);
+    }
+}
+
+}  // namespace
+
+bool gemv_sb_fits(int type, int M, int64_t K, int max_smem) {
+    if (M < 1 || M > 8 || K > (1 << 22)) return false;
+    SbParams P = {};
+    int smem = 0;
+    return plan_sb(type, M, K, max_smem, P, smem);
+}
+
+cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const float *x, int M,
+                           float *y, cudaStream_t st, int num_sms, int max_smem, int *status) {
+    SbParams P = {};
+    int smem = 0;
+    if (!plan_sb(type, M, K, max_smem, P, smem)) return cudaErrorInvalidValue;
+    const int BB = block_bytes(type);
+    P.W = static_cast<const uint8_t *>(W);
+    P.N = N;
+    P.K = static_cast<int>(K);
+    P.M = M;
+    P.nb = static_cast<int>(K / block_weights(type));
+    P.RB = P.nb * BB;
+    P.total_bytes = N * static_cast<int64_t>(P.RB);
+    P.x = x;
+    P.x_vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0 ? 1 : 0;
+    P.y = y;
+    P.status = status;
+    // one CTA per SM; more when a CTA's bytes would not fit 31 bits
+    int64_t grid = num_sms;
+    const int64_t max_rows = (int64_t(1) << 30) / P.RB;
+    if ((N + grid - 1) / grid > max_rows) grid = (N + max_rows - 1) / max_rows;
+    if (N < grid) grid = N;
+    if (grid < 1) grid = 1;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    const int g = static_cast<int>(grid);
+    P.rows_q = N / g;
+    P.rows_r = static_cast<int>(N % g);
+    switch (type) {
+    case QMM_Q8_0: return launch_m<QMM_Q8_0>(P, mt_of(M), g, smem, st);
+    case QMM_Q4_K: return launch_m<QMM_Q4_K>(P, mt_of(M), g, smem, st);
+    default: return launch_m<QMM_Q6_K>(P, mt_of(M), g, smem, st);
+    }
+}
+
+}  // namespace qk

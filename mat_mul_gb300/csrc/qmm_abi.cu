@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -14,24 +15,17 @@
 #include "../../include/qmm.h"
 #include "qmm_device.cuh"
 
-namespace qk {
-cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, int8_t *q, int64_t q_ld, float *d,
-                            int32_t *s, int64_t ds_ld, int64_t s_ld, bool sum16, cudaStream_t st,
-                            bool trigger_dependents, int num_sms);
-cudaError_t launch_dequant(int type, const void *blocks, int64_t n_elems, float *out,
-                           cudaStream_t st, int num_sms);
-cudaError_t launch_gemv(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
-                        const float *xd, const int32_t *xs, int xd_ld, int xs_ld, int M, float *y,
-                        cudaStream_t st, bool pdl, int num_sms, int max_smem, int *status);
-bool gemv_fits(int type, int M, int64_t K, int xd_ld, int xs_ld, int max_smem);
-cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
-                            const float *xd, const int32_t *xs, int xd_ld, int64_t M, float *y,
-                            cudaStream_t st);
-}  // namespace qk
+#include "qmm_internal.h"
 
 namespace {
 
 thread_local char g_err[512] = "";
+// QMM_DECODE_KERNEL=rounds selects the round-based decode kernel wherever the
+// block-per-lane one would run (for comparisons; read once at load).
+const bool g_force_round_gemv = [] {
+    const char *v = getenv("QMM_DECODE_KERNEL");
+    return v && strcmp(v, "rounds") == 0;
+}();
 std::atomic<int64_t> g_launches{0};
 
 int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -179,8 +173,13 @@ int qmm_quantize_act(const float *x, int64_t M, int64_t K, int8_t *q, float *d, 
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     DeviceInfo di;
     if (int rc = device_info(dev, di)) return rc;
-    e = qk::launch_quantize(x, M, K, q, K, d, s, K / 32, K / 32, false,
-                            static_cast<cudaStream_t>(stream), false, di.num_sms);
+    qk::QuantOut o = {};
+    o.q = q;
+    o.q_ld = K;
+    o.d = d;
+    o.s32 = s;
+    o.d_ld = K / 32;
+    e = qk::launch_quantize(x, M, K, o, static_cast<cudaStream_t>(stream), false, di.num_sms);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     g_launches.fetch_add(1);
     return QMM_OK;
@@ -215,31 +214,48 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     DeviceInfo di;
     if (int rc = device_info(dev, di)) return rc;
 
-    // workspace: q int8 [M][K] | d fp32 [M][xd_ld] | s int32 [M][xs_ld]
-    // xd_ld = K/32 and xs_ld = K/16 (decode: sums per 16-element half block)
-    // or K/32 (prefill: sums per block), both rounded up to 4.
-    const int xd_ld = static_cast<int>(align_up(static_cast<size_t>(K / 32), 4));
-    const int xs16_ld = static_cast<int>(align_up(static_cast<size_t>(K / 16), 4));
-    const bool decode = M <= 8 && qk::gemv_fits(type, static_cast<int>(M), K, xd_ld, xs16_ld, di.max_smem);
-    const int xs_ld = decode ? xs16_ld : xd_ld;
+    // Three paths, chosen by M and by what fits in shared memory:
+    //   sb   : decode, one weight block per lane, quantises x itself (one
+    //          launch, no workspace); M <= 8 when the activations fit
+    //   gemv : decode, 32 units per round, after the quantiser kernel
+    //   gemm : prefill on the integer tensor cores, after the quantiser
+    if (M <= 8 && !g_force_round_gemv && qk::gemv_sb_fits(type, static_cast<int>(M), K, di.max_smem)) {
+        e = qk::launch_gemv_sb(type, W_blocks, N, K, x, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
+                               di.status);
+        if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+        g_launches.fetch_add(1);
+        return QMM_OK;
+    }
+    // Workspace (per device and stream): q int8 [M][K] | d fp32 [M][d_ld] |
+    // s16 int32 [M][s16_ld] (gemv) or s32 int32 [M][d_ld] (gemm).
+    const int64_t d_ld = static_cast<int64_t>(align_up(static_cast<size_t>(K / 32), 4));
+    const int64_t s16_ld = static_cast<int64_t>(align_up(static_cast<size_t>(K / 16), 4));
+    const bool gemv = M <= 8 && qk::gemv_fits(type, static_cast<int>(M), K, static_cast<int>(d_ld),
+                                               static_cast<int>(s16_ld), di.max_smem);
     const size_t q_bytes = align_up(static_cast<size_t>(M * K), 256);
-    const size_t d_bytes = align_up(static_cast<size_t>(M) * xd_ld * 4, 256);
-    const size_t s_bytes = align_up(static_cast<size_t>(M) * xs_ld * 4, 256);
+    const size_t d_bytes = align_up(static_cast<size_t>(M * d_ld) * 4, 256);
+    const size_t a_bytes = align_up(static_cast<size_t>(M * (gemv ? s16_ld : d_ld)) * 4, 256);
     void *ws = nullptr;
-    if (int rc = workspace(dev, st, q_bytes + d_bytes + s_bytes, &ws)) return rc;
-    auto *xq = static_cast<int8_t *>(ws);
-    auto *xd = reinterpret_cast<float *>(static_cast<char *>(ws) + q_bytes);
-    auto *xs = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + q_bytes + d_bytes);
-
-    e = qk::launch_quantize(x, M, K, xq, K, xd, xs, xd_ld, xs_ld, decode, st, decode, di.num_sms);
+    if (int rc = workspace(dev, st, q_bytes + d_bytes + a_bytes, &ws)) return rc;
+    char *wsb = static_cast<char *>(ws);
+    qk::QuantOut o = {};
+    o.q = reinterpret_cast<int8_t *>(wsb);
+    o.q_ld = K;
+    o.d = reinterpret_cast<float *>(wsb + q_bytes);
+    o.d_ld = d_ld;
+    o.s16_ld = s16_ld;
+    if (gemv) o.s16 = reinterpret_cast<int32_t *>(wsb + q_bytes + d_bytes);
+    else o.s32 = reinterpret_cast<int32_t *>(wsb + q_bytes + d_bytes);
+    e = qk::launch_quantize(x, M, K, o, st, gemv, di.num_sms);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     g_launches.fetch_add(1);
-    if (decode) {
-        e = qk::launch_gemv(type, W_blocks, N, K, xq, xd, xs, xd_ld, xs_ld, static_cast<int>(M), y, st,
-                            true, di.num_sms, di.max_smem, di.status);
+    if (gemv) {
+        e = qk::launch_gemv(type, W_blocks, N, K, o.q, o.d, o.s16, static_cast<int>(d_ld),
+                            static_cast<int>(s16_ld), static_cast<int>(M), y, st, true, di.num_sms,
+                            di.max_smem, di.status);
         if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
     } else {
-        e = qk::launch_gemm_mma(type, W_blocks, N, K, xq, xd, xs, xd_ld, M, y, st);
+        e = qk::launch_gemm_mma(type, W_blocks, N, K, o.q, o.d, o.s32, static_cast<int>(d_ld), M, y, st);
         if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     }
     g_launches.fetch_add(1);

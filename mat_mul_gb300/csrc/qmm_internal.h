@@ -1,0 +1,54 @@
+// qmm_internal.h -- declarations shared by the translation units of libqmm:
+// the quantiser's output description and every kernel launcher.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qk {
+
+// Output layout of the quantiser.  q rows have stride q_ld bytes; with
+// swizzle != 0 the 16-byte chunk c (0..15) of every 256-element super-block
+// sb is stored at chunk position c ^ (sb & 7), so lanes that read the same
+// chunk of consecutive super-blocks hit distinct shared-memory banks.  Every
+// other output is optional (null = not written):
+//   d   [M][d_ld]   fp32 scale per block of 32
+//   s32 [M][d_ld]   int32 sum per block
+//   s16 [M][s16_ld] int32 sums of the two 16-element halves of every block
+//   dsf [M][d_ld]   fp32 product d * s32 per block
+struct QuantOut {
+    int8_t *q;
+    int64_t q_ld;
+    int swizzle;
+    float *d;
+    int32_t *s32;
+    int32_t *s16;
+    float *dsf;
+    int64_t d_ld, s16_ld;
+};
+
+cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, const QuantOut &o, cudaStream_t st,
+                            bool trigger_dependents, int num_sms);
+
+cudaError_t launch_dequant(int type, const void *blocks, int64_t n_elems, float *out,
+                           cudaStream_t st, int num_sms);
+
+// Round-based decode kernel (gemv.cu): activations q [M][K] (plain layout),
+// d [M][xd_ld], s16 [M][xs_ld].
+bool gemv_fits(int type, int M, int64_t K, int xd_ld, int xs_ld, int max_smem);
+cudaError_t launch_gemv(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
+                        const float *xd, const int32_t *xs, int xd_ld, int xs_ld, int M, float *y,
+                        cudaStream_t st, bool pdl, int num_sms, int max_smem, int *status);
+
+// Block-per-lane decode kernel (gemv_sb.cu): quantises x itself, needs no
+// workspace; launched with programmatic dependent launch.
+bool gemv_sb_fits(int type, int M, int64_t K, int max_smem);
+cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const float *x, int M,
+                           float *y, cudaStream_t st, int num_sms, int max_smem, int *status);
+
+// Prefill GEMM on mma.sync (gemm_mma.cu): q [M][K], d and s32 [M][xd_ld].
+cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
+                            const float *xd, const int32_t *xs, int xd_ld, int64_t M, float *y,
+                            cudaStream_t st);
+
+}  // namespace qk

@@ -8,19 +8,13 @@
 // Every step is a separately rounded IEEE operation, so the output is
 // bit-for-bit the same on every run and equal to a scalar CPU evaluation.
 #include "qmm_device.cuh"
+#include "qmm_internal.h"
 
 namespace qk {
 
 // One warp per block of 32 activations, lane i holding element i.
-// q rows have stride q_ld bytes and d rows ds_ld floats.  With sum16 == 0, s
-// holds one int32 sum per block (rows of ds_ld); with sum16 != 0 it holds the
-// sums of the two 16-element halves of every block (rows of s_ld), the form
-// the decode kernels use.
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x, int64_t M,
-                                                           int64_t K, int8_t *__restrict__ q,
-                                                           int64_t q_ld, float *__restrict__ d,
-                                                           int32_t *__restrict__ s, int64_t ds_ld,
-                                                           int64_t s_ld, int sum16,
+                                                           int64_t K, QuantOut o,
                                                            int trigger_dependents) {
     if (trigger_dependents) pdl_trigger();
     const int lane = threadIdx.x & 31;
@@ -40,25 +34,31 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
         r = fminf(fmaxf(r, -127.0f), 127.0f);
         const int qi = static_cast<int>(r);
         const int sum = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(qi)));
-        q[m * q_ld + 32 * b + lane] = static_cast<int8_t>(qi);
-        if (sum16) {
-            const int lo = static_cast<int>(
-                __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(lane < 16 ? qi : 0)));
-            if (lane == 0) {
-                d[m * ds_ld + b] = db;
-                s[m * s_ld + 2 * b] = lo;
-                s[m * s_ld + 2 * b + 1] = sum - lo;
+        const int64_t k = 32 * b + lane;
+        int64_t pos = k;
+        if (o.swizzle) {
+            const int64_t sb = k >> 8;
+            const int c = static_cast<int>((k >> 4) & 15) ^ static_cast<int>(sb & 7);
+            pos = (sb << 8) + 16 * c + (k & 15);
+        }
+        o.q[m * o.q_ld + pos] = static_cast<int8_t>(qi);
+        int lo = 0;
+        if (o.s16)
+            lo = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(lane < 16 ? qi : 0)));
+        if (lane == 0) {
+            if (o.d) o.d[m * o.d_ld + b] = db;
+            if (o.s32) o.s32[m * o.d_ld + b] = sum;
+            if (o.dsf) o.dsf[m * o.d_ld + b] = db * static_cast<float>(sum);
+            if (o.s16) {
+                o.s16[m * o.s16_ld + 2 * b] = lo;
+                o.s16[m * o.s16_ld + 2 * b + 1] = sum - lo;
             }
-        } else if (lane == 0) {
-            d[m * ds_ld + b] = db;
-            s[m * ds_ld + b] = sum;
         }
     }
 }
 
 // Host launcher.  Grid: enough warps for every block, capped at a few waves.
-cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, int8_t *q, int64_t q_ld, float *d,
-                            int32_t *s, int64_t ds_ld, int64_t s_ld, bool sum16, cudaStream_t st,
+cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, const QuantOut &o, cudaStream_t st,
                             bool trigger_dependents, int num_sms) {
     const int64_t nblk = M * (K / 32);
     const int threads = 256;
@@ -66,8 +66,8 @@ cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, int8_t *q, int
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    quantize_act_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(
-        x, M, K, q, q_ld, d, s, ds_ld, s_ld, sum16 ? 1 : 0, trigger_dependents ? 1 : 0);
+    quantize_act_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(x, M, K, o,
+                                                                        trigger_dependents ? 1 : 0);
     return cudaGetLastError();
 }
 

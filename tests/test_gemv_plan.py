@@ -124,3 +124,83 @@ def test_gemv_plan_fits_multi_slot(M):
     for (_, q, K, N) in synth.QWEN3_14B_LAYER:
         assert plan(q, M, K) is not None
         check(q, min(N, 400), K, M)
+
+
+# ---- the block-per-lane decode kernel (gemv_sb.cu) --------------------------
+SB_NWARP, SB_SU, SB_HEAD, SB_MAXNSW = 12, 32, 2048, 6
+
+
+def plan_sb(qtype, M, K):
+    MT = 1 if M <= 1 else 2 if M <= 2 else 4 if M <= 4 else 8
+    BB = synth.BLOCK_BYTES[qtype]
+    q_ld, d_ld, s16_ld = align(K, 256), align(K // 32, 4), align(K // 16, 4)
+    off = SB_HEAD
+    off = align(off + MT * q_ld, 128)
+    off = align(off + MT * d_ld * 4, 128)
+    if qtype == synth.Q4_K:
+        off = align(off + MT * d_ld * 4, 128)
+    if qtype == synth.Q6_K:
+        off = align(off + MT * s16_ld * 4, 128)
+    slot = align(SB_SU * BB + 32, 128)
+    nsw = min(SB_MAXNSW, (SMEM_MAX - off) // (SB_NWARP * slot))
+    if nsw < 2:
+        return None
+    return dict(NSW=nsw, slot=slot, ring=off, q_ld=q_ld, d_ld=d_ld, s16_ld=s16_ld)
+
+
+def check_sb(qtype, N, K, M=1):
+    BB, QK = synth.BLOCK_BYTES[qtype], synth.BLOCK_WEIGHTS[qtype]
+    nb = K // QK
+    RB = nb * BB
+    total = N * RB
+    P = plan_sb(qtype, M, K)
+    assert P is not None
+    assert SB_NWARP * SB_MAXNSW * 8 + 2 * SB_NWARP * 4 + 2 * SB_NWARP * 8 * 4 <= SB_HEAD
+    for nbytes in (M * P["q_ld"], M * P["d_ld"] * 4, M * P["s16_ld"] * 4):
+        assert nbytes % 16 == 0
+    grid = min(SMS, N)
+    covered = []
+    read_end = {synth.Q8_0: 38, synth.Q4_K: 144, synth.Q6_K: 212}[qtype]
+    q, r = divmod(N, grid)
+    for c in range(grid):
+        r0 = q * c + min(c, r)
+        r1 = r0 + q + (1 if c < r else 0)
+        cta_byte = r0 * RB
+        Wc, cta_off = cta_byte & ~15, cta_byte & 15
+        avail = total - Wc
+        U = (r1 - r0) * nb
+        for w in range(SB_NWARP):
+            uw0, uw1 = U * w // SB_NWARP, U * (w + 1) // SB_NWARP
+            for t in range(-(-(uw1 - uw0) // SB_SU)):
+                u0, u1 = uw0 + SB_SU * t, min(uw0 + SB_SU * (t + 1), uw1)
+                a, b = cta_off + u0 * BB, cta_off + u1 * BB
+                a16, b16 = a & ~15, (b + 15) & ~15
+                tail = 0
+                if b16 > avail:
+                    b16 = b & ~15
+                    tail = b - b16
+                assert (Wc + a16) % 16 == 0 and (b16 - a16) % 16 == 0 and b16 >= a16
+                assert Wc + b16 + tail <= total
+                assert b - a16 <= P["slot"]
+                covered.append((Wc + a, Wc + b))
+                for u in range(u0, u1):
+                    blk = cta_off + u * BB - a16
+                    assert 0 <= blk and blk + read_end <= P["slot"] and blk % 2 == 0
+                    if qtype == synth.Q4_K:
+                        assert blk % 16 == 0
+    covered.sort()
+    assert covered[0][0] == 0 and covered[-1][1] == total
+    for (x0, x1), (y0, y1) in zip(covered, covered[1:]):
+        assert x1 == y0
+
+
+@pytest.mark.parametrize("qtype,N,K", SHAPES)
+def test_gemv_sb_address_arithmetic(qtype, N, K):
+    if plan_sb(qtype, 1, K) is None:
+        pytest.skip("does not fit")
+    check_sb(qtype, N, K)
+
+
+def test_gemv_sb_fits_the_workloads():
+    for (_, q, K, N) in synth.LLAMA_1B + synth.QWEN3_14B_LAYER + synth.LM_HEAD:
+        assert plan_sb(q, 1, K) is not None, (q, K)
