@@ -111,6 +111,30 @@ QMM_API int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const floa
 QMM_API int qmm_quantize_act(const float *x, int64_t M, int64_t K, int8_t *q, float *d, int32_t *s,
                      void *stream);
 
+/*
+ * qmm_noalloc -- the same product as qmm(), for callers that cannot let the
+ * library allocate device memory: code captured into a CUDA graph (cudaMalloc
+ * is not allowed while a stream captures), serving loops that keep all device
+ * memory in their own fixed pool, and latency-critical paths that must not be
+ * serialised by cudaMalloc/cudaFree.  The pages have no counterpart of this
+ * call; it is part of this library's interface only.
+ *   Arguments, layouts and accuracy as for qmm().  Every M takes the prefill
+ *   path (activation quantiser + integer tensor-core GEMM), whose quantised
+ *   activations live in a 16 MiB scratch array compiled into the library:
+ *   it needs align256(M*K) + 2*align256(4*M*ceil4(K/32)) bytes, so about
+ *   M*K <= 13.4 million; larger calls return QMM_EINVAL_SHAPE and launch
+ *   nothing.
+ *   Nothing is allocated by the call.  The scratch is reserved on every GPU
+ *   that loads the library, until the process exits.  The first call on a
+ *   device looks the scratch's address up on that device (no allocation, but
+ *   make that first call before capturing a stream into a graph).
+ *   All calls share the one scratch array and overwrite it completely; calls
+ *   whose kernels overlap on the GPU (different streams, no ordering between
+ *   them) race on it and must be serialised by the caller.
+ */
+QMM_API int qmm_noalloc(int type, const void *W_blocks, int64_t N, int64_t K, const float *x,
+                        int64_t M, float *y, void *stream);
+
 /* Name of a status code. */
 QMM_API const char *qmm_strerror(int status);
 

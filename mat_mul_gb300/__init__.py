@@ -53,13 +53,15 @@ def load():
     P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     L.qmm_dequant.argtypes = [I, P, I64, P]
     L.qmm.argtypes = [I, P, I64, I64, P, I64, P, P]
+    L.qmm_noalloc.argtypes = [I, P, I64, I64, P, I64, P, P]
     L.qmm_quantize_act.argtypes = [P, I64, I64, P, P, P, P]
     L.qmm_strerror.argtypes = [I]
     L.qmm_strerror.restype = ctypes.c_char_p
     L.qmm_last_error.restype = ctypes.c_char_p
     L.qmm_device_status.argtypes = [P]
     L.qmm_launch_count.restype = I64
-    for f in ("qmm_dequant", "qmm", "qmm_quantize_act", "qmm_device_status", "qmm_release"):
+    for f in ("qmm_dequant", "qmm", "qmm_noalloc", "qmm_quantize_act", "qmm_device_status",
+              "qmm_release"):
         getattr(L, f).restype = I
     _lib = L
     return L
@@ -115,6 +117,21 @@ def qmm(qtype: int, W, N: int, K: int, x, y=None, stream=None):
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     _check(load().qmm(int(qtype), _ptr(W), int(N), int(K), _ptr(x), int(M), _ptr(y),
                       _stream_handle(stream)))
+    return y
+
+
+def qmm_noalloc(qtype: int, W, N: int, K: int, x, y, stream=None):
+    """Same product as qmm() without any device allocation by the library:
+    for callers that must not allocate (graph capture, fixed memory pools).
+    y must be given.  Uses a 16 MiB scratch inside the library image; calls
+    that overlap on the GPU race on it."""
+    import torch
+    _require_cuda(W, x, y)
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 tensor")
+    M = 1 if x.dim() == 1 else x.shape[0]
+    _check(load().qmm_noalloc(int(qtype), _ptr(W), int(N), int(K), _ptr(x), int(M), _ptr(y),
+                              _stream_handle(stream)))
     return y
 
 

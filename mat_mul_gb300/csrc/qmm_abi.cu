@@ -117,6 +117,11 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
 
+namespace qk {
+// Record the calling thread's last-error text for qmm_last_error(); returns code.
+int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
+}  // namespace qk
+
 extern "C" {
 
 const char *qmm_strerror(int status) {

@@ -51,4 +51,7 @@ cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const
                             const float *xd, const int32_t *xs, int xd_ld, int64_t M, float *y,
                             cudaStream_t st);
 
+// Set the calling thread's qmm_last_error() text; returns code.
+int record_error(int code, const char *msg);
+
 }  // namespace qk
