@@ -48,9 +48,10 @@ struct SbParams {
     int rows_r;      // N % gridDim.x: the first rows_r CTAs take one row more
     const float *x;  // [M][K] activations, fp32
     int x_vec;       // x is 16-byte aligned: load four at a time
-    int q_ld, d_ld, s16_ld;
+    int q_ld;        // bytes per activation row of q (a multiple of 256)
+    int meta_ld;     // bytes per activation row of scale records (Q8_0: of d)
     float *y;
-    int off_edge, off_xq, off_xd, off_xaux, off_ring;
+    int off_edge, off_xq, off_meta, off_ring;
     int *status;
 };
 
@@ -84,10 +85,21 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
+// Shared-memory activations.  q: int8, 16-byte chunks swizzled per super-
+// block.  Per super-block kb of row m, a record at meta + m*meta_ld +
+// kb*REC holds the eight block scales d (bytes 0..31) and, for Q4_K, the
+// eight products d*sum (32..63) or, for Q6_K, the sixteen half-block sums
+// (32..95); REC = 80 (Q4_K) or 112 (Q6_K) bytes, odd multiples of 16 so that
+// lanes reading consecutive super-blocks hit distinct banks.  Q8_0 keeps a
+// plain array of block scales.
+template <int T> struct Rec { static constexpr int B = 0; };
+template <> struct Rec<QMM_Q4_K> { static constexpr int B = 80; };
+template <> struct Rec<QMM_Q6_K> { static constexpr int B = 112; };
+
 struct XS {
     const uint8_t *sm;
-    int xq, xd, xaux;
-    int q_ld, d_ld, s16_ld;
+    int xq, meta;
+    int q_ld, meta_ld;
 };
 
 // Shared-memory byte offset of 16-byte chunk c of super-block kb, row m.
@@ -119,10 +131,8 @@ __device__ __forceinline__ void sb_q4k(const XS &X, int blk, int kb, float (&v)[
     for (int i = 0; i < 8; ++i) q[i] = ld16(sm, blk + 16 + 16 * i);
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        const float *dx = reinterpret_cast<const float *>(sm + X.xd + 4 * (m * X.d_ld + kb * 8));
-        const float *ds = reinterpret_cast<const float *>(sm + X.xaux + 4 * (m * X.d_ld + kb * 8));
-        const float4 dx0 = *reinterpret_cast<const float4 *>(dx), dx1 = *reinterpret_cast<const float4 *>(dx + 4);
-        const float4 ds0 = *reinterpret_cast<const float4 *>(ds), ds1 = *reinterpret_cast<const float4 *>(ds + 4);
+        const float4 *rec = reinterpret_cast<const float4 *>(sm + X.meta + m * X.meta_ld + kb * Rec<QMM_Q4_K>::B);
+        const float4 dx0 = rec[0], dx1 = rec[1], ds0 = rec[2], ds1 = rec[3];
         const float dxs[8] = {dx0.x, dx0.y, dx0.z, dx0.w, dx1.x, dx1.y, dx1.z, dx1.w};
         float acc_min = mf[0] * ds0.x;
         acc_min += mf[1] * ds0.y;
@@ -201,8 +211,9 @@ __device__ __forceinline__ void sb_q6k(const XS &X, int blk, int kb, float (&v)[
             for (int m = 0; m < MT; ++m) {
                 const uint4 xa = ld16(sm, xchunk(X, m, kb, 8 * h + 2 * g));
                 const uint4 xb = ld16(sm, xchunk(X, m, kb, 8 * h + 2 * g + 1));
-                const int2 s2 = *reinterpret_cast<const int2 *>(
-                    sm + X.xaux + 4 * (m * X.s16_ld + kb * 16 + 8 * h + 2 * g));
+                const int rec = X.meta + m * X.meta_ld + kb * Rec<QMM_Q6_K>::B;
+                const float dxg = *reinterpret_cast<const float *>(sm + rec + 4 * (4 * h + g));
+                const int2 s2 = *reinterpret_cast<const int2 *>(sm + rec + 32 + 8 * (4 * h + g));
                 int Ia = dp4a_ss(q[0], xa.x, -32 * s2.x);
                 Ia = dp4a_ss(q[1], xa.y, Ia);
                 Ia = dp4a_ss(q[2], xa.z, Ia);
@@ -211,8 +222,6 @@ __device__ __forceinline__ void sb_q6k(const XS &X, int blk, int kb, float (&v)[
                 Ib = dp4a_ss(q[5], xb.y, Ib);
                 Ib = dp4a_ss(q[6], xb.z, Ib);
                 Ib = dp4a_ss(q[7], xb.w, Ib);
-                const float dxg = *reinterpret_cast<const float *>(
-                    sm + X.xd + 4 * (m * X.d_ld + kb * 8 + 4 * h + g));
                 acc[m] += dxg * static_cast<float>(sa * Ia + sb * Ib);
             }
         }
@@ -241,7 +250,7 @@ __device__ __forceinline__ void sb_q80(const XS &X, int blk, int kb, float (&v)[
         I = dp4a_ss(qw[5], x1.y, I);
         I = dp4a_ss(qw[6], x1.z, I);
         I = dp4a_ss(qw[7], x1.w, I);
-        const float dx = *reinterpret_cast<const float *>(sm + X.xd + 4 * (m * X.d_ld + kb));
+        const float dx = *reinterpret_cast<const float *>(sm + X.meta + m * X.meta_ld + 4 * kb);
         v[m] += dx * (d * static_cast<float>(I));
     }
 }
@@ -250,56 +259,133 @@ __device__ __forceinline__ void sb_q80(const XS &X, int blk, int kb, float (&v)[
 // Same arithmetic as the standalone quantiser (and the oracle): per block of
 // 32, amax = max|x|, d = amax/127, inv = 1/d (0 if d == 0; the correctly
 // rounded reciprocal equals the IEEE quotient 1/d), q = round half away from
-// zero of x*inv clamped to +-127.  One thread per block: its 128 bytes of x
-// are loaded by eight independent 16-byte loads.  Writes the swizzled q, the
-// scale d, and d*sum (Q4_K) or the two half-block sums (Q6_K).
-template <int T>
-__device__ __forceinline__ void quantize_to_smem(const SbParams &P, uint8_t *smem) {
+// zero of x*inv clamped to +-127.  TPB consecutive threads share a block
+// (32/TPB values each, loaded 16 bytes at a time), combining the maximum and
+// the sums with shuffles; TPB is chosen so one pass covers all blocks when
+// they are few.
+// Quantise one value: round half away from zero of v = x*inv.  For finite x,
+// |x*inv| <= amax*(1/d) <= 127*(1 + 2^-22) < 127.5, so the +-127 clamp of the
+// definition can never change the result and is not applied here.
+__device__ __forceinline__ int quant1(float x, float inv) { return static_cast<int>(roundf(__fmul_rn(x, inv))); }
+
+// Pack four int8 values (given as ints) into one little-endian word.
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+    const uint32_t lo = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040);
+    const uint32_t hi = __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040);
+    return __byte_perm(lo, hi, 0x5410);
+}
+
+// max |a[i]| over N values as a balanced tree
+template <int N>
+__device__ __forceinline__ float absmax(const float (&a)[N]) {
+    float t[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) t[i] = fabsf(a[i]);
+#pragma unroll
+    for (int w = N / 2; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+    return t[0];
+}
+
+template <int T, int TPB, int R, class F>
+__device__ __forceinline__ void quantize_tpb(const SbParams &P, uint8_t *smem, F &&after_loads) {
+    constexpr int EPT = 32 / TPB;
     const int nb32 = P.K / 32;
-    const int total = P.M * nb32;
-    for (int id = threadIdx.x; id < total; id += NTHREADS) {
-        const int m = id / nb32, b = id - m * nb32;
-        const float *src = P.x + static_cast<int64_t>(m) * P.K + 32 * b;
-        float a[32];
-        if (P.x_vec) {
+    const int items = P.M * nb32 * TPB;
+    for (int base = 0; base < items; base += R * NTHREADS) {
+        // every load of this pass first: R items of EPT values per thread
+        float a[R][EPT];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + i);
-                a[4 * i] = v.x; a[4 * i + 1] = v.y; a[4 * i + 2] = v.z; a[4 * i + 3] = v.w;
+        for (int r = 0; r < R; ++r) {
+            const int it = base + r * NTHREADS + static_cast<int>(threadIdx.x);
+            const bool ok = it < items;
+            const int id = ok ? it / TPB : 0;
+            const int m = id / nb32, b = id - m * nb32;
+            const float *src = P.x + static_cast<int64_t>(m) * P.K + 32 * b + EPT * (it & (TPB - 1));
+            if (P.x_vec) {
+#pragma unroll
+                for (int i = 0; i < EPT / 4; ++i) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (ok) v = __ldg(reinterpret_cast<const float4 *>(src) + i);
+                    a[r][4 * i] = v.x; a[r][4 * i + 1] = v.y; a[r][4 * i + 2] = v.z; a[r][4 * i + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < EPT; ++i) a[r][i] = ok ? __ldg(src + i) : 0.0f;
             }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = __ldg(src + i);
         }
-        float am = 0.0f;
+        if (base == 0) after_loads();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(a[i]));
-        const float db = __fdiv_rn(am, 127.0f);
-        const float inv = (db != 0.0f) ? __frcp_rn(db) : 0.0f;
-        uint32_t w[8];
-        int s_lo = 0, s_hi = 0;
+        for (int r = 0; r < R; ++r) {
+            const int it = base + r * NTHREADS + static_cast<int>(threadIdx.x);
+            const bool ok = it < items;
+            const int id = ok ? it / TPB : 0;
+            const int part = it & (TPB - 1);
+            const int m = id / nb32, b = id - m * nb32;
+            float am = absmax<EPT>(a[r]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t word = 0;
+            for (int o = 1; o < TPB; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+            const float db = __fdiv_rn(am, 127.0f);
+            const float inv = (db != 0.0f) ? __frcp_rn(db) : 0.0f;
+            uint32_t w[EPT / 4];
+            int s0 = 0, s1 = 0;  // this thread's values in the first / second half block
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int q = static_cast<int>(fminf(fmaxf(roundf(__fmul_rn(a[4 * i + e], inv)), -127.0f), 127.0f));
-                if (i < 4) s_lo += q; else s_hi += q;
-                word |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * e);
+            for (int i = 0; i < EPT / 4; ++i) {
+                int q[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) q[e] = quant1(a[r][4 * i + e], inv);
+                const int s4 = q[0] + q[1] + q[2] + q[3];
+                if (EPT * part + 4 * i < 16) s0 += s4; else s1 += s4;
+                w[i] = pack4(q[0], q[1], q[2], q[3]);
             }
-            w[i] = word;
+#pragma unroll
+            for (int o = 1; o < TPB; o <<= 1) {
+                s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            }
+            if (!ok) continue;
+            // this thread's bytes: elements [EPT*part, EPT*part + EPT) of the block,
+            // inside chunks 2*(b & 7) and 2*(b & 7) + 1 of super-block b >> 3
+            const int sb = b >> 3;
+            uint8_t *row = smem + P.off_xq + m * P.q_ld + sb * 256;
+            if constexpr (EPT == 32) {
+                const int c0 = (2 * (b & 7)) ^ (sb & 7), c1 = (2 * (b & 7) + 1) ^ (sb & 7);
+                *reinterpret_cast<uint4 *>(row + 16 * c0) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(row + 16 * c1) = make_uint4(w[4], w[5], w[6], w[7]);
+            } else if constexpr (EPT == 16) {
+                const int c = (2 * (b & 7) + part) ^ (sb & 7);
+                *reinterpret_cast<uint4 *>(row + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+                const int c = (2 * (b & 7) + (part >> 1)) ^ (sb & 7);
+                *reinterpret_cast<uint2 *>(row + 16 * c + 8 * (part & 1)) = make_uint2(w[0], w[1]);
+            }
+            if (part == 0) {
+                if (T == QMM_Q8_0) {
+                    reinterpret_cast<float *>(smem + P.off_meta + m * P.meta_ld)[b] = db;
+                } else {
+                    uint8_t *rec = smem + P.off_meta + m * P.meta_ld + sb * Rec<T>::B;
+                    reinterpret_cast<float *>(rec)[b & 7] = db;
+                    if (T == QMM_Q4_K) reinterpret_cast<float *>(rec + 32)[b & 7] = db * static_cast<float>(s0 + s1);
+                    if (T == QMM_Q6_K) reinterpret_cast<int2 *>(rec + 32)[b & 7] = make_int2(s0, s1);
+                }
+            }
         }
-        // the two 16-byte chunks of this block, swizzled within its super-block
-        const int sb = b >> 3, c0 = (2 * (b & 7)) ^ (sb & 7), c1 = (2 * (b & 7) + 1) ^ (sb & 7);
-        uint8_t *row = smem + P.off_xq + m * P.q_ld + sb * 256;
-        *reinterpret_cast<uint4 *>(row + 16 * c0) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4 *>(row + 16 * c1) = make_uint4(w[4], w[5], w[6], w[7]);
-        reinterpret_cast<float *>(smem + P.off_xd)[m * P.d_ld + b] = db;
-        if (T == QMM_Q4_K)
-            reinterpret_cast<float *>(smem + P.off_xaux)[m * P.d_ld + b] = db * static_cast<float>(s_lo + s_hi);
-        if (T == QMM_Q6_K)
-            *reinterpret_cast<int2 *>(smem + P.off_xaux + 4 * (m * P.s16_ld + 2 * b)) = make_int2(s_lo, s_hi);
     }
+}
+
+// after_loads() runs once, after the first pass's activation loads are issued
+// and before their values are used.  The split (threads per block TPB, items
+// per thread R) keeps one pass and the fewest values per thread.
+template <int T, class F>
+__device__ __forceinline__ void quantize_to_smem(const SbParams &P, uint8_t *smem, F &&after_loads) {
+    const int total = P.M * (P.K / 32);
+    if (4 * total <= NTHREADS) quantize_tpb<T, 4, 1>(P, smem, after_loads);
+    else if (2 * total <= NTHREADS) quantize_tpb<T, 2, 1>(P, smem, after_loads);
+    else if (total <= NTHREADS) quantize_tpb<T, 1, 1>(P, smem, after_loads);
+    else if (2 * total <= 2 * NTHREADS) quantize_tpb<T, 2, 2>(P, smem, after_loads);
+    else if (2 * total <= 3 * NTHREADS) quantize_tpb<T, 2, 3>(P, smem, after_loads);
+    else quantize_tpb<T, 2, 4>(P, smem, after_loads);
 }
 
 template <int T, int MT>
@@ -355,28 +441,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_kernel(const __grid_const
         if (nbytes) bulk_g2s(smem_u32(smem + dst), Wc + a16, nbytes, my_bar + 8u * slot, pol);
     };
 
-    uint64_t pol_w = 0;
-    int issued = 0;
-    if (lane == 0) {
-        pol_w = policy_evict_first();
-        for (; issued < min(P.NSW, nst); ++issued) issue(issued, pol_w);
-    }
-    // The weights are read-only here, so streaming them may begin before the
-    // preceding kernel on the stream has finished; the activations and y may
-    // not be touched before it has.  Let the next kernel start launching too.
+    // Wait for the preceding kernel (it may produce x), issue this thread's
+    // activation loads, and only then start the weight stream, so the loads
+    // do not return behind tens of KB of bulk copies into this SM.  The next
+    // kernel on the stream may start launching now.
     pdl_trigger();
     pdl_wait();
-    quantize_to_smem<T>(P, smem);
+    uint64_t pol_w = 0;
+    int issued = 0;
+    quantize_to_smem<T>(P, smem, [&] {
+        if (lane == 0) {
+            pol_w = policy_evict_first();
+            for (; issued < min(P.NSW, nst); ++issued) issue(issued, pol_w);
+        }
+    });
     __syncthreads();
 
     XS X;
     X.sm = smem;
     X.xq = P.off_xq;
-    X.xd = P.off_xd;
-    X.xaux = P.off_xaux;
+    X.meta = P.off_meta;
     X.q_ld = P.q_ld;
-    X.d_ld = P.d_ld;
-    X.s16_ld = P.s16_ld;
+    X.meta_ld = P.meta_ld;
 
     bool failed = false;
     int carry_row = -1;
@@ -463,13 +549,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_kernel(const __grid_const
         const int e = lane;
         const int r = e < 2 * NWARP ? edge_row[e] : -1;
         const unsigned same = __match_any_sync(0xffffffffu, r);
-        float acc[MT];
+        float mine[MT], acc[MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+        for (int m = 0; m < MT; ++m) {
+            mine[m] = r >= 0 ? edge_val[e * 8 + m] : 0.0f;
+            acc[m] = 0.0f;
+        }
+#pragma unroll 4
         for (int j = 0; j < 2 * NWARP; ++j) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                const float vj = __shfl_sync(0xffffffffu, r >= 0 ? edge_val[(e < 2 * NWARP ? e : 0) * 8 + m] : 0.0f, j);
+                const float vj = __shfl_sync(0xffffffffu, mine[m], j);
                 if ((same >> j) & 1u) acc[m] += vj;
             }
         }
@@ -490,16 +580,13 @@ bool plan_sb(int type, int M, int64_t K, int max_smem, SbParams &P, int &smem) {
     const int MT = mt_of(M);
     const int BB = block_bytes(type);
     const int64_t q_ld = align64(K, 256);
-    const int64_t d_ld = align64(K / 32, 4);
-    const int64_t s16_ld = align64(K / 16, 4);
+    const int64_t meta_ld = type == QMM_Q8_0 ? align64((K / 32) * 4, 16)
+                                             : (K / 256) * (type == QMM_Q4_K ? 80 : 112);
     int64_t off = HEAD_BYTES;
     const int64_t o_xq = off;
     off = align64(off + MT * q_ld, 128);
-    const int64_t o_xd = off;
-    off = align64(off + MT * d_ld * 4, 128);
-    const int64_t o_xaux = off;
-    if (type == QMM_Q4_K) off = align64(off + MT * d_ld * 4, 128);
-    if (type == QMM_Q6_K) off = align64(off + MT * s16_ld * 4, 128);
+    const int64_t o_meta = off;
+    off = align64(off + MT * meta_ld, 128);
     const int64_t o_ring = off;
     const int64_t slot = align64(static_cast<int64_t>(SU) * BB + 32, 128);
     int64_t nsw = (max_smem - o_ring) / (NWARP * slot);
@@ -509,11 +596,9 @@ bool plan_sb(int type, int M, int64_t K, int max_smem, SbParams &P, int &smem) {
     P.slot_bytes = static_cast<int>(slot);
     P.off_edge = 8 * NWARP * MAX_NSW;
     P.q_ld = static_cast<int>(q_ld);
-    P.d_ld = static_cast<int>(d_ld);
-    P.s16_ld = static_cast<int>(s16_ld);
+    P.meta_ld = static_cast<int>(meta_ld);
     P.off_xq = static_cast<int>(o_xq);
-    P.off_xd = static_cast<int>(o_xd);
-    P.off_xaux = static_cast<int>(o_xaux);
+    P.off_meta = static_cast<int>(o_meta);
     P.off_ring = static_cast<int>(o_ring);
     smem = static_cast<int>(o_ring + NWARP * nsw * slot);
     return true;

@@ -112,6 +112,13 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// Warm L2 with [src, src + bytes) (16-byte aligned address and size).  L2 is
+// the point of coherence, so this is safe even while another grid may still
+// write the range.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding grid's results /
 // allow the next grid to start launching.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -133,19 +133,16 @@ SB_NWARP, SB_SU, SB_HEAD, SB_MAXNSW = 12, 32, 2048, 6
 def plan_sb(qtype, M, K):
     MT = 1 if M <= 1 else 2 if M <= 2 else 4 if M <= 4 else 8
     BB = synth.BLOCK_BYTES[qtype]
-    q_ld, d_ld, s16_ld = align(K, 256), align(K // 32, 4), align(K // 16, 4)
+    q_ld = align(K, 256)
+    meta_ld = align((K // 32) * 4, 16) if qtype == synth.Q8_0 else (K // 256) * (80 if qtype == synth.Q4_K else 112)
     off = SB_HEAD
     off = align(off + MT * q_ld, 128)
-    off = align(off + MT * d_ld * 4, 128)
-    if qtype == synth.Q4_K:
-        off = align(off + MT * d_ld * 4, 128)
-    if qtype == synth.Q6_K:
-        off = align(off + MT * s16_ld * 4, 128)
+    off = align(off + MT * meta_ld, 128)
     slot = align(SB_SU * BB + 32, 128)
     nsw = min(SB_MAXNSW, (SMEM_MAX - off) // (SB_NWARP * slot))
     if nsw < 2:
         return None
-    return dict(NSW=nsw, slot=slot, ring=off, q_ld=q_ld, d_ld=d_ld, s16_ld=s16_ld)
+    return dict(NSW=nsw, slot=slot, ring=off, q_ld=q_ld, meta_ld=meta_ld)
 
 
 def check_sb(qtype, N, K, M=1):
@@ -156,8 +153,7 @@ def check_sb(qtype, N, K, M=1):
     P = plan_sb(qtype, M, K)
     assert P is not None
     assert SB_NWARP * SB_MAXNSW * 8 + 2 * SB_NWARP * 4 + 2 * SB_NWARP * 8 * 4 <= SB_HEAD
-    for nbytes in (M * P["q_ld"], M * P["d_ld"] * 4, M * P["s16_ld"] * 4):
-        assert nbytes % 16 == 0
+    assert P["q_ld"] % 256 == 0 and P["meta_ld"] % 16 == 0
     grid = min(SMS, N)
     covered = []
     read_end = {synth.Q8_0: 38, synth.Q4_K: 144, synth.Q6_K: 212}[qtype]

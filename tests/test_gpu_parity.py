@@ -204,3 +204,54 @@ def test_qmm_prefill_workload_full_size(cuda_lib):
         rb = synth.row_bytes(qtype, K)
         yo, A = O.qmm(qtype, W.reshape(N, rb)[rows], len(rows), K, x)
         _assert_within_bound(y[:, rows], yo, A, f"prefill {name}")
+
+
+# ------------------------------------------- exact integer special cases
+
+def _int_activations(rng, M, K):
+    """Integer activations with max |x| = 127 in every block of 32, so the
+    quantiser maps them to themselves with scale 1."""
+    xi = rng.integers(-127, 128, (M, K)).astype(np.float64)
+    xi[:, 3::32] = 127.0
+    return xi
+
+
+@pytest.mark.parametrize("N,K,M", [(257, 1024, 1), (129, 2048, 2), (64, 512, 5), (33, 4096, 8),
+                                   (70, 1024, 24)])
+def test_qmm_q8_0_unit_scale_is_exact(cuda_lib, N, K, M):
+    """d = 1 Q8_0 weights and integer activations: every path must return the
+    exact integer product (all partial sums stay below 2^24)."""
+    rng = np.random.default_rng(N + K + M)
+    qw = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    W = np.concatenate([O.pack_q8_0(0x3C00, qw[n, 32 * b:32 * b + 32])
+                        for n in range(N) for b in range(K // 32)])
+    xi = _int_activations(rng, M, K)
+    y = _run_qmm(cuda_lib, synth.Q8_0, W, N, K, xi.astype(np.float32))
+    assert np.array_equal(y.astype(np.float64), xi @ qw.astype(np.float64).T)
+
+
+@pytest.mark.parametrize("N,K,M", [(300, 2048, 1), (129, 5120, 1), (64, 1024, 3), (40, 2048, 8),
+                                   (70, 768, 16)])
+def test_qmm_q4_k_unit_scale_is_exact(cuda_lib, N, K, M):
+    """Q4_K with d = 1, dmin = 0, every scale 1: w = q, so y is an exact
+    integer product; checks the unpacking and every index exactly."""
+    rng = np.random.default_rng(3 * N + K + M)
+    q = rng.integers(0, 16, (N, K // 256, 256)).astype(np.uint8)
+    W = np.concatenate([O.pack_q4_k(0x3C00, 0x0000, np.ones(8, np.uint8), np.zeros(8, np.uint8), q[n, b])
+                        for n in range(N) for b in range(K // 256)])
+    xi = _int_activations(rng, M, K)
+    y = _run_qmm(cuda_lib, synth.Q4_K, W, N, K, xi.astype(np.float32))
+    assert np.array_equal(y.astype(np.float64), xi @ q.reshape(N, K).astype(np.float64).T)
+
+
+@pytest.mark.parametrize("N,K,M", [(300, 2048, 1), (65, 5120, 1), (40, 1280, 4), (70, 1024, 16)])
+def test_qmm_q6_k_unit_scale_is_exact(cuda_lib, N, K, M):
+    """Q6_K with d = 1 and every scale 1: w = q - 32, exact integer product."""
+    rng = np.random.default_rng(5 * N + K + M)
+    q = rng.integers(0, 64, (N, K // 256, 256)).astype(np.uint8)
+    W = np.concatenate([O.pack_q6_k(0x3C00, np.ones(16, np.int8), q[n, b])
+                        for n in range(N) for b in range(K // 256)])
+    xi = _int_activations(rng, M, K)
+    y = _run_qmm(cuda_lib, synth.Q6_K, W, N, K, xi.astype(np.float32))
+    assert np.array_equal(y.astype(np.float64),
+                          xi @ (q.reshape(N, K).astype(np.float64) - 32).T)
