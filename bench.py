@@ -364,10 +364,10 @@ def run_ours(args):
                            "N": m["N"], "MB": round(m["bytes"] / 1e6, 3), "us": round(t_ms * 1e3, 2),
                            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4)})
             if m["name"] == "cfg2:lm_head":
-                traffic = load_traffic("gemv.cu")
+                traffic = load_traffic("gemv_sb.cu")
                 roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
                         "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
-                        "traffic": traffic, "kernel": "gemv_kernel<Q6_K,1> (qmm, lm_head 2048x128256)",
+                        "traffic": traffic, "kernel": "gemv_sb_kernel<Q6_K,1> (qmm, lm_head 2048x128256)",
                         "bytes_per_launch": m["bytes"], "us_per_launch": round(t_ms * 1e3, 2),
                         "peak_source": peaks["source"] + " hbm_gbs (copy, burst)"}
             del g, copies
@@ -451,6 +451,28 @@ class _Null:
         return False
 
 
+def run_ncu_case(name, calls=3):
+    """A few eager qmm calls of one workload matrix (for ncu captures: graphs
+    with programmatic dependent launch cannot be replayed node by node)."""
+    import torch
+
+    import mat_mul_gb300 as q
+    torch.cuda.set_device(0)
+    q.load()
+    mats = {m["name"]: m for m in decode_workload()}
+    for idx, (nm, qtype, K, N) in enumerate(synth.CONFIGS[4]["mats"]):
+        mats[f"cfg4:{nm}"] = dict(cfg=4, idx=idx, name=f"cfg4:{nm}", qtype=qtype, K=K, N=N, M=512)
+    m = mats[name]
+    W = torch.from_numpy(synth.config_weights(m["cfg"], m["idx"])).cuda()
+    x = torch.from_numpy(synth.config_activations(m["cfg"], m.get("M", 1), m["K"])).cuda()
+    for _ in range(calls):
+        y = q.qmm(m["qtype"], W, m["N"], m["K"], x)
+    torch.cuda.synchronize()
+    assert q.qmm_device_status() == 0
+    print(name, "ok", float(y.abs().sum()))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -459,7 +481,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--quick", action="store_true", help="headline and e2e only")
+    ap.add_argument("--ncu-case", default=None,
+                    help="run three eager calls of one matrix (e.g. cfg2:lm_head) and exit")
     args = ap.parse_args()
+    if args.ncu_case:
+        return run_ncu_case(args.ncu_case)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -20,6 +20,11 @@
 namespace {
 
 thread_local char g_err[512] = "";
+// QMM_PREFILL_KERNEL=mma keeps Q4_K prefill on the mma.sync kernel.
+const bool g_force_mma_gemm = [] {
+    const char *v = getenv("QMM_PREFILL_KERNEL");
+    return v && strcmp(v, "mma") == 0;
+}();
 // QMM_DECODE_KERNEL=rounds selects the round-based decode kernel wherever the
 // block-per-lane one would run (for comparisons; read once at load).
 const bool g_force_round_gemv = [] {
@@ -228,6 +233,25 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
         e = qk::launch_gemv_sb(type, W_blocks, N, K, x, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
                                di.status);
         if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+        g_launches.fetch_add(1);
+        return QMM_OK;
+    }
+    // Prefill of Q4_K on the tcgen05 kernel: fp16 activations d*q [M][K].
+    if (M > 8 && !g_force_mma_gemm && qk::gemm_tc_supported(type, N, K, M)) {
+        const size_t xh_bytes = align_up(static_cast<size_t>(M * K) * 2, 256);
+        const size_t d_bytes = align_up(static_cast<size_t>(M * (K / 32)) * 4, 256);
+        void *ws = nullptr;
+        if (int rc = workspace(dev, st, xh_bytes + d_bytes, &ws)) return rc;
+        qk::QuantOut o = {};
+        o.xh = ws;
+        o.xh_ld = K;
+        o.d = reinterpret_cast<float *>(static_cast<char *>(ws) + xh_bytes);
+        o.d_ld = K / 32;
+        e = qk::launch_quantize(x, M, K, o, st, false, di.num_sms);
+        if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+        g_launches.fetch_add(1);
+        e = qk::launch_gemm_tc(type, W_blocks, N, K, ws, M, y, st, di.num_sms, di.status);
+        if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
         g_launches.fetch_add(1);
         return QMM_OK;
     }

@@ -16,6 +16,7 @@ namespace qk {
 //   s32 [M][d_ld]   int32 sum per block
 //   s16 [M][s16_ld] int32 sums of the two 16-element halves of every block
 //   dsf [M][d_ld]   fp32 product d * s32 per block
+//   xh  [M][xh_ld]  fp16 of the dequantised activation d * q (plain layout)
 struct QuantOut {
     int8_t *q;
     int64_t q_ld;
@@ -25,6 +26,8 @@ struct QuantOut {
     int32_t *s16;
     float *dsf;
     int64_t d_ld, s16_ld;
+    void *xh;  // __half
+    int64_t xh_ld;
 };
 
 cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, const QuantOut &o, cudaStream_t st,
@@ -45,6 +48,13 @@ cudaError_t launch_gemv(int type, const void *W, int64_t N, int64_t K, const int
 bool gemv_sb_fits(int type, int M, int64_t K, int max_smem);
 cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const float *x, int M,
                            float *y, cudaStream_t st, int num_sms, int max_smem, int *status);
+
+// Prefill GEMM on tcgen05 (gemm_tc.cu): Q4_K weights, fp16 activations
+// xh [M][K] (d*q from the quantiser).  Returns cudaErrorNotSupported for
+// shapes it does not take.
+bool gemm_tc_supported(int type, int64_t N, int64_t K, int64_t M);
+cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const void *xh, int64_t M,
+                           float *y, cudaStream_t st, int num_sms, int *status);
 
 // Prefill GEMM on mma.sync (gemm_mma.cu): q [M][K], d and s32 [M][xd_ld].
 cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,

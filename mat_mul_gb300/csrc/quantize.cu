@@ -41,7 +41,9 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
             const int c = static_cast<int>((k >> 4) & 15) ^ static_cast<int>(sb & 7);
             pos = (sb << 8) + 16 * c + (k & 15);
         }
-        o.q[m * o.q_ld + pos] = static_cast<int8_t>(qi);
+        if (o.q) o.q[m * o.q_ld + pos] = static_cast<int8_t>(qi);
+        if (o.xh)
+            static_cast<__half *>(o.xh)[m * o.xh_ld + k] = __float2half_rn(__fmul_rn(db, static_cast<float>(qi)));
         int lo = 0;
         if (o.s16)
             lo = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(lane < 16 ? qi : 0)));
