@@ -5,26 +5,33 @@
 // sm_103a has no integer tcgen05 mode, so the contraction runs in kind::f16
 // with the roles chosen so that the dequantised weights never pass through
 // shared memory:
-//   A (128 x 64 per K step) = weights d*sc*q - dmin*m rounded to fp16, written
-//       straight into TMEM by eight dequantiser warps (tcgen05.st) from the
-//       raw super-block bytes that TMA brings into shared memory;
-//   B (BT x 64) = the dequantised activations d_x*q_x rounded to fp16 (from the
+//   A (128 x 128 per K step) = weights d*sc*q - dmin*m rounded to fp16,
+//       written straight into TMEM by four dequantiser warps (tcgen05.st)
+//       from the raw super-block bytes that TMA brings into shared memory;
+//   B (BT x 128) = the dequantised activations d_x*q_x rounded to fp16 (from the
 //       quantiser), loaded by TMA with the 128-byte swizzle; BT = 64/128/256
 //       tokens, so the weight tile is reused across up to 256 tokens;
 //   D (128 x BT) = fp32 in TMEM: row = weight row n, column = token m.
 // Each product term carries two fp16 roundings (relative 2^-11 each) and
 // the sum is accumulated in fp32, well inside |dy| <= 2e-3*sum|w*x| + 1e-5.
 //
-// Warp roles: 0 = TMA producer (per 64-wide K step: the token tile, the
-// 16-byte super-block header and the 32 quant bytes of each of the 128 weight
-// rows), 1 = MMA issuer (and TMEM owner), then G groups of four dequantiser
-// warps (warp w serves TMEM lanes 32*(w%4)..; group g takes the K steps
-// g, g+G, ..., so G steps are dequantised at once) that finish as the
-// epilogue (TMEM -> y).
+// CTAs run in pairs (a cluster of two along the weight tiles) that share
+// the token tile: each loads one of the step's two token boxes and
+// multicasts it to both, halving the L2 reads of the activations; each MMA
+// commit frees the stage in both CTAs.
+//
+// Warp roles (7 warps), per 128-wide K step (half a super-block):
+//   0 = token producer: one token box for the pair (ring released by the
+//       MMA commits of both CTAs);
+//   6 = raw weight producer: the 16-byte super-block header and the 64
+//       quant bytes of each of the 128 weight rows (ring released by the
+//       dequantisers, so dequantisation runs ahead of the MMA);
+//   1 = MMA issuer (and TMEM owner);
+//   2..5 = dequantiser (warp w serves TMEM lanes 32*(w%4)..), then epilogue
+//       (TMEM -> y).
 // All waits are bounded; on a timeout the CTA stops issuing, drains what it
 // issued, frees TMEM and returns with the status word set.
 #include <cuda.h>
-#include <stdlib.h>
 
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
@@ -33,34 +40,40 @@ namespace qk {
 
 namespace {
 
-constexpr int BW = 128, BK = 64;  // weight rows per tile, K per step
-constexpr int A_STAGES = 4;       // dequantised weight stages in TMEM (32 columns each)
-constexpr int W_LOAD = 0, W_MMA = 1, W_DQ0 = 2;
+constexpr int BW = 128, BK = 128;  // weight rows per tile, K per step (half a super-block)
+constexpr int A_STAGES = 4;        // dequantised weight stages in TMEM (64 columns each)
+constexpr int A_COLS = BK / 2;     // two fp16 weights per 32-bit TMEM column
+constexpr int W_XLOAD = 0, W_MMA = 1, W_RLOAD = 6;  // warps 2..5: dequantisers
+constexpr int NTHREADS = 7 * 32;
 constexpr int RAW_ROW = 144;        // one Q4_K super-block per weight row
 constexpr int H_BYTES = BW * 16;    // d, dmin and the 12 scale bytes of each row
-constexpr int Q_BYTES = BW * 32;    // this K step's 32 quant bytes of each row
+constexpr int Q_BYTES = BW * 64;    // this K step's 64 quant bytes of each row (64-byte swizzle)
+constexpr int R_BYTES = H_BYTES + Q_BYTES;
 
-template <int BT, int G>
+template <int BT>
 struct TcCfg {
-    static constexpr int NDQ = 4 * G;  // dequantiser warps: G groups of four lane quarters
-    static constexpr int NTHREADS = (W_DQ0 + NDQ) * 32;
-    static constexpr int X_BYTES = BT * BK * 2;
-    static constexpr int L_BYTES = X_BYTES + H_BYTES + Q_BYTES;  // a multiple of 1024
-    static constexpr int L_STAGES = BT == 256 ? 5 : 6;
-    static constexpr int OFF_BAR = L_STAGES * L_BYTES;
-    static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // barriers + base alignment slack
+    static constexpr int XBOX = BT * 128;   // one 64-wide K box of tokens (128-byte swizzle rows)
+    static constexpr int X_BYTES = 2 * XBOX;
+    static constexpr int X_STAGES = BT == 256 ? 3 : BT == 128 ? 5 : 8;
+    static constexpr int OFF_R = X_STAGES * X_BYTES;
+    static constexpr int R_STAGES_FIT = (232448 - 1536 - OFF_R) / R_BYTES;
+    static constexpr int R_STAGES = R_STAGES_FIT > 8 ? 8 : R_STAGES_FIT;
+    static constexpr int OFF_BAR = OFF_R + R_STAGES * R_BYTES;
+    static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // barriers + base alignment slack
     static constexpr int A_COL0 = BT;                         // TMEM columns of the A stages
-    static constexpr int TMEM_COLS = BT + 32 * A_STAGES <= 256 ? 256 : 512;
+    static constexpr int TMEM_COLS = BT + A_COLS * A_STAGES <= 256 ? 256 : 512;
     // D fp32, A and B fp16, both K-major, M = 128 weight rows, N = BT tokens
     static constexpr uint32_t IDESC = (1u << 4) | ((BT >> 3) << 17) | ((BW >> 4) << 24);
-    static_assert(L_BYTES % 1024 == 0, "stage alignment");
-    static_assert((BT / 16) % G == 0, "epilogue split");
+    static_assert(X_BYTES % 1024 == 0 && R_BYTES % 1024 == 0, "stage alignment");
+    static_assert(R_STAGES >= 3, "raw ring depth");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(16 * (X_STAGES + R_STAGES + A_STAGES) + 8 <= 480, "barrier area");
+    static_assert(BT + A_COLS * A_STAGES <= TMEM_COLS, "tensor memory");
 };
 
 struct TcParams {
     int M, N;
-    int nsteps;   // 64-wide K steps per split; split z starts at z*nsteps
+    int nsteps;   // 128-wide K steps per split; split z starts at z*nsteps
     float *y;
     int atomic;   // split K: add into y instead of storing
     int *status;
@@ -95,6 +108,38 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
+}
+
+// Token box multicast to both CTAs of the pair: it lands at the same offset
+// in each CTA's shared memory and completes bytes on each CTA's barrier at
+// the offset of `bar`.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+// Arrive on the barrier at offset `bar` in both CTAs of the pair once every
+// MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -152,11 +197,11 @@ __device__ __forceinline__ void dequant4(uint32_t w, bool hi, __half2 a, __half2
     out1 = *reinterpret_cast<const uint32_t *>(&w1);
 }
 
-template <int BT, int G>
-__global__ void __launch_bounds__(TcCfg<BT, G>::NTHREADS, 1)
+template <int BT>
+__global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
                    const __grid_constant__ CUtensorMap tmQ, const TcParams P) {
-    using C = TcCfg<BT, G>;
+    using C = TcCfg<BT>;
     extern __shared__ uint8_t smem_raw[];
     // stages need 1024-byte alignment for the 128-byte swizzle
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -164,18 +209,23 @@ __global__ void __launch_bounds__(TcCfg<BT, G>::NTHREADS, 1)
     const int n0 = blockIdx.x * BW, m0 = blockIdx.y * BT;
     const int k_step0 = blockIdx.z * P.nsteps;
 
-    const uint32_t sL = smem_u32(smem);
+    const uint32_t sX = smem_u32(smem), sR = smem_u32(smem + C::OFF_R);
     const uint32_t bar = smem_u32(smem + C::OFF_BAR);
-    const uint32_t bar_l_full = bar, bar_l_empty = bar + 8 * C::L_STAGES;
-    const uint32_t bar_a_full = bar + 16 * C::L_STAGES, bar_a_empty = bar_a_full + 8 * A_STAGES;
+    const uint32_t bar_x_full = bar, bar_x_empty = bar_x_full + 8 * C::X_STAGES;
+    const uint32_t bar_r_full = bar_x_empty + 8 * C::X_STAGES, bar_r_empty = bar_r_full + 8 * C::R_STAGES;
+    const uint32_t bar_a_full = bar_r_empty + 8 * C::R_STAGES, bar_a_empty = bar_a_full + 8 * A_STAGES;
     const uint32_t bar_acc = bar_a_empty + 8 * A_STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_BAR + 224);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + 232);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_BAR + 480);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + 488);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::L_STAGES; ++s) {
-            mbar_init(bar_l_full + 8 * s, 1);
-            mbar_init(bar_l_empty + 8 * s, 1 + 4);  // the MMA commit + the four warps of the K step's group
+        for (int s = 0; s < C::X_STAGES; ++s) {
+            mbar_init(bar_x_full + 8 * s, 1);
+            mbar_init(bar_x_empty + 8 * s, 2);  // both CTAs' MMA commits (each reads both boxes)
+        }
+        for (int s = 0; s < C::R_STAGES; ++s) {
+            mbar_init(bar_r_full + 8 * s, 1);
+            mbar_init(bar_r_empty + 8 * s, 4);  // the four dequantiser warps
         }
         for (int s = 0; s < A_STAGES; ++s) {
             mbar_init(bar_a_full + 8 * s, 4);
@@ -192,52 +242,78 @@ __global__ void __launch_bounds__(TcCfg<BT, G>::NTHREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // the peer's multicast copies and commits target this CTA's barriers:
+    // both CTAs initialise theirs before either issues anything
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int rank = static_cast<int>(cluster_rank());
 
-    if (warp == W_LOAD) {
-        // ------------------------------------------------------- producer
+    if (warp == W_XLOAD) {
+        // ------------------------------------------ token tile producer
         if (lane == 0) {
             int issued = 0;
             for (int kk = 0; kk < P.nsteps; ++kk) {
-                const int s = kk % C::L_STAGES;
-                if (kk >= C::L_STAGES &&
-                    (*abort_flag || !mbar_wait(bar_l_empty + 8 * s, ((kk / C::L_STAGES) - 1) & 1, P.status))) {
+                const int s = kk % C::X_STAGES;
+                if (kk >= C::X_STAGES &&
+                    (*abort_flag || !mbar_wait(bar_x_empty + 8 * s, ((kk / C::X_STAGES) - 1) & 1, P.status))) {
                     *abort_flag = 1;
                     break;
                 }
-                const int gk = k_step0 + kk;  // global 64-wide K step
-                const uint32_t st = sL + s * C::L_BYTES;
-                mbar_arrive_expect_tx(bar_l_full + 8 * s, C::L_BYTES);
-                tma_load_2d(st, &tmX, gk * BK, m0, bar_l_full + 8 * s);
-                tma_load_2d(st + C::X_BYTES, &tmH, (gk >> 2) * RAW_ROW, n0, bar_l_full + 8 * s);
-                tma_load_2d(st + C::X_BYTES + H_BYTES, &tmQ, (gk >> 2) * RAW_ROW + 16 + 32 * (gk & 3), n0,
-                            bar_l_full + 8 * s);
+                const int gk = k_step0 + kk;  // global 128-wide K step
+                const uint32_t st = sX + s * C::X_BYTES;
+                mbar_arrive_expect_tx(bar_x_full + 8 * s, C::X_BYTES);
+                // token box `rank` for both CTAs of the pair (the peer loads the other)
+                tma_load_2d_pair(st + rank * C::XBOX, &tmX, gk * BK + 64 * rank, m0, bar_x_full + 8 * s);
                 ++issued;
             }
-            // drain what is still in flight (only matters after an abort)
-            for (int kk = issued > C::L_STAGES ? issued - C::L_STAGES : 0; kk < issued; ++kk)
-                mbar_wait(bar_l_full + 8 * (kk % C::L_STAGES), (kk / C::L_STAGES) & 1, P.status);
+            // drain: every copy into this CTA has landed and both CTAs' last
+            // commits have arrived here before the CTA may exit
+            for (int kk = issued > C::X_STAGES ? issued - C::X_STAGES : 0; kk < issued; ++kk) {
+                mbar_wait(bar_x_full + 8 * (kk % C::X_STAGES), (kk / C::X_STAGES) & 1, P.status);
+                if (!*abort_flag) mbar_wait(bar_x_empty + 8 * (kk % C::X_STAGES), (kk / C::X_STAGES) & 1, P.status);
+            }
+        }
+    } else if (warp == W_RLOAD) {
+        // ------------------------------------------ raw weight producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int kk = 0; kk < P.nsteps; ++kk) {
+                const int r = kk % C::R_STAGES;
+                if (kk >= C::R_STAGES &&
+                    (*abort_flag || !mbar_wait(bar_r_empty + 8 * r, ((kk / C::R_STAGES) - 1) & 1, P.status))) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const int gk = k_step0 + kk;  // half gk&1 of super-block gk>>1
+                const uint32_t st = sR + r * R_BYTES;
+                mbar_arrive_expect_tx(bar_r_full + 8 * r, R_BYTES);
+                tma_load_2d(st, &tmH, (gk >> 1) * RAW_ROW, n0, bar_r_full + 8 * r);
+                tma_load_2d(st + H_BYTES, &tmQ, (gk >> 1) * RAW_ROW + 16 + 64 * (gk & 1), n0, bar_r_full + 8 * r);
+                ++issued;
+            }
+            for (int kk = issued > C::R_STAGES ? issued - C::R_STAGES : 0; kk < issued; ++kk)
+                mbar_wait(bar_r_full + 8 * (kk % C::R_STAGES), (kk / C::R_STAGES) & 1, P.status);
         }
     } else if (warp == W_MMA) {
         // -------------------------------------------------- MMA issuer
         if (lane == 0) {
             for (int kk = 0; kk < P.nsteps; ++kk) {
-                const int s = kk % C::L_STAGES, sa = kk % A_STAGES;
-                if (*abort_flag || !mbar_wait(bar_l_full + 8 * s, (kk / C::L_STAGES) & 1, P.status) ||
+                const int s = kk % C::X_STAGES, sa = kk % A_STAGES;
+                if (*abort_flag || !mbar_wait(bar_x_full + 8 * s, (kk / C::X_STAGES) & 1, P.status) ||
                     !mbar_wait(bar_a_full + 8 * sa, (kk / A_STAGES) & 1, P.status)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sx = sL + s * C::L_BYTES;
-                const uint32_t ta = tmem + C::A_COL0 + 32 * sa;
+                const uint32_t sx = sX + s * C::X_BYTES;
+                const uint32_t ta = tmem + C::A_COL0 + A_COLS * sa;
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
-                    mma_ts(tmem, ta + 8 * k, desc_sw128(sx + 32 * k), C::IDESC, (kk | k) ? 1u : 0u);
-                mma_commit(bar_l_empty + 8 * s);
+                    mma_ts(tmem, ta + 8 * k, desc_sw128(sx + (k >> 2) * C::XBOX + 32 * (k & 3)), C::IDESC,
+                           (kk | k) ? 1u : 0u);
+                mma_commit_pair(bar_x_empty + 8 * s);
                 mma_commit(bar_a_empty + 8 * sa);
             }
             // the accumulator is final once every MMA issued above completes
@@ -245,64 +321,75 @@ __global__ void __launch_bounds__(TcCfg<BT, G>::NTHREADS, 1)
         }
     } else {
         // ------------------------------------- dequantiser, then epilogue
-        // group g = (warp - 2) / 4 dequantises the K steps kk = g, g+G, ...
-        const int quarter = warp & 3, g = (warp - W_DQ0) >> 2;
+        // The four warps take every K step in order, so each parity wait on
+        // a ring stage is at most one phase ahead of the stage.
+        const int quarter = warp & 3;
         const int n = 32 * quarter + lane;  // weight row within the tile (= TMEM lane)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-        for (int kk = g; kk < P.nsteps; kk += G) {
-            const int s = kk % C::L_STAGES, sa = kk % A_STAGES, c = (k_step0 + kk) & 3;
+        for (int kk = 0; kk < P.nsteps; ++kk) {
+            const int r = kk % C::R_STAGES, sa = kk % A_STAGES;
             bool ok = !*abort_flag;
-            if (ok) ok = mbar_wait(bar_l_full + 8 * s, (kk / C::L_STAGES) & 1, P.status);
+            if (ok) ok = mbar_wait(bar_r_full + 8 * r, (kk / C::R_STAGES) & 1, P.status);
             if (ok && kk >= A_STAGES) ok = mbar_wait(bar_a_empty + 8 * sa, ((kk / A_STAGES) - 1) & 1, P.status);
             if (__any_sync(0xffffffffu, !ok)) {
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            const uint8_t *st = smem + s * C::L_BYTES + C::X_BYTES;
+            const int h = (k_step0 + kk) & 1;  // which half of the super-block
+            const uint8_t *st = smem + C::OFF_R + r * R_BYTES;
             const uint4 hdr = *reinterpret_cast<const uint4 *>(st + 16 * n);
-            const uint4 qa = *reinterpret_cast<const uint4 *>(st + H_BYTES + 32 * n);
-            const uint4 qb = *reinterpret_cast<const uint4 *>(st + H_BYTES + 32 * n + 16);
-            // six-bit scales and mins of sub-blocks 2c (low nibbles) and 2c+1
-            // (high nibbles), GGUF packing
+            // six-bit scales and mins of sub-blocks 4h..4h+3 (byte i: sub-block
+            // 4h+i), GGUF packing
             uint32_t scw, mw;
-            if (c < 2) {
+            if (h == 0) {
                 scw = hdr.y & 0x3F3F3F3Fu;
                 mw = hdr.z & 0x3F3F3F3Fu;
             } else {
                 scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
                 mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
             }
-            const int sh = 16 * (c & 1);
             const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
-            const __half2 ha0 = __float2half2_rn(d * static_cast<float>((scw >> sh) & 0xFF));
-            const __half2 ha1 = __float2half2_rn(d * static_cast<float>((scw >> (sh + 8)) & 0xFF));
-            const __half2 hb0 = __float2half2_rn(-(dmin * static_cast<float>((mw >> sh) & 0xFF)));
-            const __half2 hb1 = __float2half2_rn(-(dmin * static_cast<float>((mw >> (sh + 8)) & 0xFF)));
-            // weight l < 32 of the step is the low nibble of quant byte l,
-            // weight 32 + l its high nibble; TMEM column i holds weights 2i, 2i+1
-            const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-            uint32_t r[32];
+            // the quant row: 64 bytes whose 16-byte chunk f sits at f ^ ((n >> 1) & 3)
+            // (TMA 64-byte swizzle), so a quarter warp's loads hit distinct banks
+            const uint8_t *qrow = st + H_BYTES + 64 * n;
+            const int sw = (n >> 1) & 3;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                dequant4(qw[i], false, ha0, hb0, r[2 * i], r[2 * i + 1]);
-                dequant4(qw[i], true, ha1, hb1, r[16 + 2 * i], r[16 + 2 * i + 1]);
+            for (int cp = 0; cp < 2; ++cp) {
+                // chunk cp of 64 weights: quant bytes 32cp..32cp+31, low nibbles
+                // -> sub-block 4h+2cp, high nibbles -> sub-block 4h+2cp+1
+                const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp) ^ sw));
+                const uint4 qb = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp + 1) ^ sw));
+                const int sh = 16 * cp;
+                const __half2 ha0 = __float2half2_rn(d * static_cast<float>((scw >> sh) & 0xFF));
+                const __half2 ha1 = __float2half2_rn(d * static_cast<float>((scw >> (sh + 8)) & 0xFF));
+                const __half2 hb0 = __float2half2_rn(-(dmin * static_cast<float>((mw >> sh) & 0xFF)));
+                const __half2 hb1 = __float2half2_rn(-(dmin * static_cast<float>((mw >> (sh + 8)) & 0xFF)));
+                // weight l < 32 of the chunk is the low nibble of quant byte l,
+                // weight 32 + l its high nibble; TMEM column i holds weights 2i, 2i+1
+                const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    dequant4(qw[i], false, ha0, hb0, r[2 * i], r[2 * i + 1]);
+                    dequant4(qw[i], true, ha1, hb1, r[16 + 2 * i], r[16 + 2 * i + 1]);
+                }
+                tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
             }
-            tmem_st32(lane_base + C::A_COL0 + 32 * sa, r);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(bar_a_full + 8 * sa);
-                mbar_arrive(bar_l_empty + 8 * s);
+                mbar_arrive(bar_r_empty + 8 * r);
             }
         }
-        // epilogue: TMEM lanes of this quarter, token columns [g*BT/G, (g+1)*BT/G)
+        // epilogue: TMEM lanes of this quarter, all BT token columns
         const bool ok = mbar_wait(bar_acc, 0, P.status);
         if (__all_sync(0xffffffffu, ok) && !*abort_flag) {
             tc_fence_after();
             const int ncol = n0 + n;
 #pragma unroll 1
-            for (int cc = g * (BT / G); cc < (g + 1) * (BT / G); cc += 16) {
+            for (int cc = 0; cc < BT; cc += 16) {
                 float v[16];
                 tmem_ld16(lane_base + static_cast<uint32_t>(cc), v);
                 if (ncol < P.N) {
@@ -322,7 +409,7 @@ __global__ void __launch_bounds__(TcCfg<BT, G>::NTHREADS, 1)
         }
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     if (warp == W_MMA) {
         // every MMA must have completed before TMEM is released
         mbar_wait(bar_acc, 0, P.status);
@@ -354,16 +441,16 @@ bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
            M <= (int64_t(1) << 30) && K <= (int64_t(1) << 24) && encoder() != nullptr;
 }
 
-template <int BT, int G>
+template <int BT>
 cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, const void *xh, int64_t M, float *y,
                       cudaStream_t st, int num_sms, int *status) {
-    using C = TcCfg<BT, G>;
+    using C = TcCfg<BT>;
     CUtensorMap tx, th, tq;
     // tokens: fp16 [M][K], boxes of 64 K x BT rows, 128-byte swizzle
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {BK, BT};
+        const cuuint32_t box[2] = {64, BT};
         const cuuint32_t es[2] = {1, 1};
         if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(xh), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -371,19 +458,21 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
             return cudaErrorInvalidValue;
     }
     // raw weights as bytes [N][row bytes]: 16-byte boxes (super-block header)
-    // and 32-byte boxes (one K step's quants), 128 rows each
+    // and 64-byte boxes (one K step's quants, 64-byte swizzle), 128 rows each
     const int64_t rb = (K / 256) * RAW_ROW;
     for (int which = 0; which < 2; ++which) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
-        const cuuint32_t box[2] = {which ? 32u : 16u, static_cast<cuuint32_t>(BW)};
+        const cuuint32_t box[2] = {which ? 64u : 16u, static_cast<cuuint32_t>(BW)};
         const cuuint32_t es[2] = {1, 1};
         if (enc(which ? &tq : &th, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, which ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const int nt = static_cast<int>((N + BW - 1) / BW), mt = static_cast<int>((M + BT - 1) / BT);
+    // weight tiles in pairs (a CTA pair shares each token box by multicast)
+    const int nt = static_cast<int>(((N + BW - 1) / BW + 1) & ~int64_t(1)), mt = static_cast<int>((M + BT - 1) / BT);
     const int ksteps = static_cast<int>(K / BK);
     // Split K in two when the tiles alone would leave most SMs idle (two
     // contributions per output keep the fp32 result independent of order).
@@ -400,11 +489,22 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
         if (e != cudaSuccess) return e;
     }
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<BT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(gemm_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     P.nsteps = ksteps / splits;
-    gemm_tc_kernel<BT, G><<<dim3(nt, mt, splits), C::NTHREADS, C::SMEM_BYTES, st>>>(tx, th, tq, P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nt, mt, splits);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BT>, tx, th, tq, P);
 }
 
 }  // namespace
@@ -415,20 +515,9 @@ cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const 
                            cudaStream_t st, int num_sms, int *status) {
     if (!gemm_tc_supported(type, N, K, M)) return cudaErrorNotSupported;
     EncodeTiled enc = encoder();
-    static const int groups = [] {
-        const char *e = getenv("QMM_TC_GROUPS");
-        return e ? atoi(e) : 2;
-    }();
-#define QK_TC_LAUNCH(G)                                                                  \
-    do {                                                                                 \
-        if (M <= 64) return launch_bt<64, G>(enc, W, N, K, xh, M, y, st, num_sms, status);   \
-        if (M <= 128) return launch_bt<128, G>(enc, W, N, K, xh, M, y, st, num_sms, status); \
-        return launch_bt<256, G>(enc, W, N, K, xh, M, y, st, num_sms, status);               \
-    } while (0)
-    if (groups == 1) QK_TC_LAUNCH(1);
-    if (groups == 4) QK_TC_LAUNCH(4);
-    QK_TC_LAUNCH(2);
-#undef QK_TC_LAUNCH
+    if (M <= 64) return launch_bt<64>(enc, W, N, K, xh, M, y, st, num_sms, status);
+    if (M <= 128) return launch_bt<128>(enc, W, N, K, xh, M, y, st, num_sms, status);
+    return launch_bt<256>(enc, W, N, K, xh, M, y, st, num_sms, status);
 }
 
 }  // namespace qk

@@ -26,8 +26,11 @@ inline int block_weights(int t) { return t == QMM_Q8_0 ? 32 : 256; }
 // Status bits a kernel may raise in the per-device status word.
 enum : int { STATUS_TIMEOUT = 1 };
 
-// Wall-clock limit of every bounded wait (nanoseconds of %globaltimer).
-constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
+// Limit of every bounded wait, in SM clock cycles (2^31: about one second at
+// the 2 GHz class clocks of this part, longer at lower clocks).  The cycle
+// counter is read instead of %globaltimer because it is a register read,
+// cheap enough to sit in the polling loops of the pipelines.
+constexpr long long WAIT_LIMIT_CYCLES = 1ll << 31;
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -72,17 +75,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, giving up after
-// `limit_ns`; on expiry the status word `status` (device memory owned by the
-// library) records a timeout and the function returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status,
-                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
+// WAIT_LIMIT_CYCLES; on expiry the status word `status` (device memory owned
+// by the library) records a timeout and the function returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
+    const long long t0 = clock64();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > limit_ns) {
+        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
             atomicOr(status, STATUS_TIMEOUT);
             return false;
         }
