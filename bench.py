@@ -64,11 +64,25 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
 
 
-def load_traffic(kernel_file):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, or None when the kernel source changed since the capture."""
+TRAFFIC_SUMMARY = os.path.join("profiles", "gemv_q6k_lm_head_k2048_n128256.txt")
+TRAFFIC_SOURCES = ("mat_mul_gb300/csrc/gemv_sb.cu", "mat_mul_gb300/csrc/qmm_device.cuh",
+                   "mat_mul_gb300/csrc/qmm_internal.h")
+
+
+def sources_sha256(paths):
+    """sha256 over the named source files, concatenated in the given order."""
     import hashlib
-    summ = os.path.join(ROOT, "profiles", "gemv_q6k_lm_head_k2048_n128256.txt")
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None when the kernel's sources changed since the capture."""
+    summ = os.path.join(ROOT, TRAFFIC_SUMMARY)
     if not os.path.exists(summ):
         return None
     vals = {}
@@ -77,8 +91,7 @@ def load_traffic(kernel_file):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    src = open(os.path.join(ROOT, "mat_mul_gb300", "csrc", kernel_file), "rb").read()
-    if vals.get("source_sha256") != hashlib.sha256(src).hexdigest():
+    if vals.get("source_sha256") != sources_sha256(TRAFFIC_SOURCES):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -319,7 +332,12 @@ def run_ours(args):
             ms = float(t.item())
         return ms
 
-    launches_per_step = 2 * len(mats)
+    # kernels of this library launched per decode step, counted by the library
+    n0 = q.qmm_launch_count()
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    launches_per_step = q.qmm_launch_count() - n0
 
     # ---- headline: the decode step, weights resident
     g_step = capture(step)
@@ -364,7 +382,7 @@ def run_ours(args):
                            "N": m["N"], "MB": round(m["bytes"] / 1e6, 3), "us": round(t_ms * 1e3, 2),
                            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4)})
             if m["name"] == "cfg2:lm_head":
-                traffic = load_traffic("gemv_sb.cu")
+                traffic = load_traffic()
                 roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
                         "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
                         "traffic": traffic, "kernel": "gemv_sb_kernel<Q6_K,1> (qmm, lm_head 2048x128256)",
@@ -473,6 +491,28 @@ def run_ncu_case(name, calls=3):
     return 0
 
 
+def run_ncu_step(steps):
+    """`steps` eager decode steps (the headline workload's calls in order, no
+    graphs), for an ncu launch list with one entry per kernel launch."""
+    import torch
+
+    import mat_mul_gb300 as q
+    torch.cuda.set_device(0)
+    q.load()
+    mats = decode_workload()
+    for m in mats:
+        m["W"] = torch.from_numpy(synth.config_weights(m["cfg"], m["idx"])).cuda()
+        m["x"] = torch.from_numpy(synth.config_activations(m["cfg"], 1, m["K"])).cuda()
+        m["y"] = torch.empty((1, m["N"]), dtype=torch.float32, device="cuda")
+    for _ in range(steps):
+        for m in mats:
+            q.qmm(m["qtype"], m["W"], m["N"], m["K"], m["x"], y=m["y"])
+    torch.cuda.synchronize()
+    assert q.qmm_device_status() == 0
+    print("decode steps ok", steps, len(mats), "calls per step")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -483,7 +523,11 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline and e2e only")
     ap.add_argument("--ncu-case", default=None,
                     help="run three eager calls of one matrix (e.g. cfg2:lm_head) and exit")
+    ap.add_argument("--ncu-step", type=int, default=0,
+                    help="run this many eager decode steps (for an ncu launch list) and exit")
     args = ap.parse_args()
+    if args.ncu_step:
+        return run_ncu_step(args.ncu_step)
     if args.ncu_case:
         return run_ncu_case(args.ncu_case)
     if args.warmup < 3:

@@ -228,7 +228,8 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     //   sb   : decode, one weight block per lane, quantises x itself (one
     //          launch, no workspace); M <= 8 when the activations fit
     //   gemv : decode, 32 units per round, after the quantiser kernel
-    //   gemm : prefill on the integer tensor cores, after the quantiser
+    //   gemm : prefill after the quantiser: Q4_K on tcgen05 (fp16 operands,
+    //          fp32 accumulators), other types on the int8 mma.sync kernel
     if (M <= 8 && !g_force_round_gemv && qk::gemv_sb_fits(type, static_cast<int>(M), K, di.max_smem)) {
         e = qk::launch_gemv_sb(type, W_blocks, N, K, x, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
                                di.status);
