@@ -44,6 +44,8 @@ struct SbParams {
     int nb;  // blocks per row
     int RB;  // bytes per row
     int NSW, slot_bytes;
+    uint32_t nb_magic;  // floor(2^32 / nb) + 1 when u / nb == umulhi(u, nb_magic) for every
+                        // block index u of a CTA (u * nb < 2^32), else 0 (divide)
     int64_t rows_q;  // N / gridDim.x
     int rows_r;      // N % gridDim.x: the first rows_r CTAs take one row more
     const float *x;  // [M][K] activations, fp32
@@ -483,7 +485,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_kernel(const __grid_const
         const int base = ring + slot * P.slot_bytes - a16 + cta_off;
         const int u = u0 + lane;
         const bool valid = lane < nv;
-        const int row = valid ? u / P.nb : -1;
+        const int row = !valid ? -1
+                        : P.nb_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(u), P.nb_magic))
+                                     : u / P.nb;
         float v[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) v[m] = 0.0f;
@@ -668,6 +672,13 @@ cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const 
     const int g = static_cast<int>(grid);
     P.rows_q = N / g;
     P.rows_r = static_cast<int>(N % g);
+    // Row of block u by multiply-high: with M = floor(2^32/nb) + 1 and
+    // e = M*nb - 2^32 in (0, nb], u*M/2^32 = u/nb + u*e/(nb*2^32), whose
+    // floor is floor(u/nb) whenever u*e < 2^32, which u*nb < 2^32 ensures.
+    const uint64_t u_max = static_cast<uint64_t>(P.rows_q + 1) * static_cast<uint64_t>(P.nb);
+    P.nb_magic = u_max * static_cast<uint64_t>(P.nb) < (uint64_t(1) << 32)
+                     ? static_cast<uint32_t>((uint64_t(1) << 32) / static_cast<uint64_t>(P.nb) + 1)
+                     : 0u;
     switch (type) {
     case QMM_Q8_0: return launch_m<QMM_Q8_0>(P, mt_of(M), g, smem, st);
     case QMM_Q4_K: return launch_m<QMM_Q4_K>(P, mt_of(M), g, smem, st);

@@ -200,3 +200,42 @@ def test_gemv_sb_address_arithmetic(qtype, N, K):
 def test_gemv_sb_fits_the_workloads():
     for (_, q, K, N) in synth.LLAMA_1B + synth.QWEN3_14B_LAYER + synth.LM_HEAD:
         assert plan_sb(q, 1, K) is not None, (q, K)
+
+
+# ---- row of a block by multiply-high (gemv_sb.cu, launch_gemv_sb) ----------
+def nb_magic(rows_q, nb):
+    """Mirror of the host rule: the multiplier, or 0 when the CTA's block
+    indices are too large for the multiply-high identity."""
+    u_max = (rows_q + 1) * nb
+    return (1 << 32) // nb + 1 if u_max * nb < (1 << 32) else 0
+
+
+def umulhi(a, b):
+    return (a * b) >> 32
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 7, 8, 16, 20, 32, 68, 160, 544, 4096, 65535])
+def test_row_by_multiply_high_exact(nb):
+    rows_q = min(4096, ((1 << 32) - 1) // (nb * nb) - 1)
+    magic = nb_magic(rows_q, nb)
+    assert magic
+    U = (rows_q + 1) * nb
+    import numpy as np
+    u = np.arange(U, dtype=np.uint64)
+    got = (u * np.uint64(magic)) >> np.uint64(32)
+    assert np.array_equal(got, u // np.uint64(nb))
+
+
+def test_row_by_multiply_high_workloads():
+    for (_, q, K, N) in synth.LLAMA_1B + synth.QWEN3_14B_LAYER + synth.LM_HEAD + synth.Q8_SMALL:
+        nb = K // synth.BLOCK_WEIGHTS[q]
+        rows_q = N // min(SMS, N)
+        magic = nb_magic(rows_q, nb)
+        assert magic, (K, N)
+        for u in range((rows_q + 1) * nb):
+            assert umulhi(u, magic) == u // nb
+
+
+def test_row_by_multiply_high_refuses_large_products():
+    # Q8_0 with K = 4M (nb = 131072) and thousands of rows per CTA: divide instead
+    assert nb_magic(10000, 131072) == 0

@@ -132,6 +132,61 @@ def test_qmm_prefill_small(cuda_lib, qtype, N, K, M):
     _assert_within_bound(y, yo, A, f"type {qtype} N={N} K={K} M={M}")
 
 
+# Q4_K prefill shapes whose tiles the stream-K schedule of the tcgen05 GEMM
+# splits between CTA pairs: two pieces per tile with ragged M and N (and a
+# half-empty last pair), eight pieces (one tile summed from seven partials),
+# three pieces with an odd number of weight tiles.
+STREAM_K = [(1000, 2048, 300), (256, 8192, 70), (384, 3072, 40)]
+
+
+@pytest.mark.parametrize("N,K,M", STREAM_K)
+def test_qmm_prefill_split_tiles(cuda_lib, N, K, M):
+    qtype = synth.Q4_K
+    W = synth.weights(qtype, N, K, seed=N + K + M + 7)
+    x = synth.activations(M, K, seed=N * K + M + 7, outlier_frac=0.01)
+    y = _run_qmm(cuda_lib, qtype, W, N, K, x)
+    yo, A = O.qmm(qtype, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"split tiles N={N} K={K} M={M}")
+
+
+def test_qmm_prefill_is_deterministic(cuda_lib):
+    import torch
+    N, K, M = STREAM_K[1]
+    W = _dev(synth.weights(synth.Q4_K, N, K, seed=11))
+    x = _dev(synth.activations(M, K, seed=12))
+    y1 = torch.full((M, N), float("nan"), device="cuda")
+    cuda_lib.qmm(synth.Q4_K, W, N, K, x, y=y1)
+    for _ in range(3):
+        y2 = cuda_lib.qmm(synth.Q4_K, W, N, K, x)
+        assert torch.equal(y1, y2)
+    assert cuda_lib.qmm_device_status() == 0
+
+
+def test_qmm_prefill_in_cuda_graph_replays(cuda_lib):
+    """The split-tile hand-off flags are set and cleared inside each launch,
+    so replays of a captured call give the eager result every time."""
+    import torch
+    N, K, M = STREAM_K[1]
+    W = _dev(synth.weights(synth.Q4_K, N, K, seed=13))
+    x = _dev(synth.activations(M, K, seed=14))
+    ref = cuda_lib.qmm(synth.Q4_K, W, N, K, x)
+    st = torch.cuda.Stream()
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(st):
+        cuda_lib.qmm(synth.Q4_K, W, N, K, x, y=y, stream=st)  # workspace of this stream
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        cuda_lib.qmm(synth.Q4_K, W, N, K, x, y=y, stream=st)
+    for _ in range(3):
+        y.fill_(float("nan"))
+        with torch.cuda.stream(st):
+            g.replay()
+        st.synchronize()
+        assert torch.equal(y, ref)
+    assert cuda_lib.qmm_device_status() == 0
+
+
 def test_qmm_is_deterministic_and_overwrites_y(cuda_lib):
     import torch
     qtype, N, K = synth.Q6_K, 300, 5120
