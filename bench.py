@@ -50,6 +50,29 @@ def decode_workload():
     return mats
 
 
+# The decode step's launches: matrices that read the same activations in a
+# real layer (q/k/v of attention, gate/up of the MLP) go in one qmm_group
+# call; the others are single qmm calls.  Names index decode_workload().
+STEP_CALLS = [("cfg1:q", "cfg1:kv"), ("cfg1:gate_up",), ("cfg1:down",), ("cfg2:lm_head",),
+              ("cfg3:q", "cfg3:k", "cfg3:v"), ("cfg3:o",), ("cfg3:gate", "cfg3:up"), ("cfg3:down",)]
+LAYER_CALLS = [c for c in STEP_CALLS if c[0].startswith("cfg3:")]
+
+
+def make_calls(mats, calls):
+    by = {m["name"]: m for m in mats}
+    return [[by[n] for n in c] for c in calls]
+
+
+def run_call(q, call, stream, W_of=lambda m: m["W"]):
+    """One launch of the step: a group of matrices sharing x, or one matrix."""
+    if len(call) == 1:
+        m = call[0]
+        q.qmm(m["qtype"], W_of(m), m["N"], m["K"], m["x"], y=m["y"], stream=stream)
+    else:
+        q.qmm_group([(m["qtype"], W_of(m), m["N"], m["y"]) for m in call], call[0]["K"], call[0]["x"],
+                    stream=stream)
+
+
 WORKLOAD_NAME = ("decode M=1: Llama-3.2-1B Q4_K projections + Q6_K lm_head 2048x128256 + "
                  "Qwen3-14B Q4_K_M layer (q,k,v,o,gate,up,down)")
 
@@ -292,15 +315,24 @@ def run_ours(args):
         m["y"] = torch.empty((1, m["N"]), dtype=torch.float32, device=dev)
         m["y_host"] = torch.empty((1, m["N"]), dtype=torch.float32).pin_memory()
 
+    calls = make_calls(mats, STEP_CALLS)
+    for call in calls:
+        # a group reads one x (its members' synthetic activations coincide:
+        # same config and K); the first member's buffer is the shared one
+        for m in call[1:]:
+            assert torch.equal(m["x_host"], call[0]["x_host"])
+            m["x"], m["x_host"] = call[0]["x"], call[0]["x_host"]
+
     def step():
-        for m in mats:
-            q.qmm(m["qtype"], m["W"], m["N"], m["K"], m["x"], y=m["y"], stream=stream)
+        for call in calls:
+            run_call(q, call, stream)
 
     def step_e2e():
-        for m in mats:
-            m["x"].copy_(m["x_host"], non_blocking=True)
-            q.qmm(m["qtype"], m["W"], m["N"], m["K"], m["x"], y=m["y"], stream=stream)
-            m["y_host"].copy_(m["y"], non_blocking=True)
+        for call in calls:
+            call[0]["x"].copy_(call[0]["x_host"], non_blocking=True)
+            run_call(q, call, stream)
+            for m in call:
+                m["y_host"].copy_(m["y"], non_blocking=True)
 
     def capture(fn):
         with torch.cuda.stream(stream):
@@ -359,12 +391,13 @@ def run_ours(args):
     # ---- end to end: x copied in and y copied out every call
     g_e2e = capture(step_e2e)
     ms_e2e = timed(g_e2e, args.steps, args.warmup)
-    h2d = sum(m["K"] * 4 for m in mats)
+    h2d = sum(call[0]["K"] * 4 for call in calls)
     d2h = sum(m["N"] * 4 for m in mats)
     e2e_value = world * step_bytes / (ms_e2e * 1e-3) / 1e9
     del g_e2e, g_step
 
     detail = []
+    groups = layer = None
     roof = None
     gemm = None
     cpu = None
@@ -397,6 +430,32 @@ def run_ours(args):
                         "peak_source": peaks["source"] + " hbm_gbs (copy, burst)"}
             del g, copies
             torch.cuda.empty_cache()
+
+        # ---- the grouped launches alone, and the Qwen3-14B layer as the step
+        # runs it (four launches), over rotating copies >= 4x L2
+        def rotating(call_list):
+            nbytes = sum(m["bytes"] for c in call_list for m in c)
+            ncopy = min(64, max(2, -(-4 * L2_BYTES // nbytes)))
+            copies = {m["name"]: [m["W"]] + [m["W"].clone() for _ in range(ncopy - 1)]
+                      for c in call_list for m in c}
+            inner = max(ncopy, 8)
+
+            def fn():
+                for i in range(inner):
+                    for c in call_list:
+                        run_call(q, c, stream, W_of=lambda m, i=i: copies[m["name"]][i % ncopy])
+
+            g = capture(fn)
+            t_ms = timed(g, 5, 2) / inner
+            del g, copies
+            torch.cuda.empty_cache()
+            gbs = nbytes / (t_ms * 1e-3) / 1e9
+            return {"matrices": "+".join(m["name"] for c in call_list for m in c), "launches": len(call_list),
+                    "MB": round(nbytes / 1e6, 3), "us": round(t_ms * 1e3, 2), "GB/s": round(gbs, 1),
+                    "frac_hbm": round(gbs / peaks["hbm"], 4)}
+
+        groups = [rotating([c]) for c in make_calls(mats, STEP_CALLS) if len(c) > 1]
+        layer = rotating(make_calls(mats, LAYER_CALLS))
 
         # ---- prefill GEMM, M=512
         gemm = []
@@ -452,6 +511,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": WORKLOAD_NAME, "M": 1, "matrices": len(mats),
+                       "launches_per_step": launches_per_step,
                        "weight_bytes_per_step": step_bytes, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (447 MB of weights per step)",
                        "frac_hbm_step": round(value / world / peaks["hbm"], 4)},
@@ -460,7 +520,8 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
                     "note": "weights resident (model state); x in and y out every call"},
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks, "per_matrix": detail, "prefill_gemm": gemm,
+            "clocks": clocks, "per_matrix": detail, "groups": groups, "qwen3_14b_layer": layer,
+            "prefill_gemm": gemm,
         }
         print(json.dumps(line))
     if dist:
@@ -511,12 +572,17 @@ def run_ncu_step(steps):
         m["W"] = torch.from_numpy(synth.config_weights(m["cfg"], m["idx"])).cuda()
         m["x"] = torch.from_numpy(synth.config_activations(m["cfg"], 1, m["K"])).cuda()
         m["y"] = torch.empty((1, m["N"]), dtype=torch.float32, device="cuda")
+    calls = make_calls(mats, STEP_CALLS)
+    for call in calls:
+        for m in call[1:]:
+            m["x"] = call[0]["x"]
+    stream = torch.cuda.current_stream()
     for _ in range(steps):
-        for m in mats:
-            q.qmm(m["qtype"], m["W"], m["N"], m["K"], m["x"], y=m["y"])
+        for call in calls:
+            run_call(q, call, stream)
     torch.cuda.synchronize()
     assert q.qmm_device_status() == 0
-    print("decode steps ok", steps, len(mats), "calls per step")
+    print("decode steps ok", steps, len(calls), "launches per step")
     return 0
 
 

@@ -78,7 +78,10 @@ QMM_API int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *ou
 /*
  * qmm -- y[M,N] = W[N,K] . x[M,K]^T with the activations quantised to int8
  * in blocks of 32 (Q8_1 style: fp32 scale max|x|/127, round half away from
- * zero, block sum), exact int32 per-block dot products, fp32 scaling.
+ * zero, block sum), exact int32 per-block dot products, fp32 scaling (the
+ * Q4_K prefill instead contracts the dequantised weights and activations,
+ * each rounded to fp16, with fp32 accumulation on the tcgen05 tensor cores:
+ * sm_103a has no integer tcgen05 mode).
  *   type     : qmm_type of W.
  *   W_blocks : device, N*(K/QK) blocks, row-major by output row, 16-B aligned.
  *   N, K     : output rows and reduction length; K a multiple of QK.
@@ -98,6 +101,28 @@ QMM_API int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *ou
  */
 QMM_API int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, int64_t M,
         float *y, void *stream);
+
+/*
+ * qmm_group -- several products that read the same activations:
+ *   y_i[M,N_i] = W_i[N_i,K] . x[M,K]^T for i < n, each as
+ *   qmm(types[i], Ws[i], Ns[i], K, x, M, ys[i], stream).
+ * (An attention layer's q, k and v projections read one x, as do an MLP's
+ * gate and up; the infr page runs gate and up of an expert as one op.)
+ *   n          : 1 <= n <= QMM_GROUP_MAX.
+ *   types, Ws, Ns, ys : HOST arrays of n entries; the types may differ; every
+ *                W 16-byte aligned, K a multiple of every type's QK; an entry
+ *                with N = 0 is skipped.
+ *   K, x, M, stream : shared by all entries, as in qmm().
+ * With M <= 8 the whole group is ONE launch of the decode kernel: its CTAs are
+ * split between the matrices in proportion to their weight bytes and each
+ * quantises x itself.  Otherwise (or when a matrix does not fit that kernel)
+ * the products run one after another as qmm() calls.  Accuracy as qmm().
+ * Every entry is validated before anything is launched; errors as qmm(),
+ * QMM_EINVAL_SHAPE for n out of range, QMM_EINVAL_PTR for a null array.
+ */
+#define QMM_GROUP_MAX 8
+QMM_API int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns, int64_t K,
+                      const float *x, int64_t M, float *const *ys, void *stream);
 
 /*
  * qmm_quantize_act -- the activation quantiser on its own (test hook and

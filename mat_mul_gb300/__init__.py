@@ -55,13 +55,14 @@ def load():
     L.qmm.argtypes = [I, P, I64, I64, P, I64, P, P]
     L.qmm_noalloc.argtypes = [I, P, I64, I64, P, I64, P, P]
     L.qmm_quantize_act.argtypes = [P, I64, I64, P, P, P, P]
+    L.qmm_group.argtypes = [I, P, P, P, I64, P, I64, P, P]
     L.qmm_strerror.argtypes = [I]
     L.qmm_strerror.restype = ctypes.c_char_p
     L.qmm_last_error.restype = ctypes.c_char_p
     L.qmm_device_status.argtypes = [P]
     L.qmm_launch_count.restype = I64
     for f in ("qmm_dequant", "qmm", "qmm_noalloc", "qmm_quantize_act", "qmm_device_status",
-              "qmm_release"):
+              "qmm_release", "qmm_group"):
         getattr(L, f).restype = I
     _lib = L
     return L
@@ -118,6 +119,31 @@ def qmm(qtype: int, W, N: int, K: int, x, y=None, stream=None):
     _check(load().qmm(int(qtype), _ptr(W), int(N), int(K), _ptr(x), int(M), _ptr(y),
                       _stream_handle(stream)))
     return y
+
+
+def qmm_group(items, K: int, x, stream=None):
+    """Several products that read the same x [M, K] (or [K]): items is a list
+    of (qtype, W, N) or (qtype, W, N, y); returns the list of y tensors
+    [M, N_i].  With M <= 8 the group is one decode launch."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 tensor")
+    M = 1 if x.dim() == 1 else x.shape[0]
+    if x.shape[-1] != K:
+        raise ValueError(f"x has {x.shape[-1]} columns, K = {K}")
+    n = len(items)
+    ys = []
+    for it in items:
+        y = it[3] if len(it) > 3 and it[3] is not None else torch.empty(
+            (M, int(it[2])), dtype=torch.float32, device=x.device)
+        _require_cuda(it[1], x, y)
+        ys.append(y)
+    types = (ctypes.c_int * max(n, 1))(*[int(it[0]) for it in items])
+    Ws = (ctypes.c_void_p * max(n, 1))(*[_ptr(it[1]) for it in items])
+    Ns = (ctypes.c_int64 * max(n, 1))(*[int(it[2]) for it in items])
+    Ys = (ctypes.c_void_p * max(n, 1))(*[_ptr(y) for y in ys])
+    _check(load().qmm_group(int(n), types, Ws, Ns, int(K), _ptr(x), int(M), Ys, _stream_handle(stream)))
+    return ys
 
 
 def qmm_noalloc(qtype: int, W, N: int, K: int, x, y, stream=None):

@@ -37,6 +37,7 @@ constexpr int HEAD_BYTES = 2048; // mbarriers and warp-edge records
 constexpr int MAX_NSW = 6;
 
 struct SbParams {
+    int type;             // qmm_type of W
     const uint8_t *W;
     int64_t total_bytes;  // N * RB
     int64_t N;
@@ -46,8 +47,8 @@ struct SbParams {
     int NSW, slot_bytes;
     uint32_t nb_magic;  // floor(2^32 / nb) + 1 when u / nb == umulhi(u, nb_magic) for every
                         // block index u of a CTA (u * nb < 2^32), else 0 (divide)
-    int64_t rows_q;  // N / gridDim.x
-    int rows_r;      // N % gridDim.x: the first rows_r CTAs take one row more
+    int64_t rows_q;  // N / (CTAs of this matrix)
+    int rows_r;      // N % (CTAs of this matrix): the first rows_r CTAs take one row more
     const float *x;  // [M][K] activations, fp32
     int x_vec;       // x is 16-byte aligned: load four at a time
     int q_ld;        // bytes per activation row of q (a multiple of 256)
@@ -390,13 +391,13 @@ __device__ __forceinline__ void quantize_to_smem(const SbParams &P, uint8_t *sme
     else quantize_tpb<T, 2, 4>(P, smem, after_loads);
 }
 
+// The work of CTA `cta` of one matrix (its share of the rows).
 template <int T, int MT>
-__global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_kernel(const __grid_constant__ SbParams P) {
+__device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int BB = Fmt<T>::BB;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int cta = blockIdx.x;
     const int64_t r0 = P.rows_q * cta + min(cta, P.rows_r);
     const int64_t r1 = r0 + P.rows_q + (cta < P.rows_r ? 1 : 0);
     const int U = static_cast<int>(r1 - r0) * P.nb;  // blocks of this CTA
@@ -575,6 +576,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_kernel(const __grid_const
     }
 }
 
+template <int T, int MT>
+__global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_kernel(const __grid_constant__ SbParams P) {
+    sb_body<T, MT>(P, static_cast<int>(blockIdx.x));
+}
+
+// Several matrices that share K and x in one launch: CTAs
+// [cta_begin[i], cta_begin[i+1]) work on matrix i, each as in the single
+// launch (its own type, shared-memory plan and share of rows).
+struct SbGroup {
+    int n;
+    int cta_begin[QMM_GROUP_MAX + 1];
+    SbParams p[QMM_GROUP_MAX];
+};
+
+template <int MT>
+__global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_group_kernel(const __grid_constant__ SbGroup G) {
+    int i = 0;
+    while (i + 1 < G.n && static_cast<int>(blockIdx.x) >= G.cta_begin[i + 1]) ++i;
+    const SbParams &P = G.p[i];
+    const int cta = static_cast<int>(blockIdx.x) - G.cta_begin[i];
+    switch (P.type) {
+    case QMM_Q4_K: sb_body<QMM_Q4_K, MT>(P, cta); break;
+    case QMM_Q6_K: sb_body<QMM_Q6_K, MT>(P, cta); break;
+    default: sb_body<QMM_Q8_0, MT>(P, cta); break;
+    }
+}
+
 int mt_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
 int64_t align64(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
@@ -645,31 +673,30 @@ bool gemv_sb_fits(int type, int M, int64_t K, int max_smem) {
     return plan_sb(type, M, K, max_smem, P, smem);
 }
 
-cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const float *x, int M,
-                           float *y, cudaStream_t st, int num_sms, int max_smem, int *status) {
-    SbParams P = {};
-    int smem = 0;
-    if (!plan_sb(type, M, K, max_smem, P, smem)) return cudaErrorInvalidValue;
-    const int BB = block_bytes(type);
+namespace {
+
+// CTAs a matrix needs at least, so that one CTA's bytes fit 30 bits.
+int64_t min_ctas(int64_t N, int RB) {
+    const int64_t max_rows = (int64_t(1) << 30) / RB;
+    return (N + max_rows - 1) / max_rows;
+}
+
+// Everything but the shared-memory plan: matrix, activations, and the split
+// of the N rows over g CTAs.
+void fill(SbParams &P, int type, const void *W, int64_t N, int64_t K, const float *x, int M, float *y,
+          int *status, int g) {
+    P.type = type;
     P.W = static_cast<const uint8_t *>(W);
     P.N = N;
     P.K = static_cast<int>(K);
     P.M = M;
     P.nb = static_cast<int>(K / block_weights(type));
-    P.RB = P.nb * BB;
+    P.RB = P.nb * block_bytes(type);
     P.total_bytes = N * static_cast<int64_t>(P.RB);
     P.x = x;
     P.x_vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0 ? 1 : 0;
     P.y = y;
     P.status = status;
-    // one CTA per SM; more when a CTA's bytes would not fit 31 bits
-    int64_t grid = num_sms;
-    const int64_t max_rows = (int64_t(1) << 30) / P.RB;
-    if ((N + grid - 1) / grid > max_rows) grid = (N + max_rows - 1) / max_rows;
-    if (N < grid) grid = N;
-    if (grid < 1) grid = 1;
-    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-    const int g = static_cast<int>(grid);
     P.rows_q = N / g;
     P.rows_r = static_cast<int>(N % g);
     // Row of block u by multiply-high: with M = floor(2^32/nb) + 1 and
@@ -679,10 +706,115 @@ cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const 
     P.nb_magic = u_max * static_cast<uint64_t>(P.nb) < (uint64_t(1) << 32)
                      ? static_cast<uint32_t>((uint64_t(1) << 32) / static_cast<uint64_t>(P.nb) + 1)
                      : 0u;
+}
+
+template <int MT>
+cudaError_t launch_group_mt(const SbGroup &G, int grid, int smem, cudaStream_t st) {
+    auto kfn = gemv_sb_group_kernel<MT>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kfn, G);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const float *x, int M,
+                           float *y, cudaStream_t st, int num_sms, int max_smem, int *status) {
+    SbParams P = {};
+    int smem = 0;
+    if (!plan_sb(type, M, K, max_smem, P, smem)) return cudaErrorInvalidValue;
+    // one CTA per SM; more when a CTA's bytes would not fit 30 bits
+    int64_t grid = num_sms;
+    const int64_t need = min_ctas(N, static_cast<int>(K / block_weights(type)) * block_bytes(type));
+    if (grid < need) grid = need;
+    if (N < grid) grid = N;
+    if (grid < 1) grid = 1;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    const int g = static_cast<int>(grid);
+    fill(P, type, W, N, K, x, M, y, status, g);
     switch (type) {
     case QMM_Q8_0: return launch_m<QMM_Q8_0>(P, mt_of(M), g, smem, st);
     case QMM_Q4_K: return launch_m<QMM_Q4_K>(P, mt_of(M), g, smem, st);
     default: return launch_m<QMM_Q6_K>(P, mt_of(M), g, smem, st);
+    }
+}
+
+void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t *need, int num_sms, int *g) {
+    // CTAs in proportion to the bytes (largest remainders), at least one per
+    // matrix (and at least `need`), at most one per row
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) total += bytes[i];
+    int used = 0;
+    double frac[QMM_GROUP_MAX];
+    for (int i = 0; i < n; ++i) {
+        const double want = total > 0 ? static_cast<double>(num_sms) * static_cast<double>(bytes[i]) /
+                                            static_cast<double>(total)
+                                      : 1.0;
+        int64_t gi = static_cast<int64_t>(want);
+        frac[i] = want - static_cast<double>(gi);
+        if (gi < 1) gi = 1;
+        if (gi < need[i]) gi = need[i];
+        if (gi > rows[i]) gi = rows[i];
+        g[i] = static_cast<int>(gi);
+        used += g[i];
+    }
+    while (used < num_sms) {
+        int best = -1;
+        for (int i = 0; i < n; ++i)
+            if (frac[i] >= 0.0 && g[i] < rows[i] && (best < 0 || frac[i] > frac[best])) best = i;
+        if (best < 0) break;
+        ++g[best];
+        frac[best] = -1.0;  // at most one extra CTA each
+        ++used;
+    }
+}
+
+cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws, const int64_t *Ns, int64_t K,
+                                 const float *x, int M, float *const *ys, cudaStream_t st, int num_sms,
+                                 int max_smem, int *status) {
+    if (n < 1 || n > QMM_GROUP_MAX) return cudaErrorInvalidValue;
+    SbGroup G = {};
+    int idx[QMM_GROUP_MAX], smem = 0, m = 0;
+    int64_t bytes[QMM_GROUP_MAX], rows[QMM_GROUP_MAX], need[QMM_GROUP_MAX];
+    for (int i = 0; i < n; ++i) {
+        if (Ns[i] <= 0) continue;  // an empty matrix gets no CTA
+        int sm = 0;
+        if (!plan_sb(types[i], M, K, max_smem, G.p[m], sm)) return cudaErrorNotSupported;
+        if (sm > smem) smem = sm;
+        const int RB = static_cast<int>(K / block_weights(types[i])) * block_bytes(types[i]);
+        bytes[m] = Ns[i] * RB;
+        rows[m] = Ns[i];
+        need[m] = min_ctas(Ns[i], RB);
+        idx[m++] = i;
+    }
+    if (m == 0) return cudaSuccess;
+    int g[QMM_GROUP_MAX];
+    group_ctas(m, bytes, rows, need, num_sms, g);
+    G.n = m;
+    int64_t grid = 0;
+    for (int j = 0; j < m; ++j) {
+        const int i = idx[j];
+        G.cta_begin[j] = static_cast<int>(grid);
+        fill(G.p[j], types[i], Ws[i], Ns[i], K, x, M, ys[i], status, g[j]);
+        grid += g[j];
+    }
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    G.cta_begin[m] = static_cast<int>(grid);
+    switch (mt_of(M)) {
+    case 1: return launch_group_mt<1>(G, static_cast<int>(grid), smem, st);
+    case 2: return launch_group_mt<2>(G, static_cast<int>(grid), smem, st);
+    case 4: return launch_group_mt<4>(G, static_cast<int>(grid), smem, st);
+    default: return launch_group_mt<8>(G, static_cast<int>(grid), smem, st);
     }
 }
 

@@ -292,6 +292,55 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     return QMM_OK;
 }
 
+int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns, int64_t K, const float *x,
+              int64_t M, float *const *ys, void *stream) {
+    g_err[0] = 0;
+    if (n < 1 || n > QMM_GROUP_MAX) return fail(QMM_EINVAL_SHAPE, "n=%d: a group has 1..%d matrices", n, QMM_GROUP_MAX);
+    if (!types || !Ws || !Ns || !ys) return fail(QMM_EINVAL_PTR, "null array");
+    if (M < 0 || K < 0 || K > (int64_t(1) << 24))
+        return fail(QMM_EINVAL_SHAPE, "K=%lld M=%lld", static_cast<long long>(K), static_cast<long long>(M));
+    // types and shapes of every entry first, then pointers
+    for (int i = 0; i < n; ++i) {
+        if (int rc = check_type(types[i])) return rc;
+        if (Ns[i] < 0 || K % qk::block_weights(types[i]))
+            return fail(QMM_EINVAL_SHAPE, "entry %d: N=%lld K=%lld (K a multiple of %d)", i,
+                        static_cast<long long>(Ns[i]), static_cast<long long>(K), qk::block_weights(types[i]));
+    }
+    bool any = false;
+    for (int i = 0; i < n; ++i) {
+        if (Ns[i] == 0 || M == 0) continue;
+        any = true;
+        if (!ys[i] || !aligned(ys[i], 4)) return fail(QMM_EINVAL_PTR, "entry %d: y null or not 4-byte aligned", i);
+        if (K > 0 && (!Ws[i] || !aligned(Ws[i], 16)))
+            return fail(QMM_EINVAL_PTR, "entry %d: W null or not 16-byte aligned", i);
+    }
+    if (!any) return QMM_OK;
+    if (K > 0 && (!x || !aligned(x, 4))) return fail(QMM_EINVAL_PTR, "x null or not 4-byte aligned");
+
+    if (K > 0 && M <= 8 && !g_force_round_gemv) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+        DeviceInfo di;
+        if (int rc = device_info(dev, di)) return rc;
+        bool fits = true;
+        for (int i = 0; i < n; ++i)
+            fits = fits && (Ns[i] == 0 || qk::gemv_sb_fits(types[i], static_cast<int>(M), K, di.max_smem));
+        if (fits) {
+            e = qk::launch_gemv_sb_group(n, types, Ws, Ns, K, x, static_cast<int>(M), ys,
+                                         static_cast<cudaStream_t>(stream), di.num_sms, di.max_smem, di.status);
+            if (e != cudaSuccess) return cuda_fail(e, "group gemv launch");
+            g_launches.fetch_add(1);
+            return QMM_OK;
+        }
+    }
+    for (int i = 0; i < n; ++i) {
+        if (Ns[i] == 0) continue;
+        if (int rc = qmm(types[i], Ws[i], Ns[i], K, x, M, ys[i], stream)) return rc;
+    }
+    return QMM_OK;
+}
+
 int qmm_device_status(void *stream) {
     g_err[0] = 0;
     int dev = 0;

@@ -48,6 +48,13 @@ cudaError_t launch_gemv(int type, const void *W, int64_t N, int64_t K, const int
 bool gemv_sb_fits(int type, int M, int64_t K, int max_smem);
 cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const float *x, int M,
                            float *y, cudaStream_t st, int num_sms, int max_smem, int *status);
+// Several matrices sharing K and x (M <= 8) in one launch of the same kernel;
+// CTAs are split between them in proportion to their bytes (group_ctas).
+// cudaErrorNotSupported when one of them does not fit the kernel's plan.
+cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws, const int64_t *Ns, int64_t K,
+                                 const float *x, int M, float *const *ys, cudaStream_t st, int num_sms,
+                                 int max_smem, int *status);
+void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t *need, int num_sms, int *g);
 
 // Prefill GEMM on tcgen05 (gemm_tc.cu): Q4_K weights, fp16 activations
 // xh [M][K] (d*q from the quantiser).  Returns cudaErrorNotSupported for

@@ -72,6 +72,39 @@ def test_validation_rejects_before_launch():
     assert L.qmm_quantize_act(null, 1, 33, null, null, null, null) == q.QMM_EINVAL_SHAPE
 
 
+def test_group_validation_rejects_before_launch():
+    L = q.load()
+    null = ctypes.c_void_p(0)
+    I64 = ctypes.c_int64
+
+    def arrays(types, ns, ws=None, ys=None):
+        n = len(types)
+        return ((ctypes.c_int * n)(*types), (ctypes.c_void_p * n)(*(ws or [0] * n)),
+                (I64 * n)(*ns), (ctypes.c_void_p * n)(*(ys or [0] * n)))
+    t, w, n, y = arrays([q.Q4_K], [4])
+    assert L.qmm_group(0, t, w, n, 256, null, 1, y, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_group(9, t, w, n, 256, null, 1, y, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_group(1, null, w, n, 256, null, 1, y, null) == q.QMM_EINVAL_PTR
+    t, w, n, y = arrays([q.Q4_K, 7], [4, 4])
+    assert L.qmm_group(2, t, w, n, 256, null, 1, y, null) == q.QMM_EINVAL_TYPE
+    # K must suit every type of the group
+    t, w, n, y = arrays([q.Q8_0, q.Q6_K], [4, 4])
+    assert L.qmm_group(2, t, w, n, 96, null, 1, y, null) == q.QMM_EINVAL_SHAPE
+    # a null W or y on a non-empty entry, found before anything runs
+    buf = ctypes.create_string_buffer(4096)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    t, w, n, y = arrays([q.Q4_K, q.Q6_K], [4, 4], ws=[base, 0], ys=[base, base])
+    assert L.qmm_group(2, t, w, n, 256, ctypes.c_void_p(base), 1, y, null) == q.QMM_EINVAL_PTR
+    assert b"entry 1" in L.qmm_last_error()
+    # empty entries and M = 0 are no-ops without a launch
+    before = L.qmm_launch_count()
+    t, w, n, y = arrays([q.Q4_K, q.Q6_K], [0, 0])
+    assert L.qmm_group(2, t, w, n, 256, null, 1, y, null) == q.QMM_OK
+    t, w, n, y = arrays([q.Q4_K], [5])
+    assert L.qmm_group(1, t, w, n, 256, null, 0, y, null) == q.QMM_OK
+    assert L.qmm_launch_count() == before
+
+
 def test_empty_problems_are_noops():
     L = q.load()
     null = ctypes.c_void_p(0)

@@ -145,7 +145,7 @@ def plan_sb(qtype, M, K):
     return dict(NSW=nsw, slot=slot, ring=off, q_ld=q_ld, meta_ld=meta_ld)
 
 
-def check_sb(qtype, N, K, M=1):
+def check_sb(qtype, N, K, M=1, grid=None):
     BB, QK = synth.BLOCK_BYTES[qtype], synth.BLOCK_WEIGHTS[qtype]
     nb = K // QK
     RB = nb * BB
@@ -154,7 +154,7 @@ def check_sb(qtype, N, K, M=1):
     assert P is not None
     assert SB_NWARP * SB_MAXNSW * 8 + 2 * SB_NWARP * 4 + 2 * SB_NWARP * 8 * 4 <= SB_HEAD
     assert P["q_ld"] % 256 == 0 and P["meta_ld"] % 16 == 0
-    grid = min(SMS, N)
+    grid = min(SMS, N) if grid is None else grid
     covered = []
     read_end = {synth.Q8_0: 38, synth.Q4_K: 144, synth.Q6_K: 212}[qtype]
     q, r = divmod(N, grid)
@@ -239,3 +239,51 @@ def test_row_by_multiply_high_workloads():
 def test_row_by_multiply_high_refuses_large_products():
     # Q8_0 with K = 4M (nb = 131072) and thousands of rows per CTA: divide instead
     assert nb_magic(10000, 131072) == 0
+
+
+# ---- one launch for several matrices that share x (qmm_group) -------------
+def group_ctas(bytes_, rows, need, num_sms):
+    """Mirror of group_ctas in gemv_sb.cu: CTAs in proportion to the bytes
+    (largest remainders, at most one extra each), at least one per matrix and
+    at least `need`, at most one per row."""
+    total = sum(bytes_)
+    g, frac = [], []
+    for b, r, nd in zip(bytes_, rows, need):
+        want = num_sms * b / total if total else 1.0
+        gi = int(want)
+        frac.append(want - gi)
+        gi = min(max(gi, 1, nd), r)
+        g.append(gi)
+    used = sum(g)
+    while used < num_sms:
+        best = None
+        for i in range(len(g)):
+            if frac[i] >= 0 and g[i] < rows[i] and (best is None or frac[i] > frac[best]):
+                best = i
+        if best is None:
+            break
+        g[best] += 1
+        frac[best] = -1.0
+        used += 1
+    return g
+
+
+GROUPS = [
+    [(q, K, N) for (nm, q, K, N) in synth.QWEN3_14B_LAYER if nm in ("q", "k", "v")],
+    [(q, K, N) for (nm, q, K, N) in synth.QWEN3_14B_LAYER if nm in ("gate", "up")],
+    [(q, K, N) for (nm, q, K, N) in synth.LLAMA_1B if nm in ("q", "kv")],
+    [(synth.Q4_K, 1024, 5), (synth.Q6_K, 1024, 3000), (synth.Q8_0, 1024, 1)],
+]
+
+
+@pytest.mark.parametrize("group", GROUPS)
+def test_group_split_covers_every_matrix(group):
+    rbs = [(K // synth.BLOCK_WEIGHTS[q]) * synth.BLOCK_BYTES[q] for (q, K, N) in group]
+    bytes_ = [N * rb for (q, K, N), rb in zip(group, rbs)]
+    rows = [N for (q, K, N) in group]
+    need = [-(-N // ((1 << 30) // rb)) for (q, K, N), rb in zip(group, rbs)]
+    g = group_ctas(bytes_, rows, need, SMS)
+    assert all(1 <= gi <= N for gi, (q, K, N) in zip(g, group))
+    assert sum(g) <= SMS + len(group)
+    for (q, K, N), gi in zip(group, g):
+        check_sb(q, N, K, grid=gi)

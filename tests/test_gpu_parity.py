@@ -187,6 +187,29 @@ def test_qmm_prefill_in_cuda_graph_replays(cuda_lib):
     assert cuda_lib.qmm_device_status() == 0
 
 
+# qmm_group: several matrices reading one x, one decode launch for M <= 8
+QWEN_QKV = [(q, N) for (nm, q, K, N) in synth.QWEN3_14B_LAYER if nm in ("q", "k", "v")]
+QWEN_GATE_UP = [(q, N) for (nm, q, K, N) in synth.QWEN3_14B_LAYER if nm in ("gate", "up")]
+MIXED = [(synth.Q4_K, 5), (synth.Q6_K, 0), (synth.Q6_K, 3000), (synth.Q8_0, 1), (synth.Q4_K, 700)]
+
+
+@pytest.mark.parametrize("group,K,M", [(QWEN_QKV, 5120, 1), (QWEN_QKV, 5120, 4), (QWEN_GATE_UP, 5120, 1),
+                                       (MIXED, 1024, 2), (MIXED, 1024, 16)])
+def test_qmm_group_matches_oracle(cuda_lib, group, K, M):
+    Ws = [synth.weights(q, N, K, seed=100 + i) for i, (q, N) in enumerate(group)]
+    x = synth.activations(M, K, seed=200 + M)
+    before = cuda_lib.qmm_launch_count()
+    ys = cuda_lib.qmm_group([(q, _dev(W), N) for (q, N), W in zip(group, Ws)], K, _dev(x))
+    assert cuda_lib.qmm_device_status() == 0
+    if M <= 8:
+        assert cuda_lib.qmm_launch_count() - before == 1  # the whole group, one launch
+    for (q, N), W, y in zip(group, Ws, ys):
+        if N == 0:
+            continue
+        yo, A = O.qmm(q, W, N, K, x)
+        _assert_within_bound(y.cpu().numpy(), yo, A, f"group entry type {q} N={N} K={K} M={M}")
+
+
 def test_qmm_is_deterministic_and_overwrites_y(cuda_lib):
     import torch
     qtype, N, K = synth.Q6_K, 300, 5120
