@@ -14,9 +14,9 @@
 //   * Lane i computes block i of the stage with exact int32 dp4a dot products
 //     against the quantised activations in shared memory; the per-block
 //     scale handling (six-bit scales and mins, 16-weight groups) is amortised
-//     over 256 weights.  The activations are stored with their 16-byte chunks
-//     XOR-swizzled per super-block so lanes reading consecutive super-blocks
-//     hit distinct banks.
+//     over 256 weights.  The activations are stored at a pitch of 272 bytes
+//     per super-block so lanes reading consecutive super-blocks hit distinct
+//     banks.
 //   * A segmented shuffle scan sums the lanes of each row inside a stage;
 //     rows crossing stages carry in registers; rows cut by a warp boundary
 //     are parked in shared memory and added in warp order after a final CTA
@@ -35,6 +35,7 @@ constexpr int NTHREADS = NWARP * 32;
 constexpr int SU = 32;           // blocks per stage (one per lane)
 constexpr int HEAD_BYTES = 2048; // mbarriers and warp-edge records
 constexpr int MAX_NSW = 6;
+constexpr int XPITCH = 272;      // shared-memory bytes per super-block of activations
 
 struct SbParams {
     int type;             // qmm_type of W
@@ -51,7 +52,7 @@ struct SbParams {
     int rows_r;      // N % (CTAs of this matrix): the first rows_r CTAs take one row more
     const float *x;  // [M][K] activations, fp32
     int x_vec;       // x is 16-byte aligned: load four at a time
-    int q_ld;        // bytes per activation row of q (a multiple of 256)
+    int q_ld;        // bytes per activation row of q (super-blocks at XPITCH bytes)
     int meta_ld;     // bytes per activation row of scale records (Q8_0: of d)
     float *y;
     int off_edge, off_xq, off_meta, off_ring;
@@ -88,8 +89,10 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-// Shared-memory activations.  q: int8, 16-byte chunks swizzled per super-
-// block.  Per super-block kb of row m, a record at meta + m*meta_ld +
+// Shared-memory activations.  q: int8, super-block kb of row m at
+// m*q_ld + kb*XPITCH: the 16 spare bytes per super-block put the same chunk
+// of consecutive super-blocks (read by consecutive lanes) in distinct banks,
+// and every chunk is an immediate offset from the super-block's start.  Per super-block kb of row m, a record at meta + m*meta_ld +
 // kb*REC holds the eight block scales d (bytes 0..31) and, for Q4_K, the
 // eight products d*sum (32..63) or, for Q6_K, the sixteen half-block sums
 // (32..95); REC = 80 (Q4_K) or 112 (Q6_K) bytes, odd multiples of 16 so that
@@ -107,7 +110,7 @@ struct XS {
 
 // Shared-memory byte offset of 16-byte chunk c of super-block kb, row m.
 __device__ __forceinline__ int xchunk(const XS &X, int m, int kb, int c) {
-    return X.xq + m * X.q_ld + kb * 256 + ((c ^ (kb & 7)) << 4);
+    return X.xq + m * X.q_ld + kb * XPITCH + 16 * c;
 }
 
 // ---- Q4_K: w = d*sc*q - dmin*m over eight 32-weight sub-blocks ----------
@@ -351,16 +354,16 @@ __device__ __forceinline__ void quantize_tpb(const SbParams &P, uint8_t *smem, F
             // this thread's bytes: elements [EPT*part, EPT*part + EPT) of the block,
             // inside chunks 2*(b & 7) and 2*(b & 7) + 1 of super-block b >> 3
             const int sb = b >> 3;
-            uint8_t *row = smem + P.off_xq + m * P.q_ld + sb * 256;
+            uint8_t *row = smem + P.off_xq + m * P.q_ld + sb * XPITCH;
             if constexpr (EPT == 32) {
-                const int c0 = (2 * (b & 7)) ^ (sb & 7), c1 = (2 * (b & 7) + 1) ^ (sb & 7);
+                const int c0 = 2 * (b & 7), c1 = 2 * (b & 7) + 1;
                 *reinterpret_cast<uint4 *>(row + 16 * c0) = make_uint4(w[0], w[1], w[2], w[3]);
                 *reinterpret_cast<uint4 *>(row + 16 * c1) = make_uint4(w[4], w[5], w[6], w[7]);
             } else if constexpr (EPT == 16) {
-                const int c = (2 * (b & 7) + part) ^ (sb & 7);
+                const int c = 2 * (b & 7) + part;
                 *reinterpret_cast<uint4 *>(row + 16 * c) = make_uint4(w[0], w[1], w[2], w[3]);
             } else {
-                const int c = (2 * (b & 7) + (part >> 1)) ^ (sb & 7);
+                const int c = 2 * (b & 7) + (part >> 1);
                 *reinterpret_cast<uint2 *>(row + 16 * c + 8 * (part & 1)) = make_uint2(w[0], w[1]);
             }
             if (part == 0) {
@@ -427,9 +430,8 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
     const int64_t avail = P.total_bytes - (cta_byte & ~int64_t(15));
     const int ring = P.off_ring + warp * P.NSW * P.slot_bytes;
 
-    // issue stage t of this warp into slot t % NSW (lane 0 only)
-    auto issue = [&](int t, uint64_t pol) {
-        const int slot = t % P.NSW;
+    // issue stage t of this warp into `slot` (= t % NSW; lane 0 only)
+    auto issue = [&](int t, int slot, uint64_t pol) {
         const int u0 = uw0 + SU * t, u1 = min(u0 + SU, uw1);
         const int a = cta_off + u0 * BB, b = cta_off + u1 * BB;
         const int a16 = a & ~15;
@@ -455,7 +457,7 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
     quantize_to_smem<T>(P, smem, [&] {
         if (lane == 0) {
             pol_w = policy_evict_first();
-            for (; issued < min(P.NSW, nst); ++issued) issue(issued, pol_w);
+            for (; issued < min(P.NSW, nst); ++issued) issue(issued, issued, pol_w);
         }
     });
     __syncthreads();
@@ -473,9 +475,10 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) carry[m] = 0.0f;
     int consumed = 0;
+    int slot = 0, islot = min(P.NSW, nst) % P.NSW;  // ring slots of stage t and of the next issue
+    uint32_t phase = 0;                              // parity of stage t's slot
     for (int t = 0; t < nst && !failed; ++t) {
-        const int slot = t % P.NSW;
-        if (!mbar_wait(my_bar + 8u * slot, static_cast<uint32_t>((t / P.NSW) & 1), P.status)) {
+        if (!mbar_wait(my_bar + 8u * slot, phase, P.status)) {
             failed = true;
             break;
         }
@@ -503,8 +506,9 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
         if (lane == 0 && issued < nst) {
             // the slot just read is refilled: order the reads before the async write
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(issued, pol_w);
+            issue(issued, islot, pol_w);
             ++issued;
+            if (++islot == P.NSW) islot = 0;
         }
         // segmented suffix sums: lane i gets the sum of its row over lanes i..seg_last
         const int row_start = row * P.nb, row_end = row_start + P.nb;
@@ -523,7 +527,8 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
             for (int m = 0; m < MT; ++m) v[m] += carry[m];
         }
         // the stage's last row continues into this warp's next stage?
-        const int row_last = (u1 - 1) / P.nb;
+        const int row_last = P.nb_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(u1 - 1), P.nb_magic))
+                                         : (u1 - 1) / P.nb;
         const int head_last = max(0, row_last * P.nb - u0);
         const bool cont = (row_last + 1) * P.nb > u1 && u1 < uw1;
         if (head && !(cont && row == row_last)) {
@@ -541,6 +546,7 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
 #pragma unroll
         for (int m = 0; m < MT; ++m) carry[m] = __shfl_sync(0xffffffffu, v[m], head_last);
         carry_row = cont ? row_last : -1;
+        if (++slot == P.NSW) slot = 0, phase ^= 1u;
     }
     // no bulk copy may still be in flight when the CTA exits
     if (lane == 0)
@@ -611,7 +617,7 @@ int64_t align64(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 bool plan_sb(int type, int M, int64_t K, int max_smem, SbParams &P, int &smem) {
     const int MT = mt_of(M);
     const int BB = block_bytes(type);
-    const int64_t q_ld = align64(K, 256);
+    const int64_t q_ld = ((K + 255) / 256) * XPITCH;
     const int64_t meta_ld = type == QMM_Q8_0 ? align64((K / 32) * 4, 16)
                                              : (K / 256) * (type == QMM_Q4_K ? 80 : 112);
     int64_t off = HEAD_BYTES;

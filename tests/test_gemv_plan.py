@@ -127,13 +127,13 @@ def test_gemv_plan_fits_multi_slot(M):
 
 
 # ---- the block-per-lane decode kernel (gemv_sb.cu) --------------------------
-SB_NWARP, SB_SU, SB_HEAD, SB_MAXNSW = 12, 32, 2048, 6
+SB_NWARP, SB_SU, SB_HEAD, SB_MAXNSW, SB_XPITCH = 12, 32, 2048, 6, 272
 
 
 def plan_sb(qtype, M, K):
     MT = 1 if M <= 1 else 2 if M <= 2 else 4 if M <= 4 else 8
     BB = synth.BLOCK_BYTES[qtype]
-    q_ld = align(K, 256)
+    q_ld = -(-K // 256) * SB_XPITCH
     meta_ld = align((K // 32) * 4, 16) if qtype == synth.Q8_0 else (K // 256) * (80 if qtype == synth.Q4_K else 112)
     off = SB_HEAD
     off = align(off + MT * q_ld, 128)
@@ -153,7 +153,7 @@ def check_sb(qtype, N, K, M=1, grid=None):
     P = plan_sb(qtype, M, K)
     assert P is not None
     assert SB_NWARP * SB_MAXNSW * 8 + 2 * SB_NWARP * 4 + 2 * SB_NWARP * 8 * 4 <= SB_HEAD
-    assert P["q_ld"] % 256 == 0 and P["meta_ld"] % 16 == 0
+    assert P["q_ld"] % 16 == 0 and P["meta_ld"] % 16 == 0
     grid = min(SMS, N) if grid is None else grid
     covered = []
     read_end = {synth.Q8_0: 38, synth.Q4_K: 144, synth.Q6_K: 212}[qtype]
