@@ -446,11 +446,26 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
         if (nbytes) bulk_g2s(smem_u32(smem + dst), Wc + a16, nbytes, my_bar + 8u * slot, pol);
     };
 
-    // Wait for the preceding kernel (it may produce x), issue this thread's
-    // activation loads, and only then start the weight stream, so the loads
-    // do not return behind tens of KB of bulk copies into this SM.  The next
-    // kernel on the stream may start launching now.
+    // The next kernel on the stream may start launching now.  Until the
+    // preceding kernel completes (it may produce x) this CTA only warms L2:
+    // each warp's first stages of weights (which no kernel of the stream
+    // writes) and x (an L2 prefetch cannot leave a stale copy; x itself is
+    // read after the wait), so the weight stream of this call overlaps the
+    // tail of the last one.  After the wait: this thread's activation loads,
+    // and only then the weight stream into shared memory, so the loads do
+    // not return behind tens of KB of bulk copies into this SM.
     pdl_trigger();
+    if (lane == 0) {
+        for (int t = 0; t < min(P.NSW, nst); ++t) {
+            const int u0 = uw0 + SU * t, u1 = min(u0 + SU, uw1);
+            const int a16 = (cta_off + u0 * BB) & ~15;
+            int b16 = (cta_off + u1 * BB + 15) & ~15;
+            if (b16 > avail) b16 = (cta_off + u1 * BB) & ~15;
+            if (b16 > a16) bulk_prefetch_l2(Wc + a16, static_cast<uint32_t>(b16 - a16));
+        }
+    }
+    if (threadIdx.x == 32 && P.x_vec && ((P.M * P.K * 4) & 15) == 0)
+        bulk_prefetch_l2(P.x, static_cast<uint32_t>(P.M * P.K * 4));
     pdl_wait();
     uint64_t pol_w = 0;
     int issued = 0;
