@@ -397,7 +397,7 @@ def run_ours(args):
     del g_e2e, g_step
 
     detail = []
-    groups = layer = None
+    groups = layer = layer_m = None
     roof = None
     gemm = None
     cpu = None
@@ -456,6 +456,23 @@ def run_ours(args):
 
         groups = [rotating([c]) for c in make_calls(mats, STEP_CALLS) if len(c) > 1]
         layer = rotating(make_calls(mats, LAYER_CALLS))
+        layer["M"] = 1
+
+        # ---- the same layer with M = 2, 4, 8 activation rows (the decode of a
+        # few sequences at once): weight bytes per launch are unchanged
+        layer_m = []
+        saved = {m["name"]: (m["x"], m["y"]) for m in mats}
+        for Mb in (2, 4, 8):
+            for c in make_calls(mats, LAYER_CALLS):
+                xb = torch.from_numpy(synth.config_activations(c[0]["cfg"], Mb, c[0]["K"])).to(dev)
+                for m in c:
+                    m["x"] = xb
+                    m["y"] = torch.empty((Mb, m["N"]), dtype=torch.float32, device=dev)
+            r = rotating(make_calls(mats, LAYER_CALLS))
+            r["M"] = Mb
+            layer_m.append(r)
+        for m in mats:
+            m["x"], m["y"] = saved[m["name"]]
 
         # ---- prefill GEMM, M=512
         gemm = []
@@ -521,6 +538,7 @@ def run_ours(args):
                     "note": "weights resident (model state); x in and y out every call"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks, "per_matrix": detail, "groups": groups, "qwen3_14b_layer": layer,
+            "qwen3_14b_layer_M": layer_m,
             "prefill_gemm": gemm,
         }
         print(json.dumps(line))

@@ -61,6 +61,8 @@ def load():
     L.qmm_last_error.restype = ctypes.c_char_p
     L.qmm_device_status.argtypes = [P]
     L.qmm_launch_count.restype = I64
+    L.qmm_set_decode_path.argtypes = [I]
+    L.qmm_set_decode_path.restype = I
     for f in ("qmm_dequant", "qmm", "qmm_noalloc", "qmm_quantize_act", "qmm_device_status",
               "qmm_release", "qmm_group"):
         getattr(L, f).restype = I
@@ -185,3 +187,15 @@ def qmm_release() -> None:
 
 def qmm_launch_count() -> int:
     return int(load().qmm_launch_count())
+
+
+# Decode kernel choice (qmm_set_decode_path in the C header).
+DECODE_AUTO, DECODE_BLOCK, DECODE_TENSOR = 0, 1, 2
+
+
+def set_decode_path(path: int) -> int:
+    """Select the decode kernel for every later call; returns the previous path."""
+    rc = int(load().qmm_set_decode_path(int(path)))
+    if rc < 0:
+        raise QmmError(rc, load().qmm_last_error().decode())
+    return rc

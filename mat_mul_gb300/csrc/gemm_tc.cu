@@ -426,26 +426,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encoder() {
-    static EncodeTiled fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeTiled>(nullptr);
-        return reinterpret_cast<EncodeTiled>(p);
-    }();
-    return fn;
-}
-
 bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
     return type == QMM_Q4_K && K % 256 == 0 && K >= 256 && N >= 1 && M >= 1 && N <= (int64_t(1) << 30) &&
-           M <= (int64_t(1) << 30) && K <= (int64_t(1) << 24) && encoder() != nullptr;
+           M <= (int64_t(1) << 30) && K <= (int64_t(1) << 24) && tensor_map_encoder() != nullptr;
 }
 
 template <int BT>
@@ -516,12 +499,25 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
 
 }  // namespace
 
+EncodeTiled tensor_map_encoder() {
+    static EncodeTiled fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiled>(nullptr);
+        return reinterpret_cast<EncodeTiled>(p);
+    }();
+    return fn;
+}
+
 bool gemm_tc_supported(int type, int64_t N, int64_t K, int64_t M) { return tc_supported(type, N, K, M); }
 
 cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const void *xh, int64_t M, float *y,
                            cudaStream_t st, int num_sms, int *status) {
     if (!gemm_tc_supported(type, N, K, M)) return cudaErrorNotSupported;
-    EncodeTiled enc = encoder();
+    EncodeTiled enc = tensor_map_encoder();
     if (M <= 64) return launch_bt<64>(enc, W, N, K, xh, M, y, st, num_sms, status);
     if (M <= 128) return launch_bt<128>(enc, W, N, K, xh, M, y, st, num_sms, status);
     return launch_bt<256>(enc, W, N, K, xh, M, y, st, num_sms, status);

@@ -26,12 +26,18 @@ const bool g_force_mma_gemm = [] {
     return v && strcmp(v, "mma") == 0;
 }();
 // QMM_DECODE_KERNEL=rounds selects the round-based decode kernel wherever the
-// block-per-lane one would run (for comparisons; read once at load).
+// block-per-lane one would run; =sb keeps 2 <= M <= 8 on the block-per-lane
+// kernel instead of the tensor-core one (for comparisons; read once at load).
 const bool g_force_round_gemv = [] {
     const char *v = getenv("QMM_DECODE_KERNEL");
     return v && strcmp(v, "rounds") == 0;
 }();
+const bool g_no_mma_gemv = [] {
+    const char *v = getenv("QMM_DECODE_KERNEL");
+    return v && (strcmp(v, "sb") == 0 || strcmp(v, "rounds") == 0);
+}();
 std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_decode_path{QMM_DECODE_AUTO};
 
 int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int code, const char *fmt, ...) {
@@ -127,6 +133,17 @@ namespace qk {
 int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
 }  // namespace qk
 
+namespace {
+// The decode product of this type and M runs on the tensor-core kernel.
+bool decode_on_tensor_cores(int type, int64_t M, int64_t K, const DeviceInfo &di) {
+    if (M < 2 || M > 8 || g_force_round_gemv) return false;
+    const int path = g_decode_path.load();
+    if (path == QMM_DECODE_BLOCK) return false;
+    if (path == QMM_DECODE_AUTO && (M < QMM_TENSOR_MIN_M || g_no_mma_gemv)) return false;
+    return qk::gemv_mma_fits(type, static_cast<int>(M), K, di.max_smem);
+}
+}  // namespace
+
 extern "C" {
 
 const char *qmm_strerror(int status) {
@@ -145,6 +162,12 @@ const char *qmm_strerror(int status) {
 const char *qmm_last_error(void) { return g_err; }
 
 int64_t qmm_launch_count(void) { return g_launches.load(); }
+
+int qmm_set_decode_path(int path) {
+    if (path != QMM_DECODE_AUTO && path != QMM_DECODE_BLOCK && path != QMM_DECODE_TENSOR)
+        return fail(QMM_EINVAL_SHAPE, "unknown decode path %d", path);
+    return g_decode_path.exchange(path);
+}
 
 int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *out_f32) {
     g_err[0] = 0;
@@ -224,12 +247,33 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     DeviceInfo di;
     if (int rc = device_info(dev, di)) return rc;
 
-    // Three paths, chosen by M and by what fits in shared memory:
+    // Four paths, chosen by M and by what fits in shared memory:
+    //   mma  : decode, Q4_K with QMM_TENSOR_MIN_M <= M <= 8 (qmm_set_decode_path
+    //          widens or closes it): the quantiser (fp16 d*q into the
+    //          workspace), then sixteen weight rows per f16 mma.sync
     //   sb   : decode, one weight block per lane, quantises x itself (one
     //          launch, no workspace); M <= 8 when the activations fit
     //   gemv : decode, 32 units per round, after the quantiser kernel
     //   gemm : prefill after the quantiser: Q4_K on tcgen05 (fp16 operands,
     //          fp32 accumulators), other types on the int8 mma.sync kernel
+    if (decode_on_tensor_cores(type, M, K, di)) {
+        // the quantiser writes fp16 d*q in fragment order; the decode kernel
+        // (programmatic dependent launch) streams weights while it runs
+        void *ws = nullptr;
+        if (int rc = workspace(dev, st, align_up(static_cast<size_t>(M * (K + K / 16)) * 2, 256), &ws)) return rc;
+        qk::QuantOut o = {};
+        o.xh = ws;
+        o.xh_ld = K + K / 16;
+        o.xh_mma = 1;
+        e = qk::launch_quantize(x, M, K, o, st, true, di.num_sms, true);
+        if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+        g_launches.fetch_add(1);
+        e = qk::launch_gemv_mma(type, W_blocks, N, K, ws, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
+                                di.status);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core gemv launch");
+        g_launches.fetch_add(1);
+        return QMM_OK;
+    }
     if (M <= 8 && !g_force_round_gemv && qk::gemv_sb_fits(type, static_cast<int>(M), K, di.max_smem)) {
         e = qk::launch_gemv_sb(type, W_blocks, N, K, x, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
                                di.status);
@@ -323,9 +367,12 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
         DeviceInfo di;
         if (int rc = device_info(dev, di)) return rc;
+        // one launch when every entry takes the block-per-lane kernel (an
+        // entry for the tensor-core one makes them separate calls)
         bool fits = true;
         for (int i = 0; i < n; ++i)
-            fits = fits && (Ns[i] == 0 || qk::gemv_sb_fits(types[i], static_cast<int>(M), K, di.max_smem));
+            fits = fits && (Ns[i] == 0 || (qk::gemv_sb_fits(types[i], static_cast<int>(M), K, di.max_smem) &&
+                                           !decode_on_tensor_cores(types[i], M, K, di)));
         if (fits) {
             e = qk::launch_gemv_sb_group(n, types, Ws, Ns, K, x, static_cast<int>(M), ys,
                                          static_cast<cudaStream_t>(stream), di.num_sms, di.max_smem, di.status);

@@ -2,6 +2,7 @@
 // the quantiser's output description and every kernel launcher.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -16,7 +17,13 @@ namespace qk {
 //   s32 [M][d_ld]   int32 sum per block
 //   s16 [M][s16_ld] int32 sums of the two 16-element halves of every block
 //   dsf [M][d_ld]   fp32 product d * s32 per block
-//   xh  [M][xh_ld]  fp16 of the dequantised activation d * q (plain layout)
+//   xh  [M][xh_ld]  fp16 of the dequantised activation d * q: plain layout,
+//                   or with xh_mma != 0 the layout of the tensor-core decode
+//                   kernel (gemv_mma.cu): element l of block b at half
+//                   32b + ((l>>4)*2 + (l&1))*8 + ((l>>2)&3)*2 + ((l>>1)&1),
+//                   then after the K halves the block sums of the fp16
+//                   values as hi + lo, per super-block 8 hi then 8 lo
+//                   (xh_ld >= K + K/16)
 struct QuantOut {
     int8_t *q;
     int64_t q_ld;
@@ -28,10 +35,22 @@ struct QuantOut {
     int64_t d_ld, s16_ld;
     void *xh;  // __half
     int64_t xh_ld;
+    int xh_mma;
 };
 
+// trigger_dependents: let the next kernel (launched with programmatic
+// dependent launch) start once every CTA of this one is running; the trigger
+// comes after this kernel's own wait for its predecessor, so everything the
+// next kernel does before its wait sees all earlier kernels complete.
+// pdl_launch: launch this kernel itself with programmatic dependent launch.
 cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, const QuantOut &o, cudaStream_t st,
-                            bool trigger_dependents, int num_sms);
+                            bool trigger_dependents, int num_sms, bool pdl_launch = false);
+
+// cuTensorMapEncodeTiled from the driver (null when it cannot be found).
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled tensor_map_encoder();
 
 cudaError_t launch_dequant(int type, const void *blocks, int64_t n_elems, float *out,
                            cudaStream_t st, int num_sms);
@@ -55,6 +74,17 @@ cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws,
                                  const float *x, int M, float *const *ys, cudaStream_t st, int num_sms,
                                  int max_smem, int *status);
 void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t *need, int num_sms, int *g);
+
+// Decode for 2 <= M <= 8 on the tensor cores (gemv_mma.cu): Q4_K, sixteen
+// weight rows dequantised to fp16 per mma.sync.m16n8k16 (fp32 accumulation).
+// xh: the quantiser's fp16 output in fragment order (xh_mma), [M][K], 16-byte
+// aligned; the kernel copies it whole into shared memory (2*M*K bytes must
+// fit).  Launched with programmatic dependent launch right after that
+// quantiser (launched with trigger_dependents): the kernel streams weights
+// before it waits, and reads xh after.
+bool gemv_mma_fits(int type, int M, int64_t K, int max_smem);
+cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
+                            cudaStream_t st, int num_sms, int max_smem, int *status);
 
 // Prefill GEMM on tcgen05 (gemm_tc.cu): Q4_K weights, fp16 activations
 // xh [M][K] (d*q from the quantiser).  Returns cudaErrorNotSupported for

@@ -16,6 +16,8 @@ namespace qk {
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x, int64_t M,
                                                            int64_t K, QuantOut o,
                                                            int trigger_dependents) {
+    // a no-op unless launched with programmatic dependent launch
+    pdl_wait();
     if (trigger_dependents) pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t nb = K / 32;
@@ -42,8 +44,27 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
             pos = (sb << 8) + 16 * c + (k & 15);
         }
         if (o.q) o.q[m * o.q_ld + pos] = static_cast<int8_t>(qi);
-        if (o.xh)
-            static_cast<__half *>(o.xh)[m * o.xh_ld + k] = __float2half_rn(__fmul_rn(db, static_cast<float>(qi)));
+        if (o.xh) {
+            const __half hq = __float2half_rn(__fmul_rn(db, static_cast<float>(qi)));
+            __half *row = static_cast<__half *>(o.xh) + m * o.xh_ld;
+            if (!o.xh_mma) {
+                row[k] = hq;
+            } else {
+                // fragment order: element l of block b at 32b + ((l>>4)*2 + (l&1))*8
+                // + ((l>>2)&3)*2 + ((l>>1)&1); then the block sums of the fp16
+                // values, X = hi + lo, in two planes of 8 per super-block after K
+                row[32 * b + ((lane >> 4) * 2 + (lane & 1)) * 8 + ((lane >> 2) & 3) * 2 + ((lane >> 1) & 1)] = hq;
+                float xs = __half2float(hq);
+#pragma unroll
+                for (int o2 = 16; o2 >= 1; o2 >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, o2);
+                if (lane == 0) {
+                    const __half hi = __float2half_rn(xs);
+                    const __half lo = __float2half_rn(xs - __half2float(hi));
+                    row[K + (b >> 3) * 16 + (b & 7)] = hi;
+                    row[K + (b >> 3) * 16 + 8 + (b & 7)] = lo;
+                }
+            }
+        }
         int lo = 0;
         if (o.s16)
             lo = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(lane < 16 ? qi : 0)));
@@ -61,16 +82,28 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
 
 // Host launcher.  Grid: enough warps for every block, capped at a few waves.
 cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, const QuantOut &o, cudaStream_t st,
-                            bool trigger_dependents, int num_sms) {
+                            bool trigger_dependents, int num_sms, bool pdl_launch) {
     const int64_t nblk = M * (K / 32);
     const int threads = 256;
     int64_t grid = (nblk + 7) / 8;
     const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    quantize_act_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(x, M, K, o,
-                                                                        trigger_dependents ? 1 : 0);
-    return cudaGetLastError();
+    if (!pdl_launch) {
+        quantize_act_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(x, M, K, o,
+                                                                            trigger_dependents ? 1 : 0);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_act_kernel, x, M, K, o, trigger_dependents ? 1 : 0);
 }
 
 }  // namespace qk

@@ -120,3 +120,15 @@ def test_binding_refuses_host_tensors():
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError):
         q.qmm(q.Q4_K, torch.zeros(144, dtype=torch.uint8), 1, 256, torch.zeros(1, 256))
+
+
+def test_decode_path_setter_validates_and_returns_the_previous_path():
+    import mat_mul_gb300 as q
+    L = q.load()
+    assert L.qmm_set_decode_path(q.DECODE_BLOCK) == q.DECODE_AUTO
+    assert L.qmm_set_decode_path(q.DECODE_TENSOR) == q.DECODE_BLOCK
+    assert L.qmm_set_decode_path(7) == q.QMM_EINVAL_SHAPE
+    assert b"decode path" in L.qmm_last_error()
+    assert L.qmm_set_decode_path(q.DECODE_AUTO) == q.DECODE_TENSOR
+    with pytest.raises(q.QmmError):
+        q.set_decode_path(-1)

@@ -116,6 +116,58 @@ def test_qmm_decode_small(cuda_lib, qtype, N, K, M):
     _assert_within_bound(y, yo, A, f"type {qtype} N={N} K={K} M={M}")
 
 
+# Q4_K decode on the tensor-core kernel (the default path from M = 4 on,
+# forced here for every M): groups of sixteen rows split between warps and
+# CTAs (N=16 over two CTAs holding 8 rows each), ragged N and a K whose
+# super-blocks do not fill the last stage chunk, every M from 2 to 8.
+MMA_DECODE = [(16, 8192, 2), (16, 8192, 3), (1000, 4352, 5), (77, 256, 8), (2048, 2048, 4),
+              (300, 5120, 6), (9, 1024, 7), (4096, 4096, 8), (5120, 17408, 4)]
+
+
+@pytest.fixture
+def decode_path(cuda_lib):
+    def set_path(p):
+        cuda_lib.set_decode_path(p)
+    yield set_path
+    cuda_lib.set_decode_path(cuda_lib.DECODE_AUTO)
+
+
+@pytest.mark.parametrize("N,K,M", MMA_DECODE)
+def test_qmm_decode_tensor_core(cuda_lib, decode_path, N, K, M):
+    decode_path(cuda_lib.DECODE_TENSOR)
+    W = synth.weights(synth.Q4_K, N, K, seed=N + K + 3 * M)
+    x = synth.activations(M, K, seed=N * K + 5 * M, outlier_frac=0.01)
+    before = cuda_lib.qmm_launch_count()
+    y = _run_qmm(cuda_lib, synth.Q4_K, W, N, K, x)
+    assert cuda_lib.qmm_launch_count() - before == 2  # the quantiser, then the tensor-core kernel
+    yo, A = O.qmm(synth.Q4_K, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"tensor-core decode N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_qmm_decode_block_path_on_request(cuda_lib, decode_path, M):
+    decode_path(cuda_lib.DECODE_BLOCK)
+    N, K = 300, 5120
+    W = synth.weights(synth.Q4_K, N, K, seed=31 + M)
+    x = synth.activations(M, K, seed=32 + M, outlier_frac=0.01)
+    before = cuda_lib.qmm_launch_count()
+    y = _run_qmm(cuda_lib, synth.Q4_K, W, N, K, x)
+    assert cuda_lib.qmm_launch_count() - before == 1
+    yo, A = O.qmm(synth.Q4_K, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"block-per-lane decode N={N} K={K} M={M}")
+
+
+def test_qmm_decode_tensor_core_is_deterministic(cuda_lib, decode_path):
+    import torch
+    decode_path(cuda_lib.DECODE_TENSOR)
+    N, K, M = 300, 5120, 8
+    W = _dev(synth.weights(synth.Q4_K, N, K, seed=21))
+    x = _dev(synth.activations(M, K, seed=22))
+    y1 = cuda_lib.qmm(synth.Q4_K, W, N, K, x)
+    for _ in range(3):
+        assert torch.equal(y1, cuda_lib.qmm(synth.Q4_K, W, N, K, x))
+
+
 GEMM_SMALL = [
     (synth.Q4_K, 70, 512, 9), (synth.Q4_K, 130, 768, 64), (synth.Q4_K, 64, 256, 100),
     (synth.Q6_K, 70, 512, 9), (synth.Q6_K, 129, 1024, 65), (synth.Q8_0, 70, 544, 33),
@@ -201,7 +253,7 @@ def test_qmm_group_matches_oracle(cuda_lib, group, K, M):
     before = cuda_lib.qmm_launch_count()
     ys = cuda_lib.qmm_group([(q, _dev(W), N) for (q, N), W in zip(group, Ws)], K, _dev(x))
     assert cuda_lib.qmm_device_status() == 0
-    if M <= 8:
+    if M == 1:
         assert cuda_lib.qmm_launch_count() - before == 1  # the whole group, one launch
     for (q, N), W, y in zip(group, Ws, ys):
         if N == 0:
