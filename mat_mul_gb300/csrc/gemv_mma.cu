@@ -1,64 +1,80 @@
 // gemv_mma.cu -- decode product y[M,N] = W[N,K] . x[M,K]^T for 2 <= M <= 8
-// activation rows and Q4_K weights, on the tensor cores (mma.sync with fp16
-// operands and fp32 accumulation).
+// activation rows and Q4_K or Q6_K weights, on the tensor cores (mma.sync
+// with fp16 operands and fp32 accumulation).
 //
 // The block-per-lane decode kernel (gemv_sb.cu) gives every lane its own
 // weight block and its own slice of x, so each extra activation row adds a
 // full pass of dp4a work and of activation reads from shared memory; from
 // M = 2 on it is bound by those reads, not by the weight stream.  Here
-// sixteen weight rows are one operand of mma.m16n8k16, and the product is
-// taken per Q4_K sub-block j (32 weights with one six-bit scale sc_j and
-// min m_j):
-//   y[t][r] = sum_j d*sc_j * sum_{k in j} q_k x_k  -  sum_j dmin*m_j * X_j,
-// X_j = sum_{k in j} x_k, x = d_x*q_x the quantised activations in fp16.
-//   * The quant sums: two MMAs per sub-block, A = the sixteen rows' nibbles
-//     q as fp16 subnormals q * 2^-24 (exact; one LOP3 per pair of weights,
-//     no offset to remove), B = x (tokens in columns, columns M..7 zero).
-//     Their fp32 result is scaled by d*sc_j * 2^24 (exact in fp32) into the
-//     row's accumulators.  High nibbles are read in place as 16q * 2^-24, so
-//     their scale carries 2^20.
-//   * The min term: one MMA per super-block, A = -dmin*m_j in fp16 (rows x
-//     sub-blocks), B = X_j in two fp16 parts hi + lo (sub-blocks x tokens),
-//     so X_j enters with about 22 bits.
-// Rounding: x to fp16 (as the prefill kernel) and dmin*m_j to fp16; the
-// scale d*sc_j is exact and every sum is fp32.  The int8 form of the
+// sixteen weight rows are the A operand of mma.m16n8k16 and the tokens the B
+// operand (columns M..7 zero), and no weight is dequantised: the quants go
+// into the MMA exactly, as fp16 subnormals v * 2^-24, and each MMA covers one
+// scale group, so its fp32 result is scaled once by the group's exact fp32
+// scale.  x = d_x*q_x are the quantised activations rounded to fp16.
+//   Q4_K (sub-blocks j of 32, scale sc_j, min m_j):
+//     y = sum_j d*sc_j * sum_{k in j} q_k x_k  -  sum_j dmin*m_j * X_j
+//     two MMAs per sub-block (A = nibbles, one LOP3 per pair; high nibbles
+//     read in place as 16q, the 16 folded into the scale); the min term is
+//     one MMA per super-block, A = -dmin*m_j (fp16), B = X_j = sum_{k in j}
+//     x_k as fp16 hi + lo (about 22 bits).
+//   Q6_K (groups G of 16, int8 scale sc_G, q = 6 bits, offset 32):
+//     y = sum_G d*sc_G * (sum_{k in G} q_k x_k  -  32 * X_G)
+//     one MMA per group; A = the six-bit values assembled from the 4-bit and
+//     2-bit fields in place (two LOP3 and one IMAD per pair; groups 8..15 of
+//     a half read the high nibbles as 16x); X_G = the fp32 sum of the group's
+//     fp16 x, subtracted in fp32 before the scaling.
+// Rounding: x to fp16 (as the Q4_K prefill kernel) and, for Q4_K, dmin*m_j
+// to fp16; every scale is exact and every sum fp32.  The int8 form of the
 // instruction runs at about 158 TOPS on this part, a quarter of the f16
 // rate, too slow for the weight stream once the dots are scaled.
 //
 // k order inside one MMA.  The sum over the 16 k slots does not depend on
 // which k each slot holds, as long as A and B agree.  Lane (g, t) supplies
-// slots 2t, 2t+1, 2t+8, 2t+9.  For the MMA of half e of sub-block
-// j = 2c + h they hold weights l = 16e + 4t + (0, 2 | 1, 3) of the
-// sub-block: the nibbles h of the four bytes at 32c + 16e + 4t, in the order
-// (byte 0, byte 2 | byte 1, byte 3) that one LOP3 per fp16 pair produces
-// (bytes 1 and 3 after one shift).  ldmatrix delivers exactly that word to
-// lane (g, t) from 8 rows of 16 bytes; the quantiser stores x so that
+// slots 2t, 2t+1, 2t+8, 2t+9; for the 16 weights l0..l0+15 of an MMA they
+// hold l0 + 4t + (0, 2 | 1, 3): the four bytes of one 32-bit quant word in
+// the order (byte 0, byte 2 | byte 1, byte 3) that one LOP3 per fp16 pair
+// produces (bytes 1 and 3 after one shift).  ldmatrix delivers exactly that
+// word of 8 rows of 16 bytes to lane (g, t); the quantiser stores x so that
 // ldmatrix delivers the matching B registers (see quantize.cu, xh_mma).
 //
 // Streaming.  Rows are taken in groups of 16.  CTA c (one per SM) owns a
 // range of 8-row halves, balanced to within one half, i.e. whole groups plus
 // at most one half group; its (group, chunk of CH super-blocks) units are
 // split evenly between eight warps.  Each warp streams its units through a
-// private ring: a stage is one chunk of the group's rows, brought in by one
-// or two 2-D tensor copies of 8 rows x CH super-blocks (rows past N and
-// bytes past the row end arrive as zeros).  The rows land densely, 144*CH
-// bytes apart; CH is odd (5, 3 or 1), so the eight rows of an ldmatrix are
-// eight distinct 16-byte bank groups.  A group whose units are split between
-// warps leaves partial sums in shared memory that are added in warp order at
-// the end; every y element is written once (deterministic).
+// private ring.
+//   Q4_K: a stage is one or two 2-D tensor copies of 8 rows x CH super-blocks
+//     (rows past N and bytes past the row end arrive as zeros); the rows land
+//     densely 144*CH bytes apart, CH odd (5, 3 or 1), so the eight rows of an
+//     ldmatrix are eight distinct 16-byte bank groups.
+//   Q6_K: rows are 210-byte multiples, not 16-byte ones, so each row segment
+//     is one bulk copy of its span rounded out to 16 bytes (the matrix's last
+//     bytes excepted: they are loaded after the wait instead of reading past
+//     the end), read from its offset inside the copy.  With CH even (4 or 2)
+//     and an even number of super-blocks per row, a chunk's even super-blocks
+//     are 4-byte aligned and its odd ones 2-byte aligned (their words are
+//     loaded in two aligned halves and shifted together).
+// When the activations of all of K do not fit in shared memory beside the
+// rings, K is taken in P phases: the activations of one K window at a time,
+// every warp's units of that window, then the next; a group's phase results
+// are added in phase order in a shared table.  A group whose units are split
+// between warps leaves partial sums in shared memory that are added in warp
+// order; every y element is written once (deterministic).
 //
 // Activations.  The activation quantiser runs just before this kernel and
-// writes x (fp16, fragment order) and the block sums (hi, lo) per token row;
-// this kernel copies all of it into shared memory with one bulk copy per
-// token row.  It is launched with programmatic dependent launch and the
-// quantiser triggers it only after its own wait for the kernels before it,
-// so the first weight stages are issued before this kernel waits (every
-// kernel that could write the weights has completed by then) and the
-// activations are read after.  All waits are bounded.
+// writes x (fp16, fragment order), the Q4_K block sums (hi, lo) per token
+// row and the Q6_K group sums ([K/16][8 tokens], zeros for tokens >= M); this
+// kernel copies each K window into shared memory with bulk copies.  It is
+// launched with programmatic dependent launch and the quantiser triggers it
+// only after its own wait for the kernels before it, so the first weight
+// stages are issued before this kernel waits (every kernel that could write
+// the weights has completed by then) and the activations are read after.
+// All waits are bounded.
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 namespace qk {
 
@@ -68,35 +84,71 @@ constexpr int FW = 8;  // warps
 constexpr int FTHREADS = FW * 32;
 constexpr int GR = 16;            // weight rows per group (the MMA's m)
 constexpr int MAX_NS = 4;         // stages per warp ring
+constexpr int MAX_PHASES = 8;
 constexpr int EDGE_FLOATS = 128;  // a partial group: 16 rows x 8 tokens
 // shared-memory head: stage barriers | activation barrier | edge groups |
-// zeros (the B rows of tokens M..7) | edge sums.  The activation rows start
-// on a 128-byte boundary and are 16 bytes past a 128-byte multiple apart, so
-// token m's 16-byte ldmatrix rows sit in bank group m (+ a common offset);
-// the zero rows sit in bank group 7, which no token uses while M < 8.
+// failure flag | zeros (the B rows of tokens M..7) | edge sums.  The
+// activation rows start on a 128-byte boundary and are 16 bytes past a
+// 128-byte multiple apart, so token m's 16-byte ldmatrix rows sit in bank
+// group m (+ a common offset); the zero rows sit in bank group 7, which no
+// token uses while M < 8.
 constexpr int OFF_XBAR = 8 * FW * MAX_NS;
 constexpr int OFF_EDGE_GROUP = OFF_XBAR + 16;
+constexpr int OFF_FAIL = OFF_EDGE_GROUP + 2 * FW * 4;
 constexpr int OFF_ZERO = 624;
 constexpr int ZERO_BYTES = 512;
 constexpr int OFF_EDGE_SUM = 1152;
 constexpr int HEAD = OFF_EDGE_SUM + 2 * FW * EDGE_FLOATS * 4;
-static_assert(OFF_EDGE_GROUP + 2 * FW * 4 <= OFF_ZERO && OFF_ZERO + ZERO_BYTES <= OFF_EDGE_SUM, "head layout");
+static_assert(OFF_FAIL + 16 <= OFF_ZERO && OFF_ZERO + ZERO_BYTES <= OFF_EDGE_SUM, "head layout");
 static_assert(OFF_ZERO % 128 == 112 && HEAD % 128 == 0, "zero rows in bank group 7");
-constexpr int SB_WORDS = 144 / 8;  // a super-block in the tensor map's 8-byte elements
+constexpr int SB_WORDS = 144 / 8;  // a Q4_K super-block in the tensor map's 8-byte elements
+
+// f(integral_constant<int, I>) for I = B .. E-1: the loop index is a
+// compile-time constant in the body (register arrays, masks, shuffle sources)
+template <int B, int E, class F>
+__device__ __forceinline__ void static_for(F &&f) {
+    if constexpr (B < E) {
+        f(std::integral_constant<int, B>{});
+        static_for<B + 1, E>(f);
+    }
+}
+
+template <int T>
+struct Mm;
+template <>
+struct Mm<QMM_Q4_K> {
+    static constexpr int BB = 144;
+    static constexpr int NCH = 3;
+    static constexpr int CHS[3] = {5, 3, 1};
+    static constexpr int XS_TOKEN = 32;  // per super-block per token: block sums hi | lo
+};
+template <>
+struct Mm<QMM_Q6_K> {
+    static constexpr int BB = 210;
+    static constexpr int NCH = 2;
+    static constexpr int CHS[2] = {4, 2};
+    static constexpr int XS_TOKEN = 0;   // the group sums are one array for all tokens
+};
 
 struct MmParams {
+    const uint8_t *W;   // the blocks (Q6_K: per-row bulk copies)
+    uint64_t w_end;     // first byte past the matrix
     int64_t N;
     int K, M;
-    int nb;            // super-blocks per row
-    int64_t halves_q;  // 8-row halves per CTA: halves / gridDim.x
-    int halves_r;      // halves % gridDim.x: the first halves_r CTAs take one more
-    const uint8_t *xh; // quantiser output [M][2K + K/8 bytes]: x fp16 | block sums
-    int x_ld;          // bytes per token row in shared memory (= 16 mod 128)
+    int nb;             // super-blocks per row
+    int64_t RB;         // bytes per row
+    int64_t halves_q;   // 8-row halves per CTA: halves / gridDim.x
+    int halves_r;       // halves % gridDim.x: the first halves_r CTAs take one more
+    const uint8_t *xh;  // quantiser output [M][2K + K/8 bytes]: x fp16 | Q4_K block sums
+    const uint8_t *xs16;  // Q6_K group sums [K/16][8] fp32
+    int nphase;         // K phases
+    int nbp;            // super-blocks per phase (a multiple of CH when nphase > 1)
+    int x_ld;           // bytes per token row of the activation window (= 16 mod 128)
     float *y;
     int NS, slot_bytes;
-    int CH;            // super-blocks per row per stage (5, 3 or 1)
-    int row_pitch;     // stage bytes per row, 144 * CH
-    int off_x, off_ring;
+    int CH;             // super-blocks per row per stage
+    int row_pitch;      // stage bytes per row
+    int off_x, off_xs, off_table, off_ring;
     int *status;
 };
 
@@ -141,6 +193,15 @@ __device__ __forceinline__ void mma_new(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 
+// A 32-bit word of shared memory at a 4-byte (ODD false) or 2-byte (ODD
+// true: two aligned loads shifted together) aligned address.
+template <bool ODD>
+__device__ __forceinline__ uint32_t word_at(const uint8_t *p) {
+    if (!ODD) return *reinterpret_cast<const uint32_t *>(p);
+    const uint32_t *a = reinterpret_cast<const uint32_t *>(p - 2);
+    return __funnelshift_r(a[0], a[1], 16);
+}
+
 // Scales of this lane's sub-blocks 2t (low nibbles) and 2t+1 (high nibbles)
 // from a Q4_K header (d, dmin, GGUF six-bit packing): s0, s1 = d*sc * 2^24
 // and d*sc * 2^20 in fp32 (exact), m01 = (-dmin*m_2t, -dmin*m_2t+1) in fp16.
@@ -162,11 +223,147 @@ __device__ __forceinline__ void q4k_lane_scales(uint4 h, int t, float &s0, float
     m01 = *reinterpret_cast<const uint32_t *>(&m);
 }
 
+// One Q4_K super-block of the 16 rows: ra_sb = this lane's ldmatrix address
+// of the weight words, hdr_a / hdr_b = the headers of rows g and g+8,
+// x_sb = the lane's ldmatrix address of the activations, xs_sb = of the
+// block sums.
+__device__ __forceinline__ void q4k_superblock(uint32_t a_sb, const uint8_t *hdr_a, const uint8_t *hdr_b,
+                                               uint32_t x_sb, uint32_t xs_sb, int t, int quad, float (&c)[4],
+                                               float (&c2)[4]) {
+    float sa0, sa1, sb0, sb1;
+    uint32_t ma, mb;
+    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_a), t, sa0, sa1, ma);
+    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_b), t, sb0, sb1, mb);
+    // the min term: k slots 2t, 2t+1 = sub-blocks 2t, 2t+1 (sums hi), slots
+    // 2t+8, 2t+9 = the same sub-blocks (sums lo)
+    {
+        uint32_t xhi, xlo;
+        ldsm_x2(xs_sb, xhi, xlo);
+        mma_acc(c2, ma, mb, ma, mb, xhi, xlo);
+    }
+    static_for<0, 4>([&](auto cc_) {  // quant bytes 32cc..32cc+31: sub-blocks 2cc, 2cc+1
+        constexpr int cc = decltype(cc_)::value;
+        uint32_t wa0, wb0, wa1, wb1;  // rows g | g+8, halves e = 0 | 1
+        ldsm_x4(a_sb + 32 * cc, wa0, wb0, wa1, wb1);
+        const uint32_t wa0s = wa0 >> 8, wb0s = wb0 >> 8, wa1s = wa1 >> 8, wb1s = wb1 >> 8;
+        // scales of sub-blocks 2cc, 2cc+1 from the quad's lane cc
+        const float s_a0 = __shfl_sync(0xffffffffu, sa0, quad | cc);
+        const float s_a1 = __shfl_sync(0xffffffffu, sa1, quad | cc);
+        const float s_b0 = __shfl_sync(0xffffffffu, sb0, quad | cc);
+        const float s_b1 = __shfl_sync(0xffffffffu, sb1, quad | cc);
+        static_for<0, 2>([&](auto h_) {  // sub-block 2cc + h: low or high nibbles
+            constexpr int h = decltype(h_)::value;
+            constexpr uint32_t mk = h ? 0x00F000F0u : 0x000F000Fu;
+            uint32_t x0, x1, x2, x3;
+            ldsm_x4(x_sb + 64 * (2 * cc + h), x0, x1, x2, x3);
+            float d[4];
+            mma_new(d, wa0 & mk, wb0 & mk, wa0s & mk, wb0s & mk, x0, x1);
+            mma_acc(d, wa1 & mk, wb1 & mk, wa1s & mk, wb1s & mk, x2, x3);
+            float(&acc)[4] = h ? c2 : c;
+            const float sa = h ? s_a1 : s_a0, sb = h ? s_b1 : s_b0;
+            acc[0] = fmaf(sa, d[0], acc[0]);
+            acc[1] = fmaf(sa, d[1], acc[1]);
+            acc[2] = fmaf(sb, d[2], acc[2]);
+            acc[3] = fmaf(sb, d[3], acc[3]);
+        });
+    });
+}
+
+// One Q6_K super-block of the 16 rows: ra / rb = its bytes for rows g and
+// g+8 (2-byte aligned when ODD), x_sb = the lane's ldmatrix address of the
+// activations, xs_sb = the group sums [16][8 tokens].
+template <bool ODD>
+__device__ __forceinline__ void q6k_superblock(const uint8_t *ra, const uint8_t *rb, uint32_t x_sb,
+                                               const float *xs_sb, int t, int quad, float (&c)[4], float (&c2)[4]) {
+    // scales of groups 4t..4t+3 for rows g and g+8: d*sc * 2^24 / f, f = 16
+    // for the groups read from high nibbles (groups 4..7 and 12..15: t odd)
+    const float fs = (t & 1) ? 1048576.0f : 16777216.0f;
+    const float da = __half2float(*reinterpret_cast<const __half *>(ra + 208)) * fs;
+    const float db = __half2float(*reinterpret_cast<const __half *>(rb + 208)) * fs;
+    const uint32_t sca = word_at<ODD>(ra + 192 + 4 * t), scb = word_at<ODD>(rb + 192 + 4 * t);
+    float Sa[4], Sb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        Sa[i] = da * static_cast<float>(static_cast<int8_t>(sca >> (8 * i)));
+        Sb[i] = db * static_cast<float>(static_cast<int8_t>(scb >> (8 * i)));
+    }
+    static_for<0, 2>([&](auto n_) {  // weights 128n .. 128n+127
+        constexpr int n = decltype(n_)::value;
+        // quant words of this lane for l = 16lh + 4t .. +3: low fields (q1,
+        // q3: ql bytes 64n + l), (q2, q4: 64n + 32 + l), high fields 128 + 32n + l
+        uint32_t la[2][2], lb[2][2], ha[2], hb[2];
+        static_for<0, 2>([&](auto lh_) {
+            constexpr int lh = decltype(lh_)::value;
+            la[lh][0] = word_at<ODD>(ra + 64 * n + 16 * lh + 4 * t);
+            la[lh][1] = word_at<ODD>(ra + 64 * n + 32 + 16 * lh + 4 * t);
+            lb[lh][0] = word_at<ODD>(rb + 64 * n + 16 * lh + 4 * t);
+            lb[lh][1] = word_at<ODD>(rb + 64 * n + 32 + 16 * lh + 4 * t);
+            ha[lh] = word_at<ODD>(ra + 128 + 32 * n + 16 * lh + 4 * t);
+            hb[lh] = word_at<ODD>(rb + 128 + 32 * n + 16 * lh + 4 * t);
+        });
+        static_for<0, 4>([&](auto qi_) {  // weights 128n + 32qi + l
+            constexpr int qi = decltype(qi_)::value;
+            uint32_t x0, x1, x2, x3;  // the 32-block 4n + qi: halves lh = 0 | 1
+            ldsm_x4(x_sb + 64 * (4 * n + qi), x0, x1, x2, x3);
+            constexpr uint32_t mlo = qi >= 2 ? 0x00F000F0u : 0x000F000Fu;
+            constexpr uint32_t mhi = 0x00030003u << (2 * qi);
+            constexpr uint32_t mul = (qi & 1) ? 4u : 16u;
+            // 32 * f * 2^-24: the offset 32 in the units of the MMA result
+            constexpr float kf = qi >= 2 ? 3.0517578125e-05f : 1.9073486328125e-06f;
+            static_for<0, 2>([&](auto lh_) {
+                constexpr int lh = decltype(lh_)::value;
+                constexpr int G = 8 * n + 2 * qi + lh;
+                const uint32_t qla = la[lh][qi & 1], qlb = lb[lh][qi & 1];
+                const uint32_t a0 = (ha[lh] & mhi) * mul + (qla & mlo);
+                const uint32_t a1 = (hb[lh] & mhi) * mul + (qlb & mlo);
+                const uint32_t a2 = ((ha[lh] >> 8) & mhi) * mul + ((qla >> 8) & mlo);
+                const uint32_t a3 = ((hb[lh] >> 8) & mhi) * mul + ((qlb >> 8) & mlo);
+                float d[4];
+                mma_new(d, a0, a1, a2, a3, lh ? x2 : x0, lh ? x3 : x1);
+                // minus 32 * the group sums of tokens 2t, 2t+1
+                const float2 X = *reinterpret_cast<const float2 *>(xs_sb + G * 8 + 2 * t);
+                d[0] = fmaf(-kf, X.x, d[0]);
+                d[1] = fmaf(-kf, X.y, d[1]);
+                d[2] = fmaf(-kf, X.x, d[2]);
+                d[3] = fmaf(-kf, X.y, d[3]);
+                const float sa = __shfl_sync(0xffffffffu, Sa[G & 3], quad | (G >> 2));
+                const float sb = __shfl_sync(0xffffffffu, Sb[G & 3], quad | (G >> 2));
+                float(&acc)[4] = lh ? c2 : c;
+                acc[0] = fmaf(sa, d[0], acc[0]);
+                acc[1] = fmaf(sa, d[1], acc[1]);
+                acc[2] = fmaf(sb, d[2], acc[2]);
+                acc[3] = fmaf(sb, d[3], acc[3]);
+            });
+        });
+    });
+}
+
+// This warp's units of phase p: [begin, end) of the phase's ng * nq units.
+struct PhaseUnits {
+    int begin, end;
+    int nq;   // chunks per row in the phase
+    int sb;   // first super-block of the phase
+    int nsb;  // super-blocks of the phase
+};
+
+__device__ __forceinline__ PhaseUnits phase_units(const MmParams &P, int p, int ng, int warp) {
+    PhaseUnits r;
+    r.sb = p * P.nbp;
+    r.nsb = min(P.nbp, P.nb - r.sb);
+    r.nq = (r.nsb + P.CH - 1) / P.CH;
+    const int U = ng * r.nq;
+    r.begin = static_cast<int>((static_cast<int64_t>(U) * warp) / FW);
+    r.end = static_cast<int>((static_cast<int64_t>(U) * (warp + 1)) / FW);
+    return r;
+}
+
+template <int T>
 __global__ void __launch_bounds__(FTHREADS, 1)
-    gemv_mma_q4k_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ MmParams P) {
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ MmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
+    const int quad = lane & ~3;
 
     // this CTA's rows [r0, r1): whole 8-row halves; groups of 16 from r0
     const int cta = blockIdx.x;
@@ -175,306 +372,422 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     const int64_t r0 = 8 * h0;
     const int64_t r1 = min(P.N, 8 * (h0 + nh));
     const int ng = (nh + 1) / 2;
-    const int nq = (P.nb + P.CH - 1) / P.CH;
-    const int U = ng * nq;
-    const int uw0 = static_cast<int>((static_cast<int64_t>(U) * warp) / FW);
-    const int uw1 = static_cast<int>((static_cast<int64_t>(U) * (warp + 1)) / FW);
-    const int nst = uw1 - uw0;
 
     const uint32_t my_bar = smem_u32(smem) + 8u * warp * MAX_NS;
     const uint32_t xbar = smem_u32(smem + OFF_XBAR);
     int *edge_group = reinterpret_cast<int *>(smem + OFF_EDGE_GROUP);
+    volatile int *fail_flag = reinterpret_cast<volatile int *>(smem + OFF_FAIL);
     float *edge_sum = reinterpret_cast<float *>(smem + OFF_EDGE_SUM);
+    float *table = reinterpret_cast<float *>(smem + P.off_table);
     if (lane == 0) {
         for (int i = 0; i < P.NS; ++i) mbar_init(my_bar + 8u * i, 1);
         if (warp == 0) mbar_init(xbar, 1);
         fence_mbar_init();
     }
     if (lane < 2) edge_group[2 * warp + lane] = -1;
+    if (threadIdx.x == 0) *fail_flag = 0;
     if (threadIdx.x < ZERO_BYTES / 16)
         reinterpret_cast<uint4 *>(smem + OFF_ZERO)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+    if (P.nphase > 1)
+        for (int i = threadIdx.x; i < ng * EDGE_FLOATS; i += FTHREADS) table[i] = 0.0f;
     __syncthreads();
 
     const int ring = P.off_ring + warp * P.NS * P.slot_bytes;
     const uint64_t pol_w = policy_evict_first();
-    // unit u (group, chunk) into `slot`: rows 0..7 of the group, and 8..15
-    // when the CTA owns them (a CTA's rows end on a half or at N)
-    auto issue = [&](int u, int slot) {
-        if (lane != 0) return;
-        const int gi = u / nq, qi = u - gi * nq;
+    auto group_rows = [&](int gi) {
+        const int64_t left = r1 - (r0 + GR * gi);
+        return left < GR ? static_cast<int>(left) : GR;
+    };
+    // unit u of phase r into `slot`
+    auto issue = [&](const PhaseUnits &r, int u, int slot) {
+        const int gi = u / r.nq, qi = u - gi * r.nq;
+        const int sb0 = r.sb + qi * P.CH, nsb = min(P.CH, r.sb + r.nsb - sb0);
         const int64_t row0 = r0 + GR * gi;
-        const int boxes = r1 - row0 > 8 ? 2 : 1;
         const uint32_t bar = my_bar + 8u * slot;
         const uint32_t dst = smem_u32(smem + ring + slot * P.slot_bytes);
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(boxes * 8 * P.row_pitch));
-        for (int bx = 0; bx < boxes; ++bx)
-            tma_load_2d_hint(dst + bx * 8 * P.row_pitch, &tmW, qi * P.CH * SB_WORDS, static_cast<int>(row0 + 8 * bx),
-                             bar, pol_w);
+        if constexpr (T == QMM_Q4_K) {
+            // rows 0..7 of the group, and 8..15 when the CTA owns them (a
+            // CTA's rows end on a half or at N); the box is CH super-blocks
+            if (lane != 0) return;
+            const int boxes = r1 - row0 > 8 ? 2 : 1;
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(boxes * 8 * P.row_pitch));
+            for (int bx = 0; bx < boxes; ++bx)
+                tma_load_2d_hint(dst + bx * 8 * P.row_pitch, &tmW, sb0 * SB_WORDS, static_cast<int>(row0 + 8 * bx),
+                                 bar, pol_w);
+        } else {
+            // lane r copies row r's span rounded out to 16 bytes (never past
+            // the end of the matrix)
+            const int rows = group_rows(gi);
+            uint64_t src = 0;
+            uint32_t bytes = 0;
+            if (lane < rows) {
+                const uint64_t start = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(row0 + lane) * P.RB +
+                                       static_cast<uint64_t>(210) * sb0;
+                src = start & ~uint64_t(15);
+                uint64_t end = (start + static_cast<uint64_t>(210) * nsb + 15) & ~uint64_t(15);
+                if (end > P.w_end) end = P.w_end & ~uint64_t(15);
+                bytes = static_cast<uint32_t>(end - src);
+            }
+            const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+            if (lane == 0) mbar_arrive_expect_tx(bar, total);
+            if (bytes > 0)
+                bulk_g2s(dst + lane * P.row_pitch, reinterpret_cast<const void *>(src), bytes, bar, pol_w);
+        }
+    };
+
+    // issue cursor over this warp's units in phase order
+    int ip = 0, iu = 0, issued = 0, islot = 0;
+    PhaseUnits ir = phase_units(P, 0, ng, warp);
+    iu = ir.begin;
+    auto issue_next = [&]() {
+        while (ip < P.nphase && iu >= ir.end) {
+            if (++ip < P.nphase) {
+                ir = phase_units(P, ip, ng, warp);
+                iu = ir.begin;
+            }
+        }
+        if (ip >= P.nphase) return;
+        issue(ir, iu, islot);
+        ++iu;
+        ++issued;
+        if (++islot == P.NS) islot = 0;
     };
 
     // the first stage of every warp before the wait for the quantiser (see
-    // the header); the others after the activation copy, which would wait
-    // behind them in the copy engine otherwise
+    // the header); the others after the first activation copy, which would
+    // wait behind them in the copy engine otherwise
     pdl_trigger();
-    int issued = 0;
-    if (nst > 0) issue(uw0, 0), issued = 1;
+    issue_next();
     pdl_wait();
-    if (threadIdx.x == 0) {
-        const uint32_t row_bytes = static_cast<uint32_t>(2 * P.K + P.K / 8);
-        mbar_arrive_expect_tx(xbar, row_bytes * P.M);
-        for (int m = 0; m < P.M; ++m)
-            bulk_g2s(smem_u32(smem + P.off_x + m * P.x_ld), P.xh + static_cast<int64_t>(m) * row_bytes, row_bytes,
-                     xbar, pol_w);
-    }
-    __syncthreads();  // the activation copy goes first
-    for (; issued < min(P.NS, nst); ++issued) issue(uw0 + issued, issued);
-    bool failed = !__all_sync(0xffffffffu, mbar_wait(xbar, 0, P.status));
 
     // ldmatrix row addresses of this lane (it names row lane & 7 of matrix lane >> 3)
     const int lr = lane & 7, lm = lane >> 3;
-    // weights: matrices (rows 0-7 | 8-15) x (16-byte segment 2c | 2c + 1)
+    // Q4_K weights: matrices (rows 0-7 | 8-15) x (16-byte segment 2c | 2c + 1)
     const uint32_t a_off = static_cast<uint32_t>((lr + 8 * (lm & 1)) * P.row_pitch + 16 + 16 * (lm >> 1));
-    // activations of token lr: matrices (half e, B register) of one
-    // sub-block, and the block sums (hi | lo); tokens >= M read zeros
+    // activations of token lr: matrices (half e, B register) of one 32-block;
+    // Q4_K block sums (hi | lo); tokens >= M read zeros
     const bool tok_ok = lr < P.M;
     const uint32_t x_row = smem_u32(smem + P.off_x + lr * P.x_ld);
     const uint32_t zero = smem_u32(smem + OFF_ZERO);
     const uint32_t x_base = (tok_ok ? x_row : zero) + 16 * lm;
-    const uint32_t xs_base = (tok_ok ? x_row + 2 * P.K : zero) + 16 * (lm & 1);
+    const uint32_t xs_base = (tok_ok ? x_row + 512 * P.nbp : zero) + 16 * (lm & 1);
     const uint32_t x_step = tok_ok ? 512u : 0u, xs_step = tok_ok ? 32u : 0u;  // per super-block
-    const int quad = lane & ~3;
+    const float *xs16 = reinterpret_cast<const float *>(smem + P.off_xs);
 
-    // rows g, g+8 of the current group x tokens 2t, 2t+1; even and odd
-    // sub-blocks accumulate separately (two independent chains), c = c + c2
+    // rows g, g+8 of the current group x tokens 2t, 2t+1; two independent
+    // accumulator chains, c = c + c2
     float c[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int cur = -1;       // group of c (CTA-local), -1 none
-    int cur_first = 0;  // c holds the group from its first chunk
-    int consumed = 0, slot = 0, islot = min(P.NS, nst) % P.NS;
+    int consumed = 0, slot = 0;
     uint32_t phase = 0;
+    bool failed = false;
 
-    // c of group `gi` complete for this warp: y if it covered the group's
-    // whole K, else an edge record (first or last group of this warp's range)
-    auto flush = [&](int gi, bool whole) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c[i] += c2[i];
-        if (whole) {
-            const int64_t row = r0 + GR * gi + g;
-            const int tk = 2 * t;
-            if (row < r1) {
-                if (tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row] = c[0];
-                if (tk + 1 < P.M) P.y[static_cast<int64_t>(tk + 1) * P.N + row] = c[1];
-            }
-            if (row + 8 < r1) {
-                if (tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row + 8] = c[2];
-                if (tk + 1 < P.M) P.y[static_cast<int64_t>(tk + 1) * P.N + row + 8] = c[3];
-            }
+    // a group's complete result for the phase, in fragment order
+    auto store_y = [&](int gi, const float (&v)[4]) {
+        const int64_t row = r0 + GR * gi + g;
+        const int tk = 2 * t;
+        if (row < r1) {
+            if (tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row] = v[0];
+            if (tk + 1 < P.M) P.y[static_cast<int64_t>(tk + 1) * P.N + row] = v[1];
+        }
+        if (row + 8 < r1) {
+            if (tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row + 8] = v[2];
+            if (tk + 1 < P.M) P.y[static_cast<int64_t>(tk + 1) * P.N + row + 8] = v[3];
+        }
+    };
+    auto out = [&](int gi, const float (&v)[4]) {
+        if (P.nphase == 1) {
+            store_y(gi, v);
         } else {
-            const int e = 2 * warp + (gi == (uw0 / nq) ? 0 : 1);
-            if (lane == 0) edge_group[e] = gi;
-            *reinterpret_cast<float4 *>(edge_sum + e * EDGE_FLOATS + 4 * lane) = make_float4(c[0], c[1], c[2], c[3]);
+            float *tb = table + gi * EDGE_FLOATS + 4 * lane;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tb[i] += v[i];
         }
     };
 
-    for (int k = 0; k < nst && !failed; ++k) {
-        // every lane waits; the warp goes on only if all of them saw the stage
-        if (!__all_sync(0xffffffffu, mbar_wait(my_bar + 8u * slot, phase, P.status))) {
-            failed = true;
-            break;
-        }
-        consumed = k + 1;
-        const int u = uw0 + k, gi = u / nq, qi = u - gi * nq;
-        if (gi != cur) {  // a new group (the last one was flushed at its last unit)
-            cur = gi;
-            cur_first = qi == 0;
-            c[0] = c[1] = c[2] = c[3] = 0.0f;
-            c2[0] = c2[1] = c2[2] = c2[3] = 0.0f;
-        }
-        const int sb0 = qi * P.CH, nsb = min(P.CH, P.nb - sb0);
-        const uint8_t *st = smem + ring + slot * P.slot_bytes;
-        const uint32_t a_stage = smem_u32(st) + a_off;
-#pragma unroll 1
-        for (int s = 0; s < nsb; ++s) {
-            const int kb = sb0 + s;
-            // scales of sub-blocks 2t, 2t+1 for rows g and g+8
-            float sa0, sa1, sb0f, sb1f;
-            uint32_t ma, mb;
-            q4k_lane_scales(*reinterpret_cast<const uint4 *>(st + g * P.row_pitch + 144 * s), t, sa0, sa1, ma);
-            q4k_lane_scales(*reinterpret_cast<const uint4 *>(st + (g + 8) * P.row_pitch + 144 * s), t, sb0f, sb1f,
-                            mb);
-            // the min term: k slots 2t, 2t+1 = sub-blocks 2t, 2t+1 (sums hi),
-            // slots 2t+8, 2t+9 = the same sub-blocks (sums lo)
-            {
-                uint32_t xhi, xlo;
-                ldsm_x2(xs_base + kb * xs_step, xhi, xlo);
-                mma_acc(c2, ma, mb, ma, mb, xhi, xlo);
+    for (int p = 0; p < P.nphase; ++p) {
+        const PhaseUnits cr = phase_units(P, p, ng, warp);
+        // the activation window of phase p
+        if (p > 0) __syncthreads();  // every warp is done with the previous window
+        if (threadIdx.x == 0 && *fail_flag == 0) {
+            if (p > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            const int K = P.K;
+            const uint32_t xb = static_cast<uint32_t>(512 * cr.nsb);
+            const uint32_t xsb = static_cast<uint32_t>((T == QMM_Q4_K ? 32 : 512) * cr.nsb);
+            mbar_arrive_expect_tx(xbar, P.M * xb + (T == QMM_Q4_K ? P.M : 1) * xsb);
+            const uint8_t *src_row = P.xh;
+            for (int m = 0; m < P.M; ++m, src_row += 2 * K + K / 8) {
+                const uint32_t dst = smem_u32(smem + P.off_x + m * P.x_ld);
+                bulk_g2s(dst, src_row + static_cast<int64_t>(512) * cr.sb, xb, xbar, pol_w);
+                if (T == QMM_Q4_K)
+                    bulk_g2s(dst + 512 * P.nbp, src_row + 2 * K + static_cast<int64_t>(32) * cr.sb, xsb, xbar, pol_w);
             }
-            const uint32_t a_sb = a_stage + 144 * s;
-            const uint32_t x_sb = x_base + kb * x_step;
+            if (T == QMM_Q6_K)
+                bulk_g2s(smem_u32(smem + P.off_xs), P.xs16 + static_cast<int64_t>(512) * cr.sb, xsb, xbar, pol_w);
+        }
+        if (p == 0) {
+            __syncthreads();  // the activation copy goes first
+            while (issued < P.NS && !(ip >= P.nphase)) issue_next();
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(xbar, static_cast<uint32_t>(p & 1), P.status))) {
+            failed = true;
+            if (lane == 0) *fail_flag = 1;
+        }
+
+        int cur = -1, cur_first = 0;
+        for (int u = cr.begin; u < cr.end; ++u) {
+            if (failed) continue;
+            // every lane waits; the warp goes on only if all of them saw the stage
+            if (!__all_sync(0xffffffffu, mbar_wait(my_bar + 8u * slot, phase, P.status))) {
+                failed = true;
+                if (lane == 0) *fail_flag = 1;
+                continue;
+            }
+            ++consumed;
+            const int gi = u / cr.nq, qi = u - gi * cr.nq;
+            if (gi != cur) {
+                cur = gi;
+                cur_first = qi == 0;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {  // quant bytes 32cc..32cc+31: sub-blocks 2cc, 2cc+1
-                uint32_t wa0, wb0, wa1, wb1;  // rows g | g+8, halves e = 0 | 1
-                ldsm_x4(a_sb + 32 * cc, wa0, wb0, wa1, wb1);
-                const uint32_t wa0s = wa0 >> 8, wb0s = wb0 >> 8, wa1s = wa1 >> 8, wb1s = wb1 >> 8;
-                // scales of sub-blocks 2cc, 2cc+1 from the quad's lane cc
-                const float s_a0 = __shfl_sync(0xffffffffu, sa0, quad | cc);
-                const float s_a1 = __shfl_sync(0xffffffffu, sa1, quad | cc);
-                const float s_b0 = __shfl_sync(0xffffffffu, sb0f, quad | cc);
-                const float s_b1 = __shfl_sync(0xffffffffu, sb1f, quad | cc);
+                for (int i = 0; i < 4; ++i) c[i] = c2[i] = 0.0f;
+            }
+            const int sb0 = cr.sb + qi * P.CH, nsb = min(P.CH, cr.sb + cr.nsb - sb0);
+            const uint8_t *st = smem + ring + slot * P.slot_bytes;
+            if constexpr (T == QMM_Q4_K) {
+                const uint32_t a_stage = smem_u32(st) + a_off;
+#pragma unroll 1
+                for (int s = 0; s < nsb; ++s) {
+                    const int kw = sb0 + s - cr.sb;  // super-block inside the window
+                    q4k_superblock(a_stage + 144 * s, st + g * P.row_pitch + 144 * s,
+                                   st + (g + 8) * P.row_pitch + 144 * s, x_base + kw * x_step,
+                                   xs_base + kw * xs_step, t, quad, c, c2);
+                }
+            } else {
+                // the data of rows g and g+8 start at their byte offsets inside the copies
+                const int64_t row0 = r0 + GR * gi;
+                const uint64_t base = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(210) * sb0;
+                const int oa = static_cast<int>((base + static_cast<uint64_t>(row0 + g) * P.RB) & 15);
+                const int ob = static_cast<int>((base + static_cast<uint64_t>(row0 + g + 8) * P.RB) & 15);
+                // the matrix's last bytes, not copied: loaded here
+                if (row0 + group_rows(gi) == P.N && sb0 + nsb == P.nb && (P.w_end & 15) != 0) {
+                    const int rl = static_cast<int>(P.N - 1 - row0);
+                    const uint64_t start = base + static_cast<uint64_t>(P.N - 1) * P.RB;
+                    const uint64_t copied = (P.w_end & ~uint64_t(15)) - (start & ~uint64_t(15));
+                    const int tail = static_cast<int>(P.w_end & 15);
+                    if (lane < tail / 4) {
+                        const uint32_t v = __ldg(reinterpret_cast<const unsigned int *>((P.w_end & ~uint64_t(15)) + 4 * lane));
+                        *reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(st) + rl * P.row_pitch + copied + 4 * lane) = v;
+                    }
+                    __syncwarp();
+                }
+                const uint8_t *ra = st + g * P.row_pitch + oa;
+                const uint8_t *rb = st + (g + 8) * P.row_pitch + ob;
+#pragma unroll 1
+                for (int s = 0; s < nsb; s += 2) {
+                    const int kw = sb0 + s - cr.sb;
+                    q6k_superblock<false>(ra + 210 * s, rb + 210 * s, x_base + kw * x_step, xs16 + kw * 128, t,
+                                          quad, c, c2);
+                    if (s + 1 < nsb)
+                        q6k_superblock<true>(ra + 210 * (s + 1), rb + 210 * (s + 1), x_base + (kw + 1) * x_step,
+                                             xs16 + (kw + 1) * 128, t, quad, c, c2);
+                }
+            }
+            __syncwarp();
+            if (!(ip >= P.nphase)) {
+                // the slot just read is refilled: order the reads before the async write
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_next();
+            }
+            if (++slot == P.NS) slot = 0, phase ^= 1u;
+            // the group ends here for this warp in this phase
+            if (u == cr.end - 1 || (u + 1) / cr.nq != gi) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {  // sub-block 2cc + h: low or high nibbles
-                    const uint32_t mk = h ? 0x00F000F0u : 0x000F000Fu;
-                    uint32_t x0, x1, x2, x3;
-                    ldsm_x4(x_sb + 64 * (2 * cc + h), x0, x1, x2, x3);
-                    float d[4];
-                    mma_new(d, wa0 & mk, wb0 & mk, wa0s & mk, wb0s & mk, x0, x1);
-                    mma_acc(d, wa1 & mk, wb1 & mk, wa1s & mk, wb1s & mk, x2, x3);
-                    float(&acc)[4] = h ? c2 : c;
-                    const float sa = h ? s_a1 : s_a0, sb = h ? s_b1 : s_b0;
-                    acc[0] = fmaf(sa, d[0], acc[0]);
-                    acc[1] = fmaf(sa, d[1], acc[1]);
-                    acc[2] = fmaf(sb, d[2], acc[2]);
-                    acc[3] = fmaf(sb, d[3], acc[3]);
+                for (int i = 0; i < 4; ++i) c[i] += c2[i];
+                if (cur_first && qi == cr.nq - 1) {
+                    out(gi, c);
+                } else {
+                    const int e = 2 * warp + (gi == cr.begin / cr.nq ? 0 : 1);
+                    if (lane == 0) edge_group[e] = gi;
+                    *reinterpret_cast<float4 *>(edge_sum + e * EDGE_FLOATS + 4 * lane) =
+                        make_float4(c[0], c[1], c[2], c[3]);
                 }
             }
         }
-        __syncwarp();
-        if (issued < nst) {
-            // the slot just read is refilled: order the reads before the async write
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(uw0 + issued, islot);
-            ++issued;
-            if (++islot == P.NS) islot = 0;
+        // groups of this phase cut by warp boundaries: records e = 2w + {0, 1}
+        // in warp order; the first record of a group adds the others in order
+        __syncthreads();
+        if (*fail_flag == 0) {
+            for (int e = warp; e < 2 * FW; e += FW) {
+                const int gi = edge_group[e];
+                if (gi < 0) continue;
+                bool first = true;
+                for (int f = 0; f < e; ++f) first = first && edge_group[f] != gi;
+                if (!first) continue;
+                float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int f = e; f < 2 * FW; ++f)
+                    if (edge_group[f] == gi) {
+                        const float4 v = *reinterpret_cast<const float4 *>(edge_sum + f * EDGE_FLOATS + 4 * lane);
+                        s[0] += v.x;
+                        s[1] += v.y;
+                        s[2] += v.z;
+                        s[3] += v.w;
+                    }
+                out(gi, s);
+            }
         }
-        if (++slot == P.NS) slot = 0, phase ^= 1u;
-        // the group ends here for this warp: flush
-        if (k == nst - 1 || (uw0 + k + 1) / nq != gi) flush(gi, cur_first && qi == nq - 1);
+        __syncthreads();
+        if (lane < 2) edge_group[2 * warp + lane] = -1;
     }
     // no bulk copy may still be in flight when the CTA exits
     if (lane == 0)
         for (int k = consumed; k < issued; ++k)
             mbar_wait(my_bar + 8u * (k % P.NS), static_cast<uint32_t>((k / P.NS) & 1), P.status);
-    if (threadIdx.x == 0) mbar_wait(xbar, 0, P.status);
+    if (threadIdx.x == 0) mbar_wait(xbar, static_cast<uint32_t>((P.nphase - 1) & 1), P.status);
     __syncthreads();
-    if (failed) return;
-    // groups cut by warp boundaries: records e = 2w + {0, 1} in warp order;
-    // the first record of a group adds the others in record order
-    for (int e = warp; e < 2 * FW; e += FW) {
-        const int gi = edge_group[e];
-        if (gi < 0) continue;
-        bool first = true;
-        for (int f = 0; f < e; ++f) first = first && edge_group[f] != gi;
-        if (!first) continue;
-        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int f = e; f < 2 * FW; ++f)
-            if (edge_group[f] == gi) {
-                const float4 v = *reinterpret_cast<const float4 *>(edge_sum + f * EDGE_FLOATS + 4 * lane);
-                s[0] += v.x;
-                s[1] += v.y;
-                s[2] += v.z;
-                s[3] += v.w;
+    if (*fail_flag != 0 || P.nphase == 1) return;
+    for (int gi = warp; gi < ng; gi += FW) {
+        const float *tb = table + gi * EDGE_FLOATS + 4 * lane;
+        const float v[4] = {tb[0], tb[1], tb[2], tb[3]};
+        store_y(gi, v);
+    }
+}
+
+// Shared-memory plan: head | activation window [M][x_ld] | Q6_K group sums
+// window | phase table | FW rings of NS slots of GR rows.  The fewest phases
+// that fit; within them the widest chunk that leaves two stages per warp and,
+// when there is a choice, at least three units per warp.
+struct Plan {
+    int CH, NS, nphase, nbp, x_ld, row_pitch, slot_bytes, off_x, off_xs, off_table, off_ring, smem;
+};
+
+template <int T>
+bool plan_mm(int M, int64_t K, int64_t max_groups, int max_smem, Plan &pl) {
+    using C = Mm<T>;
+    const int nb = static_cast<int>(K / 256);
+    for (int P = 1; P <= MAX_PHASES; ++P) {
+        int best = -1;
+        Plan cand = {};
+        for (int ci = 0; ci < C::NCH; ++ci) {
+            const int ch = C::CHS[ci];
+            int nbp = nb;
+            if (P > 1) {
+                nbp = (nb + P - 1) / P;
+                nbp = (nbp + ch - 1) / ch * ch;
+                if (static_cast<int64_t>(nbp) * (P - 1) >= nb) continue;  // an empty last phase
             }
-        c[0] = s[0];
-        c[1] = s[1];
-        c[2] = s[2];
-        c[3] = s[3];
-        c2[0] = c2[1] = c2[2] = c2[3] = 0.0f;
-        flush(gi, true);
+            const int64_t x_ld = (static_cast<int64_t>(nbp) * (512 + C::XS_TOKEN) + 127) / 128 * 128 + 16;
+            const int64_t o_x = (HEAD + 127) / 128 * 128;
+            const int64_t o_xs = (o_x + M * x_ld + 127) / 128 * 128;
+            const int64_t o_table = o_xs + (T == QMM_Q6_K ? static_cast<int64_t>(nbp) * 512 : 0);
+            const int64_t o_ring = (o_table + (P > 1 ? max_groups * EDGE_FLOATS * 4 : 0) + 127) / 128 * 128;
+            const int pitch = T == QMM_Q4_K ? 144 * ch : ((210 * ch + 26 + 15) / 16 | 1) * 16;
+            const int64_t slot = static_cast<int64_t>(GR) * pitch;
+            int64_t ns = (max_smem - o_ring) / (FW * slot);
+            if (ns < 2) continue;
+            if (ns > MAX_NS) ns = MAX_NS;
+            cand = {ch, static_cast<int>(ns), P, nbp, static_cast<int>(x_ld), pitch, static_cast<int>(slot),
+                    static_cast<int>(o_x), static_cast<int>(o_xs), static_cast<int>(o_table),
+                    static_cast<int>(o_ring), static_cast<int>(o_ring + FW * ns * slot)};
+            best = ci;
+            const int64_t units = max_groups * ((nbp + ch - 1) / ch) * P;
+            if (max_groups <= 0 || units >= 3 * FW) break;
+        }
+        if (best >= 0) {
+            pl = cand;
+            return true;
+        }
     }
+    return false;
 }
 
-// Shared-memory plan: head | activation rows [M][x_ld] | FW rings of NS
-// slots, each GR rows of CH super-blocks.  CH is the widest of 5, 3, 1 that
-// leaves two stages per warp and, when there is a choice, at least three
-// units per warp (units_at(ch) = a CTA's units for that chunk width; <= 0
-// when unknown).
-template <typename F>
-bool plan_mm(int M, int64_t K, int max_smem, F units_at, MmParams &P, int &smem) {
-    const int64_t x_ld = ((2 * K + K / 8 + 127) / 128) * 128 + 16;
-    const int64_t o_x = (HEAD + 127) / 128 * 128;
-    const int64_t o_ring = (o_x + M * x_ld + 127) / 128 * 128;
-    int best = 0;
-    int64_t best_ns = 0;
-    for (int ch = 5; ch >= 1; ch -= 2) {
-        const int64_t slot = static_cast<int64_t>(GR) * 144 * ch;
-        const int64_t ns = (max_smem - o_ring) / (FW * slot);
-        if (ns < 2) continue;
-        best = ch;
-        best_ns = ns;
-        const int64_t units = units_at(ch);
-        if (units <= 0 || units >= 3 * FW) break;
-    }
-    if (best == 0) return false;
-    const int64_t ns = best_ns > MAX_NS ? MAX_NS : best_ns;
-    P.NS = static_cast<int>(ns);
-    P.CH = best;
-    P.row_pitch = 144 * best;
-    P.slot_bytes = GR * P.row_pitch;
-    P.x_ld = static_cast<int>(x_ld);
-    P.off_x = static_cast<int>(o_x);
-    P.off_ring = static_cast<int>(o_ring);
-    smem = static_cast<int>(o_ring + FW * ns * P.slot_bytes);
-    return true;
-}
-
-}  // namespace
-
-bool gemv_mma_fits(int type, int M, int64_t K, int max_smem) {
-    if (type != QMM_Q4_K || M < 2 || M > 8 || K < 256 || K % 256 || K > (1 << 20)) return false;
-    if (tensor_map_encoder() == nullptr) return false;
-    MmParams P = {};
-    int smem = 0;
-    return plan_mm(M, K, max_smem, [](int) { return int64_t(0); }, P, smem);
-}
-
-cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
-                            cudaStream_t st, int num_sms, int max_smem, int *status) {
-    if (!gemv_mma_fits(type, M, K, max_smem) || N > (int64_t(1) << 30)) return cudaErrorNotSupported;
+int64_t max_groups_of(int64_t N, int num_sms, int64_t *grid_out) {
     const int64_t halves = (N + 7) / 8;
     int64_t grid = num_sms;
     if (grid > halves) grid = halves;
     if (grid < 1) grid = 1;
+    if (grid_out) *grid_out = grid;
+    return (halves / grid + 2) / 2;
+}
+
+bool type_ok(int type, int M, int64_t K, int64_t N) {
+    if (M < 2 || M > 8 || K < 256 || K % 256 || K > (1 << 20) || N < 1 || N > (int64_t(1) << 30)) return false;
+    if (type == QMM_Q4_K) return tensor_map_encoder() != nullptr;
+    if (type == QMM_Q6_K) return (K / 256) % 2 == 0;
+    return false;
+}
+
+}  // namespace
+
+bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_sms) {
+    if (!type_ok(type, M, K, N)) return false;
+    const int64_t mg = max_groups_of(N, num_sms, nullptr);
+    Plan pl;
+    return type == QMM_Q4_K ? plan_mm<QMM_Q4_K>(M, K, mg, max_smem, pl) : plan_mm<QMM_Q6_K>(M, K, mg, max_smem, pl);
+}
+
+cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
+                            cudaStream_t st, int num_sms, int max_smem, int *status) {
+    if (!type_ok(type, M, K, N)) return cudaErrorNotSupported;
+    int64_t grid = 0;
+    const int64_t mg = max_groups_of(N, num_sms, &grid);
+    Plan pl;
+    const bool ok =
+        type == QMM_Q4_K ? plan_mm<QMM_Q4_K>(M, K, mg, max_smem, pl) : plan_mm<QMM_Q6_K>(M, K, mg, max_smem, pl);
+    if (!ok) return cudaErrorNotSupported;
     const int nb = static_cast<int>(K / 256);
-    // a CTA's units for chunk width ch: its groups x chunks per row
-    const int64_t max_groups = (halves / grid + 2) / 2;
-    auto units_at = [&](int ch) { return max_groups * ((nb + ch - 1) / ch); };
+    const int bb = type == QMM_Q4_K ? Mm<QMM_Q4_K>::BB : Mm<QMM_Q6_K>::BB;
+    if (mg * ((nb + pl.CH - 1) / pl.CH) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     MmParams P = {};
-    int smem = 0;
-    plan_mm(M, K, max_smem, units_at, P, smem);
-    if (units_at(P.CH) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
-    // the weights as 8-byte elements [N][18 * nb]: boxes of CH super-blocks x 8 rows
-    CUtensorMap tmW;
-    {
+    P.W = static_cast<const uint8_t *>(W);
+    P.RB = static_cast<int64_t>(nb) * bb;
+    P.w_end = reinterpret_cast<uint64_t>(W) + static_cast<uint64_t>(N) * P.RB;
+    P.N = N;
+    P.K = static_cast<int>(K);
+    P.M = M;
+    P.nb = nb;
+    const int64_t halves = (N + 7) / 8;
+    P.halves_q = halves / grid;
+    P.halves_r = static_cast<int>(halves % grid);
+    P.xh = static_cast<const uint8_t *>(xh);
+    P.xs16 = P.xh + static_cast<int64_t>(M) * (2 * K + K / 8);
+    P.nphase = pl.nphase;
+    P.nbp = pl.nbp;
+    P.x_ld = pl.x_ld;
+    P.y = y;
+    P.NS = pl.NS;
+    P.slot_bytes = pl.slot_bytes;
+    P.CH = pl.CH;
+    P.row_pitch = pl.row_pitch;
+    P.off_x = pl.off_x;
+    P.off_xs = pl.off_xs;
+    P.off_table = pl.off_table;
+    P.off_ring = pl.off_ring;
+    P.status = status;
+    CUtensorMap tmW = {};
+    if (type == QMM_Q4_K) {
+        // the weights as 8-byte elements [N][18 * nb]: boxes of CH super-blocks x 8 rows
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb) * SB_WORDS, static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * 144};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(P.CH * SB_WORDS), 8u};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(pl.CH * SB_WORDS), 8u};
         const cuuint32_t es[2] = {1, 1};
         if (tensor_map_encoder()(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), dims, strides, box,
                                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    P.N = N;
-    P.K = static_cast<int>(K);
-    P.M = M;
-    P.nb = nb;
-    P.halves_q = halves / grid;
-    P.halves_r = static_cast<int>(halves % grid);
-    P.xh = static_cast<const uint8_t *>(xh);
-    P.y = y;
-    P.status = status;
-    cudaError_t e = cudaFuncSetAttribute(gemv_mma_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = type == QMM_Q4_K ? gemv_mma_kernel<QMM_Q4_K> : gemv_mma_kernel<QMM_Q6_K>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(FTHREADS);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_mma_q4k_kernel, tmW, P);
+    return cudaLaunchKernelEx(&cfg, kern, tmW, P);
 }
 
 }  // namespace qk

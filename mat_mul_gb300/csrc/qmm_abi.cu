@@ -134,13 +134,13 @@ int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
 }  // namespace qk
 
 namespace {
-// The decode product of this type and M runs on the tensor-core kernel.
-bool decode_on_tensor_cores(int type, int64_t M, int64_t K, const DeviceInfo &di) {
+// The decode product of this type and shape runs on the tensor-core kernel.
+bool decode_on_tensor_cores(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo &di) {
     if (M < 2 || M > 8 || g_force_round_gemv) return false;
     const int path = g_decode_path.load();
     if (path == QMM_DECODE_BLOCK) return false;
     if (path == QMM_DECODE_AUTO && (M < QMM_TENSOR_MIN_M || g_no_mma_gemv)) return false;
-    return qk::gemv_mma_fits(type, static_cast<int>(M), K, di.max_smem);
+    return qk::gemv_mma_fits(type, static_cast<int>(M), N, K, di.max_smem, di.num_sms);
 }
 }  // namespace
 
@@ -248,23 +248,27 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     if (int rc = device_info(dev, di)) return rc;
 
     // Four paths, chosen by M and by what fits in shared memory:
-    //   mma  : decode, Q4_K with QMM_TENSOR_MIN_M <= M <= 8 (qmm_set_decode_path
-    //          widens or closes it): the quantiser (fp16 d*q into the
-    //          workspace), then sixteen weight rows per f16 mma.sync
+    //   mma  : decode, Q4_K / Q6_K with QMM_TENSOR_MIN_M <= M <= 8
+    //          (qmm_set_decode_path widens or closes it): the quantiser (fp16
+    //          d*q and sums into the workspace), then sixteen weight rows per
+    //          f16 mma.sync
     //   sb   : decode, one weight block per lane, quantises x itself (one
     //          launch, no workspace); M <= 8 when the activations fit
     //   gemv : decode, 32 units per round, after the quantiser kernel
     //   gemm : prefill after the quantiser: Q4_K on tcgen05 (fp16 operands,
     //          fp32 accumulators), other types on the int8 mma.sync kernel
-    if (decode_on_tensor_cores(type, M, K, di)) {
-        // the quantiser writes fp16 d*q in fragment order; the decode kernel
-        // (programmatic dependent launch) streams weights while it runs
+    if (decode_on_tensor_cores(type, M, N, K, di)) {
+        // the quantiser writes fp16 d*q in fragment order and the sums; the
+        // decode kernel (programmatic dependent launch) streams weights while
+        // it runs.  Workspace: [M][2K + K/8 bytes] | [K/16][8] fp32
         void *ws = nullptr;
-        if (int rc = workspace(dev, st, align_up(static_cast<size_t>(M * (K + K / 16)) * 2, 256), &ws)) return rc;
+        const size_t xh_bytes = static_cast<size_t>(M * (K + K / 16)) * 2;
+        if (int rc = workspace(dev, st, align_up(xh_bytes + static_cast<size_t>(K) * 2, 256), &ws)) return rc;
         qk::QuantOut o = {};
         o.xh = ws;
         o.xh_ld = K + K / 16;
         o.xh_mma = 1;
+        o.xs16 = reinterpret_cast<float *>(static_cast<char *>(ws) + xh_bytes);
         e = qk::launch_quantize(x, M, K, o, st, true, di.num_sms, true);
         if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
         g_launches.fetch_add(1);
@@ -372,7 +376,7 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
         bool fits = true;
         for (int i = 0; i < n; ++i)
             fits = fits && (Ns[i] == 0 || (qk::gemv_sb_fits(types[i], static_cast<int>(M), K, di.max_smem) &&
-                                           !decode_on_tensor_cores(types[i], M, K, di)));
+                                           !decode_on_tensor_cores(types[i], M, Ns[i], K, di)));
         if (fits) {
             e = qk::launch_gemv_sb_group(n, types, Ws, Ns, K, x, static_cast<int>(M), ys,
                                          static_cast<cudaStream_t>(stream), di.num_sms, di.max_smem, di.status);

@@ -36,6 +36,7 @@ struct QuantOut {
     void *xh;  // __half
     int64_t xh_ld;
     int xh_mma;
+    float *xs16;  // with xh_mma: the sums of the fp16 values per 16 elements, [K/16][8], tokens >= M zero
 };
 
 // trigger_dependents: let the next kernel (launched with programmatic
@@ -75,14 +76,15 @@ cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws,
                                  int max_smem, int *status);
 void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t *need, int num_sms, int *g);
 
-// Decode for 2 <= M <= 8 on the tensor cores (gemv_mma.cu): Q4_K, sixteen
-// weight rows dequantised to fp16 per mma.sync.m16n8k16 (fp32 accumulation).
-// xh: the quantiser's fp16 output in fragment order (xh_mma), [M][K], 16-byte
-// aligned; the kernel copies it whole into shared memory (2*M*K bytes must
-// fit).  Launched with programmatic dependent launch right after that
-// quantiser (launched with trigger_dependents): the kernel streams weights
-// before it waits, and reads xh after.
-bool gemv_mma_fits(int type, int M, int64_t K, int max_smem);
+// Decode for 2 <= M <= 8 on the tensor cores (gemv_mma.cu): Q4_K or Q6_K,
+// sixteen weight rows per mma.sync.m16n8k16 (fp16 operands, fp32
+// accumulation).  xh: the quantiser's output with xh_mma, [M][2K + K/8
+// bytes] (16-byte aligned), then for Q6_K the group sums [K/16][8] fp32
+// (xs16); the kernel copies one K window of it at a time into shared memory.
+// Launched with programmatic dependent launch right after that quantiser
+// (launched with trigger_dependents): the kernel streams weights before it
+// waits, and reads xh after.
+bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_sms);
 cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
                             cudaStream_t st, int num_sms, int max_smem, int *status);
 

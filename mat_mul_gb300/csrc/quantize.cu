@@ -54,9 +54,18 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
                 // + ((l>>2)&3)*2 + ((l>>1)&1); then the block sums of the fp16
                 // values, X = hi + lo, in two planes of 8 per super-block after K
                 row[32 * b + ((lane >> 4) * 2 + (lane & 1)) * 8 + ((lane >> 2) & 3) * 2 + ((lane >> 1) & 1)] = hq;
-                float xs = __half2float(hq);
+                float x16 = __half2float(hq);
 #pragma unroll
-                for (int o2 = 16; o2 >= 1; o2 >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, o2);
+                for (int o2 = 8; o2 >= 1; o2 >>= 1) x16 += __shfl_xor_sync(0xffffffffu, x16, o2);
+                const float xs = x16 + __shfl_xor_sync(0xffffffffu, x16, 16);
+                // the sums of the two groups of 16: [K/16][8 tokens], zeros for
+                // the tokens M..7 (written with token 0)
+                if (o.xs16 && (lane & 15) == 0) {
+                    float *gs = o.xs16 + (2 * b + (lane >> 4)) * 8;
+                    gs[m] = x16;
+                    if (m == 0)
+                        for (int64_t mm = M; mm < 8; ++mm) gs[mm] = 0.0f;
+                }
                 if (lane == 0) {
                     const __half hi = __float2half_rn(xs);
                     const __half lo = __float2half_rn(xs - __half2float(hi));

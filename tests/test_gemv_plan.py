@@ -291,122 +291,164 @@ def test_group_split_covers_every_matrix(group):
 
 
 # ---- the tensor-core decode kernel for 2 <= M <= 8 (gemv_mma.cu) ----------
-MM_W, MM_GR, MM_MAXNS = 8, 16, 4
-MM_HEAD = 1152 + 2 * MM_W * 128 * 4  # barriers, groups | zeros | edge sums
+MM_W, MM_GR, MM_MAXNS, MM_MAXP = 8, 16, 4, 8
+MM_HEAD = 1152 + 2 * MM_W * 128 * 4  # barriers, groups, flag | zeros | edge sums
 
 
-def plan_mm(M, K, units_at=None):
-    x_ld = align(2 * K + K // 8, 128) + 16
-    o_x = align(MM_HEAD, 128)
-    ring = align(o_x + M * x_ld, 128)
-    best = None
-    for ch in (5, 3, 1):
-        slot = MM_GR * 144 * ch
-        ns = (SMEM_MAX - ring) // (MM_W * slot)
-        if ns < 2:
-            continue
-        best = (ch, ns, slot)
-        u = units_at(ch) if units_at else 0
-        if u <= 0 or u >= 3 * MM_W:
-            break
-    if best is None:
-        return None
-    ch, ns, slot = best
-    ns = min(MM_MAXNS, ns)
-    return dict(NS=ns, CH=ch, pitch=144 * ch, slot=slot, ring=ring, x_ld=x_ld, off_x=o_x,
-                smem=ring + MM_W * ns * slot)
+def mm_pitch(qtype, ch):
+    return 144 * ch if qtype == synth.Q4_K else (((210 * ch + 41) // 16) | 1) * 16
 
 
-def mm_launch(N, K, M):
+def mm_max_groups(N):
     halves = -(-N // 8)
     grid = max(1, min(SMS, halves))
+    return (halves // grid + 2) // 2, halves, grid
+
+
+def plan_mm(qtype, M, K, max_groups=0):
     nb = K // 256
-    max_groups = (halves // grid + 2) // 2
-    P = plan_mm(M, K, lambda ch: max_groups * (-(-nb // ch)))
-    return P, halves, grid
+    chs = (5, 3, 1) if qtype == synth.Q4_K else (4, 2)
+    xs_token = 32 if qtype == synth.Q4_K else 0
+    if qtype == synth.Q6_K and nb % 2:
+        return None
+    for P in range(1, MM_MAXP + 1):
+        best = None
+        for ch in chs:
+            nbp = nb
+            if P > 1:
+                nbp = -(-nb // P)
+                nbp = -(-nbp // ch) * ch
+                if nbp * (P - 1) >= nb:
+                    continue
+            x_ld = align(nbp * (512 + xs_token), 128) + 16
+            o_x = align(MM_HEAD, 128)
+            o_xs = align(o_x + M * x_ld, 128)
+            o_table = o_xs + (nbp * 512 if qtype == synth.Q6_K else 0)
+            o_ring = align(o_table + (max_groups * 512 if P > 1 else 0), 128)
+            pitch = mm_pitch(qtype, ch)
+            slot = MM_GR * pitch
+            ns = (SMEM_MAX - o_ring) // (MM_W * slot)
+            if ns < 2:
+                continue
+            ns = min(MM_MAXNS, ns)
+            best = dict(CH=ch, NS=ns, P=P, nbp=nbp, x_ld=x_ld, pitch=pitch, slot=slot, off_x=o_x,
+                        off_xs=o_xs, off_table=o_table, ring=o_ring, smem=o_ring + MM_W * ns * slot)
+            if max_groups <= 0 or max_groups * -(-nbp // ch) * P >= 3 * MM_W:
+                break
+        if best:
+            return best
+    return None
 
 
-def check_mm(N, K, M):
-    P, halves, grid = mm_launch(N, K, M)
+def check_mm(qtype, N, K, M):
+    mg, halves, grid = mm_max_groups(N)
+    P = plan_mm(qtype, M, K, mg)
     assert P is not None and P["smem"] <= SMEM_MAX
-    CH, pitch = P["CH"], P["pitch"]
-    # activation rows: bulk copies of 2K + K/8 bytes to 16-byte aligned rows
-    # whose 8 ldmatrix rows (tokens) fall in distinct 16-byte bank groups
-    row_bytes = 2 * K + K // 8
+    CH, pitch, nbp, nph = P["CH"], P["pitch"], P["nbp"], P["P"]
+    nb = K // 256
+    BB = synth.BLOCK_BYTES[qtype]
+    RB = nb * BB
+    w_end = N * RB            # the matrix at address 0 (16-byte aligned)
     assert P["x_ld"] % 128 == 16 and P["off_x"] % 128 == 0 and P["off_x"] >= MM_HEAD
-    assert P["ring"] >= P["off_x"] + M * P["x_ld"] and row_bytes % 16 == 0 and M * row_bytes < 2 ** 20
-    assert row_bytes <= P["x_ld"]
-    # tensor copies: 128-byte aligned destinations, box inner extent of 18*CH
-    # 8-byte elements (<= 256, a multiple of 16 bytes), inner coordinate
-    # 18*sb0 elements = 144*sb0 bytes (a multiple of 16)
-    assert CH % 2 == 1 and 18 * CH <= 256 and (144 * CH) % 16 == 0
-    assert P["ring"] % 128 == 0 and P["slot"] % 128 == 0 and (8 * pitch) % 128 == 0
+    assert P["ring"] % 128 == 0 and P["slot"] % 16 == 0
     # an ldmatrix reads 16 bytes of 8 consecutive rows: 8 distinct bank groups
     assert len({(r * pitch // 16) % 8 for r in range(8)}) == 8
-    nb = K // 256
+    if qtype == synth.Q4_K:
+        assert CH % 2 == 1 and 18 * CH <= 256 and P["slot"] % 128 == 0 and (8 * pitch) % 128 == 0
+    else:
+        assert CH % 2 == 0 and nb % 2 == 0 and pitch >= 210 * CH + 26
+    if nph > 1:
+        assert nbp % CH == 0 and nbp * (nph - 1) < nb
+    row_bytes = 2 * K + K // 8   # quantiser output per token; then [K/16][8] fp32 sums
+    xs16_at = M * row_bytes
+    for p in range(nph):
+        sb, nsb = p * nbp, min(nbp, nb - p * nbp)
+        assert nsb > 0
+        # the window copies: 16-byte sizes and sources, inside their buffers
+        xb = 512 * nsb
+        assert xb % 16 == 0 and 512 * sb + xb <= 2 * K and xb <= P["x_ld"]
+        if qtype == synth.Q4_K:
+            assert 2 * K + 32 * sb + 32 * nsb <= row_bytes and 512 * nbp + 32 * nsb + 16 <= P["x_ld"]
+            tx = M * xb + M * 32 * nsb
+        else:
+            # the group sums [K/16][8] fp32: 512 bytes per super-block, 2K bytes in all
+            assert xs16_at % 16 == 0 and 512 * sb + 512 * nsb <= 2 * K
+            assert P["off_xs"] % 128 == 0 and P["off_xs"] + 512 * nsb <= P["off_table"]
+            tx = M * xb + 512 * nsb
+        assert tx < 2 ** 20
     q, r = divmod(halves, grid)
-    nq = -(-nb // CH)
     covered = set()
     for c in range(grid):
         h0 = q * c + min(c, r)
         nh = q + (1 if c < r else 0)
         r0, r1 = 8 * h0, min(N, 8 * (h0 + nh))
-        assert r1 > r0
         ng = (nh + 1) // 2
-        U = ng * nq
-        for w in range(MM_W):
-            uw0, uw1 = U * w // MM_W, U * (w + 1) // MM_W
-            groups_of_warp = sorted({u // nq for u in range(uw0, uw1)})
-            for u in range(uw0, uw1):
-                gi, qi = divmod(u, nq)
-                sb0 = qi * CH
-                nsb = min(CH, nb - sb0)
-                row0 = r0 + MM_GR * gi
-                boxes = 2 if r1 - row0 > 8 else 1
-                assert (18 * sb0 * 8) % 16 == 0 and row0 + 8 * boxes <= 8 * halves
-                # the boxes load rows [row0, row0 + 8*boxes): every one this CTA owns,
-                # none of another CTA's (rows past N arrive as zeros)
-                assert row0 + 8 * boxes >= min(r1, row0 + 16) and (boxes == 1 or row0 + 16 <= r1 or r1 == N)
-                for rr in range(min(8 * boxes, N - row0)):
-                    for s in range(nsb):
-                        key = (row0 + rr, sb0 + s)
-                        assert key not in covered
-                        covered.add(key)
-                # every read of the stage stays inside the slot: headers and the
-                # ldmatrix rows (row 15, segment 7 of the last super-block)
-                assert 15 * pitch + 144 * (nsb - 1) + 16 + 16 * 7 + 16 <= P["slot"]
-                # activation reads: x of sub-block 7, matrix 3; sums hi | lo
-                last = sb0 + nsb - 1
-                assert last * 512 + 64 * 7 + 16 * 3 + 16 <= 2 * K
-                assert 2 * K + 32 * last + 16 + 16 <= row_bytes
-            # only the first and the last group of a warp's range can be partial
-            for gi in groups_of_warp[1:-1]:
-                assert all(uw0 <= gi * nq + qi < uw1 for qi in range(nq))
+        assert ng <= mg
+        for p in range(nph):
+            sbp, nsbp = p * nbp, min(nbp, nb - p * nbp)
+            nq = -(-nsbp // CH)
+            U = ng * nq
+            for w in range(MM_W):
+                b, e = U * w // MM_W, U * (w + 1) // MM_W
+                for u in range(b, e):
+                    gi, qi = divmod(u, nq)
+                    sb0 = sbp + qi * CH
+                    nsb = min(CH, sbp + nsbp - sb0)
+                    row0 = r0 + MM_GR * gi
+                    rows = min(MM_GR, r1 - row0)
+                    assert 1 <= rows <= MM_GR and nsb >= 1
+                    if qtype == synth.Q4_K:
+                        boxes = 2 if r1 - row0 > 8 else 1
+                        assert (18 * sb0 * 8) % 16 == 0
+                        assert row0 + 8 * boxes >= min(r1, row0 + 16) and (boxes == 1 or row0 + 16 <= r1 or r1 == N)
+                        assert 15 * pitch + 144 * (nsb - 1) + 16 + 16 * 7 + 16 <= P["slot"]
+                    else:
+                        for rr in range(rows):
+                            start = (row0 + rr) * RB + 210 * sb0
+                            src = start & ~15
+                            end = min((start + 210 * nsb + 15) & ~15, w_end & ~15)
+                            nbytes = end - src
+                            assert nbytes > 0 and nbytes % 16 == 0 and src % 16 == 0
+                            assert src >= 0 and end <= w_end
+                            assert rr * pitch + nbytes <= P["slot"]
+                            oa = start & 15
+                            assert oa % 4 == 0        # even super-blocks 4-byte aligned
+                            data_end = oa + 210 * nsb
+                            tail = (src + data_end) - end   # bytes loaded after the wait
+                            if tail > 0:
+                                assert row0 + rr == N - 1 and sb0 + nsb == nb and tail == (w_end & 15)
+                                assert tail % 4 == 0 and rr * pitch + nbytes + tail <= P["slot"]
+                            assert rr * pitch + data_end <= P["slot"]
+                    for rr in range(rows):
+                        for s in range(nsb):
+                            key = (row0 + rr, sb0 + s)
+                            assert key not in covered
+                            covered.add(key)
     assert len(covered) == N * nb
 
 
 MM_SHAPES = [(5120, 5120), (1024, 5120), (17408, 5120), (5120, 17408), (2048, 2048), (512, 2048),
-             (8192, 2048), (2048, 8192), (1000, 4352), (77, 256), (16, 17408), (9, 1024), (14336, 4096)]
+             (8192, 2048), (2048, 8192), (1000, 4352), (77, 256), (16, 17408), (9, 1024), (14336, 4096),
+             (128256, 2048), (301, 1536)]
 
 
+@pytest.mark.parametrize("qtype", [synth.Q4_K, synth.Q6_K])
 @pytest.mark.parametrize("N,K", MM_SHAPES)
 @pytest.mark.parametrize("M", [2, 4, 8])
-def test_gemv_mma_address_arithmetic(N, K, M):
-    if plan_mm(M, K) is None:
+def test_gemv_mma_address_arithmetic(qtype, N, K, M):
+    if plan_mm(qtype, M, K, mm_max_groups(N)[0]) is None:
         pytest.skip("does not fit (the block-per-lane kernel runs it)")
-    check_mm(N, K, M)
+    check_mm(qtype, N, K, M)
 
 
-def test_gemv_mma_fits_the_q4k_workloads():
-    fits = {}
-    for (_, q, K, N) in synth.LLAMA_1B + synth.QWEN3_14B_LAYER:
-        if q == synth.Q4_K:
-            for M in (2, 4, 8):
-                fits[(K, M)] = plan_mm(M, K) is not None
-    # fp16 activations of M tokens take 2*M*K bytes of shared memory: all the
-    # Q4_K shapes fit but M = 8 at K = 17408 (none of which is Q4_K here)
-    assert all(fits.values()), fits
-    assert plan_mm(8, 17408) is None and plan_mm(4, 17408) is not None
+def test_gemv_mma_fits_the_workloads():
+    for (_, q, K, N) in synth.LLAMA_1B + synth.QWEN3_14B_LAYER + synth.LM_HEAD:
+        for M in (2, 4, 8):
+            P = plan_mm(q, M, K, mm_max_groups(N)[0])
+            assert P is not None, (q, K, N, M)
+    # x of 8 tokens at K = 17408 needs phases
+    assert plan_mm(synth.Q6_K, 8, 17408, mm_max_groups(5120)[0])["P"] > 1
+    assert plan_mm(synth.Q4_K, 2, 5120, mm_max_groups(5120)[0])["P"] == 1
 
 
 def quantiser_mma_position(l):
@@ -555,3 +597,76 @@ def test_gemv_mma_fragments_reproduce_the_product(M):
     # fp16 of dmin*m (relative 2^-11) is the only rounding left in the weights
     assert (err <= 2e-3 * scale + 1e-7).all(), float((err / (scale + 1e-30)).max())
     assert np.all(C[:, M:] == 0.0)
+
+
+def _lane_q6k_scales(blk, t):
+    """Sa[0..3] as q6k_superblock: d * 2^24/f * sc[4t + i] in fp32 (exact)."""
+    fs = np.float32(2.0 ** 20 if t & 1 else 2.0 ** 24)
+    d = np.float32(np.float32(_h(_u32(blk, 208) & 0xFFFF)) * fs)
+    return [np.float32(d * np.float32(np.int8(blk[192 + 4 * t + i]))) for i in range(4)]
+
+
+def q6k_mma_replay(rows, xh, M):
+    """y[16 rows][8 tokens] of one Q6_K super-block column, with the registers
+    built as q6k_superblock builds them: six-bit fields assembled by
+    mask/multiply/add into fp16 subnormals, one MMA per group of 16, minus
+    32 * the group sums, scaled by the shuffled group scale."""
+    zero = np.zeros(512, np.uint8)
+    tok = [_token_row(xh[m])[:512] for m in range(M)] + [zero] * (8 - M)
+    xs = np.zeros((16, 8), np.float32)   # the quantiser's group sums of the fp16 values
+    for m in range(M):
+        for G in range(16):
+            acc = np.float32(0)
+            for v in xh[m, 16 * G:16 * G + 16]:
+                acc = np.float32(acc + np.float32(v))
+            xs[G, m] = acc
+    S = [(_lane_q6k_scales(rows[lane >> 2], lane & 3), _lane_q6k_scales(rows[(lane >> 2) + 8], lane & 3))
+         for lane in range(32)]
+    c = np.zeros((16, 8))
+    for n in range(2):
+        for qi in range(4):
+            xw = [_ldmatrix([tok[r][64 * (4 * n + qi) + 16 * q_: 64 * (4 * n + qi) + 16 * q_ + 16]
+                             for r in range(8)]) for q_ in range(4)]
+            mlo = 0x00F000F0 if qi >= 2 else 0x000F000F
+            mhi = 0x00030003 << (2 * qi)
+            mul = 4 if qi & 1 else 16
+            kf = 2.0 ** -15 if qi >= 2 else 2.0 ** -19
+            for lh in range(2):
+                G = 8 * n + 2 * qi + lh
+                a = []
+                for lane in range(32):
+                    g, t = lane >> 2, lane & 3
+                    regs = []
+                    for r in (g, g + 8):
+                        ql = _u32(rows[r], 64 * n + 32 * (qi & 1) + 16 * lh + 4 * t)
+                        qh = _u32(rows[r], 128 + 32 * n + 16 * lh + 4 * t)
+                        regs.append(((((qh & mhi) * mul) + (ql & mlo)) & 0xFFFFFFFF,
+                                     ((((qh >> 8) & mhi) * mul) + ((ql >> 8) & mlo)) & 0xFFFFFFFF))
+                    a.append((regs[0][0], regs[1][0], regs[0][1], regs[1][1]))
+                b = [((xw[2][l], xw[3][l]) if lh else (xw[0][l], xw[1][l])) for l in range(32)]
+                d = _mma(a, b)
+                d -= kf * xs[G][None, :]
+                for lane in range(32):
+                    g, t = lane >> 2, lane & 3
+                    src = (lane & ~3) | (G >> 2)
+                    c[g, 2 * t:2 * t + 2] += float(S[src][0][G & 3]) * d[g, 2 * t:2 * t + 2]
+                    c[g + 8, 2 * t:2 * t + 2] += float(S[src][1][G & 3]) * d[g + 8, 2 * t:2 * t + 2]
+    return c
+
+
+@pytest.mark.parametrize("M", [2, 5, 8])
+def test_gemv_mma_q6k_fragments_reproduce_the_product(M):
+    import oracle as O
+    rows = synth.weights(synth.Q6_K, 16, 256, seed=60 + M).reshape(16, 210)
+    x = synth.activations(M, 256, seed=70 + M, outlier_frac=0.05)
+    q, d, _ = O.quantize_act(x)
+    xh = np.array([[_f16(np.float32(d[m, k // 32]) * np.float32(q[m, k])) for k in range(256)]
+                   for m in range(M)], np.float16)
+    C = q6k_mma_replay(rows, xh, M)
+    w = O.dequant(synth.Q6_K, rows.reshape(-1), 16 * 256).reshape(16, 256).astype(np.float64)
+    exact = w @ xh.astype(np.float64).T
+    scale = np.abs(w) @ np.abs(xh.astype(np.float64)).T
+    err = np.abs(C[:, :M] - exact)
+    # no rounding left in the weights: only fp32 sums differ
+    assert (err <= 1e-5 * scale + 1e-9).all(), float((err / (scale + 1e-30)).max())
+    assert np.all(np.abs(C[:, M:]) == 0.0)

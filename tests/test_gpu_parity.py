@@ -121,7 +121,15 @@ def test_qmm_decode_small(cuda_lib, qtype, N, K, M):
 # CTAs (N=16 over two CTAs holding 8 rows each), ragged N and a K whose
 # super-blocks do not fill the last stage chunk, every M from 2 to 8.
 MMA_DECODE = [(16, 8192, 2), (16, 8192, 3), (1000, 4352, 5), (77, 256, 8), (2048, 2048, 4),
-              (300, 5120, 6), (9, 1024, 7), (4096, 4096, 8), (5120, 17408, 4)]
+              (300, 5120, 6), (9, 1024, 7), (4096, 4096, 8), (5120, 17408, 4),
+              # x of all of K does not fit: K taken in phases
+              (300, 17408, 8), (40, 17408, 6)]
+
+# Q6_K: rows that are not 16-byte multiples (N*K ragged at the end of the
+# matrix: the last bytes are loaded after the wait), odd and even
+# super-blocks of a chunk, K in phases (K = 17408 at M = 8), ragged N.
+MMA_DECODE_Q6K = [(301, 1536, 2), (1024, 5120, 4), (300, 17408, 8), (77, 2048, 3), (16, 4608, 5),
+                  (5120, 17408, 2), (129, 5120, 7)]
 
 
 @pytest.fixture
@@ -144,6 +152,18 @@ def test_qmm_decode_tensor_core(cuda_lib, decode_path, N, K, M):
     _assert_within_bound(y, yo, A, f"tensor-core decode N={N} K={K} M={M}")
 
 
+@pytest.mark.parametrize("N,K,M", MMA_DECODE_Q6K)
+def test_qmm_decode_tensor_core_q6k(cuda_lib, decode_path, N, K, M):
+    decode_path(cuda_lib.DECODE_TENSOR)
+    W = synth.weights(synth.Q6_K, N, K, seed=N + K + 7 * M)
+    x = synth.activations(M, K, seed=N * K + 11 * M, outlier_frac=0.01)
+    before = cuda_lib.qmm_launch_count()
+    y = _run_qmm(cuda_lib, synth.Q6_K, W, N, K, x)
+    assert cuda_lib.qmm_launch_count() - before == 2  # the quantiser, then the tensor-core kernel
+    yo, A = O.qmm(synth.Q6_K, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"tensor-core decode Q6_K N={N} K={K} M={M}")
+
+
 @pytest.mark.parametrize("M", [2, 4, 8])
 def test_qmm_decode_block_path_on_request(cuda_lib, decode_path, M):
     decode_path(cuda_lib.DECODE_BLOCK)
@@ -157,15 +177,16 @@ def test_qmm_decode_block_path_on_request(cuda_lib, decode_path, M):
     _assert_within_bound(y, yo, A, f"block-per-lane decode N={N} K={K} M={M}")
 
 
-def test_qmm_decode_tensor_core_is_deterministic(cuda_lib, decode_path):
+@pytest.mark.parametrize("qtype,K", [(synth.Q4_K, 5120), (synth.Q6_K, 17408)])
+def test_qmm_decode_tensor_core_is_deterministic(cuda_lib, decode_path, qtype, K):
     import torch
     decode_path(cuda_lib.DECODE_TENSOR)
-    N, K, M = 300, 5120, 8
-    W = _dev(synth.weights(synth.Q4_K, N, K, seed=21))
+    N, M = 300, 8
+    W = _dev(synth.weights(qtype, N, K, seed=21))
     x = _dev(synth.activations(M, K, seed=22))
-    y1 = cuda_lib.qmm(synth.Q4_K, W, N, K, x)
+    y1 = cuda_lib.qmm(qtype, W, N, K, x)
     for _ in range(3):
-        assert torch.equal(y1, cuda_lib.qmm(synth.Q4_K, W, N, K, x))
+        assert torch.equal(y1, cuda_lib.qmm(qtype, W, N, K, x))
 
 
 GEMM_SMALL = [
