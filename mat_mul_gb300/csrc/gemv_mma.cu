@@ -39,26 +39,29 @@
 //
 // Streaming.  Rows are taken in groups of 16.  CTA c (one per SM) owns a
 // range of 8-row halves, balanced to within one half, i.e. whole groups plus
-// at most one half group; its (group, chunk of CH super-blocks) units are
-// split evenly between eight warps.  Each warp streams its units through a
-// private ring.
-//   Q4_K: a stage is one or two 2-D tensor copies of 8 rows x CH super-blocks
-//     (rows past N and bytes past the row end arrive as zeros); the rows land
-//     densely 144*CH bytes apart, CH odd (5, 3 or 1), so the eight rows of an
-//     ldmatrix are eight distinct 16-byte bank groups.
-//   Q6_K: rows are 210-byte multiples, not 16-byte ones, so each row segment
-//     is one bulk copy of its span rounded out to 16 bytes (the matrix's last
-//     bytes excepted: they are loaded after the wait instead of reading past
-//     the end), read from its offset inside the copy.  With CH even (4 or 2)
-//     and an even number of super-blocks per row, a chunk's even super-blocks
-//     are 4-byte aligned and its odd ones 2-byte aligned (their words are
-//     loaded in two aligned halves and shifted together).
-// When the activations of all of K do not fit in shared memory beside the
-// rings, K is taken in P phases: the activations of one K window at a time,
-// every warp's units of that window, then the next; a group's phase results
-// are added in phase order in a shared table.  A group whose units are split
-// between warps leaves partial sums in shared memory that are added in warp
+// at most one half group.  A producer warp fills a ring of stages shared by
+// eight consumer warps; a stage is one group's 16 rows x 8 super-blocks, and
+// consumer warp w computes super-block (w + chunk) mod 8 of it, so the copies
+// are about 1.2 KB (Q4_K) or 1.7 KB (Q6_K) per row and the warps share every
+// stage evenly (the copy engine's cost per copy is what limits small ones).
+//   Q4_K: a stage is two 2-D tensor copies of 8 rows x (8 super-blocks and
+//     16 bytes), rows past N and bytes past the row end arriving as zeros, so
+//     rows land 16 bytes past a 128-byte multiple apart and the eight rows of
+//     an ldmatrix are eight distinct 16-byte bank groups.
+//   Q6_K: rows are 210-byte multiples, not 16-byte ones, so each row span is
+//     one bulk copy rounded out to 16 bytes (the matrix's last bytes
+//     excepted: they are loaded after the wait instead of reading past the
+//     end), read from its offset inside the copy, in a pitch of an odd number
+//     of 16-byte chunks.  With an even number of super-blocks per row a
+//     stage's even super-blocks are 4-byte aligned and its odd ones 2-byte
+//     aligned (their words are loaded in two aligned halves and shifted
+//     together); the rotation gives every warp both kinds in turn.
+// At a group's last stage the consumers' partial sums are added in warp
 // order; every y element is written once (deterministic).
+// When the activations of all of K do not fit in shared memory beside the
+// ring, K is taken in P phases: the activations of one K window at a time,
+// the CTA's stages of that window, then the next; a group's phase results
+// are added in phase order in a shared table.
 //
 // Activations.  The activation quantiser runs just before this kernel and
 // writes x (fp16, fragment order), the Q4_K block sums (hi, lo) per token
@@ -80,26 +83,34 @@ namespace qk {
 
 namespace {
 
-constexpr int FW = 8;  // warps
-constexpr int FTHREADS = FW * 32;
-constexpr int GR = 16;            // weight rows per group (the MMA's m)
-constexpr int MAX_NS = 4;         // stages per warp ring
+constexpr int CW = 8;                  // consumer warps; warp CW is the producer
+constexpr int NTHREADS = (CW + 1) * 32;
+constexpr int GR = 16;                 // weight rows per group (the MMA's m)
+constexpr int CHS = 8;                 // super-blocks per stage: one per consumer warp
+constexpr int MAX_NS = 6;              // stages in the ring
 constexpr int MAX_PHASES = 8;
-constexpr int EDGE_FLOATS = 128;  // a partial group: 16 rows x 8 tokens
-// shared-memory head: stage barriers | activation barrier | edge groups |
-// failure flag | zeros (the B rows of tokens M..7) | edge sums.  The
-// activation rows start on a 128-byte boundary and are 16 bytes past a
-// 128-byte multiple apart, so token m's 16-byte ldmatrix rows sit in bank
-// group m (+ a common offset); the zero rows sit in bank group 7, which no
-// token uses while M < 8.
-constexpr int OFF_XBAR = 8 * FW * MAX_NS;
-constexpr int OFF_EDGE_GROUP = OFF_XBAR + 16;
-constexpr int OFF_FAIL = OFF_EDGE_GROUP + 2 * FW * 4;
+constexpr int EDGE_FLOATS = 128;       // a group's result: 16 rows x 8 tokens
+// stage bytes per row: Q4_K boxes of 8 super-blocks and 16 bytes (so rows
+// sit 16 bytes past a 128-byte multiple apart), Q6_K spans of 8 super-blocks
+// rounded out to 16 bytes in a pitch of an odd number of 16-byte chunks
+constexpr int Q4K_PITCH = 8 * 144 + 16;
+constexpr int Q6K_PITCH = ((8 * 210 + 41) / 16 | 1) * 16;
+static_assert(Q4K_PITCH % 128 == 16 && (Q6K_PITCH / 16) % 2 == 1, "row pitches");
+// shared-memory head: full barriers | empty barriers | activation barrier |
+// failure flag | zeros (the B rows of tokens M..7) | partial sums of the
+// consumer warps, two groups.  The activation rows start on a 128-byte
+// boundary and are 16 bytes past a 128-byte multiple apart, so token m's
+// 16-byte ldmatrix rows sit in bank group m (+ a common offset); the zero
+// rows sit in bank group 7, which no token uses while M < 8.
+constexpr int OFF_FULL = 0;
+constexpr int OFF_EMPTY = 64;
+constexpr int OFF_XBAR = 128;
+constexpr int OFF_FAIL = 144;
 constexpr int OFF_ZERO = 624;
 constexpr int ZERO_BYTES = 512;
-constexpr int OFF_EDGE_SUM = 1152;
-constexpr int HEAD = OFF_EDGE_SUM + 2 * FW * EDGE_FLOATS * 4;
-static_assert(OFF_FAIL + 16 <= OFF_ZERO && OFF_ZERO + ZERO_BYTES <= OFF_EDGE_SUM, "head layout");
+constexpr int OFF_PART = 1152;
+constexpr int HEAD = OFF_PART + 2 * CW * EDGE_FLOATS * 4;
+static_assert(8 * MAX_NS <= 64 && OFF_ZERO + ZERO_BYTES <= OFF_PART, "head layout");
 static_assert(OFF_ZERO % 128 == 112 && HEAD % 128 == 0, "zero rows in bank group 7");
 constexpr int SB_WORDS = 144 / 8;  // a Q4_K super-block in the tensor map's 8-byte elements
 
@@ -118,15 +129,11 @@ struct Mm;
 template <>
 struct Mm<QMM_Q4_K> {
     static constexpr int BB = 144;
-    static constexpr int NCH = 3;
-    static constexpr int CHS[3] = {5, 3, 1};
     static constexpr int XS_TOKEN = 32;  // per super-block per token: block sums hi | lo
 };
 template <>
 struct Mm<QMM_Q6_K> {
     static constexpr int BB = 210;
-    static constexpr int NCH = 2;
-    static constexpr int CHS[2] = {4, 2};
     static constexpr int XS_TOKEN = 0;   // the group sums are one array for all tokens
 };
 
@@ -142,11 +149,11 @@ struct MmParams {
     const uint8_t *xh;  // quantiser output [M][2K + K/8 bytes]: x fp16 | Q4_K block sums
     const uint8_t *xs16;  // Q6_K group sums [K/16][8] fp32
     int nphase;         // K phases
-    int nbp;            // super-blocks per phase (a multiple of CH when nphase > 1)
+    int nbp;            // super-blocks per phase (a multiple of 8 when nphase > 1)
     int x_ld;           // bytes per token row of the activation window (= 16 mod 128)
     float *y;
-    int NS, slot_bytes;
-    int CH;             // super-blocks per row per stage
+    int NS;             // stages in the ring
+    int stage_bytes;
     int row_pitch;      // stage bytes per row
     int off_x, off_xs, off_table, off_ring;
     int *status;
@@ -338,32 +345,35 @@ __device__ __forceinline__ void q6k_superblock(const uint8_t *ra, const uint8_t 
     });
 }
 
-// This warp's units of phase p: [begin, end) of the phase's ng * nq units.
-struct PhaseUnits {
-    int begin, end;
-    int nq;   // chunks per row in the phase
-    int sb;   // first super-block of the phase
-    int nsb;  // super-blocks of the phase
+// Stage s of the CTA (phase p, group gi, chunk kc), in the order the
+// producer fills the ring and the consumers use it.
+struct StageCursor {
+    int p, gi, kc;
+    int sb, nsb;  // the phase's first super-block and its count
+    int nq;       // chunks per row in the phase
 };
 
-__device__ __forceinline__ PhaseUnits phase_units(const MmParams &P, int p, int ng, int warp) {
-    PhaseUnits r;
-    r.sb = p * P.nbp;
-    r.nsb = min(P.nbp, P.nb - r.sb);
-    r.nq = (r.nsb + P.CH - 1) / P.CH;
-    const int U = ng * r.nq;
-    r.begin = static_cast<int>((static_cast<int64_t>(U) * warp) / FW);
-    r.end = static_cast<int>((static_cast<int64_t>(U) * (warp + 1)) / FW);
-    return r;
+__device__ __forceinline__ void cursor_phase(const MmParams &P, StageCursor &c, int p) {
+    c.p = p;
+    c.gi = 0;
+    c.kc = 0;
+    c.sb = p * P.nbp;
+    c.nsb = min(P.nbp, P.nb - c.sb);
+    c.nq = (c.nsb + CHS - 1) / CHS;
+}
+
+__device__ __forceinline__ void cursor_next(const MmParams &P, StageCursor &c, int ng) {
+    if (++c.kc == c.nq) {
+        c.kc = 0;
+        if (++c.gi == ng) cursor_phase(P, c, c.p + 1);
+    }
 }
 
 template <int T>
-__global__ void __launch_bounds__(FTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ MmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int quad = lane & ~3;
 
     // this CTA's rows [r0, r1): whole 8-row halves; groups of 16 from r0
     const int cta = blockIdx.x;
@@ -372,94 +382,123 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     const int64_t r0 = 8 * h0;
     const int64_t r1 = min(P.N, 8 * (h0 + nh));
     const int ng = (nh + 1) / 2;
-
-    const uint32_t my_bar = smem_u32(smem) + 8u * warp * MAX_NS;
-    const uint32_t xbar = smem_u32(smem + OFF_XBAR);
-    int *edge_group = reinterpret_cast<int *>(smem + OFF_EDGE_GROUP);
-    volatile int *fail_flag = reinterpret_cast<volatile int *>(smem + OFF_FAIL);
-    float *edge_sum = reinterpret_cast<float *>(smem + OFF_EDGE_SUM);
-    float *table = reinterpret_cast<float *>(smem + P.off_table);
-    if (lane == 0) {
-        for (int i = 0; i < P.NS; ++i) mbar_init(my_bar + 8u * i, 1);
-        if (warp == 0) mbar_init(xbar, 1);
-        fence_mbar_init();
+    int total = 0;  // stages of the CTA
+    for (int p = 0; p < P.nphase; ++p) {
+        const int nsb = min(P.nbp, P.nb - p * P.nbp);
+        total += ng * ((nsb + CHS - 1) / CHS);
     }
-    if (lane < 2) edge_group[2 * warp + lane] = -1;
-    if (threadIdx.x == 0) *fail_flag = 0;
+
+    const uint32_t full0 = smem_u32(smem + OFF_FULL), empty0 = smem_u32(smem + OFF_EMPTY);
+    const uint32_t xbar = smem_u32(smem + OFF_XBAR);
+    volatile int *fail_flag = reinterpret_cast<volatile int *>(smem + OFF_FAIL);
+    float *part = reinterpret_cast<float *>(smem + OFF_PART);
+    float *table = reinterpret_cast<float *>(smem + P.off_table);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P.NS; ++i) {
+            mbar_init(full0 + 8u * i, 1);
+            mbar_init(empty0 + 8u * i, CW);
+        }
+        mbar_init(xbar, 1);
+        fence_mbar_init();
+        *fail_flag = 0;
+    }
     if (threadIdx.x < ZERO_BYTES / 16)
         reinterpret_cast<uint4 *>(smem + OFF_ZERO)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
     if (P.nphase > 1)
-        for (int i = threadIdx.x; i < ng * EDGE_FLOATS; i += FTHREADS) table[i] = 0.0f;
+        for (int i = threadIdx.x; i < ng * EDGE_FLOATS; i += NTHREADS) table[i] = 0.0f;
     __syncthreads();
-
-    const int ring = P.off_ring + warp * P.NS * P.slot_bytes;
-    const uint64_t pol_w = policy_evict_first();
-    auto group_rows = [&](int gi) {
-        const int64_t left = r1 - (r0 + GR * gi);
-        return left < GR ? static_cast<int>(left) : GR;
-    };
-    // unit u of phase r into `slot`
-    auto issue = [&](const PhaseUnits &r, int u, int slot) {
-        const int gi = u / r.nq, qi = u - gi * r.nq;
-        const int sb0 = r.sb + qi * P.CH, nsb = min(P.CH, r.sb + r.nsb - sb0);
-        const int64_t row0 = r0 + GR * gi;
-        const uint32_t bar = my_bar + 8u * slot;
-        const uint32_t dst = smem_u32(smem + ring + slot * P.slot_bytes);
-        if constexpr (T == QMM_Q4_K) {
-            // rows 0..7 of the group, and 8..15 when the CTA owns them (a
-            // CTA's rows end on a half or at N); the box is CH super-blocks
-            if (lane != 0) return;
-            const int boxes = r1 - row0 > 8 ? 2 : 1;
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(boxes * 8 * P.row_pitch));
-            for (int bx = 0; bx < boxes; ++bx)
-                tma_load_2d_hint(dst + bx * 8 * P.row_pitch, &tmW, sb0 * SB_WORDS, static_cast<int>(row0 + 8 * bx),
-                                 bar, pol_w);
-        } else {
-            // lane r copies row r's span rounded out to 16 bytes (never past
-            // the end of the matrix)
-            const int rows = group_rows(gi);
-            uint64_t src = 0;
-            uint32_t bytes = 0;
-            if (lane < rows) {
-                const uint64_t start = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(row0 + lane) * P.RB +
-                                       static_cast<uint64_t>(210) * sb0;
-                src = start & ~uint64_t(15);
-                uint64_t end = (start + static_cast<uint64_t>(210) * nsb + 15) & ~uint64_t(15);
-                if (end > P.w_end) end = P.w_end & ~uint64_t(15);
-                bytes = static_cast<uint32_t>(end - src);
-            }
-            const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
-            if (lane == 0) mbar_arrive_expect_tx(bar, total);
-            if (bytes > 0)
-                bulk_g2s(dst + lane * P.row_pitch, reinterpret_cast<const void *>(src), bytes, bar, pol_w);
-        }
-    };
-
-    // issue cursor over this warp's units in phase order
-    int ip = 0, iu = 0, issued = 0, islot = 0;
-    PhaseUnits ir = phase_units(P, 0, ng, warp);
-    iu = ir.begin;
-    auto issue_next = [&]() {
-        while (ip < P.nphase && iu >= ir.end) {
-            if (++ip < P.nphase) {
-                ir = phase_units(P, ip, ng, warp);
-                iu = ir.begin;
-            }
-        }
-        if (ip >= P.nphase) return;
-        issue(ir, iu, islot);
-        ++iu;
-        ++issued;
-        if (++islot == P.NS) islot = 0;
-    };
-
-    // the first stage of every warp before the wait for the quantiser (see
-    // the header); the others after the first activation copy, which would
-    // wait behind them in the copy engine otherwise
     pdl_trigger();
-    issue_next();
-    pdl_wait();
+    const uint64_t pol = policy_evict_first();
 
+    // the activation window of phase p (one thread): x rows, then the sums
+    auto load_x = [&](int p) {
+        const int K = P.K;
+        const int sb = p * P.nbp, nsb = min(P.nbp, P.nb - sb);
+        const uint32_t xb = static_cast<uint32_t>(512 * nsb);
+        const uint32_t xsb = static_cast<uint32_t>((T == QMM_Q4_K ? 32 : 512) * nsb);
+        mbar_arrive_expect_tx(xbar, P.M * xb + (T == QMM_Q4_K ? P.M : 1) * xsb);
+        const uint8_t *src_row = P.xh;
+        for (int m = 0; m < P.M; ++m, src_row += 2 * K + K / 8) {
+            const uint32_t dst = smem_u32(smem + P.off_x + m * P.x_ld);
+            bulk_g2s(dst, src_row + static_cast<int64_t>(512) * sb, xb, xbar, pol);
+            if (T == QMM_Q4_K)
+                bulk_g2s(dst + 512 * P.nbp, src_row + 2 * K + static_cast<int64_t>(32) * sb, xsb, xbar, pol);
+        }
+        if (T == QMM_Q6_K) bulk_g2s(smem_u32(smem + P.off_xs), P.xs16 + static_cast<int64_t>(512) * sb, xsb, xbar, pol);
+    };
+
+    if (warp == CW) {
+        // ---- producer: fills the ring in stage order --------------------
+        StageCursor c;
+        cursor_phase(P, c, 0);
+        for (int s = 0; s < total; ++s, cursor_next(P, c, ng)) {
+            const int slot = s % P.NS;
+            if (s >= P.NS) {
+                // the consumers' release of this slot's previous stage
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(empty0 + 8u * slot, static_cast<uint32_t>((s / P.NS - 1) & 1), P.status);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                    if (lane == 0) *fail_flag = 1;
+                    break;
+                }
+            }
+            const int sb0 = c.sb + c.kc * CHS, nsb = min(CHS, c.sb + c.nsb - sb0);
+            const int64_t row0 = r0 + GR * c.gi;
+            const uint32_t bar = full0 + 8u * slot;
+            const uint32_t dst = smem_u32(smem + P.off_ring) + slot * P.stage_bytes;
+            if constexpr (T == QMM_Q4_K) {
+                // rows 0..7 of the group, and 8..15 when the CTA owns them (a
+                // CTA's rows end on a half or at N); a box is 8 super-blocks
+                // and 16 bytes (rows 16 bytes past a 128-byte multiple apart)
+                if (lane == 0) {
+                    const int boxes = r1 - row0 > 8 ? 2 : 1;
+                    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(boxes * 8 * P.row_pitch));
+                    for (int bx = 0; bx < boxes; ++bx)
+                        tma_load_2d_hint(dst + bx * 8 * P.row_pitch, &tmW, sb0 * SB_WORDS,
+                                         static_cast<int>(row0 + 8 * bx), bar, pol);
+                }
+            } else {
+                // lane r copies row r's span rounded out to 16 bytes (never past
+                // the end of the matrix)
+                const int64_t left = r1 - row0;
+                const int rows = left < GR ? static_cast<int>(left) : GR;
+                uint64_t src = 0;
+                uint32_t bytes = 0;
+                if (lane < rows) {
+                    const uint64_t start = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(row0 + lane) * P.RB +
+                                           static_cast<uint64_t>(210) * sb0;
+                    src = start & ~uint64_t(15);
+                    uint64_t end = (start + static_cast<uint64_t>(210) * nsb + 15) & ~uint64_t(15);
+                    if (end > P.w_end) end = P.w_end & ~uint64_t(15);
+                    bytes = static_cast<uint32_t>(end - src);
+                }
+                const uint32_t all = __reduce_add_sync(0xffffffffu, bytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar, all);
+                if (bytes > 0)
+                    bulk_g2s(dst + lane * P.row_pitch, reinterpret_cast<const void *>(src), bytes, bar, pol);
+            }
+            if (s == 0) {
+                // the first stage before the wait for the quantiser (see the
+                // header); the activations next, the other stages after them
+                pdl_wait();
+                if (lane == 0) load_x(0);
+            }
+        }
+        if (total == 0) {
+            pdl_wait();
+            if (lane == 0) load_x(0);
+        }
+        // no copy may still be in flight when the CTA exits
+        if (lane == 0)
+            for (int s = max(0, total - P.NS); s < total; ++s)
+                mbar_wait(full0 + 8u * (s % P.NS), static_cast<uint32_t>((s / P.NS) & 1), P.status);
+        return;
+    }
+
+    // ---- consumers: warp w takes super-block (w + kc) mod 8 of each stage ---
+    pdl_wait();  // y is written after the kernels before the quantiser completed
+    const int g = lane >> 2, t = lane & 3;
+    const int quad = lane & ~3;
     // ldmatrix row addresses of this lane (it names row lane & 7 of matrix lane >> 3)
     const int lr = lane & 7, lm = lane >> 3;
     // Q4_K weights: matrices (rows 0-7 | 8-15) x (16-byte segment 2c | 2c + 1)
@@ -473,228 +512,132 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     const uint32_t xs_base = (tok_ok ? x_row + 512 * P.nbp : zero) + 16 * (lm & 1);
     const uint32_t x_step = tok_ok ? 512u : 0u, xs_step = tok_ok ? 32u : 0u;  // per super-block
     const float *xs16 = reinterpret_cast<const float *>(smem + P.off_xs);
+    const int tid = threadIdx.x;  // 0 .. 255
 
-    // rows g, g+8 of the current group x tokens 2t, 2t+1; two independent
-    // accumulator chains, c = c + c2
-    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int consumed = 0, slot = 0;
-    uint32_t phase = 0;
+    // an element of a group's 16 x 8 result in fragment order -> y
+    auto store_y = [&](int gi, int e, float v) {
+        const int ln = e >> 2, i = e & 3;
+        const int64_t row = r0 + GR * gi + (ln >> 2) + 8 * (i >> 1);
+        const int tk = 2 * (ln & 3) + (i & 1);
+        if (row < r1 && tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row] = v;
+    };
+
     bool failed = false;
-
-    // a group's complete result for the phase, in fragment order
-    auto store_y = [&](int gi, const float (&v)[4]) {
-        const int64_t row = r0 + GR * gi + g;
-        const int tk = 2 * t;
-        if (row < r1) {
-            if (tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row] = v[0];
-            if (tk + 1 < P.M) P.y[static_cast<int64_t>(tk + 1) * P.N + row] = v[1];
-        }
-        if (row + 8 < r1) {
-            if (tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row + 8] = v[2];
-            if (tk + 1 < P.M) P.y[static_cast<int64_t>(tk + 1) * P.N + row + 8] = v[3];
-        }
-    };
-    auto out = [&](int gi, const float (&v)[4]) {
-        if (P.nphase == 1) {
-            store_y(gi, v);
-        } else {
-            float *tb = table + gi * EDGE_FLOATS + 4 * lane;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) tb[i] += v[i];
-        }
-    };
-
+    int s = 0;
     for (int p = 0; p < P.nphase; ++p) {
-        const PhaseUnits cr = phase_units(P, p, ng, warp);
-        // the activation window of phase p
-        if (p > 0) __syncthreads();  // every warp is done with the previous window
-        if (threadIdx.x == 0 && *fail_flag == 0) {
-            if (p > 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            const int K = P.K;
-            const uint32_t xb = static_cast<uint32_t>(512 * cr.nsb);
-            const uint32_t xsb = static_cast<uint32_t>((T == QMM_Q4_K ? 32 : 512) * cr.nsb);
-            mbar_arrive_expect_tx(xbar, P.M * xb + (T == QMM_Q4_K ? P.M : 1) * xsb);
-            const uint8_t *src_row = P.xh;
-            for (int m = 0; m < P.M; ++m, src_row += 2 * K + K / 8) {
-                const uint32_t dst = smem_u32(smem + P.off_x + m * P.x_ld);
-                bulk_g2s(dst, src_row + static_cast<int64_t>(512) * cr.sb, xb, xbar, pol_w);
-                if (T == QMM_Q4_K)
-                    bulk_g2s(dst + 512 * P.nbp, src_row + 2 * K + static_cast<int64_t>(32) * cr.sb, xsb, xbar, pol_w);
-            }
-            if (T == QMM_Q6_K)
-                bulk_g2s(smem_u32(smem + P.off_xs), P.xs16 + static_cast<int64_t>(512) * cr.sb, xsb, xbar, pol_w);
-        }
-        if (p == 0) {
-            __syncthreads();  // the activation copy goes first
-            while (issued < P.NS && !(ip >= P.nphase)) issue_next();
-        }
-        if (!__all_sync(0xffffffffu, mbar_wait(xbar, static_cast<uint32_t>(p & 1), P.status))) {
-            failed = true;
-            if (lane == 0) *fail_flag = 1;
-        }
-
-        int cur = -1, cur_first = 0;
-        for (int u = cr.begin; u < cr.end; ++u) {
-            if (failed) continue;
-            // every lane waits; the warp goes on only if all of them saw the stage
-            if (!__all_sync(0xffffffffu, mbar_wait(my_bar + 8u * slot, phase, P.status))) {
-                failed = true;
-                if (lane == 0) *fail_flag = 1;
-                continue;
-            }
-            ++consumed;
-            const int gi = u / cr.nq, qi = u - gi * cr.nq;
-            if (gi != cur) {
-                cur = gi;
-                cur_first = qi == 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) c[i] = c2[i] = 0.0f;
-            }
-            const int sb0 = cr.sb + qi * P.CH, nsb = min(P.CH, cr.sb + cr.nsb - sb0);
-            const uint8_t *st = smem + ring + slot * P.slot_bytes;
-            if constexpr (T == QMM_Q4_K) {
-                const uint32_t a_stage = smem_u32(st) + a_off;
-#pragma unroll 1
-                for (int s = 0; s < nsb; ++s) {
-                    const int kw = sb0 + s - cr.sb;  // super-block inside the window
-                    q4k_superblock(a_stage + 144 * s, st + g * P.row_pitch + 144 * s,
-                                   st + (g + 8) * P.row_pitch + 144 * s, x_base + kw * x_step,
-                                   xs_base + kw * xs_step, t, quad, c, c2);
-                }
-            } else {
-                // the data of rows g and g+8 start at their byte offsets inside the copies
-                const int64_t row0 = r0 + GR * gi;
-                const uint64_t base = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(210) * sb0;
-                const int oa = static_cast<int>((base + static_cast<uint64_t>(row0 + g) * P.RB) & 15);
-                const int ob = static_cast<int>((base + static_cast<uint64_t>(row0 + g + 8) * P.RB) & 15);
-                // the matrix's last bytes, not copied: loaded here
-                if (row0 + group_rows(gi) == P.N && sb0 + nsb == P.nb && (P.w_end & 15) != 0) {
-                    const int rl = static_cast<int>(P.N - 1 - row0);
-                    const uint64_t start = base + static_cast<uint64_t>(P.N - 1) * P.RB;
-                    const uint64_t copied = (P.w_end & ~uint64_t(15)) - (start & ~uint64_t(15));
-                    const int tail = static_cast<int>(P.w_end & 15);
-                    if (lane < tail / 4) {
-                        const uint32_t v = __ldg(reinterpret_cast<const unsigned int *>((P.w_end & ~uint64_t(15)) + 4 * lane));
-                        *reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(st) + rl * P.row_pitch + copied + 4 * lane) = v;
-                    }
-                    __syncwarp();
-                }
-                const uint8_t *ra = st + g * P.row_pitch + oa;
-                const uint8_t *rb = st + (g + 8) * P.row_pitch + ob;
-#pragma unroll 1
-                for (int s = 0; s < nsb; s += 2) {
-                    const int kw = sb0 + s - cr.sb;
-                    q6k_superblock<false>(ra + 210 * s, rb + 210 * s, x_base + kw * x_step, xs16 + kw * 128, t,
-                                          quad, c, c2);
-                    if (s + 1 < nsb)
-                        q6k_superblock<true>(ra + 210 * (s + 1), rb + 210 * (s + 1), x_base + (kw + 1) * x_step,
-                                             xs16 + (kw + 1) * 128, t, quad, c, c2);
-                }
-            }
-            __syncwarp();
-            if (!(ip >= P.nphase)) {
-                // the slot just read is refilled: order the reads before the async write
+        StageCursor c;
+        cursor_phase(P, c, p);
+        if (p > 0) {
+            // every consumer is done with the previous window
+            named_barrier(1, CW * 32);
+            if (tid == 0 && *fail_flag == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue_next();
-            }
-            if (++slot == P.NS) slot = 0, phase ^= 1u;
-            // the group ends here for this warp in this phase
-            if (u == cr.end - 1 || (u + 1) / cr.nq != gi) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) c[i] += c2[i];
-                if (cur_first && qi == cr.nq - 1) {
-                    out(gi, c);
-                } else {
-                    const int e = 2 * warp + (gi == cr.begin / cr.nq ? 0 : 1);
-                    if (lane == 0) edge_group[e] = gi;
-                    *reinterpret_cast<float4 *>(edge_sum + e * EDGE_FLOATS + 4 * lane) =
-                        make_float4(c[0], c[1], c[2], c[3]);
-                }
+                load_x(p);
             }
         }
-        // groups of this phase cut by warp boundaries: records e = 2w + {0, 1}
-        // in warp order; the first record of a group adds the others in order
-        __syncthreads();
-        if (*fail_flag == 0) {
-            for (int e = warp; e < 2 * FW; e += FW) {
-                const int gi = edge_group[e];
-                if (gi < 0) continue;
-                bool first = true;
-                for (int f = 0; f < e; ++f) first = first && edge_group[f] != gi;
-                if (!first) continue;
-                float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                for (int f = e; f < 2 * FW; ++f)
-                    if (edge_group[f] == gi) {
-                        const float4 v = *reinterpret_cast<const float4 *>(edge_sum + f * EDGE_FLOATS + 4 * lane);
-                        s[0] += v.x;
-                        s[1] += v.y;
-                        s[2] += v.z;
-                        s[3] += v.w;
+        if (!failed && !__all_sync(0xffffffffu, mbar_wait(xbar, static_cast<uint32_t>(p & 1), P.status)))
+            failed = true;
+        for (int gi = 0; gi < ng; ++gi) {
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int kc = 0; kc < c.nq; ++kc, ++s) {
+                const int slot = s % P.NS;
+                if (!failed && !__all_sync(0xffffffffu, mbar_wait(full0 + 8u * slot,
+                                                                    static_cast<uint32_t>((s / P.NS) & 1), P.status)))
+                    failed = true;
+                const int sb0 = c.sb + kc * CHS, nsb = min(CHS, c.sb + c.nsb - sb0);
+                const int idx = (warp + kc) & (CHS - 1);
+                const uint8_t *st = smem + P.off_ring + slot * P.stage_bytes;
+                if (!failed && idx < nsb) {
+                    const int kw = sb0 + idx - c.sb;  // super-block inside the window
+                    if constexpr (T == QMM_Q4_K) {
+                        q4k_superblock(smem_u32(st) + a_off + 144 * idx, st + g * P.row_pitch + 144 * idx,
+                                       st + (g + 8) * P.row_pitch + 144 * idx, x_base + kw * x_step,
+                                       xs_base + kw * xs_step, t, quad, acc, acc2);
+                    } else {
+                        const int64_t row0 = r0 + GR * gi;
+                        const uint64_t base = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(210) * sb0;
+                        const int oa = static_cast<int>((base + static_cast<uint64_t>(row0 + g) * P.RB) & 15);
+                        const int ob = static_cast<int>((base + static_cast<uint64_t>(row0 + g + 8) * P.RB) & 15);
+                        // the matrix's last bytes, not copied: loaded here by the
+                        // warp that reads them (the last row's last super-block)
+                        if (sb0 + idx == P.nb - 1 && r1 == P.N && row0 + GR >= P.N && (P.w_end & 15) != 0) {
+                            const int rl = static_cast<int>(P.N - 1 - row0);
+                            const uint64_t start = base + static_cast<uint64_t>(P.N - 1) * P.RB;
+                            const uint64_t copied = (P.w_end & ~uint64_t(15)) - (start & ~uint64_t(15));
+                            const int tail = static_cast<int>(P.w_end & 15);
+                            if (lane < tail / 4) {
+                                const uint32_t v = __ldg(reinterpret_cast<const unsigned int *>(
+                                    (P.w_end & ~uint64_t(15)) + 4 * lane));
+                                *reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(st) + rl * P.row_pitch + copied +
+                                                              4 * lane) = v;
+                            }
+                            __syncwarp();
+                        }
+                        const uint8_t *ra = st + g * P.row_pitch + oa + 210 * idx;
+                        const uint8_t *rb = st + (g + 8) * P.row_pitch + ob + 210 * idx;
+                        if (idx & 1)
+                            q6k_superblock<true>(ra, rb, x_base + kw * x_step, xs16 + kw * 128, t, quad, acc, acc2);
+                        else
+                            q6k_superblock<false>(ra, rb, x_base + kw * x_step, xs16 + kw * 128, t, quad, acc, acc2);
                     }
-                out(gi, s);
+                }
+                // this warp is done with the stage
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+            }
+            // the group's phase result: the warps' partial sums added in warp order
+            float *pb = part + (gi & 1) * (CW * EDGE_FLOATS);
+            *reinterpret_cast<float4 *>(pb + warp * EDGE_FLOATS + 4 * lane) =
+                make_float4(acc[0] + acc2[0], acc[1] + acc2[1], acc[2] + acc2[2], acc[3] + acc2[3]);
+            if (failed && lane == 0) *fail_flag = 1;
+            named_barrier(2, CW * 32);
+            if (tid < EDGE_FLOATS && *fail_flag == 0) {
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < CW; ++w) v += pb[w * EDGE_FLOATS + tid];
+                if (P.nphase == 1) store_y(gi, tid, v);
+                else table[gi * EDGE_FLOATS + tid] += v;
             }
         }
-        __syncthreads();
-        if (lane < 2) edge_group[2 * warp + lane] = -1;
     }
-    // no bulk copy may still be in flight when the CTA exits
-    if (lane == 0)
-        for (int k = consumed; k < issued; ++k)
-            mbar_wait(my_bar + 8u * (k % P.NS), static_cast<uint32_t>((k / P.NS) & 1), P.status);
-    if (threadIdx.x == 0) mbar_wait(xbar, static_cast<uint32_t>((P.nphase - 1) & 1), P.status);
-    __syncthreads();
-    if (*fail_flag != 0 || P.nphase == 1) return;
-    for (int gi = warp; gi < ng; gi += FW) {
-        const float *tb = table + gi * EDGE_FLOATS + 4 * lane;
-        const float v[4] = {tb[0], tb[1], tb[2], tb[3]};
-        store_y(gi, v);
-    }
+    if (tid == 0 && P.nphase > 0) mbar_wait(xbar, static_cast<uint32_t>((P.nphase - 1) & 1), P.status);
+    if (P.nphase == 1) return;
+    named_barrier(1, CW * 32);
+    if (*fail_flag != 0) return;
+    for (int e = tid; e < ng * EDGE_FLOATS; e += CW * 32) store_y(e / EDGE_FLOATS, e % EDGE_FLOATS, table[e]);
 }
 
 // Shared-memory plan: head | activation window [M][x_ld] | Q6_K group sums
-// window | phase table | FW rings of NS slots of GR rows.  The fewest phases
-// that fit; within them the widest chunk that leaves two stages per warp and,
-// when there is a choice, at least three units per warp.
+// window | phase table | ring of NS stages of GR rows x 8 super-blocks.  The
+// fewest phases that fit with at least two stages.
 struct Plan {
-    int CH, NS, nphase, nbp, x_ld, row_pitch, slot_bytes, off_x, off_xs, off_table, off_ring, smem;
+    int NS, nphase, nbp, x_ld, row_pitch, stage_bytes, off_x, off_xs, off_table, off_ring, smem;
 };
 
 template <int T>
 bool plan_mm(int M, int64_t K, int64_t max_groups, int max_smem, Plan &pl) {
-    using C = Mm<T>;
     const int nb = static_cast<int>(K / 256);
+    const int pitch = T == QMM_Q4_K ? Q4K_PITCH : Q6K_PITCH;
+    const int64_t stage = static_cast<int64_t>(GR) * pitch;
     for (int P = 1; P <= MAX_PHASES; ++P) {
-        int best = -1;
-        Plan cand = {};
-        for (int ci = 0; ci < C::NCH; ++ci) {
-            const int ch = C::CHS[ci];
-            int nbp = nb;
-            if (P > 1) {
-                nbp = (nb + P - 1) / P;
-                nbp = (nbp + ch - 1) / ch * ch;
-                if (static_cast<int64_t>(nbp) * (P - 1) >= nb) continue;  // an empty last phase
-            }
-            const int64_t x_ld = (static_cast<int64_t>(nbp) * (512 + C::XS_TOKEN) + 127) / 128 * 128 + 16;
-            const int64_t o_x = (HEAD + 127) / 128 * 128;
-            const int64_t o_xs = (o_x + M * x_ld + 127) / 128 * 128;
-            const int64_t o_table = o_xs + (T == QMM_Q6_K ? static_cast<int64_t>(nbp) * 512 : 0);
-            const int64_t o_ring = (o_table + (P > 1 ? max_groups * EDGE_FLOATS * 4 : 0) + 127) / 128 * 128;
-            const int pitch = T == QMM_Q4_K ? 144 * ch : ((210 * ch + 26 + 15) / 16 | 1) * 16;
-            const int64_t slot = static_cast<int64_t>(GR) * pitch;
-            int64_t ns = (max_smem - o_ring) / (FW * slot);
-            if (ns < 2) continue;
-            if (ns > MAX_NS) ns = MAX_NS;
-            cand = {ch, static_cast<int>(ns), P, nbp, static_cast<int>(x_ld), pitch, static_cast<int>(slot),
-                    static_cast<int>(o_x), static_cast<int>(o_xs), static_cast<int>(o_table),
-                    static_cast<int>(o_ring), static_cast<int>(o_ring + FW * ns * slot)};
-            best = ci;
-            const int64_t units = max_groups * ((nbp + ch - 1) / ch) * P;
-            if (max_groups <= 0 || units >= 3 * FW) break;
+        int nbp = nb;
+        if (P > 1) {
+            nbp = (nb + P - 1) / P;
+            nbp = (nbp + CHS - 1) / CHS * CHS;
+            if (static_cast<int64_t>(nbp) * (P - 1) >= nb) continue;  // an empty last phase
         }
-        if (best >= 0) {
-            pl = cand;
-            return true;
-        }
+        const int64_t x_ld = (static_cast<int64_t>(nbp) * (512 + Mm<T>::XS_TOKEN) + 127) / 128 * 128 + 16;
+        const int64_t o_x = HEAD;
+        const int64_t o_xs = (o_x + M * x_ld + 127) / 128 * 128;
+        const int64_t o_table = o_xs + (T == QMM_Q6_K ? static_cast<int64_t>(nbp) * 512 : 0);
+        const int64_t o_ring = (o_table + (P > 1 ? max_groups * EDGE_FLOATS * 4 : 0) + 127) / 128 * 128;
+        int64_t ns = (max_smem - o_ring) / stage;
+        if (ns < 2) continue;
+        if (ns > MAX_NS) ns = MAX_NS;
+        pl = {static_cast<int>(ns), P, nbp, static_cast<int>(x_ld), pitch, static_cast<int>(stage),
+              static_cast<int>(o_x), static_cast<int>(o_xs), static_cast<int>(o_table), static_cast<int>(o_ring),
+              static_cast<int>(o_ring + ns * stage)};
+        return true;
     }
     return false;
 }
@@ -735,7 +678,8 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     if (!ok) return cudaErrorNotSupported;
     const int nb = static_cast<int>(K / 256);
     const int bb = type == QMM_Q4_K ? Mm<QMM_Q4_K>::BB : Mm<QMM_Q6_K>::BB;
-    if (mg * ((nb + pl.CH - 1) / pl.CH) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    // a CTA's stages count in int
+    if (mg * ((nb + CHS - 1) / CHS + pl.nphase) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     MmParams P = {};
     P.W = static_cast<const uint8_t *>(W);
     P.RB = static_cast<int64_t>(nb) * bb;
@@ -754,8 +698,7 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     P.x_ld = pl.x_ld;
     P.y = y;
     P.NS = pl.NS;
-    P.slot_bytes = pl.slot_bytes;
-    P.CH = pl.CH;
+    P.stage_bytes = pl.stage_bytes;
     P.row_pitch = pl.row_pitch;
     P.off_x = pl.off_x;
     P.off_xs = pl.off_xs;
@@ -764,10 +707,11 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     P.status = status;
     CUtensorMap tmW = {};
     if (type == QMM_Q4_K) {
-        // the weights as 8-byte elements [N][18 * nb]: boxes of CH super-blocks x 8 rows
+        // the weights as 8-byte elements [N][18 * nb]: boxes of 8 super-blocks
+        // and 2 elements (the next header, or zeros past the row end) x 8 rows
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb) * SB_WORDS, static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * 144};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(pl.CH * SB_WORDS), 8u};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(Q4K_PITCH / 8), 8u};
         const cuuint32_t es[2] = {1, 1};
         if (tensor_map_encoder()(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), dims, strides, box,
                                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -779,7 +723,7 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(FTHREADS);
+    cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

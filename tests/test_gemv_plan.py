@@ -291,12 +291,10 @@ def test_group_split_covers_every_matrix(group):
 
 
 # ---- the tensor-core decode kernel for 2 <= M <= 8 (gemv_mma.cu) ----------
-MM_W, MM_GR, MM_MAXNS, MM_MAXP = 8, 16, 4, 8
-MM_HEAD = 1152 + 2 * MM_W * 128 * 4  # barriers, groups, flag | zeros | edge sums
-
-
-def mm_pitch(qtype, ch):
-    return 144 * ch if qtype == synth.Q4_K else (((210 * ch + 41) // 16) | 1) * 16
+MM_CW, MM_GR, MM_CHS, MM_MAXNS, MM_MAXP = 8, 16, 8, 6, 8
+MM_HEAD = 1152 + 2 * MM_CW * 128 * 4  # barriers, flag | zeros | partial sums
+Q4K_PITCH = 8 * 144 + 16
+Q6K_PITCH = (((8 * 210 + 41) // 16) | 1) * 16
 
 
 def mm_max_groups(N):
@@ -307,36 +305,28 @@ def mm_max_groups(N):
 
 def plan_mm(qtype, M, K, max_groups=0):
     nb = K // 256
-    chs = (5, 3, 1) if qtype == synth.Q4_K else (4, 2)
-    xs_token = 32 if qtype == synth.Q4_K else 0
     if qtype == synth.Q6_K and nb % 2:
         return None
+    pitch = Q4K_PITCH if qtype == synth.Q4_K else Q6K_PITCH
+    xs_token = 32 if qtype == synth.Q4_K else 0
+    stage = MM_GR * pitch
     for P in range(1, MM_MAXP + 1):
-        best = None
-        for ch in chs:
-            nbp = nb
-            if P > 1:
-                nbp = -(-nb // P)
-                nbp = -(-nbp // ch) * ch
-                if nbp * (P - 1) >= nb:
-                    continue
-            x_ld = align(nbp * (512 + xs_token), 128) + 16
-            o_x = align(MM_HEAD, 128)
-            o_xs = align(o_x + M * x_ld, 128)
-            o_table = o_xs + (nbp * 512 if qtype == synth.Q6_K else 0)
-            o_ring = align(o_table + (max_groups * 512 if P > 1 else 0), 128)
-            pitch = mm_pitch(qtype, ch)
-            slot = MM_GR * pitch
-            ns = (SMEM_MAX - o_ring) // (MM_W * slot)
-            if ns < 2:
+        nbp = nb
+        if P > 1:
+            nbp = -(-(-(-nb // P)) // MM_CHS) * MM_CHS
+            if nbp * (P - 1) >= nb:
                 continue
-            ns = min(MM_MAXNS, ns)
-            best = dict(CH=ch, NS=ns, P=P, nbp=nbp, x_ld=x_ld, pitch=pitch, slot=slot, off_x=o_x,
-                        off_xs=o_xs, off_table=o_table, ring=o_ring, smem=o_ring + MM_W * ns * slot)
-            if max_groups <= 0 or max_groups * -(-nbp // ch) * P >= 3 * MM_W:
-                break
-        if best:
-            return best
+        x_ld = align(nbp * (512 + xs_token), 128) + 16
+        o_x = MM_HEAD
+        o_xs = align(o_x + M * x_ld, 128)
+        o_table = o_xs + (nbp * 512 if qtype == synth.Q6_K else 0)
+        o_ring = align(o_table + (max_groups * 512 if P > 1 else 0), 128)
+        ns = (SMEM_MAX - o_ring) // stage
+        if ns < 2:
+            continue
+        ns = min(MM_MAXNS, ns)
+        return dict(NS=ns, P=P, nbp=nbp, x_ld=x_ld, pitch=pitch, stage=stage, off_x=o_x, off_xs=o_xs,
+                    off_table=o_table, ring=o_ring, smem=o_ring + ns * stage)
     return None
 
 
@@ -344,35 +334,31 @@ def check_mm(qtype, N, K, M):
     mg, halves, grid = mm_max_groups(N)
     P = plan_mm(qtype, M, K, mg)
     assert P is not None and P["smem"] <= SMEM_MAX
-    CH, pitch, nbp, nph = P["CH"], P["pitch"], P["nbp"], P["P"]
+    pitch, nbp, nph, stage = P["pitch"], P["nbp"], P["P"], P["stage"]
     nb = K // 256
-    BB = synth.BLOCK_BYTES[qtype]
-    RB = nb * BB
+    RB = nb * synth.BLOCK_BYTES[qtype]
     w_end = N * RB            # the matrix at address 0 (16-byte aligned)
     assert P["x_ld"] % 128 == 16 and P["off_x"] % 128 == 0 and P["off_x"] >= MM_HEAD
-    assert P["ring"] % 128 == 0 and P["slot"] % 16 == 0
+    assert P["ring"] % 128 == 0 and stage % 128 == 0
     # an ldmatrix reads 16 bytes of 8 consecutive rows: 8 distinct bank groups
     assert len({(r * pitch // 16) % 8 for r in range(8)}) == 8
     if qtype == synth.Q4_K:
-        assert CH % 2 == 1 and 18 * CH <= 256 and P["slot"] % 128 == 0 and (8 * pitch) % 128 == 0
+        assert pitch % 16 == 0 and (pitch // 8) <= 256 and (8 * pitch) % 128 == 0
     else:
-        assert CH % 2 == 0 and nb % 2 == 0 and pitch >= 210 * CH + 26
+        assert nb % 2 == 0 and pitch >= 210 * MM_CHS + 26
     if nph > 1:
-        assert nbp % CH == 0 and nbp * (nph - 1) < nb
+        assert nbp % MM_CHS == 0 and nbp * (nph - 1) < nb
     row_bytes = 2 * K + K // 8   # quantiser output per token; then [K/16][8] fp32 sums
-    xs16_at = M * row_bytes
     for p in range(nph):
         sb, nsb = p * nbp, min(nbp, nb - p * nbp)
         assert nsb > 0
-        # the window copies: 16-byte sizes and sources, inside their buffers
         xb = 512 * nsb
         assert xb % 16 == 0 and 512 * sb + xb <= 2 * K and xb <= P["x_ld"]
         if qtype == synth.Q4_K:
             assert 2 * K + 32 * sb + 32 * nsb <= row_bytes and 512 * nbp + 32 * nsb + 16 <= P["x_ld"]
             tx = M * xb + M * 32 * nsb
         else:
-            # the group sums [K/16][8] fp32: 512 bytes per super-block, 2K bytes in all
-            assert xs16_at % 16 == 0 and 512 * sb + 512 * nsb <= 2 * K
+            assert (M * row_bytes) % 16 == 0 and 512 * sb + 512 * nsb <= 2 * K
             assert P["off_xs"] % 128 == 0 and P["off_xs"] + 512 * nsb <= P["off_table"]
             tx = M * xb + 512 * nsb
         assert tx < 2 ** 20
@@ -386,42 +372,46 @@ def check_mm(qtype, N, K, M):
         assert ng <= mg
         for p in range(nph):
             sbp, nsbp = p * nbp, min(nbp, nb - p * nbp)
-            nq = -(-nsbp // CH)
-            U = ng * nq
-            for w in range(MM_W):
-                b, e = U * w // MM_W, U * (w + 1) // MM_W
-                for u in range(b, e):
-                    gi, qi = divmod(u, nq)
-                    sb0 = sbp + qi * CH
-                    nsb = min(CH, sbp + nsbp - sb0)
-                    row0 = r0 + MM_GR * gi
-                    rows = min(MM_GR, r1 - row0)
-                    assert 1 <= rows <= MM_GR and nsb >= 1
+            nq = -(-nsbp // MM_CHS)
+            for gi in range(ng):
+                row0 = r0 + MM_GR * gi
+                rows = min(MM_GR, r1 - row0)
+                assert 1 <= rows <= MM_GR
+                for kc in range(nq):
+                    sb0 = sbp + kc * MM_CHS
+                    nsb = min(MM_CHS, sbp + nsbp - sb0)
+                    assert nsb >= 1
                     if qtype == synth.Q4_K:
                         boxes = 2 if r1 - row0 > 8 else 1
-                        assert (18 * sb0 * 8) % 16 == 0
-                        assert row0 + 8 * boxes >= min(r1, row0 + 16) and (boxes == 1 or row0 + 16 <= r1 or r1 == N)
-                        assert 15 * pitch + 144 * (nsb - 1) + 16 + 16 * 7 + 16 <= P["slot"]
+                        assert (sb0 * 144) % 16 == 0 and boxes * 8 * pitch < 2 ** 20
+                        # the boxes load rows [row0, row0 + 8*boxes): every one this CTA
+                        # owns, none of another CTA's (rows past N arrive as zeros)
+                        assert row0 + 8 * boxes >= row0 + rows and (boxes == 1 or row0 + 16 <= r1 or r1 == N)
+                        assert 15 * pitch + 144 * (MM_CHS - 1) + 16 + 16 * 7 + 16 <= stage
                     else:
+                        total = 0
                         for rr in range(rows):
                             start = (row0 + rr) * RB + 210 * sb0
                             src = start & ~15
                             end = min((start + 210 * nsb + 15) & ~15, w_end & ~15)
                             nbytes = end - src
+                            total += nbytes
                             assert nbytes > 0 and nbytes % 16 == 0 and src % 16 == 0
                             assert src >= 0 and end <= w_end
-                            assert rr * pitch + nbytes <= P["slot"]
+                            assert rr * pitch + nbytes <= stage
                             oa = start & 15
                             assert oa % 4 == 0        # even super-blocks 4-byte aligned
                             data_end = oa + 210 * nsb
                             tail = (src + data_end) - end   # bytes loaded after the wait
                             if tail > 0:
                                 assert row0 + rr == N - 1 and sb0 + nsb == nb and tail == (w_end & 15)
-                                assert tail % 4 == 0 and rr * pitch + nbytes + tail <= P["slot"]
-                            assert rr * pitch + data_end <= P["slot"]
-                    for rr in range(rows):
-                        for s in range(nsb):
-                            key = (row0 + rr, sb0 + s)
+                                assert r1 == N and row0 + MM_GR >= N
+                                assert tail % 4 == 0 and rr * pitch + nbytes + tail <= stage
+                            assert rr * pitch + data_end <= stage
+                        assert total < 2 ** 20
+                    for idx in range(nsb):
+                        for rr in range(rows):
+                            key = (row0 + rr, sb0 + idx)
                             assert key not in covered
                             covered.add(key)
     assert len(covered) == N * nb
