@@ -88,8 +88,8 @@ QMM_API int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *ou
  *   x        : device, M*K floats row-major (the activations).
  *   M        : activation rows.  M <= 8 runs the decode GEMV (weights
  *              streamed once through shared memory by bulk async copies;
- *              dp4a dot products, or for Q4_K at 2 <= M <= 8 mma.sync on
- *              sixteen weight rows dequantised to fp16 at a time, fp32
+ *              dp4a dot products, or for Q4_K / Q6_K from M = 3 mma.sync on
+ *              sixteen weight rows at a time, fp16 operands and fp32
  *              accumulation); M > 8 runs the prefill GEMM.
  *   y        : device, M*N floats, overwritten.
  *   stream   : cudaStream_t to run on (NULL = legacy default stream).
@@ -115,12 +115,13 @@ QMM_API int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const floa
  *                W 16-byte aligned, K a multiple of every type's QK; an entry
  *                with N = 0 is skipped.
  *   K, x, M, stream : shared by all entries, as in qmm().
- * With M = 1 (and with M <= 8 when no entry is Q4_K) the whole group is ONE
- * launch of the block-per-lane decode kernel: its CTAs are split between the
- * matrices in proportion to their weight bytes and each quantises x itself.
- * Otherwise (Q4_K entries at 2 <= M <= 8 run on the tensor-core decode
- * kernel, or a matrix does not fit that kernel) the products run one after
- * another as qmm() calls.  Accuracy as qmm().
+ * When every entry takes the block-per-lane decode kernel (M = 1, M = 2,
+ * see qmm_set_decode_path) the whole group is ONE launch of it: its CTAs are
+ * split between the matrices in proportion to their weight bytes and each
+ * quantises x itself.  When every entry takes the tensor-core decode kernel
+ * (Q4_K / Q6_K at QMM_TENSOR_MIN_M <= M <= 8) x is quantised once and each
+ * matrix is one decode launch.  Otherwise the products run one after another
+ * as qmm() calls.  Accuracy as qmm().
  * Every entry is validated before anything is launched; errors as qmm(),
  * QMM_EINVAL_SHAPE for n out of range, QMM_EINVAL_PTR for a null array.
  */
@@ -189,13 +190,14 @@ QMM_API int64_t qmm_launch_count(void);
 /*
  * qmm_set_decode_path -- which kernel qmm() and qmm_group() use for the
  * decode product (M <= 8), process-wide, for every later call:
- *   QMM_DECODE_AUTO   : chosen by type and M (default).  Q4_K with
- *                       QMM_TENSOR_MIN_M <= M <= 8 runs on the tensor-core
+ *   QMM_DECODE_AUTO   : chosen by type and M (default).  Q4_K and Q6_K with
+ *                       QMM_TENSOR_MIN_M <= M <= 8 run on the tensor-core
  *                       decode kernel (quantiser + mma.sync, two launches),
  *                       everything else on the block-per-lane dp4a kernel.
  *   QMM_DECODE_BLOCK  : the block-per-lane kernel wherever it fits.
- *   QMM_DECODE_TENSOR : the tensor-core kernel for every Q4_K product with
- *                       2 <= M <= 8 that fits it.
+ *   QMM_DECODE_TENSOR : the tensor-core kernel for every Q4_K / Q6_K product
+ *                       with 2 <= M <= 8 that fits it (Q6_K: K a multiple
+ *                       of 512).
  * Results of the paths agree within the accuracy bound of qmm(), not bit
  * for bit.  Returns the previous path, or QMM_EINVAL_SHAPE for an unknown
  * value (nothing changes).  Needs no GPU.
@@ -203,7 +205,7 @@ QMM_API int64_t qmm_launch_count(void);
 #define QMM_DECODE_AUTO 0
 #define QMM_DECODE_BLOCK 1
 #define QMM_DECODE_TENSOR 2
-#define QMM_TENSOR_MIN_M 4
+#define QMM_TENSOR_MIN_M 3
 QMM_API int qmm_set_decode_path(int path);
 
 #ifdef __cplusplus

@@ -134,6 +134,25 @@ int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
 }  // namespace qk
 
 namespace {
+// The quantiser for the tensor-core decode: fp16 d*q in fragment order and
+// the block and group sums into the workspace ([M][2K + K/8 bytes] |
+// [K/16][8] fp32), launched so that the decode kernels after it (programmatic
+// dependent launch) stream weights while it runs.
+int quantize_for_tensor_cores(int dev, cudaStream_t st, const float *x, int64_t M, int64_t K, const DeviceInfo &di,
+                              void **ws) {
+    const size_t xh_bytes = static_cast<size_t>(M * (K + K / 16)) * 2;
+    if (int rc = workspace(dev, st, align_up(xh_bytes + static_cast<size_t>(K) * 2, 256), ws)) return rc;
+    qk::QuantOut o = {};
+    o.xh = *ws;
+    o.xh_ld = K + K / 16;
+    o.xh_mma = 1;
+    o.xs16 = reinterpret_cast<float *>(static_cast<char *>(*ws) + xh_bytes);
+    cudaError_t e = qk::launch_quantize(x, M, K, o, st, true, di.num_sms, true);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    g_launches.fetch_add(1);
+    return QMM_OK;
+}
+
 // The decode product of this type and shape runs on the tensor-core kernel.
 bool decode_on_tensor_cores(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo &di) {
     if (M < 2 || M > 8 || g_force_round_gemv) return false;
@@ -258,20 +277,8 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     //   gemm : prefill after the quantiser: Q4_K on tcgen05 (fp16 operands,
     //          fp32 accumulators), other types on the int8 mma.sync kernel
     if (decode_on_tensor_cores(type, M, N, K, di)) {
-        // the quantiser writes fp16 d*q in fragment order and the sums; the
-        // decode kernel (programmatic dependent launch) streams weights while
-        // it runs.  Workspace: [M][2K + K/8 bytes] | [K/16][8] fp32
         void *ws = nullptr;
-        const size_t xh_bytes = static_cast<size_t>(M * (K + K / 16)) * 2;
-        if (int rc = workspace(dev, st, align_up(xh_bytes + static_cast<size_t>(K) * 2, 256), &ws)) return rc;
-        qk::QuantOut o = {};
-        o.xh = ws;
-        o.xh_ld = K + K / 16;
-        o.xh_mma = 1;
-        o.xs16 = reinterpret_cast<float *>(static_cast<char *>(ws) + xh_bytes);
-        e = qk::launch_quantize(x, M, K, o, st, true, di.num_sms, true);
-        if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
-        g_launches.fetch_add(1);
+        if (int rc = quantize_for_tensor_cores(dev, st, x, M, K, di, &ws)) return rc;
         e = qk::launch_gemv_mma(type, W_blocks, N, K, ws, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
                                 di.status);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core gemv launch");
@@ -382,6 +389,24 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
                                          static_cast<cudaStream_t>(stream), di.num_sms, di.max_smem, di.status);
             if (e != cudaSuccess) return cuda_fail(e, "group gemv launch");
             g_launches.fetch_add(1);
+            return QMM_OK;
+        }
+        // every entry on the tensor-core kernel: x quantised once, then one
+        // decode launch per matrix (each later one starts as the one before
+        // it starts, so it streams its weights meanwhile)
+        bool tensor = true;
+        for (int i = 0; i < n; ++i) tensor = tensor && (Ns[i] == 0 || decode_on_tensor_cores(types[i], M, Ns[i], K, di));
+        if (tensor) {
+            cudaStream_t st = static_cast<cudaStream_t>(stream);
+            void *ws = nullptr;
+            if (int rc = quantize_for_tensor_cores(dev, st, x, M, K, di, &ws)) return rc;
+            for (int i = 0; i < n; ++i) {
+                if (Ns[i] == 0) continue;
+                e = qk::launch_gemv_mma(types[i], Ws[i], Ns[i], K, ws, static_cast<int>(M), ys[i], st, di.num_sms,
+                                        di.max_smem, di.status);
+                if (e != cudaSuccess) return cuda_fail(e, "tensor-core gemv launch");
+                g_launches.fetch_add(1);
+            }
             return QMM_OK;
         }
     }

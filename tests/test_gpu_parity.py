@@ -267,7 +267,7 @@ MIXED = [(synth.Q4_K, 5), (synth.Q6_K, 0), (synth.Q6_K, 3000), (synth.Q8_0, 1), 
 
 
 @pytest.mark.parametrize("group,K,M", [(QWEN_QKV, 5120, 1), (QWEN_QKV, 5120, 4), (QWEN_GATE_UP, 5120, 1),
-                                       (MIXED, 1024, 2), (MIXED, 1024, 16)])
+                                       (QWEN_GATE_UP, 5120, 8), (MIXED, 1024, 2), (MIXED, 1024, 16)])
 def test_qmm_group_matches_oracle(cuda_lib, group, K, M):
     Ws = [synth.weights(q, N, K, seed=100 + i) for i, (q, N) in enumerate(group)]
     x = synth.activations(M, K, seed=200 + M)
@@ -276,6 +276,9 @@ def test_qmm_group_matches_oracle(cuda_lib, group, K, M):
     assert cuda_lib.qmm_device_status() == 0
     if M == 1:
         assert cuda_lib.qmm_launch_count() - before == 1  # the whole group, one launch
+    if group is not MIXED and M >= 3:
+        # the tensor-core path: x quantised once, one decode launch per matrix
+        assert cuda_lib.qmm_launch_count() - before == 1 + len(group)
     for (q, N), W, y in zip(group, Ws, ys):
         if N == 0:
             continue
