@@ -88,8 +88,9 @@ def load_peaks():
 
 
 TRAFFIC_SUMMARY = os.path.join("profiles", "gemv_q6k_lm_head_k2048_n128256.txt")
-TRAFFIC_SOURCES = ("mat_mul_gb300/csrc/gemv_sb.cu", "mat_mul_gb300/csrc/qmm_device.cuh",
-                   "mat_mul_gb300/csrc/qmm_internal.h")
+# the files whose code makes up the lm_head kernel (qmm_internal.h only
+# declares host launchers)
+TRAFFIC_SOURCES = ("mat_mul_gb300/csrc/gemv_sb.cu", "mat_mul_gb300/csrc/qmm_device.cuh")
 
 
 def sources_sha256(paths):
@@ -572,9 +573,10 @@ def run_ncu_case(name, calls=3):
     mats = {m["name"]: m for m in decode_workload()}
     for idx, (nm, qtype, K, N) in enumerate(synth.CONFIGS[4]["mats"]):
         mats[f"cfg4:{nm}"] = dict(cfg=4, idx=idx, name=f"cfg4:{nm}", qtype=qtype, K=K, N=N, M=512)
+    name, _, rows = name.partition("@")  # "cfg3:gate@4": the matrix with M = 4 activation rows
     m = mats[name]
     W = torch.from_numpy(synth.config_weights(m["cfg"], m["idx"])).cuda()
-    x = torch.from_numpy(synth.config_activations(m["cfg"], m.get("M", 1), m["K"])).cuda()
+    x = torch.from_numpy(synth.config_activations(m["cfg"], int(rows) if rows else m.get("M", 1), m["K"])).cuda()
     for _ in range(calls):
         y = q.qmm(m["qtype"], W, m["N"], m["K"], x)
     torch.cuda.synchronize()
@@ -619,7 +621,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--quick", action="store_true", help="headline and e2e only")
     ap.add_argument("--ncu-case", default=None,
-                    help="run three eager calls of one matrix (e.g. cfg2:lm_head) and exit")
+                    help="run three eager calls of one matrix (e.g. cfg2:lm_head, cfg3:gate@4 for M = 4) and exit")
     ap.add_argument("--ncu-step", type=int, default=0,
                     help="run this many eager decode steps (for an ncu launch list) and exit")
     args = ap.parse_args()

@@ -40,11 +40,13 @@
 // Streaming.  Rows are taken in groups of 16.  CTA c (one per SM) owns a
 // range of 8-row halves, balanced to within one half, i.e. whole groups plus
 // at most one half group.  A producer warp fills a ring of stages shared by
-// eight consumer warps; a stage is one group's 16 rows x 8 super-blocks, and
-// consumer warp w computes super-block (w + chunk) mod 8 of it, so the copies
-// are about 1.2 KB (Q4_K) or 1.7 KB (Q6_K) per row and the warps share every
-// stage evenly (the copy engine's cost per copy is what limits small ones).
-//   Q4_K: a stage is two 2-D tensor copies of 8 rows x (8 super-blocks and
+// CW consumer warps (8 or 10, whichever tiles a row's super-blocks with
+// fewer empty slots); a stage is one group's 16 rows x CW super-blocks, and
+// consumer warp w computes super-block (w + chunk) mod CW of it, so the
+// copies are 1.2-1.5 KB (Q4_K) or 1.7-2.1 KB (Q6_K) per row and the warps
+// share every stage evenly (the copy engine's cost per row segment is what
+// limits short ones).
+//   Q4_K: a stage is two 2-D tensor copies of 8 rows x (CW super-blocks and
 //     16 bytes), rows past N and bytes past the row end arriving as zeros, so
 //     rows land 16 bytes past a 128-byte multiple apart and the eight rows of
 //     an ldmatrix are eight distinct 16-byte bank groups.
@@ -83,19 +85,14 @@ namespace qk {
 
 namespace {
 
-constexpr int CW = 8;                  // consumer warps; warp CW is the producer
-constexpr int NTHREADS = (CW + 1) * 32;
 constexpr int GR = 16;                 // weight rows per group (the MMA's m)
-constexpr int CHS = 8;                 // super-blocks per stage: one per consumer warp
 constexpr int MAX_NS = 6;              // stages in the ring
 constexpr int MAX_PHASES = 8;
 constexpr int EDGE_FLOATS = 128;       // a group's result: 16 rows x 8 tokens
 // stage bytes per row: Q4_K boxes of 8 super-blocks and 16 bytes (so rows
 // sit 16 bytes past a 128-byte multiple apart), Q6_K spans of 8 super-blocks
 // rounded out to 16 bytes in a pitch of an odd number of 16-byte chunks
-constexpr int Q4K_PITCH = 8 * 144 + 16;
-constexpr int Q6K_PITCH = ((8 * 210 + 41) / 16 | 1) * 16;
-static_assert(Q4K_PITCH % 128 == 16 && (Q6K_PITCH / 16) % 2 == 1, "row pitches");
+
 // shared-memory head: full barriers | empty barriers | activation barrier |
 // failure flag | zeros (the B rows of tokens M..7) | partial sums of the
 // consumer warps, two groups.  The activation rows start on a 128-byte
@@ -109,9 +106,25 @@ constexpr int OFF_FAIL = 144;
 constexpr int OFF_ZERO = 624;
 constexpr int ZERO_BYTES = 512;
 constexpr int OFF_PART = 1152;
-constexpr int HEAD = OFF_PART + 2 * CW * EDGE_FLOATS * 4;
 static_assert(8 * MAX_NS <= 64 && OFF_ZERO + ZERO_BYTES <= OFF_PART, "head layout");
-static_assert(OFF_ZERO % 128 == 112 && HEAD % 128 == 0, "zero rows in bank group 7");
+static_assert(OFF_ZERO % 128 == 112 && OFF_PART % 128 == 0, "zero rows in bank group 7");
+
+// The kernel for CW consumer warps (warp CW is the producer): a stage is one
+// group's 16 rows x CW super-blocks, one per consumer warp.  Stage bytes per
+// row: Q4_K boxes of CW super-blocks and 16 bytes, Q6_K spans of CW
+// super-blocks rounded out to 16 bytes; both an odd number of 16-byte
+// chunks, so the 8 rows of an ldmatrix sit in 8 distinct bank groups.
+template <int CW>
+struct Shape {
+    static constexpr int NTHREADS = (CW + 1) * 32;
+    static constexpr int CHS = CW;
+    static constexpr int Q4K_PITCH = CW * 144 + 16;
+    static constexpr int Q6K_PITCH = ((CW * 210 + 41) / 16 | 1) * 16;
+    static constexpr int HEAD = OFF_PART + 2 * CW * EDGE_FLOATS * 4;  // partial sums of two groups
+    static_assert((Q4K_PITCH / 16) % 2 == 1 && (Q6K_PITCH / 16) % 2 == 1, "row pitches");
+    static_assert(HEAD % 128 == 0 && Q4K_PITCH / 8 <= 256, "head and box");
+};
+constexpr int CW_CHOICES[2] = {8, 10};
 constexpr int SB_WORDS = 144 / 8;  // a Q4_K super-block in the tensor map's 8-byte elements
 
 // f(integral_constant<int, I>) for I = B .. E-1: the loop index is a
@@ -353,6 +366,7 @@ struct StageCursor {
     int nq;       // chunks per row in the phase
 };
 
+template <int CHS>
 __device__ __forceinline__ void cursor_phase(const MmParams &P, StageCursor &c, int p) {
     c.p = p;
     c.gi = 0;
@@ -362,16 +376,18 @@ __device__ __forceinline__ void cursor_phase(const MmParams &P, StageCursor &c, 
     c.nq = (c.nsb + CHS - 1) / CHS;
 }
 
+template <int CHS>
 __device__ __forceinline__ void cursor_next(const MmParams &P, StageCursor &c, int ng) {
     if (++c.kc == c.nq) {
         c.kc = 0;
-        if (++c.gi == ng) cursor_phase(P, c, c.p + 1);
+        if (++c.gi == ng) cursor_phase<CHS>(P, c, c.p + 1);
     }
 }
 
-template <int T>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int T, int CW>
+__global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ MmParams P) {
+    constexpr int NTHREADS = Shape<CW>::NTHREADS, CHS = Shape<CW>::CHS;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -430,8 +446,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == CW) {
         // ---- producer: fills the ring in stage order --------------------
         StageCursor c;
-        cursor_phase(P, c, 0);
-        for (int s = 0; s < total; ++s, cursor_next(P, c, ng)) {
+        cursor_phase<CHS>(P, c, 0);
+        for (int s = 0; s < total; ++s, cursor_next<CHS>(P, c, ng)) {
             const int slot = s % P.NS;
             if (s >= P.NS) {
                 // the consumers' release of this slot's previous stage
@@ -526,7 +542,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int s = 0;
     for (int p = 0; p < P.nphase; ++p) {
         StageCursor c;
-        cursor_phase(P, c, p);
+        cursor_phase<CHS>(P, c, p);
         if (p > 0) {
             // every consumer is done with the previous window
             named_barrier(1, CW * 32);
@@ -545,7 +561,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                                                     static_cast<uint32_t>((s / P.NS) & 1), P.status)))
                     failed = true;
                 const int sb0 = c.sb + kc * CHS, nsb = min(CHS, c.sb + c.nsb - sb0);
-                const int idx = (warp + kc) & (CHS - 1);
+                const int idx = (warp + kc) % CHS;
                 const uint8_t *st = smem + P.off_ring + slot * P.stage_bytes;
                 if (!failed && idx < nsb) {
                     const int kw = sb0 + idx - c.sb;  // super-block inside the window
@@ -608,16 +624,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // Shared-memory plan: head | activation window [M][x_ld] | Q6_K group sums
-// window | phase table | ring of NS stages of GR rows x 8 super-blocks.  The
+// window | phase table | ring of NS stages of GR rows x CW super-blocks.  The
 // fewest phases that fit with at least two stages.
 struct Plan {
     int NS, nphase, nbp, x_ld, row_pitch, stage_bytes, off_x, off_xs, off_table, off_ring, smem;
 };
 
-template <int T>
+template <int T, int CW>
 bool plan_mm(int M, int64_t K, int64_t max_groups, int max_smem, Plan &pl) {
+    using S = Shape<CW>;
+    constexpr int CHS = S::CHS, HEAD = S::HEAD;
     const int nb = static_cast<int>(K / 256);
-    const int pitch = T == QMM_Q4_K ? Q4K_PITCH : Q6K_PITCH;
+    const int pitch = T == QMM_Q4_K ? S::Q4K_PITCH : S::Q6K_PITCH;
     const int64_t stage = static_cast<int64_t>(GR) * pitch;
     for (int P = 1; P <= MAX_PHASES; ++P) {
         int nbp = nb;
@@ -658,13 +676,35 @@ bool type_ok(int type, int M, int64_t K, int64_t N) {
     return false;
 }
 
+// Consumer warps (= super-blocks per stage): the count of CW_CHOICES that
+// leaves the fewest empty slots in a row's stages, the larger on a tie.
+int consumer_warps(int64_t K) {
+    const int64_t nb = K / 256;
+    int best = CW_CHOICES[0];
+    int64_t best_slots = -1;
+    for (int cw : CW_CHOICES) {
+        const int64_t slots = (nb + cw - 1) / cw * cw;
+        if (best_slots < 0 || slots <= best_slots) {
+            best = cw;
+            best_slots = slots;
+        }
+    }
+    return best;
+}
+
+bool plan_for(int type, int cw, int M, int64_t K, int64_t mg, int max_smem, Plan &pl) {
+    if (type == QMM_Q4_K)
+        return cw == 10 ? plan_mm<QMM_Q4_K, 10>(M, K, mg, max_smem, pl) : plan_mm<QMM_Q4_K, 8>(M, K, mg, max_smem, pl);
+    return cw == 10 ? plan_mm<QMM_Q6_K, 10>(M, K, mg, max_smem, pl) : plan_mm<QMM_Q6_K, 8>(M, K, mg, max_smem, pl);
+}
+
 }  // namespace
 
 bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_sms) {
     if (!type_ok(type, M, K, N)) return false;
     const int64_t mg = max_groups_of(N, num_sms, nullptr);
     Plan pl;
-    return type == QMM_Q4_K ? plan_mm<QMM_Q4_K>(M, K, mg, max_smem, pl) : plan_mm<QMM_Q6_K>(M, K, mg, max_smem, pl);
+    return plan_for(type, consumer_warps(K), M, K, mg, max_smem, pl);
 }
 
 cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
@@ -672,14 +712,13 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     if (!type_ok(type, M, K, N)) return cudaErrorNotSupported;
     int64_t grid = 0;
     const int64_t mg = max_groups_of(N, num_sms, &grid);
+    const int cw = consumer_warps(K);
     Plan pl;
-    const bool ok =
-        type == QMM_Q4_K ? plan_mm<QMM_Q4_K>(M, K, mg, max_smem, pl) : plan_mm<QMM_Q6_K>(M, K, mg, max_smem, pl);
-    if (!ok) return cudaErrorNotSupported;
+    if (!plan_for(type, cw, M, K, mg, max_smem, pl)) return cudaErrorNotSupported;
     const int nb = static_cast<int>(K / 256);
     const int bb = type == QMM_Q4_K ? Mm<QMM_Q4_K>::BB : Mm<QMM_Q6_K>::BB;
     // a CTA's stages count in int
-    if (mg * ((nb + CHS - 1) / CHS + pl.nphase) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    if (mg * ((nb + cw - 1) / cw + pl.nphase) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
     MmParams P = {};
     P.W = static_cast<const uint8_t *>(W);
     P.RB = static_cast<int64_t>(nb) * bb;
@@ -711,19 +750,20 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
         // and 2 elements (the next header, or zeros past the row end) x 8 rows
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb) * SB_WORDS, static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * 144};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(Q4K_PITCH / 8), 8u};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(pl.row_pitch / 8), 8u};
         const cuuint32_t es[2] = {1, 1};
         if (tensor_map_encoder()(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), dims, strides, box,
                                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    auto kern = type == QMM_Q4_K ? gemv_mma_kernel<QMM_Q4_K> : gemv_mma_kernel<QMM_Q6_K>;
+    auto kern = type == QMM_Q4_K ? (cw == 10 ? gemv_mma_kernel<QMM_Q4_K, 10> : gemv_mma_kernel<QMM_Q4_K, 8>)
+                                 : (cw == 10 ? gemv_mma_kernel<QMM_Q6_K, 10> : gemv_mma_kernel<QMM_Q6_K, 8>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(NTHREADS);
+    cfg.blockDim = dim3((cw + 1) * 32);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -291,10 +291,21 @@ def test_group_split_covers_every_matrix(group):
 
 
 # ---- the tensor-core decode kernel for 2 <= M <= 8 (gemv_mma.cu) ----------
-MM_CW, MM_GR, MM_CHS, MM_MAXNS, MM_MAXP = 8, 16, 8, 6, 8
-MM_HEAD = 1152 + 2 * MM_CW * 128 * 4  # barriers, flag | zeros | partial sums
-Q4K_PITCH = 8 * 144 + 16
-Q6K_PITCH = (((8 * 210 + 41) // 16) | 1) * 16
+MM_GR, MM_MAXNS, MM_MAXP = 16, 6, 8
+
+
+def mm_cw(K):
+    """Consumer warps = super-blocks per stage: 8 or 10, fewer empty slots, 10 on a tie."""
+    nb = K // 256
+    return min((8, 10), key=lambda cw: (-(-nb // cw) * cw, -cw))
+
+
+def mm_head(cw):
+    return 1152 + 2 * cw * 128 * 4  # barriers, flag | zeros | partial sums of two groups
+
+
+def mm_pitch(qtype, cw):
+    return cw * 144 + 16 if qtype == synth.Q4_K else (((cw * 210 + 41) // 16) | 1) * 16
 
 
 def mm_max_groups(N):
@@ -307,17 +318,18 @@ def plan_mm(qtype, M, K, max_groups=0):
     nb = K // 256
     if qtype == synth.Q6_K and nb % 2:
         return None
-    pitch = Q4K_PITCH if qtype == synth.Q4_K else Q6K_PITCH
+    cw = mm_cw(K)
+    pitch = mm_pitch(qtype, cw)
     xs_token = 32 if qtype == synth.Q4_K else 0
     stage = MM_GR * pitch
     for P in range(1, MM_MAXP + 1):
         nbp = nb
         if P > 1:
-            nbp = -(-(-(-nb // P)) // MM_CHS) * MM_CHS
+            nbp = -(-(-(-nb // P)) // cw) * cw
             if nbp * (P - 1) >= nb:
                 continue
         x_ld = align(nbp * (512 + xs_token), 128) + 16
-        o_x = MM_HEAD
+        o_x = mm_head(cw)
         o_xs = align(o_x + M * x_ld, 128)
         o_table = o_xs + (nbp * 512 if qtype == synth.Q6_K else 0)
         o_ring = align(o_table + (max_groups * 512 if P > 1 else 0), 128)
@@ -325,7 +337,7 @@ def plan_mm(qtype, M, K, max_groups=0):
         if ns < 2:
             continue
         ns = min(MM_MAXNS, ns)
-        return dict(NS=ns, P=P, nbp=nbp, x_ld=x_ld, pitch=pitch, stage=stage, off_x=o_x, off_xs=o_xs,
+        return dict(NS=ns, P=P, nbp=nbp, CW=cw, x_ld=x_ld, pitch=pitch, stage=stage, off_x=o_x, off_xs=o_xs,
                     off_table=o_table, ring=o_ring, smem=o_ring + ns * stage)
     return None
 
@@ -334,20 +346,21 @@ def check_mm(qtype, N, K, M):
     mg, halves, grid = mm_max_groups(N)
     P = plan_mm(qtype, M, K, mg)
     assert P is not None and P["smem"] <= SMEM_MAX
-    pitch, nbp, nph, stage = P["pitch"], P["nbp"], P["P"], P["stage"]
+    pitch, nbp, nph, stage, CW = P["pitch"], P["nbp"], P["P"], P["stage"], P["CW"]
     nb = K // 256
     RB = nb * synth.BLOCK_BYTES[qtype]
     w_end = N * RB            # the matrix at address 0 (16-byte aligned)
-    assert P["x_ld"] % 128 == 16 and P["off_x"] % 128 == 0 and P["off_x"] >= MM_HEAD
+    assert P["x_ld"] % 128 == 16 and P["off_x"] % 128 == 0 and P["off_x"] >= mm_head(CW)
     assert P["ring"] % 128 == 0 and stage % 128 == 0
     # an ldmatrix reads 16 bytes of 8 consecutive rows: 8 distinct bank groups
     assert len({(r * pitch // 16) % 8 for r in range(8)}) == 8
+    assert (pitch // 16) % 2 == 1 and pitch % 16 == 0
     if qtype == synth.Q4_K:
-        assert pitch % 16 == 0 and (pitch // 8) <= 256 and (8 * pitch) % 128 == 0
+        assert (pitch // 8) <= 256 and (8 * pitch) % 128 == 0
     else:
-        assert nb % 2 == 0 and pitch >= 210 * MM_CHS + 26
+        assert nb % 2 == 0 and CW % 2 == 0 and pitch >= 210 * CW + 26
     if nph > 1:
-        assert nbp % MM_CHS == 0 and nbp * (nph - 1) < nb
+        assert nbp % CW == 0 and nbp * (nph - 1) < nb
     row_bytes = 2 * K + K // 8   # quantiser output per token; then [K/16][8] fp32 sums
     for p in range(nph):
         sb, nsb = p * nbp, min(nbp, nb - p * nbp)
@@ -372,14 +385,14 @@ def check_mm(qtype, N, K, M):
         assert ng <= mg
         for p in range(nph):
             sbp, nsbp = p * nbp, min(nbp, nb - p * nbp)
-            nq = -(-nsbp // MM_CHS)
+            nq = -(-nsbp // CW)
             for gi in range(ng):
                 row0 = r0 + MM_GR * gi
                 rows = min(MM_GR, r1 - row0)
                 assert 1 <= rows <= MM_GR
                 for kc in range(nq):
-                    sb0 = sbp + kc * MM_CHS
-                    nsb = min(MM_CHS, sbp + nsbp - sb0)
+                    sb0 = sbp + kc * CW
+                    nsb = min(CW, sbp + nsbp - sb0)
                     assert nsb >= 1
                     if qtype == synth.Q4_K:
                         boxes = 2 if r1 - row0 > 8 else 1
@@ -387,7 +400,7 @@ def check_mm(qtype, N, K, M):
                         # the boxes load rows [row0, row0 + 8*boxes): every one this CTA
                         # owns, none of another CTA's (rows past N arrive as zeros)
                         assert row0 + 8 * boxes >= row0 + rows and (boxes == 1 or row0 + 16 <= r1 or r1 == N)
-                        assert 15 * pitch + 144 * (MM_CHS - 1) + 16 + 16 * 7 + 16 <= stage
+                        assert 15 * pitch + 144 * (CW - 1) + 16 + 16 * 7 + 16 <= stage
                     else:
                         total = 0
                         for rr in range(rows):
