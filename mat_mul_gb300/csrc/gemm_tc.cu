@@ -33,12 +33,17 @@
 // issued, frees TMEM and returns with the status word set.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 
 namespace qk {
 
 namespace {
+
+__host__ __device__ constexpr int qk_weights(int t) { return t == QMM_Q8_0 ? 32 : 256; }
+__host__ __device__ constexpr int qk_block_bytes(int t) { return t == QMM_Q8_0 ? 34 : t == QMM_Q6_K ? 210 : 144; }
 
 constexpr int BW = 128, BK = 128;  // weight rows per tile, K per step (half a super-block)
 constexpr int A_STAGES = 4;        // dequantised weight stages in TMEM (64 columns each)
@@ -50,28 +55,51 @@ constexpr int H_BYTES = BW * 16;    // d, dmin and the 12 scale bytes of each ro
 constexpr int Q_BYTES = BW * 64;    // this K step's 64 quant bytes of each row (64-byte swizzle)
 constexpr int R_BYTES = H_BYTES + Q_BYTES;
 
-template <int BT>
+// Q6_K and Q8_0: rows are not 16-byte multiples, so no tensor map describes
+// them; each dequantiser warp copies the raw bytes of its 32 rows itself, one
+// super-step (two K steps, 256 weights: one Q6_K super-block, eight Q8_0
+// blocks) ahead, into two buffers of 32 rows x PITCH_W words (the bytes plus
+// up to 2 of alignment, an odd number of words: conflict-free per-row reads).
+template <int T>
+struct RawStep {
+    static constexpr int BYTES = 0, PITCH_W = 0;
+};
+template <>
+struct RawStep<QMM_Q6_K> {
+    static constexpr int BYTES = 210, PITCH_W = 55;
+};
+template <>
+struct RawStep<QMM_Q8_0> {
+    static constexpr int BYTES = 272, PITCH_W = 69;
+};
+
+template <int BT, int T>
 struct TcCfg {
+    static constexpr bool OWN = T != QMM_Q4_K;  // the dequantisers copy their own raw bytes
     static constexpr int XBOX = BT * 128;   // one 64-wide K box of tokens (128-byte swizzle rows)
     static constexpr int X_BYTES = 2 * XBOX;
-    static constexpr int X_STAGES = BT == 256 ? 3 : BT == 128 ? 5 : 8;
+    static constexpr int X_STAGES = OWN ? (BT == 256 ? 2 : BT == 128 ? 4 : 8) : (BT == 256 ? 3 : BT == 128 ? 5 : 8);
     static constexpr int OFF_R = X_STAGES * X_BYTES;
-    static constexpr int R_STAGES_FIT = (232448 - 1536 - OFF_R) / R_BYTES;
+    static constexpr int RAW_WARP = 2 * 32 * RawStep<T>::PITCH_W * 4;  // per dequantiser warp (OWN)
+    static constexpr int R_STAGES_FIT = OWN ? 0 : (232448 - 1536 - OFF_R) / R_BYTES;
     static constexpr int R_STAGES = R_STAGES_FIT > 8 ? 8 : R_STAGES_FIT;
-    static constexpr int OFF_BAR = OFF_R + R_STAGES * R_BYTES;
+    static constexpr int OFF_BAR = OFF_R + (OWN ? 4 * RAW_WARP : R_STAGES * R_BYTES);
     static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // barriers + base alignment slack
     static constexpr int A_COL0 = BT;                         // TMEM columns of the A stages
     static constexpr int TMEM_COLS = BT + A_COLS * A_STAGES <= 256 ? 256 : 512;
     // D fp32, A and B fp16, both K-major, M = 128 weight rows, N = BT tokens
     static constexpr uint32_t IDESC = (1u << 4) | ((BT >> 3) << 17) | ((BW >> 4) << 24);
     static_assert(X_BYTES % 1024 == 0 && R_BYTES % 1024 == 0, "stage alignment");
-    static_assert(R_STAGES >= 3, "raw ring depth");
+    static_assert(OWN || R_STAGES >= 3, "raw ring depth");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(16 * (X_STAGES + R_STAGES + A_STAGES) + 8 <= 480, "barrier area");
     static_assert(BT + A_COLS * A_STAGES <= TMEM_COLS, "tensor memory");
 };
 
 struct TcParams {
+    const uint8_t *W;  // the blocks (read by the dequantisers for Q6_K, Q8_0)
+    int64_t RB;        // bytes per weight row
+    uint64_t w_end;    // first byte past the matrix
     int M, N;
     int nsteps;   // 128-wide K steps per split; split z starts at z*nsteps
     float *y;
@@ -189,6 +217,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (both 4-byte aligned), and its
+// group bookkeeping.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The 32-bit word at byte offset `off` (2-byte aligned) of a row buffer that
+// is 4-byte aligned: two aligned words shifted together.
+__device__ __forceinline__ uint32_t row_word(const uint8_t *row, int off) {
+    const uint32_t *a = reinterpret_cast<const uint32_t *>(row + (off & ~3));
+    return __funnelshift_r(a[0], a[1], (off & 2) * 8);
+}
+
 // Four fp16 weights from the four bytes of a quant word (low nibbles, or
 // high ones when hi): w = q*a + nb with q recovered exactly from the fp16
 // bit pattern 0x6400 | q = 1024 + q.  Weights (b0,b1) -> out0, (b2,b3) -> out1.
@@ -204,11 +250,11 @@ __device__ __forceinline__ void dequant4(uint32_t w, bool hi, __half2 a, __half2
     out1 = *reinterpret_cast<const uint32_t *>(&w1);
 }
 
-template <int BT>
+template <int T, int BT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
                    const __grid_constant__ CUtensorMap tmQ, const TcParams P) {
-    using C = TcCfg<BT>;
+    using C = TcCfg<BT, T>;
     extern __shared__ uint8_t smem_raw[];
     // stages need 1024-byte alignment for the 128-byte swizzle
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -283,8 +329,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     } else if (warp == W_RLOAD) {
-        // ------------------------------------------ raw weight producer
-        if (lane == 0) {
+        // ------------------------------------------ raw weight producer (Q4_K)
+        if (!C::OWN && lane == 0) {
             int issued = 0;
             for (int kk = 0; kk < P.nsteps; ++kk) {
                 const int r = kk % C::R_STAGES;
@@ -333,62 +379,196 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int quarter = warp & 3;
         const int n = 32 * quarter + lane;  // weight row within the tile (= TMEM lane)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-        for (int kk = 0; kk < P.nsteps; ++kk) {
-            const int r = kk % C::R_STAGES, sa = kk % A_STAGES;
-            bool ok = !*abort_flag;
-            if (ok) ok = mbar_wait(bar_r_full + 8 * r, (kk / C::R_STAGES) & 1, P.status);
-            if (ok && kk >= A_STAGES) ok = mbar_wait(bar_a_empty + 8 * sa, ((kk / A_STAGES) - 1) & 1, P.status);
-            if (__any_sync(0xffffffffu, !ok)) {
-                *abort_flag = 1;
-                break;
-            }
-            tc_fence_after();
-            const int h = (k_step0 + kk) & 1;  // which half of the super-block
-            const uint8_t *st = smem + C::OFF_R + r * R_BYTES;
-            const uint4 hdr = *reinterpret_cast<const uint4 *>(st + 16 * n);
-            // six-bit scales and mins of sub-blocks 4h..4h+3 (byte i: sub-block
-            // 4h+i), GGUF packing
-            uint32_t scw, mw;
-            if (h == 0) {
-                scw = hdr.y & 0x3F3F3F3Fu;
-                mw = hdr.z & 0x3F3F3F3Fu;
-            } else {
-                scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-                mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-            }
-            const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
-            // the quant row: 64 bytes whose 16-byte chunk f sits at f ^ ((n >> 1) & 3)
-            // (TMA 64-byte swizzle), so a quarter warp's loads hit distinct banks
-            const uint8_t *qrow = st + H_BYTES + 64 * n;
-            const int sw = (n >> 1) & 3;
-#pragma unroll
-            for (int cp = 0; cp < 2; ++cp) {
-                // chunk cp of 64 weights: quant bytes 32cp..32cp+31, low nibbles
-                // -> sub-block 4h+2cp, high nibbles -> sub-block 4h+2cp+1
-                const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp) ^ sw));
-                const uint4 qb = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp + 1) ^ sw));
-                const int sh = 16 * cp;
-                const __half2 ha0 = __float2half2_rn(d * static_cast<float>((scw >> sh) & 0xFF));
-                const __half2 ha1 = __float2half2_rn(d * static_cast<float>((scw >> (sh + 8)) & 0xFF));
-                const __half2 hb0 = __float2half2_rn(-(dmin * static_cast<float>((mw >> sh) & 0xFF)));
-                const __half2 hb1 = __float2half2_rn(-(dmin * static_cast<float>((mw >> (sh + 8)) & 0xFF)));
-                // weight l < 32 of the chunk is the low nibble of quant byte l,
-                // weight 32 + l its high nibble; TMEM column i holds weights 2i, 2i+1
-                const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-                uint32_t r[32];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    dequant4(qw[i], false, ha0, hb0, r[2 * i], r[2 * i + 1]);
-                    dequant4(qw[i], true, ha1, hb1, r[16 + 2 * i], r[16 + 2 * i + 1]);
+        if constexpr (!C::OWN) {
+            for (int kk = 0; kk < P.nsteps; ++kk) {
+                const int r = kk % C::R_STAGES, sa = kk % A_STAGES;
+                bool ok = !*abort_flag;
+                if (ok) ok = mbar_wait(bar_r_full + 8 * r, (kk / C::R_STAGES) & 1, P.status);
+                if (ok && kk >= A_STAGES) ok = mbar_wait(bar_a_empty + 8 * sa, ((kk / A_STAGES) - 1) & 1, P.status);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    *abort_flag = 1;
+                    break;
                 }
-                tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
+                tc_fence_after();
+                const int h = (k_step0 + kk) & 1;  // which half of the super-block
+                const uint8_t *st = smem + C::OFF_R + r * R_BYTES;
+                const uint4 hdr = *reinterpret_cast<const uint4 *>(st + 16 * n);
+                // six-bit scales and mins of sub-blocks 4h..4h+3 (byte i: sub-block
+                // 4h+i), GGUF packing
+                uint32_t scw, mw;
+                if (h == 0) {
+                    scw = hdr.y & 0x3F3F3F3Fu;
+                    mw = hdr.z & 0x3F3F3F3Fu;
+                } else {
+                    scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+                    mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+                }
+                const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
+                // the quant row: 64 bytes whose 16-byte chunk f sits at f ^ ((n >> 1) & 3)
+                // (TMA 64-byte swizzle), so a quarter warp's loads hit distinct banks
+                const uint8_t *qrow = st + H_BYTES + 64 * n;
+                const int sw = (n >> 1) & 3;
+    #pragma unroll
+                for (int cp = 0; cp < 2; ++cp) {
+                    // chunk cp of 64 weights: quant bytes 32cp..32cp+31, low nibbles
+                    // -> sub-block 4h+2cp, high nibbles -> sub-block 4h+2cp+1
+                    const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp) ^ sw));
+                    const uint4 qb = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp + 1) ^ sw));
+                    const int sh = 16 * cp;
+                    const __half2 ha0 = __float2half2_rn(d * static_cast<float>((scw >> sh) & 0xFF));
+                    const __half2 ha1 = __float2half2_rn(d * static_cast<float>((scw >> (sh + 8)) & 0xFF));
+                    const __half2 hb0 = __float2half2_rn(-(dmin * static_cast<float>((mw >> sh) & 0xFF)));
+                    const __half2 hb1 = __float2half2_rn(-(dmin * static_cast<float>((mw >> (sh + 8)) & 0xFF)));
+                    // weight l < 32 of the chunk is the low nibble of quant byte l,
+                    // weight 32 + l its high nibble; TMEM column i holds weights 2i, 2i+1
+                    const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                    uint32_t r[32];
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        dequant4(qw[i], false, ha0, hb0, r[2 * i], r[2 * i + 1]);
+                        dequant4(qw[i], true, ha1, hb1, r[16 + 2 * i], r[16 + 2 * i + 1]);
+                    }
+                    tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_a_full + 8 * sa);
+                    mbar_arrive(bar_r_empty + 8 * r);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar_a_full + 8 * sa);
-                mbar_arrive(bar_r_empty + 8 * r);
+        } else {
+            // Q6_K / Q8_0: this warp's 32 rows, one super-step at a time
+            constexpr int SSB = RawStep<T>::BYTES, PW = RawStep<T>::PITCH_W;
+            uint8_t *raw = smem + C::OFF_R + quarter * C::RAW_WARP;
+            const int nss = P.nsteps / 2;  // super-steps of this CTA (its K range starts on one)
+            const int js0 = k_step0 / 2;
+            const uint64_t wbase = reinterpret_cast<uint64_t>(P.W);
+            // copy super-step js (local) of the warp's rows into buffer js & 1:
+            // lane i copies words i, i+32, ... of each row, from the row's
+            // bytes rounded down to 4; the matrix's last 2 bytes, when they
+            // would need a word past its end, by a 2-byte load instead
+            auto fetch = [&](int js) {
+                uint8_t *buf = raw + (js & 1) * (32 * PW * 4);
+                for (int r = 0; r < 32; ++r) {
+                    const int64_t row = n0 + 32 * quarter + r;
+                    if (row >= P.N) break;
+                    const uint64_t seg = wbase + static_cast<uint64_t>(row) * P.RB +
+                                         static_cast<uint64_t>(js0 + js) * SSB;
+                    const uint64_t base = seg & ~uint64_t(3);
+                    const int nw = static_cast<int>((seg + SSB - base + 3) >> 2);
+                    const bool past = base + 4 * static_cast<uint64_t>(nw) > P.w_end;
+                    for (int i = lane; i < nw; i += 32) {
+                        uint8_t *dst = buf + (r * PW + i) * 4;
+                        if (past && i == nw - 1)
+                            *reinterpret_cast<uint32_t *>(dst) =
+                                __ldg(reinterpret_cast<const unsigned short *>(base + 4 * static_cast<uint64_t>(i)));
+                        else
+                            cp_async4(smem_u32(dst), reinterpret_cast<const void *>(base + 4 * static_cast<uint64_t>(i)));
+                    }
+                }
+                cp_async_commit();
+            };
+            fetch(0);
+            if (nss > 1) fetch(1);
+            const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+            for (int kk = 0; kk < P.nsteps; ++kk) {
+                const int js = kk >> 1, h = kk & 1, sa = kk % A_STAGES;
+                bool ok = !*abort_flag;
+                if (ok && kk >= A_STAGES) ok = mbar_wait(bar_a_empty + 8 * sa, ((kk / A_STAGES) - 1) & 1, P.status);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (h == 0) {
+                    // super-step js has landed: every group but the newest
+                    if (js + 1 < nss) cp_async_wait<1>();
+                    else cp_async_wait<0>();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                const uint8_t *row = raw + (js & 1) * (32 * PW * 4) + lane * PW * 4;
+                // the row's bytes start at this offset inside its buffer
+                const int dl = static_cast<int>((wbase + static_cast<uint64_t>(n0 + n) * P.RB +
+                                                 static_cast<uint64_t>(js0 + js) * SSB) & 3);
+                if constexpr (T == QMM_Q6_K) {
+                    // half h of the super-block: ql bytes 64h.., qh 128+32h.., scales
+                    // 192+8h.., d at 208; weight 32qi + l: low bits from ql byte
+                    // 32(qi&1) + l (nibble qi>>1), high bits (qh byte l >> 2qi) & 3,
+                    // scale 8h + 2qi + (l >= 16); w = d*sc * (q - 32)
+                    const float d = __half2float(*reinterpret_cast<const __half *>(row + dl + 208));
+                    const uint32_t sc0 = row_word(row, dl + 192 + 8 * h), sc1 = row_word(row, dl + 196 + 8 * h);
+                    uint32_t qh[8], ql[2][8];
+#pragma unroll
+                    for (int lw = 0; lw < 8; ++lw) {
+                        qh[lw] = row_word(row, dl + 128 + 32 * h + 4 * lw);
+                        ql[0][lw] = row_word(row, dl + 64 * h + 4 * lw);
+                        ql[1][lw] = row_word(row, dl + 64 * h + 32 + 4 * lw);
+                    }
+                    const __half2 k1056 = __half2half2(__ushort_as_half(0x6420));  // 1056 = 1024 + 32
+#pragma unroll
+                    for (int cp = 0; cp < 2; ++cp) {  // weights 64cp .. 64cp+63 (qi = 2cp, 2cp+1)
+                        uint32_t r[32];
+#pragma unroll
+                        for (int qq = 0; qq < 2; ++qq) {
+                            const int qi = 2 * cp + qq;
+                            const uint32_t scw = qi < 2 ? sc0 : sc1;
+                            const int sb = 16 * (qi & 1);  // byte of scale 8h + 2qi in its word
+                            const __half2 s_lo = __float2half2_rn(
+                                d * static_cast<float>(static_cast<int8_t>(scw >> sb)));
+                            const __half2 s_hi = __float2half2_rn(
+                                d * static_cast<float>(static_cast<int8_t>(scw >> (sb + 8))));
+#pragma unroll
+                            for (int lw = 0; lw < 8; ++lw) {
+                                const uint32_t lo = qi < 2 ? (ql[qi & 1][lw] & 0x0F0F0F0Fu)
+                                                           : ((ql[qi & 1][lw] >> 4) & 0x0F0F0F0Fu);
+                                const uint32_t q6 = lo | (((qh[lw] >> (2 * qi)) & 0x03030303u) << 4);
+                                const uint32_t p0 = __byte_perm(q6, 0x64646464u, 0x4140u);
+                                const uint32_t p1 = __byte_perm(q6, 0x64646464u, 0x4342u);
+                                const __half2 s = lw < 4 ? s_lo : s_hi;
+                                const __half2 w0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1056), s);
+                                const __half2 w1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1056), s);
+                                r[16 * qq + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
+                                r[16 * qq + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
+                            }
+                        }
+                        tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
+                    }
+                    (void)k1024;
+                } else {
+                    // blocks 4h .. 4h+3 of the eight: d (fp16), then 32 int8; w = d * q
+                    const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));  // 1152 = 1024 + 128
+#pragma unroll
+                    for (int cp = 0; cp < 2; ++cp) {  // blocks 4h + 2cp, 4h + 2cp + 1
+                        uint32_t r[32];
+#pragma unroll
+                        for (int bb = 0; bb < 2; ++bb) {
+                            const int ob = 34 * (4 * h + 2 * cp + bb);
+                            const __half dh = *reinterpret_cast<const __half *>(row + dl + ob);
+                            const __half2 s = __half2half2(dh);
+#pragma unroll
+                            for (int lw = 0; lw < 8; ++lw) {
+                                const uint32_t q = row_word(row, dl + ob + 2 + 4 * lw);
+                                // bytes (q0 ^ 0x80, 0x64, q1 ^ 0x80, 0x64): 1024 + 128 + q
+                                const uint32_t p0 = __byte_perm(q, 0x64646464u, 0x4140u) ^ 0x00800080u;
+                                const uint32_t p1 = __byte_perm(q, 0x64646464u, 0x4342u) ^ 0x00800080u;
+                                const __half2 w0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1152), s);
+                                const __half2 w1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1152), s);
+                                r[16 * bb + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
+                                r[16 * bb + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
+                            }
+                        }
+                        tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
+                    }
+                    (void)k1024;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_a_full + 8 * sa);
+                // buffer js & 1 is read by every lane: the super-step after next
+                if (h == 1 && js + 2 < nss) fetch(js + 2);
             }
+            cp_async_wait<0>();  // no copy in flight at exit
         }
         // epilogue: TMEM lanes of this quarter, all BT token columns
         const bool ok = mbar_wait(bar_acc, 0, P.status);
@@ -427,15 +607,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
-    return type == QMM_Q4_K && K % 256 == 0 && K >= 256 && N >= 1 && M >= 1 && N <= (int64_t(1) << 30) &&
+    return (type == QMM_Q4_K || type == QMM_Q6_K || type == QMM_Q8_0) && K % 256 == 0 && K >= 256 && N >= 1 && M >= 1 && N <= (int64_t(1) << 30) &&
            M <= (int64_t(1) << 30) && K <= (int64_t(1) << 24) && tensor_map_encoder() != nullptr;
 }
 
-template <int BT>
+template <int T, int BT>
 cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, const void *xh, int64_t M, float *y,
                       cudaStream_t st, int num_sms, int *status) {
-    using C = TcCfg<BT>;
-    CUtensorMap tx, th, tq;
+    using C = TcCfg<BT, T>;
+    CUtensorMap tx = {}, th = {}, tq = {};
     // tokens: fp16 [M][K], boxes of 64 K x BT rows, 128-byte swizzle
     {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
@@ -450,7 +630,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     // raw weights as bytes [N][row bytes]: 16-byte boxes (super-block header)
     // and 64-byte boxes (one K step's quants, 64-byte swizzle), 128 rows each
     const int64_t rb = (K / 256) * RAW_ROW;
-    for (int which = 0; which < 2; ++which) {
+    for (int which = 0; which < 2 && T == QMM_Q4_K; ++which) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
         const cuuint32_t box[2] = {which ? 64u : 16u, static_cast<cuuint32_t>(BW)};
@@ -466,9 +646,13 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     const int ksteps = static_cast<int>(K / BK);
     // Split K in two when the tiles alone would leave most SMs idle (two
     // contributions per output keep the fp32 result independent of order).
+    // (Q6_K, Q8_0: each half must start on a super-step of two K steps)
     int splits = 1;
-    if (2 * static_cast<int64_t>(nt) * mt <= num_sms && ksteps % 2 == 0) splits = 2;
+    if (2 * static_cast<int64_t>(nt) * mt <= num_sms && ksteps % (C::OWN ? 4 : 2) == 0) splits = 2;
     TcParams P;
+    P.W = static_cast<const uint8_t *>(W);
+    P.RB = (K / qk_weights(T)) * qk_block_bytes(T);
+    P.w_end = reinterpret_cast<uint64_t>(W) + static_cast<uint64_t>(N) * P.RB;
     P.M = static_cast<int>(M);
     P.N = static_cast<int>(N);
     P.y = y;
@@ -479,7 +663,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
         if (e != cudaSuccess) return e;
     }
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(gemm_tc_kernel<T, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     P.nsteps = ksteps / splits;
     cudaLaunchConfig_t cfg = {};
@@ -494,7 +678,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BT>, tx, th, tq, P);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T, BT>, tx, th, tq, P);
 }
 
 }  // namespace
@@ -518,9 +702,15 @@ cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const 
                            cudaStream_t st, int num_sms, int *status) {
     if (!gemm_tc_supported(type, N, K, M)) return cudaErrorNotSupported;
     EncodeTiled enc = tensor_map_encoder();
-    if (M <= 64) return launch_bt<64>(enc, W, N, K, xh, M, y, st, num_sms, status);
-    if (M <= 128) return launch_bt<128>(enc, W, N, K, xh, M, y, st, num_sms, status);
-    return launch_bt<256>(enc, W, N, K, xh, M, y, st, num_sms, status);
+    auto run = [&](auto t) {
+        constexpr int T = decltype(t)::value;
+        if (M <= 64) return launch_bt<T, 64>(enc, W, N, K, xh, M, y, st, num_sms, status);
+        if (M <= 128) return launch_bt<T, 128>(enc, W, N, K, xh, M, y, st, num_sms, status);
+        return launch_bt<T, 256>(enc, W, N, K, xh, M, y, st, num_sms, status);
+    };
+    if (type == QMM_Q6_K) return run(std::integral_constant<int, QMM_Q6_K>{});
+    if (type == QMM_Q8_0) return run(std::integral_constant<int, QMM_Q8_0>{});
+    return run(std::integral_constant<int, QMM_Q4_K>{});
 }
 
 }  // namespace qk

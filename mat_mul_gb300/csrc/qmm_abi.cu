@@ -274,8 +274,9 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     //   sb   : decode, one weight block per lane, quantises x itself (one
     //          launch, no workspace); M <= 8 when the activations fit
     //   gemv : decode, 32 units per round, after the quantiser kernel
-    //   gemm : prefill after the quantiser: Q4_K on tcgen05 (fp16 operands,
-    //          fp32 accumulators), other types on the int8 mma.sync kernel
+    //   gemm : prefill after the quantiser: on tcgen05 (fp16 operands, fp32
+    //          accumulators) when K is a multiple of 256, else on the int8
+    //          mma.sync kernel
     if (decode_on_tensor_cores(type, M, N, K, di)) {
         void *ws = nullptr;
         if (int rc = quantize_for_tensor_cores(dev, st, x, M, K, di, &ws)) return rc;
@@ -292,7 +293,7 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
         g_launches.fetch_add(1);
         return QMM_OK;
     }
-    // Prefill of Q4_K on the tcgen05 kernel: fp16 activations d*q [M][K].
+    // Prefill on the tcgen05 kernel: fp16 activations d*q [M][K].
     if (M > 8 && !g_force_mma_gemm && qk::gemm_tc_supported(type, N, K, M)) {
         const size_t xh_bytes = align_up(static_cast<size_t>(M * K) * 2, 256);
         const size_t d_bytes = align_up(static_cast<size_t>(M * (K / 32)) * 4, 256);

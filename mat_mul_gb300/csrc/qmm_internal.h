@@ -88,8 +88,8 @@ bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_
 cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
                             cudaStream_t st, int num_sms, int max_smem, int *status);
 
-// Prefill GEMM on tcgen05 (gemm_tc.cu): Q4_K weights, fp16 activations
-// xh [M][K] (d*q from the quantiser).  Returns cudaErrorNotSupported for
+// Prefill GEMM on tcgen05 (gemm_tc.cu): Q4_K, Q6_K or Q8_0 weights with K a
+// multiple of 256, fp16 activations xh [M][K] (d*q from the quantiser).  Returns cudaErrorNotSupported for
 // shapes it does not take.
 bool gemm_tc_supported(int type, int64_t N, int64_t K, int64_t M);
 cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const void *xh, int64_t M,

@@ -205,6 +205,24 @@ def test_qmm_prefill_small(cuda_lib, qtype, N, K, M):
     _assert_within_bound(y, yo, A, f"type {qtype} N={N} K={K} M={M}")
 
 
+# Q6_K and Q8_0 prefill on tcgen05 (the dequantisers copy their rows' raw
+# bytes): ragged N with the matrix ending off a 4-byte boundary, an odd
+# number of super-blocks per row (rows alternately 4- and 2-byte aligned),
+# split K (two CTAs per tile), M in each token-tile size.
+PREFILL_TC_OTHER = [(synth.Q6_K, 301, 768, 70), (synth.Q6_K, 1000, 2048, 64), (synth.Q6_K, 130, 5120, 300),
+                    (synth.Q6_K, 77, 256, 9), (synth.Q8_0, 301, 768, 70), (synth.Q8_0, 1000, 2048, 64),
+                    (synth.Q8_0, 257, 4352, 200), (synth.Q8_0, 33, 256, 129)]
+
+
+@pytest.mark.parametrize("qtype,N,K,M", PREFILL_TC_OTHER)
+def test_qmm_prefill_tcgen05_q6k_q8_0(cuda_lib, qtype, N, K, M):
+    W = synth.weights(qtype, N, K, seed=N + K + M + 17)
+    x = synth.activations(M, K, seed=N * K + M + 17, outlier_frac=0.01)
+    y = _run_qmm(cuda_lib, qtype, W, N, K, x)
+    yo, A = O.qmm(qtype, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"tcgen05 prefill type {qtype} N={N} K={K} M={M}")
+
+
 # Q4_K prefill shapes whose tiles the stream-K schedule of the tcgen05 GEMM
 # splits between CTA pairs: two pieces per tile with ragged M and N (and a
 # half-empty last pair), eight pieces (one tile summed from seven partials),
