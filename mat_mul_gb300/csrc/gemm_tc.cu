@@ -56,21 +56,24 @@ constexpr int Q_BYTES = BW * 64;    // this K step's 64 quant bytes of each row 
 constexpr int R_BYTES = H_BYTES + Q_BYTES;
 
 // Q6_K and Q8_0: rows are not 16-byte multiples, so no tensor map describes
-// them; each dequantiser warp copies the raw bytes of its 32 rows itself, one
-// super-step (two K steps, 256 weights: one Q6_K super-block, eight Q8_0
-// blocks) ahead, into two buffers of 32 rows x PITCH_W words (the bytes plus
-// up to 2 of alignment, an odd number of words: conflict-free per-row reads).
+// them; each dequantiser warp reads the raw bytes of its 32 rows itself with
+// coalesced loads into registers, one super-step (two K steps, 256 weights:
+// one Q6_K super-block, eight Q8_0 blocks) ahead, and stores them into two
+// buffers of 32 rows x PITCH_W words.  Q6_K: the 53 words from the
+// super-block's 4-byte aligned start (2-byte aligned rows), an odd pitch so
+// that per-row word reads are conflict-free.  Q8_0: the 272 bytes (16-byte
+// aligned), 17 chunks of 16 bytes per row, read back as whole chunks.
 template <int T>
 struct RawStep {
     static constexpr int BYTES = 0, PITCH_W = 0;
 };
 template <>
 struct RawStep<QMM_Q6_K> {
-    static constexpr int BYTES = 210, PITCH_W = 55;
+    static constexpr int BYTES = 210, PITCH_W = 53;
 };
 template <>
 struct RawStep<QMM_Q8_0> {
-    static constexpr int BYTES = 272, PITCH_W = 69;
+    static constexpr int BYTES = 272, PITCH_W = 68;
 };
 
 template <int BT, int T>
@@ -217,15 +220,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 4-byte asynchronous copy global -> shared (both 4-byte aligned), and its
-// group bookkeeping.
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+// Weight bytes read from global memory into registers (read once per CTA:
+// not kept in L1).
+__device__ __forceinline__ uint32_t ldg_b32(uint64_t a) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(a));
+    return v;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ uint32_t ldg_u16(uint64_t a) {
+    unsigned short v;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg_b128(uint64_t a) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(a));
+    return v;
 }
 
 // The 32-bit word at byte offset `off` (2-byte aligned) of a row buffer that
@@ -330,24 +342,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp == W_RLOAD) {
         // ------------------------------------------ raw weight producer (Q4_K)
-        if (!C::OWN && lane == 0) {
-            int issued = 0;
-            for (int kk = 0; kk < P.nsteps; ++kk) {
-                const int r = kk % C::R_STAGES;
-                if (kk >= C::R_STAGES &&
-                    (*abort_flag || !mbar_wait(bar_r_empty + 8 * r, ((kk / C::R_STAGES) - 1) & 1, P.status))) {
-                    *abort_flag = 1;
-                    break;
+        if constexpr (!C::OWN) {
+            if (lane == 0) {
+                int issued = 0;
+                for (int kk = 0; kk < P.nsteps; ++kk) {
+                    const int r = kk % C::R_STAGES;
+                    if (kk >= C::R_STAGES &&
+                        (*abort_flag || !mbar_wait(bar_r_empty + 8 * r, ((kk / C::R_STAGES) - 1) & 1, P.status))) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const int gk = k_step0 + kk;  // half gk&1 of super-block gk>>1
+                    const uint32_t st = sR + r * R_BYTES;
+                    mbar_arrive_expect_tx(bar_r_full + 8 * r, R_BYTES);
+                    tma_load_2d(st, &tmH, (gk >> 1) * RAW_ROW, n0, bar_r_full + 8 * r);
+                    tma_load_2d(st + H_BYTES, &tmQ, (gk >> 1) * RAW_ROW + 16 + 64 * (gk & 1), n0, bar_r_full + 8 * r);
+                    ++issued;
                 }
-                const int gk = k_step0 + kk;  // half gk&1 of super-block gk>>1
-                const uint32_t st = sR + r * R_BYTES;
-                mbar_arrive_expect_tx(bar_r_full + 8 * r, R_BYTES);
-                tma_load_2d(st, &tmH, (gk >> 1) * RAW_ROW, n0, bar_r_full + 8 * r);
-                tma_load_2d(st + H_BYTES, &tmQ, (gk >> 1) * RAW_ROW + 16 + 64 * (gk & 1), n0, bar_r_full + 8 * r);
-                ++issued;
+                for (int kk = issued > C::R_STAGES ? issued - C::R_STAGES : 0; kk < issued; ++kk)
+                    mbar_wait(bar_r_full + 8 * (kk % C::R_STAGES), (kk / C::R_STAGES) & 1, P.status);
             }
-            for (int kk = issued > C::R_STAGES ? issued - C::R_STAGES : 0; kk < issued; ++kk)
-                mbar_wait(bar_r_full + 8 * (kk % C::R_STAGES), (kk / C::R_STAGES) & 1, P.status);
         }
     } else if (warp == W_MMA) {
         // -------------------------------------------------- MMA issuer
@@ -443,35 +457,68 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint8_t *raw = smem + C::OFF_R + quarter * C::RAW_WARP;
             const int nss = P.nsteps / 2;  // super-steps of this CTA (its K range starts on one)
             const int js0 = k_step0 / 2;
-            const uint64_t wbase = reinterpret_cast<uint64_t>(P.W);
-            // copy super-step js (local) of the warp's rows into buffer js & 1:
-            // lane i copies words i, i+32, ... of each row, from the row's
-            // bytes rounded down to 4; the matrix's last 2 bytes, when they
-            // would need a word past its end, by a 2-byte load instead
-            auto fetch = [&](int js) {
-                uint8_t *buf = raw + (js & 1) * (32 * PW * 4);
-                for (int r = 0; r < 32; ++r) {
-                    const int64_t row = n0 + 32 * quarter + r;
-                    if (row >= P.N) break;
-                    const uint64_t seg = wbase + static_cast<uint64_t>(row) * P.RB +
-                                         static_cast<uint64_t>(js0 + js) * SSB;
-                    const uint64_t base = seg & ~uint64_t(3);
-                    const int nw = static_cast<int>((seg + SSB - base + 3) >> 2);
-                    const bool past = base + 4 * static_cast<uint64_t>(nw) > P.w_end;
-                    for (int i = lane; i < nw; i += 32) {
-                        uint8_t *dst = buf + (r * PW + i) * 4;
-                        if (past && i == nw - 1)
-                            *reinterpret_cast<uint32_t *>(dst) =
-                                __ldg(reinterpret_cast<const unsigned short *>(base + 4 * static_cast<uint64_t>(i)));
-                        else
-                            cp_async4(smem_u32(dst), reinterpret_cast<const void *>(base + 4 * static_cast<uint64_t>(i)));
+            const int nrows = min(32, P.N - (n0 + 32 * quarter));  // rows of the matrix (may be <= 0)
+            const uint64_t rows0 = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(n0 + 32 * quarter) * P.RB;
+            // the next super-step in flight: Q6_K lane l holds words l and
+            // 32 + l (l < 21) of each row; Q8_0 chunk lane + 32t of the 544
+            constexpr int NSTG = T == QMM_Q6_K ? 64 : 68;
+            uint32_t stg[NSTG];
+            auto load = [&](int js) {
+                const uint64_t seg0 = rows0 + static_cast<uint64_t>(js0 + js) * SSB;
+                if constexpr (T == QMM_Q6_K) {
+                    // only the matrix's final super-block can end within the
+                    // last word: there its final 2 bytes come from a 2-byte load
+                    const bool careful =
+                        nrows > 0 && ((seg0 + static_cast<uint64_t>(nrows - 1) * P.RB) & ~uint64_t(3)) + 4 * PW > P.w_end;
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        uint32_t v0 = 0, v1 = 0;
+                        if (r < nrows) {
+                            const uint64_t a = ((seg0 + static_cast<uint64_t>(r) * P.RB) & ~uint64_t(3)) + 4 * lane;
+                            if (!careful) {
+                                v0 = ldg_b32(a);
+                                if (lane < PW - 32) v1 = ldg_b32(a + 128);
+                            } else {
+                                v0 = a + 4 <= P.w_end ? ldg_b32(a) : ldg_u16(a);
+                                if (lane < PW - 32) v1 = a + 132 <= P.w_end ? ldg_b32(a + 128) : ldg_u16(a + 128);
+                            }
+                        }
+                        stg[2 * r] = v0;
+                        stg[2 * r + 1] = v1;
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 17; ++t) {
+                        const int f = lane + 32 * t, r = f / 17, c = f - 17 * r;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (r < nrows) v = ldg_b128(seg0 + static_cast<uint64_t>(r) * P.RB + 16 * c);
+                        stg[4 * t] = v.x;
+                        stg[4 * t + 1] = v.y;
+                        stg[4 * t + 2] = v.z;
+                        stg[4 * t + 3] = v.w;
                     }
                 }
-                cp_async_commit();
             };
-            fetch(0);
-            if (nss > 1) fetch(1);
-            const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+            // into buffer js & 1 (its previous super-step is read by every lane)
+            auto store = [&](int js) {
+                uint32_t *buf = reinterpret_cast<uint32_t *>(raw + (js & 1) * (32 * PW * 4));
+                if constexpr (T == QMM_Q6_K) {
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        buf[r * PW + lane] = stg[2 * r];
+                        if (lane < PW - 32) buf[r * PW + 32 + lane] = stg[2 * r + 1];
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 17; ++t)
+                        *reinterpret_cast<uint4 *>(buf + 4 * (lane + 32 * t)) =
+                            make_uint4(stg[4 * t], stg[4 * t + 1], stg[4 * t + 2], stg[4 * t + 3]);
+                }
+            };
+            load(0);
+            store(0);
+            __syncwarp();
+            if (nss > 1) load(1);
             for (int kk = 0; kk < P.nsteps; ++kk) {
                 const int js = kk >> 1, h = kk & 1, sa = kk % A_STAGES;
                 bool ok = !*abort_flag;
@@ -480,18 +527,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     *abort_flag = 1;
                     break;
                 }
-                if (h == 0) {
-                    // super-step js has landed: every group but the newest
-                    if (js + 1 < nss) cp_async_wait<1>();
-                    else cp_async_wait<0>();
-                    __syncwarp();
-                }
                 tc_fence_after();
                 const uint8_t *row = raw + (js & 1) * (32 * PW * 4) + lane * PW * 4;
-                // the row's bytes start at this offset inside its buffer
-                const int dl = static_cast<int>((wbase + static_cast<uint64_t>(n0 + n) * P.RB +
-                                                 static_cast<uint64_t>(js0 + js) * SSB) & 3);
                 if constexpr (T == QMM_Q6_K) {
+                    // the row's bytes start at this offset (0 or 2) of its words
+                    const int dl = static_cast<int>((rows0 + static_cast<uint64_t>(lane) * P.RB +
+                                                     static_cast<uint64_t>(js0 + js) * SSB) & 3);
                     // half h of the super-block: ql bytes 64h.., qh 128+32h.., scales
                     // 192+8h.., d at 208; weight 32qi + l: low bits from ql byte
                     // 32(qi&1) + l (nibble qi>>1), high bits (qh byte l >> 2qi) & 3,
@@ -534,41 +575,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
                         tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
                     }
-                    (void)k1024;
                 } else {
-                    // blocks 4h .. 4h+3 of the eight: d (fp16), then 32 int8; w = d * q
-                    const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));  // 1152 = 1024 + 128
+                    // blocks 4h .. 4h+3 of the eight: d (fp16), then 32 int8; w = d * q.
+                    // They lie in bytes 136h .. 136h+135 of the row: chunks 8h .. 8h+8
+                    // (h a constant below, so that every word index is one).
+                    auto dequant_half = [&](auto hc) {
+                        constexpr int H = decltype(hc)::value;
+                        uint32_t w[36];
 #pragma unroll
-                    for (int cp = 0; cp < 2; ++cp) {  // blocks 4h + 2cp, 4h + 2cp + 1
-                        uint32_t r[32];
-#pragma unroll
-                        for (int bb = 0; bb < 2; ++bb) {
-                            const int ob = 34 * (4 * h + 2 * cp + bb);
-                            const __half dh = *reinterpret_cast<const __half *>(row + dl + ob);
-                            const __half2 s = __half2half2(dh);
-#pragma unroll
-                            for (int lw = 0; lw < 8; ++lw) {
-                                const uint32_t q = row_word(row, dl + ob + 2 + 4 * lw);
-                                // bytes (q0 ^ 0x80, 0x64, q1 ^ 0x80, 0x64): 1024 + 128 + q
-                                const uint32_t p0 = __byte_perm(q, 0x64646464u, 0x4140u) ^ 0x00800080u;
-                                const uint32_t p1 = __byte_perm(q, 0x64646464u, 0x4342u) ^ 0x00800080u;
-                                const __half2 w0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1152), s);
-                                const __half2 w1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1152), s);
-                                r[16 * bb + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
-                                r[16 * bb + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
-                            }
+                        for (int c = 0; c < 9; ++c) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (8 * H + c));
+                            w[4 * c] = v.x;
+                            w[4 * c + 1] = v.y;
+                            w[4 * c + 2] = v.z;
+                            w[4 * c + 3] = v.w;
                         }
-                        tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
-                    }
-                    (void)k1024;
+                        // the 32-bit word at (even) byte offset o of those chunks
+                        auto word_at = [&](int o) {
+                            return (o & 2) ? __funnelshift_r(w[o >> 2], w[(o >> 2) + 1], 16) : w[o >> 2];
+                        };
+                        const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));  // 1152 = 1024 + 128
+#pragma unroll
+                        for (int cp = 0; cp < 2; ++cp) {  // blocks 4H + 2cp, 4H + 2cp + 1
+                            uint32_t r[32];
+#pragma unroll
+                            for (int bb = 0; bb < 2; ++bb) {
+                                const int ob = 34 * (2 * cp + bb) + 8 * H;  // within chunk 8H
+                                const __half2 s =
+                                    __half2half2(__ushort_as_half(static_cast<unsigned short>(word_at(ob))));
+#pragma unroll
+                                for (int lw = 0; lw < 8; ++lw) {
+                                    const uint32_t q = word_at(ob + 2 + 4 * lw);
+                                    // bytes (q0 ^ 0x80, 0x64, q1 ^ 0x80, 0x64): 1024 + 128 + q
+                                    const uint32_t p0 = __byte_perm(q, 0x64646464u, 0x4140u) ^ 0x00800080u;
+                                    const uint32_t p1 = __byte_perm(q, 0x64646464u, 0x4342u) ^ 0x00800080u;
+                                    const __half2 w0 =
+                                        __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1152), s);
+                                    const __half2 w1 =
+                                        __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1152), s);
+                                    r[16 * bb + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
+                                    r[16 * bb + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
+                                }
+                            }
+                            tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
+                        }
+                    };
+                    if (h == 0) dequant_half(std::integral_constant<int, 0>{});
+                    else dequant_half(std::integral_constant<int, 1>{});
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_a_full + 8 * sa);
-                // buffer js & 1 is read by every lane: the super-step after next
-                if (h == 1 && js + 2 < nss) fetch(js + 2);
+                // super-step js is done: the next one goes into the other
+                // buffer (read by every lane two steps ago), the one after
+                // that into the registers
+                if (h == 1 && js + 1 < nss) {
+                    store(js + 1);
+                    __syncwarp();
+                    if (js + 2 < nss) load(js + 2);
+                }
             }
-            cp_async_wait<0>();  // no copy in flight at exit
         }
         // epilogue: TMEM lanes of this quarter, all BT token columns
         const bool ok = mbar_wait(bar_acc, 0, P.status);
