@@ -11,7 +11,8 @@ decode GEMV).  `value` is the step's weight bytes / device time (GB/s); the
 447 MB of weights per step exceed the 129 MB L2, so every matrix is re-read
 from HBM.  The same run also times:
   * every matrix alone over rotating copies (>= 4x L2) -> per-matrix GB/s,
-  * the Q4_K prefill GEMM at M=512 (Mistral-7B MLP up and down) -> TOPS,
+  * the prefill GEMM at M=512 -> TOPS: Q4_K (Mistral-7B MLP up and down),
+    Q6_K (the Qwen3-14B-shaped layer's v and down), Q8_0 (Mistral up shape),
   * the dominant kernel (the Q6_K lm_head GEMV) for the roofline object,
   * the end-to-end step with host buffers (x copied in, y copied out),
   * the CPU oracle on a bounded sample (cpu_baseline).
@@ -483,9 +484,21 @@ def run_ours(args):
 
         # ---- prefill GEMM, M=512
         gemm = []
-        for idx, (name, qtype, K, N) in enumerate(synth.CONFIGS[4]["mats"]):
-            W = torch.from_numpy(synth.config_weights(4, idx)).to(dev)
-            x = torch.from_numpy(synth.config_activations(4, 512, K)).to(dev)
+        # the Q4_K Mistral-7B MLP, the Q6_K matrices of the Qwen3-14B-shaped
+        # layer, and Q8_0 weights in the Mistral up shape (cfg 0's Q8_0
+        # value distribution), all at M=512
+        prefill_cases = [(f"mistral_{name}", qtype, K, N, synth.config_weights(4, idx),
+                          synth.config_activations(4, 512, K))
+                         for idx, (name, qtype, K, N) in enumerate(synth.CONFIGS[4]["mats"])]
+        prefill_cases += [(f"qwen3_14b_{name}", qtype, K, N, synth.config_weights(3, idx),
+                           synth.config_activations(4, 512, K))
+                          for idx, (name, qtype, K, N) in enumerate(synth.CONFIGS[3]["mats"]) if qtype == synth.Q6_K]
+        prefill_cases.append(("q8_0_mistral_up", synth.Q8_0, 4096, 14336,
+                              synth.weights(synth.Q8_0, 14336, 4096, seed=4100),
+                              synth.config_activations(4, 512, 4096)))
+        for name, qtype, K, N, w_np, x_np in prefill_cases:
+            W = torch.from_numpy(w_np).to(dev)
+            x = torch.from_numpy(x_np).to(dev)
             y = torch.empty((512, N), dtype=torch.float32, device=dev)
 
             def gcall(W=W, x=x, y=y, qtype=qtype, K=K, N=N):
@@ -495,7 +508,7 @@ def run_ours(args):
             g = capture(gcall)
             t_ms = timed(g, 4, 1) / 5
             tops = 2 * 512 * N * K / (t_ms * 1e-3) / 1e12
-            gemm.append({"matrix": f"mistral_{name}", "M": 512, "K": K, "N": N,
+            gemm.append({"matrix": name, "type": ["Q8_0", "Q4_K", "Q6_K"][qtype], "M": 512, "K": K, "N": N,
                          "us": round(t_ms * 1e3, 1), "TOPS": round(tops, 1)})
             del g
         int8_peak = None

@@ -57,23 +57,23 @@ constexpr int R_BYTES = H_BYTES + Q_BYTES;
 
 // Q6_K and Q8_0: rows are not 16-byte multiples, so no tensor map describes
 // them; each dequantiser warp reads the raw bytes of its 32 rows itself with
-// coalesced loads into registers, one super-step (two K steps, 256 weights:
+// 16-byte loads into registers, one super-step (two K steps, 256 weights:
 // one Q6_K super-block, eight Q8_0 blocks) ahead, and stores them into two
-// buffers of 32 rows x PITCH_W words.  Q6_K: the 53 words from the
-// super-block's 4-byte aligned start (2-byte aligned rows), an odd pitch so
-// that per-row word reads are conflict-free.  Q8_0: the 272 bytes (16-byte
-// aligned), 17 chunks of 16 bytes per row, read back as whole chunks.
+// buffers of 32 rows x PITCH_W words, read back as whole 16-byte chunks (an
+// odd number of chunks per row: conflict-free).  Q6_K: the 14 chunks from
+// the 16-byte boundary at or below the super-block's start (rows are only
+// 2-byte aligned), Q8_0: the 17 chunks of its 272 bytes.
 template <int T>
 struct RawStep {
-    static constexpr int BYTES = 0, PITCH_W = 0;
+    static constexpr int BYTES = 0, CHUNKS = 0, PITCH_W = 0;
 };
 template <>
 struct RawStep<QMM_Q6_K> {
-    static constexpr int BYTES = 210, PITCH_W = 53;
+    static constexpr int BYTES = 210, CHUNKS = 14, PITCH_W = 60;
 };
 template <>
 struct RawStep<QMM_Q8_0> {
-    static constexpr int BYTES = 272, PITCH_W = 68;
+    static constexpr int BYTES = 272, CHUNKS = 17, PITCH_W = 68;
 };
 
 template <int BT, int T>
@@ -245,6 +245,21 @@ __device__ __forceinline__ uint4 ldg_b128(uint64_t a) {
 __device__ __forceinline__ uint32_t row_word(const uint8_t *row, int off) {
     const uint32_t *a = reinterpret_cast<const uint32_t *>(row + (off & ~3));
     return __funnelshift_r(a[0], a[1], (off & 2) * 8);
+}
+
+// out[j] = the 32-bit word at byte 4j + o (o even, o < 16) of the words w,
+// for registers w: the word offset o >> 2 is chosen by two selects per word
+// (no indexing of w by a variable), then the half-word offset by a shift.
+template <int NIN, int NOUT>
+__device__ __forceinline__ void realign(const uint32_t (&w)[NIN], int o, uint32_t (&out)[NOUT]) {
+    static_assert(NIN >= NOUT + 4, "realign reads NOUT + 4 words");
+    uint32_t t[NOUT + 3], u[NOUT + 1];
+#pragma unroll
+    for (int j = 0; j < NOUT + 3; ++j) t[j] = (o & 4) ? w[j + 1] : w[j];
+#pragma unroll
+    for (int j = 0; j < NOUT + 1; ++j) u[j] = (o & 8) ? t[j + 2] : t[j];
+#pragma unroll
+    for (int j = 0; j < NOUT; ++j) out[j] = __funnelshift_r(u[j], u[j + 1], (o & 2) * 8);
 }
 
 // Four fp16 weights from the four bytes of a quant word (low nibbles, or
@@ -459,60 +474,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int js0 = k_step0 / 2;
             const int nrows = min(32, P.N - (n0 + 32 * quarter));  // rows of the matrix (may be <= 0)
             const uint64_t rows0 = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(n0 + 32 * quarter) * P.RB;
-            // the next super-step in flight: Q6_K lane l holds words l and
-            // 32 + l (l < 21) of each row; Q8_0 chunk lane + 32t of the 544
-            constexpr int NSTG = T == QMM_Q6_K ? 64 : 68;
-            uint32_t stg[NSTG];
+            // the next super-step in flight: chunk lane + 32t of the warp's
+            // 32 x CH (row-major)
+            constexpr int CH = RawStep<T>::CHUNKS, NT = 32 * CH / 32;
+            uint32_t stg[4 * NT];
             auto load = [&](int js) {
                 const uint64_t seg0 = rows0 + static_cast<uint64_t>(js0 + js) * SSB;
-                if constexpr (T == QMM_Q6_K) {
-                    // only the matrix's final super-block can end within the
-                    // last word: there its final 2 bytes come from a 2-byte load
-                    const bool careful =
-                        nrows > 0 && ((seg0 + static_cast<uint64_t>(nrows - 1) * P.RB) & ~uint64_t(3)) + 4 * PW > P.w_end;
+                // Q6_K: the chunks of the matrix's final super-block may reach
+                // past its end; there each word is loaded only as far as it lies
+                // inside (a 2-byte load for a word that straddles the end)
+                const bool careful = T == QMM_Q6_K && nrows > 0 &&
+                                     ((seg0 + static_cast<uint64_t>(nrows - 1) * P.RB) & ~uint64_t(15)) + 16 * CH > P.w_end;
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) {
-                        uint32_t v0 = 0, v1 = 0;
-                        if (r < nrows) {
-                            const uint64_t a = ((seg0 + static_cast<uint64_t>(r) * P.RB) & ~uint64_t(3)) + 4 * lane;
-                            if (!careful) {
-                                v0 = ldg_b32(a);
-                                if (lane < PW - 32) v1 = ldg_b32(a + 128);
-                            } else {
-                                v0 = a + 4 <= P.w_end ? ldg_b32(a) : ldg_u16(a);
-                                if (lane < PW - 32) v1 = a + 132 <= P.w_end ? ldg_b32(a + 128) : ldg_u16(a + 128);
+                for (int t = 0; t < NT; ++t) {
+                    const int f = lane + 32 * t, r = f / CH, c = f - CH * r;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < nrows) {
+                        const uint64_t a = ((seg0 + static_cast<uint64_t>(r) * P.RB) & ~uint64_t(15)) + 16 * c;
+                        if (!careful || a + 16 <= P.w_end) {
+                            v = ldg_b128(a);
+                        } else {
+                            uint32_t e[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint64_t ai = a + 4 * i;
+                                e[i] = ai + 4 <= P.w_end ? ldg_b32(ai) : ai + 2 <= P.w_end ? ldg_u16(ai) : 0u;
                             }
+                            v = make_uint4(e[0], e[1], e[2], e[3]);
                         }
-                        stg[2 * r] = v0;
-                        stg[2 * r + 1] = v1;
                     }
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 17; ++t) {
-                        const int f = lane + 32 * t, r = f / 17, c = f - 17 * r;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (r < nrows) v = ldg_b128(seg0 + static_cast<uint64_t>(r) * P.RB + 16 * c);
-                        stg[4 * t] = v.x;
-                        stg[4 * t + 1] = v.y;
-                        stg[4 * t + 2] = v.z;
-                        stg[4 * t + 3] = v.w;
-                    }
+                    stg[4 * t] = v.x;
+                    stg[4 * t + 1] = v.y;
+                    stg[4 * t + 2] = v.z;
+                    stg[4 * t + 3] = v.w;
                 }
             };
             // into buffer js & 1 (its previous super-step is read by every lane)
             auto store = [&](int js) {
-                uint32_t *buf = reinterpret_cast<uint32_t *>(raw + (js & 1) * (32 * PW * 4));
-                if constexpr (T == QMM_Q6_K) {
+                uint8_t *buf = raw + (js & 1) * (32 * PW * 4);
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) {
-                        buf[r * PW + lane] = stg[2 * r];
-                        if (lane < PW - 32) buf[r * PW + 32 + lane] = stg[2 * r + 1];
-                    }
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 17; ++t)
-                        *reinterpret_cast<uint4 *>(buf + 4 * (lane + 32 * t)) =
-                            make_uint4(stg[4 * t], stg[4 * t + 1], stg[4 * t + 2], stg[4 * t + 3]);
+                for (int t = 0; t < NT; ++t) {
+                    const int f = lane + 32 * t, r = f / CH, c = f - CH * r;
+                    *reinterpret_cast<uint4 *>(buf + r * (PW * 4) + 16 * c) =
+                        make_uint4(stg[4 * t], stg[4 * t + 1], stg[4 * t + 2], stg[4 * t + 3]);
                 }
             };
             load(0);
@@ -530,21 +534,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_after();
                 const uint8_t *row = raw + (js & 1) * (32 * PW * 4) + lane * PW * 4;
                 if constexpr (T == QMM_Q6_K) {
-                    // the row's bytes start at this offset (0 or 2) of its words
+                    // the super-block starts at this (even) byte of its first chunk
                     const int dl = static_cast<int>((rows0 + static_cast<uint64_t>(lane) * P.RB +
-                                                     static_cast<uint64_t>(js0 + js) * SSB) & 3);
+                                                     static_cast<uint64_t>(js0 + js) * SSB) & 15);
                     // half h of the super-block: ql bytes 64h.., qh 128+32h.., scales
                     // 192+8h.., d at 208; weight 32qi + l: low bits from ql byte
                     // 32(qi&1) + l (nibble qi>>1), high bits (qh byte l >> 2qi) & 3,
                     // scale 8h + 2qi + (l >= 16); w = d*sc * (q - 32)
                     const float d = __half2float(*reinterpret_cast<const __half *>(row + dl + 208));
                     const uint32_t sc0 = row_word(row, dl + 192 + 8 * h), sc1 = row_word(row, dl + 196 + 8 * h);
-                    uint32_t qh[8], ql[2][8];
+                    // ql bytes 64h .. 64h+63 lie in chunks 4h .. 4h+4, qh bytes
+                    // 128+32h .. 128+32h+31 in chunks 8+2h .. 10+2h
+                    uint32_t wl[20], wh[12], qh[8], ql[2][8];
+#pragma unroll
+                    for (int c = 0; c < 5; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (4 * h + c));
+                        wl[4 * c] = v.x;
+                        wl[4 * c + 1] = v.y;
+                        wl[4 * c + 2] = v.z;
+                        wl[4 * c + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 3; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (8 + 2 * h + c));
+                        wh[4 * c] = v.x;
+                        wh[4 * c + 1] = v.y;
+                        wh[4 * c + 2] = v.z;
+                        wh[4 * c + 3] = v.w;
+                    }
+                    uint32_t qlw[16];
+                    realign(wl, dl, qlw);
+                    realign(wh, dl, qh);
 #pragma unroll
                     for (int lw = 0; lw < 8; ++lw) {
-                        qh[lw] = row_word(row, dl + 128 + 32 * h + 4 * lw);
-                        ql[0][lw] = row_word(row, dl + 64 * h + 4 * lw);
-                        ql[1][lw] = row_word(row, dl + 64 * h + 32 + 4 * lw);
+                        ql[0][lw] = qlw[lw];
+                        ql[1][lw] = qlw[8 + lw];
                     }
                     const __half2 k1056 = __half2half2(__ushort_as_half(0x6420));  // 1056 = 1024 + 32
 #pragma unroll
