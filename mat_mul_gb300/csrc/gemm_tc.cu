@@ -1,13 +1,14 @@
-// gemm_tc.cu -- prefill product y[M,N] = W[N,K] . x[M,K]^T for Q4_K weights
-// on the fifth-generation tensor cores (tcgen05, operands and accumulators in
-// tensor memory).
+// gemm_tc.cu -- prefill product y[M,N] = W[N,K] . x[M,K]^T for Q4_K, Q6_K
+// and Q8_0 weights on the fifth-generation tensor cores (tcgen05, operands
+// and accumulators in tensor memory).
 //
 // sm_103a has no integer tcgen05 mode, so the contraction runs in kind::f16
 // with the roles chosen so that the dequantised weights never pass through
 // shared memory:
-//   A (128 x 128 per K step) = weights d*sc*q - dmin*m rounded to fp16,
-//       written straight into TMEM by four dequantiser warps (tcgen05.st)
-//       from the raw super-block bytes that TMA brings into shared memory;
+//   A (128 x 128 per K step) = the weights (Q4_K d*sc*q - dmin*m, Q6_K
+//       d*sc*(q-32), Q8_0 d*q) rounded to fp16, written straight into TMEM
+//       by eight dequantiser warps (tcgen05.st) from the raw block bytes in
+//       shared memory;
 //   B (BT x 128) = the dequantised activations d_x*q_x rounded to fp16 (from the
 //       quantiser), loaded by TMA with the 128-byte swizzle; BT = 64/128/256
 //       tokens, so the weight tile is reused across up to 256 tokens;
@@ -20,15 +21,18 @@
 // multicasts it to both, halving the L2 reads of the activations; each MMA
 // commit frees the stage in both CTAs.
 //
-// Warp roles (7 warps), per 128-wide K step (half a super-block):
+// Warp roles (11 warps), per 128-wide K step (half a super-block):
 //   0 = token producer: one token box for the pair (ring released by the
 //       MMA commits of both CTAs);
-//   6 = raw weight producer: the 16-byte super-block header and the 64
-//       quant bytes of each of the 128 weight rows (ring released by the
-//       dequantisers, so dequantisation runs ahead of the MMA);
+//   10 = raw weight producer (Q4_K): the 16-byte super-block header and the
+//       64 quant bytes of each of the 128 weight rows (ring released by the
+//       dequantisers, so dequantisation runs ahead of the MMA); Q6_K and
+//       Q8_0 rows are not 16-byte multiples, so there the dequantisers load
+//       their rows' bytes themselves;
 //   1 = MMA issuer (and TMEM owner);
-//   2..5 = dequantiser (warp w serves TMEM lanes 32*(w%4)..), then epilogue
-//       (TMEM -> y).
+//   2..9 = dequantisers, two per TMEM lane quarter (warp w serves lanes
+//       32*(w%4).. and the K step's weights 64*((w-2)/4)..), then epilogue
+//       (TMEM -> y, half of the token columns each).
 // All waits are bounded; on a timeout the CTA stops issuing, drains what it
 // issued, frees TMEM and returns with the status word set.
 #include <cuda.h>
@@ -48,8 +52,10 @@ __host__ __device__ constexpr int qk_block_bytes(int t) { return t == QMM_Q8_0 ?
 constexpr int BW = 128, BK = 128;  // weight rows per tile, K per step (half a super-block)
 constexpr int A_STAGES = 4;        // dequantised weight stages in TMEM (64 columns each)
 constexpr int A_COLS = BK / 2;     // two fp16 weights per 32-bit TMEM column
-constexpr int W_XLOAD = 0, W_MMA = 1, W_RLOAD = 6;  // warps 2..5: dequantisers
-constexpr int NTHREADS = 7 * 32;
+// warps 2..9: dequantisers, two per TMEM lane quarter (warp w serves lanes
+// 32*(w%4).. and weights 64*((w-2)/4).. of every K step)
+constexpr int W_XLOAD = 0, W_MMA = 1, W_RLOAD = 10;
+constexpr int NTHREADS = 11 * 32;
 constexpr int RAW_ROW = 144;        // one Q4_K super-block per weight row
 constexpr int H_BYTES = BW * 16;    // d, dmin and the 12 scale bytes of each row
 constexpr int Q_BYTES = BW * 64;    // this K step's 64 quant bytes of each row (64-byte swizzle)
@@ -81,12 +87,13 @@ struct TcCfg {
     static constexpr bool OWN = T != QMM_Q4_K;  // the dequantisers copy their own raw bytes
     static constexpr int XBOX = BT * 128;   // one 64-wide K box of tokens (128-byte swizzle rows)
     static constexpr int X_BYTES = 2 * XBOX;
-    static constexpr int X_STAGES = OWN ? (BT == 256 ? 2 : BT == 128 ? 4 : 8) : (BT == 256 ? 3 : BT == 128 ? 5 : 8);
+    static constexpr int RAW_Q = 32 * RawStep<T>::PITCH_W * 4;  // one super-step of a lane quarter's rows (OWN)
+    static constexpr int X_FIT = (232448 - 1536 - 4 * RAW_Q) / X_BYTES;
+    static constexpr int X_STAGES = OWN ? (X_FIT > 8 ? 8 : X_FIT) : (BT == 256 ? 3 : BT == 128 ? 5 : 8);
     static constexpr int OFF_R = X_STAGES * X_BYTES;
-    static constexpr int RAW_WARP = 2 * 32 * RawStep<T>::PITCH_W * 4;  // per dequantiser warp (OWN)
     static constexpr int R_STAGES_FIT = OWN ? 0 : (232448 - 1536 - OFF_R) / R_BYTES;
     static constexpr int R_STAGES = R_STAGES_FIT > 8 ? 8 : R_STAGES_FIT;
-    static constexpr int OFF_BAR = OFF_R + (OWN ? 4 * RAW_WARP : R_STAGES * R_BYTES);
+    static constexpr int OFF_BAR = OFF_R + (OWN ? 4 * RAW_Q : R_STAGES * R_BYTES);
     static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // barriers + base alignment slack
     static constexpr int A_COL0 = BT;                         // TMEM columns of the A stages
     static constexpr int TMEM_COLS = BT + A_COLS * A_STAGES <= 256 ? 256 : 512;
@@ -95,7 +102,7 @@ struct TcCfg {
     static_assert(X_BYTES % 1024 == 0 && R_BYTES % 1024 == 0, "stage alignment");
     static_assert(OWN || R_STAGES >= 3, "raw ring depth");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
-    static_assert(16 * (X_STAGES + R_STAGES + A_STAGES) + 8 <= 480, "barrier area");
+    static_assert(16 * (X_STAGES + R_STAGES + A_STAGES) + 8 + 64 <= 480, "barrier area");
     static_assert(BT + A_COLS * A_STAGES <= TMEM_COLS, "tensor memory");
 };
 
@@ -207,7 +214,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 // 32 consecutive 32-bit columns (64 fp16 weights) into this warp's 32 TMEM
-// lanes; the stores are complete when the function returns.
+// lanes; complete after tmem_wait_st().
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -217,8 +224,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Weight bytes read from global memory into registers (read once per CTA:
 // not kept in L1).
@@ -295,6 +302,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t bar_r_full = bar_x_empty + 8 * C::X_STAGES, bar_r_empty = bar_r_full + 8 * C::R_STAGES;
     const uint32_t bar_a_full = bar_r_empty + 8 * C::R_STAGES, bar_a_empty = bar_a_full + 8 * A_STAGES;
     const uint32_t bar_acc = bar_a_empty + 8 * A_STAGES;
+    // Q6_K / Q8_0: per lane quarter, its raw super-step buffer is full / has been read
+    const uint32_t bar_p_full = bar_acc + 8, bar_p_empty = bar_p_full + 32;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_BAR + 480);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_BAR + 488);
 
@@ -305,13 +314,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int s = 0; s < C::R_STAGES; ++s) {
             mbar_init(bar_r_full + 8 * s, 1);
-            mbar_init(bar_r_empty + 8 * s, 4);  // the four dequantiser warps
+            mbar_init(bar_r_empty + 8 * s, 8);  // the eight dequantiser warps
         }
         for (int s = 0; s < A_STAGES; ++s) {
-            mbar_init(bar_a_full + 8 * s, 4);
+            mbar_init(bar_a_full + 8 * s, 8);
             mbar_init(bar_a_empty + 8 * s, 1);
         }
         mbar_init(bar_acc, 1);
+        for (int qd = 0; qd < 4; ++qd) {
+            mbar_init(bar_p_full + 8 * qd, 64);  // every lane of the quarter's two warps
+            mbar_init(bar_p_empty + 8 * qd, 64);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -403,11 +416,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else {
         // ------------------------------------- dequantiser, then epilogue
-        // The four warps take every K step in order, so each parity wait on
-        // a ring stage is at most one phase ahead of the stage.
-        const int quarter = warp & 3;
+        // The eight warps take every K step in order, so each parity wait on
+        // a ring stage is at most one phase ahead of the stage.  Warp w fills
+        // the TMEM lanes of quarter w % 4 (weight rows 32*(w%4)..) with weights
+        // 64*cp .. 64*cp+63 of the K step, cp = (w - 2) / 4.
+        const int quarter = warp & 3, cp = (warp - 2) >> 2;
         const int n = 32 * quarter + lane;  // weight row within the tile (= TMEM lane)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+        const uint32_t a_col = C::A_COL0 + 32 * cp;  // + A_COLS * stage
         if constexpr (!C::OWN) {
             for (int kk = 0; kk < P.nsteps; ++kk) {
                 const int r = kk % C::R_STAGES, sa = kk % A_STAGES;
@@ -437,28 +453,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // (TMA 64-byte swizzle), so a quarter warp's loads hit distinct banks
                 const uint8_t *qrow = st + H_BYTES + 64 * n;
                 const int sw = (n >> 1) & 3;
-    #pragma unroll
-                for (int cp = 0; cp < 2; ++cp) {
-                    // chunk cp of 64 weights: quant bytes 32cp..32cp+31, low nibbles
-                    // -> sub-block 4h+2cp, high nibbles -> sub-block 4h+2cp+1
-                    const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp) ^ sw));
-                    const uint4 qb = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp + 1) ^ sw));
-                    const int sh = 16 * cp;
-                    const __half2 ha0 = __float2half2_rn(d * static_cast<float>((scw >> sh) & 0xFF));
-                    const __half2 ha1 = __float2half2_rn(d * static_cast<float>((scw >> (sh + 8)) & 0xFF));
-                    const __half2 hb0 = __float2half2_rn(-(dmin * static_cast<float>((mw >> sh) & 0xFF)));
-                    const __half2 hb1 = __float2half2_rn(-(dmin * static_cast<float>((mw >> (sh + 8)) & 0xFF)));
-                    // weight l < 32 of the chunk is the low nibble of quant byte l,
-                    // weight 32 + l its high nibble; TMEM column i holds weights 2i, 2i+1
-                    const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-                    uint32_t r[32];
-    #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        dequant4(qw[i], false, ha0, hb0, r[2 * i], r[2 * i + 1]);
-                        dequant4(qw[i], true, ha1, hb1, r[16 + 2 * i], r[16 + 2 * i + 1]);
-                    }
-                    tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
+                // chunk cp of 64 weights: quant bytes 32cp..32cp+31, low nibbles
+                // -> sub-block 4h+2cp, high nibbles -> sub-block 4h+2cp+1
+                const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp) ^ sw));
+                const uint4 qb = *reinterpret_cast<const uint4 *>(qrow + 16 * ((2 * cp + 1) ^ sw));
+                const int sh = 16 * cp;
+                const __half2 ha0 = __float2half2_rn(d * static_cast<float>((scw >> sh) & 0xFF));
+                const __half2 ha1 = __float2half2_rn(d * static_cast<float>((scw >> (sh + 8)) & 0xFF));
+                const __half2 hb0 = __float2half2_rn(-(dmin * static_cast<float>((mw >> sh) & 0xFF)));
+                const __half2 hb1 = __float2half2_rn(-(dmin * static_cast<float>((mw >> (sh + 8)) & 0xFF)));
+                // weight l < 32 of the chunk is the low nibble of quant byte l,
+                // weight 32 + l its high nibble; TMEM column i holds weights 2i, 2i+1
+                const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                uint32_t rr[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    dequant4(qw[i], false, ha0, hb0, rr[2 * i], rr[2 * i + 1]);
+                    dequant4(qw[i], true, ha1, hb1, rr[16 + 2 * i], rr[16 + 2 * i + 1]);
                 }
+                tmem_st32(lane_base + a_col + A_COLS * sa, rr);
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -467,16 +481,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         } else {
-            // Q6_K / Q8_0: this warp's 32 rows, one super-step at a time
+            // Q6_K / Q8_0: the quarter's 32 rows, one super-step at a time, in
+            // one buffer that its two warps fill (half the chunks each) and
+            // read; p_full / p_empty hand it over (each completes once per
+            // super-step, 64 lanes arriving)
             constexpr int SSB = RawStep<T>::BYTES, PW = RawStep<T>::PITCH_W;
-            uint8_t *raw = smem + C::OFF_R + quarter * C::RAW_WARP;
+            uint8_t *raw = smem + C::OFF_R + quarter * C::RAW_Q;
+            const uint32_t p_full = bar_p_full + 8 * quarter, p_empty = bar_p_empty + 8 * quarter;
             const int nss = P.nsteps / 2;  // super-steps of this CTA (its K range starts on one)
             const int js0 = k_step0 / 2;
             const int nrows = min(32, P.N - (n0 + 32 * quarter));  // rows of the matrix (may be <= 0)
             const uint64_t rows0 = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(n0 + 32 * quarter) * P.RB;
-            // the next super-step in flight: chunk lane + 32t of the warp's
-            // 32 x CH (row-major)
-            constexpr int CH = RawStep<T>::CHUNKS, NT = 32 * CH / 32;
+            // this warp's half of the 32 x CH chunks (row-major): chunk
+            // HALF*cp + lane + 32t, t < NT, while lane + 32t < HALF
+            constexpr int CH = RawStep<T>::CHUNKS, HALF = 32 * CH / 2, NT = (HALF + 31) / 32;
             uint32_t stg[4 * NT];
             auto load = [&](int js) {
                 const uint64_t seg0 = rows0 + static_cast<uint64_t>(js0 + js) * SSB;
@@ -487,18 +505,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                      ((seg0 + static_cast<uint64_t>(nrows - 1) * P.RB) & ~uint64_t(15)) + 16 * CH > P.w_end;
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    const int f = lane + 32 * t, r = f / CH, c = f - CH * r;
+                    const int i = lane + 32 * t, g = HALF * cp + i, r = g / CH, c = g - CH * r;
                     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (r < nrows) {
+                    if ((HALF % 32 == 0 || i < HALF) && r < nrows) {
                         const uint64_t a = ((seg0 + static_cast<uint64_t>(r) * P.RB) & ~uint64_t(15)) + 16 * c;
                         if (!careful || a + 16 <= P.w_end) {
                             v = ldg_b128(a);
                         } else {
                             uint32_t e[4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const uint64_t ai = a + 4 * i;
-                                e[i] = ai + 4 <= P.w_end ? ldg_b32(ai) : ai + 2 <= P.w_end ? ldg_u16(ai) : 0u;
+                            for (int q = 0; q < 4; ++q) {
+                                const uint64_t aq = a + 4 * q;
+                                e[q] = aq + 4 <= P.w_end ? ldg_b32(aq) : aq + 2 <= P.w_end ? ldg_u16(aq) : 0u;
                             }
                             v = make_uint4(e[0], e[1], e[2], e[3]);
                         }
@@ -509,30 +527,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     stg[4 * t + 3] = v.w;
                 }
             };
-            // into buffer js & 1 (its previous super-step is read by every lane)
-            auto store = [&](int js) {
-                uint8_t *buf = raw + (js & 1) * (32 * PW * 4);
+            // into the buffer (the quarter's reads of the previous super-step are done)
+            auto store = [&]() {
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    const int f = lane + 32 * t, r = f / CH, c = f - CH * r;
-                    *reinterpret_cast<uint4 *>(buf + r * (PW * 4) + 16 * c) =
-                        make_uint4(stg[4 * t], stg[4 * t + 1], stg[4 * t + 2], stg[4 * t + 3]);
+                    const int i = lane + 32 * t, g = HALF * cp + i, r = g / CH, c = g - CH * r;
+                    if (HALF % 32 == 0 || i < HALF)
+                        *reinterpret_cast<uint4 *>(raw + r * (PW * 4) + 16 * c) =
+                            make_uint4(stg[4 * t], stg[4 * t + 1], stg[4 * t + 2], stg[4 * t + 3]);
                 }
             };
             load(0);
-            store(0);
-            __syncwarp();
+            store();
+            mbar_arrive(p_full);
             if (nss > 1) load(1);
+            const uint8_t *row = raw + lane * PW * 4;
             for (int kk = 0; kk < P.nsteps; ++kk) {
                 const int js = kk >> 1, h = kk & 1, sa = kk % A_STAGES;
                 bool ok = !*abort_flag;
                 if (ok && kk >= A_STAGES) ok = mbar_wait(bar_a_empty + 8 * sa, ((kk / A_STAGES) - 1) & 1, P.status);
+                if (ok && h == 0) ok = mbar_wait(p_full, js & 1, P.status);
                 if (__any_sync(0xffffffffu, !ok)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint8_t *row = raw + (js & 1) * (32 * PW * 4) + lane * PW * 4;
+                uint32_t rr[32];
                 if constexpr (T == QMM_Q6_K) {
                     // the super-block starts at this (even) byte of its first chunk
                     const int dl = static_cast<int>((rows0 + static_cast<uint64_t>(lane) * P.RB +
@@ -540,12 +560,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // half h of the super-block: ql bytes 64h.., qh 128+32h.., scales
                     // 192+8h.., d at 208; weight 32qi + l: low bits from ql byte
                     // 32(qi&1) + l (nibble qi>>1), high bits (qh byte l >> 2qi) & 3,
-                    // scale 8h + 2qi + (l >= 16); w = d*sc * (q - 32)
+                    // scale 8h + 2qi + (l >= 16); w = d*sc * (q - 32).  This warp:
+                    // qi = 2cp, 2cp+1.
                     const float d = __half2float(*reinterpret_cast<const __half *>(row + dl + 208));
-                    const uint32_t sc0 = row_word(row, dl + 192 + 8 * h), sc1 = row_word(row, dl + 196 + 8 * h);
+                    const uint32_t scw = row_word(row, dl + 192 + 8 * h + 4 * cp);
                     // ql bytes 64h .. 64h+63 lie in chunks 4h .. 4h+4, qh bytes
                     // 128+32h .. 128+32h+31 in chunks 8+2h .. 10+2h
-                    uint32_t wl[20], wh[12], qh[8], ql[2][8];
+                    uint32_t wl[20], wh[12], qh[8], ql[16];
 #pragma unroll
                     for (int c = 0; c < 5; ++c) {
                         const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (4 * h + c));
@@ -562,111 +583,105 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         wh[4 * c + 2] = v.z;
                         wh[4 * c + 3] = v.w;
                     }
-                    uint32_t qlw[16];
-                    realign(wl, dl, qlw);
+                    realign(wl, dl, ql);
                     realign(wh, dl, qh);
-#pragma unroll
-                    for (int lw = 0; lw < 8; ++lw) {
-                        ql[0][lw] = qlw[lw];
-                        ql[1][lw] = qlw[8 + lw];
-                    }
                     const __half2 k1056 = __half2half2(__ushort_as_half(0x6420));  // 1056 = 1024 + 32
 #pragma unroll
-                    for (int cp = 0; cp < 2; ++cp) {  // weights 64cp .. 64cp+63 (qi = 2cp, 2cp+1)
-                        uint32_t r[32];
+                    for (int qq = 0; qq < 2; ++qq) {
+                        const int sb = 16 * qq;  // byte of scale 8h + 2qi in scw
+                        const __half2 s_lo = __float2half2_rn(d * static_cast<float>(static_cast<int8_t>(scw >> sb)));
+                        const __half2 s_hi =
+                            __float2half2_rn(d * static_cast<float>(static_cast<int8_t>(scw >> (sb + 8))));
+                        const int hsh = 4 * cp + 2 * qq;  // 2qi: the qh bit pair
 #pragma unroll
-                        for (int qq = 0; qq < 2; ++qq) {
-                            const int qi = 2 * cp + qq;
-                            const uint32_t scw = qi < 2 ? sc0 : sc1;
-                            const int sb = 16 * (qi & 1);  // byte of scale 8h + 2qi in its word
-                            const __half2 s_lo = __float2half2_rn(
-                                d * static_cast<float>(static_cast<int8_t>(scw >> sb)));
-                            const __half2 s_hi = __float2half2_rn(
-                                d * static_cast<float>(static_cast<int8_t>(scw >> (sb + 8))));
-#pragma unroll
-                            for (int lw = 0; lw < 8; ++lw) {
-                                const uint32_t lo = qi < 2 ? (ql[qi & 1][lw] & 0x0F0F0F0Fu)
-                                                           : ((ql[qi & 1][lw] >> 4) & 0x0F0F0F0Fu);
-                                const uint32_t q6 = lo | (((qh[lw] >> (2 * qi)) & 0x03030303u) << 4);
-                                const uint32_t p0 = __byte_perm(q6, 0x64646464u, 0x4140u);
-                                const uint32_t p1 = __byte_perm(q6, 0x64646464u, 0x4342u);
-                                const __half2 s = lw < 4 ? s_lo : s_hi;
-                                const __half2 w0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1056), s);
-                                const __half2 w1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1056), s);
-                                r[16 * qq + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
-                                r[16 * qq + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
-                            }
+                        for (int lw = 0; lw < 8; ++lw) {
+                            const uint32_t lo = cp == 0 ? (ql[8 * qq + lw] & 0x0F0F0F0Fu)
+                                                        : ((ql[8 * qq + lw] >> 4) & 0x0F0F0F0Fu);
+                            const uint32_t q6 = lo | (((qh[lw] >> hsh) & 0x03030303u) << 4);
+                            const uint32_t p0 = __byte_perm(q6, 0x64646464u, 0x4140u);
+                            const uint32_t p1 = __byte_perm(q6, 0x64646464u, 0x4342u);
+                            const __half2 s = lw < 4 ? s_lo : s_hi;
+                            const __half2 w0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1056), s);
+                            const __half2 w1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1056), s);
+                            rr[16 * qq + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
+                            rr[16 * qq + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
                         }
-                        tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
                     }
                 } else {
-                    // blocks 4h .. 4h+3 of the eight: d (fp16), then 32 int8; w = d * q.
-                    // They lie in bytes 136h .. 136h+135 of the row: chunks 8h .. 8h+8
-                    // (h a constant below, so that every word index is one).
-                    auto dequant_half = [&](auto hc) {
-                        constexpr int H = decltype(hc)::value;
-                        uint32_t w[36];
+                    // blocks 4h+2cp, 4h+2cp+1 of the eight: d (fp16), then 32 int8;
+                    // w = d * q.  They are the 68 bytes from byte 4E of chunk 4E,
+                    // E = 2h + cp (a constant below, so that every word index is one).
+                    auto dequant_pair = [&](auto ec) {
+                        constexpr int E = decltype(ec)::value;
+                        uint32_t w[20];
 #pragma unroll
-                        for (int c = 0; c < 9; ++c) {
-                            const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (8 * H + c));
+                        for (int c = 0; c < 5; ++c) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (4 * E + c));
                             w[4 * c] = v.x;
                             w[4 * c + 1] = v.y;
                             w[4 * c + 2] = v.z;
                             w[4 * c + 3] = v.w;
                         }
-                        // the 32-bit word at (even) byte offset o of those chunks
+                        // the 32-bit word at (even) byte offset o of the 68
                         auto word_at = [&](int o) {
-                            return (o & 2) ? __funnelshift_r(w[o >> 2], w[(o >> 2) + 1], 16) : w[o >> 2];
+                            return ((o + 4 * E) & 2) ? __funnelshift_r(w[(o >> 2) + E], w[(o >> 2) + E + 1], 16)
+                                                     : w[(o >> 2) + E];
                         };
                         const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));  // 1152 = 1024 + 128
 #pragma unroll
-                        for (int cp = 0; cp < 2; ++cp) {  // blocks 4H + 2cp, 4H + 2cp + 1
-                            uint32_t r[32];
+                        for (int bb = 0; bb < 2; ++bb) {
+                            const int ob = 34 * bb;
+                            const __half2 s =
+                                __half2half2(__ushort_as_half(static_cast<unsigned short>(word_at(ob))));
 #pragma unroll
-                            for (int bb = 0; bb < 2; ++bb) {
-                                const int ob = 34 * (2 * cp + bb) + 8 * H;  // within chunk 8H
-                                const __half2 s =
-                                    __half2half2(__ushort_as_half(static_cast<unsigned short>(word_at(ob))));
-#pragma unroll
-                                for (int lw = 0; lw < 8; ++lw) {
-                                    const uint32_t q = word_at(ob + 2 + 4 * lw);
-                                    // bytes (q0 ^ 0x80, 0x64, q1 ^ 0x80, 0x64): 1024 + 128 + q
-                                    const uint32_t p0 = __byte_perm(q, 0x64646464u, 0x4140u) ^ 0x00800080u;
-                                    const uint32_t p1 = __byte_perm(q, 0x64646464u, 0x4342u) ^ 0x00800080u;
-                                    const __half2 w0 =
-                                        __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1152), s);
-                                    const __half2 w1 =
-                                        __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1152), s);
-                                    r[16 * bb + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
-                                    r[16 * bb + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
-                                }
+                            for (int lw = 0; lw < 8; ++lw) {
+                                const uint32_t q = word_at(ob + 2 + 4 * lw);
+                                // bytes (q0 ^ 0x80, 0x64, q1 ^ 0x80, 0x64): 1024 + 128 + q
+                                const uint32_t p0 = __byte_perm(q, 0x64646464u, 0x4140u) ^ 0x00800080u;
+                                const uint32_t p1 = __byte_perm(q, 0x64646464u, 0x4342u) ^ 0x00800080u;
+                                const __half2 w0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1152), s);
+                                const __half2 w1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1152), s);
+                                rr[16 * bb + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
+                                rr[16 * bb + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
                             }
-                            tmem_st32(lane_base + C::A_COL0 + A_COLS * sa + 32 * cp, r);
                         }
                     };
-                    if (h == 0) dequant_half(std::integral_constant<int, 0>{});
-                    else dequant_half(std::integral_constant<int, 1>{});
+                    switch (2 * h + cp) {
+                        case 0: dequant_pair(std::integral_constant<int, 0>{}); break;
+                        case 1: dequant_pair(std::integral_constant<int, 1>{}); break;
+                        case 2: dequant_pair(std::integral_constant<int, 2>{}); break;
+                        default: dequant_pair(std::integral_constant<int, 3>{}); break;
+                    }
                 }
+                tmem_st32(lane_base + a_col + A_COLS * sa, rr);
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_a_full + 8 * sa);
-                // super-step js is done: the next one goes into the other
-                // buffer (read by every lane two steps ago), the one after
-                // that into the registers
-                if (h == 1 && js + 1 < nss) {
-                    store(js + 1);
-                    __syncwarp();
-                    if (js + 2 < nss) load(js + 2);
+                if (h == 1) {
+                    // super-step js is read; once the other warp has read it too,
+                    // the next one goes into the buffer and the one after that
+                    // into the registers
+                    mbar_arrive(p_empty);
+                    if (js + 1 < nss) {
+                        if (__any_sync(0xffffffffu, !mbar_wait(p_empty, js & 1, P.status))) {
+                            *abort_flag = 1;
+                            break;
+                        }
+                        store();
+                        mbar_arrive(p_full);
+                        if (js + 2 < nss) load(js + 2);
+                    }
                 }
             }
         }
-        // epilogue: TMEM lanes of this quarter, all BT token columns
+        // epilogue: TMEM lanes of this quarter, token columns of this warp's half
         const bool ok = mbar_wait(bar_acc, 0, P.status);
         if (__all_sync(0xffffffffu, ok) && !*abort_flag) {
             tc_fence_after();
             const int ncol = n0 + n;
 #pragma unroll 1
-            for (int cc = 0; cc < BT; cc += 16) {
+            for (int cc = cp * (BT / 2); cc < (cp + 1) * (BT / 2); cc += 16) {
                 float v[16];
                 tmem_ld16(lane_base + static_cast<uint32_t>(cc), v);
                 if (ncol < P.N) {
