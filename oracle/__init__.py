@@ -151,3 +151,32 @@ def qmm(qtype: int, W, N: int, K: int, x, nthreads: int = 0):
     if rc:
         raise ValueError(f"oracle_qmm failed: {rc}")
     return y, A
+
+
+def qmm_t(qtype: int, W, H: int, N: int, K: int, x):
+    """Product with the transposed matrices: y[h, m, k] = sum_n x[h, m, n] *
+    w[h, n, k] for H matrices of N rows of K weights, w the dequantised
+    weights (exact fp32 values of d*q), x used as given (not quantised).
+
+    Follows the value side of attention over a KV cache kept in q8_0 (infr
+    landing page, "why > Paged experts, spillable KV": the KV cache can be
+    stored as q8_0): each cached position is one row of head_dim weights and
+    the output is the probability-weighted sum of the rows.  The definition
+    written out: the dequantised rows times x in f64 (numpy's matmul as the
+    only library step).  Returns (y, A) in f64, A = sum_n |x w| (the scale of
+    the tolerance bound)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.ndim == 3 and x.shape[0] == H and x.shape[2] == N, x.shape
+    M = x.shape[1]
+    nblk = N * (K // BLOCK_WEIGHTS[qtype])
+    per = nblk * BLOCK_BYTES[qtype]
+    assert W.size >= H * per, (W.size, H * per)
+    y = np.zeros((H, M, K), np.float64)
+    A = np.zeros((H, M, K), np.float64)
+    for h in range(H):
+        w = dequant(qtype, W[h * per:(h + 1) * per], N * K).reshape(N, K).astype(np.float64)
+        xh = x[h].astype(np.float64)
+        y[h] = xh @ w
+        A[h] = np.abs(xh) @ np.abs(w)
+    return y, A

@@ -335,3 +335,87 @@ def test_planted_mistake_is_caught():
     blk[16:] = ((qs & 15) << 4) | (qs >> 4)   # the mistake, applied to the input
     _, _, _, _, q = O.unpack_q4_k(blk)
     assert any(q[p] != int(qv) for p, qv, _ in ws)
+
+
+# ------------------------------------------- qmm_t (the value side of attention)
+
+def _q8_0_rows_from_bytes(blob, N, K):
+    """Q8_0 rows decoded straight from the bytes, independently of the oracle's
+    C code: fp16 d by numpy's binary16, int8 q by two's complement."""
+    nb = K // 32
+    w = np.zeros((N, K))
+    for n in range(N):
+        for b in range(nb):
+            off = (n * nb + b) * 34
+            d = float(np.frombuffer(bytes(blob[off:off + 2]), np.float16)[0])
+            for i in range(32):
+                q = int(blob[off + 2 + i])
+                w[n, 32 * b + i] = d * (q - 256 if q >= 128 else q)
+    return w
+
+
+def test_qmm_t_matches_brute_force_sums():
+    """y[h,m,k] = sum_n x[h,m,n] w[h,n,k] by explicit Python loops over the
+    byte-decoded rows, on a case small enough to sum term by term."""
+    H, N, K, M = 2, 5, 64, 3
+    rng = np.random.default_rng(11)
+    W = synth.weights(synth.Q8_0, H * N, K, seed=12)
+    x = rng.standard_normal((H, M, N)).astype(np.float32)
+    y, A = O.qmm_t(O.Q8_0, W, H, N, K, x)
+    per = N * (K // 32) * 34
+    for h in range(H):
+        w = _q8_0_rows_from_bytes(W[h * per:(h + 1) * per], N, K)
+        for m in range(M):
+            for k in range(K):
+                terms = [float(x[h, m, n]) * w[n, k] for n in range(N)]
+                s, a = sum(terms), sum(abs(t) for t in terms)
+                assert abs(y[h, m, k] - s) <= 1e-12 * max(1.0, a)
+                assert abs(A[h, m, k] - a) <= 1e-12 * max(1.0, a)
+
+
+def test_qmm_t_golden_block_row():
+    """One cached position holding the hand-packed golden block: x = 2 gives
+    twice the block's hand-worked weights (exact)."""
+    rows, ws = _read_fixture("q8_0_block.txt")
+    d = bytes.fromhex(rows["d"][0])
+    q = bytes((int(v) & 255) for v in rows["q"])
+    blk = np.frombuffer(d + q, np.uint8).copy()
+    y, _ = O.qmm_t(O.Q8_0, blk, 1, 1, 32, np.full((1, 1, 1), 2.0, np.float32))
+    for p, wv, _ in ws:
+        assert y[0, 0, p] == 2.0 * float(wv)
+
+
+def test_qmm_t_unit_rows_pick_rows_and_heads_are_independent():
+    """x = e_n picks dequantised row n of its own matrix; permuting the
+    matrices together with their x permutes y (no mixing across h)."""
+    H, N, K = 3, 7, 96
+    W = synth.weights(synth.Q8_0, H * N, K, seed=21)
+    per = N * (K // 32) * 34
+    x = np.zeros((H, N, N), np.float32)
+    for h in range(H):
+        x[h] = np.eye(N, dtype=np.float32)
+    y, _ = O.qmm_t(O.Q8_0, W, H, N, K, x)
+    for h in range(H):
+        w = _q8_0_rows_from_bytes(W[h * per:(h + 1) * per], N, K)
+        assert np.array_equal(y[h], w)
+    perm = [2, 0, 1]
+    Wp = np.concatenate([W[p * per:(p + 1) * per] for p in perm])
+    rng = np.random.default_rng(5)
+    xr = rng.standard_normal((H, 2, N)).astype(np.float32)
+    y1, _ = O.qmm_t(O.Q8_0, W, H, N, K, xr)
+    y2, _ = O.qmm_t(O.Q8_0, Wp, H, N, K, xr[perm])
+    assert np.array_equal(y2, y1[perm])
+
+
+def test_qmm_t_planted_transpose_is_caught():
+    """A transposed operand (w^T in place of w, same shape when N == K) fails
+    the brute-force pin: the pin tells the two orientations apart."""
+    N = K = 32
+    W = synth.weights(synth.Q8_0, N, K, seed=31)
+    x = np.random.default_rng(3).standard_normal((1, 1, N)).astype(np.float32)
+    w = _q8_0_rows_from_bytes(W, N, K)
+    y, _ = O.qmm_t(O.Q8_0, W, 1, N, K, x)
+    right = x[0].astype(np.float64) @ w
+    wrong = x[0].astype(np.float64) @ w.T   # the mistake
+    assert np.allclose(y[0], right, rtol=1e-12, atol=1e-12)
+    assert not np.allclose(wrong, right, rtol=1e-6, atol=1e-6)
