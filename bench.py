@@ -13,6 +13,8 @@ from HBM.  The same run also times:
   * every matrix alone over rotating copies (>= 4x L2) -> per-matrix GB/s,
   * the prefill GEMM at M=512 -> TOPS: Q4_K (Mistral-7B MLP up and down),
     Q6_K (the Qwen3-14B-shaped layer's v and down), Q8_0 (Mistral up shape),
+  * the value side of attention over a q8_0 KV cache (qmm_t, Qwen3-14B
+    shaped: 8 heads x 32768 positions x 128) -> GB/s,
   * the dominant kernel (the Q6_K lm_head GEMV) for the roofline object,
   * the end-to-end step with host buffers (x copied in, y copied out),
   * the CPU oracle on a bounded sample (cpu_baseline).
@@ -535,6 +537,31 @@ def run_ours(args):
         gemm = {"kernels": gemm, "int8_peak_tops_torch_int_mm": round(int8_peak, 1) if int8_peak else None,
                 "f16_peak_tflops": peaks["bf16"]}
 
+        # ---- the value side of attention over a q8_0 KV cache (qmm_t):
+        # Qwen3-14B-shaped, 8 cache heads x 32768 positions x head_dim 128,
+        # 5 probability rows per head; rotating copies of the cache (> L2)
+        kv = synth.KV_CACHE
+        kvH, kvN, kvK, kvM = kv["H"], kv["N"], kv["K"], kv["M"]
+        Wkv = torch.from_numpy(synth.kv_cache(kvH, kvN, kvK, seed=9)).to(dev)
+        xkv = torch.from_numpy(synth.attention_probs(kvH, kvM, kvN, seed=9)).to(dev)
+        ykv = torch.empty((kvH, kvM, kvK), dtype=torch.float32, device=dev)
+        kv_bytes = Wkv.numel()
+        kv_copies = [Wkv] + [Wkv.clone() for _ in range(max(1, -(-4 * L2_BYTES // kv_bytes)) - 1)]
+        kv_inner = max(len(kv_copies), 8)
+
+        def kvcall():
+            for i in range(kv_inner):
+                q.qmm_t(synth.Q8_0, kv_copies[i % len(kv_copies)], kvH, kvN, kvK, xkv, y=ykv, stream=stream)
+
+        g = capture(kvcall)
+        t_ms = timed(g, 5, 2) / kv_inner
+        del g, kv_copies
+        torch.cuda.empty_cache()
+        kv_gbs = kv_bytes / (t_ms * 1e-3) / 1e9
+        kv_line = {"what": "qmm_t, " + kv["name"], "H": kvH, "N": kvN, "K": kvK, "M": kvM,
+                   "MB": round(kv_bytes / 1e6, 3), "us": round(t_ms * 1e3, 2), "GB/s": round(kv_gbs, 1),
+                   "frac_hbm": round(kv_gbs / peaks["hbm"], 4)}
+
         # ---- CPU oracle on a bounded sample
         cores = len(os.sched_getaffinity(0))
         rate, sample = oracle_rate(mats, args.cpu_seconds, cores)
@@ -560,6 +587,7 @@ def run_ours(args):
             "clocks": clocks, "per_matrix": detail, "groups": groups, "qwen3_14b_layer": layer,
             "qwen3_14b_layer_M": layer_m,
             "prefill_gemm": gemm,
+            "kv_value_cache": kv_line,
         }
         print(json.dumps(line))
     if dist:
@@ -583,6 +611,16 @@ def run_ncu_case(name, calls=3):
     import mat_mul_gb300 as q
     torch.cuda.set_device(0)
     q.load()
+    if name == "kv":  # the value side of attention over the q8_0 KV cache (qmm_t)
+        kv = synth.KV_CACHE
+        W = torch.from_numpy(synth.kv_cache(kv["H"], kv["N"], kv["K"], seed=9)).cuda()
+        x = torch.from_numpy(synth.attention_probs(kv["H"], kv["M"], kv["N"], seed=9)).cuda()
+        for _ in range(calls):
+            y = q.qmm_t(synth.Q8_0, W, kv["H"], kv["N"], kv["K"], x)
+        torch.cuda.synchronize()
+        assert q.qmm_device_status() == 0
+        print(name, "ok", float(y.abs().sum()))
+        return 0
     mats = {m["name"]: m for m in decode_workload()}
     for idx, (nm, qtype, K, N) in enumerate(synth.CONFIGS[4]["mats"]):
         mats[f"cfg4:{nm}"] = dict(cfg=4, idx=idx, name=f"cfg4:{nm}", qtype=qtype, K=K, N=N, M=512)
@@ -634,7 +672,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--quick", action="store_true", help="headline and e2e only")
     ap.add_argument("--ncu-case", default=None,
-                    help="run three eager calls of one matrix (e.g. cfg2:lm_head, cfg3:gate@4 for M = 4) and exit")
+                    help="run three eager calls of one matrix (e.g. cfg2:lm_head, cfg3:gate@4 for M = 4; kv for the "
+                         "q8_0 value cache) and exit")
     ap.add_argument("--ncu-step", type=int, default=0,
                     help="run this many eager decode steps (for an ncu launch list) and exit")
     args = ap.parse_args()

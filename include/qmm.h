@@ -165,6 +165,35 @@ QMM_API int qmm_quantize_act(const float *x, int64_t M, int64_t K, int8_t *q, fl
 QMM_API int qmm_noalloc(int type, const void *W_blocks, int64_t N, int64_t K, const float *x,
                         int64_t M, float *y, void *stream);
 
+/*
+ * qmm_t -- y[h][m][k] = sum_n x[h][m][n] * w[h][n][k]: H independent products
+ * with the transposed weight matrices, the value side of attention over a KV
+ * cache kept as q8_0 (infr landing page, "why > Paged experts, spillable KV":
+ * the KV cache can be stored as q8_0).  Matrix h holds N rows (cached
+ * positions) of K weights (head_dim); x[h] holds the M probability rows of
+ * the query heads that share it.  The score side, x . w^T over the key cache,
+ * is qmm itself (one call per cache head, N = positions, K = head_dim).
+ *   type     : QMM_Q8_0 (other types: QMM_EINVAL_TYPE).
+ *   W_blocks : device, H*N*(K/32) blocks, matrix-major then row-major, 16-B aligned.
+ *   H        : matrices, 0 <= H <= 65535.
+ *   N        : rows per matrix (>= 0; N = 0 writes y = 0).
+ *   K        : weights per row, a multiple of 32, at most 256.
+ *   x        : device, H*M*N floats ([H][M][N]), 4-byte aligned; not quantised.
+ *   M        : rows of x per matrix (>= 0).
+ *   y        : device, H*M*K floats ([H][M][K]), overwritten.
+ *   stream   : cudaStream_t to run on (NULL = legacy default stream).
+ * The cache rows are streamed once through shared memory and contracted on
+ * the tensor cores: each weight d*q enters as fp16 (one rounding of the exact
+ * value) and each x scaled by a power of two as fp16 (one rounding), products
+ * summed in fp32 in a fixed order, so the result is bitwise reproducible and
+ * |y - y_exact| <= 2e-3 * sum_n |x w| + 1e-5 with y_exact the f64 product of
+ * x and qmm_dequant's weights.  Uses the per-(device, stream) workspace of
+ * qmm (about H*16*K*4 bytes per SM-sized chunk) and H counters per (device,
+ * stream); one kernel launch per 16 rows of x.
+ */
+QMM_API int qmm_t(int type, const void *W_blocks, int64_t H, int64_t N, int64_t K, const float *x, int64_t M,
+                  float *y, void *stream);
+
 /* Name of a status code. */
 QMM_API const char *qmm_strerror(int status);
 

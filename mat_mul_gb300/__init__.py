@@ -56,6 +56,7 @@ def load():
     L.qmm_noalloc.argtypes = [I, P, I64, I64, P, I64, P, P]
     L.qmm_quantize_act.argtypes = [P, I64, I64, P, P, P, P]
     L.qmm_group.argtypes = [I, P, P, P, I64, P, I64, P, P]
+    L.qmm_t.argtypes = [I, P, I64, I64, I64, P, I64, P, P]
     L.qmm_strerror.argtypes = [I]
     L.qmm_strerror.restype = ctypes.c_char_p
     L.qmm_last_error.restype = ctypes.c_char_p
@@ -120,6 +121,24 @@ def qmm(qtype: int, W, N: int, K: int, x, y=None, stream=None):
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
     _check(load().qmm(int(qtype), _ptr(W), int(N), int(K), _ptr(x), int(M), _ptr(y),
                       _stream_handle(stream)))
+    return y
+
+
+def qmm_t(qtype: int, W, H: int, N: int, K: int, x, y=None, stream=None):
+    """y[h, m, k] = sum_n x[h, m, n] * w[h, n, k] for H matrices of N rows of
+    K weights (uint8 device tensor W of packed Q8_0 blocks) and a device f32
+    tensor x of shape [H, M, N]; returns y of shape [H, M, K]."""
+    import torch
+    _require_cuda(W, x, y)
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 tensor")
+    if x.dim() != 3 or x.shape[0] != H or x.shape[2] != N:
+        raise ValueError(f"x has shape {tuple(x.shape)}, expected [H={H}, M, N={N}]")
+    M = x.shape[1]
+    if y is None:
+        y = torch.empty((H, M, K), dtype=torch.float32, device=x.device)
+    _check(load().qmm_t(int(qtype), _ptr(W), int(H), int(N), int(K), _ptr(x), int(M), _ptr(y),
+                        _stream_handle(stream)))
     return y
 
 

@@ -66,6 +66,9 @@ struct Workspace {
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_dev;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+// qmm_t's per-matrix completion counters, per (device, stream): zero between
+// calls (each call's last CTA of a matrix resets its counter)
+std::map<std::pair<int, cudaStream_t>, Workspace> g_counters;
 
 int device_info(int dev, DeviceInfo &out) {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -113,6 +116,37 @@ int workspace(int dev, cudaStream_t st, size_t bytes, void **ptr) {
     }
     w.bytes = want;
     *ptr = w.ptr;
+    return QMM_OK;
+}
+
+// At least n zeroed counters for (dev, stream).  Growing synchronises the
+// stream before the old array is released; the new one is zeroed on it.
+int counters(int dev, cudaStream_t st, int64_t n, unsigned **ptr) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = g_counters[{dev, st}];
+    const size_t bytes = static_cast<size_t>(n) * sizeof(unsigned);
+    if (w.bytes >= bytes) {
+        *ptr = static_cast<unsigned *>(w.ptr);
+        return QMM_OK;
+    }
+    size_t want = 4096;
+    while (want < bytes) want *= 2;
+    if (w.ptr) {
+        cudaError_t e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "counters grow (sync)");
+        cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&w.ptr, want);
+    if (e != cudaSuccess) {
+        w.ptr = nullptr;
+        return fail(QMM_ENOMEM, "counters of %zu bytes: %s", want, cudaGetErrorString(e));
+    }
+    e = cudaMemsetAsync(w.ptr, 0, want, st);
+    if (e != cudaSuccess) return cuda_fail(e, "counters init");
+    w.bytes = want;
+    *ptr = static_cast<unsigned *>(w.ptr);
     return QMM_OK;
 }
 
@@ -348,6 +382,46 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     return QMM_OK;
 }
 
+int qmm_t(int type, const void *W_blocks, int64_t H, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+          void *stream) {
+    g_err[0] = 0;
+    if (int rc = check_type(type)) return rc;
+    if (type != QMM_Q8_0) return fail(QMM_EINVAL_TYPE, "qmm_t takes Q8_0 blocks (the KV cache format), not type %d", type);
+    if (H < 0 || N < 0 || K < 0 || M < 0 || K % 32 || K > 256)
+        return fail(QMM_EINVAL_SHAPE, "H=%lld N=%lld K=%lld M=%lld: sizes must be >= 0 and K a multiple of 32 up to 256",
+                    static_cast<long long>(H), static_cast<long long>(N), static_cast<long long>(K),
+                    static_cast<long long>(M));
+    if (H > 65535 || N > (int64_t(1) << 31) || M > (int64_t(1) << 24))
+        return fail(QMM_EINVAL_SHAPE, "H=%lld N=%lld M=%lld: H <= 65535, N <= 2^31, M <= 2^24",
+                    static_cast<long long>(H), static_cast<long long>(N), static_cast<long long>(M));
+    if (H == 0 || M == 0 || K == 0) return QMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!y) return fail(QMM_EINVAL_PTR, "null y");
+    if (!aligned(y, 4)) return fail(QMM_EINVAL_PTR, "y must be 4-byte aligned");
+    if (N == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(H * M * K) * sizeof(float), st);
+        if (e != cudaSuccess) return cuda_fail(e, "zero fill");
+        return QMM_OK;
+    }
+    if (!W_blocks || !x) return fail(QMM_EINVAL_PTR, "null pointer");
+    if (!aligned(W_blocks, 16)) return fail(QMM_EINVAL_PTR, "W_blocks must be 16-byte aligned");
+    if (!aligned(x, 4)) return fail(QMM_EINVAL_PTR, "x must be 4-byte aligned");
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo di;
+    if (int rc = device_info(dev, di)) return rc;
+    void *ws = nullptr;
+    if (int rc = workspace(dev, st, qk::qmm_t_part_bytes(H, N, K, di.num_sms), &ws)) return rc;
+    unsigned *cnt = nullptr;
+    if (int rc = counters(dev, st, H, &cnt)) return rc;
+    e = qk::launch_qmm_t(W_blocks, H, N, K, x, M, y, static_cast<float *>(ws), cnt, st, di.num_sms, di.status);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm_t launch");
+    g_launches.fetch_add((M + 15) / 16);
+    return QMM_OK;
+}
+
 int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns, int64_t K, const float *x,
               int64_t M, float *const *ys, void *stream) {
     g_err[0] = 0;
@@ -446,12 +520,14 @@ int qmm_release(void) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
     std::lock_guard<std::mutex> lk(g_mu);
-    for (auto it = g_ws.begin(); it != g_ws.end();) {
-        if (it->first.first == dev) {
-            cudaFree(it->second.ptr);
-            it = g_ws.erase(it);
-        } else {
-            ++it;
+    for (auto *m : {&g_ws, &g_counters}) {
+        for (auto it = m->begin(); it != m->end();) {
+            if (it->first.first == dev) {
+                cudaFree(it->second.ptr);
+                it = m->erase(it);
+            } else {
+                ++it;
+            }
         }
     }
     return QMM_OK;

@@ -100,6 +100,15 @@ cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const
                             const float *xd, const int32_t *xs, int xd_ld, int64_t M, float *y,
                             cudaStream_t st);
 
+// Product with the transposed Q8_0 matrices (qmm_t.cu): y[h][m][k] =
+// sum_n x[h][m][n] * w[h][n][k], K a multiple of 32 up to 256.  part: the
+// workspace of qmm_t_part_bytes() bytes; count: H unsigned counters that are
+// zero before the call and are left zero by it.  One launch per 16 rows of x.
+int64_t qmm_t_chunk_rows(int64_t H, int64_t N, int num_sms);
+size_t qmm_t_part_bytes(int64_t H, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_qmm_t(const void *W, int64_t H, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+                         float *part, unsigned *count, cudaStream_t st, int num_sms, int *status);
+
 // Set the calling thread's qmm_last_error() text; returns code.
 int record_error(int code, const char *msg);
 

@@ -1,0 +1,398 @@
+// qmm_t.cu -- the product with the transposed block matrices,
+//   y[h][m][k] = sum_n x[h][m][n] * w[h][n][k],   h < H, m < M, k < K,
+// for H matrices of N rows of K Q8_0 weights: the value side of attention
+// over a KV cache stored as q8_0 (infr landing page, "why > Paged experts,
+// spillable KV": the KV cache can be kept in q8_0), one row of head_dim
+// weights per cached position, x the attention probabilities of the M query
+// heads that share the cache head.
+//
+// Memory-bound: every weight byte is read once.  Each CTA owns a contiguous
+// range of one matrix's rows (a chunk), split evenly between its eight warps;
+// each warp streams its rows through a private ring of shared-memory stages
+// with bulk async copies (its lane 0 refills a stage as soon as the warp has
+// read it), so 8 copy streams per SM keep the bytes in flight.  A warp
+// contracts 16 rows at a time on the tensor cores (mma.sync m16n8k16, fp16
+// operands, fp32 accumulation):
+//   A (16 x 16) = x[m][n] * 2^e for the 16 positions n (rows m >= M zero),
+//       2^e a power of two per warp that puts the largest |x| the warp has
+//       met into [2^12, 2^13) (fp16's normal range): when a group of 16
+//       positions raises that maximum, the accumulators are rescaled by the
+//       exact power of two, and the scale is undone at the end;
+//   B (16 x 8)  = d*q of the 16 positions for eight of the K columns: the
+//       int8 q of two rows are paired by one byte permute, made exact fp16
+//       integers by the 0x6400 exponent trick, and scaled by their rows' d
+//       (one fp16 rounding of the exact d*q).
+// Columns: the MMA j (0..3) of block b covers columns 32b + 4g + j (g the
+// MMA's column index), so each lane reads one aligned 4-byte group of quants
+// per row and block, and ends up holding 8 consecutive columns.
+// Reduction, in a fixed order so that the result is bitwise reproducible:
+// the eight warps' sums are added in warp order in shared memory and scaled
+// back, each CTA writes its chunk sum to the workspace, and the CTA that
+// finishes a matrix last (a counter per matrix, reset by that CTA) adds the
+// chunk sums in chunk order and writes y.
+//
+// Bounded waits only: a wait that expires raises the status word; the warp
+// still drains its copies and the CTA completes the reduction protocol.
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace qk {
+
+namespace {
+
+constexpr int VT_WARPS = 8;
+constexpr int VT_THREADS = 32 * VT_WARPS;
+constexpr int VT_ROWS = 16 * VT_WARPS;                 // chunks are multiples of this
+constexpr int VT_MG = 16;                              // rows of x per launch
+constexpr int VT_RING = 192 * 1024;                    // shared-memory ring bytes of all warps (about)
+
+template <int NB>
+struct VtCfg {
+    static constexpr int K = 32 * NB, RB = 34 * NB;
+    static constexpr int SR = NB <= 4 ? 32 : 16;             // rows per stage
+    // a stage, + room for the 16-byte rounding of both ends
+    static constexpr int SLOT = (SR * RB + 32 + 15) & ~15;
+    static constexpr int D_FIT = VT_RING / (VT_WARPS * SLOT);
+    static constexpr int D = D_FIT > 8 ? 8 : D_FIT;           // ring depth per warp
+    static constexpr int RK = K + 1;                          // row pitch of the warps' sums
+    static constexpr int SMEM = VT_WARPS * D * SLOT + 8 * VT_WARPS * D + 16;
+    // after the stream the rings hold the eight warps' sums, [warp][16][RK] floats
+    static_assert(VT_WARPS * 16 * RK * 4 <= VT_WARPS * D * SLOT, "warp sums fit in the rings");
+};
+
+// 2^(e - 127) as a float for a biased exponent 1 <= e <= 254, else 0
+__device__ __forceinline__ float pow2_biased(int e) {
+    return e >= 1 && e <= 254 ? __uint_as_float(static_cast<uint32_t>(e) << 23) : 0.0f;
+}
+
+struct VtParams {
+    const uint8_t *W;   // H*N rows of RB bytes
+    uint64_t w_end;     // first byte past the matrices
+    int64_t N;          // rows per matrix
+    int64_t R;          // rows per chunk (a multiple of VT_ROWS)
+    int nchunk;         // chunks per matrix
+    const float *x;     // [H][M][N]
+    int64_t M;
+    int m0, mg;         // this launch's rows of x: m0 .. m0 + mg - 1 (mg <= 16)
+    float *y;           // [H][M][K]
+    float *part;        // [H][nchunk][16][K] chunk sums
+    unsigned *count;    // [H] finished chunks, zero between calls
+    int *status;
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// The B pair (d_a*q_a[j], d_b*q_b[j]) from byte j of the quant words of two
+// rows: bytes (q_a ^ 0x80, 0x64, q_b ^ 0x80, 0x64) are the fp16 values
+// 1152 + q, so subtracting 1152 gives q exactly; then one multiply by (d_a, d_b).
+template <int J>
+__device__ __forceinline__ uint32_t b_pair(uint32_t wa, uint32_t wb, __half2 dd) {
+    const uint32_t u = __byte_perm(wa, wb, J | (J << 4) | ((4 + J) << 8) | ((4 + J) << 12));
+    const uint32_t v = (u & 0x00FF00FFu) ^ 0x64806480u;
+    const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));
+    const __half2 r = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&v), k1152), dd);
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// The fp16 d of block b of a row at shared address `row` (2-byte aligned), as
+// raw bits; zero for a row past the matrix.
+__device__ __forceinline__ uint32_t row_d(uint32_t row, int b, bool valid) {
+    return valid ? lds16(row + 34u * b) : 0u;
+}
+
+// Quant bytes 4g .. 4g+3 of block b of a row (2-byte aligned).
+__device__ __forceinline__ uint32_t row_q4(uint32_t row, int b, int g, bool valid) {
+    if (!valid) return 0u;
+    const uint32_t a = row + 34u * b + 2u + 4u * g;
+    const uint32_t base = a & ~3u;
+    return __funnelshift_r(lds32(base), lds32(base + 4u), (a & 3u) * 8u);
+}
+
+template <int NB>
+__global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
+    using C = VtCfg<NB>;
+    constexpr int K = C::K, RB = C::RB, SR = C::SR, SLOT = C::SLOT, D = C::D, RK = C::RK;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + VT_WARPS * D * SLOT);  // [warp][D]
+    int *last = reinterpret_cast<int *>(bars + VT_WARPS * D);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y, c = blockIdx.x;
+    // this warp's rows: the w-th eighth of the chunk
+    const int64_t n_lo = static_cast<int64_t>(c) * P.R, n_hi = min(P.N, n_lo + P.R);
+    const int64_t rw = P.R / VT_WARPS;
+    const int64_t w_lo = min(n_hi, n_lo + warp * rw), w_hi = min(n_hi, w_lo + rw);
+    const int nst = static_cast<int>((w_hi - w_lo + SR - 1) / SR);
+    const uint64_t mat0 = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(h) * P.N * RB;
+    uint8_t *ring = smem + warp * D * SLOT;
+    const uint32_t bar0 = smem_u32(bars + warp * D);
+
+    if (lane == 0) {
+        for (int s = 0; s < D; ++s) mbar_init(bar0 + 8u * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    // issue stage t of this warp into slot t % D (lane 0): its rows rounded out
+    // to 16 bytes (the bulk-copy rule); the matrices' last bytes, past the
+    // final 16-byte boundary, by plain loads
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int t) {
+        const int s = t % D;
+        const int64_t r0 = w_lo + static_cast<int64_t>(t) * SR, r1 = min(w_hi, r0 + SR);
+        const uint64_t a = mat0 + static_cast<uint64_t>(r0) * RB, b = mat0 + static_cast<uint64_t>(r1) * RB;
+        const uint64_t a16 = a & ~uint64_t(15);
+        uint64_t b16 = (b + 15) & ~uint64_t(15);
+        uint8_t *dst = ring + s * SLOT;
+        if (b16 > P.w_end) {
+            b16 = b & ~uint64_t(15);
+            for (uint64_t i = b16; i < b; ++i) dst[i - a16] = *reinterpret_cast<const uint8_t *>(i);
+        }
+        const uint32_t bytes = static_cast<uint32_t>(b16 - a16);
+        mbar_arrive_expect_tx(bar0 + 8u * s, bytes);
+        if (bytes) bulk_g2s(smem_u32(dst), reinterpret_cast<const void *>(a16), bytes, bar0 + 8u * s, pol);
+    };
+    int issued = 0;
+    if (lane == 0)
+        for (; issued < min(D, nst); ++issued) issue(issued);
+
+    const int g = lane >> 2, tq = lane & 3;
+    const float *xh = P.x + (static_cast<int64_t>(h) * P.M + P.m0) * P.N;  // row m of this launch: xh + m*N
+    const int ra = 2 * tq, rb = ra + 1, rc = ra + 8, rd = ra + 9;  // this lane's four rows of a group
+    // x of this lane's four positions of the group at n0, rows g and g + 8
+    // (zero past the warp's rows or past this launch's rows of x)
+    auto load_x = [&](int64_t n0, float (&v)[2][4]) {
+#pragma unroll
+        for (int hm = 0; hm < 2; ++hm) {
+            const int m = g + 8 * hm;
+            const float *xr = xh + m * P.N + n0;
+            const bool vm = m < P.mg;
+            v[hm][0] = vm && n0 + ra < w_hi ? __ldg(xr + ra) : 0.0f;
+            v[hm][1] = vm && n0 + rb < w_hi ? __ldg(xr + rb) : 0.0f;
+            v[hm][2] = vm && n0 + rc < w_hi ? __ldg(xr + rc) : 0.0f;
+            v[hm][3] = vm && n0 + rd < w_hi ? __ldg(xr + rd) : 0.0f;
+        }
+    };
+
+    float acc[NB][4][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[b][j][e] = 0.0f;
+    int ew = 12;           // biased exponent of the warp's running max |x| (at least 12)
+    float up = 0x1p127f;   // 2^(139 - ew): that max times up lies in [2^12, 2^13)
+
+    float xn[2][4];  // x of the next group, in flight while the current one is contracted
+    load_x(w_lo, xn);
+    bool ok = true;
+    for (int t = 0; t < nst && ok; ++t) {
+        const int s = t % D;
+        // an expired wait leaves this chunk's sum incomplete (the status word
+        // reports it); the CTA still takes part in the reduction
+        ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8u * s, (t / D) & 1, P.status));
+        if (!ok) break;
+        const int64_t r0 = w_lo + static_cast<int64_t>(t) * SR;
+        const uint64_t a = mat0 + static_cast<uint64_t>(r0) * RB;
+        const uint32_t stage = smem_u32(ring + s * SLOT) + static_cast<uint32_t>(a & 15);
+#pragma unroll 1
+        for (int gi = 0; gi < SR / 16; ++gi) {
+            const int64_t n0 = r0 + 16 * gi;  // these 16 positions
+            if (n0 >= w_hi) break;
+            float xc[2][4];
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) xc[hm][e] = xn[hm][e];
+            if (n0 + 16 < w_hi) load_x(n0 + 16, xn);
+            // the running scale: the warp's max |x| so far
+            float mloc = 0.0f;
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mloc = fmaxf(mloc, fabsf(xc[hm][e]));
+            const uint32_t mbits = __reduce_max_sync(0xffffffffu, __float_as_uint(mloc));
+            const int eg = min(254, static_cast<int>(mbits >> 23));
+            if (eg > ew) {
+                const float f = pow2_biased(127 + ew - eg);  // exact: a power of two, or 0 far below
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[b][j][e] *= f;
+                ew = eg;
+                up = pow2_biased(266 - ew);
+            }
+            const uint32_t rows = stage + static_cast<uint32_t>(16 * gi * RB);
+            const int nv = static_cast<int>(min(static_cast<int64_t>(16), w_hi - n0));
+            const bool va = ra < nv, vb = rb < nv, vc = rc < nv, vd = rd < nv;
+            // A: x * up of positions ra, rb (a0, a1) and rc, rd (a2, a3); rows g, g + 8
+            const uint32_t a0 = pack_half2(xc[0][0] * up, xc[0][1] * up), a1 = pack_half2(xc[1][0] * up, xc[1][1] * up);
+            const uint32_t a2 = pack_half2(xc[0][2] * up, xc[0][3] * up), a3 = pack_half2(xc[1][2] * up, xc[1][3] * up);
+            const uint32_t row_a = rows + ra * RB, row_b = rows + rb * RB, row_c = rows + rc * RB,
+                           row_dd = rows + rd * RB;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const uint32_t wa = row_q4(row_a, b, g, va), wb = row_q4(row_b, b, g, vb);
+                const uint32_t wc = row_q4(row_c, b, g, vc), wd = row_q4(row_dd, b, g, vd);
+                const uint32_t dab = row_d(row_a, b, va) | (row_d(row_b, b, vb) << 16);
+                const uint32_t dcd = row_d(row_c, b, vc) | (row_d(row_dd, b, vd) << 16);
+                const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
+                const __half2 d89 = *reinterpret_cast<const __half2 *>(&dcd);
+                mma16816(acc[b][0], a0, a1, a2, a3, b_pair<0>(wa, wb, d01), b_pair<0>(wc, wd, d89));
+                mma16816(acc[b][1], a0, a1, a2, a3, b_pair<1>(wa, wb, d01), b_pair<1>(wc, wd, d89));
+                mma16816(acc[b][2], a0, a1, a2, a3, b_pair<2>(wa, wb, d01), b_pair<2>(wc, wd, d89));
+                mma16816(acc[b][3], a0, a1, a2, a3, b_pair<3>(wa, wb, d01), b_pair<3>(wc, wd, d89));
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && issued < nst) {
+            // the slot just read is refilled: order the reads before the async write
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(issued);
+            ++issued;
+        }
+    }
+    // no copy into this warp's ring may be in flight when its slots are reused
+    if (lane == 0)
+        for (int t = issued > D ? issued - D : 0; t < issued; ++t) mbar_wait(bar0 + 8u * (t % D), (t / D) & 1, P.status);
+    // back to the true scale: 1 / up = 2^(ew - 139) (exact)
+    const float down = ew > 12 ? pow2_biased(ew - 12) : 0x1p-127f;
+    // every warp's ring is drained: the rings now hold the warps' sums,
+    // [warp][m][RK] (pitch K + 1: the lanes' columns fall in distinct banks);
+    // lane (g, tq) holds, for block b, columns 32b + 8tq + j (acc[b][j][0],
+    // row g; [2], row g + 8) and 32b + 8tq + 4 + j ([1] and [3])
+    __syncthreads();
+    float *sums = reinterpret_cast<float *>(smem);
+    {
+        float *r0p = sums + (warp * 16 + g) * RK, *r1p = r0p + 8 * RK;
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k0 = 32 * b + 8 * tq + j, k1 = k0 + 4;
+                r0p[k0] = acc[b][j][0] * down;
+                r0p[k1] = acc[b][j][1] * down;
+                r1p[k0] = acc[b][j][2] * down;
+                r1p[k1] = acc[b][j][3] * down;
+            }
+    }
+    __syncthreads();
+    // the chunk sum into the workspace
+    float *part_hc = P.part + (static_cast<int64_t>(h) * P.nchunk + c) * 16 * K;
+    for (int i = threadIdx.x; i < P.mg * K; i += VT_THREADS) {
+        const int off = (i / K) * RK + i % K;
+        float v[VT_WARPS];
+#pragma unroll
+        for (int w = 0; w < VT_WARPS; ++w) v[w] = sums[w * 16 * RK + off];
+        float sum = v[0];
+#pragma unroll
+        for (int w = 1; w < VT_WARPS; ++w) sum += v[w];  // in warp order
+        part_hc[i] = sum;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned done = atomicAdd(P.count + h, 1u);
+        *last = done == static_cast<unsigned>(P.nchunk - 1);
+    }
+    __syncthreads();
+    if (!*last) return;
+    // the last CTA of matrix h: chunk sums in chunk order
+    __threadfence();
+    const float *part_h = P.part + static_cast<int64_t>(h) * P.nchunk * 16 * K;
+    float *yh = P.y + (static_cast<int64_t>(h) * P.M + P.m0) * K;
+    for (int i = threadIdx.x; i < P.mg * K; i += VT_THREADS) {
+        // eight chunk sums in flight at a time, added in chunk order
+        float sum = 0.0f;
+        for (int c0 = 0; c0 < P.nchunk; c0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = c0 + u < P.nchunk ? __ldcg(part_h + static_cast<int64_t>(c0 + u) * 16 * K + i) : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + u < P.nchunk) sum += v[u];
+        }
+        yh[i] = sum;
+    }
+    if (threadIdx.x == 0) P.count[h] = 0u;  // ready for the next call on this stream
+}
+
+template <int NB>
+cudaError_t launch_nb(const VtParams &P, int64_t H, cudaStream_t st) {
+    const size_t smem = VtCfg<NB>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(qmm_t_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    qmm_t_kernel<NB><<<dim3(P.nchunk, static_cast<unsigned>(H)), VT_THREADS, smem, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t qmm_t_chunk_rows(int64_t H, int64_t N, int num_sms) {
+    // one CTA per SM over all matrices (the kernel's registers allow one
+    // resident CTA), whole stages per chunk
+    const int64_t want = static_cast<int64_t>(num_sms);
+    int64_t per = (want + H - 1) / H;  // chunks per matrix
+    if (per < 1) per = 1;
+    int64_t R = (N + per - 1) / per;
+    R = (R + VT_ROWS - 1) / VT_ROWS * VT_ROWS;
+    return R < VT_ROWS ? VT_ROWS : R;
+}
+
+size_t qmm_t_part_bytes(int64_t H, int64_t N, int64_t K, int num_sms) {
+    const int64_t R = qmm_t_chunk_rows(H, N, num_sms);
+    const int64_t nchunk = (N + R - 1) / R;
+    return static_cast<size_t>(H * nchunk * 16 * K) * sizeof(float);
+}
+
+cudaError_t launch_qmm_t(const void *W, int64_t H, int64_t N, int64_t K, const float *x, int64_t M, float *y,
+                         float *part, unsigned *count, cudaStream_t st, int num_sms, int *status) {
+    VtParams P;
+    P.W = static_cast<const uint8_t *>(W);
+    P.N = N;
+    P.w_end = reinterpret_cast<uint64_t>(W) + static_cast<uint64_t>(H * N) * (K / 32) * 34;
+    P.R = qmm_t_chunk_rows(H, N, num_sms);
+    P.nchunk = static_cast<int>((N + P.R - 1) / P.R);
+    P.x = x;
+    P.M = M;
+    P.y = y;
+    P.part = part;
+    P.count = count;
+    P.status = status;
+    const int nb = static_cast<int>(K / 32);
+    for (int64_t m0 = 0; m0 < M; m0 += VT_MG) {
+        P.m0 = static_cast<int>(m0);
+        P.mg = static_cast<int>(min(static_cast<int64_t>(VT_MG), M - m0));
+        cudaError_t e;
+        switch (nb) {
+        case 1: e = launch_nb<1>(P, H, st); break;
+        case 2: e = launch_nb<2>(P, H, st); break;
+        case 3: e = launch_nb<3>(P, H, st); break;
+        case 4: e = launch_nb<4>(P, H, st); break;
+        case 5: e = launch_nb<5>(P, H, st); break;
+        case 6: e = launch_nb<6>(P, H, st); break;
+        case 7: e = launch_nb<7>(P, H, st); break;
+        default: e = launch_nb<8>(P, H, st); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace qk

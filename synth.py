@@ -136,3 +136,28 @@ def config_activations(cfg: int, M: int, K: int) -> np.ndarray:
     if cfg == 0:
         return activations(M, K, seed=0)
     return activations(M, K, seed=1000 * cfg + 500 + M + K, outlier_frac=c["outliers"])
+
+
+# --- the value side of attention over a q8_0 KV cache -------------------------
+# Qwen3-14B-shaped attention: 8 KV heads of head_dim 128 shared by 40 query
+# heads (5 per KV head), 32768 cached positions; the cache rows are Q8_0
+# blocks with the Q8_0 value distribution above.
+
+KV_CACHE = dict(name="Qwen3-14B-shaped q8_0 value cache", H=8, N=32768, K=128, M=5)
+
+
+def kv_cache(H: int, N: int, K: int, seed: int) -> np.ndarray:
+    """H matrices of N cached rows of K Q8_0 weights, matrix after matrix."""
+    return weights(Q8_0, H * N, K, seed)
+
+
+def attention_probs(H: int, M: int, N: int, seed: int, temperature: float = 3.0) -> np.ndarray:
+    """Probability rows x[h, m, :] (non-negative, each summing to 1): the
+    normalised exponentials of N(0, temperature^2) logits, so that a few
+    positions carry most of the weight, as after a softmax over scores."""
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal((H, M, N)) * temperature
+    z -= z.max(axis=2, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=2, keepdims=True)
+    return p.astype(np.float32)

@@ -132,3 +132,33 @@ def test_decode_path_setter_validates_and_returns_the_previous_path():
     assert L.qmm_set_decode_path(q.DECODE_AUTO) == q.DECODE_TENSOR
     with pytest.raises(q.QmmError):
         q.set_decode_path(-1)
+
+
+def test_qmm_t_validation_rejects_before_launch():
+    L = q.load()
+    null = ctypes.c_void_p(0)
+    before = L.qmm_launch_count()
+    # the KV cache format only
+    assert L.qmm_t(q.Q4_K, null, 1, 4, 128, null, 1, null, null) == q.QMM_EINVAL_TYPE
+    assert b"Q8_0" in L.qmm_last_error()
+    assert L.qmm_t(9, null, 1, 4, 128, null, 1, null, null) == q.QMM_EINVAL_TYPE
+    # K a multiple of 32, at most 256; sizes >= 0; H <= 65535
+    assert L.qmm_t(q.Q8_0, null, 1, 4, 48, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_t(q.Q8_0, null, 1, 4, 288, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_t(q.Q8_0, null, -1, 4, 128, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_t(q.Q8_0, null, 1, -4, 128, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_t(q.Q8_0, null, 1, 4, 128, null, -1, null, null) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_t(q.Q8_0, null, 70000, 4, 128, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+    # empty problems
+    assert L.qmm_t(q.Q8_0, null, 0, 4, 128, null, 1, null, null) == q.QMM_OK
+    assert L.qmm_t(q.Q8_0, null, 2, 4, 128, null, 0, null, null) == q.QMM_OK
+    assert L.qmm_t(q.Q8_0, null, 2, 4, 0, null, 3, null, null) == q.QMM_OK
+    # null and misaligned pointers
+    assert L.qmm_t(q.Q8_0, null, 1, 4, 128, null, 1, null, null) == q.QMM_EINVAL_PTR
+    buf = ctypes.create_string_buffer(4096)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    assert L.qmm_t(q.Q8_0, ctypes.c_void_p(base + 2), 1, 4, 128, ctypes.c_void_p(base), 1,
+                   ctypes.c_void_p(base), null) == q.QMM_EINVAL_PTR
+    assert L.qmm_t(q.Q8_0, ctypes.c_void_p(base), 1, 4, 128, ctypes.c_void_p(base + 2), 1,
+                   ctypes.c_void_p(base), null) == q.QMM_EINVAL_PTR
+    assert L.qmm_launch_count() == before

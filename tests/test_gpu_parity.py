@@ -427,3 +427,88 @@ def test_qmm_q6_k_unit_scale_is_exact(cuda_lib, N, K, M):
     y = _run_qmm(cuda_lib, synth.Q6_K, W, N, K, xi.astype(np.float32))
     assert np.array_equal(y.astype(np.float64),
                           xi @ (q.reshape(N, K).astype(np.float64) - 32).T)
+
+
+# ------------------------------------------- qmm_t: the value side of attention
+
+def _run_qmm_t(q, W, H, N, K, x, stream=None):
+    y = q.qmm_t(synth.Q8_0, _dev(W), H, N, K, _dev(x), stream=stream)
+    assert q.qmm_device_status() == 0
+    return y.cpu().numpy()
+
+
+QMM_T_CASES = [(1, 1, 32, 1), (1, 16, 128, 5), (2, 300, 128, 5), (3, 1000, 64, 8), (1, 777, 256, 16),
+               (2, 129, 96, 17), (4, 2049, 160, 3), (1, 5000, 224, 1), (5, 64, 32, 2), (6, 12345, 128, 4)]
+
+
+@pytest.mark.parametrize("H,N,K,M", QMM_T_CASES)
+def test_qmm_t_matches_oracle(cuda_lib, H, N, K, M):
+    """Probability rows and signed rows, against the f64 oracle, element-wise
+    within the stated bound (M > 16 takes two launches; ragged stages)."""
+    W = synth.kv_cache(H, N, K, seed=H * 1000 + N)
+    for x in (synth.attention_probs(H, M, N, seed=N + M),
+              np.random.default_rng(N).standard_normal((H, M, N)).astype(np.float32)):
+        got = _run_qmm_t(cuda_lib, W, H, N, K, x)
+        want, A = O.qmm_t(O.Q8_0, W, H, N, K, x)
+        _assert_within_bound(got, want, A, f"qmm_t H={H} N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e-6, 1.0, 1e4, 1e30])
+def test_qmm_t_any_magnitude_of_x(cuda_lib, scale):
+    """The per-chunk power-of-two scaling keeps tiny and huge x inside fp16's
+    normal range: the bound holds from 1e-30 to 1e30."""
+    H, N, K, M = 2, 700, 128, 5
+    W = synth.kv_cache(H, N, K, seed=77)
+    x = (np.random.default_rng(8).standard_normal((H, M, N)) * scale).astype(np.float32)
+    got = _run_qmm_t(cuda_lib, W, H, N, K, x)
+    want, A = O.qmm_t(O.Q8_0, W, H, N, K, x)
+    _assert_within_bound(got, want, A, f"scale {scale}")
+
+
+def test_qmm_t_deterministic_overwrites_and_empty(cuda_lib):
+    import torch
+    H, N, K, M = 3, 3000, 128, 5
+    W = _dev(synth.kv_cache(H, N, K, seed=4))
+    x = _dev(synth.attention_probs(H, M, N, seed=4))
+    y1 = cuda_lib.qmm_t(synth.Q8_0, W, H, N, K, x)
+    y2 = torch.full_like(y1, float("nan"))
+    cuda_lib.qmm_t(synth.Q8_0, W, H, N, K, x, y=y2)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    # N = 0: y = 0
+    y0 = torch.full((H, M, K), 7.0, device="cuda")
+    cuda_lib.qmm_t(synth.Q8_0, W, H, 0, K, torch.zeros((H, M, 0), device="cuda"), y=y0)
+    assert torch.count_nonzero(y0).item() == 0
+    assert cuda_lib.qmm_device_status() == 0
+
+
+def test_qmm_t_alternating_shapes_and_streams(cuda_lib):
+    """The per-matrix counters return to zero after every call: calls of
+    different H, on the default and on a side stream, all stay right."""
+    import torch
+    side = torch.cuda.Stream()
+    for i, (H, N, K, M) in enumerate([(8, 4096, 128, 5), (2, 100, 64, 1), (16, 333, 128, 8), (8, 4096, 128, 5)]):
+        W = synth.kv_cache(H, N, K, seed=40 + i)
+        x = synth.attention_probs(H, M, N, seed=41 + i)
+        st = side if i % 2 else None
+        if st is not None:
+            with torch.cuda.stream(st):
+                Wd, xd = _dev(W), _dev(x)
+                y = cuda_lib.qmm_t(synth.Q8_0, Wd, H, N, K, xd, stream=st)
+            st.synchronize()
+            got = y.cpu().numpy()
+        else:
+            got = _run_qmm_t(cuda_lib, W, H, N, K, x)
+        want, A = O.qmm_t(O.Q8_0, W, H, N, K, x)
+        _assert_within_bound(got, want, A, f"call {i}")
+
+
+def test_qmm_t_kv_cache_full_size(cuda_lib):
+    """The Qwen3-14B-shaped value cache (8 heads x 32768 positions x 128) at
+    the size the bench times: every output against the oracle."""
+    c = synth.KV_CACHE
+    H, N, K, M = c["H"], c["N"], c["K"], c["M"]
+    W = synth.kv_cache(H, N, K, seed=9)
+    x = synth.attention_probs(H, M, N, seed=9)
+    got = _run_qmm_t(cuda_lib, W, H, N, K, x)
+    want, A = O.qmm_t(O.Q8_0, W, H, N, K, x)
+    _assert_within_bound(got, want, A, "kv cache full size")
