@@ -22,9 +22,11 @@
 //       int8 q of two rows are paired by one byte permute, made exact fp16
 //       integers by the 0x6400 exponent trick, and scaled by their rows' d
 //       (one fp16 rounding of the exact d*q).
-// Columns: the MMA j (0..3) of block b covers columns 32b + 4g + j (g the
-// MMA's column index), so each lane reads one aligned 4-byte group of quants
-// per row and block, and ends up holding 8 consecutive columns.
+// Columns (g the MMA's column index, 0..7): for K = 32, 64, 128 or 256 the
+// MMA j covers columns CPG*g + j with CPG = K/8, so each lane reads CPG
+// contiguous quant bytes of one block per row (one d per row) and ends up
+// holding 2*CPG consecutive columns; for the other K the MMA j (0..3) of
+// block b covers columns 32b + 4g + j, a 4-byte group per row and block.
 // Reduction, in a fixed order so that the result is bitwise reproducible:
 // the eight warps' sums are added in warp order in shared memory and scaled
 // back, each CTA writes its chunk sum to the workspace, and the CTA that
@@ -97,9 +99,8 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // The B pair (d_a*q_a[j], d_b*q_b[j]) from byte j of the quant words of two
 // rows: bytes (q_a ^ 0x80, 0x64, q_b ^ 0x80, 0x64) are the fp16 values
 // 1152 + q, so subtracting 1152 gives q exactly; then one multiply by (d_a, d_b).
-template <int J>
-__device__ __forceinline__ uint32_t b_pair(uint32_t wa, uint32_t wb, __half2 dd) {
-    const uint32_t u = __byte_perm(wa, wb, J | (J << 4) | ((4 + J) << 8) | ((4 + J) << 12));
+__device__ __forceinline__ uint32_t b_pair(uint32_t wa, uint32_t wb, int j, __half2 dd) {
+    const uint32_t u = __byte_perm(wa, wb, j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12));
     const uint32_t v = (u & 0x00FF00FFu) ^ 0x64806480u;
     const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));
     const __half2 r = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&v), k1152), dd);
@@ -110,6 +111,18 @@ __device__ __forceinline__ uint32_t b_pair(uint32_t wa, uint32_t wb, __half2 dd)
 // raw bits; zero for a row past the matrix.
 __device__ __forceinline__ uint32_t row_d(uint32_t row, int b, bool valid) {
     return valid ? lds16(row + 34u * b) : 0u;
+}
+
+// NW consecutive 32-bit words from the 2-byte-aligned shared address a;
+// zeros for a row past the matrix.
+template <int NW>
+__device__ __forceinline__ void row_words(uint32_t a, bool valid, uint32_t (&w)[NW]) {
+    if (valid) {
+        lds_words_u16aligned(a, w);
+    } else {
+#pragma unroll
+        for (int i = 0; i < NW; ++i) w[i] = 0u;
+    }
 }
 
 // Quant bytes 4g .. 4g+3 of block b of a row (2-byte aligned).
@@ -124,6 +137,8 @@ template <int NB>
 __global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
     using C = VtCfg<NB>;
     constexpr int K = C::K, RB = C::RB, SR = C::SR, SLOT = C::SLOT, D = C::D, RK = C::RK;
+    constexpr bool CONTIG = NB == 1 || NB == 2 || NB == 4 || NB == 8;
+    constexpr int CPG = 4 * NB, NW = CPG / 4;  // columns per MMA column index, their words
     extern __shared__ __align__(16) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + VT_WARPS * D * SLOT);  // [warp][D]
     int *last = reinterpret_cast<int *>(bars + VT_WARPS * D);
@@ -168,6 +183,9 @@ __global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
         for (; issued < min(D, nst); ++issued) issue(issued);
 
     const int g = lane >> 2, tq = lane & 3;
+    // contiguous mapping: this lane's columns CPG*g .. lie in block bb of each row
+    const int bb = (CPG * g) / 32;
+    const uint32_t qoff = 34u * bb + 2u + static_cast<uint32_t>((CPG * g) % 32);
     const float *xh = P.x + (static_cast<int64_t>(h) * P.M + P.m0) * P.N;  // row m of this launch: xh + m*N
     const int ra = 2 * tq, rb = ra + 1, rc = ra + 8, rd = ra + 9;  // this lane's four rows of a group
     // x of this lane's four positions of the group at n0, rows g and g + 8
@@ -244,18 +262,34 @@ __global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
             const uint32_t a2 = pack_half2(xc[0][2] * up, xc[0][3] * up), a3 = pack_half2(xc[1][2] * up, xc[1][3] * up);
             const uint32_t row_a = rows + ra * RB, row_b = rows + rb * RB, row_c = rows + rc * RB,
                            row_dd = rows + rd * RB;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const uint32_t wa = row_q4(row_a, b, g, va), wb = row_q4(row_b, b, g, vb);
-                const uint32_t wc = row_q4(row_c, b, g, vc), wd = row_q4(row_dd, b, g, vd);
-                const uint32_t dab = row_d(row_a, b, va) | (row_d(row_b, b, vb) << 16);
-                const uint32_t dcd = row_d(row_c, b, vc) | (row_d(row_dd, b, vd) << 16);
+            if constexpr (CONTIG) {
+                // CPG contiguous quant bytes of block bb per row, one d per row
+                uint32_t wa[NW], wb[NW], wc[NW], wd[NW];
+                row_words(row_a + qoff, va, wa);
+                row_words(row_b + qoff, vb, wb);
+                row_words(row_c + qoff, vc, wc);
+                row_words(row_dd + qoff, vd, wd);
+                const uint32_t dab = row_d(row_a, bb, va) | (row_d(row_b, bb, vb) << 16);
+                const uint32_t dcd = row_d(row_c, bb, vc) | (row_d(row_dd, bb, vd) << 16);
                 const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
                 const __half2 d89 = *reinterpret_cast<const __half2 *>(&dcd);
-                mma16816(acc[b][0], a0, a1, a2, a3, b_pair<0>(wa, wb, d01), b_pair<0>(wc, wd, d89));
-                mma16816(acc[b][1], a0, a1, a2, a3, b_pair<1>(wa, wb, d01), b_pair<1>(wc, wd, d89));
-                mma16816(acc[b][2], a0, a1, a2, a3, b_pair<2>(wa, wb, d01), b_pair<2>(wc, wd, d89));
-                mma16816(acc[b][3], a0, a1, a2, a3, b_pair<3>(wa, wb, d01), b_pair<3>(wc, wd, d89));
+#pragma unroll
+                for (int j = 0; j < CPG; ++j)
+                    mma16816(acc[j >> 2][j & 3], a0, a1, a2, a3, b_pair(wa[j >> 2], wb[j >> 2], j & 3, d01),
+                             b_pair(wc[j >> 2], wd[j >> 2], j & 3, d89));
+            } else {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const uint32_t wa = row_q4(row_a, b, g, va), wb = row_q4(row_b, b, g, vb);
+                    const uint32_t wc = row_q4(row_c, b, g, vc), wd = row_q4(row_dd, b, g, vd);
+                    const uint32_t dab = row_d(row_a, b, va) | (row_d(row_b, b, vb) << 16);
+                    const uint32_t dcd = row_d(row_c, b, vc) | (row_d(row_dd, b, vd) << 16);
+                    const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
+                    const __half2 d89 = *reinterpret_cast<const __half2 *>(&dcd);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma16816(acc[b][j], a0, a1, a2, a3, b_pair(wa, wb, j, d01), b_pair(wc, wd, j, d89));
+                }
             }
         }
         __syncwarp();
@@ -272,9 +306,8 @@ __global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
     // back to the true scale: 1 / up = 2^(ew - 139) (exact)
     const float down = ew > 12 ? pow2_biased(ew - 12) : 0x1p-127f;
     // every warp's ring is drained: the rings now hold the warps' sums,
-    // [warp][m][RK] (pitch K + 1: the lanes' columns fall in distinct banks);
-    // lane (g, tq) holds, for block b, columns 32b + 8tq + j (acc[b][j][0],
-    // row g; [2], row g + 8) and 32b + 8tq + 4 + j ([1] and [3])
+    // [warp][m][RK] (pitch K + 1); lane (g, tq) holds rows g ([0], [1]) and
+    // g + 8 ([2], [3]) of the MMA's output columns 2tq and 2tq + 1
     __syncthreads();
     float *sums = reinterpret_cast<float *>(smem);
     {
@@ -283,7 +316,9 @@ __global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
         for (int b = 0; b < NB; ++b)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int k0 = 32 * b + 8 * tq + j, k1 = k0 + 4;
+                // contiguous mapping: MMA jj = 4b + j, columns CPG*2tq + jj and CPG*(2tq+1) + jj
+                const int k0 = CONTIG ? CPG * 2 * tq + 4 * b + j : 32 * b + 8 * tq + j;
+                const int k1 = CONTIG ? k0 + CPG : k0 + 4;
                 r0p[k0] = acc[b][j][0] * down;
                 r0p[k1] = acc[b][j][1] * down;
                 r1p[k0] = acc[b][j][2] * down;

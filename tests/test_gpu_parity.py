@@ -512,3 +512,14 @@ def test_qmm_t_kv_cache_full_size(cuda_lib):
     got = _run_qmm_t(cuda_lib, W, H, N, K, x)
     want, A = O.qmm_t(O.Q8_0, W, H, N, K, x)
     _assert_within_bound(got, want, A, "kv cache full size")
+
+
+@pytest.mark.parametrize("N,K,M", [(4096, 128, 5), (777, 64, 1), (32768, 128, 8), (1500, 256, 4)])
+def test_attention_scores_on_q8_0_key_cache(cuda_lib, N, K, M):
+    """The score side over a q8_0 key cache is qmm itself: N cached positions of
+    head_dim K, M query heads (the queries quantised as any activation)."""
+    W = synth.kv_cache(1, N, K, seed=N + K)
+    x = synth.activations(M, K, seed=M + K)
+    got = _run_qmm(cuda_lib, synth.Q8_0, W, N, K, x)
+    want, A = O.qmm(synth.Q8_0, W, N, K, x)
+    _assert_within_bound(got, want, A, f"scores N={N} K={K} M={M}")
