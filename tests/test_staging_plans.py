@@ -1,0 +1,213 @@
+"""CPU models of the address arithmetic of two staging paths, checked before
+any GPU run (no GPU needed):
+
+* the value-cache product (qmm_t.cu): the chunks of all CTAs and the row
+  ranges of their eight warps cover every matrix exactly once; every bulk
+  copy starts 16-byte aligned, has a 16-byte multiple size, stays inside the
+  cache and its shared-memory slot; the bytes a lane reads (quant words,
+  scales) lie inside what its stage copied; the warps' sums fit in the rings
+  after the stream; shared memory stays within the per-block limit;
+* the tcgen05 prefill's Q6_K / Q8_0 staging (gemm_tc.cu): each dequantiser
+  warp's 16-byte chunk loads stay inside the matrix unless the kernel's
+  "careful" test selects the word-by-word path, which it does exactly when a
+  chunk would cross the matrix end; the read-back words of a super-block lie
+  inside its staged chunks; the shared-memory plan fits.
+
+The constants mirror the kernels (8 warps, ~192 KB of rings, 32- or 16-row
+stages; 14 / 17 chunks per super-step, 60 / 68-word rows)."""
+import pytest
+
+SMEM_MAX = 232448
+SMS = 152
+
+# --------------------------------------------------------------- qmm_t
+
+
+def vt_cfg(nb):
+    K, RB = 32 * nb, 34 * nb
+    SR = 32 if nb <= 4 else 16
+    SLOT = (SR * RB + 32 + 15) & ~15
+    D = min(8, (192 * 1024) // (8 * SLOT))
+    RK = K + 1
+    SMEM = 8 * D * SLOT + 8 * 8 * D + 16
+    return dict(K=K, RB=RB, SR=SR, SLOT=SLOT, D=D, RK=RK, SMEM=SMEM)
+
+
+def vt_chunk_rows(H, N, num_sms=SMS):
+    want = num_sms
+    per = max(1, -(-want // H))
+    R = -(-N // per)
+    R = -(-R // 128) * 128
+    return max(R, 128)
+
+
+@pytest.mark.parametrize("nb", range(1, 9))
+def test_qmm_t_shared_memory_plan(nb):
+    C = vt_cfg(nb)
+    assert C["D"] >= 2
+    assert C["SMEM"] <= SMEM_MAX
+    assert C["SLOT"] % 16 == 0
+    # after the stream the rings hold the eight warps' sums [warp][16][RK]
+    assert 8 * 16 * C["RK"] * 4 <= 8 * C["D"] * C["SLOT"]
+
+
+@pytest.mark.parametrize("H,N,K", [(1, 1, 32), (1, 15, 64), (2, 300, 128), (8, 4096, 128), (8, 32768, 128),
+                                   (3, 1000, 96), (1, 777, 256), (5, 64, 32), (6, 12345, 128), (4, 2049, 160),
+                                   (1, 5000, 224), (16, 333, 128), (8, 131072, 128), (1, 129, 256)])
+def test_qmm_t_chunks_and_copies(H, N, K):
+    nb = K // 32
+    C = vt_cfg(nb)
+    RB, SR, SLOT = C["RB"], C["SR"], C["SLOT"]
+    R = vt_chunk_rows(H, N)
+    assert R % 128 == 0
+    nchunk = -(-N // R)
+    assert nchunk < 2 ** 31 and H <= 65535
+    base = 1 << 20  # W is 16-byte aligned
+    w_end = base + H * N * RB
+    CPG = 4 * nb
+    contig = nb in (1, 2, 4, 8)
+    for h in range(H):
+        seen = []
+        mat0 = base + h * N * RB
+        for c in range(nchunk):
+            n_lo, n_hi = c * R, min(N, c * R + R)
+            rw = R // 8
+            assert rw % 16 == 0
+            for w in range(8):
+                w_lo = min(n_hi, n_lo + w * rw)
+                w_hi = min(n_hi, w_lo + rw)
+                if w_lo < w_hi:
+                    seen.append((w_lo, w_hi))
+                nst = -(-(w_hi - w_lo) // SR)
+                for t in range(nst):
+                    r0, r1 = w_lo + t * SR, min(w_hi, w_lo + t * SR + SR)
+                    a, b = mat0 + r0 * RB, mat0 + r1 * RB
+                    a16, b16 = a & ~15, (b + 15) & ~15
+                    if b16 > w_end:
+                        b16 = b & ~15  # the final bytes by plain loads
+                    assert a16 >= base and b16 <= w_end and a16 % 16 == 0 and (b16 - a16) % 16 == 0
+                    assert b - a16 <= SLOT  # copied bytes plus plain tail fit the slot
+                    # reads of the stage's rows: offset from the slot start
+                    off0 = a - a16
+                    for r in range(r1 - r0):
+                        row = off0 + r * RB
+                        if contig:
+                            bb = (CPG * 7) // 32  # the lane group with the largest offset
+                            q = row + 34 * bb + 2 + (CPG * 7) % 32
+                            last = (q & ~3) + 4 * (CPG // 4) + 4  # aligned words read
+                        else:
+                            q = row + 34 * (nb - 1) + 2 + 4 * 7
+                            last = (q & ~3) + 8
+                        assert last <= SLOT
+                        assert row + RB <= b - a16  # the row itself was copied
+        seen.sort()
+        pos = 0
+        for lo, hi in seen:
+            assert lo == pos
+            pos = hi
+        assert pos == N
+
+
+def test_qmm_t_counters_and_parts():
+    for H, N, K in [(8, 32768, 128), (1, 1, 32), (65535, 16, 32)]:
+        R = vt_chunk_rows(H, N)
+        nchunk = -(-N // R)
+        part = H * nchunk * 16 * K * 4
+        assert part > 0 and nchunk >= 1
+
+
+# --------------------------------------------- tcgen05 prefill staging
+
+QMM_Q8_0, QMM_Q4_K, QMM_Q6_K = 0, 1, 2
+SSB = {QMM_Q6_K: 210, QMM_Q8_0: 272}
+CHUNKS = {QMM_Q6_K: 14, QMM_Q8_0: 17}
+PITCH_W = {QMM_Q6_K: 60, QMM_Q8_0: 68}
+
+
+def tc_smem(BT, T):
+    XBOX = BT * 128
+    X_BYTES = 2 * XBOX
+    RAW_Q = 32 * PITCH_W[T] * 4
+    X_FIT = (232448 - 1536 - 4 * RAW_Q) // X_BYTES
+    X = min(8, X_FIT)
+    OFF_R = X * X_BYTES
+    OFF_BAR = OFF_R + 4 * RAW_Q
+    return dict(X=X, SMEM=OFF_BAR + 512 + 1024, RAW_Q=RAW_Q)
+
+
+@pytest.mark.parametrize("T", [QMM_Q6_K, QMM_Q8_0])
+@pytest.mark.parametrize("BT", [64, 128, 256])
+def test_tc_own_shared_memory_plan(T, BT):
+    P = tc_smem(BT, T)
+    assert P["X"] >= 2
+    assert P["SMEM"] <= SMEM_MAX
+    assert 16 * (P["X"] + 4) + 8 + 64 <= 480  # barrier area
+    # the quarter's buffer: 32 rows of CH chunks at a pitch of PW words
+    assert CHUNKS[T] * 16 <= PITCH_W[T] * 4
+    # odd number of 16-byte chunks per row: conflict-free chunk reads
+    assert (PITCH_W[T] * 4 // 16) % 2 == 1
+
+
+@pytest.mark.parametrize("T,N,K", [(QMM_Q6_K, 301, 768), (QMM_Q6_K, 1000, 2048), (QMM_Q6_K, 130, 5120),
+                                   (QMM_Q6_K, 77, 256), (QMM_Q6_K, 5120, 17408), (QMM_Q6_K, 3, 4352),
+                                   (QMM_Q8_0, 301, 768), (QMM_Q8_0, 257, 4352), (QMM_Q8_0, 33, 256)])
+def test_tc_own_chunk_loads(T, N, K):
+    """Every 16-byte chunk load of the staging (two warps per quarter, half the
+    chunks each) stays inside [W, w_end) unless the careful path is taken, and
+    the careful path is taken exactly for the matrix's final super-block
+    reaching past the end."""
+    ssb, CH = SSB[T], CHUNKS[T]
+    RB = (K // (32 if T == QMM_Q8_0 else 256)) * (34 if T == QMM_Q8_0 else 210)
+    W = 1 << 24
+    w_end = W + N * RB
+    nss = K // 256
+    HALF = 32 * CH // 2
+    NT = -(-HALF // 32)
+    careful_seen = 0
+    for n0 in range(0, -(-N // 128) * 128, 128):
+        for quarter in range(4):
+            nrows = min(32, N - (n0 + 32 * quarter))
+            rows0 = W + (n0 + 32 * quarter) * RB
+            for js in range(nss):
+                seg0 = rows0 + js * ssb
+                careful = T == QMM_Q6_K and nrows > 0 and \
+                    ((seg0 + (nrows - 1) * RB) & ~15) + 16 * CH > w_end
+                need = False
+                for cp in range(2):
+                    for lane in range(32):
+                        for t in range(NT):
+                            i = lane + 32 * t
+                            if i >= HALF:
+                                continue
+                            g = HALF * cp + i
+                            r, c = g // CH, g % CH
+                            if r >= nrows:
+                                continue
+                            a = ((seg0 + r * RB) & ~15) + 16 * c
+                            assert a >= W and a % 16 == 0
+                            if a + 16 > w_end:
+                                need = True
+                                assert careful, (n0, quarter, js, r, c)
+                            # the super-block's bytes lie inside the row's 14 / 17 chunks
+                            seg = seg0 + r * RB
+                            assert seg + ssb <= ((seg0 + r * RB) & ~15) + 16 * CH
+                            if T == QMM_Q6_K:
+                                dl = seg & 15
+                                assert dl % 2 == 0
+                                # read-back: ql 5 chunks from 4h, qh 3 from 8 + 2h, scale words
+                                for h in range(2):
+                                    assert 4 * h + 5 <= CH and 8 + 2 * h + 3 <= CH
+                                    # the scale word: two aligned words from (dl + 192 + 8h + 4cp) & ~3
+                                    assert ((dl + 192 + 8 * h + 4) & ~3) + 8 <= 16 * CH
+                                    assert dl + 208 + 2 <= 16 * CH  # d
+                                    # realign reads the aligned words (dl >> 2) .. (dl >> 2) + NOUT of
+                                    # the loaded chunks: the last byte it touches must lie in them
+                                    assert (dl & ~3) + 4 * 16 + 3 < 16 * 5   # ql: 16 words from 5 chunks
+                                    assert (dl & ~3) + 4 * 8 + 3 < 16 * 3    # qh: 8 words from 3 chunks
+                            else:
+                                assert seg % 16 == 0
+                if careful:
+                    careful_seen += 1
+                    assert need or T == QMM_Q6_K
+    if T == QMM_Q6_K and (N * RB) % 16:
+        assert careful_seen >= 1
