@@ -39,7 +39,7 @@
 #include <omp.h>
 #endif
 
-enum { OR_Q8_0 = 0, OR_Q4_K = 1, OR_Q6_K = 2 };
+enum { OR_Q8_0 = 0, OR_Q4_K = 1, OR_Q6_K = 2, OR_Q5_K = 3 };
 
 /* ----------------------------------------------------------------------- */
 /* binary16 -> binary32, from the IEEE-754 bit definition (sign, 5-bit      */
@@ -70,6 +70,7 @@ int oracle_block_bytes(int type)
     case OR_Q8_0: return 34;
     case OR_Q4_K: return 144;
     case OR_Q6_K: return 210;
+    case OR_Q5_K: return 176;
     default: return -1;
     }
 }
@@ -80,6 +81,7 @@ int oracle_block_weights(int type)
     case OR_Q8_0: return 32;
     case OR_Q4_K: return 256;
     case OR_Q6_K: return 256;
+    case OR_Q5_K: return 256;
     default: return -1;
     }
 }
@@ -200,9 +202,50 @@ void oracle_pack_q6_k(uint16_t d_bits, const int8_t sc[16], const uint8_t q[256]
 }
 
 /* ----------------------------------------------------------------------- */
+/* Q5_K: [0,2) d, [2,4) dmin, [4,16) scale bytes S[12] (packed as Q4_K's),  */
+/* [16,48) qh[32], [48,176) qs[128].  Weight p = 64c + 32s + l (c = 0..3,   */
+/* s = 0,1, l = 0..31) is in sub-block j = 2c + s; its low four bits are    */
+/* the low (s = 0) or high (s = 1) nibble of qs[32c + l] as in Q4_K, its    */
+/* fifth bit is bit j of qh[l]; q = low | fifth << 4 in 0..31 and the       */
+/* weight is d*sc[j]*q - dmin*m[j] (GGUF convention, as Q4_K with one more  */
+/* bit per quant).                                                          */
+/* ----------------------------------------------------------------------- */
+void oracle_unpack_q5_k(const uint8_t *blk, uint16_t *d_bits, uint16_t *dmin_bits,
+                        uint8_t sc[8], uint8_t m[8], uint8_t q[256])
+{
+    /* the fields shared with Q4_K: d, dmin, scales; then the two bit planes */
+    uint8_t as4[144];
+    memcpy(as4, blk, 16);
+    memcpy(as4 + 16, blk + 48, 128);
+    oracle_unpack_q4_k(as4, d_bits, dmin_bits, sc, m, q);
+    const uint8_t *qh = blk + 16;
+    for (int p = 0; p < 256; ++p) {
+        int j = p / 32, l = p % 32;
+        q[p] = (uint8_t)(q[p] | (((qh[l] >> j) & 1) << 4));
+    }
+}
+
+void oracle_pack_q5_k(uint16_t d_bits, uint16_t dmin_bits, const uint8_t sc[8],
+                      const uint8_t m[8], const uint8_t q[256], uint8_t *blk)
+{
+    uint8_t as4[144], lo[256];
+    for (int p = 0; p < 256; ++p)
+        lo[p] = (uint8_t)(q[p] & 15);
+    oracle_pack_q4_k(d_bits, dmin_bits, sc, m, lo, as4);
+    memcpy(blk, as4, 16);
+    memcpy(blk + 48, as4 + 16, 128);
+    uint8_t *qh = blk + 16;
+    memset(qh, 0, 32);
+    for (int p = 0; p < 256; ++p) {
+        int j = p / 32, l = p % 32;
+        qh[l] = (uint8_t)(qh[l] | (((q[p] >> 4) & 1) << j));
+    }
+}
+
+/* ----------------------------------------------------------------------- */
 /* Dequantisation of one block into fp32, fixed operation order, no FMA:    */
 /*   Q8_0: w = d*q                                                          */
-/*   Q4_K: t1 = d*sc, t2 = t1*q, t3 = dmin*m, w = t2 - t3                   */
+/*   Q4_K, Q5_K: t1 = d*sc, t2 = t1*q, t3 = dmin*m, w = t2 - t3             */
 /*   Q6_K: t1 = d*sc, w = t1*(q-32)                                         */
 /* (the scale products are formed first, reading "d*sc*q - dmin*m" from     */
 /* left to right).                                                          */
@@ -216,10 +259,13 @@ static void dequant_block(int type, const uint8_t *blk, float *w)
         float d = oracle_half_to_float(db);
         for (int i = 0; i < 32; ++i)
             w[i] = d * (float)q[i];
-    } else if (type == OR_Q4_K) {
+    } else if (type == OR_Q4_K || type == OR_Q5_K) {
         uint16_t db, dmb;
         uint8_t sc[8], m[8], q[256];
-        oracle_unpack_q4_k(blk, &db, &dmb, sc, m, q);
+        if (type == OR_Q4_K)
+            oracle_unpack_q4_k(blk, &db, &dmb, sc, m, q);
+        else
+            oracle_unpack_q5_k(blk, &db, &dmb, sc, m, q);
         float d = oracle_half_to_float(db), dmin = oracle_half_to_float(dmb);
         for (int p = 0; p < 256; ++p) {
             int j = p / 32;
@@ -320,10 +366,13 @@ static void qmm_row(int type, const uint8_t *row, int64_t K, const int8_t *xq, c
                 for (int i = 0; i < 32; ++i)
                     I += (int32_t)q[i] * (int32_t)qx[blk * 32 + i];
                 acc += (double)dx[blk] * (double)oracle_half_to_float(db) * (double)I;
-            } else if (type == OR_Q4_K) {
+            } else if (type == OR_Q4_K || type == OR_Q5_K) {
                 uint16_t db, dmb;
                 uint8_t sc[8], m[8], q[256];
-                oracle_unpack_q4_k(B, &db, &dmb, sc, m, q);
+                if (type == OR_Q4_K)
+                    oracle_unpack_q4_k(B, &db, &dmb, sc, m, q);
+                else
+                    oracle_unpack_q5_k(B, &db, &dmb, sc, m, q);
                 double d = oracle_half_to_float(db), dmin = oracle_half_to_float(dmb);
                 for (int j = 0; j < 8; ++j) {
                     int64_t b32 = blk * 8 + j;

@@ -419,3 +419,115 @@ def test_qmm_t_planted_transpose_is_caught():
     wrong = x[0].astype(np.float64) @ w.T   # the mistake
     assert np.allclose(y[0], right, rtol=1e-12, atol=1e-12)
     assert not np.allclose(wrong, right, rtol=1e-6, atol=1e-6)
+
+
+# ----------------------------------------------- Q5_K (the next K-quant)
+
+def _pack_q5_k_from_layout(d_bits, dmin_bits, sc, m, q):
+    """Q5_K bytes written straight from the layout in the golden file's
+    header (independent of the oracle's packer)."""
+    blk = np.zeros(176, np.uint8)
+    blk[0:2] = np.array([d_bits], np.uint16).view(np.uint8)
+    blk[2:4] = np.array([dmin_bits], np.uint16).view(np.uint8)
+    S = blk[4:16]
+    for j in range(4):
+        S[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+        S[j + 4] = (m[j] & 63) | ((m[j + 4] >> 4) << 6)
+        S[j + 8] = (sc[j + 4] & 15) | ((m[j + 4] & 15) << 4)
+    for p in range(256):
+        j, l = p // 32, p % 32
+        blk[16 + l] |= ((int(q[p]) >> 4) & 1) << j
+        c, s = p // 64, (p // 32) % 2
+        blk[48 + 32 * c + l] |= (int(q[p]) & 15) << (4 * s)
+    return blk
+
+
+def test_golden_q5_k_block():
+    rows, ws = _read_fixture("q5_k_block.txt")
+    d, dm = int(rows["d"][0], 16), int(rows["dmin"][0], 16)
+    sc = np.array([int(v) for v in rows["sc"]], np.uint8)
+    m = np.array([int(v) for v in rows["m"]], np.uint8)
+    q = np.array([(5 * p + 3) % 32 for p in range(256)], np.uint8)
+    blk = _pack_q5_k_from_layout(d, dm, sc, m, q)
+    d2, dm2, sc2, m2, q2 = O.unpack_q5_k(blk)
+    assert (d2, dm2) == (d, dm)
+    assert np.array_equal(sc2, sc) and np.array_equal(m2, m) and np.array_equal(q2, q)
+    w = O.dequant(O.Q5_K, blk, 256)
+    for p, qv, wv in ws:
+        assert q[p] == int(qv)
+        assert w[p] == np.float32(float(wv)), (p, w[p], wv)
+    # the oracle's packer writes the same bytes
+    assert np.array_equal(O.pack_q5_k(d, dm, sc, m, q), blk)
+
+
+def test_q5_k_without_fifth_bits_is_q4_k():
+    """With qh all zero a Q5_K block is the Q4_K block of the same d, dmin,
+    scales and nibbles (the pinned Q4_K oracle decides every weight)."""
+    W4 = synth.weights(synth.Q4_K, 6, 512, seed=77)
+    blocks4 = W4.reshape(-1, 144)
+    blocks5 = np.concatenate([np.concatenate([b[:16], np.zeros(32, np.uint8), b[16:]]) for b in blocks4])
+    n = blocks4.shape[0] * 256
+    assert np.array_equal(O.dequant(O.Q5_K, blocks5, n).view(np.uint32),
+                          O.dequant(O.Q4_K, W4, n).view(np.uint32))
+
+
+def test_q5_k_fifth_bit_index_closed_form():
+    """qh[l] = 1 << (l mod 8) sets the fifth bit of weight 32j + l exactly when
+    l mod 8 == j: those weights gain 16*d*sc[j] over the Q4_K weight (d = 1,
+    dmin = 0: every weight is a small integer, exact), the others are unchanged."""
+    W4 = synth.weights(synth.Q4_K, 1, 256, seed=5).reshape(144).copy()
+    W4[0:2] = np.array([0x3C00], np.uint16).view(np.uint8)   # d = 1
+    W4[2:4] = 0                                               # dmin = 0
+    qh = np.array([1 << (l % 8) for l in range(32)], np.uint8)
+    blk5 = np.concatenate([W4[:16], qh, W4[16:]])
+    w4 = O.dequant(O.Q4_K, W4, 256).astype(np.float64)
+    w5 = O.dequant(O.Q5_K, blk5, 256).astype(np.float64)
+    _, _, sc, _, _ = O.unpack_q4_k(W4)
+    for p in range(256):
+        j, l = p // 32, p % 32
+        extra = 16.0 * sc[j] if l % 8 == j else 0.0
+        assert w5[p] == w4[p] + extra, (p, w5[p], w4[p], extra)
+
+
+def _q5_k_fields(rng, N, K):
+    nb = K // 256
+    f = dict(d=rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16),
+             dm=rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16),
+             sc=rng.integers(0, 64, (N, nb, 8)).astype(np.uint8),
+             m=rng.integers(0, 64, (N, nb, 8)).astype(np.uint8),
+             q=rng.integers(0, 32, (N, nb, 256)).astype(np.uint8))
+    W = np.concatenate([_pack_q5_k_from_layout(f["d"][n, b], f["dm"][n, b], f["sc"][n, b], f["m"][n, b],
+                                               f["q"][n, b]) for n in range(N) for b in range(nb)])
+    d = f["d"].view(np.float16).astype(np.float64)
+    dm = f["dm"].view(np.float16).astype(np.float64)
+    Wd = (d[:, :, None] * np.repeat(f["sc"], 32, axis=2) * f["q"]
+          - dm[:, :, None] * np.repeat(f["m"], 32, axis=2)).reshape(N, K)
+    return W, Wd
+
+
+@pytest.mark.parametrize("K", [256, 512])
+def test_qmm_q5_k_matches_dense_f64(K):
+    rng = np.random.default_rng(300 + K)
+    N, M = 5, 3
+    W, Wd = _q5_k_fields(rng, N, K)
+    xi = rng.integers(-127, 128, (M, K)).astype(np.float64)
+    xi[:, 7::32] = 127
+    scale = np.array([1.0, 0.5, 4.0])[:, None]
+    x = (xi * scale).astype(np.float32)
+    y, A = O.qmm(O.Q5_K, W, N, K, x)
+    yd = (xi * scale) @ Wd.T
+    np.testing.assert_allclose(y, yd, rtol=1e-12, atol=1e-12 * np.abs(yd).max())
+    assert np.all(np.abs(y) <= A * (1 + 1e-9))
+
+
+def test_q5_k_planted_bit_index_mistake_is_caught():
+    """Reading the fifth bit of sub-block j from bit j + 1 (a plausible slip)
+    breaks the golden pin: applied to the input, the listed weights change."""
+    rows, ws = _read_fixture("q5_k_block.txt")
+    sc = np.array([int(v) for v in rows["sc"]], np.uint8)
+    m = np.array([int(v) for v in rows["m"]], np.uint8)
+    q = np.array([(5 * p + 3) % 32 for p in range(256)], np.uint8)
+    blk = _pack_q5_k_from_layout(int(rows["d"][0], 16), int(rows["dmin"][0], 16), sc, m, q)
+    blk[16:48] = (blk[16:48].astype(np.uint16) << 1).astype(np.uint8)   # the mistake
+    w = O.dequant(O.Q5_K, blk, 256)
+    assert any(w[p] != np.float32(float(wv)) for p, _, wv in ws)
