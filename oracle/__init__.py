@@ -4,8 +4,8 @@ TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
 CPU-baseline leg of bench.py, never by the product package.  It shares no
 code with the CUDA library.
 
-Types follow the library numbering: 0 = Q8_0, 1 = Q4_K, 2 = Q6_K; 3 = Q5_K
-(the next K-quant, checked here ahead of its kernels).
+Types follow the library numbering: 0 = Q8_0, 1 = Q4_K, 2 = Q6_K; 3 = Q5_K,
+4 = Q3_K, 5 = Q2_K (the other K-quants, checked here ahead of their kernels).
 """
 import ctypes
 import os
@@ -14,9 +14,9 @@ import numpy as np
 
 from . import build as _build
 
-Q8_0, Q4_K, Q6_K, Q5_K = 0, 1, 2, 3
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q5_K: 176}
-BLOCK_WEIGHTS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_K: 256}
+Q8_0, Q4_K, Q6_K, Q5_K, Q3_K, Q2_K = 0, 1, 2, 3, 4, 5
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q5_K: 176, Q3_K: 110, Q2_K: 84}
+BLOCK_WEIGHTS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_K: 256, Q3_K: 256, Q2_K: 256}
 
 _lib = None
 
@@ -36,6 +36,10 @@ def lib():
         L.oracle_pack_q4_k.argtypes = [ctypes.c_uint16, ctypes.c_uint16, P, P, P, P]
         L.oracle_unpack_q5_k.argtypes = [P, P, P, P, P, P]
         L.oracle_pack_q5_k.argtypes = [ctypes.c_uint16, ctypes.c_uint16, P, P, P, P]
+        L.oracle_unpack_q3_k.argtypes = [P, P, P, P]
+        L.oracle_pack_q3_k.argtypes = [ctypes.c_uint16, P, P, P]
+        L.oracle_unpack_q2_k.argtypes = [P, P, P, P, P, P]
+        L.oracle_pack_q2_k.argtypes = [ctypes.c_uint16, ctypes.c_uint16, P, P, P, P]
         L.oracle_unpack_q6_k.argtypes = [P, P, P, P]
         L.oracle_pack_q6_k.argtypes = [ctypes.c_uint16, P, P, P]
         L.oracle_dequant.argtypes = [ctypes.c_int, P, i64, P]
@@ -112,6 +116,44 @@ def pack_q5_k(d_bits, dmin_bits, sc, m, q):
     q = np.ascontiguousarray(q, dtype=np.uint8)
     out = np.zeros(176, np.uint8)
     lib().oracle_pack_q5_k(int(d_bits), int(dmin_bits), _p(sc), _p(m), _p(q), _p(out))
+    return out
+
+
+def unpack_q3_k(blk):
+    """(d bits, signed scales sc - 32 [16], q in -4..3 [256])"""
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    d = np.zeros(1, np.uint16)
+    sc = np.zeros(16, np.int8)
+    q = np.zeros(256, np.int8)
+    lib().oracle_unpack_q3_k(_p(blk), _p(d), _p(sc), _p(q))
+    return int(d[0]), sc, q
+
+
+def pack_q3_k(d_bits, sc, q):
+    sc = np.ascontiguousarray(sc, dtype=np.int8)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    out = np.zeros(110, np.uint8)
+    lib().oracle_pack_q3_k(int(d_bits), _p(sc), _p(q), _p(out))
+    return out
+
+
+def unpack_q2_k(blk):
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    d = np.zeros(1, np.uint16)
+    dm = np.zeros(1, np.uint16)
+    sc = np.zeros(16, np.uint8)
+    m = np.zeros(16, np.uint8)
+    q = np.zeros(256, np.uint8)
+    lib().oracle_unpack_q2_k(_p(blk), _p(d), _p(dm), _p(sc), _p(m), _p(q))
+    return int(d[0]), int(dm[0]), sc, m, q
+
+
+def pack_q2_k(d_bits, dmin_bits, sc, m, q):
+    sc = np.ascontiguousarray(sc, dtype=np.uint8)
+    m = np.ascontiguousarray(m, dtype=np.uint8)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    out = np.zeros(84, np.uint8)
+    lib().oracle_pack_q2_k(int(d_bits), int(dmin_bits), _p(sc), _p(m), _p(q), _p(out))
     return out
 
 

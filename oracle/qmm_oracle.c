@@ -39,7 +39,7 @@
 #include <omp.h>
 #endif
 
-enum { OR_Q8_0 = 0, OR_Q4_K = 1, OR_Q6_K = 2, OR_Q5_K = 3 };
+enum { OR_Q8_0 = 0, OR_Q4_K = 1, OR_Q6_K = 2, OR_Q5_K = 3, OR_Q3_K = 4, OR_Q2_K = 5 };
 
 /* ----------------------------------------------------------------------- */
 /* binary16 -> binary32, from the IEEE-754 bit definition (sign, 5-bit      */
@@ -71,6 +71,8 @@ int oracle_block_bytes(int type)
     case OR_Q4_K: return 144;
     case OR_Q6_K: return 210;
     case OR_Q5_K: return 176;
+    case OR_Q3_K: return 110;
+    case OR_Q2_K: return 84;
     default: return -1;
     }
 }
@@ -82,6 +84,8 @@ int oracle_block_weights(int type)
     case OR_Q4_K: return 256;
     case OR_Q6_K: return 256;
     case OR_Q5_K: return 256;
+    case OR_Q3_K: return 256;
+    case OR_Q2_K: return 256;
     default: return -1;
     }
 }
@@ -243,10 +247,105 @@ void oracle_pack_q5_k(uint16_t d_bits, uint16_t dmin_bits, const uint8_t sc[8],
 }
 
 /* ----------------------------------------------------------------------- */
+/* Q3_K: [0,32) hmask, [32,96) qs (2-bit low parts), [96,108) scale bytes   */
+/* S[12] (sixteen 6-bit scales), [108,110) d.  Weight p = 128h + 32j + l    */
+/* (h = 0,1, j = 0..3, l = 0..31) is in sub-block i = 8h + 2j + (l >= 16)   */
+/* of 16 weights; its low two bits are (qs[32h + l] >> 2j) & 3 and its high */
+/* bit is bit 4h + j of hmask[l]; q = low - 4 when that bit is clear, else  */
+/* low, in -4..3.  Scale i = low nibble | high pair << 4, with k = i mod 4  */
+/* and G = i / 4: the low nibble of S[k], S[4+k] for G = 0, 1, the high     */
+/* nibble of S[k], S[4+k] for G = 2, 3, and the pair (S[8+k] >> 2G) & 3;    */
+/* the weight is d*(sc - 32)*q (GGUF convention).                           */
+/* ----------------------------------------------------------------------- */
+void oracle_unpack_q3_k(const uint8_t *blk, uint16_t *d_bits, int8_t sc[16], int8_t q[256])
+{
+    const uint8_t *hm = blk, *qs = blk + 32, *S = blk + 96;
+    *d_bits = rd16(blk + 108);
+    for (int i = 0; i < 16; ++i) {
+        int k = i % 4, G = i / 4;
+        int lo = (G == 0) ? (S[k] & 15) : (G == 1) ? (S[4 + k] & 15) : (G == 2) ? (S[k] >> 4) : (S[4 + k] >> 4);
+        int hi = (S[8 + k] >> (2 * G)) & 3;
+        sc[i] = (int8_t)((lo | (hi << 4)) - 32);
+    }
+    for (int h = 0; h < 2; ++h)
+        for (int j = 0; j < 4; ++j)
+            for (int l = 0; l < 32; ++l) {
+                int low = (qs[32 * h + l] >> (2 * j)) & 3;
+                int bit = (hm[l] >> (4 * h + j)) & 1;
+                q[128 * h + 32 * j + l] = (int8_t)(bit ? low : low - 4);
+            }
+}
+
+/* sc: the signed scales (sc - 32 in -32..31); q in -4..3 */
+void oracle_pack_q3_k(uint16_t d_bits, const int8_t sc[16], const int8_t q[256], uint8_t *blk)
+{
+    uint8_t *hm = blk, *qs = blk + 32, *S = blk + 96;
+    memset(blk, 0, 110);
+    for (int i = 0; i < 16; ++i) {
+        int v = (sc[i] + 32) & 63, k = i % 4, G = i / 4;
+        int lo = v & 15, hi = v >> 4;
+        if (G == 0) S[k] = (uint8_t)(S[k] | lo);
+        else if (G == 1) S[4 + k] = (uint8_t)(S[4 + k] | lo);
+        else if (G == 2) S[k] = (uint8_t)(S[k] | (lo << 4));
+        else S[4 + k] = (uint8_t)(S[4 + k] | (lo << 4));
+        S[8 + k] = (uint8_t)(S[8 + k] | (hi << (2 * G)));
+    }
+    for (int h = 0; h < 2; ++h)
+        for (int j = 0; j < 4; ++j)
+            for (int l = 0; l < 32; ++l) {
+                int v = q[128 * h + 32 * j + l];  /* -4..3 */
+                int bit = v >= 0, low = bit ? v : v + 4;
+                qs[32 * h + l] = (uint8_t)(qs[32 * h + l] | (low << (2 * j)));
+                hm[l] = (uint8_t)(hm[l] | (bit << (4 * h + j)));
+            }
+    wr16(blk + 108, d_bits);
+}
+
+/* ----------------------------------------------------------------------- */
+/* Q2_K: [0,16) scale bytes (sub-block i: scale = low nibble, min = high    */
+/* nibble), [16,80) qs (2-bit quants), [80,82) d, [82,84) dmin.  Weight     */
+/* p = 128h + 32j + l is in sub-block i = 8h + 2j + (l >= 16); its quant    */
+/* is (qs[32h + l] >> 2j) & 3 in 0..3 and the weight d*sc*q - dmin*m (GGUF  */
+/* convention).                                                             */
+/* ----------------------------------------------------------------------- */
+void oracle_unpack_q2_k(const uint8_t *blk, uint16_t *d_bits, uint16_t *dmin_bits, uint8_t sc[16],
+                        uint8_t m[16], uint8_t q[256])
+{
+    const uint8_t *qs = blk + 16;
+    for (int i = 0; i < 16; ++i) {
+        sc[i] = blk[i] & 15;
+        m[i] = blk[i] >> 4;
+    }
+    *d_bits = rd16(blk + 80);
+    *dmin_bits = rd16(blk + 82);
+    for (int h = 0; h < 2; ++h)
+        for (int j = 0; j < 4; ++j)
+            for (int l = 0; l < 32; ++l)
+                q[128 * h + 32 * j + l] = (uint8_t)((qs[32 * h + l] >> (2 * j)) & 3);
+}
+
+void oracle_pack_q2_k(uint16_t d_bits, uint16_t dmin_bits, const uint8_t sc[16], const uint8_t m[16],
+                      const uint8_t q[256], uint8_t *blk)
+{
+    uint8_t *qs = blk + 16;
+    memset(blk, 0, 84);
+    for (int i = 0; i < 16; ++i)
+        blk[i] = (uint8_t)((sc[i] & 15) | ((m[i] & 15) << 4));
+    for (int h = 0; h < 2; ++h)
+        for (int j = 0; j < 4; ++j)
+            for (int l = 0; l < 32; ++l)
+                qs[32 * h + l] = (uint8_t)(qs[32 * h + l] | ((q[128 * h + 32 * j + l] & 3) << (2 * j)));
+    wr16(blk + 80, d_bits);
+    wr16(blk + 82, dmin_bits);
+}
+
+/* ----------------------------------------------------------------------- */
 /* Dequantisation of one block into fp32, fixed operation order, no FMA:    */
 /*   Q8_0: w = d*q                                                          */
 /*   Q4_K, Q5_K: t1 = d*sc, t2 = t1*q, t3 = dmin*m, w = t2 - t3             */
 /*   Q6_K: t1 = d*sc, w = t1*(q-32)                                         */
+/*   Q3_K: t1 = d*(sc-32), w = t1*q                                         */
+/*   Q2_K: t1 = d*sc, t2 = t1*q, t3 = dmin*m, w = t2 - t3 (16-weight sub-blocks) */
 /* (the scale products are formed first, reading "d*sc*q - dmin*m" from     */
 /* left to right).                                                          */
 /* ----------------------------------------------------------------------- */
@@ -272,6 +371,27 @@ static void dequant_block(int type, const uint8_t *blk, float *w)
             float t1 = d * (float)sc[j];
             float t2 = t1 * (float)q[p];
             float t3 = dmin * (float)m[j];
+            w[p] = t2 - t3;
+        }
+    } else if (type == OR_Q3_K) {
+        uint16_t db;
+        int8_t sc[16], q[256];
+        oracle_unpack_q3_k(blk, &db, sc, q);
+        float d = oracle_half_to_float(db);
+        for (int p = 0; p < 256; ++p) {
+            float t1 = d * (float)sc[p / 16];
+            w[p] = t1 * (float)q[p];
+        }
+    } else if (type == OR_Q2_K) {
+        uint16_t db, dmb;
+        uint8_t sc[16], m[16], q[256];
+        oracle_unpack_q2_k(blk, &db, &dmb, sc, m, q);
+        float d = oracle_half_to_float(db), dmin = oracle_half_to_float(dmb);
+        for (int p = 0; p < 256; ++p) {
+            int i = p / 16;
+            float t1 = d * (float)sc[i];
+            float t2 = t1 * (float)q[p];
+            float t3 = dmin * (float)m[i];
             w[p] = t2 - t3;
         }
     } else {
@@ -382,6 +502,37 @@ static void qmm_row(int type, const uint8_t *row, int64_t K, const int8_t *xq, c
                     int32_t scI = (int32_t)sc[j] * I;
                     int32_t ms = (int32_t)m[j] * sx[b32];
                     acc += (double)dx[b32] * (d * (double)scI - dmin * (double)ms);
+                }
+            } else if (type == OR_Q3_K || type == OR_Q2_K) {
+                /* sixteen sub-blocks of 16: exact int32 dots per sub-block */
+                int8_t qs3[256], sc3[16];
+                uint8_t q2[256], sc2[16], m2[16];
+                uint16_t db, dmb = 0;
+                if (type == OR_Q3_K)
+                    oracle_unpack_q3_k(B, &db, sc3, qs3);
+                else
+                    oracle_unpack_q2_k(B, &db, &dmb, sc2, m2, q2);
+                double d = oracle_half_to_float(db), dmin = oracle_half_to_float(dmb);
+                for (int j = 0; j < 8; ++j) {
+                    int64_t b32 = blk * 8 + j;
+                    int32_t J = 0, Mn = 0;
+                    for (int half = 0; half < 2; ++half) {
+                        int i16 = 2 * j + half;
+                        int32_t I = 0, S = 0;
+                        for (int i = 0; i < 16; ++i) {
+                            int p = 16 * i16 + i;
+                            int32_t qv = (type == OR_Q3_K) ? (int32_t)qs3[p] : (int32_t)q2[p];
+                            I += qv * (int32_t)qx[blk * 256 + p];
+                            S += (int32_t)qx[blk * 256 + p];
+                        }
+                        if (type == OR_Q3_K) {
+                            J += (int32_t)sc3[i16] * I;
+                        } else {
+                            J += (int32_t)sc2[i16] * I;
+                            Mn += (int32_t)m2[i16] * S;
+                        }
+                    }
+                    acc += (double)dx[b32] * (d * (double)J - dmin * (double)Mn);
                 }
             } else {
                 uint16_t db;

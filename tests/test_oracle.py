@@ -531,3 +531,186 @@ def test_q5_k_planted_bit_index_mistake_is_caught():
     blk[16:48] = (blk[16:48].astype(np.uint16) << 1).astype(np.uint8)   # the mistake
     w = O.dequant(O.Q5_K, blk, 256)
     assert any(w[p] != np.float32(float(wv)) for p, _, wv in ws)
+
+
+# ---------------------------------------- Q3_K and Q2_K (16-weight sub-blocks)
+
+def _w_rows(name):
+    """The 'w' lines of a fixture with every column: position first, the
+    expected weight last."""
+    out = []
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            parts = line.split()
+            if parts and parts[0] == "w":
+                out.append((int(parts[1]), parts[2:-1], parts[-1]))
+    return out
+
+
+def _sub16(p):
+    h, r = divmod(p, 128)
+    j, l = divmod(r, 32)
+    return 8 * h + 2 * j + (l >= 16)
+
+
+def _pack_q2_k_from_layout(d_bits, dmin_bits, sc, m, q):
+    blk = np.zeros(84, np.uint8)
+    for i in range(16):
+        blk[i] = (int(sc[i]) & 15) | ((int(m[i]) & 15) << 4)
+    for p in range(256):
+        h, r = divmod(p, 128)
+        j, l = divmod(r, 32)
+        blk[16 + 32 * h + l] |= (int(q[p]) & 3) << (2 * j)
+    blk[80:82] = np.array([d_bits], np.uint16).view(np.uint8)
+    blk[82:84] = np.array([dmin_bits], np.uint16).view(np.uint8)
+    return blk
+
+
+def _pack_q3_k_from_layout(d_bits, sc_signed, q):
+    blk = np.zeros(110, np.uint8)
+    S = blk[96:108]
+    for i in range(16):
+        v = (int(sc_signed[i]) + 32) & 63
+        k, G = i % 4, i // 4
+        lo, hi = v & 15, v >> 4
+        if G == 0:
+            S[k] |= lo
+        elif G == 1:
+            S[4 + k] |= lo
+        elif G == 2:
+            S[k] |= lo << 4
+        else:
+            S[4 + k] |= lo << 4
+        S[8 + k] |= hi << (2 * G)
+    for p in range(256):
+        h, r = divmod(p, 128)
+        j, l = divmod(r, 32)
+        v = int(q[p])
+        bit = 1 if v >= 0 else 0
+        low = v if bit else v + 4
+        blk[32 + 32 * h + l] |= low << (2 * j)
+        blk[l] |= bit << (4 * h + j)
+    blk[108:110] = np.array([d_bits], np.uint16).view(np.uint8)
+    return blk
+
+
+def test_golden_q2_k_block():
+    rows, _ = _read_fixture("q2_k_block.txt")
+    ws = [(p, cols[0], wv) for p, cols, wv in _w_rows("q2_k_block.txt")]
+    d, dm = int(rows["d"][0], 16), int(rows["dmin"][0], 16)
+    sc = np.array([(3 * i + 1) % 16 for i in range(16)], np.uint8)
+    m = np.array([(5 * i + 2) % 16 for i in range(16)], np.uint8)
+    q = np.array([(3 * p + 1 + 2 * (p // 128)) % 4 for p in range(256)], np.uint8)
+    blk = _pack_q2_k_from_layout(d, dm, sc, m, q)
+    d2, dm2, sc2, m2, q2 = O.unpack_q2_k(blk)
+    assert (d2, dm2) == (d, dm) and np.array_equal(sc2, sc) and np.array_equal(m2, m) and np.array_equal(q2, q)
+    w = O.dequant(O.Q2_K, blk, 256)
+    for p, qv, wv in ws:
+        assert q[p] == int(qv)
+        assert w[p] == np.float32(float(wv)), (p, w[p], wv)
+    assert np.array_equal(O.pack_q2_k(d, dm, sc, m, q), blk)
+
+
+def test_golden_q3_k_block():
+    rows, _ = _read_fixture("q3_k_block.txt")
+    ws = [(p, cols[0], wv) for p, cols, wv in _w_rows("q3_k_block.txt")]
+    d = int(rows["d"][0], 16)
+    sc = np.array([(7 * i + 3) % 64 - 32 for i in range(16)], np.int8)
+    q = np.array([(5 * p + 2 + 3 * (p // 128)) % 8 - 4 for p in range(256)], np.int8)
+    blk = _pack_q3_k_from_layout(d, sc, q)
+    d2, sc2, q2 = O.unpack_q3_k(blk)
+    assert d2 == d and np.array_equal(sc2, sc) and np.array_equal(q2, q)
+    w = O.dequant(O.Q3_K, blk, 256)
+    for p, qv, wv in ws:
+        assert q[p] == int(qv)
+        assert w[p] == np.float32(float(wv)), (p, w[p], wv)
+    assert np.array_equal(O.pack_q3_k(d, sc, q), blk)
+
+
+def test_q3_k_high_bit_closed_forms():
+    """All high bits set: q is the 2-bit low part (0..3); all clear: low - 4.
+    With d = 1 and every scale 33 (sc - 32 = 1) the weights are those integers."""
+    S = np.zeros(12, np.uint8)
+    for i in range(16):       # every 6-bit scale = 33 = 0b100001
+        k, G = i % 4, i // 4
+        if G == 0:
+            S[k] |= 1
+        elif G == 1:
+            S[4 + k] |= 1
+        elif G == 2:
+            S[k] |= 1 << 4
+        else:
+            S[4 + k] |= 1 << 4
+        S[8 + k] |= 2 << (2 * G)
+    rng = np.random.default_rng(17)
+    qs = rng.integers(0, 256, 64).astype(np.uint8)
+    low = np.array([(int(qs[32 * (p // 128) + p % 32]) >> (2 * ((p % 128) // 32))) & 3 for p in range(256)])
+    for hm, want in ((0xFF, low), (0x00, low - 4)):
+        blk = np.concatenate([np.full(32, hm, np.uint8), qs, S, np.array([0x3C00], np.uint16).view(np.uint8)])
+        w = O.dequant(O.Q3_K, blk, 256)
+        assert np.array_equal(w, want.astype(np.float32))
+
+
+def test_q2_k_unit_scales_give_the_quants():
+    """dmin = 0 and every scale 1: the weights are d times the 2-bit quants."""
+    rng = np.random.default_rng(19)
+    qs = rng.integers(0, 256, 64).astype(np.uint8)
+    blk = np.concatenate([np.full(16, 0x01, np.uint8), qs, np.array([0x3C00, 0x0000], np.uint16).view(np.uint8)])
+    want = np.array([(int(qs[32 * (p // 128) + p % 32]) >> (2 * ((p % 128) // 32))) & 3 for p in range(256)])
+    assert np.array_equal(O.dequant(O.Q2_K, blk, 256), want.astype(np.float32))
+
+
+def test_q3_k_planted_high_bit_mistake_is_caught():
+    """Reading the high bit from bit j instead of 4h + j (a plausible slip)
+    breaks the golden pin: applied to the input, the listed weights change."""
+    rows, _ = _read_fixture("q3_k_block.txt")
+    sc = np.array([(7 * i + 3) % 64 - 32 for i in range(16)], np.int8)
+    q = np.array([(5 * p + 2 + 3 * (p // 128)) % 8 - 4 for p in range(256)], np.int8)
+    blk = _pack_q3_k_from_layout(int(rows["d"][0], 16), sc, q)
+    hm = blk[:32].copy()
+    blk[:32] = (hm & 0x0F) | ((hm & 0x0F) << 4)   # the mistake: second half reads the first half's bits
+    w = O.dequant(O.Q3_K, blk, 256)
+    assert any(w[p] != np.float32(float(wv)) for p, _, wv in _w_rows("q3_k_block.txt"))
+
+
+def _q2_k_fields(rng, N, K):
+    nb = K // 256
+    d = rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16)
+    dm = rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16)
+    sc = rng.integers(0, 16, (N, nb, 16)).astype(np.uint8)
+    m = rng.integers(0, 16, (N, nb, 16)).astype(np.uint8)
+    q = rng.integers(0, 4, (N, nb, 256)).astype(np.uint8)
+    W = np.concatenate([_pack_q2_k_from_layout(d[n, b], dm[n, b], sc[n, b], m[n, b], q[n, b])
+                        for n in range(N) for b in range(nb)])
+    sub = np.array([_sub16(p) for p in range(256)])
+    df, dmf = d.view(np.float16).astype(np.float64), dm.view(np.float16).astype(np.float64)
+    Wd = (df[:, :, None] * sc[:, :, sub] * q - dmf[:, :, None] * m[:, :, sub]).reshape(N, K)
+    return W, Wd
+
+
+def _q3_k_fields(rng, N, K):
+    nb = K // 256
+    d = rng.integers(0x1000, 0x3C00, (N, nb)).astype(np.uint16)
+    sc = rng.integers(-32, 32, (N, nb, 16)).astype(np.int8)
+    q = rng.integers(-4, 4, (N, nb, 256)).astype(np.int8)
+    W = np.concatenate([_pack_q3_k_from_layout(d[n, b], sc[n, b], q[n, b]) for n in range(N) for b in range(nb)])
+    sub = np.array([_sub16(p) for p in range(256)])
+    df = d.view(np.float16).astype(np.float64)
+    Wd = (df[:, :, None] * sc[:, :, sub].astype(np.float64) * q).reshape(N, K)
+    return W, Wd
+
+
+@pytest.mark.parametrize("qtype,make", [(O.Q2_K, _q2_k_fields), (O.Q3_K, _q3_k_fields)])
+@pytest.mark.parametrize("K", [256, 512])
+def test_qmm_q2_k_q3_k_match_dense_f64(qtype, make, K):
+    rng = np.random.default_rng(400 + 10 * qtype + K)
+    N, M = 5, 3
+    W, Wd = make(rng, N, K)
+    xi = rng.integers(-127, 128, (M, K)).astype(np.float64)
+    xi[:, 3::32] = -127
+    scale = np.array([1.0, 0.125, 2.0])[:, None]
+    x = (xi * scale).astype(np.float32)
+    y, A = O.qmm(qtype, W, N, K, x)
+    yd = (xi * scale) @ Wd.T
+    np.testing.assert_allclose(y, yd, rtol=1e-12, atol=1e-12 * np.abs(yd).max())
+    assert np.all(np.abs(y) <= A * (1 + 1e-9))
