@@ -447,7 +447,7 @@ def test_golden_q5_k_block():
     d, dm = int(rows["d"][0], 16), int(rows["dmin"][0], 16)
     sc = np.array([int(v) for v in rows["sc"]], np.uint8)
     m = np.array([int(v) for v in rows["m"]], np.uint8)
-    q = np.array([(5 * p + 3) % 32 for p in range(256)], np.uint8)
+    q = np.array([(5 * p + 3 + 7 * (p // 32)) % 32 for p in range(256)], np.uint8)
     blk = _pack_q5_k_from_layout(d, dm, sc, m, q)
     d2, dm2, sc2, m2, q2 = O.unpack_q5_k(blk)
     assert (d2, dm2) == (d, dm)
@@ -526,7 +526,7 @@ def test_q5_k_planted_bit_index_mistake_is_caught():
     rows, ws = _read_fixture("q5_k_block.txt")
     sc = np.array([int(v) for v in rows["sc"]], np.uint8)
     m = np.array([int(v) for v in rows["m"]], np.uint8)
-    q = np.array([(5 * p + 3) % 32 for p in range(256)], np.uint8)
+    q = np.array([(5 * p + 3 + 7 * (p // 32)) % 32 for p in range(256)], np.uint8)
     blk = _pack_q5_k_from_layout(int(rows["d"][0], 16), int(rows["dmin"][0], 16), sc, m, q)
     blk[16:48] = (blk[16:48].astype(np.uint16) << 1).astype(np.uint8)   # the mistake
     w = O.dequant(O.Q5_K, blk, 256)
