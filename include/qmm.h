@@ -47,8 +47,16 @@ typedef enum {
     QMM_Q8_0 = 0, /* fp16 d | int8 q[32]                         34 B / 32 w  */
     QMM_Q4_K = 1, /* fp16 d | fp16 dmin | 12 B six-bit sc,m | 128 B nibbles
                      w = d*sc*q - dmin*m                        144 B / 256 w */
-    QMM_Q6_K = 2  /* 128 B ql | 64 B qh | int8 sc[16] | fp16 d
+    QMM_Q6_K = 2, /* 128 B ql | 64 B qh | int8 sc[16] | fp16 d
                      w = d*sc*(q-32)                            210 B / 256 w */
+    /* The other K-quants: qmm_dequant only so far (the products return
+       QMM_EINVAL_TYPE for them). */
+    QMM_Q5_K = 3, /* fp16 d | fp16 dmin | 12 B six-bit sc,m | 32 B fifth bits
+                     | 128 B nibbles; w = d*sc*q - dmin*m, q 0..31  176 B / 256 w */
+    QMM_Q3_K = 4, /* 32 B high bits | 64 B 2-bit parts | 12 B sixteen six-bit sc
+                     | fp16 d; w = d*(sc-32)*q, q -4..3            110 B / 256 w */
+    QMM_Q2_K = 5  /* 16 B 4-bit sc,m | 64 B 2-bit quants | fp16 d | fp16 dmin
+                     w = d*sc*q - dmin*m, q 0..3                   84 B / 256 w  */
 } qmm_type;
 
 /* Status codes. */
@@ -69,7 +77,8 @@ enum {
  *   n_elems  : number of weights, a multiple of QK (32 or 256).
  *   out_f32  : device, n_elems floats, 16-byte aligned.
  * Each weight is computed with a fixed fp32 order and no FMA contraction:
- *   Q8_0: d*q;  Q4_K: ((d*sc)*q) - (dmin*m);  Q6_K: (d*sc)*(q-32),
+ *   Q8_0: d*q;  Q4_K, Q5_K, Q2_K: ((d*sc)*q) - (dmin*m);  Q6_K: (d*sc)*(q-32);
+ *   Q3_K: (d*(sc-32))*q,
  * so the result is bit-for-bit reproducible.  Runs asynchronously on the
  * legacy default stream (the call has no stream argument).
  */

@@ -13,9 +13,9 @@ from __future__ import annotations
 import ctypes
 import os
 
-Q8_0, Q4_K, Q6_K = 0, 1, 2
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210}
-BLOCK_WEIGHTS = {Q8_0: 32, Q4_K: 256, Q6_K: 256}
+Q8_0, Q4_K, Q6_K, Q5_K, Q3_K, Q2_K = 0, 1, 2, 3, 4, 5  # Q5_K, Q3_K, Q2_K: qmm_dequant only so far
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q5_K: 176, Q3_K: 110, Q2_K: 84}
+BLOCK_WEIGHTS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_K: 256, Q3_K: 256, Q2_K: 256}
 
 QMM_OK = 0
 QMM_EINVAL_TYPE = -1

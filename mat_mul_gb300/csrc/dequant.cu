@@ -6,6 +6,9 @@
 //   Q8_0 : w = d*q
 //   Q4_K : w = ((d*sc)*q) - (dmin*m)      (sc, m: six-bit, from 12 bytes)
 //   Q6_K : w = (d*sc)*(q-32)              (q: 4 low bits from ql, 2 from qh)
+//   Q5_K : as Q4_K, q with a fifth bit    (0..31)
+//   Q3_K : w = (d*(sc-32))*q              (q: 2 low bits and a high bit, -4..3)
+//   Q2_K : w = ((d*sc)*q) - (dmin*m)      (sc, m: four-bit, per 16 weights)
 //
 // Work split: a warp produces 128 consecutive weights per step (lane i the
 // four weights 4i..4i+3, one 16-byte store), so the fp32 output -- four to
@@ -87,6 +90,80 @@ __device__ __forceinline__ void dequant4<QMM_Q6_K>(const uint8_t *__restrict__ b
     o = make_float4(v[0], v[1], v[2], v[3]);
 }
 
+// Q5_K: the Q4_K fields (scales at 4, nibbles at 48 + 32c) plus the fifth
+// bit of weight r, bit r/32 of qh[r mod 32] (qh at 16).
+template <>
+__device__ __forceinline__ void dequant4<QMM_Q5_K>(const uint8_t *__restrict__ blocks, int64_t p,
+                                                   float4 &o) {
+    const uint8_t *B = blocks + (p >> 8) * 176;
+    const int r = static_cast<int>(p & 255);
+    const int j = r >> 5, c = r >> 6, l = r & 31;
+    const uint32_t hdr = *reinterpret_cast<const uint32_t *>(B);
+    const float d = half_bits_to_float(hdr), dmin = half_bits_to_float(hdr >> 16);
+    int sc, m;
+    q4k_scale_min(B + 4, j, sc, m);
+    uint32_t qw = *reinterpret_cast<const uint32_t *>(B + 48 + 32 * c + l);
+    if (j & 1) qw >>= 4;
+    const uint32_t hb = *reinterpret_cast<const uint32_t *>(B + 16 + l) >> j;  // bit j of bytes l..l+3
+    const float t1 = __fmul_rn(d, static_cast<float>(sc));
+    const float t3 = __fmul_rn(dmin, static_cast<float>(m));
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int q = static_cast<int>(((qw >> (8 * e)) & 15) | (((hb >> (8 * e)) & 1) << 4));
+        v[e] = __fsub_rn(__fmul_rn(t1, static_cast<float>(q)), t3);
+    }
+    o = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+// Q3_K (110-byte blocks: only 2-byte aligned, so bytes are read one by one):
+// weight r = 128h + 32j + l takes its low two bits from (qs[32h + l] >> 2j)
+// and its high bit from bit 4h + j of hmask[l] (q = low - 4 when clear);
+// scale i = r/16 is six bits: a nibble of S[k] or S[4+k] (k = i mod 4) and
+// the pair (S[8+k] >> 2(i/4)) & 3, offset by 32.
+template <>
+__device__ __forceinline__ void dequant4<QMM_Q3_K>(const uint8_t *__restrict__ blocks, int64_t p,
+                                                   float4 &o) {
+    const uint8_t *B = blocks + (p >> 8) * 110;
+    const int r = static_cast<int>(p & 255);
+    const int h = r >> 7, j = (r >> 5) & 3, l = r & 31, i = r >> 4;
+    const uint8_t *S = B + 96;
+    const int k = i & 3, G = i >> 2;
+    const int lo = (G == 0) ? (S[k] & 15) : (G == 1) ? (S[4 + k] & 15) : (G == 2) ? (S[k] >> 4) : (S[4 + k] >> 4);
+    const int sc = (lo | (((S[8 + k] >> (2 * G)) & 3) << 4)) - 32;
+    const float d = half_bits_to_float(B[108] | (B[109] << 8));
+    const float t1 = __fmul_rn(d, static_cast<float>(sc));
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int low = (B[32 + 32 * h + l + e] >> (2 * j)) & 3;
+        const int bit = (B[l + e] >> (4 * h + j)) & 1;
+        v[e] = __fmul_rn(t1, static_cast<float>(bit ? low : low - 4));
+    }
+    o = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+// Q2_K: weight r = 128h + 32j + l is (qs[32h + l] >> 2j) & 3 (qs at 16) with
+// the four-bit scale and min of sub-block r/16 (byte r/16); d, dmin at 80.
+template <>
+__device__ __forceinline__ void dequant4<QMM_Q2_K>(const uint8_t *__restrict__ blocks, int64_t p,
+                                                   float4 &o) {
+    const uint8_t *B = blocks + (p >> 8) * 84;
+    const int r = static_cast<int>(p & 255);
+    const int h = r >> 7, j = (r >> 5) & 3, l = r & 31;
+    const int sm = B[r >> 4];
+    const uint32_t hdr = *reinterpret_cast<const uint32_t *>(B + 80);
+    const float d = half_bits_to_float(hdr), dmin = half_bits_to_float(hdr >> 16);
+    const uint32_t qw = *reinterpret_cast<const uint32_t *>(B + 16 + 32 * h + l) >> (2 * j);
+    const float t1 = __fmul_rn(d, static_cast<float>(sm & 15));
+    const float t3 = __fmul_rn(dmin, static_cast<float>(sm >> 4));
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        v[e] = __fsub_rn(__fmul_rn(t1, static_cast<float>((qw >> (8 * e)) & 3)), t3);
+    o = make_float4(v[0], v[1], v[2], v[3]);
+}
+
 template <int T>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ blocks,
                                                       int64_t n_elems, float *__restrict__ out) {
@@ -116,6 +193,9 @@ cudaError_t launch_dequant(int type, const void *blocks, int64_t n_elems, float 
     switch (type) {
     case QMM_Q8_0: dequant_kernel<QMM_Q8_0><<<gx, 256, 0, st>>>(b, n_elems, out); break;
     case QMM_Q4_K: dequant_kernel<QMM_Q4_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
+    case QMM_Q5_K: dequant_kernel<QMM_Q5_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
+    case QMM_Q3_K: dequant_kernel<QMM_Q3_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
+    case QMM_Q2_K: dequant_kernel<QMM_Q2_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
     default: dequant_kernel<QMM_Q6_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
     }
     return cudaGetLastError();

@@ -152,9 +152,18 @@ int counters(int dev, cudaStream_t st, int64_t n, unsigned **ptr) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// The products (qmm, qmm_group, qmm_t, qmm_noalloc) take Q8_0, Q4_K, Q6_K.
 int check_type(int type) {
+    if (type == QMM_Q5_K || type == QMM_Q3_K || type == QMM_Q2_K)
+        return fail(QMM_EINVAL_TYPE, "block type %d: only qmm_dequant takes it so far", type);
     if (type != QMM_Q8_0 && type != QMM_Q4_K && type != QMM_Q6_K)
         return fail(QMM_EINVAL_TYPE, "unknown block type %d", type);
+    return QMM_OK;
+}
+
+// qmm_dequant takes every type of the enum.
+int check_dequant_type(int type) {
+    if (type < QMM_Q8_0 || type > QMM_Q2_K) return fail(QMM_EINVAL_TYPE, "unknown block type %d", type);
     return QMM_OK;
 }
 
@@ -224,7 +233,7 @@ int qmm_set_decode_path(int path) {
 
 int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *out_f32) {
     g_err[0] = 0;
-    if (int rc = check_type(type)) return rc;
+    if (int rc = check_dequant_type(type)) return rc;
     const int qk_ = qk::block_weights(type);
     if (n_elems < 0 || n_elems % qk_)
         return fail(QMM_EINVAL_SHAPE, "n_elems=%lld is not a non-negative multiple of %d",

@@ -12,6 +12,12 @@ Field positions per block (the block layouts of the GGUF formats):
   Q6_K (210 B): [0,128) ql (two 4-bit low parts per byte) | [128,192) qh
                 (four 2-bit high parts per byte) | [192,208) int8 scales[16]
                 | [208,210) fp16 d
+  Q5_K (176 B): [0,2) fp16 d | [2,4) fp16 dmin | [4,16) 12 scale/min bytes
+                | [16,48) fifth bits | [48,176) 128 nibble bytes
+  Q3_K (110 B): [0,32) high bits | [32,96) 2-bit parts | [96,108) 12 bytes
+                of sixteen 6-bit scales | [108,110) fp16 d
+  Q2_K (84 B) : [0,16) 4-bit scale and min per 16 weights | [16,80) 2-bit
+                quants | [80,82) fp16 d | [82,84) fp16 dmin
 
 Drawing uniform random bytes for the packed fields gives uniform fields for
 any bijective bit packing: the 12 Q4_K scale bytes carry exactly sixteen 6-bit
@@ -28,10 +34,10 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K = 0, 1, 2
-TYPE_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K"}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210}
-BLOCK_WEIGHTS = {Q8_0: 32, Q4_K: 256, Q6_K: 256}
+Q8_0, Q4_K, Q6_K, Q5_K, Q3_K, Q2_K = 0, 1, 2, 3, 4, 5
+TYPE_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q5_K: "Q5_K", Q3_K: "Q3_K", Q2_K: "Q2_K"}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, Q5_K: 176, Q3_K: 110, Q2_K: 84}
+BLOCK_WEIGHTS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_K: 256, Q3_K: 256, Q2_K: 256}
 
 
 def row_bytes(qtype: int, K: int) -> int:
@@ -77,6 +83,32 @@ def q6_k_blocks(rng, nblocks: int, sigma: float = 5e-4) -> np.ndarray:
     return out.reshape(-1)
 
 
+def q5_k_blocks(rng, nblocks: int, sigma: float = 1e-3) -> np.ndarray:
+    """d, dmin fp16 = |N(0, sigma)|; scales/mins, fifth bits and nibbles uniform."""
+    out = np.empty((nblocks, 176), np.uint8)
+    out[:, 0:2] = _halfnormal_f16(rng, nblocks, sigma).view(np.uint8).reshape(nblocks, 2)
+    out[:, 2:4] = _halfnormal_f16(rng, nblocks, sigma).view(np.uint8).reshape(nblocks, 2)
+    out[:, 4:176] = rng.integers(0, 256, size=(nblocks, 172), dtype=np.uint8)
+    return out.reshape(-1)
+
+
+def q3_k_blocks(rng, nblocks: int, sigma: float = 1e-3) -> np.ndarray:
+    """High bits, 2-bit parts and 6-bit scales uniform; d = |N(0, sigma)|."""
+    out = np.empty((nblocks, 110), np.uint8)
+    out[:, 0:108] = rng.integers(0, 256, size=(nblocks, 108), dtype=np.uint8)
+    out[:, 108:110] = _halfnormal_f16(rng, nblocks, sigma).view(np.uint8).reshape(nblocks, 2)
+    return out.reshape(-1)
+
+
+def q2_k_blocks(rng, nblocks: int, sigma: float = 1e-3) -> np.ndarray:
+    """4-bit scales/mins and 2-bit quants uniform; d, dmin = |N(0, sigma)|."""
+    out = np.empty((nblocks, 84), np.uint8)
+    out[:, 0:80] = rng.integers(0, 256, size=(nblocks, 80), dtype=np.uint8)
+    out[:, 80:82] = _halfnormal_f16(rng, nblocks, sigma).view(np.uint8).reshape(nblocks, 2)
+    out[:, 82:84] = _halfnormal_f16(rng, nblocks, sigma).view(np.uint8).reshape(nblocks, 2)
+    return out.reshape(-1)
+
+
 def weights(qtype: int, N: int, K: int, seed: int) -> np.ndarray:
     """Packed weight rows for an N x K matrix (row-major by output row)."""
     rng = np.random.default_rng(seed)
@@ -87,6 +119,12 @@ def weights(qtype: int, N: int, K: int, seed: int) -> np.ndarray:
         return q4_k_blocks(rng, nblk)
     if qtype == Q6_K:
         return q6_k_blocks(rng, nblk)
+    if qtype == Q5_K:
+        return q5_k_blocks(rng, nblk)
+    if qtype == Q3_K:
+        return q3_k_blocks(rng, nblk)
+    if qtype == Q2_K:
+        return q2_k_blocks(rng, nblk)
     raise ValueError(qtype)
 
 

@@ -66,7 +66,7 @@ def test_validation_rejects_before_launch():
     assert L.qmm(q.Q4_K, ctypes.c_void_p(base + 2), 1, 256, ctypes.c_void_p(base),
                  1, ctypes.c_void_p(base), null) == q.QMM_EINVAL_PTR
     # dequant
-    assert L.qmm_dequant(3, null, 32, null) == q.QMM_EINVAL_TYPE
+    assert L.qmm_dequant(6, null, 32, null) == q.QMM_EINVAL_TYPE
     assert L.qmm_dequant(q.Q4_K, null, 100, null) == q.QMM_EINVAL_SHAPE
     assert L.qmm_dequant(q.Q4_K, null, 256, null) == q.QMM_EINVAL_PTR
     assert L.qmm_quantize_act(null, 1, 33, null, null, null, null) == q.QMM_EINVAL_SHAPE
@@ -162,3 +162,19 @@ def test_qmm_t_validation_rejects_before_launch():
     assert L.qmm_t(q.Q8_0, ctypes.c_void_p(base), 1, 4, 128, ctypes.c_void_p(base + 2), 1,
                    ctypes.c_void_p(base), null) == q.QMM_EINVAL_PTR
     assert L.qmm_launch_count() == before
+
+
+def test_other_k_quants_dequant_only():
+    """Q5_K, Q3_K and Q2_K: qmm_dequant validates them like the others; the
+    products reject them with QMM_EINVAL_TYPE (no product kernels yet)."""
+    L = q.load()
+    null = ctypes.c_void_p(0)
+    for t in (q.Q5_K, q.Q3_K, q.Q2_K):
+        assert L.qmm_dequant(t, null, 100, null) == q.QMM_EINVAL_SHAPE
+        assert L.qmm_dequant(t, null, 256, null) == q.QMM_EINVAL_PTR
+        assert L.qmm_dequant(t, null, 0, null) == q.QMM_OK
+        assert L.qmm(t, null, 4, 256, null, 1, null, null) == q.QMM_EINVAL_TYPE
+        assert b"only qmm_dequant" in L.qmm_last_error()
+        assert L.qmm_t(t, null, 1, 4, 128, null, 1, null, null) == q.QMM_EINVAL_TYPE
+    assert L.qmm_dequant(6, null, 256, null) == q.QMM_EINVAL_TYPE
+

@@ -46,6 +46,17 @@ def test_dequant_bitwise(cuda_lib, qtype, nblocks):
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
+@pytest.mark.parametrize("qtype", [synth.Q5_K, synth.Q3_K, synth.Q2_K])
+@pytest.mark.parametrize("nblocks", [1, 3, 37, 1000])
+def test_dequant_bitwise_other_k_quants(cuda_lib, qtype, nblocks):
+    """Q5_K, Q3_K, Q2_K dequantised on the GPU bit for bit as the oracle."""
+    W = synth.weights(qtype, nblocks, 256, seed=nblocks + 10 * qtype)
+    n = nblocks * 256
+    got = cuda_lib.qmm_dequant(qtype, _dev(W), n).cpu().numpy()
+    want = O.dequant(qtype, W, n)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
 @pytest.mark.parametrize("cfg,idx", [(0, 0), (1, 0), (2, 0), (3, 2), (3, 6), (4, 0)])
 def test_dequant_bitwise_workload_weights(cuda_lib, cfg, idx):
     name, qtype, K, N = synth.CONFIGS[cfg]["mats"][idx]
