@@ -88,10 +88,10 @@ QMM_API int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *ou
  * qmm -- y[M,N] = W[N,K] . x[M,K]^T with the activations quantised to int8
  * in blocks of 32 (Q8_1 style: fp32 scale max|x|/127, round half away from
  * zero, block sum), exact int32 per-block dot products, fp32 scaling (the
- * Q4_K prefill instead contracts the dequantised weights and activations,
- * each rounded to fp16, with fp32 accumulation on the tcgen05 tensor cores:
- * sm_103a has no integer tcgen05 mode).
- *   type     : qmm_type of W.
+ * prefill with K a multiple of 256 instead contracts the dequantised weights
+ * and activations, each rounded to fp16, with fp32 accumulation on the
+ * tcgen05 tensor cores: sm_103a has no integer tcgen05 mode).
+ *   type     : qmm_type of W: QMM_Q8_0, QMM_Q4_K or QMM_Q6_K.
  *   W_blocks : device, N*(K/QK) blocks, row-major by output row, 16-B aligned.
  *   N, K     : output rows and reduction length; K a multiple of QK.
  *   x        : device, M*K floats row-major (the activations).

@@ -23,7 +23,7 @@
 //     2-bit fields in place (two LOP3 and one IMAD per pair; groups 8..15 of
 //     a half read the high nibbles as 16x); X_G = the fp32 sum of the group's
 //     fp16 x, subtracted in fp32 before the scaling.
-// Rounding: x to fp16 (as the Q4_K prefill kernel) and, for Q4_K, dmin*m_j
+// Rounding: x to fp16 (as the tcgen05 prefill kernel) and, for Q4_K, dmin*m_j
 // to fp16; every scale is exact and every sum fp32.  The int8 form of the
 // instruction runs at about 158 TOPS on this part, a quarter of the f16
 // rate, too slow for the weight stream once the dots are scaled.

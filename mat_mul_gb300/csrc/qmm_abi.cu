@@ -20,7 +20,7 @@
 namespace {
 
 thread_local char g_err[512] = "";
-// QMM_PREFILL_KERNEL=mma keeps Q4_K prefill on the mma.sync kernel.
+// QMM_PREFILL_KERNEL=mma keeps the prefill on the mma.sync kernel.
 const bool g_force_mma_gemm = [] {
     const char *v = getenv("QMM_PREFILL_KERNEL");
     return v && strcmp(v, "mma") == 0;
