@@ -5,7 +5,9 @@ used for device memory and streams.  There is no CPU fallback: when the
 library is missing or no GPU is present the calls raise.
 
     import mat_mul_gb300 as q
-    y = q.qmm(q.Q4_K, W_blocks, N, K, x)          # x: cuda f32 [M, K]
+    y = q.qmm(q.Q4_K, W_blocks, N, K, x)          # x: cuda f32 [M, K] -> [M, N]
+    ys = q.qmm_group([(q.Q4_K, Wg, N), (q.Q4_K, Wu, N)], K, x)   # one launch, shared x
+    o = q.qmm_t(q.Q8_0, V_cache, H, T, D, p)      # p: [H, M, T] -> [H, M, D]
     w = q.qmm_dequant(q.Q6_K, blocks, n_elems)    # cuda f32 [n_elems]
 """
 from __future__ import annotations
