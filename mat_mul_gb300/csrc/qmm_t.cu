@@ -380,8 +380,8 @@ cudaError_t launch_nb(const VtParams &P, int64_t H, cudaStream_t st) {
 }  // namespace
 
 int64_t qmm_t_chunk_rows(int64_t H, int64_t N, int num_sms) {
-    // one CTA per SM over all matrices (the kernel's registers allow one
-    // resident CTA), whole stages per chunk
+    // one CTA per SM over all matrices (the rings fill most of an SM's shared
+    // memory, so one CTA is resident per SM), whole stages per chunk
     const int64_t want = static_cast<int64_t>(num_sms);
     int64_t per = (want + H - 1) / H;  // chunks per matrix
     if (per < 1) per = 1;
