@@ -211,3 +211,22 @@ def test_tc_own_chunk_loads(T, N, K):
                     assert need or T == QMM_Q6_K
     if T == QMM_Q6_K and (N * RB) % 16:
         assert careful_seen >= 1
+
+
+# ------------------------------------------- tcgen05 prefill TMA coordinates
+
+@pytest.mark.parametrize("K", [256, 512, 4096, 14336, 17408])
+@pytest.mark.parametrize("BT", [64, 128, 256])
+def test_tc_tma_x_coordinates_are_16_byte_multiples(K, BT):
+    """Every tiled TMA copy of the prefill starts at an inner coordinate whose
+    byte offset is a multiple of 16 (the rule the hardware does not check):
+    the Q4_K header box at 144*sb, its quant box at 144*sb + 16 + 64*half,
+    and the fp16 token boxes at 128*gk + 64*rank elements."""
+    for gk in range(K // 128):
+        sb, half = gk >> 1, gk & 1
+        for x_bytes in (144 * sb, 144 * sb + 16 + 64 * half):
+            assert x_bytes % 16 == 0
+        for rank in (0, 1):
+            assert ((gk * 128 + 64 * rank) * 2) % 16 == 0
+    # tensor map strides: the Q4_K rows and the fp16 token rows are 16-byte multiples
+    assert ((K // 256) * 144) % 16 == 0 and (K * 2) % 16 == 0
