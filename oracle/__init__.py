@@ -245,3 +245,34 @@ def qmm_t(qtype: int, W, H: int, N: int, K: int, x):
         y[h] = xh @ w
         A[h] = np.abs(xh) @ np.abs(w)
     return y, A
+
+
+def silu(v):
+    """v * sigmoid(v) = v / (1 + exp(-v)), in f64 (overflow-safe for v << 0)."""
+    v = np.asarray(v, dtype=np.float64)
+    out = np.empty_like(v)
+    pos = v >= 0
+    out[pos] = v[pos] / (1.0 + np.exp(-v[pos]))
+    e = np.exp(v[~pos])
+    out[~pos] = v[~pos] * e / (1.0 + e)
+    return out
+
+
+def gate_up_silu(type_gate: int, W_gate, type_up: int, W_up, N: int, K: int, x):
+    """The MLP's gated product of one decode step: h = silu(W_gate . x) * (W_up . x),
+    the two products as qmm (quantised x) and the activation in f64.
+
+    The pages' infr engine runs gate and up as one dispatch (infr landing page,
+    "why > Per-op device profiling": the expert_gateup role); the activation
+    between them is the SiLU of the Qwen3 / Llama MLPs those engines serve.
+    Returns (h, B): B bounds |h_gpu - h| from the products' bound
+    e = 2e-3 * A + 1e-5 through the slopes: |silu'| <= 1.1 everywhere, so
+    B = 1.1 * |u| * e_g + |silu(g)| * e_u + e_g * e_u."""
+    g, Ag = qmm(type_gate, W_gate, N, K, x)
+    u, Au = qmm(type_up, W_up, N, K, x)
+    eg, eu = 2e-3 * Ag + 1e-5, 2e-3 * Au + 1e-5
+    sg = silu(g)
+    h = sg * u
+    B = 1.1 * np.abs(u) * eg + np.abs(sg) * eu + 1.1 * eg * eu
+    return h, B
+

@@ -714,3 +714,39 @@ def test_qmm_q2_k_q3_k_match_dense_f64(qtype, make, K):
     yd = (xi * scale) @ Wd.T
     np.testing.assert_allclose(y, yd, rtol=1e-12, atol=1e-12 * np.abs(yd).max())
     assert np.all(np.abs(y) <= A * (1 + 1e-9))
+
+
+# ---------------------------------------------- the gate/up SiLU epilogue
+
+def test_silu_closed_forms():
+    """silu(0) = 0, silu(v) - silu(-v) = v (odd part is v/2), silu(v) -> v for
+    large v and -> 0 for very negative v; the slope stays below 1.1."""
+    v = np.array([0.0, 1.0, -1.0, 2.5, -40.0, 40.0, -1000.0])
+    s = O.silu(v)
+    assert s[0] == 0.0
+    np.testing.assert_allclose(O.silu(v) - O.silu(-v), v, rtol=1e-15, atol=1e-300)
+    assert abs(s[5] - 40.0) < 1e-15 * 40 + 40 * np.exp(-40) * 1.01
+    assert s[6] == 0.0 or abs(s[6]) < 1e-300
+    np.testing.assert_allclose(O.silu(np.array([1.0]))[0], 1.0 / (1.0 + np.exp(-1.0)), rtol=1e-15)
+    grid = np.linspace(-20, 20, 400001)
+    slope = np.diff(O.silu(grid)) / np.diff(grid)
+    assert slope.max() < 1.1 and slope.min() > -0.1
+
+
+def test_gate_up_silu_composes_the_pinned_products():
+    """h is silu of the gate product times the up product, both as the pinned
+    qmm oracle computes them; the bound is positive and covers a perturbation
+    of either product by its own bound."""
+    N, K, M = 9, 512, 3
+    Wg = synth.weights(synth.Q4_K, N, K, seed=61)
+    Wu = synth.weights(synth.Q6_K, N, K, seed=62)
+    x = synth.activations(M, K, seed=63)
+    h, B = O.gate_up_silu(O.Q4_K, Wg, O.Q6_K, Wu, N, K, x)
+    g, Ag = O.qmm(O.Q4_K, Wg, N, K, x)
+    u, Au = O.qmm(O.Q6_K, Wu, N, K, x)
+    assert np.array_equal(h, O.silu(g) * u)
+    assert np.all(B > 0)
+    eg, eu = 2e-3 * Ag + 1e-5, 2e-3 * Au + 1e-5
+    for sg_, su_ in ((1, 1), (1, -1), (-1, 1), (-1, -1)):
+        hp = O.silu(g + sg_ * eg) * (u + su_ * eu)
+        assert np.all(np.abs(hp - h) <= B * (1 + 1e-9))
