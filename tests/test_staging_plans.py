@@ -230,3 +230,131 @@ def test_tc_tma_x_coordinates_are_16_byte_multiples(K, BT):
             assert ((gk * 128 + 64 * rank) * 2) % 16 == 0
     # tensor map strides: the Q4_K rows and the fp16 token rows are 16-byte multiples
     assert ((K // 256) * 144) % 16 == 0 and (K * 2) % 16 == 0
+
+
+# ------------------------------------------- qmm_t: replay of the lanes' arithmetic
+
+import numpy as np  # noqa: E402
+
+import oracle as O  # noqa: E402
+import synth  # noqa: E402
+
+
+def _byte_perm(x, y, s):
+    """PTX prmt (default mode): byte i of the result is byte (s >> 4i) & 7 of
+    the 8 bytes y:x (x the low word)."""
+    src = [(x >> (8 * k)) & 255 for k in range(4)] + [(y >> (8 * k)) & 255 for k in range(4)]
+    return sum(src[(s >> (4 * i)) & 7] << (8 * i) for i in range(4))
+
+
+def _h2(v):
+    """the fp16 rounding of v (round to nearest even)"""
+    return float(np.float16(v))
+
+
+def _b_pair(wa, wb, j, da, db):
+    u = _byte_perm(wa, wb, j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12))
+    v = (u & 0x00FF00FF) ^ 0x64806480
+    lo = float(np.array([v & 0xFFFF], np.uint16).view(np.float16)[0])
+    hi = float(np.array([v >> 16], np.uint16).view(np.float16)[0])
+    # (value - 1152) is exact; then one fp16 product with d
+    return _h2((lo - 1152.0) * da), _h2((hi - 1152.0) * db)
+
+
+def _qmm_t_replay(W, N, K, x):
+    """One matrix, all rows in 16-position groups, the lanes of one warp as the
+    kernel assigns them; A = x * up rounded to fp16, B pairs as above, the MMA
+    summed in f64 from the fragments; returns y[m][k] (m < 16) scaled back."""
+    nb = K // 32
+    RB = 34 * nb
+    CPG = 4 * nb
+    contig = nb in (1, 2, 4, 8)
+    M = x.shape[0]
+    mx = np.abs(x).max()
+    ew = max(12, int(np.float32(mx).view(np.uint32) >> 23)) if mx > 0 else 12
+    up = 2.0 ** (139 - ew)
+    y = np.zeros((16, K))
+
+    def word(row, off):  # 32-bit little-endian word at a 2-byte-aligned byte offset of a row
+        b = W[row * RB + off: row * RB + off + 4]
+        return int(b[0]) | (int(b[1]) << 8) | (int(b[2]) << 16) | (int(b[3]) << 24)
+
+    def dval(row, blk):
+        return float(np.frombuffer(bytes(W[row * RB + 34 * blk: row * RB + 34 * blk + 2]), np.float16)[0])
+
+    for n0 in range(0, N, 16):
+        for lane in range(32):
+            g, t = lane >> 2, lane & 3
+            rows = [n0 + 2 * t, n0 + 2 * t + 1, n0 + 2 * t + 8, n0 + 2 * t + 9]
+            valid = [r < N for r in rows]
+            # A fragment: rows g, g + 8 of x times up, fp16
+            A = {}
+            for mm in (g, g + 8):
+                for kk, r in zip((2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9), rows):
+                    A[(mm, kk)] = _h2(x[mm, r] * up) if (mm < M and r < N) else 0.0
+            mmas = []  # (column index of B's n = g, the four B values by k)
+            if contig:
+                bb = (CPG * g) // 32
+                qoff = 34 * bb + 2 + (CPG * g) % 32
+                for jj in range(CPG):
+                    ws = [word(r, qoff + 4 * (jj >> 2)) if v else 0 for r, v in zip(rows, valid)]
+                    ds = [dval(r, bb) if v else 0.0 for r, v in zip(rows, valid)]
+                    b01 = _b_pair(ws[0], ws[1], jj & 3, ds[0], ds[1])
+                    b89 = _b_pair(ws[2], ws[3], jj & 3, ds[2], ds[3])
+                    mmas.append((CPG * g + jj, jj, b01 + b89))
+            else:
+                for b in range(nb):
+                    for j in range(4):
+                        ws = [word(r, 34 * b + 2 + 4 * g) if v else 0 for r, v in zip(rows, valid)]
+                        ds = [dval(r, b) if v else 0.0 for r, v in zip(rows, valid)]
+                        b01 = _b_pair(ws[0], ws[1], j, ds[0], ds[1])
+                        b89 = _b_pair(ws[2], ws[3], j, ds[2], ds[3])
+                        mmas.append((32 * b + 4 * g + j, 4 * b + j, b01 + b89))
+            # this lane's B values at (k, column) for each MMA; the D element
+            # (m, column) sums over k the A of lanes (m, k) -- gather per column
+            for col, _, bvals in mmas:
+                for kk, bv in zip((2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9), bvals):
+                    for mm in range(16):
+                        a = A.get((mm, kk))
+                        if a is None:  # A[m][k] of another lane group: recompute
+                            r = n0 + kk
+                            a = _h2(x[mm, r] * up) if (mm < M and r < N) else 0.0
+                        y[mm, col] += a * bv
+    return y[:M] / up
+
+
+@pytest.mark.parametrize("N,K,M", [(40, 128, 5), (33, 96, 3), (16, 32, 8), (21, 256, 2)])
+def test_qmm_t_lane_replay_matches_oracle(N, K, M):
+    """The replayed lanes (byte permutes, exact fp16 integers, fp16 roundings of
+    x*up and d*q, both column mappings) give the oracle's product within the
+    stated bound, and every output column is produced exactly once."""
+    W = synth.kv_cache(1, N, K, seed=N + K)
+    x = synth.attention_probs(1, M, N, seed=M)[0]
+    y = _qmm_t_replay(W, N, K, x)
+    want, A = O.qmm_t(O.Q8_0, W, 1, N, K, x[None])
+    assert np.all(np.abs(y - want[0]) <= 2e-3 * A[0] + 1e-5)
+
+
+@pytest.mark.parametrize("nb", range(1, 9))
+def test_qmm_t_output_columns_match_the_mma_columns(nb):
+    """The reduction writes lane (g, tq)'s accumulator of MMA jj = 4b + j to
+    the columns that MMA's output columns 2tq and 2tq + 1 stand for, and the
+    lanes of a warp write every column of every row exactly once."""
+    CPG = 4 * nb
+    contig = nb in (1, 2, 4, 8)
+
+    def col_of(nprime, b, j):  # the head-dim column of MMA (b, j)'s column index nprime
+        return CPG * nprime + 4 * b + j if contig else 32 * b + 4 * nprime + j
+
+    seen = {}
+    for lane in range(32):
+        g, tq = lane >> 2, lane & 3
+        for b in range(nb):
+            for j in range(4):
+                k0 = CPG * 2 * tq + 4 * b + j if contig else 32 * b + 8 * tq + j
+                k1 = k0 + CPG if contig else k0 + 4
+                assert k0 == col_of(2 * tq, b, j) and k1 == col_of(2 * tq + 1, b, j)
+                for m in (g, g + 8):
+                    for k in (k0, k1):
+                        seen[(m, k)] = seen.get((m, k), 0) + 1
+    assert len(seen) == 16 * 32 * nb and all(v == 1 for v in seen.values())
