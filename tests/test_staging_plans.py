@@ -358,3 +358,83 @@ def test_qmm_t_output_columns_match_the_mma_columns(nb):
                     for k in (k0, k1):
                         seen[(m, k)] = seen.get((m, k), 0) + 1
     assert len(seen) == 16 * 32 * nb and all(v == 1 for v in seen.values())
+
+
+# ------------------------- tcgen05 prefill: replay of the Q6_K / Q8_0 dequantisers
+
+def _realign(words, o, nout):
+    """out[j] = the 32-bit word at byte 4j + o of `words` (o even, < 16), by
+    the kernel's two selects and a funnel shift."""
+    t = [words[j + 1] if (o & 4) else words[j] for j in range(nout + 3)]
+    u = [t[j + 2] if (o & 8) else t[j] for j in range(nout + 1)]
+    sh = (o & 2) * 8
+    return [((u[j] >> sh) | (u[j + 1] << (32 - sh))) & 0xFFFFFFFF if sh else u[j] for j in range(nout)]
+
+
+def _words(buf, byte0, n):
+    return [int.from_bytes(bytes(buf[byte0 + 4 * i: byte0 + 4 * i + 4]), "little") for i in range(n)]
+
+
+def _half_bits(v):
+    return float(np.array([v & 0xFFFF], np.uint16).view(np.float16)[0])
+
+
+@pytest.mark.parametrize("dl", [0, 2, 4, 6, 8, 10, 12, 14])
+def test_tc_q6k_dequantiser_replay(dl):
+    """A Q6_K super-block staged at byte dl of its 14 chunks: the realigned ql
+    and qh words, the 4+2-bit assembly, the 0x6400 exponent trick and the
+    scale words give, for every one of the 256 weights of both K steps, q - 32
+    exactly as the oracle unpacks it, times the fp16 rounding of d*sc."""
+    blk = synth.weights(synth.Q6_K, 1, 256, seed=dl + 1)
+    buf = np.zeros(224, np.uint8)
+    buf[dl:dl + 210] = blk
+    d_or, sc_or, q_or = O.unpack_q6_k(blk)
+    d = _half_bits(d_or)
+    for h in range(2):
+        wl = _words(buf, 64 * h, 20)
+        wh = _words(buf, 128 + 32 * h, 12)
+        ql = _realign(wl, dl, 16)
+        qh = _realign(wh, dl, 8)
+        for cp in range(2):
+            off = dl + 192 + 8 * h + 4 * cp
+            scw = int.from_bytes(bytes(buf[off: off + 4]), "little")
+            for qq in range(2):
+                qi = 2 * cp + qq
+                for half_l in range(2):  # s_lo for lw < 4, s_hi for lw >= 4
+                    sbyte = (scw >> (16 * qq + 8 * half_l)) & 255
+                    s = _half_bits(int(np.float16(np.float32(d) * np.float32(sbyte - 256 if sbyte > 127 else sbyte)).view(np.uint16)))
+                    for lw in range(4 * half_l, 4 * half_l + 4):
+                        w = ql[8 * qq + lw]
+                        lo = (w & 0x0F0F0F0F) if cp == 0 else ((w >> 4) & 0x0F0F0F0F)
+                        q6 = lo | (((qh[lw] >> (4 * cp + 2 * qq)) & 0x03030303) << 4)
+                        for e in range(4):
+                            l = 4 * lw + e
+                            p = 128 * h + 32 * qi + l
+                            qv = (q6 >> (8 * e)) & 255
+                            # 0x6400 | q is 1024 + q; minus 1056 is q - 32, exact
+                            assert qv - 32 == int(q_or[p]) - 32, (h, cp, qq, lw, e)
+                            assert s == _half_bits(int(np.float16(np.float32(d) * np.float32(sc_or[p // 16])).view(np.uint16)))
+
+
+@pytest.mark.parametrize("E", range(4))
+def test_tc_q8_0_dequantiser_replay(E):
+    """The Q8_0 dequantiser of half h = E // 2, cp = E % 2 reads blocks 4h + 2cp
+    and 4h + 2cp + 1 from the 5 chunks at chunk 4E: every d and quant it
+    extracts is the oracle's."""
+    W = synth.weights(synth.Q8_0, 1, 256, seed=40 + E)  # eight blocks = one super-step
+    words = _words(W, 64 * E, 20)
+
+    def word_at(o):
+        i = (o >> 2) + E
+        return ((words[i] >> 16) | (words[i + 1] << 16)) & 0xFFFFFFFF if (o + 4 * E) & 2 else words[i]
+
+    for bb in range(2):
+        blk = 2 * E + bb  # 4h + 2cp + bb
+        d_or, q_or = O.unpack_q8_0(W[34 * blk: 34 * blk + 34])
+        ob = 34 * bb
+        assert word_at(ob) & 0xFFFF == d_or
+        for lw in range(8):
+            q = word_at(ob + 2 + 4 * lw)
+            for e in range(4):
+                b = (q >> (8 * e)) & 255
+                assert (b - 256 if b > 127 else b) == int(q_or[4 * lw + e])
