@@ -287,6 +287,25 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------------ the ranks of a job
+
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (the job is as slow as its slowest
+    rank); the value itself without a process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, bytes_per_step, ms_per_step):
+    """GB/s of the whole job: each of the world's replicas streams
+    bytes_per_step every step (weak scaling)."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------- GPU arm
 
 def run_ours(args):
@@ -368,12 +387,7 @@ def run_ours(args):
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
-        if dist:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1) / steps, dist, dev)
 
     # kernels of this library launched per decode step, counted by the library
     n0 = q.qmm_launch_count()
@@ -388,7 +402,7 @@ def run_ours(args):
     ms = timed(g_step, args.steps, args.warmup, sampler)
     clocks = sampler.summary()
     sampler.close()
-    value = world * step_bytes / (ms * 1e-3) / 1e9
+    value = job_throughput(world, step_bytes, ms)
     status = q.qmm_device_status(stream)
     assert status == 0, f"device status {status}"
 
@@ -397,7 +411,7 @@ def run_ours(args):
     ms_e2e = timed(g_e2e, args.steps, args.warmup)
     h2d = sum(call[0]["K"] * 4 for call in calls)
     d2h = sum(m["N"] * 4 for m in mats)
-    e2e_value = world * step_bytes / (ms_e2e * 1e-3) / 1e9
+    e2e_value = job_throughput(world, step_bytes, ms_e2e)
     del g_e2e, g_step
 
     detail = []
