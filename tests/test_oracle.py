@@ -750,3 +750,19 @@ def test_gate_up_silu_composes_the_pinned_products():
     for sg_, su_ in ((1, 1), (1, -1), (-1, 1), (-1, -1)):
         hp = O.silu(g + sg_ * eg) * (u + su_ * eu)
         assert np.all(np.abs(hp - h) <= B * (1 + 1e-9))
+
+
+def test_synth_new_generators():
+    """The other K-quants' blocks have their sizes and unpack to in-range
+    fields; the attention probabilities are non-negative rows summing to 1."""
+    for qt, bb in ((synth.Q5_K, 176), (synth.Q3_K, 110), (synth.Q2_K, 84)):
+        W = synth.weights(qt, 3, 512, seed=7)
+        assert W.size == 3 * 2 * bb and synth.BLOCK_BYTES[qt] == bb
+    _, _, _, _, q5 = O.unpack_q5_k(synth.weights(synth.Q5_K, 1, 256, seed=1))
+    assert q5.max() <= 31 and q5.max() >= 16          # the fifth bits are drawn
+    _, sc3, q3 = O.unpack_q3_k(synth.weights(synth.Q3_K, 1, 256, seed=1))
+    assert q3.min() >= -4 and q3.max() <= 3 and sc3.min() >= -32 and sc3.max() <= 31
+    p = synth.attention_probs(2, 3, 1000, seed=4)
+    assert p.shape == (2, 3, 1000) and p.min() >= 0
+    np.testing.assert_allclose(p.sum(axis=2), 1.0, rtol=1e-5)
+    assert synth.kv_cache(2, 10, 128, seed=1).size == 2 * 10 * 4 * 34
