@@ -152,24 +152,28 @@ QMM_API int qmm_quantize_act(const float *x, int64_t M, int64_t K, int8_t *q, fl
 
 /*
  * qmm_noalloc -- the same product as qmm(), for callers that cannot let the
- * library allocate device memory: code captured into a CUDA graph (cudaMalloc
- * is not allowed while a stream captures), serving loops that keep all device
- * memory in their own fixed pool, and latency-critical paths that must not be
- * serialised by cudaMalloc/cudaFree.  The pages have no counterpart of this
- * call; it is part of this library's interface only.
+ * library allocate device memory: serving loops that hold all device memory
+ * in their own fixed pool (a cudaMalloc by the library would fall outside
+ * that budget, and can fail once the pool has taken the rest), and loops
+ * that must not stall on cudaFree, which waits for the whole device.  The
+ * pages have no counterpart of this call; it is part of this library's
+ * interface only.
  *   Arguments, layouts and accuracy as for qmm().  Every M takes the prefill
- *   path (activation quantiser + integer tensor-core GEMM), whose quantised
- *   activations live in a 16 MiB scratch array compiled into the library:
- *   it needs align256(M*K) + 2*align256(4*M*ceil4(K/32)) bytes, so about
- *   M*K <= 13.4 million; larger calls return QMM_EINVAL_SHAPE and launch
- *   nothing.
- *   Nothing is allocated by the call.  The scratch is reserved on every GPU
- *   that loads the library, until the process exits.  The first call on a
- *   device looks the scratch's address up on that device (no allocation, but
- *   make that first call before capturing a stream into a graph).
- *   All calls share the one scratch array and overwrite it completely; calls
- *   whose kernels overlap on the GPU (different streams, no ordering between
- *   them) race on it and must be serialised by the caller.
+ *   path (activation quantiser + integer mma.sync GEMM, exact int32 block
+ *   dots), whose quantised activations live in a 16 MiB scratch array
+ *   compiled into the library: it needs
+ *   align256(M*K) + 2*align256(4*M*ceil4(K/32)) bytes, so about
+ *   M*K <= 13.4 million; larger calls (and K > 2^24, N > 2^31) return
+ *   QMM_EINVAL_SHAPE and launch nothing.
+ *   Nothing is allocated by the call (no cudaMalloc, no cudaFree, no
+ *   allocating library routine).  The scratch is reserved on every GPU that
+ *   loads the library, until the process exits.  The first call on a device
+ *   looks the scratch's device address up with cudaGetSymbolAddress while
+ *   that device is current; make that first call before any stream capture.
+ *   All calls share the one scratch array, which keeps the last call's
+ *   contents; each call overwrites every part it reads.  Calls whose kernels
+ *   overlap on the GPU (different streams, no ordering between them) race on
+ *   it and must be serialised by the caller.  Two kernel launches per call.
  */
 QMM_API int qmm_noalloc(int type, const void *W_blocks, int64_t N, int64_t K, const float *x,
                         int64_t M, float *y, void *stream);
@@ -245,6 +249,21 @@ QMM_API int64_t qmm_launch_count(void);
 #define QMM_DECODE_TENSOR 2
 #define QMM_TENSOR_MIN_M 3
 QMM_API int qmm_set_decode_path(int path);
+
+/*
+ * qmm_set_prefill_path -- which kernel qmm() and qmm_group() use for the
+ * prefill product (M > 8), process-wide, for every later call:
+ *   QMM_PREFILL_AUTO : the tcgen05 kernel (fp16 operands, fp32 accumulation
+ *                      in tensor memory) when K is a multiple of 256, else
+ *                      the int8 mma.sync kernel (default).
+ *   QMM_PREFILL_INT8 : the int8 mma.sync kernel for every shape: exact int32
+ *                      block dots as in the decode kernels, fp32 scaling.
+ * Both stay within the accuracy bound of qmm().  Returns the previous path,
+ * or QMM_EINVAL_SHAPE for an unknown value (nothing changes).  Needs no GPU.
+ */
+#define QMM_PREFILL_AUTO 0
+#define QMM_PREFILL_INT8 1
+QMM_API int qmm_set_prefill_path(int path);
 
 #ifdef __cplusplus
 }

@@ -66,6 +66,8 @@ def load():
     L.qmm_launch_count.restype = I64
     L.qmm_set_decode_path.argtypes = [I]
     L.qmm_set_decode_path.restype = I
+    L.qmm_set_prefill_path.argtypes = [I]
+    L.qmm_set_prefill_path.restype = I
     for f in ("qmm_dequant", "qmm", "qmm_noalloc", "qmm_quantize_act", "qmm_device_status",
               "qmm_release", "qmm_group"):
         getattr(L, f).restype = I
@@ -121,6 +123,8 @@ def qmm(qtype: int, W, N: int, K: int, x, y=None, stream=None):
         raise ValueError(f"x has {x.shape[-1]} columns, K = {K}")
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    elif y.dtype != torch.float32 or not y.is_contiguous() or y.device != x.device or y.numel() < M * N:
+        raise ValueError(f"y must be a contiguous float32 tensor on {x.device} with at least M*N = {M * N} elements")
     _check(load().qmm(int(qtype), _ptr(W), int(N), int(K), _ptr(x), int(M), _ptr(y),
                       _stream_handle(stream)))
     return y
@@ -170,15 +174,20 @@ def qmm_group(items, K: int, x, stream=None):
 
 
 def qmm_noalloc(qtype: int, W, N: int, K: int, x, y, stream=None):
-    """Same product as qmm() without any device allocation by the library:
-    for callers that must not allocate (graph capture, fixed memory pools).
-    y must be given.  Uses a 16 MiB scratch inside the library image; calls
-    that overlap on the GPU race on it."""
+    """Same product as qmm() without any device allocation by the library,
+    for callers that keep all device memory in their own fixed pool or must
+    not stall on cudaFree.  y [M, N] float32 must be given.  Uses a 16 MiB
+    scratch inside the library image; calls that overlap on the GPU race on
+    it."""
     import torch
     _require_cuda(W, x, y)
     if x.dtype != torch.float32 or not x.is_contiguous():
         raise ValueError("x must be a contiguous float32 tensor")
     M = 1 if x.dim() == 1 else x.shape[0]
+    if x.shape[-1] != K:
+        raise ValueError(f"x has {x.shape[-1]} columns, K = {K}")
+    if y.dtype != torch.float32 or not y.is_contiguous() or y.device != x.device or y.numel() < M * N:
+        raise ValueError(f"y must be a contiguous float32 tensor on {x.device} with at least M*N = {M * N} elements")
     _check(load().qmm_noalloc(int(qtype), _ptr(W), int(N), int(K), _ptr(x), int(M), _ptr(y),
                               _stream_handle(stream)))
     return y
@@ -217,6 +226,18 @@ DECODE_AUTO, DECODE_BLOCK, DECODE_TENSOR = 0, 1, 2
 def set_decode_path(path: int) -> int:
     """Select the decode kernel for every later call; returns the previous path."""
     rc = int(load().qmm_set_decode_path(int(path)))
+    if rc < 0:
+        raise QmmError(rc, load().qmm_last_error().decode())
+    return rc
+
+
+# Prefill kernel choice (qmm_set_prefill_path in the C header).
+PREFILL_AUTO, PREFILL_INT8 = 0, 1
+
+
+def set_prefill_path(path: int) -> int:
+    """Select the prefill kernel for every later call; returns the previous path."""
+    rc = int(load().qmm_set_prefill_path(int(path)))
     if rc < 0:
         raise QmmError(rc, load().qmm_last_error().decode())
     return rc

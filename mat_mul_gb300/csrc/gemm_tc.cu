@@ -16,14 +16,13 @@
 // Each product term carries two fp16 roundings (relative 2^-11 each) and
 // the sum is accumulated in fp32, well inside |dy| <= 2e-3*sum|w*x| + 1e-5.
 //
-// CTAs run in pairs (a cluster of two along the weight tiles) that share
-// the token tile: each loads one of the step's two token boxes and
-// multicasts it to both, halving the L2 reads of the activations; each MMA
-// commit frees the stage in both CTAs.
+// Every CTA loads its own token tile (CTAs run alone, no clusters): the
+// activations are re-read from L2 by each weight tile, which the L2 serves
+// far below its bandwidth at these arithmetic intensities.
 //
 // Warp roles (11 warps), per 128-wide K step (half a super-block):
-//   0 = token producer: one token box for the pair (ring released by the
-//       MMA commits of both CTAs);
+//   0 = token producer: the step's two 64-wide token boxes (ring released
+//       by this CTA's MMA commits);
 //   10 = raw weight producer (Q4_K): the 16-byte super-block header and the
 //       64 quant bytes of each of the 128 weight rows (ring released by the
 //       dequantisers, so dequantisation runs ahead of the MMA); Q6_K and
@@ -146,38 +145,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
-}
-
-// Token box multicast to both CTAs of the pair: it lands at the same offset
-// in each CTA's shared memory and completes bytes on each CTA's barrier at
-// the offset of `bar`.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                                 uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(static_cast<uint16_t>(3))
-        : "memory");
-}
-
-// Arrive on the barrier at offset `bar` in both CTAs of the pair once every
-// MMA issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(static_cast<uint16_t>(3))
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -310,7 +277,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::X_STAGES; ++s) {
             mbar_init(bar_x_full + 8 * s, 1);
-            mbar_init(bar_x_empty + 8 * s, 2);  // both CTAs' MMA commits (each reads both boxes)
+            mbar_init(bar_x_empty + 8 * s, 1);  // this CTA's MMA commit
         }
         for (int s = 0; s < C::R_STAGES; ++s) {
             mbar_init(bar_r_full + 8 * s, 1);
@@ -335,13 +302,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // the peer's multicast copies and commits target this CTA's barriers:
-    // both CTAs initialise theirs before either issues anything
+    // barriers initialised and the TMEM address published before any role starts
     tc_fence_before();
-    cluster_sync_all();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int rank = static_cast<int>(cluster_rank());
 
     if (warp == W_XLOAD) {
         // ------------------------------------------ token tile producer
@@ -357,12 +322,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int gk = k_step0 + kk;  // global 128-wide K step
                 const uint32_t st = sX + s * C::X_BYTES;
                 mbar_arrive_expect_tx(bar_x_full + 8 * s, C::X_BYTES);
-                // token box `rank` for both CTAs of the pair (the peer loads the other)
-                tma_load_2d_pair(st + rank * C::XBOX, &tmX, gk * BK + 64 * rank, m0, bar_x_full + 8 * s);
+                tma_load_2d(st, &tmX, gk * BK, m0, bar_x_full + 8 * s);
+                tma_load_2d(st + C::XBOX, &tmX, gk * BK + 64, m0, bar_x_full + 8 * s);
                 ++issued;
             }
-            // drain: every copy into this CTA has landed and both CTAs' last
-            // commits have arrived here before the CTA may exit
+            // drain: every copy into this CTA has landed and the last MMA
+            // commits have arrived before the CTA may exit
             for (int kk = issued > C::X_STAGES ? issued - C::X_STAGES : 0; kk < issued; ++kk) {
                 mbar_wait(bar_x_full + 8 * (kk % C::X_STAGES), (kk / C::X_STAGES) & 1, P.status);
                 if (!*abort_flag) mbar_wait(bar_x_empty + 8 * (kk % C::X_STAGES), (kk / C::X_STAGES) & 1, P.status);
@@ -408,7 +373,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int k = 0; k < BK / 16; ++k)
                     mma_ts(tmem, ta + 8 * k, desc_sw128(sx + (k >> 2) * C::XBOX + 32 * (k & 3)), C::IDESC,
                            (kk | k) ? 1u : 0u);
-                mma_commit_pair(bar_x_empty + 8 * s);
+                mma_commit(bar_x_empty + 8 * s);
                 mma_commit(bar_a_empty + 8 * sa);
             }
             // the accumulator is final once every MMA issued above completes
@@ -701,7 +666,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
     tc_fence_before();
-    cluster_sync_all();
+    __syncthreads();
     if (warp == W_MMA) {
         // every MMA must have completed before TMEM is released
         mbar_wait(bar_acc, 0, P.status);
@@ -746,8 +711,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    // weight tiles in pairs (a CTA pair shares each token box by multicast)
-    const int nt = static_cast<int>(((N + BW - 1) / BW + 1) & ~int64_t(1)), mt = static_cast<int>((M + BT - 1) / BT);
+    const int nt = static_cast<int>((N + BW - 1) / BW), mt = static_cast<int>((M + BT - 1) / BT);
     const int ksteps = static_cast<int>(K / BK);
     // Split K in two when the tiles alone would leave most SMs idle (two
     // contributions per output keep the fp32 result independent of order).
@@ -776,13 +740,6 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T, BT>, tx, th, tq, P);
 }
 

@@ -38,6 +38,7 @@ const bool g_no_mma_gemv = [] {
 }();
 std::atomic<int64_t> g_launches{0};
 std::atomic<int> g_decode_path{QMM_DECODE_AUTO};
+std::atomic<int> g_prefill_path{QMM_PREFILL_AUTO};
 
 int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int code, const char *fmt, ...) {
@@ -174,6 +175,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 namespace qk {
 // Record the calling thread's last-error text for qmm_last_error(); returns code.
 int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
+// Add n kernel launches to qmm_launch_count().
+void count_launches(int64_t n) { g_launches.fetch_add(n); }
 }  // namespace qk
 
 namespace {
@@ -229,6 +232,12 @@ int qmm_set_decode_path(int path) {
     if (path != QMM_DECODE_AUTO && path != QMM_DECODE_BLOCK && path != QMM_DECODE_TENSOR)
         return fail(QMM_EINVAL_SHAPE, "unknown decode path %d", path);
     return g_decode_path.exchange(path);
+}
+
+int qmm_set_prefill_path(int path) {
+    if (path != QMM_PREFILL_AUTO && path != QMM_PREFILL_INT8)
+        return fail(QMM_EINVAL_SHAPE, "unknown prefill path %d", path);
+    return g_prefill_path.exchange(path);
 }
 
 int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *out_f32) {
@@ -337,7 +346,8 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
         return QMM_OK;
     }
     // Prefill on the tcgen05 kernel: fp16 activations d*q [M][K].
-    if (M > 8 && !g_force_mma_gemm && qk::gemm_tc_supported(type, N, K, M)) {
+    if (M > 8 && !g_force_mma_gemm && g_prefill_path.load() == QMM_PREFILL_AUTO &&
+        qk::gemm_tc_supported(type, N, K, M)) {
         const size_t xh_bytes = align_up(static_cast<size_t>(M * K) * 2, 256);
         const size_t d_bytes = align_up(static_cast<size_t>(M * (K / 32)) * 4, 256);
         void *ws = nullptr;

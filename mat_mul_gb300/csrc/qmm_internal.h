@@ -111,5 +111,7 @@ cudaError_t launch_qmm_t(const void *W, int64_t H, int64_t N, int64_t K, const f
 
 // Set the calling thread's qmm_last_error() text; returns code.
 int record_error(int code, const char *msg);
+// Add n kernel launches to the count qmm_launch_count() reports.
+void count_launches(int64_t n);
 
 }  // namespace qk

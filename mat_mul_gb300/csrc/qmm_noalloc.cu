@@ -3,16 +3,17 @@
 // is part of the library image, so the call itself never allocates.
 //
 // Who needs it: callers that cannot let a library allocate device memory --
-// code being captured into a CUDA graph (cudaMalloc is not allowed while a
-// stream is capturing), serving loops that own a fixed memory budget through
-// their own pool allocator, and latency-critical paths that must not pay for
-// (or be serialised by) cudaMalloc/cudaFree.  qmm() grows a per-stream
-// workspace on demand instead.
+// serving loops that keep every byte of device memory in their own fixed
+// pool (a library cudaMalloc would take memory outside that budget, and may
+// fail at the worst moment when the pool has claimed the rest), and
+// latency-critical loops that must not stall on cudaFree, which synchronises
+// the whole device.  qmm() instead grows a per-stream workspace on demand.
 //
 // The scratch is a file-scope __device__ array: every GPU that loads the
 // library reserves it until the process exits.  Host code must not use the
-// array's name as a device address; each device's address is looked up once
-// with cudaGetSymbolAddress while that device is current.
+// array's name as a device address (on the host it names a stand-in, not
+// the GPU copy); each device's address is looked up once with
+// cudaGetSymbolAddress while that device is current.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -60,6 +61,12 @@ extern "C" QMM_API int qmm_noalloc(int type, const void *W_blocks, int64_t N, in
     const int qkw = qk::block_weights(type);
     if (N < 0 || M < 0 || K < 0 || K % qkw)
         return err(QMM_EINVAL_SHAPE, "N, K, M must be >= 0 and K a multiple of %lld (K=%lld)", qkw, K);
+    if (K > (int64_t(1) << 24)) return err(QMM_EINVAL_SHAPE, "K=%lld exceeds 2^24", K);
+    // M*K and M*ld*4 below must not wrap: M is bounded by what the scratch
+    // could hold at all before anything is multiplied
+    if (K > 0 && M > static_cast<int64_t>(kScratchBytes) / K)
+        return err(QMM_EINVAL_SHAPE, "M=%lld rows of K=%lld exceed the static scratch", M, K);
+    if (N > (int64_t(1) << 31)) return err(QMM_EINVAL_SHAPE, "N=%lld exceeds 2^31", N);
     if (M == 0 || N == 0) return qk::record_error(QMM_OK, "");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!y || (reinterpret_cast<uintptr_t>(y) & 3)) return err(QMM_EINVAL_PTR, "y must be non-null and 4-byte aligned");
@@ -111,7 +118,9 @@ extern "C" QMM_API int qmm_noalloc(int type, const void *W_blocks, int64_t N, in
     o.d_ld = ld;
     e = qk::launch_quantize(x, M, K, o, st, false, d.num_sms);
     if (e != cudaSuccess) return err(QMM_ECUDA, "quantize launch failed (cuda error %lld)", e);
+    qk::count_launches(1);
     e = qk::launch_gemm_mma(type, W_blocks, N, K, o.q, o.d, o.s32, static_cast<int>(ld), M, y, st);
     if (e != cudaSuccess) return err(QMM_ECUDA, "gemm launch failed (cuda error %lld)", e);
+    qk::count_launches(1);
     return qk::record_error(QMM_OK, "");
 }

@@ -178,3 +178,41 @@ def test_other_k_quants_dequant_only():
         assert L.qmm_t(t, null, 1, 4, 128, null, 1, null, null) == q.QMM_EINVAL_TYPE
     assert L.qmm_dequant(6, null, 256, null) == q.QMM_EINVAL_TYPE
 
+
+
+def test_prefill_path_setter_validates_and_returns_the_previous_path():
+    L = q.load()
+    assert L.qmm_set_prefill_path(q.PREFILL_INT8) == q.PREFILL_AUTO
+    assert L.qmm_set_prefill_path(5) == q.QMM_EINVAL_SHAPE
+    assert b"prefill path" in L.qmm_last_error()
+    assert L.qmm_set_prefill_path(q.PREFILL_AUTO) == q.PREFILL_INT8
+    with pytest.raises(q.QmmError):
+        q.set_prefill_path(-1)
+
+
+def test_noalloc_rejects_sizes_that_would_wrap_before_launch():
+    """M*K products that wrap 64 bits (M*K = 2^67 here) or exceed the static
+    scratch are rejected with QMM_EINVAL_SHAPE before anything is computed,
+    and so is K > 2^24."""
+    L = q.load()
+    buf = ctypes.create_string_buffer(4096)
+    base = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    before = L.qmm_launch_count()
+    assert L.qmm_noalloc(q.Q4_K, base, 4, 1 << 24, base, 1 << 43, base, None) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_noalloc(q.Q8_0, base, 4, 1 << 14, base, (1 << 50) + 1, base, None) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_noalloc(q.Q4_K, base, 4, 1 << 25, base, 1, base, None) == q.QMM_EINVAL_SHAPE
+    assert b"2^24" in L.qmm_last_error()
+    assert L.qmm_noalloc(q.Q4_K, base, 4, 4096, base, 4097, base, None) == q.QMM_EINVAL_SHAPE
+    assert b"scratch" in L.qmm_last_error()
+    assert L.qmm_noalloc(q.Q5_K, base, 4, 256, base, 1, base, None) == q.QMM_EINVAL_TYPE
+    assert L.qmm_launch_count() == before
+
+
+def test_noalloc_binding_checks_x_and_y():
+    torch = pytest.importorskip("torch")
+    W = torch.zeros(144, dtype=torch.uint8)
+    x = torch.zeros(2, 256)
+    y = torch.zeros(2, 1)
+    # host tensors are refused before any size check reaches the library
+    with pytest.raises(ValueError):
+        q.qmm_noalloc(q.Q4_K, W, 1, 256, x, y)

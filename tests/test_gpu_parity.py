@@ -234,10 +234,9 @@ def test_qmm_prefill_tcgen05_q6k_q8_0(cuda_lib, qtype, N, K, M):
     _assert_within_bound(y, yo, A, f"tcgen05 prefill type {qtype} N={N} K={K} M={M}")
 
 
-# Q4_K prefill shapes whose tiles the stream-K schedule of the tcgen05 GEMM
-# splits between CTA pairs: two pieces per tile with ragged M and N (and a
-# half-empty last pair), eight pieces (one tile summed from seven partials),
-# three pieces with an odd number of weight tiles.
+# Q4_K prefill shapes on the tcgen05 GEMM with ragged M and N; the two with
+# few tiles (256 x 70 and 384 x 40) split K in two, so each output is the
+# sum of two partial products added onto a zeroed y.
 STREAM_K = [(1000, 2048, 300), (256, 8192, 70), (384, 3072, 40)]
 
 
@@ -249,6 +248,47 @@ def test_qmm_prefill_split_tiles(cuda_lib, N, K, M):
     y = _run_qmm(cuda_lib, qtype, W, N, K, x)
     yo, A = O.qmm(qtype, W, N, K, x)
     _assert_within_bound(y, yo, A, f"split tiles N={N} K={K} M={M}")
+
+
+@pytest.fixture
+def prefill_path(cuda_lib):
+    def set_path(p):
+        cuda_lib.set_prefill_path(p)
+    yield set_path
+    cuda_lib.set_prefill_path(cuda_lib.PREFILL_AUTO)
+
+
+# The int8 mma.sync prefill (exact int32 block dots) forced for every shape,
+# including K multiples of 256 that would otherwise take tcgen05: tiles of 64
+# rows with ragged M and N, all three types.
+PREFILL_INT8 = GEMM_SMALL + PREFILL_TC_OTHER + [(synth.Q4_K, 1000, 2048, 300), (synth.Q6_K, 200, 5120, 130)]
+
+
+@pytest.mark.parametrize("qtype,N,K,M", PREFILL_INT8)
+def test_qmm_prefill_int8_path(cuda_lib, prefill_path, qtype, N, K, M):
+    prefill_path(cuda_lib.PREFILL_INT8)
+    W = synth.weights(qtype, N, K, seed=N + K + M + 23)
+    x = synth.activations(M, K, seed=N * K + M + 23, outlier_frac=0.01)
+    before = cuda_lib.qmm_launch_count()
+    y = _run_qmm(cuda_lib, qtype, W, N, K, x)
+    assert cuda_lib.qmm_launch_count() - before == 2  # the quantiser, then the mma.sync GEMM
+    yo, A = O.qmm(qtype, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"int8 prefill type {qtype} N={N} K={K} M={M}")
+
+
+def test_qmm_prefill_int8_path_workload_full_size(cuda_lib, prefill_path):
+    """The Mistral-7B MLP up projection at M=512 on the mma.sync kernel, on
+    sampled rows against the oracle."""
+    prefill_path(cuda_lib.PREFILL_INT8)
+    name, qtype, K, N = synth.CONFIGS[4]["mats"][0]
+    W = synth.config_weights(4, 0)
+    x = synth.config_activations(4, 512, K)
+    y = cuda_lib.qmm(qtype, _dev(W), N, K, _dev(x)).cpu().numpy()
+    assert cuda_lib.qmm_device_status() == 0
+    rows = _sample_rows(N, k=96, seed=5)
+    rb = synth.row_bytes(qtype, K)
+    yo, A = O.qmm(qtype, W.reshape(N, rb)[rows], len(rows), K, x)
+    _assert_within_bound(y[:, rows], yo, A, f"int8 prefill {name}")
 
 
 def test_qmm_prefill_is_deterministic(cuda_lib):
