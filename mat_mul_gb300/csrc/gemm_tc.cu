@@ -16,6 +16,16 @@
 // Each product term carries two fp16 roundings (relative 2^-11 each) and
 // the sum is accumulated in fp32, well inside |dy| <= 2e-3*sum|w*x| + 1e-5.
 //
+// fp16 holds 2^-24 .. 65504, so both operands are scaled by powers of two
+// into its normal range and the scales are undone exactly in fp32 in the
+// epilogue: each token row arrives from the quantiser times 2^e_m (its
+// largest |d*q| in [2^14, 2^15)), and each weight row n is dequantised times
+// 2^f_n, f_n chosen from the super-block scales as they stream (the first
+// puts the row's largest possible |w| 2^8 below fp16's top; when a later
+// super-block would overflow, f_n drops and the row's accumulator in TMEM
+// is multiplied by the exact factor once the MMAs of the earlier K steps
+// have completed).
+//
 // Every CTA loads its own token tile (CTAs run alone, no clusters): the
 // activations are re-read from L2 by each weight tile, which the L2 serves
 // far below its bandwidth at these arithmetic intensities.
@@ -107,6 +117,7 @@ struct TcCfg {
 
 struct TcParams {
     const uint8_t *W;  // the blocks (read by the dequantisers for Q6_K, Q8_0)
+    const float *xinv; // [M] 2^-e_m: undoes the quantiser's power of two of token row m
     int64_t RB;        // bytes per weight row
     uint64_t w_end;    // first byte past the matrix
     int M, N;
@@ -193,6 +204,37 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive 32-bit columns into this warp's 32 TMEM lanes; complete
+// after tmem_wait_st().
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// Weight-row scale: largest exponent E + f_n of a super-block scale that the
+// type's largest |w| keeps below fp16's top (Q4_K |w| < 2^10 * max(|d|,
+// |dmin|), Q6_K < 2^12 |d|, Q8_0 < 2^8 |d|, each bounded by 2^15), and the
+// headroom left when f_n is (re)chosen.
+// The first K step sets f_n from the larger of the row's own scale and 2^-6
+// of the largest scale among the warp's 32 rows (but at most 2^6 above the
+// row's own), so that a row whose first super-block happens to be small
+// does not start far below its later ones, while the row's largest
+// super-block always keeps its weights at or above 2^(TMAX-14)*|q| (fp16
+// normals).
+template <int T>
+struct RowScale {
+    static constexpr int TMAX = T == QMM_Q4_K ? 4 : T == QMM_Q6_K ? 2 : 7;
+    static constexpr int HEAD = 8;
+    static constexpr int NEIGHBOUR = 6;
+    static constexpr int UNSET = 1 << 20;  // no non-zero scale seen yet (the accumulator row is zero)
+};
+
+__device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
 
 // Weight bytes read from global memory into registers (read once per CTA:
 // not kept in L1).
@@ -389,6 +431,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int n = 32 * quarter + lane;  // weight row within the tile (= TMEM lane)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
         const uint32_t a_col = C::A_COL0 + 32 * cp;  // + A_COLS * stage
+        // this row's power of two f_n; both warps of the quarter see the same
+        // scales in the same order, so they hold the same f_n throughout
+        using RS = RowScale<T>;
+        int f = RS::UNSET;
+        // K step kk's largest super-block scale (bits of |v|, 0 if all are
+        // zero): f_n is set or lowered; on a drop, warp cp == 0 rescales the
+        // quarter's accumulator rows after the MMAs of step kk - 1 complete
+        // (the MMA of step kk waits for this warp's arrival).  False when a
+        // wait gave up.
+        auto scale_step = [&](uint32_t ab, int kk) -> bool {
+            bool grow = false;
+            float fac = 1.0f;
+            if (kk == 0) {
+                const int E = ab != 0 ? min(exponent_of(ab), 15) : -1000;
+                const int Ew = __reduce_max_sync(0xffffffffu, E);
+                if (ab != 0) f = RS::TMAX - RS::HEAD - min(max(E, Ew - RS::NEIGHBOUR), E + RS::NEIGHBOUR);
+                return true;
+            }
+            if (ab != 0) {
+                const int E = min(exponent_of(ab), 15);
+                if (f == RS::UNSET) {
+                    f = RS::TMAX - RS::HEAD - E;
+                } else if (E + f > RS::TMAX) {
+                    const int fn = RS::TMAX - RS::HEAD - E;
+                    fac = pow2f(fn - f);
+                    f = fn;
+                    grow = true;
+                }
+            }
+            if (cp != 0 || kk == 0 || !__any_sync(0xffffffffu, grow)) return true;
+            const int kp = kk - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_a_empty + 8 * (kp % A_STAGES), (kp / A_STAGES) & 1, P.status)))
+                return false;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < BT; c += 16) {
+                float v[16];
+                tmem_ld16(lane_base + static_cast<uint32_t>(c), v);
+                uint32_t r[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i] * fac);
+                tmem_st16(lane_base + static_cast<uint32_t>(c), r);
+            }
+            tmem_wait_st();
+            return true;
+        };
+        auto wfac = [&]() { return f == RS::UNSET ? 1.0f : pow2f(f); };
         if constexpr (!C::OWN) {
             for (int kk = 0; kk < P.nsteps; ++kk) {
                 const int r = kk % C::R_STAGES, sa = kk % A_STAGES;
@@ -413,7 +502,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
                     mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
                 }
-                const float d = half_bits_to_float(hdr.x), dmin = half_bits_to_float(hdr.x >> 16);
+                const float d0 = half_bits_to_float(hdr.x), dm0 = half_bits_to_float(hdr.x >> 16);
+                if (!scale_step(max(abs_bits(d0), abs_bits(dm0)), kk)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const float d = d0 * wfac(), dmin = dm0 * wfac();
                 // the quant row: 64 bytes whose 16-byte chunk f sits at f ^ ((n >> 1) & 3)
                 // (TMA 64-byte swizzle), so a quarter warp's loads hit distinct banks
                 const uint8_t *qrow = st + H_BYTES + 64 * n;
@@ -527,7 +621,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // 32(qi&1) + l (nibble qi>>1), high bits (qh byte l >> 2qi) & 3,
                     // scale 8h + 2qi + (l >= 16); w = d*sc * (q - 32).  This warp:
                     // qi = 2cp, 2cp+1.
-                    const float d = __half2float(*reinterpret_cast<const __half *>(row + dl + 208));
+                    const float d0 = __half2float(*reinterpret_cast<const __half *>(row + dl + 208));
+                    if (!scale_step(abs_bits(d0), kk)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const float d = d0 * wfac();
                     const uint32_t scw = row_word(row, dl + 192 + 8 * h + 4 * cp);
                     // ql bytes 64h .. 64h+63 lie in chunks 4h .. 4h+4, qh bytes
                     // 128+32h .. 128+32h+31 in chunks 8+2h .. 10+2h
@@ -573,6 +672,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
                     }
                 } else {
+                    // the K step's four blocks 4h..4h+3 (both warps): their largest d
+                    uint32_t ab = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        ab = max(ab, abs_bits(half_bits_to_float(
+                                         *reinterpret_cast<const unsigned short *>(row + 34 * (4 * h + i)))));
+                    if (!scale_step(ab, kk)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const float wf = wfac();
                     // blocks 4h+2cp, 4h+2cp+1 of the eight: d (fp16), then 32 int8;
                     // w = d * q.  They are the 68 bytes from byte 4E of chunk 4E,
                     // E = 2h + cp (a constant below, so that every word index is one).
@@ -596,8 +706,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int bb = 0; bb < 2; ++bb) {
                             const int ob = 34 * bb;
-                            const __half2 s =
-                                __half2half2(__ushort_as_half(static_cast<unsigned short>(word_at(ob))));
+                            const __half2 s = __float2half2_rn(half_bits_to_float(word_at(ob)) * wf);
 #pragma unroll
                             for (int lw = 0; lw < 8; ++lw) {
                                 const uint32_t q = word_at(ob + 2 + 4 * lw);
@@ -645,21 +754,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (__all_sync(0xffffffffu, ok) && !*abort_flag) {
             tc_fence_after();
             const int ncol = n0 + n;
+            const float rowf = f == RS::UNSET ? 1.0f : pow2f(-f);
 #pragma unroll 1
             for (int cc = cp * (BT / 2); cc < (cp + 1) * (BT / 2); cc += 16) {
                 float v[16];
                 tmem_ld16(lane_base + static_cast<uint32_t>(cc), v);
                 if (ncol < P.N) {
                     float *yc = P.y + static_cast<int64_t>(m0 + cc) * P.N + ncol;
+                    const float *xf = P.xinv + m0 + cc;
                     const int mrem = P.M - (m0 + cc);
                     if (P.atomic) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            if (i < mrem) atomicAdd(yc + static_cast<int64_t>(i) * P.N, v[i]);
+                            if (i < mrem) atomicAdd(yc + static_cast<int64_t>(i) * P.N, v[i] * rowf * __ldg(xf + i));
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            if (i < mrem) yc[static_cast<int64_t>(i) * P.N] = v[i];
+                            if (i < mrem) yc[static_cast<int64_t>(i) * P.N] = v[i] * rowf * __ldg(xf + i);
                     }
                 }
             }
@@ -682,8 +793,8 @@ bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
 }
 
 template <int T, int BT>
-cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, const void *xh, int64_t M, float *y,
-                      cudaStream_t st, int num_sms, int *status) {
+cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, const void *xh, const float *xinv,
+                      int64_t M, float *y, cudaStream_t st, int num_sms, int *status) {
     using C = TcCfg<BT, T>;
     CUtensorMap tx = {}, th = {}, tq = {};
     // tokens: fp16 [M][K], boxes of 64 K x BT rows, 128-byte swizzle
@@ -720,6 +831,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     if (2 * static_cast<int64_t>(nt) * mt <= num_sms && ksteps % (C::OWN ? 4 : 2) == 0) splits = 2;
     TcParams P;
     P.W = static_cast<const uint8_t *>(W);
+    P.xinv = xinv;
     P.RB = (K / qk_weights(T)) * qk_block_bytes(T);
     P.w_end = reinterpret_cast<uint64_t>(W) + static_cast<uint64_t>(N) * P.RB;
     P.M = static_cast<int>(M);
@@ -760,15 +872,15 @@ EncodeTiled tensor_map_encoder() {
 
 bool gemm_tc_supported(int type, int64_t N, int64_t K, int64_t M) { return tc_supported(type, N, K, M); }
 
-cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const void *xh, int64_t M, float *y,
-                           cudaStream_t st, int num_sms, int *status) {
+cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const void *xh, const float *xinv,
+                           int64_t M, float *y, cudaStream_t st, int num_sms, int *status) {
     if (!gemm_tc_supported(type, N, K, M)) return cudaErrorNotSupported;
     EncodeTiled enc = tensor_map_encoder();
     auto run = [&](auto t) {
         constexpr int T = decltype(t)::value;
-        if (M <= 64) return launch_bt<T, 64>(enc, W, N, K, xh, M, y, st, num_sms, status);
-        if (M <= 128) return launch_bt<T, 128>(enc, W, N, K, xh, M, y, st, num_sms, status);
-        return launch_bt<T, 256>(enc, W, N, K, xh, M, y, st, num_sms, status);
+        if (M <= 64) return launch_bt<T, 64>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
+        if (M <= 128) return launch_bt<T, 128>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
+        return launch_bt<T, 256>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
     };
     if (type == QMM_Q6_K) return run(std::integral_constant<int, QMM_Q6_K>{});
     if (type == QMM_Q8_0) return run(std::integral_constant<int, QMM_Q8_0>{});

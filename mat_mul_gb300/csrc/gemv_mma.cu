@@ -24,7 +24,13 @@
 //     a half read the high nibbles as 16x); X_G = the fp32 sum of the group's
 //     fp16 x, subtracted in fp32 before the scaling.
 // Rounding: x to fp16 (as the tcgen05 prefill kernel) and, for Q4_K, dmin*m_j
-// to fp16; every scale is exact and every sum fp32.  The int8 form of the
+// to fp16; every scale is exact and every sum fp32.  Both fp16 operands are
+// scaled by powers of two into fp16's normal range first: x per token row
+// by the quantiser (its fp32 results are multiplied by the row's xinv at the
+// store), -dmin*m_j per row and super-block by 2^g with dmin*2^g in
+// [2^8, 2^9) (and X_j arrives times 2^-5), the min-term MMA's result then
+// multiplied by 2^(5-g) in fp32, so any fp16 dmin and any finite x stay
+// inside the accuracy bound.  The int8 form of the
 // instruction runs at about 158 TOPS on this part, a quarter of the f16
 // rate, too slow for the weight stream once the dots are scaled.
 //
@@ -161,6 +167,7 @@ struct MmParams {
     int halves_r;       // halves % gridDim.x: the first halves_r CTAs take one more
     const uint8_t *xh;  // quantiser output [M][2K + K/8 bytes]: x fp16 | Q4_K block sums
     const uint8_t *xs16;  // Q6_K group sums [K/16][8] fp32
+    const float *xinv;    // [M] 2^-e_m: undoes the quantiser's power of two of token row m
     int nphase;         // K phases
     int nbp;            // super-blocks per phase (a multiple of 8 when nphase > 1)
     int x_ld;           // bytes per token row of the activation window (= 16 mod 128)
@@ -224,9 +231,17 @@ __device__ __forceinline__ uint32_t word_at(const uint8_t *p) {
 
 // Scales of this lane's sub-blocks 2t (low nibbles) and 2t+1 (high nibbles)
 // from a Q4_K header (d, dmin, GGUF six-bit packing): s0, s1 = d*sc * 2^24
-// and d*sc * 2^20 in fp32 (exact), m01 = (-dmin*m_2t, -dmin*m_2t+1) in fp16.
-__device__ __forceinline__ void q4k_lane_scales(uint4 h, int t, float &s0, float &s1, uint32_t &m01) {
-    const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+// and d*sc * 2^20 in fp32 (exact), m01 = (-dmin*m_2t, -dmin*m_2t+1) * 2^g in
+// fp16 with |dmin|*2^g in [2^8, 2^9) (g = 0 when dmin is 0), um = 2^(5-g):
+// the factor that takes the min-term MMA (whose B operand carries 2^-5)
+// back to the scale of the other terms.
+__device__ __forceinline__ void q4k_lane_scales(uint4 h, int t, float &s0, float &s1, uint32_t &m01, float &um) {
+    const float d = half_bits_to_float(h.x);
+    const float dmin0 = half_bits_to_float(h.x >> 16);
+    const uint32_t mb = __float_as_uint(dmin0) & 0x7fffffffu;
+    const int g = mb ? 8 - exponent_of(mb) : 0;
+    const float dmin = dmin0 * pow2f(g);
+    um = pow2f(5 - g);
     uint32_t scw, mnw;  // bytes: scales (mins) of sub-blocks 0..3 or 4..7
     if (t < 2) {
         scw = h.y & 0x3F3F3F3Fu;
@@ -250,16 +265,22 @@ __device__ __forceinline__ void q4k_lane_scales(uint4 h, int t, float &s0, float
 __device__ __forceinline__ void q4k_superblock(uint32_t a_sb, const uint8_t *hdr_a, const uint8_t *hdr_b,
                                                uint32_t x_sb, uint32_t xs_sb, int t, int quad, float (&c)[4],
                                                float (&c2)[4]) {
-    float sa0, sa1, sb0, sb1;
+    float sa0, sa1, sb0, sb1, ua, ub;
     uint32_t ma, mb;
-    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_a), t, sa0, sa1, ma);
-    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_b), t, sb0, sb1, mb);
+    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_a), t, sa0, sa1, ma, ua);
+    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_b), t, sb0, sb1, mb, ub);
     // the min term: k slots 2t, 2t+1 = sub-blocks 2t, 2t+1 (sums hi), slots
-    // 2t+8, 2t+9 = the same sub-blocks (sums lo)
+    // 2t+8, 2t+9 = the same sub-blocks (sums lo); rows g | g+8 scaled back
+    // by their own factors
     {
         uint32_t xhi, xlo;
         ldsm_x2(xs_sb, xhi, xlo);
-        mma_acc(c2, ma, mb, ma, mb, xhi, xlo);
+        float dm[4];
+        mma_new(dm, ma, mb, ma, mb, xhi, xlo);
+        c2[0] = fmaf(ua, dm[0], c2[0]);
+        c2[1] = fmaf(ua, dm[1], c2[1]);
+        c2[2] = fmaf(ub, dm[2], c2[2]);
+        c2[3] = fmaf(ub, dm[3], c2[3]);
     }
     static_for<0, 4>([&](auto cc_) {  // quant bytes 32cc..32cc+31: sub-blocks 2cc, 2cc+1
         constexpr int cc = decltype(cc_)::value;
@@ -535,7 +556,7 @@ __global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
         const int ln = e >> 2, i = e & 3;
         const int64_t row = r0 + GR * gi + (ln >> 2) + 8 * (i >> 1);
         const int tk = 2 * (ln & 3) + (i & 1);
-        if (row < r1 && tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row] = v;
+        if (row < r1 && tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row] = v * __ldg(P.xinv + tk);
     };
 
     bool failed = false;
@@ -732,6 +753,7 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     P.halves_r = static_cast<int>(halves % grid);
     P.xh = static_cast<const uint8_t *>(xh);
     P.xs16 = P.xh + static_cast<int64_t>(M) * (2 * K + K / 8);
+    P.xinv = reinterpret_cast<const float *>(P.xs16 + 2 * K);
     P.nphase = pl.nphase;
     P.nbp = pl.nbp;
     P.x_ld = pl.x_ld;

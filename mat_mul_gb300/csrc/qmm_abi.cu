@@ -180,19 +180,22 @@ void count_launches(int64_t n) { g_launches.fetch_add(n); }
 }  // namespace qk
 
 namespace {
-// The quantiser for the tensor-core decode: fp16 d*q in fragment order and
-// the block and group sums into the workspace ([M][2K + K/8 bytes] |
-// [K/16][8] fp32), launched so that the decode kernels after it (programmatic
-// dependent launch) stream weights while it runs.
+// The quantiser for the tensor-core decode: fp16 d*q*2^e_m in fragment
+// order, the block and group sums and the row factors into the workspace
+// ([M][2K + K/8 bytes] | [K/16][8] fp32 | [8] fp32), launched so that the
+// decode kernels after it (programmatic dependent launch) stream weights
+// while it runs.
 int quantize_for_tensor_cores(int dev, cudaStream_t st, const float *x, int64_t M, int64_t K, const DeviceInfo &di,
                               void **ws) {
     const size_t xh_bytes = static_cast<size_t>(M * (K + K / 16)) * 2;
-    if (int rc = workspace(dev, st, align_up(xh_bytes + static_cast<size_t>(K) * 2, 256), ws)) return rc;
+    const size_t xs_bytes = static_cast<size_t>(K) * 2;  // [K/16][8] fp32
+    if (int rc = workspace(dev, st, align_up(xh_bytes + xs_bytes + 8 * sizeof(float), 256), ws)) return rc;
     qk::QuantOut o = {};
     o.xh = *ws;
     o.xh_ld = K + K / 16;
     o.xh_mma = 1;
     o.xs16 = reinterpret_cast<float *>(static_cast<char *>(*ws) + xh_bytes);
+    o.xinv = reinterpret_cast<float *>(static_cast<char *>(*ws) + xh_bytes + xs_bytes);
     cudaError_t e = qk::launch_quantize(x, M, K, o, st, true, di.num_sms, true);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
     g_launches.fetch_add(1);
@@ -349,18 +352,17 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     if (M > 8 && !g_force_mma_gemm && g_prefill_path.load() == QMM_PREFILL_AUTO &&
         qk::gemm_tc_supported(type, N, K, M)) {
         const size_t xh_bytes = align_up(static_cast<size_t>(M * K) * 2, 256);
-        const size_t d_bytes = align_up(static_cast<size_t>(M * (K / 32)) * 4, 256);
+        const size_t xinv_bytes = align_up(static_cast<size_t>(M) * 4, 256);
         void *ws = nullptr;
-        if (int rc = workspace(dev, st, xh_bytes + d_bytes, &ws)) return rc;
+        if (int rc = workspace(dev, st, xh_bytes + xinv_bytes, &ws)) return rc;
         qk::QuantOut o = {};
         o.xh = ws;
         o.xh_ld = K;
-        o.d = reinterpret_cast<float *>(static_cast<char *>(ws) + xh_bytes);
-        o.d_ld = K / 32;
+        o.xinv = reinterpret_cast<float *>(static_cast<char *>(ws) + xh_bytes);
         e = qk::launch_quantize(x, M, K, o, st, false, di.num_sms);
         if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
         g_launches.fetch_add(1);
-        e = qk::launch_gemm_tc(type, W_blocks, N, K, ws, M, y, st, di.num_sms, di.status);
+        e = qk::launch_gemm_tc(type, W_blocks, N, K, ws, o.xinv, M, y, st, di.num_sms, di.status);
         if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
         g_launches.fetch_add(1);
         return QMM_OK;

@@ -187,6 +187,16 @@ __device__ __forceinline__ void lds_words_u16aligned(uint32_t a, uint32_t (&w)[N
     }
 }
 
+// 2^e as fp32 for -126 <= e <= 127 (exact).
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+// floor(log2 |v|) of a finite non-zero fp32 given by its bits (subnormals
+// count as -127: below every normal value).
+__device__ __forceinline__ int exponent_of(uint32_t bits) {
+    const int be = static_cast<int>((bits >> 23) & 0xFF);
+    return be == 0 ? -127 : be - 127;
+}
+
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits & 0xffffu)));
 }

@@ -17,13 +17,15 @@ namespace qk {
 //   s32 [M][d_ld]   int32 sum per block
 //   s16 [M][s16_ld] int32 sums of the two 16-element halves of every block
 //   dsf [M][d_ld]   fp32 product d * s32 per block
-//   xh  [M][xh_ld]  fp16 of the dequantised activation d * q: plain layout,
-//                   or with xh_mma != 0 the layout of the tensor-core decode
-//                   kernel (gemv_mma.cu): element l of block b at half
+//   xh  [M][xh_ld]  fp16 of the dequantised activation times a power of
+//                   two per row, d * q * 2^e_m (xinv[m] = 2^-e_m): plain
+//                   layout, or with xh_mma != 0 the layout of the tensor-core
+//                   decode kernel (gemv_mma.cu): element l of block b at half
 //                   32b + ((l>>4)*2 + (l&1))*8 + ((l>>2)&3)*2 + ((l>>1)&1),
 //                   then after the K halves the block sums of the fp16
-//                   values as hi + lo, per super-block 8 hi then 8 lo
-//                   (xh_ld >= K + K/16)
+//                   values times 2^-5 as hi + lo, per super-block 8 hi then
+//                   8 lo (xh_ld >= K + K/16).  When xh is set only the fp16
+//                   outputs (xh, xs16, xinv) are written.
 struct QuantOut {
     int8_t *q;
     int64_t q_ld;
@@ -37,6 +39,7 @@ struct QuantOut {
     int64_t xh_ld;
     int xh_mma;
     float *xs16;  // with xh_mma: the sums of the fp16 values per 16 elements, [K/16][8], tokens >= M zero
+    float *xinv;  // with xh: [M] the factor 2^-e_m that undoes row m's power of two
 };
 
 // trigger_dependents: let the next kernel (launched with programmatic
@@ -79,8 +82,9 @@ void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t 
 // Decode for 2 <= M <= 8 on the tensor cores (gemv_mma.cu): Q4_K or Q6_K,
 // sixteen weight rows per mma.sync.m16n8k16 (fp16 operands, fp32
 // accumulation).  xh: the quantiser's output with xh_mma, [M][2K + K/8
-// bytes] (16-byte aligned), then for Q6_K the group sums [K/16][8] fp32
-// (xs16); the kernel copies one K window of it at a time into shared memory.
+// bytes] (16-byte aligned), then the group sums [K/16][8] fp32 (xs16), then
+// the row factors xinv [8] fp32; the kernel copies one K window of it at a
+// time into shared memory.
 // Launched with programmatic dependent launch right after that quantiser
 // (launched with trigger_dependents): the kernel streams weights before it
 // waits, and reads xh after.
@@ -89,11 +93,12 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
                             cudaStream_t st, int num_sms, int max_smem, int *status);
 
 // Prefill GEMM on tcgen05 (gemm_tc.cu): Q4_K, Q6_K or Q8_0 weights with K a
-// multiple of 256, fp16 activations xh [M][K] (d*q from the quantiser).  Returns cudaErrorNotSupported for
-// shapes it does not take.
+// multiple of 256, fp16 activations xh [M][K] (d*q*2^e_m from the
+// quantiser) and the row factors xinv [M] = 2^-e_m.  Returns
+// cudaErrorNotSupported for shapes it does not take.
 bool gemm_tc_supported(int type, int64_t N, int64_t K, int64_t M);
-cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const void *xh, int64_t M,
-                           float *y, cudaStream_t st, int num_sms, int *status);
+cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const void *xh, const float *xinv,
+                           int64_t M, float *y, cudaStream_t st, int num_sms, int *status);
 
 // Prefill GEMM on mma.sync (gemm_mma.cu): q [M][K], d and s32 [M][xd_ld].
 cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,

@@ -128,6 +128,34 @@ def weights(qtype: int, N: int, K: int, seed: int) -> np.ndarray:
     raise ValueError(qtype)
 
 
+# Byte offsets of the fp16 scale fields inside each block: d, and dmin where
+# the format has one (Q5_K's fields sit where Q4_K's do).
+D_FIELD = {Q8_0: 0, Q4_K: 0, Q6_K: 208, Q5_K: 0, Q3_K: 108, Q2_K: 80}
+DMIN_FIELD = {Q4_K: 2, Q5_K: 2, Q2_K: 82}
+
+
+def with_scale_fields(qtype: int, W: np.ndarray, d_bits, dmin_bits=None) -> np.ndarray:
+    """A copy of the packed blocks W with every block's fp16 d (and dmin, for
+    the formats that have one) replaced by the given bit patterns: a scalar
+    or one value per block."""
+    bb = BLOCK_BYTES[qtype]
+    out = np.array(W, dtype=np.uint8).reshape(-1, bb).copy()
+    n = out.shape[0]
+    pos = D_FIELD[qtype]
+    out[:, pos:pos + 2] = np.broadcast_to(np.asarray(d_bits, np.uint16), (n,)).astype("<u2").view(
+        np.uint8).reshape(n, 2)
+    if dmin_bits is not None and qtype in DMIN_FIELD:
+        pos = DMIN_FIELD[qtype]
+        out[:, pos:pos + 2] = np.broadcast_to(np.asarray(dmin_bits, np.uint16), (n,)).astype("<u2").view(
+            np.uint8).reshape(n, 2)
+    return out.reshape(-1)
+
+
+def loguniform_f16_bits(rng, n: int, lo: float, hi: float) -> np.ndarray:
+    """n fp16 bit patterns of values log-uniform in [lo, hi] (rounded to fp16)."""
+    return _f16_bits(np.exp(rng.uniform(np.log(lo), np.log(hi), size=n)))
+
+
 def activations(M: int, K: int, seed: int, outlier_frac: float = 0.0,
                 outlier_scale: float = 20.0) -> np.ndarray:
     """x f32 ~ N(0, 1); with outlier_frac > 0, a Bernoulli mask scales entries."""
