@@ -330,32 +330,41 @@ def run_ours(args):
 
     mats = decode_workload()
     step_bytes = sum(m["bytes"] for m in mats)
-    for m in mats:
-        W = synth.config_weights(m["cfg"], m["idx"])
-        m["W"] = torch.from_numpy(W).to(dev)
-        m["x_host"] = torch.from_numpy(synth.config_activations(m["cfg"], 1, m["K"])).pin_memory()
-        m["x"] = m["x_host"].to(dev)
-        m["y"] = torch.empty((1, m["N"]), dtype=torch.float32, device=dev)
-        m["y_host"] = torch.empty((1, m["N"]), dtype=torch.float32).pin_memory()
-
     calls = make_calls(mats, STEP_CALLS)
+    # every call's x is a slice of one device buffer and every y a slice of
+    # another, so that the end-to-end step moves its inputs in one
+    # host-to-device copy and its outputs in one device-to-host copy (a
+    # group reads one x: its members' synthetic activations coincide)
+    x_len = sum(call[0]["K"] for call in calls)
+    y_len = sum(m["N"] for m in mats)
+    x_host_all = torch.empty(x_len, dtype=torch.float32).pin_memory()
+    y_host_all = torch.empty(y_len, dtype=torch.float32).pin_memory()
+    x_dev_all = torch.empty(x_len, dtype=torch.float32, device=dev)
+    y_dev_all = torch.empty(y_len, dtype=torch.float32, device=dev)
+    xo = yo = 0
     for call in calls:
-        # a group reads one x (its members' synthetic activations coincide:
-        # same config and K); the first member's buffer is the shared one
+        xv = torch.from_numpy(synth.config_activations(call[0]["cfg"], 1, call[0]["K"])).reshape(-1)
         for m in call[1:]:
-            assert torch.equal(m["x_host"], call[0]["x_host"])
-            m["x"], m["x_host"] = call[0]["x"], call[0]["x_host"]
+            assert torch.equal(torch.from_numpy(synth.config_activations(m["cfg"], 1, m["K"])).reshape(-1), xv)
+        x_host_all[xo:xo + xv.numel()] = xv
+        for m in call:
+            m["x"] = x_dev_all[xo:xo + xv.numel()].view(1, -1)
+        xo += xv.numel()
+    x_dev_all.copy_(x_host_all)
+    for m in mats:
+        m["W"] = torch.from_numpy(synth.config_weights(m["cfg"], m["idx"])).to(dev)
+        m["y"] = y_dev_all[yo:yo + m["N"]].view(1, -1)
+        yo += m["N"]
 
     def step():
         for call in calls:
             run_call(q, call, stream)
 
     def step_e2e():
+        x_dev_all.copy_(x_host_all, non_blocking=True)
         for call in calls:
-            call[0]["x"].copy_(call[0]["x_host"], non_blocking=True)
             run_call(q, call, stream)
-            for m in call:
-                m["y_host"].copy_(m["y"], non_blocking=True)
+        y_host_all.copy_(y_dev_all, non_blocking=True)
 
     def capture(fn):
         with torch.cuda.stream(stream):
@@ -409,13 +418,13 @@ def run_ours(args):
     # ---- end to end: x copied in and y copied out every call
     g_e2e = capture(step_e2e)
     ms_e2e = timed(g_e2e, args.steps, args.warmup)
-    h2d = sum(call[0]["K"] * 4 for call in calls)
-    d2h = sum(m["N"] * 4 for m in mats)
+    h2d = x_host_all.numel() * 4
+    d2h = y_host_all.numel() * 4
     e2e_value = job_throughput(world, step_bytes, ms_e2e)
     del g_e2e, g_step
 
     detail = []
-    groups = layer = layer_m = None
+    groups = layer = layer_m = gate_up = None
     roof = None
     gemm = None
     cpu = None
@@ -479,6 +488,34 @@ def run_ours(args):
                     "frac_hbm": round(gbs / peaks["hbm"], 4)}
 
         groups = [rotating([c]) for c in make_calls(mats, STEP_CALLS) if len(c) > 1]
+
+        # ---- the gated MLP product h = silu(gate x) * (up x) of the
+        # Qwen3-14B layer in one launch (qmm_gate_up), over rotating copies
+        by_name = {m["name"]: m for m in mats}
+        mg, mu = by_name["cfg3:gate"], by_name["cfg3:up"]
+        gu_bytes = mg["bytes"] + mu["bytes"]
+        ncopy = min(64, max(2, -(-4 * L2_BYTES // gu_bytes)))
+        cg = [mg["W"]] + [mg["W"].clone() for _ in range(ncopy - 1)]
+        cu = [mu["W"]] + [mu["W"].clone() for _ in range(ncopy - 1)]
+        h_gu = torch.empty((1, mg["N"]), dtype=torch.float32, device=dev)
+        inner = max(ncopy, 8)
+
+        def gu_call():
+            for i in range(inner):
+                q.qmm_gate_up(mg["qtype"], cg[i % ncopy], mu["qtype"], cu[i % ncopy], mg["N"], mg["K"], mg["x"],
+                              h=h_gu, stream=stream)
+
+        before = q.qmm_launch_count()
+        q.qmm_gate_up(mg["qtype"], mg["W"], mu["qtype"], mu["W"], mg["N"], mg["K"], mg["x"], h=h_gu, stream=stream)
+        gu_launches = q.qmm_launch_count() - before
+        g = capture(gu_call)
+        t_ms = timed(g, 5, 2) / inner
+        del g, cg, cu
+        torch.cuda.empty_cache()
+        gbs = gu_bytes / (t_ms * 1e-3) / 1e9
+        gate_up = {"what": "qmm_gate_up: h = silu(gate x) * (up x), Qwen3-14B 5120->17408 Q4_K pair, M=1",
+                   "launches": gu_launches, "MB": round(gu_bytes / 1e6, 3), "us": round(t_ms * 1e3, 2),
+                   "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4)}
         layer = rotating(make_calls(mats, LAYER_CALLS))
         layer["M"] = 1
 
@@ -513,16 +550,22 @@ def run_ours(args):
                               synth.weights(synth.Q8_0, 14336, 4096, seed=4100),
                               synth.config_activations(4, 512, 4096)))
         for name, qtype, K, N, w_np, x_np in prefill_cases:
+            # rotating weight copies (>= 4x L2), so every call reads its
+            # weights from HBM as a model's layers would
             W = torch.from_numpy(w_np).to(dev)
+            ncopy = max(2, -(-4 * L2_BYTES // W.numel()))
+            copies = [W] + [W.clone() for _ in range(ncopy - 1)]
             x = torch.from_numpy(x_np).to(dev)
             y = torch.empty((512, N), dtype=torch.float32, device=dev)
+            inner = max(ncopy, 8)
 
-            def gcall(W=W, x=x, y=y, qtype=qtype, K=K, N=N):
-                for _ in range(5):
-                    q.qmm(qtype, W, N, K, x, y=y, stream=stream)
+            def gcall(copies=copies, x=x, y=y, qtype=qtype, K=K, N=N, inner=inner):
+                for i in range(inner):
+                    q.qmm(qtype, copies[i % len(copies)], N, K, x, y=y, stream=stream)
 
             g = capture(gcall)
-            t_ms = timed(g, 4, 1) / 5
+            t_ms = timed(g, 3, 1) / inner
+            del copies
             tops = 2 * 512 * N * K / (t_ms * 1e-3) / 1e12
             gemm.append({"matrix": name, "type": ["Q8_0", "Q4_K", "Q6_K"][qtype], "M": 512, "K": K, "N": N,
                          "us": round(t_ms * 1e3, 1), "TOPS": round(tops, 1)})
@@ -596,9 +639,11 @@ def run_ours(args):
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
-                    "note": "weights resident (model state); x in and y out every call"},
+                    "note": "weights resident (model state); every step: all x in (one pinned H2D copy), "
+                            "all y out (one D2H copy)"},
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks, "per_matrix": detail, "groups": groups, "qwen3_14b_layer": layer,
+            "clocks": clocks, "per_matrix": detail, "groups": groups, "gate_up_fused": gate_up,
+            "qwen3_14b_layer": layer,
             "qwen3_14b_layer_M": layer_m,
             "prefill_gemm": gemm,
             "kv_value_cache": kv_line,

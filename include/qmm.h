@@ -207,6 +207,31 @@ QMM_API int qmm_noalloc(int type, const void *W_blocks, int64_t N, int64_t K, co
 QMM_API int qmm_t(int type, const void *W_blocks, int64_t H, int64_t N, int64_t K, const float *x, int64_t M,
                   float *y, void *stream);
 
+/*
+ * qmm_gate_up -- the gated MLP product of one step:
+ *   h[M,N] = silu(W_gate . x^T) * (W_up . x^T),  silu(v) = v / (1 + e^-v),
+ * the two products as qmm() (the same quantised x) and the SiLU between
+ * them; the infr landing page runs an expert's gate and up as one dispatch
+ * ("why > Per-op device profiling": expert_gateup) and its Qwen3 / Llama
+ * MLPs apply the SiLU there.
+ *   type_gate, W_gate, type_up, W_up : the two matrices, N x K each, as in
+ *              qmm() (the types may differ; K a multiple of both QK).
+ *   N, K, x, M, stream : as in qmm().
+ *   h        : device, M*N floats, overwritten.
+ * Launches: M <= 2 with one type for both on the block-per-lane decode
+ * kernel is ONE launch (each CTA streams the same rows of both matrices and
+ * writes h); on the tensor-core decode (Q4_K / Q6_K, 3 <= M <= 8) x is
+ * quantised once and the up launch applies the SiLU to the gate launch's
+ * result (three launches); every other case runs the two products, then an
+ * elementwise kernel.  The last two use a per-(device, stream) buffer of the
+ * library for g (and u), grown on demand like qmm()'s workspace.
+ * Accuracy: with e = 2e-3 * sum_k |w_k xhat_k| + 1e-5 the bound of each
+ * product, |h - h_exact| <= 1.1 |u| e_gate + |silu(g)| e_up + 1.1 e_gate e_up
+ * (|silu'| < 1.1).  Errors as qmm().
+ */
+QMM_API int qmm_gate_up(int type_gate, const void *W_gate, int type_up, const void *W_up, int64_t N, int64_t K,
+                        const float *x, int64_t M, float *h, void *stream);
+
 /* Name of a status code. */
 QMM_API const char *qmm_strerror(int status);
 
@@ -264,6 +289,21 @@ QMM_API int qmm_set_decode_path(int path);
 #define QMM_PREFILL_AUTO 0
 #define QMM_PREFILL_INT8 1
 QMM_API int qmm_set_prefill_path(int path);
+
+/*
+ * qmm_inject_stall -- test hook for failure detection (no counterpart in
+ * the pages).  The next `launches` launches of the weight-streaming product
+ * kernels (block-per-lane and tensor-core decode, tcgen05 prefill) are
+ * launched with their first CTA's weight producer stopping after its first
+ * stage, so a consumer's bounded wait (about 2^31 SM cycles, one second at
+ * full clock) expires: the kernel records the timeout in the device status
+ * word, stops, waits for the copies it did issue, releases its tensor memory
+ * and returns.  That call returns QMM_OK with y incomplete, and the next
+ * qmm_device_status() reports QMM_ETIMEOUT; later calls run normally.  No
+ * fault, trap or unbounded wait is involved.  launches >= 0 (0 cancels);
+ * returns the previous pending count, or QMM_EINVAL_SHAPE.  Needs no GPU.
+ */
+QMM_API int qmm_inject_stall(int launches);
 
 #ifdef __cplusplus
 }

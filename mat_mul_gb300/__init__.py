@@ -7,6 +7,7 @@ library is missing or no GPU is present the calls raise.
     import mat_mul_gb300 as q
     y = q.qmm(q.Q4_K, W_blocks, N, K, x)          # x: cuda f32 [M, K] -> [M, N]
     ys = q.qmm_group([(q.Q4_K, Wg, N), (q.Q4_K, Wu, N)], K, x)   # one launch, shared x
+    h = q.qmm_gate_up(q.Q4_K, Wg, q.Q4_K, Wu, N, K, x)           # silu(Wg x) * (Wu x)
     o = q.qmm_t(q.Q8_0, V_cache, H, T, D, p)      # p: [H, M, T] -> [H, M, D]
     w = q.qmm_dequant(q.Q6_K, blocks, n_elems)    # cuda f32 [n_elems]
 """
@@ -59,6 +60,7 @@ def load():
     L.qmm_quantize_act.argtypes = [P, I64, I64, P, P, P, P]
     L.qmm_group.argtypes = [I, P, P, P, I64, P, I64, P, P]
     L.qmm_t.argtypes = [I, P, I64, I64, I64, P, I64, P, P]
+    L.qmm_gate_up.argtypes = [I, P, I, P, I64, I64, P, I64, P, P]
     L.qmm_strerror.argtypes = [I]
     L.qmm_strerror.restype = ctypes.c_char_p
     L.qmm_last_error.restype = ctypes.c_char_p
@@ -68,8 +70,10 @@ def load():
     L.qmm_set_decode_path.restype = I
     L.qmm_set_prefill_path.argtypes = [I]
     L.qmm_set_prefill_path.restype = I
+    L.qmm_inject_stall.argtypes = [I]
+    L.qmm_inject_stall.restype = I
     for f in ("qmm_dequant", "qmm", "qmm_noalloc", "qmm_quantize_act", "qmm_device_status",
-              "qmm_release", "qmm_group"):
+              "qmm_release", "qmm_group", "qmm_t", "qmm_gate_up"):
         getattr(L, f).restype = I
     _lib = L
     return L
@@ -173,6 +177,25 @@ def qmm_group(items, K: int, x, stream=None):
     return ys
 
 
+def qmm_gate_up(type_gate: int, W_gate, type_up: int, W_up, N: int, K: int, x, h=None, stream=None):
+    """h[M,N] = silu(W_gate . x^T) * (W_up . x^T) for device x [M, K] (or
+    [K]); one launch for M <= 2 when both matrices have one type."""
+    import torch
+    _require_cuda(W_gate, W_up, x, h)
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 tensor")
+    M = 1 if x.dim() == 1 else x.shape[0]
+    if x.shape[-1] != K:
+        raise ValueError(f"x has {x.shape[-1]} columns, K = {K}")
+    if h is None:
+        h = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    elif h.dtype != torch.float32 or not h.is_contiguous() or h.device != x.device or h.numel() < M * N:
+        raise ValueError(f"h must be a contiguous float32 tensor on {x.device} with at least M*N = {M * N} elements")
+    _check(load().qmm_gate_up(int(type_gate), _ptr(W_gate), int(type_up), _ptr(W_up), int(N), int(K), _ptr(x),
+                              int(M), _ptr(h), _stream_handle(stream)))
+    return h
+
+
 def qmm_noalloc(qtype: int, W, N: int, K: int, x, y, stream=None):
     """Same product as qmm() without any device allocation by the library,
     for callers that keep all device memory in their own fixed pool or must
@@ -238,6 +261,17 @@ PREFILL_AUTO, PREFILL_INT8 = 0, 1
 def set_prefill_path(path: int) -> int:
     """Select the prefill kernel for every later call; returns the previous path."""
     rc = int(load().qmm_set_prefill_path(int(path)))
+    if rc < 0:
+        raise QmmError(rc, load().qmm_last_error().decode())
+    return rc
+
+
+def inject_stall(launches: int) -> int:
+    """Failure-detection test hook: the next `launches` weight-streaming
+    launches stop their first CTA's copies after one stage, so a bounded wait
+    expires and qmm_device_status() reports QMM_ETIMEOUT.  Returns the
+    previous pending count."""
+    rc = int(load().qmm_inject_stall(int(launches)))
     if rc < 0:
         raise QmmError(rc, load().qmm_last_error().decode())
     return rc

@@ -125,6 +125,7 @@ struct TcParams {
     float *y;
     int atomic;   // split K: add into y instead of storing
     int *status;
+    int stop_step;  // the first CTA's token producer issues no step from this one on (failure test hook)
 };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -353,8 +354,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == W_XLOAD) {
         // ------------------------------------------ token tile producer
         if (lane == 0) {
+            // steps from `stop` on are never issued (only with the test hook:
+            // the MMA issuer's bounded wait on step `stop` then expires)
+            const int stop = (blockIdx.x | blockIdx.y | blockIdx.z) == 0 ? P.stop_step : NO_STOP;
             int issued = 0;
-            for (int kk = 0; kk < P.nsteps; ++kk) {
+            for (int kk = 0; kk < P.nsteps && kk < stop; ++kk) {
                 const int s = kk % C::X_STAGES;
                 if (kk >= C::X_STAGES &&
                     (*abort_flag || !mbar_wait(bar_x_empty + 8 * s, ((kk / C::X_STAGES) - 1) & 1, P.status))) {
@@ -839,6 +843,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     P.y = y;
     P.atomic = splits > 1;
     P.status = status;
+    P.stop_step = inject_stop_stage();
     if (splits > 1) {
         cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(M * N) * sizeof(float), st);
         if (e != cudaSuccess) return e;

@@ -168,6 +168,7 @@ struct MmParams {
     const uint8_t *xh;  // quantiser output [M][2K + K/8 bytes]: x fp16 | Q4_K block sums
     const uint8_t *xs16;  // Q6_K group sums [K/16][8] fp32
     const float *xinv;    // [M] 2^-e_m: undoes the quantiser's power of two of token row m
+    const float *gate;    // null, or g [M][N] from the preceding launch: y = silu(g) * (this product)
     int nphase;         // K phases
     int nbp;            // super-blocks per phase (a multiple of 8 when nphase > 1)
     int x_ld;           // bytes per token row of the activation window (= 16 mod 128)
@@ -177,6 +178,7 @@ struct MmParams {
     int row_pitch;      // stage bytes per row
     int off_x, off_xs, off_table, off_ring;
     int *status;
+    int stop_stage;  // the first CTA's producer issues no stage from this one on (failure test hook)
 };
 
 // 2-D tensor copy global -> shared completing on `bar`, with an L2 policy.
@@ -468,6 +470,10 @@ __global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
         // ---- producer: fills the ring in stage order --------------------
         StageCursor c;
         cursor_phase<CHS>(P, c, 0);
+        // stages from `stop` on are never issued (only with the test hook:
+        // the consumers' bounded wait on stage `stop` then expires)
+        const int stop = cta == 0 ? P.stop_stage : NO_STOP;
+        int issued = 0;
         for (int s = 0; s < total; ++s, cursor_next<CHS>(P, c, ng)) {
             const int slot = s % P.NS;
             if (s >= P.NS) {
@@ -479,6 +485,8 @@ __global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
                     break;
                 }
             }
+            if (s >= stop) break;
+            issued = s + 1;
             const int sb0 = c.sb + c.kc * CHS, nsb = min(CHS, c.sb + c.nsb - sb0);
             const int64_t row0 = r0 + GR * c.gi;
             const uint32_t bar = full0 + 8u * slot;
@@ -525,9 +533,10 @@ __global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
             pdl_wait();
             if (lane == 0) load_x(0);
         }
-        // no copy may still be in flight when the CTA exits
+        // no copy may still be in flight when the CTA exits (stages that were
+        // never issued are not waited for)
         if (lane == 0)
-            for (int s = max(0, total - P.NS); s < total; ++s)
+            for (int s = max(0, issued - P.NS); s < issued; ++s)
                 mbar_wait(full0 + 8u * (s % P.NS), static_cast<uint32_t>((s / P.NS) & 1), P.status);
         return;
     }
@@ -556,7 +565,16 @@ __global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
         const int ln = e >> 2, i = e & 3;
         const int64_t row = r0 + GR * gi + (ln >> 2) + 8 * (i >> 1);
         const int tk = 2 * (ln & 3) + (i & 1);
-        if (row < r1 && tk < P.M) P.y[static_cast<int64_t>(tk) * P.N + row] = v * __ldg(P.xinv + tk);
+        if (row < r1 && tk < P.M) {
+            float val = v * __ldg(P.xinv + tk);
+            if (P.gate) {
+                // gate.x, written by the launch before this one (complete:
+                // the consumers passed griddepcontrol.wait)
+                const float g = P.gate[static_cast<int64_t>(tk) * P.N + row];
+                val = g / (1.0f + expf(-g)) * val;
+            }
+            P.y[static_cast<int64_t>(tk) * P.N + row] = val;
+        }
     };
 
     bool failed = false;
@@ -729,7 +747,7 @@ bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_
 }
 
 cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
-                            cudaStream_t st, int num_sms, int max_smem, int *status) {
+                            cudaStream_t st, int num_sms, int max_smem, int *status, const float *gate) {
     if (!type_ok(type, M, K, N)) return cudaErrorNotSupported;
     int64_t grid = 0;
     const int64_t mg = max_groups_of(N, num_sms, &grid);
@@ -754,6 +772,7 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     P.xh = static_cast<const uint8_t *>(xh);
     P.xs16 = P.xh + static_cast<int64_t>(M) * (2 * K + K / 8);
     P.xinv = reinterpret_cast<const float *>(P.xs16 + 2 * K);
+    P.gate = gate;
     P.nphase = pl.nphase;
     P.nbp = pl.nbp;
     P.x_ld = pl.x_ld;
@@ -766,6 +785,7 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     P.off_table = pl.off_table;
     P.off_ring = pl.off_ring;
     P.status = status;
+    P.stop_stage = inject_stop_stage();
     CUtensorMap tmW = {};
     if (type == QMM_Q4_K) {
         // the weights as 8-byte elements [N][18 * nb]: boxes of 8 super-blocks

@@ -57,6 +57,12 @@ struct SbParams {
     float *y;
     int off_edge, off_xq, off_meta, off_ring;
     int *status;
+    int stop_stage;  // the first CTA's warps issue no stage from this one on (failure test hook)
+    // gate+up launch: W is the gate matrix, W2 the up matrix (same type and
+    // shape), y receives h = silu(gate.x) * (up.x); off_tab is the
+    // shared-memory table of the CTA's row results [2][rows][MT]
+    const uint8_t *W2;
+    int off_tab;
 };
 
 __device__ __forceinline__ uint4 ld16(const uint8_t *sm, int off) {
@@ -394,18 +400,27 @@ __device__ __forceinline__ void quantize_to_smem(const SbParams &P, uint8_t *sme
     else quantize_tpb<T, 2, 4>(P, smem, after_loads);
 }
 
-// The work of CTA `cta` of one matrix (its share of the rows).
-template <int T, int MT>
+// The work of CTA `cta` of one matrix (its share of the rows).  With GATEUP
+// the CTA takes the same rows of two matrices, gate (W) and up (W2): warps
+// 0..5 stream the gate rows, warps 6..11 the up rows, both from the one
+// quantised x; the row results meet in a shared-memory table and the CTA
+// writes h = silu(gate) * up.
+template <int T, int MT, bool GATEUP = false>
 __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int BB = Fmt<T>::BB;
+    constexpr int NW = GATEUP ? NWARP / 2 : NWARP;  // warps per matrix
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = GATEUP ? warp / NW : 0;  // the matrix of this warp: 0 = W, 1 = W2
+    const int wi = warp - wg * NW;          // the warp's index among its matrix's warps
 
     const int64_t r0 = P.rows_q * cta + min(cta, P.rows_r);
     const int64_t r1 = r0 + P.rows_q + (cta < P.rows_r ? 1 : 0);
-    const int U = static_cast<int>(r1 - r0) * P.nb;  // blocks of this CTA
-    const int uw0 = static_cast<int>((static_cast<int64_t>(U) * warp) / NWARP);
-    const int uw1 = static_cast<int>((static_cast<int64_t>(U) * (warp + 1)) / NWARP);
+    const int rows = static_cast<int>(r1 - r0);
+    const int U = rows * P.nb;  // blocks of this CTA (of each matrix)
+    const int uw0 = static_cast<int>((static_cast<int64_t>(U) * wi) / NW);
+    const int uw1 = static_cast<int>((static_cast<int64_t>(U) * (wi + 1)) / NW);
+    float *tab = reinterpret_cast<float *>(smem + P.off_tab);  // GATEUP: [2][rows][MT]
     const int nst = (uw1 - uw0 + SU - 1) / SU;
 
     const uint32_t bar0 = smem_u32(smem);
@@ -425,13 +440,17 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
 
     // weights of this CTA, relative to its first byte rounded down to 16
     const int64_t cta_byte = r0 * P.RB;
-    const uint8_t *Wc = P.W + (cta_byte & ~int64_t(15));
+    const uint8_t *Wc = (wg ? P.W2 : P.W) + (cta_byte & ~int64_t(15));
     const int cta_off = static_cast<int>(cta_byte & 15);
     const int64_t avail = P.total_bytes - (cta_byte & ~int64_t(15));
     const int ring = P.off_ring + warp * P.NSW * P.slot_bytes;
 
+    // stages from `stop` on are never issued (only with the test hook: the
+    // consumer's bounded wait on stage `stop` then expires)
+    const int stop = cta == 0 ? P.stop_stage : NO_STOP;
     // issue stage t of this warp into `slot` (= t % NSW; lane 0 only)
     auto issue = [&](int t, int slot, uint64_t pol) {
+        if (t >= stop) return;
         const int u0 = uw0 + SU * t, u1 = min(u0 + SU, uw1);
         const int a = cta_off + u0 * BB, b = cta_off + u1 * BB;
         const int a16 = a & ~15;
@@ -549,9 +568,12 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
         if (head && !(cont && row == row_last)) {
             if (row_start < uw0 || row_end > uw1) {
                 const int e = 2 * warp + (row_start < uw0 ? 0 : 1);
-                edge_row[e] = row;
+                edge_row[e] = row + (wg << 30);  // (matrix, row): rows < 2^30
 #pragma unroll
                 for (int m = 0; m < MT; ++m) edge_val[e * 8 + m] = v[m];
+            } else if (GATEUP) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) tab[(wg * rows + row) * MT + m] = v[m];
             } else {
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
@@ -565,7 +587,7 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
     }
     // no bulk copy may still be in flight when the CTA exits
     if (lane == 0)
-        for (int t = consumed; t < issued; ++t)
+        for (int t = consumed; t < min(issued, stop); ++t)
             mbar_wait(my_bar + 8u * (t % P.NSW), static_cast<uint32_t>((t / P.NSW) & 1), P.status);
     __syncthreads();
     if (warp == 0) {
@@ -590,9 +612,21 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
             }
         }
         if (r >= 0 && (__ffs(same) - 1) == lane) {
+            const int rw = r & ((1 << 30) - 1), mw = r >> 30;
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < P.M) P.y[static_cast<int64_t>(m) * P.N + r0 + r] = acc[m];
+            for (int m = 0; m < MT; ++m) {
+                if (GATEUP) tab[(mw * rows + rw) * MT + m] = acc[m];
+                else if (m < P.M) P.y[static_cast<int64_t>(m) * P.N + r0 + rw] = acc[m];
+            }
+        }
+    }
+    if constexpr (GATEUP) {
+        // h = silu(g) * u for every row of the CTA, silu(g) = g / (1 + e^-g)
+        __syncthreads();
+        for (int i = threadIdx.x; i < rows * P.M; i += NTHREADS) {
+            const int row = i / P.M, m = i - row * P.M;
+            const float g = tab[row * MT + m], u = tab[(rows + row) * MT + m];
+            P.y[static_cast<int64_t>(m) * P.N + r0 + row] = g / (1.0f + expf(-g)) * u;
         }
     }
 }
@@ -600,6 +634,12 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
 template <int T, int MT>
 __global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_kernel(const __grid_constant__ SbParams P) {
     sb_body<T, MT>(P, static_cast<int>(blockIdx.x));
+}
+
+// gate and up (same type and shape) in one launch, writing h = silu(g) * u
+template <int T, int MT>
+__global__ void __launch_bounds__(NTHREADS, 1) gemv_sb_gateup_kernel(const __grid_constant__ SbParams P) {
+    sb_body<T, MT, true>(P, static_cast<int>(blockIdx.x));
 }
 
 // Several matrices that share K and x in one launch: CTAs
@@ -660,6 +700,8 @@ bool plan_sb(int type, int M, int64_t K, int max_smem, SbParams &P, int &smem) {
 template <int T, int MT>
 cudaError_t launch_t(const SbParams &P, int grid, int smem, cudaStream_t st) {
     auto kfn = gemv_sb_kernel<T, MT>;
+    if constexpr (MT <= 2)
+        if (P.W2) kfn = gemv_sb_gateup_kernel<T, MT>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -718,6 +760,7 @@ void fill(SbParams &P, int type, const void *W, int64_t N, int64_t K, const floa
     P.x_vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0 ? 1 : 0;
     P.y = y;
     P.status = status;
+    P.stop_stage = NO_STOP;
     P.rows_q = N / g;
     P.rows_r = static_cast<int>(N % g);
     // Row of block u by multiply-high: with M = floor(2^32/nb) + 1 and
@@ -763,10 +806,40 @@ cudaError_t launch_gemv_sb(int type, const void *W, int64_t N, int64_t K, const 
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     const int g = static_cast<int>(grid);
     fill(P, type, W, N, K, x, M, y, status, g);
+    P.stop_stage = inject_stop_stage();
     switch (type) {
     case QMM_Q8_0: return launch_m<QMM_Q8_0>(P, mt_of(M), g, smem, st);
     case QMM_Q4_K: return launch_m<QMM_Q4_K>(P, mt_of(M), g, smem, st);
     default: return launch_m<QMM_Q6_K>(P, mt_of(M), g, smem, st);
+    }
+}
+
+cudaError_t launch_gemv_sb_gateup(int type, const void *Wg, const void *Wu, int64_t N, int64_t K, const float *x,
+                                  int M, float *h, cudaStream_t st, int num_sms, int max_smem, int *status) {
+    if (M > 2) return cudaErrorNotSupported;  // the table holds MT <= 2 values per row
+    int64_t grid = num_sms;
+    const int64_t need = min_ctas(N, static_cast<int>(K / block_weights(type)) * block_bytes(type));
+    if (grid < need) grid = need;
+    if (N < grid) grid = N;
+    if (grid < 1) grid = 1;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    const int g = static_cast<int>(grid);
+    const int MT = mt_of(M);
+    // the row table after the rings: 2 matrices x (rows of the largest CTA) x MT floats
+    const int64_t tab_bytes = align64(2 * (N / g + 1) * MT * 4, 128);
+    if (tab_bytes > max_smem / 4) return cudaErrorNotSupported;
+    SbParams P = {};
+    int smem = 0;
+    if (!plan_sb(type, M, K, max_smem - static_cast<int>(tab_bytes), P, smem)) return cudaErrorNotSupported;
+    fill(P, type, Wg, N, K, x, M, h, status, g);
+    P.W2 = static_cast<const uint8_t *>(Wu);
+    P.off_tab = smem;
+    smem += static_cast<int>(tab_bytes);
+    P.stop_stage = inject_stop_stage();
+    switch (type) {
+    case QMM_Q8_0: return launch_m<QMM_Q8_0>(P, MT, g, smem, st);
+    case QMM_Q4_K: return launch_m<QMM_Q4_K>(P, MT, g, smem, st);
+    default: return launch_m<QMM_Q6_K>(P, MT, g, smem, st);
     }
 }
 
@@ -831,6 +904,7 @@ cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws,
     }
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     G.cta_begin[m] = static_cast<int>(grid);
+    G.p[0].stop_stage = inject_stop_stage();
     switch (mt_of(M)) {
     case 1: return launch_group_mt<1>(G, static_cast<int>(grid), smem, st);
     case 2: return launch_group_mt<2>(G, static_cast<int>(grid), smem, st);

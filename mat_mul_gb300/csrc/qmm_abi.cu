@@ -39,6 +39,7 @@ const bool g_no_mma_gemv = [] {
 std::atomic<int64_t> g_launches{0};
 std::atomic<int> g_decode_path{QMM_DECODE_AUTO};
 std::atomic<int> g_prefill_path{QMM_PREFILL_AUTO};
+std::atomic<int> g_inject{0};  // pending qmm_inject_stall launches
 
 int fail(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int code, const char *fmt, ...) {
@@ -70,6 +71,8 @@ std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 // qmm_t's per-matrix completion counters, per (device, stream): zero between
 // calls (each call's last CTA of a matrix resets its counter)
 std::map<std::pair<int, cudaStream_t>, Workspace> g_counters;
+// qmm_gate_up's intermediate products g (and u), per (device, stream)
+std::map<std::pair<int, cudaStream_t>, Workspace> g_gate;
 
 int device_info(int dev, DeviceInfo &out) {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -117,6 +120,31 @@ int workspace(int dev, cudaStream_t st, size_t bytes, void **ptr) {
     }
     w.bytes = want;
     *ptr = w.ptr;
+    return QMM_OK;
+}
+
+// The gate/up intermediate buffer of at least `bytes` for (dev, stream);
+// growing synchronises the stream before the old buffer is released.
+int gate_buffer(int dev, cudaStream_t st, size_t bytes, float **ptr) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = g_gate[{dev, st}];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            cudaError_t e = cudaStreamSynchronize(st);
+            if (e != cudaSuccess) return cuda_fail(e, "gate buffer grow (sync)");
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        const size_t want = (bytes + (2u << 20) - 1) & ~size_t((2u << 20) - 1);
+        cudaError_t e = cudaMalloc(&w.ptr, want);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            return fail(QMM_ENOMEM, "gate buffer of %zu bytes: %s", want, cudaGetErrorString(e));
+        }
+        w.bytes = want;
+    }
+    *ptr = static_cast<float *>(w.ptr);
     return QMM_OK;
 }
 
@@ -177,6 +205,12 @@ namespace qk {
 int record_error(int code, const char *msg) { return fail(code, "%s", msg); }
 // Add n kernel launches to qmm_launch_count().
 void count_launches(int64_t n) { g_launches.fetch_add(n); }
+int inject_stop_stage() {
+    int v = g_inject.load();
+    while (v > 0)
+        if (g_inject.compare_exchange_weak(v, v - 1)) return 1;
+    return NO_STOP;
+}
 }  // namespace qk
 
 namespace {
@@ -235,6 +269,11 @@ int qmm_set_decode_path(int path) {
     if (path != QMM_DECODE_AUTO && path != QMM_DECODE_BLOCK && path != QMM_DECODE_TENSOR)
         return fail(QMM_EINVAL_SHAPE, "unknown decode path %d", path);
     return g_decode_path.exchange(path);
+}
+
+int qmm_inject_stall(int launches) {
+    if (launches < 0) return fail(QMM_EINVAL_SHAPE, "launches=%d must be >= 0", launches);
+    return g_inject.exchange(launches);
 }
 
 int qmm_set_prefill_path(int path) {
@@ -513,6 +552,71 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
     return QMM_OK;
 }
 
+int qmm_gate_up(int type_gate, const void *W_gate, int type_up, const void *W_up, int64_t N, int64_t K,
+                const float *x, int64_t M, float *h, void *stream) {
+    g_err[0] = 0;
+    if (int rc = check_type(type_gate)) return rc;
+    if (int rc = check_type(type_up)) return rc;
+    if (N < 0 || M < 0 || K < 0 || K % qk::block_weights(type_gate) || K % qk::block_weights(type_up))
+        return fail(QMM_EINVAL_SHAPE, "N=%lld K=%lld M=%lld: sizes must be >= 0 and K a multiple of both block sizes",
+                    static_cast<long long>(N), static_cast<long long>(K), static_cast<long long>(M));
+    if (K > (int64_t(1) << 24)) return fail(QMM_EINVAL_SHAPE, "K=%lld exceeds 2^24", static_cast<long long>(K));
+    if (M == 0 || N == 0) return QMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!h || !aligned(h, 4)) return fail(QMM_EINVAL_PTR, "h null or not 4-byte aligned");
+    if (K == 0) {  // g = u = 0, so h = silu(0) * 0 = 0
+        cudaError_t e = cudaMemsetAsync(h, 0, static_cast<size_t>(M * N) * sizeof(float), st);
+        if (e != cudaSuccess) return cuda_fail(e, "zero fill");
+        return QMM_OK;
+    }
+    if (!W_gate || !W_up || !x) return fail(QMM_EINVAL_PTR, "null pointer");
+    if (!aligned(W_gate, 16) || !aligned(W_up, 16)) return fail(QMM_EINVAL_PTR, "W_gate and W_up must be 16-byte aligned");
+    if (!aligned(x, 4)) return fail(QMM_EINVAL_PTR, "x must be 4-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo di;
+    if (int rc = device_info(dev, di)) return rc;
+
+    // one launch: both matrices of one type on the block-per-lane kernel
+    if (type_gate == type_up && M <= 2 && !g_force_round_gemv && !decode_on_tensor_cores(type_gate, M, N, K, di) &&
+        qk::gemv_sb_fits(type_gate, static_cast<int>(M), K, di.max_smem)) {
+        e = qk::launch_gemv_sb_gateup(type_gate, W_gate, W_up, N, K, x, static_cast<int>(M), h, st, di.num_sms,
+                                      di.max_smem, di.status);
+        if (e == cudaSuccess) {
+            g_launches.fetch_add(1);
+            return QMM_OK;
+        }
+        if (e != cudaErrorNotSupported) return cuda_fail(e, "gate+up launch");
+    }
+    float *gbuf = nullptr;
+    // tensor-core decode: x quantised once, g into the buffer, then the up
+    // launch, which reads g and writes h (three launches)
+    if (decode_on_tensor_cores(type_gate, M, N, K, di) && decode_on_tensor_cores(type_up, M, N, K, di)) {
+        if (int rc = gate_buffer(dev, st, static_cast<size_t>(M * N) * sizeof(float), &gbuf)) return rc;
+        void *ws = nullptr;
+        if (int rc = quantize_for_tensor_cores(dev, st, x, M, K, di, &ws)) return rc;
+        e = qk::launch_gemv_mma(type_gate, W_gate, N, K, ws, static_cast<int>(M), gbuf, st, di.num_sms, di.max_smem,
+                                di.status);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core gemv launch (gate)");
+        g_launches.fetch_add(1);
+        e = qk::launch_gemv_mma(type_up, W_up, N, K, ws, static_cast<int>(M), h, st, di.num_sms, di.max_smem,
+                                di.status, gbuf);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core gemv launch (up)");
+        g_launches.fetch_add(1);
+        return QMM_OK;
+    }
+    // otherwise the two products as qmm(), then h = silu(g) * u
+    if (int rc = gate_buffer(dev, st, static_cast<size_t>(2 * M * N) * sizeof(float), &gbuf)) return rc;
+    float *ubuf = gbuf + M * N;
+    if (int rc = qmm(type_gate, W_gate, N, K, x, M, gbuf, stream)) return rc;
+    if (int rc = qmm(type_up, W_up, N, K, x, M, ubuf, stream)) return rc;
+    e = qk::launch_silu_mul(gbuf, ubuf, h, M * N, st, di.num_sms);
+    if (e != cudaSuccess) return cuda_fail(e, "silu-mul launch");
+    g_launches.fetch_add(1);
+    return QMM_OK;
+}
+
 int qmm_device_status(void *stream) {
     g_err[0] = 0;
     int dev = 0;
@@ -541,7 +645,7 @@ int qmm_release(void) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
     std::lock_guard<std::mutex> lk(g_mu);
-    for (auto *m : {&g_ws, &g_counters}) {
+    for (auto *m : {&g_ws, &g_counters, &g_gate}) {
         for (auto it = m->begin(); it != m->end();) {
             if (it->first.first == dev) {
                 cudaFree(it->second.ptr);

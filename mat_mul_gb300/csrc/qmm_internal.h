@@ -78,6 +78,14 @@ cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws,
                                  const float *x, int M, float *const *ys, cudaStream_t st, int num_sms,
                                  int max_smem, int *status);
 void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t *need, int num_sms, int *g);
+// The gate and up products of one MLP (same type and shape, M <= 2) in one
+// launch of the block-per-lane kernel: h = silu(Wg.x) * (Wu.x).
+// cudaErrorNotSupported when the pair does not fit the kernel's plan.
+cudaError_t launch_gemv_sb_gateup(int type, const void *Wg, const void *Wu, int64_t N, int64_t K, const float *x,
+                                  int M, float *h, cudaStream_t st, int num_sms, int max_smem, int *status);
+
+// h = silu(g) * u elementwise over n values (gate_up.cu).
+cudaError_t launch_silu_mul(const float *g, const float *u, float *h, int64_t n, cudaStream_t st, int num_sms);
 
 // Decode for 2 <= M <= 8 on the tensor cores (gemv_mma.cu): Q4_K or Q6_K,
 // sixteen weight rows per mma.sync.m16n8k16 (fp16 operands, fp32
@@ -88,9 +96,11 @@ void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t 
 // Launched with programmatic dependent launch right after that quantiser
 // (launched with trigger_dependents): the kernel streams weights before it
 // waits, and reads xh after.
+// With gate (g [M][N], written by the launch just before on the stream)
+// the kernel writes y = silu(g) * (W.x) instead of W.x.
 bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_sms);
 cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
-                            cudaStream_t st, int num_sms, int max_smem, int *status);
+                            cudaStream_t st, int num_sms, int max_smem, int *status, const float *gate = nullptr);
 
 // Prefill GEMM on tcgen05 (gemm_tc.cu): Q4_K, Q6_K or Q8_0 weights with K a
 // multiple of 256, fp16 activations xh [M][K] (d*q*2^e_m from the
@@ -118,5 +128,12 @@ cudaError_t launch_qmm_t(const void *W, int64_t H, int64_t N, int64_t K, const f
 int record_error(int code, const char *msg);
 // Add n kernel launches to the count qmm_launch_count() reports.
 void count_launches(int64_t n);
+
+// Failure-detection test hook (qmm_inject_stall): the stage at which the
+// first CTA's producer of the next weight-streaming launch stops issuing
+// copies (1 while an injection is pending, consumed by this call), else a
+// value no launch reaches.
+int inject_stop_stage();
+constexpr int NO_STOP = 0x7fffffff;
 
 }  // namespace qk

@@ -216,3 +216,33 @@ def test_noalloc_binding_checks_x_and_y():
     # host tensors are refused before any size check reaches the library
     with pytest.raises(ValueError):
         q.qmm_noalloc(q.Q4_K, W, 1, 256, x, y)
+
+
+def test_inject_stall_setter_validates_and_returns_the_previous_count():
+    L = q.load()
+    assert L.qmm_inject_stall(0) == 0
+    assert L.qmm_inject_stall(2) == 0
+    assert L.qmm_inject_stall(-1) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_inject_stall(0) == 2
+    with pytest.raises(q.QmmError):
+        q.inject_stall(-3)
+
+
+def test_gate_up_validation_rejects_before_launch():
+    L = q.load()
+    null = ctypes.c_void_p(0)
+    before = L.qmm_launch_count()
+    assert L.qmm_gate_up(q.Q4_K, null, 9, null, 4, 256, null, 1, null, None) == q.QMM_EINVAL_TYPE
+    assert L.qmm_gate_up(q.Q5_K, null, q.Q4_K, null, 4, 256, null, 1, null, None) == q.QMM_EINVAL_TYPE
+    # K a multiple of both block sizes
+    assert L.qmm_gate_up(q.Q8_0, null, q.Q4_K, null, 4, 96, null, 1, null, None) == q.QMM_EINVAL_SHAPE
+    assert L.qmm_gate_up(q.Q4_K, null, q.Q4_K, null, -1, 256, null, 1, null, None) == q.QMM_EINVAL_SHAPE
+    # empty problems launch nothing; null pointers on a real one are refused
+    assert L.qmm_gate_up(q.Q4_K, null, q.Q4_K, null, 0, 256, null, 1, null, None) == q.QMM_OK
+    assert L.qmm_gate_up(q.Q4_K, null, q.Q4_K, null, 4, 256, null, 0, null, None) == q.QMM_OK
+    assert L.qmm_gate_up(q.Q4_K, null, q.Q4_K, null, 4, 256, null, 1, null, None) == q.QMM_EINVAL_PTR
+    buf = ctypes.create_string_buffer(4096)
+    base = (ctypes.addressof(buf) + 15) & ~15
+    assert L.qmm_gate_up(q.Q4_K, ctypes.c_void_p(base), q.Q4_K, ctypes.c_void_p(base + 2), 4, 256,
+                         ctypes.c_void_p(base), 1, ctypes.c_void_p(base), None) == q.QMM_EINVAL_PTR
+    assert L.qmm_launch_count() == before
