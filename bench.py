@@ -424,7 +424,7 @@ def run_ours(args):
     del g_e2e, g_step
 
     detail = []
-    groups = layer = layer_m = gate_up = None
+    groups = layer = layer_m = gate_up = kq = None
     roof = None
     gemm = None
     cpu = None
@@ -594,6 +594,50 @@ def run_ours(args):
         gemm = {"kernels": gemm, "int8_peak_tops_torch_int_mm": round(int8_peak, 1) if int8_peak else None,
                 "f16_peak_tflops": peaks["bf16"]}
 
+        # ---- the other K-quants: decode at M=1 (Qwen3-14B gate shape,
+        # rotating copies) and prefill at M=512 (Mistral-7B up shape)
+        kq = []
+        for qtype in (synth.Q5_K, synth.Q3_K, synth.Q2_K):
+            K, N = 5120, 17408
+            W = torch.from_numpy(synth.weights(qtype, N, K, seed=5000 + qtype)).to(dev)
+            nbytes = W.numel()
+            ncopy = max(2, -(-4 * L2_BYTES // nbytes))
+            copies = [W] + [W.clone() for _ in range(ncopy - 1)]
+            xk = torch.from_numpy(synth.config_activations(3, 1, K)).to(dev)
+            yk = torch.empty((1, N), dtype=torch.float32, device=dev)
+            inner = max(ncopy, 16)
+
+            def kcall(copies=copies, xk=xk, yk=yk, qtype=qtype, K=K, N=N, inner=inner):
+                for i in range(inner):
+                    q.qmm(qtype, copies[i % len(copies)], N, K, xk, y=yk, stream=stream)
+
+            g = capture(kcall)
+            t_dec = timed(g, 5, 2) / inner
+            del g, copies
+            K, N = 4096, 14336
+            W = torch.from_numpy(synth.weights(qtype, N, K, seed=6000 + qtype)).to(dev)
+            ncopy = max(2, -(-4 * L2_BYTES // W.numel()))
+            copies = [W] + [W.clone() for _ in range(ncopy - 1)]
+            xp = torch.from_numpy(synth.config_activations(4, 512, K)).to(dev)
+            yp = torch.empty((512, N), dtype=torch.float32, device=dev)
+            inner = max(ncopy, 8)
+
+            def pcall(copies=copies, xp=xp, yp=yp, qtype=qtype, K=K, N=N, inner=inner):
+                for i in range(inner):
+                    q.qmm(qtype, copies[i % len(copies)], N, K, xp, y=yp, stream=stream)
+
+            g = capture(pcall)
+            t_pre = timed(g, 3, 1) / inner
+            del g, copies
+            torch.cuda.empty_cache()
+            dgbs = nbytes / (t_dec * 1e-3) / 1e9
+            tops = 2 * 512 * N * K / (t_pre * 1e-3) / 1e12
+            kq.append({"type": synth.TYPE_NAMES[qtype],
+                       "decode_M1": {"K": 5120, "N": 17408, "MB": round(nbytes / 1e6, 3), "us": round(t_dec * 1e3, 2),
+                                     "GB/s": round(dgbs, 1), "frac_hbm": round(dgbs / peaks["hbm"], 4)},
+                       "prefill_M512": {"K": K, "N": N, "us": round(t_pre * 1e3, 1), "TOPS": round(tops, 1),
+                                        "kernel": "int8 mma.sync (exact block dots)"}})
+
         # ---- the value side of attention over a q8_0 KV cache (qmm_t):
         # Qwen3-14B-shaped, 8 cache heads x 32768 positions x head_dim 128,
         # 5 probability rows per head; rotating copies of the cache (> L2)
@@ -645,7 +689,7 @@ def run_ours(args):
             "clocks": clocks, "per_matrix": detail, "groups": groups, "gate_up_fused": gate_up,
             "qwen3_14b_layer": layer,
             "qwen3_14b_layer_M": layer_m,
-            "prefill_gemm": gemm,
+            "prefill_gemm": gemm, "other_k_quants": kq,
             "kv_value_cache": kv_line,
         }
         print(json.dumps(line))

@@ -3,16 +3,20 @@
 // per-block dot products and fp32 per-block scaling.
 //
 // This is the reference-grade tensor-core path: simple, exact per block, and
-// used for shapes the tcgen05 pipeline does not cover.  The activations
-// arrive quantised (int8 q, fp32 scale, int32 sum per 32-block) from the
-// quantiser kernel; the weights are unpacked to int8 in shared memory by the
-// CTA (Q4_K: q in 0..15, Q6_K: q-32, Q8_0: q) together with their scales.
+// used for shapes and types the tcgen05 pipeline does not cover.  The
+// activations arrive quantised (int8 q, fp32 scale, int32 sum per 32-block,
+// for Q2_K the sums of the 16-element halves) from the quantiser kernel; the
+// weights are unpacked to int8 in shared memory by the CTA (Q4_K: q in
+// 0..15, Q5_K: 0..31, Q6_K: q-32, Q3_K: -4..3, Q2_K: 0..3, Q8_0: q) together
+// with their scales (and mins).
 //
 // Tile: 64 activation rows x 64 weight rows per CTA, one 256-wide K step per
-// iteration (one Q4_K/Q6_K super-block, eight Q8_0 blocks); four warps of
-// 32x32 outputs, each issuing m16n8k32 (Q4_K, Q8_0: one 32-block) or two
-// m16n8k16 (Q6_K: one 16-sub-block each) per 32-wide block.
+// iteration (one super-block, eight Q8_0 blocks); four warps of 32x32
+// outputs, each issuing m16n8k32 (Q4_K, Q5_K, Q8_0: one 32-block) or two
+// m16n8k16 (Q6_K, Q3_K, Q2_K: one 16-weight group each) per 32-wide block.
 #include "qmm_device.cuh"
+
+#include <type_traits>
 
 namespace qk {
 
@@ -26,12 +30,16 @@ struct GemmSmem {
     int8_t b[BN][LDS_ROW];
     float xd[BM][8];
     int32_t xs[BM][8];
-    float wd[BN];       // d (Q4_K, Q6_K)
-    float wdmin[BN];    // dmin (Q4_K)
+    int16_t xs2[BM][16];  // Q2_K: the sums of the two 16-element halves of every block
+    float wd[BN];       // d (the K-quants)
+    float wdmin[BN];    // dmin (Q4_K, Q5_K, Q2_K)
     float wd8[BN][8];   // per-block d (Q8_0)
-    int16_t wsc[BN][16];  // Q4_K: sc[8]; Q6_K: sc[16]
-    int16_t wm[BN][8];    // Q4_K: m[8]
+    int16_t wsc[BN][16];  // Q4_K, Q5_K: sc[8]; Q6_K, Q3_K (sc - 32), Q2_K: sc[16]
+    int16_t wm[BN][16];   // Q4_K, Q5_K: m[8]; Q2_K: m[16]
 };
+
+// Sixteen 16-weight groups per 32-block pair of K-steps (two mma k16 per block)
+template <int T> constexpr bool kGroups16 = T == QMM_Q6_K || T == QMM_Q3_K || T == QMM_Q2_K;
 
 __device__ __forceinline__ void mma_k32(int (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile(
@@ -56,7 +64,8 @@ __device__ void load_weights(GemmSmem &S, const uint8_t *__restrict__ W, int64_t
     const int r = tid >> 1, part = tid & 1;  // 128 threads: two per weight row
     const int64_t n = n0 + r;
     int8_t *dst = S.b[r];
-    if constexpr (T == QMM_Q4_K) {
+    if constexpr (T == QMM_Q4_K || T == QMM_Q5_K) {
+        constexpr int BB = Fmt<T>::BB, QOFF = T == QMM_Q5_K ? 48 : 16;  // quant bytes
         if (n >= N) {
             for (int i = part * 128; i < part * 128 + 128; ++i) dst[i] = 0;
             if (part == 0) {
@@ -66,7 +75,7 @@ __device__ void load_weights(GemmSmem &S, const uint8_t *__restrict__ W, int64_t
             }
             return;
         }
-        const uint8_t *B = W + (n * (K / 256) + k0 / 256) * 144;
+        const uint8_t *B = W + (n * (K / 256) + k0 / 256) * BB;
         if (part == 0) {
             const uint8_t *Sb = B + 4;
             S.wd[r] = half_bits_to_float(B[0] | (B[1] << 8));
@@ -84,16 +93,22 @@ __device__ void load_weights(GemmSmem &S, const uint8_t *__restrict__ W, int64_t
                 S.wm[r][j] = static_cast<int16_t>(m);
             }
         }
-        // chunks c = 2*part, 2*part+1: qs[32c+l] -> weights 64c+l (low), 64c+32+l (high)
+        // chunks c = 2*part, 2*part+1: qs[32c+l] -> weights 64c+l (low), 64c+32+l
+        // (high); Q5_K: plus bit 2c (low) / 2c+1 (high) of fifth-bit byte l as bit 4
         for (int c = 2 * part; c < 2 * part + 2; ++c) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(B + 16 + 32 * c);
+            const uint4 *src = reinterpret_cast<const uint4 *>(B + QOFF + 32 * c);
             for (int v = 0; v < 2; ++v) {
                 const uint4 w = __ldg(src + v);
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
                 uint32_t lo[4], hi[4];
+                uint32_t hb[4] = {0u, 0u, 0u, 0u};
+                if constexpr (T == QMM_Q5_K) {
+                    const uint4 h = __ldg(reinterpret_cast<const uint4 *>(B + 16) + v);
+                    hb[0] = h.x, hb[1] = h.y, hb[2] = h.z, hb[3] = h.w;
+                }
                 for (int e = 0; e < 4; ++e) {
-                    lo[e] = ws[e] & 0x0F0F0F0Fu;
-                    hi[e] = (ws[e] >> 4) & 0x0F0F0F0Fu;
+                    lo[e] = (ws[e] & 0x0F0F0F0Fu) | (((hb[e] >> (2 * c)) & 0x01010101u) << 4);
+                    hi[e] = ((ws[e] >> 4) & 0x0F0F0F0Fu) | (((hb[e] >> (2 * c + 1)) & 0x01010101u) << 4);
                 }
                 *reinterpret_cast<uint4 *>(dst + 64 * c + 16 * v) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 *reinterpret_cast<uint4 *>(dst + 64 * c + 32 + 16 * v) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -120,6 +135,55 @@ __device__ void load_weights(GemmSmem &S, const uint8_t *__restrict__ W, int64_t
                 const int hi = (B[128 + 32 * h + l] >> (2 * g)) & 3;
                 dst[128 * h + 32 * g + l] = static_cast<int8_t>((lo | (hi << 4)) - 32);
             }
+    } else if constexpr (T == QMM_Q3_K) {
+        if (n >= N) {
+            for (int i = part * 128; i < part * 128 + 128; ++i) dst[i] = 0;
+            if (part == 0) {
+                S.wd[r] = 0.f;
+                for (int j = 0; j < 16; ++j) S.wsc[r][j] = 0;
+            }
+            return;
+        }
+        const uint8_t *B = W + (n * (K / 256) + k0 / 256) * 110;
+        if (part == 0) {
+            const uint8_t *Sb = B + 96;
+            S.wd[r] = half_bits_to_float(B[108] | (B[109] << 8));
+            for (int i = 0; i < 16; ++i) {
+                const int k = i & 3, G = i >> 2;
+                const int lo = (G & 2 ? Sb[(G & 1) * 4 + k] >> 4 : Sb[(G & 1) * 4 + k]) & 15;
+                const int hi = (Sb[8 + k] >> (2 * G)) & 3;
+                S.wsc[r][i] = static_cast<int16_t>((lo | (hi << 4)) - 32);
+            }
+        }
+        const int h = part;  // half h: weights 128h + 32j + l
+        for (int j = 0; j < 4; ++j)
+            for (int l = 0; l < 32; ++l) {
+                const int low = (B[32 + 32 * h + l] >> (2 * j)) & 3;
+                const int bit = (B[l] >> (4 * h + j)) & 1;
+                dst[128 * h + 32 * j + l] = static_cast<int8_t>(bit ? low : low - 4);
+            }
+    } else if constexpr (T == QMM_Q2_K) {
+        if (n >= N) {
+            for (int i = part * 128; i < part * 128 + 128; ++i) dst[i] = 0;
+            if (part == 0) {
+                S.wd[r] = S.wdmin[r] = 0.f;
+                for (int j = 0; j < 16; ++j) S.wsc[r][j] = S.wm[r][j] = 0;
+            }
+            return;
+        }
+        const uint8_t *B = W + (n * (K / 256) + k0 / 256) * 84;
+        if (part == 0) {
+            S.wd[r] = half_bits_to_float(B[80] | (B[81] << 8));
+            S.wdmin[r] = half_bits_to_float(B[82] | (B[83] << 8));
+            for (int i = 0; i < 16; ++i) {
+                S.wsc[r][i] = static_cast<int16_t>(B[i] & 15);
+                S.wm[r][i] = static_cast<int16_t>(B[i] >> 4);
+            }
+        }
+        const int h = part;
+        for (int j = 0; j < 4; ++j)
+            for (int l = 0; l < 32; ++l)
+                dst[128 * h + 32 * j + l] = static_cast<int8_t>((B[16 + 32 * h + l] >> (2 * j)) & 3);
     } else {
         // Q8_0: this thread covers blocks 4*part .. 4*part+3 of the K step
         for (int bb = 4 * part; bb < 4 * part + 4; ++bb) {
@@ -141,6 +205,7 @@ __global__ void __launch_bounds__(128) gemm_mma_kernel(const uint8_t *__restrict
                                                        int64_t K, const int8_t *__restrict__ xq,
                                                        const float *__restrict__ xd,
                                                        const int32_t *__restrict__ xs, int xd_ld,
+                                                       const int32_t *__restrict__ xs16, int xs16_ld,
                                                        int64_t M, float *__restrict__ y) {
     __shared__ __align__(16) GemmSmem S;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -173,7 +238,13 @@ __global__ void __launch_bounds__(128) gemm_mma_kernel(const uint8_t *__restrict
             const int64_t m = m0 + r;
             const bool ok = m < M && j < nsub;
             S.xd[r][j] = ok ? xd[m * xd_ld + k0 / 32 + j] : 0.f;
-            S.xs[r][j] = ok ? xs[m * xd_ld + k0 / 32 + j] : 0;
+            if constexpr (T == QMM_Q2_K) {
+                // |half-block sum| <= 16 * 127: fits int16
+                S.xs2[r][2 * j] = static_cast<int16_t>(ok ? xs16[m * xs16_ld + 2 * (k0 / 32 + j)] : 0);
+                S.xs2[r][2 * j + 1] = static_cast<int16_t>(ok ? xs16[m * xs16_ld + 2 * (k0 / 32 + j) + 1] : 0);
+            } else {
+                S.xs[r][j] = ok ? xs[m * xd_ld + k0 / 32 + j] : 0;
+            }
         }
         load_weights<T>(S, W, N, K, n0, k0);
         __syncthreads();
@@ -197,7 +268,7 @@ __global__ void __launch_bounds__(128) gemm_mma_kernel(const uint8_t *__restrict
                     b[1] = *reinterpret_cast<const uint32_t *>(&S.b[cb][32 * j + 16 + 4 * t]);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) I[mi][ni][e] = I2[mi][ni][e] = 0;
-                    if constexpr (T == QMM_Q6_K) {
+                    if constexpr (kGroups16<T>) {
                         mma_k16(I[mi][ni], a[0], a[1], b[0]);
                         mma_k16(I2[mi][ni], a[2], a[3], b[1]);
                     } else {
@@ -212,7 +283,8 @@ __global__ void __launch_bounds__(128) gemm_mma_kernel(const uint8_t *__restrict
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = 32 * wm + 16 * mi + g + 8 * hh;
                     const float dx = S.xd[r][j];
-                    const int sx = S.xs[r][j];
+                    const int sx = T == QMM_Q2_K ? 0 : S.xs[r][j];
+                    const int sa = T == QMM_Q2_K ? S.xs2[r][2 * j] : 0, sb = T == QMM_Q2_K ? S.xs2[r][2 * j + 1] : 0;
 #pragma unroll
                     for (int ni = 0; ni < 4; ++ni)
 #pragma unroll
@@ -220,12 +292,16 @@ __global__ void __launch_bounds__(128) gemm_mma_kernel(const uint8_t *__restrict
                             const int c = 32 * wn + 8 * ni + 2 * t + cc;
                             const int e = 2 * hh + cc;
                             float v;
-                            if constexpr (T == QMM_Q4_K) {
+                            if constexpr (T == QMM_Q4_K || T == QMM_Q5_K) {
                                 v = S.wd[c] * static_cast<float>(S.wsc[c][j] * I[mi][ni][e]) -
                                     S.wdmin[c] * static_cast<float>(S.wm[c][j] * sx);
-                            } else if constexpr (T == QMM_Q6_K) {
+                            } else if constexpr (T == QMM_Q6_K || T == QMM_Q3_K) {
                                 const int J = S.wsc[c][2 * j] * I[mi][ni][e] + S.wsc[c][2 * j + 1] * I2[mi][ni][e];
                                 v = S.wd[c] * static_cast<float>(J);
+                            } else if constexpr (T == QMM_Q2_K) {
+                                const int J = S.wsc[c][2 * j] * I[mi][ni][e] + S.wsc[c][2 * j + 1] * I2[mi][ni][e];
+                                const int Mn = S.wm[c][2 * j] * sa + S.wm[c][2 * j + 1] * sb;
+                                v = S.wd[c] * static_cast<float>(J) - S.wdmin[c] * static_cast<float>(Mn);
                             } else {
                                 v = S.wd8[c][j] * static_cast<float>(I[mi][ni][e]);
                             }
@@ -256,13 +332,21 @@ __global__ void __launch_bounds__(128) gemm_mma_kernel(const uint8_t *__restrict
 
 cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
                             const float *xd, const int32_t *xs, int xd_ld, int64_t M, float *y,
-                            cudaStream_t st) {
+                            cudaStream_t st, const int32_t *xs16, int xs16_ld) {
+    if (type == QMM_Q2_K && !xs16) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
     const auto *w = static_cast<const uint8_t *>(W);
+    auto run = [&](auto t) {
+        constexpr int T = decltype(t)::value;
+        gemm_mma_kernel<T><<<grid, 128, 0, st>>>(w, N, K, xq, xd, xs, xd_ld, xs16, xs16_ld, M, y);
+    };
     switch (type) {
-    case QMM_Q8_0: gemm_mma_kernel<QMM_Q8_0><<<grid, 128, 0, st>>>(w, N, K, xq, xd, xs, xd_ld, M, y); break;
-    case QMM_Q4_K: gemm_mma_kernel<QMM_Q4_K><<<grid, 128, 0, st>>>(w, N, K, xq, xd, xs, xd_ld, M, y); break;
-    default: gemm_mma_kernel<QMM_Q6_K><<<grid, 128, 0, st>>>(w, N, K, xq, xd, xs, xd_ld, M, y); break;
+    case QMM_Q8_0: run(std::integral_constant<int, QMM_Q8_0>{}); break;
+    case QMM_Q4_K: run(std::integral_constant<int, QMM_Q4_K>{}); break;
+    case QMM_Q5_K: run(std::integral_constant<int, QMM_Q5_K>{}); break;
+    case QMM_Q3_K: run(std::integral_constant<int, QMM_Q3_K>{}); break;
+    case QMM_Q2_K: run(std::integral_constant<int, QMM_Q2_K>{}); break;
+    default: run(std::integral_constant<int, QMM_Q6_K>{}); break;
     }
     return cudaGetLastError();
 }

@@ -531,6 +531,7 @@ bool plan_gemv(int type, int M, int K, int xd_ld, int xs_ld, int max_smem, GemvP
 // True when the decode kernel can hold M rows of K activations.
 bool gemv_fits(int type, int M, int64_t K, int xd_ld, int xs_ld, int max_smem) {
     if (M < 1 || M > 8 || K > (1 << 22)) return false;
+    if (type != QMM_Q8_0 && type != QMM_Q4_K && type != QMM_Q6_K) return false;  // its three unit kinds
     GemvParams P = {};
     int smem = 0;
     return plan_gemv(type, M, static_cast<int>(K), xd_ld, xs_ld, max_smem, P, smem);

@@ -181,12 +181,10 @@ int counters(int dev, cudaStream_t st, int64_t n, unsigned **ptr) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// The products (qmm, qmm_group, qmm_t, qmm_noalloc) take Q8_0, Q4_K, Q6_K.
+// The products (qmm, qmm_group, qmm_gate_up) take every type of the enum;
+// qmm_t takes Q8_0 and qmm_noalloc Q8_0, Q4_K, Q6_K (checked there).
 int check_type(int type) {
-    if (type == QMM_Q5_K || type == QMM_Q3_K || type == QMM_Q2_K)
-        return fail(QMM_EINVAL_TYPE, "block type %d: only qmm_dequant takes it so far", type);
-    if (type != QMM_Q8_0 && type != QMM_Q4_K && type != QMM_Q6_K)
-        return fail(QMM_EINVAL_TYPE, "unknown block type %d", type);
+    if (type < QMM_Q8_0 || type > QMM_Q2_K) return fail(QMM_EINVAL_TYPE, "unknown block type %d", type);
     return QMM_OK;
 }
 
@@ -412,9 +410,12 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     const int64_t s16_ld = static_cast<int64_t>(align_up(static_cast<size_t>(K / 16), 4));
     const bool gemv = M <= 8 && qk::gemv_fits(type, static_cast<int>(M), K, static_cast<int>(d_ld),
                                                static_cast<int>(s16_ld), di.max_smem);
+    // the round-based decode and the Q2_K prefill read 16-element sums, the
+    // other prefills 32-element ones
+    const bool halves = gemv || type == QMM_Q2_K;
     const size_t q_bytes = align_up(static_cast<size_t>(M * K), 256);
     const size_t d_bytes = align_up(static_cast<size_t>(M * d_ld) * 4, 256);
-    const size_t a_bytes = align_up(static_cast<size_t>(M * (gemv ? s16_ld : d_ld)) * 4, 256);
+    const size_t a_bytes = align_up(static_cast<size_t>(M * (halves ? s16_ld : d_ld)) * 4, 256);
     void *ws = nullptr;
     if (int rc = workspace(dev, st, q_bytes + d_bytes + a_bytes, &ws)) return rc;
     char *wsb = static_cast<char *>(ws);
@@ -424,7 +425,7 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     o.d = reinterpret_cast<float *>(wsb + q_bytes);
     o.d_ld = d_ld;
     o.s16_ld = s16_ld;
-    if (gemv) o.s16 = reinterpret_cast<int32_t *>(wsb + q_bytes + d_bytes);
+    if (halves) o.s16 = reinterpret_cast<int32_t *>(wsb + q_bytes + d_bytes);
     else o.s32 = reinterpret_cast<int32_t *>(wsb + q_bytes + d_bytes);
     e = qk::launch_quantize(x, M, K, o, st, gemv, di.num_sms);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
@@ -435,7 +436,8 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
                             di.max_smem, di.status);
         if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
     } else {
-        e = qk::launch_gemm_mma(type, W_blocks, N, K, o.q, o.d, o.s32, static_cast<int>(d_ld), M, y, st);
+        e = qk::launch_gemm_mma(type, W_blocks, N, K, o.q, o.d, o.s32, static_cast<int>(d_ld), M, y, st, o.s16,
+                                static_cast<int>(s16_ld));
         if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     }
     g_launches.fetch_add(1);
@@ -522,9 +524,12 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
         if (fits) {
             e = qk::launch_gemv_sb_group(n, types, Ws, Ns, K, x, static_cast<int>(M), ys,
                                          static_cast<cudaStream_t>(stream), di.num_sms, di.max_smem, di.status);
-            if (e != cudaSuccess) return cuda_fail(e, "group gemv launch");
-            g_launches.fetch_add(1);
-            return QMM_OK;
+            if (e == cudaSuccess) {
+                g_launches.fetch_add(1);
+                return QMM_OK;
+            }
+            // (the one-launch group takes Q8_0, Q4_K and Q6_K; other types run entry by entry)
+            if (e != cudaErrorNotSupported) return cuda_fail(e, "group gemv launch");
         }
         // every entry on the tensor-core kernel: x quantised once, then one
         // decode launch per matrix (each later one starts as the one before

@@ -19,8 +19,20 @@ template <int T> struct Fmt;
 template <> struct Fmt<QMM_Q8_0> { static constexpr int BB = 34, QK = 32; };
 template <> struct Fmt<QMM_Q4_K> { static constexpr int BB = 144, QK = 256; };
 template <> struct Fmt<QMM_Q6_K> { static constexpr int BB = 210, QK = 256; };
+template <> struct Fmt<QMM_Q5_K> { static constexpr int BB = 176, QK = 256; };
+template <> struct Fmt<QMM_Q3_K> { static constexpr int BB = 110, QK = 256; };
+template <> struct Fmt<QMM_Q2_K> { static constexpr int BB = 84, QK = 256; };
 
-inline int block_bytes(int t) { return t == QMM_Q8_0 ? 34 : t == QMM_Q4_K ? 144 : 210; }
+inline int block_bytes(int t) {
+    switch (t) {
+    case QMM_Q8_0: return 34;
+    case QMM_Q4_K: return 144;
+    case QMM_Q6_K: return 210;
+    case QMM_Q5_K: return 176;
+    case QMM_Q3_K: return 110;
+    default: return 84;  // QMM_Q2_K
+    }
+}
 inline int block_weights(int t) { return t == QMM_Q8_0 ? 32 : 256; }
 
 // Status bits a kernel may raise in the per-device status word.

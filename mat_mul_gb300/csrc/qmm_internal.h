@@ -110,10 +110,12 @@ bool gemm_tc_supported(int type, int64_t N, int64_t K, int64_t M);
 cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const void *xh, const float *xinv,
                            int64_t M, float *y, cudaStream_t st, int num_sms, int *status);
 
-// Prefill GEMM on mma.sync (gemm_mma.cu): q [M][K], d and s32 [M][xd_ld].
+// Prefill GEMM on mma.sync (gemm_mma.cu), every block type: q [M][K], d
+// and s32 [M][xd_ld]; Q2_K also needs the 16-element sums s16 [M][xs16_ld]
+// (two per block).
 cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const int8_t *xq,
                             const float *xd, const int32_t *xs, int xd_ld, int64_t M, float *y,
-                            cudaStream_t st);
+                            cudaStream_t st, const int32_t *xs16 = nullptr, int xs16_ld = 0);
 
 // Product with the transposed Q8_0 matrices (qmm_t.cu): y[h][m][k] =
 // sum_n x[h][m][n] * w[h][n][k], K a multiple of 32 up to 256.  part: the

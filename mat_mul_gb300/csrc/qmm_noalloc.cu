@@ -57,7 +57,7 @@ int err(int code, const char *fmt, long long a = 0, long long b = 0) {
 extern "C" QMM_API int qmm_noalloc(int type, const void *W_blocks, int64_t N, int64_t K, const float *x,
                                    int64_t M, float *y, void *stream) {
     if (type != QMM_Q8_0 && type != QMM_Q4_K && type != QMM_Q6_K)
-        return err(QMM_EINVAL_TYPE, "unknown block type %lld", type);
+        return err(QMM_EINVAL_TYPE, "block type %lld: qmm_noalloc takes Q8_0, Q4_K and Q6_K", type);
     const int qkw = qk::block_weights(type);
     if (N < 0 || M < 0 || K < 0 || K % qkw)
         return err(QMM_EINVAL_SHAPE, "N, K, M must be >= 0 and K a multiple of %lld (K=%lld)", qkw, K);

@@ -164,19 +164,21 @@ def test_qmm_t_validation_rejects_before_launch():
     assert L.qmm_launch_count() == before
 
 
-def test_other_k_quants_dequant_only():
-    """Q5_K, Q3_K and Q2_K: qmm_dequant validates them like the others; the
-    products reject them with QMM_EINVAL_TYPE (no product kernels yet)."""
+def test_other_k_quants_validation():
+    """Q5_K, Q3_K and Q2_K: qmm_dequant and the products validate them like
+    the others; qmm_t (the q8_0 KV cache) and qmm_noalloc reject them."""
     L = q.load()
     null = ctypes.c_void_p(0)
     for t in (q.Q5_K, q.Q3_K, q.Q2_K):
         assert L.qmm_dequant(t, null, 100, null) == q.QMM_EINVAL_SHAPE
         assert L.qmm_dequant(t, null, 256, null) == q.QMM_EINVAL_PTR
         assert L.qmm_dequant(t, null, 0, null) == q.QMM_OK
-        assert L.qmm(t, null, 4, 256, null, 1, null, null) == q.QMM_EINVAL_TYPE
-        assert b"only qmm_dequant" in L.qmm_last_error()
+        assert L.qmm(t, null, 4, 128, null, 1, null, null) == q.QMM_EINVAL_SHAPE
+        assert L.qmm(t, null, 4, 256, null, 1, null, null) == q.QMM_EINVAL_PTR
         assert L.qmm_t(t, null, 1, 4, 128, null, 1, null, null) == q.QMM_EINVAL_TYPE
+        assert L.qmm_noalloc(t, null, 4, 256, null, 1, null, null) == q.QMM_EINVAL_TYPE
     assert L.qmm_dequant(6, null, 256, null) == q.QMM_EINVAL_TYPE
+    assert L.qmm(6, null, 4, 256, null, 1, null, null) == q.QMM_EINVAL_TYPE
 
 
 
@@ -205,6 +207,7 @@ def test_noalloc_rejects_sizes_that_would_wrap_before_launch():
     assert L.qmm_noalloc(q.Q4_K, base, 4, 4096, base, 4097, base, None) == q.QMM_EINVAL_SHAPE
     assert b"scratch" in L.qmm_last_error()
     assert L.qmm_noalloc(q.Q5_K, base, 4, 256, base, 1, base, None) == q.QMM_EINVAL_TYPE
+    assert b"Q8_0, Q4_K and Q6_K" in L.qmm_last_error()
     assert L.qmm_launch_count() == before
 
 
@@ -233,7 +236,7 @@ def test_gate_up_validation_rejects_before_launch():
     null = ctypes.c_void_p(0)
     before = L.qmm_launch_count()
     assert L.qmm_gate_up(q.Q4_K, null, 9, null, 4, 256, null, 1, null, None) == q.QMM_EINVAL_TYPE
-    assert L.qmm_gate_up(q.Q5_K, null, q.Q4_K, null, 4, 256, null, 1, null, None) == q.QMM_EINVAL_TYPE
+    assert L.qmm_gate_up(6, null, q.Q4_K, null, 4, 256, null, 1, null, None) == q.QMM_EINVAL_TYPE
     # K a multiple of both block sizes
     assert L.qmm_gate_up(q.Q8_0, null, q.Q4_K, null, 4, 96, null, 1, null, None) == q.QMM_EINVAL_SHAPE
     assert L.qmm_gate_up(q.Q4_K, null, q.Q4_K, null, -1, 256, null, 1, null, None) == q.QMM_EINVAL_SHAPE
