@@ -104,6 +104,10 @@ QMM_API int qmm_dequant(int type, const void *blocks, int64_t n_elems, float *ou
  *   stream   : cudaStream_t to run on (NULL = legacy default stream).
  * Accuracy: |y - y_exact| <= 2e-3 * sum_k |w_k * xhat_k| + 1e-5, where
  * y_exact is the f64 result of the same quantised arithmetic.
+ * Decode launches use programmatic dependent launch: they start streaming W
+ * while the preceding kernel of this library on the stream finishes (x is
+ * read only after it completes), which is safe because no kernel of this
+ * library writes block data.
  * The call uses a library-owned device workspace per (device, stream) for
  * the quantised activations.  It is allocated, or grown, on the first call
  * that needs it, so make one call of the largest M*K on a stream before

@@ -26,9 +26,9 @@
 // is multiplied by the exact factor once the MMAs of the earlier K steps
 // have completed).
 //
-// Every CTA loads its own token tile (CTAs run alone, no clusters): the
-// activations are re-read from L2 by each weight tile, which the L2 serves
-// far below its bandwidth at these arithmetic intensities.
+// Every CTA loads its own token tile: the activations are re-read from L2
+// by each weight tile, which the L2 serves far below its bandwidth at these
+// arithmetic intensities.
 //
 // Warp roles (11 warps), per 128-wide K step (half a super-block):
 //   0 = token producer: the step's two 64-wide token boxes (ring released
@@ -42,6 +42,10 @@
 //   2..9 = dequantisers, two per TMEM lane quarter (warp w serves lanes
 //       32*(w%4).. and the K step's weights 64*((w-2)/4)..), then epilogue
 //       (TMEM -> y, half of the token columns each).
+// When the tiles alone would leave SMs idle, K is split (grid z): the
+// splits of a tile form a cluster, each keeps its partial tile in its own
+// shared memory, and each sums a share of the tile over the cluster's CTAs
+// in K order (distributed shared memory; deterministic, no atomics on y).
 // All waits are bounded; on a timeout the CTA stops issuing, drains what it
 // issued, frees TMEM and returns with the status word set.
 #include <cuda.h>
@@ -121,9 +125,9 @@ struct TcParams {
     int64_t RB;        // bytes per weight row
     uint64_t w_end;    // first byte past the matrix
     int M, N;
-    int nsteps;   // 128-wide K steps per split; split z starts at z*nsteps
+    int ksteps;   // 128-wide K steps of the whole product
+    int splits;   // K ranges per tile (grid z); split z takes its share of whole super-steps
     float *y;
-    int atomic;   // split K: add into y instead of storing
     int *status;
     int stop_step;  // the first CTA's token producer issues no step from this one on (failure test hook)
 };
@@ -157,6 +161,23 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The four fp32 at the (16-byte aligned) address of `p` in this CTA's
+// shared memory, read from the shared memory of the cluster's CTA `rank`.
+__device__ __forceinline__ float4 ld_cluster_f32x4(const float *p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -304,7 +325,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BW, m0 = blockIdx.y * BT;
-    const int k_step0 = blockIdx.z * P.nsteps;
+    // this split's K steps [k_step0, k_step0 + nsteps): an even share of the
+    // product's super-steps (Q6_K, Q8_0 load whole super-steps) or K steps
+    constexpr int KU = C::OWN ? 2 : 1;
+    const int ku = P.ksteps / KU;
+    const int k_step0 = KU * static_cast<int>(static_cast<int64_t>(blockIdx.z) * ku / P.splits);
+    const int nsteps = KU * static_cast<int>(static_cast<int64_t>(blockIdx.z + 1) * ku / P.splits) - k_step0;
 
     const uint32_t sX = smem_u32(smem), sR = smem_u32(smem + C::OFF_R);
     const uint32_t bar = smem_u32(smem + C::OFF_BAR);
@@ -358,7 +384,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // the MMA issuer's bounded wait on step `stop` then expires)
             const int stop = (blockIdx.x | blockIdx.y | blockIdx.z) == 0 ? P.stop_step : NO_STOP;
             int issued = 0;
-            for (int kk = 0; kk < P.nsteps && kk < stop; ++kk) {
+            for (int kk = 0; kk < nsteps && kk < stop; ++kk) {
                 const int s = kk % C::X_STAGES;
                 if (kk >= C::X_STAGES &&
                     (*abort_flag || !mbar_wait(bar_x_empty + 8 * s, ((kk / C::X_STAGES) - 1) & 1, P.status))) {
@@ -384,7 +410,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if constexpr (!C::OWN) {
             if (lane == 0) {
                 int issued = 0;
-                for (int kk = 0; kk < P.nsteps; ++kk) {
+                for (int kk = 0; kk < nsteps; ++kk) {
                     const int r = kk % C::R_STAGES;
                     if (kk >= C::R_STAGES &&
                         (*abort_flag || !mbar_wait(bar_r_empty + 8 * r, ((kk / C::R_STAGES) - 1) & 1, P.status))) {
@@ -405,7 +431,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp == W_MMA) {
         // -------------------------------------------------- MMA issuer
         if (lane == 0) {
-            for (int kk = 0; kk < P.nsteps; ++kk) {
+            for (int kk = 0; kk < nsteps; ++kk) {
                 const int s = kk % C::X_STAGES, sa = kk % A_STAGES;
                 if (*abort_flag || !mbar_wait(bar_x_full + 8 * s, (kk / C::X_STAGES) & 1, P.status) ||
                     !mbar_wait(bar_a_full + 8 * sa, (kk / A_STAGES) & 1, P.status)) {
@@ -483,7 +509,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         };
         auto wfac = [&]() { return f == RS::UNSET ? 1.0f : pow2f(f); };
         if constexpr (!C::OWN) {
-            for (int kk = 0; kk < P.nsteps; ++kk) {
+            for (int kk = 0; kk < nsteps; ++kk) {
                 const int r = kk % C::R_STAGES, sa = kk % A_STAGES;
                 bool ok = !*abort_flag;
                 if (ok) ok = mbar_wait(bar_r_full + 8 * r, (kk / C::R_STAGES) & 1, P.status);
@@ -551,7 +577,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             constexpr int SSB = RawStep<T>::BYTES, PW = RawStep<T>::PITCH_W;
             uint8_t *raw = smem + C::OFF_R + quarter * C::RAW_Q;
             const uint32_t p_full = bar_p_full + 8 * quarter, p_empty = bar_p_empty + 8 * quarter;
-            const int nss = P.nsteps / 2;  // super-steps of this CTA (its K range starts on one)
+            const int nss = nsteps / 2;  // super-steps of this CTA (its K range starts on one)
             const int js0 = k_step0 / 2;
             const int nrows = min(32, P.N - (n0 + 32 * quarter));  // rows of the matrix (may be <= 0)
             const uint64_t rows0 = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(n0 + 32 * quarter) * P.RB;
@@ -605,7 +631,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_arrive(p_full);
             if (nss > 1) load(1);
             const uint8_t *row = raw + lane * PW * 4;
-            for (int kk = 0; kk < P.nsteps; ++kk) {
+            for (int kk = 0; kk < nsteps; ++kk) {
                 const int js = kk >> 1, h = kk & 1, sa = kk % A_STAGES;
                 bool ok = !*abort_flag;
                 if (ok && kk >= A_STAGES) ok = mbar_wait(bar_a_empty + 8 * sa, ((kk / A_STAGES) - 1) & 1, P.status);
@@ -753,32 +779,73 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-        // epilogue: TMEM lanes of this quarter, token columns of this warp's half
+        // epilogue: TMEM lanes of this quarter, token columns of this warp's
+        // half, into y (one split) or into this CTA's partial tile in shared
+        // memory (split K: the rings are idle once the accumulator is final)
         const bool ok = mbar_wait(bar_acc, 0, P.status);
+        const int ncol = n0 + n;
         if (__all_sync(0xffffffffu, ok) && !*abort_flag) {
             tc_fence_after();
-            const int ncol = n0 + n;
             const float rowf = f == RS::UNSET ? 1.0f : pow2f(-f);
+            float *red = reinterpret_cast<float *>(smem);  // [BT][BW] fp32, token-major
 #pragma unroll 1
             for (int cc = cp * (BT / 2); cc < (cp + 1) * (BT / 2); cc += 16) {
                 float v[16];
                 tmem_ld16(lane_base + static_cast<uint32_t>(cc), v);
-                if (ncol < P.N) {
+                const float *xf = P.xinv + m0 + cc;
+                const int mrem = P.M - (m0 + cc);
+                if (P.splits > 1) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        red[(cc + i) * BW + n] = i < mrem ? v[i] * rowf * __ldg(xf + i) : 0.0f;
+                } else if (ncol < P.N) {
                     float *yc = P.y + static_cast<int64_t>(m0 + cc) * P.N + ncol;
-                    const float *xf = P.xinv + m0 + cc;
-                    const int mrem = P.M - (m0 + cc);
-                    if (P.atomic) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (i < mrem) atomicAdd(yc + static_cast<int64_t>(i) * P.N, v[i] * rowf * __ldg(xf + i));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (i < mrem) yc[static_cast<int64_t>(i) * P.N] = v[i] * rowf * __ldg(xf + i);
-                    }
+                    for (int i = 0; i < 16; ++i)
+                        if (i < mrem) yc[static_cast<int64_t>(i) * P.N] = v[i] * rowf * __ldg(xf + i);
                 }
             }
         }
+    }
+    if (P.splits > 1) {
+        // Split K: the tile's splits are the CTAs of one cluster (along z).
+        // Once every one holds its partial tile in shared memory, CTA r sums
+        // token columns [r*BT/s, (r+1)*BT/s) of the tile over the cluster's
+        // CTAs in rank (= K) order -- a fixed order, so the result is
+        // deterministic -- and writes them to y.  Every thread takes part in
+        // both cluster barriers, also after a failed wait.
+        cluster_sync_all();
+        const int s_ = P.splits, r = static_cast<int>(blockIdx.z);
+        const int c0 = r * BT / s_, c1 = (r + 1) * BT / s_;
+        const float *red = reinterpret_cast<const float *>(smem);
+        // four consecutive weight rows per thread and item; every split's
+        // load of an item is issued before the sum
+        constexpr int MAXS = 8;
+        for (int idx = threadIdx.x; idx < (c1 - c0) * (BW / 4); idx += NTHREADS) {
+            const int c = c0 + idx / (BW / 4), nn = 4 * (idx % (BW / 4));
+            float4 v[MAXS];
+#pragma unroll
+            for (int q = 0; q < MAXS; ++q)
+                if (q < s_) v[q] = ld_cluster_f32x4(red + c * BW + nn, static_cast<uint32_t>(q));
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int q = 0; q < MAXS; ++q)
+                if (q < s_) {
+                    acc.x += v[q].x;
+                    acc.y += v[q].y;
+                    acc.z += v[q].z;
+                    acc.w += v[q].w;
+                }
+            if (m0 + c < P.M) {
+                float *yr = P.y + static_cast<int64_t>(m0 + c) * P.N + n0 + nn;
+                const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (n0 + nn + i < P.N) yr[i] = a4[i];
+            }
+        }
+        // no CTA leaves while another may still read its shared memory
+        cluster_sync_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -794,6 +861,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
     return (type == QMM_Q4_K || type == QMM_Q6_K || type == QMM_Q8_0) && K % 256 == 0 && K >= 256 && N >= 1 && M >= 1 && N <= (int64_t(1) << 30) &&
            M <= (int64_t(1) << 30) && K <= (int64_t(1) << 24) && tensor_map_encoder() != nullptr;
+}
+
+// K splits per tile (cluster size along z, at most 8), only while the tiles
+// alone leave SMs idle: the count that minimises the estimated time, waves
+// of clusters x (K steps per split + a fixed cost of about 6 K steps per
+// CTA, + 1 for the cluster's sum), with the clusters that fit at once taken
+// from the occupancy calculator (a cluster's CTAs must share one GPC).
+// Cached per kernel and cluster size.
+template <int T, int BT>
+int choose_splits(int64_t tiles, int ksteps, int num_sms) {
+    using C = TcCfg<BT, T>;
+    static int fit[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s CTAs resident at once (0: not asked yet)
+    const int kunits = C::OWN ? ksteps / 2 : ksteps;
+    int best = 1;
+    double best_cost = 0.0;
+    for (int s = 1; s <= 8 && s <= kunits; ++s) {
+        if (fit[s] == 0) {
+            int n = 0;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1, 1, s);
+            cfg.blockDim = dim3(NTHREADS);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = s;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<T, BT>, &cfg) != cudaSuccess || n < 1) {
+                (void)cudaGetLastError();
+                n = s == 1 ? num_sms : -1;  // unknown: do not split this way
+            }
+            fit[s] = n;
+        }
+        if (fit[s] < 1) continue;
+        // splitting pays only while the tiles leave SMs idle in one wave
+        if (s > 1 && tiles >= fit[1]) break;
+        const int64_t waves = (tiles + fit[s] - 1) / fit[s];
+        const double cost =
+            static_cast<double>(waves) * (static_cast<double>(ksteps) / s + 6.0 + (s > 1 ? 1.0 : 0.0));
+        if (s == 1 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 template <int T, int BT>
@@ -828,11 +942,10 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     }
     const int nt = static_cast<int>((N + BW - 1) / BW), mt = static_cast<int>((M + BT - 1) / BT);
     const int ksteps = static_cast<int>(K / BK);
-    // Split K in two when the tiles alone would leave most SMs idle (two
-    // contributions per output keep the fp32 result independent of order).
-    // (Q6_K, Q8_0: each half must start on a super-step of two K steps)
-    int splits = 1;
-    if (2 * static_cast<int64_t>(nt) * mt <= num_sms && ksteps % (C::OWN ? 4 : 2) == 0) splits = 2;
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<T, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int splits = choose_splits<T, BT>(static_cast<int64_t>(nt) * mt, ksteps, num_sms);
     TcParams P;
     P.W = static_cast<const uint8_t *>(W);
     P.xinv = xinv;
@@ -841,22 +954,22 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     P.M = static_cast<int>(M);
     P.N = static_cast<int>(N);
     P.y = y;
-    P.atomic = splits > 1;
+    P.ksteps = ksteps;
+    P.splits = splits;
     P.status = status;
     P.stop_step = inject_stop_stage();
-    if (splits > 1) {
-        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(M * N) * sizeof(float), st);
-        if (e != cudaSuccess) return e;
-    }
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<T, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    P.nsteps = ksteps / splits;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nt, mt, splits);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T, BT>, tx, th, tq, P);
 }
 

@@ -626,15 +626,22 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
 
     // The next kernel on the stream may start launching now.  Until the
     // preceding kernel completes (it may produce x) this CTA only warms L2:
-    // each warp's first stages of weights (which no kernel of the stream
+    // each warp's first stages of weights (which no kernel of the library
     // writes) and x (an L2 prefetch cannot leave a stale copy; x itself is
     // read after the wait), so the weight stream of this call overlaps the
     // tail of the last one.  After the wait: this thread's activation loads,
-    // and only then the weight stream into shared memory, so the loads do
-    // not return behind tens of KB of bulk copies into this SM.
+    // and only then the rest of the weight stream into shared memory, so the
+    // loads do not return behind tens of KB of bulk copies into this SM.
     pdl_trigger();
+    uint64_t pol_w = 0;
+    int issued = 0;
     if (lane == 0) {
-        for (int t = 0; t < min(P.NSW, nst); ++t) {
+        pol_w = policy_evict_first();
+        // Q4_K: the first stage goes into shared memory at once (measured:
+        // 3-6 % off the Q4_K launches; for the other types the copies then
+        // delay x's loads more than they gain)
+        if (T == QMM_Q4_K && nst > 0) issue(0, 0, pol_w), issued = 1;
+        for (int t = issued; t < min(P.NSW, nst); ++t) {
             const int u0 = uw0 + SU * t, u1 = min(u0 + SU, uw1);
             const int a16 = (cta_off + u0 * BB) & ~15;
             int b16 = (cta_off + u1 * BB + 15) & ~15;
@@ -645,13 +652,9 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
     if (threadIdx.x == 32 && P.x_vec && ((P.M * P.K * 4) & 15) == 0)
         bulk_prefetch_l2(P.x, static_cast<uint32_t>(P.M * P.K * 4));
     pdl_wait();
-    uint64_t pol_w = 0;
-    int issued = 0;
     quantize_to_smem<T>(P, smem, [&] {
-        if (lane == 0) {
-            pol_w = policy_evict_first();
+        if (lane == 0)
             for (; issued < min(P.NSW, nst); ++issued) issue(issued, issued, pol_w);
-        }
     });
     __syncthreads();
 
