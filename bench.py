@@ -93,7 +93,7 @@ def load_peaks():
 TRAFFIC_SUMMARY = os.path.join("profiles", "gemv_q6k_lm_head_k2048_n128256.txt")
 # the files whose code makes up the lm_head kernel (qmm_internal.h only
 # declares host launchers)
-TRAFFIC_SOURCES = ("mat_mul_gb300/csrc/gemv_sb.cu", "mat_mul_gb300/csrc/qmm_device.cuh")
+TRAFFIC_SOURCES = ("mat_mul_gb300/csrc/gemv_sb.cuh", "mat_mul_gb300/csrc/qmm_device.cuh")
 
 
 def sources_sha256(paths):
