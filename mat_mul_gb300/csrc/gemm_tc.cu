@@ -60,7 +60,9 @@ namespace qk {
 namespace {
 
 __host__ __device__ constexpr int qk_weights(int t) { return t == QMM_Q8_0 ? 32 : 256; }
-__host__ __device__ constexpr int qk_block_bytes(int t) { return t == QMM_Q8_0 ? 34 : t == QMM_Q6_K ? 210 : 144; }
+__host__ __device__ constexpr int qk_block_bytes(int t) {
+    return t == QMM_Q8_0 ? 34 : t == QMM_Q6_K ? 210 : t == QMM_Q5_K ? 176 : 144;
+}
 
 constexpr int BW = 128, BK = 128;  // weight rows per tile, K per step (half a super-block)
 constexpr int A_STAGES = 4;        // dequantised weight stages in TMEM (64 columns each)
@@ -69,10 +71,19 @@ constexpr int A_COLS = BK / 2;     // two fp16 weights per 32-bit TMEM column
 // 32*(w%4).. and weights 64*((w-2)/4).. of every K step)
 constexpr int W_XLOAD = 0, W_MMA = 1, W_RLOAD = 10;
 constexpr int NTHREADS = 11 * 32;
-constexpr int RAW_ROW = 144;        // one Q4_K super-block per weight row
-constexpr int H_BYTES = BW * 16;    // d, dmin and the 12 scale bytes of each row
-constexpr int Q_BYTES = BW * 64;    // this K step's 64 quant bytes of each row (64-byte swizzle)
-constexpr int R_BYTES = H_BYTES + Q_BYTES;
+// Q4_K and Q5_K raw-weight stages (TMA): per weight row the super-block's
+// head -- d, dmin and the 12 scale bytes (Q4_K: 16 bytes), plus the 32
+// bytes of fifth bits (Q5_K: 48 bytes) -- and this K step's 64 quant bytes
+// (64-byte swizzle)
+template <int T>
+struct RawTma {
+    static constexpr int ROW = T == QMM_Q5_K ? 176 : 144;  // bytes per super-block
+    static constexpr int HB = T == QMM_Q5_K ? 48 : 16;     // head bytes per row
+    static constexpr int QOFF = HB;                        // first quant byte of a super-block
+    static constexpr int H_BYTES = BW * HB;
+    static constexpr int Q_BYTES = BW * 64;
+    static constexpr int R_BYTES = H_BYTES + Q_BYTES;
+};
 
 // Q6_K and Q8_0: rows are not 16-byte multiples, so no tensor map describes
 // them; each dequantiser warp reads the raw bytes of its 32 rows itself with
@@ -97,12 +108,15 @@ struct RawStep<QMM_Q8_0> {
 
 template <int BT, int T>
 struct TcCfg {
-    static constexpr bool OWN = T != QMM_Q4_K;  // the dequantisers copy their own raw bytes
+    static constexpr bool OWN = T != QMM_Q4_K && T != QMM_Q5_K;  // the dequantisers copy their own raw bytes
+    static constexpr int R_BYTES = RawTma<T>::R_BYTES;
     static constexpr int XBOX = BT * 128;   // one 64-wide K box of tokens (128-byte swizzle rows)
     static constexpr int X_BYTES = 2 * XBOX;
     static constexpr int RAW_Q = 32 * RawStep<T>::PITCH_W * 4;  // one super-step of a lane quarter's rows (OWN)
     static constexpr int X_FIT = (232448 - 1536 - 4 * RAW_Q) / X_BYTES;
-    static constexpr int X_STAGES = OWN ? (X_FIT > 8 ? 8 : X_FIT) : (BT == 256 ? 3 : BT == 128 ? 5 : 8);
+    // (Q5_K's larger raw stages leave room for two 256-token stages)
+    static constexpr int X_STAGES =
+        OWN ? (X_FIT > 8 ? 8 : X_FIT) : (BT == 256 ? (T == QMM_Q5_K ? 2 : 3) : BT == 128 ? 5 : 8);
     static constexpr int OFF_R = X_STAGES * X_BYTES;
     static constexpr int R_STAGES_FIT = OWN ? 0 : (232448 - 1536 - OFF_R) / R_BYTES;
     static constexpr int R_STAGES = R_STAGES_FIT > 8 ? 8 : R_STAGES_FIT;
@@ -250,7 +264,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 // normals).
 template <int T>
 struct RowScale {
-    static constexpr int TMAX = T == QMM_Q4_K ? 4 : T == QMM_Q6_K ? 2 : 7;
+    static constexpr int TMAX = T == QMM_Q4_K ? 4 : T == QMM_Q5_K ? 3 : T == QMM_Q6_K ? 2 : 7;
     static constexpr int HEAD = 8;
     static constexpr int NEIGHBOUR = 6;
     static constexpr int UNSET = 1 << 20;  // no non-zero scale seen yet (the accumulator row is zero)
@@ -301,12 +315,13 @@ __device__ __forceinline__ void realign(const uint32_t (&w)[NIN], int o, uint32_
 }
 
 // Four fp16 weights from the four bytes of a quant word (low nibbles, or
-// high ones when hi): w = q*a + nb with q recovered exactly from the fp16
-// bit pattern 0x6400 | q = 1024 + q.  Weights (b0,b1) -> out0, (b2,b3) -> out1.
-__device__ __forceinline__ void dequant4(uint32_t w, bool hi, __half2 a, __half2 nb, uint32_t &out0,
-                                         uint32_t &out1) {
+// high ones when hi; plus, for Q5_K, the fifth bits at bit 4 of each byte):
+// w = q*a + nb with q recovered exactly from the fp16 bit pattern
+// 0x6400 | q = 1024 + q.  Weights (b0,b1) -> out0, (b2,b3) -> out1.
+__device__ __forceinline__ void dequant4(uint32_t w, bool hi, uint32_t fifth, __half2 a, __half2 nb,
+                                         uint32_t &out0, uint32_t &out1) {
     const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
-    const uint32_t m = (hi ? (w >> 4) : w) & 0x0F0F0F0Fu;
+    const uint32_t m = ((hi ? (w >> 4) : w) & 0x0F0F0F0Fu) | fifth;
     uint32_t t0 = __byte_perm(m, 0x64646464u, 0x4140u);
     uint32_t t1 = __byte_perm(m, 0x64646464u, 0x4342u);
     const __half2 w0 = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&t0), k1024), a, nb);
@@ -418,10 +433,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         break;
                     }
                     const int gk = k_step0 + kk;  // half gk&1 of super-block gk>>1
-                    const uint32_t st = sR + r * R_BYTES;
-                    mbar_arrive_expect_tx(bar_r_full + 8 * r, R_BYTES);
-                    tma_load_2d(st, &tmH, (gk >> 1) * RAW_ROW, n0, bar_r_full + 8 * r);
-                    tma_load_2d(st + H_BYTES, &tmQ, (gk >> 1) * RAW_ROW + 16 + 64 * (gk & 1), n0, bar_r_full + 8 * r);
+                    using RT = RawTma<T>;
+                    const uint32_t st = sR + r * RT::R_BYTES;
+                    mbar_arrive_expect_tx(bar_r_full + 8 * r, RT::R_BYTES);
+                    tma_load_2d(st, &tmH, (gk >> 1) * RT::ROW, n0, bar_r_full + 8 * r);
+                    tma_load_2d(st + RT::H_BYTES, &tmQ, (gk >> 1) * RT::ROW + RT::QOFF + 64 * (gk & 1), n0,
+                                bar_r_full + 8 * r);
                     ++issued;
                 }
                 for (int kk = issued > C::R_STAGES ? issued - C::R_STAGES : 0; kk < issued; ++kk)
@@ -519,9 +536,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     break;
                 }
                 tc_fence_after();
+                using RT = RawTma<T>;
                 const int h = (k_step0 + kk) & 1;  // which half of the super-block
-                const uint8_t *st = smem + C::OFF_R + r * R_BYTES;
-                const uint4 hdr = *reinterpret_cast<const uint4 *>(st + 16 * n);
+                const uint8_t *st = smem + C::OFF_R + r * RT::R_BYTES;
+                const uint4 hdr = *reinterpret_cast<const uint4 *>(st + RT::HB * n);
                 // six-bit scales and mins of sub-blocks 4h..4h+3 (byte i: sub-block
                 // 4h+i), GGUF packing
                 uint32_t scw, mw;
@@ -540,7 +558,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float d = d0 * wfac(), dmin = dm0 * wfac();
                 // the quant row: 64 bytes whose 16-byte chunk f sits at f ^ ((n >> 1) & 3)
                 // (TMA 64-byte swizzle), so a quarter warp's loads hit distinct banks
-                const uint8_t *qrow = st + H_BYTES + 64 * n;
+                const uint8_t *qrow = st + RT::H_BYTES + 64 * n;
                 const int sw = (n >> 1) & 3;
                 // chunk cp of 64 weights: quant bytes 32cp..32cp+31, low nibbles
                 // -> sub-block 4h+2cp, high nibbles -> sub-block 4h+2cp+1
@@ -554,11 +572,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // weight l < 32 of the chunk is the low nibble of quant byte l,
                 // weight 32 + l its high nibble; TMEM column i holds weights 2i, 2i+1
                 const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                // Q5_K: the fifth bit of weight l of sub-block j is bit j of byte l
+                // of the fifth-bit plane (bytes 16..47 of the head), moved to bit 4
+                uint32_t qh[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if constexpr (T == QMM_Q5_K) {
+                    const uint4 h0 = *reinterpret_cast<const uint4 *>(st + RT::HB * n + 16);
+                    const uint4 h1 = *reinterpret_cast<const uint4 *>(st + RT::HB * n + 32);
+                    qh[0] = h0.x, qh[1] = h0.y, qh[2] = h0.z, qh[3] = h0.w;
+                    qh[4] = h1.x, qh[5] = h1.y, qh[6] = h1.z, qh[7] = h1.w;
+                }
+                const int jlo = 4 * h + 2 * cp;  // the chunk's two sub-blocks: jlo (low nibbles), jlo + 1
                 uint32_t rr[32];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    dequant4(qw[i], false, ha0, hb0, rr[2 * i], rr[2 * i + 1]);
-                    dequant4(qw[i], true, ha1, hb1, rr[16 + 2 * i], rr[16 + 2 * i + 1]);
+                    const uint32_t f_lo = ((qh[i] >> jlo) & 0x01010101u) << 4;
+                    const uint32_t f_hi = ((qh[i] >> (jlo + 1)) & 0x01010101u) << 4;
+                    dequant4(qw[i], false, f_lo, ha0, hb0, rr[2 * i], rr[2 * i + 1]);
+                    dequant4(qw[i], true, f_hi, ha1, hb1, rr[16 + 2 * i], rr[16 + 2 * i + 1]);
                 }
                 tmem_st32(lane_base + a_col + A_COLS * sa, rr);
                 tmem_wait_st();
@@ -859,7 +889,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
-    return (type == QMM_Q4_K || type == QMM_Q6_K || type == QMM_Q8_0) && K % 256 == 0 && K >= 256 && N >= 1 && M >= 1 && N <= (int64_t(1) << 30) &&
+    return (type == QMM_Q4_K || type == QMM_Q5_K || type == QMM_Q6_K || type == QMM_Q8_0) && K % 256 == 0 &&
+           K >= 256 && N >= 1 && M >= 1 && N <= (int64_t(1) << 30) &&
            M <= (int64_t(1) << 30) && K <= (int64_t(1) << 24) && tensor_map_encoder() != nullptr;
 }
 
@@ -928,11 +959,11 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     }
     // raw weights as bytes [N][row bytes]: 16-byte boxes (super-block header)
     // and 64-byte boxes (one K step's quants, 64-byte swizzle), 128 rows each
-    const int64_t rb = (K / 256) * RAW_ROW;
-    for (int which = 0; which < 2 && T == QMM_Q4_K; ++which) {
+    const int64_t rb = (K / 256) * RawTma<T>::ROW;
+    for (int which = 0; which < 2 && !C::OWN; ++which) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
-        const cuuint32_t box[2] = {which ? 64u : 16u, static_cast<cuuint32_t>(BW)};
+        const cuuint32_t box[2] = {which ? 64u : static_cast<cuuint32_t>(RawTma<T>::HB), static_cast<cuuint32_t>(BW)};
         const cuuint32_t es[2] = {1, 1};
         if (enc(which ? &tq : &th, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, which ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1001,6 +1032,7 @@ cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const 
         return launch_bt<T, 256>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
     };
     if (type == QMM_Q6_K) return run(std::integral_constant<int, QMM_Q6_K>{});
+    if (type == QMM_Q5_K) return run(std::integral_constant<int, QMM_Q5_K>{});
     if (type == QMM_Q8_0) return run(std::integral_constant<int, QMM_Q8_0>{});
     return run(std::integral_constant<int, QMM_Q4_K>{});
 }

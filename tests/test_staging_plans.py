@@ -220,16 +220,24 @@ def test_tc_own_chunk_loads(T, N, K):
 def test_tc_tma_x_coordinates_are_16_byte_multiples(K, BT):
     """Every tiled TMA copy of the prefill starts at an inner coordinate whose
     byte offset is a multiple of 16 (the rule the hardware does not check):
-    the Q4_K header box at 144*sb, its quant box at 144*sb + 16 + 64*half,
-    and the fp16 token boxes at 128*gk + 64*rank elements."""
+    the Q4_K head box (16 bytes) at 144*sb, its quant box at 144*sb + 16 +
+    64*half; the Q5_K head box (48 bytes: head and fifth bits) at 176*sb, its
+    quant box at 176*sb + 48 + 64*half; and the fp16 token boxes at 128*gk
+    and 128*gk + 64 elements.  Box widths are 16-byte multiples too."""
+    for row, head in ((144, 16), (176, 48)):
+        assert head % 16 == 0
+        for gk in range(K // 128):
+            sb, half = gk >> 1, gk & 1
+            for x_bytes in (row * sb, row * sb + head + 64 * half):
+                assert x_bytes % 16 == 0
+            # the quant box lies inside the super-block
+            assert row * sb + head + 64 * half + 64 <= row * (sb + 1)
+        # tensor map strides: the rows are 16-byte multiples
+        assert ((K // 256) * row) % 16 == 0
     for gk in range(K // 128):
-        sb, half = gk >> 1, gk & 1
-        for x_bytes in (144 * sb, 144 * sb + 16 + 64 * half):
-            assert x_bytes % 16 == 0
-        for rank in (0, 1):
-            assert ((gk * 128 + 64 * rank) * 2) % 16 == 0
-    # tensor map strides: the Q4_K rows and the fp16 token rows are 16-byte multiples
-    assert ((K // 256) * 144) % 16 == 0 and (K * 2) % 16 == 0
+        for box in (0, 1):
+            assert ((gk * 128 + 64 * box) * 2) % 16 == 0
+    assert (K * 2) % 16 == 0
 
 
 # ------------------------------------------- qmm_t: replay of the lanes' arithmetic
