@@ -424,7 +424,7 @@ def run_ours(args):
     del g_e2e, g_step
 
     detail = []
-    groups = layer = layer_m = gate_up = kq = None
+    groups = layer = layer_m = gate_up = kq = kv_line = None
     roof = None
     gemm = None
     cpu = None
