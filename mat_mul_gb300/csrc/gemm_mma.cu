@@ -155,13 +155,26 @@ __device__ void load_weights(GemmSmem &S, const uint8_t *__restrict__ W, int64_t
                 S.wsc[r][i] = static_cast<int16_t>((lo | (hi << 4)) - 32);
             }
         }
-        const int h = part;  // half h: weights 128h + 32j + l
-        for (int j = 0; j < 4; ++j)
-            for (int l = 0; l < 32; ++l) {
-                const int low = (B[32 + 32 * h + l] >> (2 * j)) & 3;
-                const int bit = (B[l] >> (4 * h + j)) & 1;
-                dst[128 * h + 32 * j + l] = static_cast<int8_t>(bit ? low : low - 4);
-            }
+        // half h: weights 128h + 32j + l; four weights per 32-bit word: the
+        // low bits (byte l of the 2-bit plane >> 2j) & 3 and the high bit
+        // (mask byte l >> 4h + j) & 1 make q + 4, one SIMD byte subtract q
+        // (the block is 2-byte aligned: its words are read as halves)
+        const int h = part;
+        uint32_t qs[8], hm[8];
+        for (int e = 0; e < 8; ++e) {
+            const uint16_t *p2 = reinterpret_cast<const uint16_t *>(B + 32 + 32 * h + 4 * e);
+            const uint16_t *m2 = reinterpret_cast<const uint16_t *>(B + 4 * e);
+            qs[e] = static_cast<uint32_t>(__ldg(p2)) | (static_cast<uint32_t>(__ldg(p2 + 1)) << 16);
+            hm[e] = static_cast<uint32_t>(__ldg(m2)) | (static_cast<uint32_t>(__ldg(m2 + 1)) << 16);
+        }
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[8];
+            for (int e = 0; e < 8; ++e)
+                w[e] = __vsub4(((qs[e] >> (2 * j)) & 0x03030303u) | (((hm[e] >> (4 * h + j)) & 0x01010101u) << 2),
+                               0x04040404u);
+            *reinterpret_cast<uint4 *>(dst + 128 * h + 32 * j) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(dst + 128 * h + 32 * j + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
     } else if constexpr (T == QMM_Q2_K) {
         if (n >= N) {
             for (int i = part * 128; i < part * 128 + 128; ++i) dst[i] = 0;
@@ -180,10 +193,16 @@ __device__ void load_weights(GemmSmem &S, const uint8_t *__restrict__ W, int64_t
                 S.wm[r][i] = static_cast<int16_t>(B[i] >> 4);
             }
         }
+        // half h: four weights per 32-bit word (the block is 4-byte aligned)
         const int h = part;
-        for (int j = 0; j < 4; ++j)
-            for (int l = 0; l < 32; ++l)
-                dst[128 * h + 32 * j + l] = static_cast<int8_t>((B[16 + 32 * h + l] >> (2 * j)) & 3);
+        uint32_t qs[8];
+        for (int e = 0; e < 8; ++e) qs[e] = __ldg(reinterpret_cast<const uint32_t *>(B + 16 + 32 * h + 4 * e));
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[8];
+            for (int e = 0; e < 8; ++e) w[e] = (qs[e] >> (2 * j)) & 0x03030303u;
+            *reinterpret_cast<uint4 *>(dst + 128 * h + 32 * j) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(dst + 128 * h + 32 * j + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
     } else {
         // Q8_0: this thread covers blocks 4*part .. 4*part+3 of the K step
         for (int bb = 4 * part; bb < 4 * part + 4; ++bb) {
