@@ -636,8 +636,7 @@ def run_ours(args):
                        "decode_M1": {"K": 5120, "N": 17408, "MB": round(nbytes / 1e6, 3), "us": round(t_dec * 1e3, 2),
                                      "GB/s": round(dgbs, 1), "frac_hbm": round(dgbs / peaks["hbm"], 4)},
                        "prefill_M512": {"K": K, "N": N, "us": round(t_pre * 1e3, 1), "TOPS": round(tops, 1),
-                                        "kernel": "tcgen05 (fp16 operands)" if qtype == synth.Q5_K
-                                        else "int8 mma.sync (exact block dots)"}})
+                                        "kernel": "tcgen05 (fp16 operands)"}})
 
         # ---- the value side of attention over a q8_0 KV cache (qmm_t):
         # Qwen3-14B-shaped, 8 cache heads x 32768 positions x head_dim 128,

@@ -61,7 +61,7 @@ namespace {
 
 __host__ __device__ constexpr int qk_weights(int t) { return t == QMM_Q8_0 ? 32 : 256; }
 __host__ __device__ constexpr int qk_block_bytes(int t) {
-    return t == QMM_Q8_0 ? 34 : t == QMM_Q6_K ? 210 : t == QMM_Q5_K ? 176 : 144;
+    return t == QMM_Q8_0 ? 34 : t == QMM_Q6_K ? 210 : t == QMM_Q5_K ? 176 : t == QMM_Q3_K ? 110 : t == QMM_Q2_K ? 84 : 144;
 }
 
 constexpr int BW = 128, BK = 128;  // weight rows per tile, K per step (half a super-block)
@@ -104,6 +104,16 @@ struct RawStep<QMM_Q6_K> {
 template <>
 struct RawStep<QMM_Q8_0> {
     static constexpr int BYTES = 272, CHUNKS = 17, PITCH_W = 68;
+};
+// Q3_K: 110-byte super-blocks (2-byte aligned), 8 chunks from the boundary
+// at or below the start; Q2_K: 84 bytes (4-byte aligned), 6 chunks
+template <>
+struct RawStep<QMM_Q3_K> {
+    static constexpr int BYTES = 110, CHUNKS = 8, PITCH_W = 36;
+};
+template <>
+struct RawStep<QMM_Q2_K> {
+    static constexpr int BYTES = 84, CHUNKS = 6, PITCH_W = 28;
 };
 
 template <int BT, int T>
@@ -264,7 +274,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 // normals).
 template <int T>
 struct RowScale {
-    static constexpr int TMAX = T == QMM_Q4_K ? 4 : T == QMM_Q5_K ? 3 : T == QMM_Q6_K ? 2 : 7;
+    // (Q3_K |w| < 2^7 |d|, Q2_K < 2^6 max(|d|, |dmin|))
+    static constexpr int TMAX =
+        T == QMM_Q4_K ? 4 : T == QMM_Q5_K ? 3 : T == QMM_Q6_K ? 2 : T == QMM_Q2_K ? 8 : 7;
     static constexpr int HEAD = 8;
     static constexpr int NEIGHBOUR = 6;
     static constexpr int UNSET = 1 << 20;  // no non-zero scale seen yet (the accumulator row is zero)
@@ -617,10 +629,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t stg[4 * NT];
             auto load = [&](int js) {
                 const uint64_t seg0 = rows0 + static_cast<uint64_t>(js0 + js) * SSB;
-                // Q6_K: the chunks of the matrix's final super-block may reach
-                // past its end; there each word is loaded only as far as it lies
-                // inside (a 2-byte load for a word that straddles the end)
-                const bool careful = T == QMM_Q6_K && nrows > 0 &&
+                // Q6_K, Q3_K, Q2_K: the chunks of the matrix's final super-block
+                // may reach past its end; there each word is loaded only as far
+                // as it lies inside (a 2-byte load for a word that straddles it)
+                const bool careful = (T == QMM_Q6_K || T == QMM_Q3_K || T == QMM_Q2_K) && nrows > 0 &&
                                      ((seg0 + static_cast<uint64_t>(nrows - 1) * P.RB) & ~uint64_t(15)) + 16 * CH > P.w_end;
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
@@ -729,6 +741,105 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             const __half2 w1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1056), s);
                             rr[16 * qq + 2 * lw] = *reinterpret_cast<const uint32_t *>(&w0);
                             rr[16 * qq + 2 * lw + 1] = *reinterpret_cast<const uint32_t *>(&w1);
+                        }
+                    }
+                } else if constexpr (T == QMM_Q3_K) {
+                    // the super-block starts at this (even) byte of its first chunk
+                    const int dl = static_cast<int>((rows0 + static_cast<uint64_t>(lane) * P.RB +
+                                                     static_cast<uint64_t>(js0 + js) * SSB) & 15);
+                    // weight 128h + 32j + l, j = 2cp + jj: low bits (byte 32 + 32h + l
+                    // >> 2j) & 3, high bit (mask byte l >> 4h + j) & 1, q + 4 = low |
+                    // high << 2; its group 8h + 2j + (l >= 16) = 4G + k with G = 2h + cp,
+                    // k = 2jj + (l >= 16), so one word of scale bytes serves the warp:
+                    // the low (G < 2) or high nibble of byte (G & 1) * 4 + k and the
+                    // pair (byte 8 + k >> 2G) & 3; w = d*(sc - 32) * q
+                    const float d0 = half_bits_to_float(row_word(row, dl + 108));
+                    if (!scale_step(abs_bits(d0), kk)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const float d = d0 * wfac();
+                    const int G = 2 * h + cp;
+                    const uint32_t sw = row_word(row, dl + 96 + 4 * (G & 1)), s8 = row_word(row, dl + 104);
+                    const uint32_t sc4 = (((G & 2) ? (sw >> 4) : sw) & 0x0F0F0F0Fu) | (((s8 >> (2 * G)) & 0x03030303u) << 4);
+                    __half2 sk[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        sk[k] = __float2half2_rn(d * static_cast<float>(static_cast<int>((sc4 >> (8 * k)) & 0xFFu) - 32));
+                    // mask bytes 0..31 lie in chunks 0..2, the 2-bit bytes 32 + 32h ..
+                    // in chunks 2 + 2h .. 4 + 2h
+                    uint32_t wm[12], wq[12], hm[8], qs[8];
+#pragma unroll
+                    for (int c = 0; c < 3; ++c) {
+                        const uint4 vm = *reinterpret_cast<const uint4 *>(row + 16 * c);
+                        const uint4 vq = *reinterpret_cast<const uint4 *>(row + 16 * (2 + 2 * h + c));
+                        wm[4 * c] = vm.x, wm[4 * c + 1] = vm.y, wm[4 * c + 2] = vm.z, wm[4 * c + 3] = vm.w;
+                        wq[4 * c] = vq.x, wq[4 * c + 1] = vq.y, wq[4 * c + 2] = vq.z, wq[4 * c + 3] = vq.w;
+                    }
+                    realign(wm, dl, hm);
+                    realign(wq, dl, qs);
+                    const __half2 k1028 = __half2half2(__ushort_as_half(0x6404));  // 1028 = 1024 + 4
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * cp + jj;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const uint32_t q3 =
+                                ((qs[e] >> (2 * j)) & 0x03030303u) | (((hm[e] >> (4 * h + j)) & 0x01010101u) << 2);
+                            const uint32_t p0 = __byte_perm(q3, 0x64646464u, 0x4140u);
+                            const uint32_t p1 = __byte_perm(q3, 0x64646464u, 0x4342u);
+                            const __half2 sc = sk[2 * jj + (e >> 2)];
+                            const __half2 w0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1028), sc);
+                            const __half2 w1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1028), sc);
+                            rr[16 * jj + 2 * e] = *reinterpret_cast<const uint32_t *>(&w0);
+                            rr[16 * jj + 2 * e + 1] = *reinterpret_cast<const uint32_t *>(&w1);
+                        }
+                    }
+                } else if constexpr (T == QMM_Q2_K) {
+                    // the super-block starts at this (4-byte multiple) byte of its first chunk
+                    const int dl = static_cast<int>((rows0 + static_cast<uint64_t>(lane) * P.RB +
+                                                     static_cast<uint64_t>(js0 + js) * SSB) & 15);
+                    // weight 128h + 32j + l, j = 2cp + jj: q = (byte 16 + 32h + l >> 2j)
+                    // & 3; its group 8h + 4cp + k, k = 2jj + (l >= 16), with scale and
+                    // min the low and high nibble of scale byte 8h + 4cp + k;
+                    // w = (d*sc)*q - dmin*m
+                    // (dl is a multiple of 4: the words are read directly)
+                    const uint32_t dd = *reinterpret_cast<const uint32_t *>(row + dl + 80);  // d | dmin << 16
+                    const float d0 = half_bits_to_float(dd), dm0 = half_bits_to_float(dd >> 16);
+                    if (!scale_step(max(abs_bits(d0), abs_bits(dm0)), kk)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const float d = d0 * wfac(), dmin = dm0 * wfac();
+                    const uint32_t sw = *reinterpret_cast<const uint32_t *>(row + dl + 8 * h + 4 * cp);
+                    __half2 ak[4], bk[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        ak[k] = __float2half2_rn(d * static_cast<float>((sw >> (8 * k)) & 15u));
+                        bk[k] = __float2half2_rn(-(dmin * static_cast<float>((sw >> (8 * k + 4)) & 15u)));
+                    }
+                    // the 2-bit bytes 16 + 32h .. lie in chunks 1 + 2h .. 3 + 2h
+                    uint32_t wq[12], qs[8];
+#pragma unroll
+                    for (int c = 0; c < 3; ++c) {
+                        const uint4 vq = *reinterpret_cast<const uint4 *>(row + 16 * (1 + 2 * h + c));
+                        wq[4 * c] = vq.x, wq[4 * c + 1] = vq.y, wq[4 * c + 2] = vq.z, wq[4 * c + 3] = vq.w;
+                    }
+                    realign(wq, dl, qs);
+                    const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * cp + jj;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const uint32_t q2 = (qs[e] >> (2 * j)) & 0x03030303u;
+                            const uint32_t p0 = __byte_perm(q2, 0x64646464u, 0x4140u);
+                            const uint32_t p1 = __byte_perm(q2, 0x64646464u, 0x4342u);
+                            const int k = 2 * jj + (e >> 2);
+                            const __half2 w0 = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&p0), k1024), ak[k], bk[k]);
+                            const __half2 w1 = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&p1), k1024), ak[k], bk[k]);
+                            rr[16 * jj + 2 * e] = *reinterpret_cast<const uint32_t *>(&w0);
+                            rr[16 * jj + 2 * e + 1] = *reinterpret_cast<const uint32_t *>(&w1);
                         }
                     }
                 } else {
@@ -889,7 +1000,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
-    return (type == QMM_Q4_K || type == QMM_Q5_K || type == QMM_Q6_K || type == QMM_Q8_0) && K % 256 == 0 &&
+    return (type == QMM_Q4_K || type == QMM_Q5_K || type == QMM_Q6_K || type == QMM_Q3_K || type == QMM_Q2_K ||
+            type == QMM_Q8_0) && K % 256 == 0 &&
            K >= 256 && N >= 1 && M >= 1 && N <= (int64_t(1) << 30) &&
            M <= (int64_t(1) << 30) && K <= (int64_t(1) << 24) && tensor_map_encoder() != nullptr;
 }
@@ -1033,6 +1145,8 @@ cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const 
     };
     if (type == QMM_Q6_K) return run(std::integral_constant<int, QMM_Q6_K>{});
     if (type == QMM_Q5_K) return run(std::integral_constant<int, QMM_Q5_K>{});
+    if (type == QMM_Q3_K) return run(std::integral_constant<int, QMM_Q3_K>{});
+    if (type == QMM_Q2_K) return run(std::integral_constant<int, QMM_Q2_K>{});
     if (type == QMM_Q8_0) return run(std::integral_constant<int, QMM_Q8_0>{});
     return run(std::integral_constant<int, QMM_Q4_K>{});
 }

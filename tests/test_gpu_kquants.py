@@ -118,39 +118,43 @@ def test_group_and_gate_up_with_other_k_quants(cuda_lib):
         assert np.all(np.abs(h - ho) <= B), (tg, tu, M)
 
 
+@pytest.mark.parametrize("qtype", KQ)
 @pytest.mark.parametrize("N,K,M", [(300, 1024, 64), (200, 2048, 300), (77, 256, 9), (1000, 4096, 130),
-                                   (129, 5120, 512)])
-def test_q5k_prefill_on_tcgen05_and_int8(cuda_lib, N, K, M):
-    """Q5_K prefill on the tcgen05 kernel (the TMA raw ring with the fifth-bit
-    plane in the head box) and, forced, on the int8 mma.sync kernel; both
-    against the oracle, and the launch count of each path."""
+                                   (129, 5120, 512), (301, 768, 70), (3, 4352, 33)])
+def test_prefill_on_tcgen05_and_int8(cuda_lib, qtype, N, K, M):
+    """Prefill of the other K-quants on the tcgen05 kernel (Q5_K: the TMA raw
+    ring with the fifth-bit plane in the head box; Q3_K, Q2_K: rows staged by
+    the dequantiser warps, ragged matrix ends) and, forced, on the int8
+    mma.sync kernel; both against the oracle."""
     q = cuda_lib
-    W = synth.weights(synth.Q5_K, N, K, seed=N + K + 5)
+    W = synth.weights(qtype, N, K, seed=N + K + 5 + qtype)
     x = synth.activations(M, K, seed=N + M, outlier_frac=0.01)
-    yo, A = O.qmm(synth.Q5_K, W, N, K, x)
+    yo, A = O.qmm(qtype, W, N, K, x)
     for path in (q.PREFILL_AUTO, q.PREFILL_INT8):
         q.set_prefill_path(path)
         try:
-            y = q.qmm(synth.Q5_K, _dev(W), N, K, _dev(x)).cpu().numpy()
+            y = q.qmm(qtype, _dev(W), N, K, _dev(x)).cpu().numpy()
         finally:
             q.set_prefill_path(q.PREFILL_AUTO)
         assert q.qmm_device_status() == 0
-        _assert_bound(y, yo, A, f"Q5_K prefill path {path} N={N} K={K} M={M}")
+        _assert_bound(y, yo, A, f"type {qtype} prefill path {path} N={N} K={K} M={M}")
 
 
-def test_q5k_prefill_any_magnitude_and_scales(cuda_lib):
-    """The Q5_K tcgen05 prefill with x at 1e-30 / 1e30 and with super-block
-    scales spread over the whole fp16 range (the per-row power of two)."""
+@pytest.mark.parametrize("qtype", KQ)
+def test_prefill_any_magnitude_and_scales(cuda_lib, qtype):
+    """The tcgen05 prefill of the other K-quants with x at 1e-30 / 1e30 and
+    with super-block scales spread over the whole fp16 range (the per-row
+    power of two)."""
     q = cuda_lib
     N, K, M = 200, 2048, 96
-    rng = np.random.default_rng(1)
+    rng = np.random.default_rng(1 + qtype)
     nblk = N * (K // 256)
     for scale, spread in ((1e-30, False), (1e30, False), (1.0, True)):
-        W = synth.weights(synth.Q5_K, N, K, seed=9)
+        W = synth.weights(qtype, N, K, seed=9 + qtype)
         if spread:
-            W = synth.with_scale_fields(synth.Q5_K, W, synth.loguniform_f16_bits(rng, nblk, 2.0 ** -24, 6.0e4),
+            W = synth.with_scale_fields(qtype, W, synth.loguniform_f16_bits(rng, nblk, 2.0 ** -24, 6.0e4),
                                         synth.loguniform_f16_bits(rng, nblk, 2.0 ** -24, 6.0e4))
         x = (synth.activations(M, K, seed=3).astype(np.float64) * scale).astype(np.float32)
-        y = q.qmm(synth.Q5_K, _dev(W), N, K, _dev(x)).cpu().numpy().astype(np.float64)
-        yo, A = O.qmm(synth.Q5_K, W, N, K, x)
-        assert np.all(np.abs(y - yo) <= 2e-3 * A + 1e-5 * min(1.0, scale)), (scale, spread)
+        y = q.qmm(qtype, _dev(W), N, K, _dev(x)).cpu().numpy().astype(np.float64)
+        yo, A = O.qmm(qtype, W, N, K, x)
+        assert np.all(np.abs(y - yo) <= 2e-3 * A + 1e-5 * min(1.0, scale)), (qtype, scale, spread)

@@ -118,10 +118,11 @@ def test_qmm_t_counters_and_parts():
 
 # --------------------------------------------- tcgen05 prefill staging
 
-QMM_Q8_0, QMM_Q4_K, QMM_Q6_K = 0, 1, 2
-SSB = {QMM_Q6_K: 210, QMM_Q8_0: 272}
-CHUNKS = {QMM_Q6_K: 14, QMM_Q8_0: 17}
-PITCH_W = {QMM_Q6_K: 60, QMM_Q8_0: 68}
+QMM_Q8_0, QMM_Q4_K, QMM_Q6_K, QMM_Q3_K, QMM_Q2_K = 0, 1, 2, 4, 5
+SSB = {QMM_Q6_K: 210, QMM_Q8_0: 272, QMM_Q3_K: 110, QMM_Q2_K: 84}
+CHUNKS = {QMM_Q6_K: 14, QMM_Q8_0: 17, QMM_Q3_K: 8, QMM_Q2_K: 6}
+PITCH_W = {QMM_Q6_K: 60, QMM_Q8_0: 68, QMM_Q3_K: 36, QMM_Q2_K: 28}
+BLOCK_BYTES_TC = {QMM_Q6_K: 210, QMM_Q3_K: 110, QMM_Q2_K: 84}
 
 
 def tc_smem(BT, T):
@@ -135,7 +136,7 @@ def tc_smem(BT, T):
     return dict(X=X, SMEM=OFF_BAR + 512 + 1024, RAW_Q=RAW_Q)
 
 
-@pytest.mark.parametrize("T", [QMM_Q6_K, QMM_Q8_0])
+@pytest.mark.parametrize("T", [QMM_Q6_K, QMM_Q8_0, QMM_Q3_K, QMM_Q2_K])
 @pytest.mark.parametrize("BT", [64, 128, 256])
 def test_tc_own_shared_memory_plan(T, BT):
     P = tc_smem(BT, T)
@@ -150,14 +151,18 @@ def test_tc_own_shared_memory_plan(T, BT):
 
 @pytest.mark.parametrize("T,N,K", [(QMM_Q6_K, 301, 768), (QMM_Q6_K, 1000, 2048), (QMM_Q6_K, 130, 5120),
                                    (QMM_Q6_K, 77, 256), (QMM_Q6_K, 5120, 17408), (QMM_Q6_K, 3, 4352),
-                                   (QMM_Q8_0, 301, 768), (QMM_Q8_0, 257, 4352), (QMM_Q8_0, 33, 256)])
+                                   (QMM_Q8_0, 301, 768), (QMM_Q8_0, 257, 4352), (QMM_Q8_0, 33, 256),
+                                   (QMM_Q3_K, 301, 768), (QMM_Q3_K, 77, 256), (QMM_Q3_K, 130, 5120),
+                                   (QMM_Q3_K, 3, 4352), (QMM_Q2_K, 301, 768), (QMM_Q2_K, 77, 256),
+                                   (QMM_Q2_K, 1000, 2048), (QMM_Q2_K, 3, 4352)])
 def test_tc_own_chunk_loads(T, N, K):
     """Every 16-byte chunk load of the staging (two warps per quarter, half the
     chunks each) stays inside [W, w_end) unless the careful path is taken, and
     the careful path is taken exactly for the matrix's final super-block
     reaching past the end."""
     ssb, CH = SSB[T], CHUNKS[T]
-    RB = (K // (32 if T == QMM_Q8_0 else 256)) * (34 if T == QMM_Q8_0 else 210)
+    RB = (K // 32) * 34 if T == QMM_Q8_0 else (K // 256) * BLOCK_BYTES_TC[T]
+    odd = T in (QMM_Q6_K, QMM_Q3_K, QMM_Q2_K)  # super-steps not 16-byte multiples
     W = 1 << 24
     w_end = W + N * RB
     nss = K // 256
@@ -170,7 +175,7 @@ def test_tc_own_chunk_loads(T, N, K):
             rows0 = W + (n0 + 32 * quarter) * RB
             for js in range(nss):
                 seg0 = rows0 + js * ssb
-                careful = T == QMM_Q6_K and nrows > 0 and \
+                careful = odd and nrows > 0 and \
                     ((seg0 + (nrows - 1) * RB) & ~15) + 16 * CH > w_end
                 need = False
                 for cp in range(2):
@@ -204,12 +209,28 @@ def test_tc_own_chunk_loads(T, N, K):
                                     # the loaded chunks: the last byte it touches must lie in them
                                     assert (dl & ~3) + 4 * 16 + 3 < 16 * 5   # ql: 16 words from 5 chunks
                                     assert (dl & ~3) + 4 * 8 + 3 < 16 * 3    # qh: 8 words from 3 chunks
+                            elif T == QMM_Q3_K:
+                                dl = seg & 15
+                                assert dl % 2 == 0
+                                for h in range(2):
+                                    # mask words from chunks 0..2, 2-bit words from 2 + 2h .. 4 + 2h
+                                    assert 4 + 2 * h < CH and (dl & ~3) + 4 * 8 + 3 < 16 * 3
+                                # scale words at dl + 96 .. dl + 104 and d at dl + 108, two
+                                # aligned words each
+                                assert ((dl + 108) & ~3) + 8 <= 16 * CH and ((dl + 104) & ~3) + 8 <= 16 * CH
+                            elif T == QMM_Q2_K:
+                                dl = seg & 15
+                                assert dl % 4 == 0
+                                for h in range(2):
+                                    assert 3 + 2 * h < CH  # 2-bit words from chunks 1 + 2h .. 3 + 2h
+                                    assert dl + 8 * h + 4 + 4 <= 16 * CH  # the scale word
+                                assert dl + 80 + 4 <= 16 * CH  # d | dmin
                             else:
                                 assert seg % 16 == 0
                 if careful:
                     careful_seen += 1
-                    assert need or T == QMM_Q6_K
-    if T == QMM_Q6_K and (N * RB) % 16:
+                    assert need or odd
+    if odd and (N * RB) % 16:
         assert careful_seen >= 1
 
 
@@ -446,3 +467,70 @@ def test_tc_q8_0_dequantiser_replay(E):
             for e in range(4):
                 b = (q >> (8 * e)) & 255
                 assert (b - 256 if b > 127 else b) == int(q_or[4 * lw + e])
+
+
+@pytest.mark.parametrize("dl", [0, 2, 4, 6, 8, 10, 12, 14])
+def test_tc_q3k_dequantiser_replay(dl):
+    """A Q3_K super-block staged at byte dl of its 8 chunks: the scale word of
+    the warp's four groups, the realigned mask and 2-bit words and the
+    0x6400 exponent trick give, for every weight of both K steps and both
+    warps of a lane quarter, the oracle's q (-4..3) and signed scale."""
+    blk = synth.weights(synth.Q3_K, 1, 256, seed=dl + 3)
+    buf = np.zeros(144, np.uint8)
+    buf[dl:dl + 110] = blk
+    d_or, sc_or, q_or = O.unpack_q3_k(blk)
+
+    def word(o):
+        return int.from_bytes(bytes(buf[o:o + 4]), "little")
+    assert word(dl + 108) & 0xFFFF == d_or
+    for h in range(2):
+        for cp in range(2):
+            G = 2 * h + cp
+            sw, s8 = word(dl + 96 + 4 * (G & 1)), word(dl + 104)
+            sc4 = (((sw >> 4) if G & 2 else sw) & 0x0F0F0F0F) | (((s8 >> (2 * G)) & 0x03030303) << 4)
+            for k in range(4):
+                assert ((sc4 >> (8 * k)) & 255) - 32 == int(sc_or[8 * h + 4 * cp + k])
+            hm = _realign(_words(buf, 0, 12), dl, 8)
+            qs = _realign(_words(buf, 16 * (2 + 2 * h), 12), dl, 8)
+            for jj in range(2):
+                j = 2 * cp + jj
+                for e in range(8):
+                    q3 = ((qs[e] >> (2 * j)) & 0x03030303) | (((hm[e] >> (4 * h + j)) & 0x01010101) << 2)
+                    for b in range(4):
+                        l = 4 * e + b
+                        p = 128 * h + 32 * j + l
+                        assert ((q3 >> (8 * b)) & 255) - 4 == int(q_or[p]), (h, cp, jj, e, b)
+                        # the scale the kernel applies is group 8h + 4cp + 2jj + (e >= 4)
+                        assert 8 * h + 4 * cp + 2 * jj + (e >> 2) == p // 16
+
+
+@pytest.mark.parametrize("dl", [0, 4, 8, 12])
+def test_tc_q2k_dequantiser_replay(dl):
+    """A Q2_K super-block staged at byte dl (a multiple of 4) of its 6 chunks:
+    d, dmin, the scale/min word of the warp's four groups and the realigned
+    2-bit words give every weight's q, scale and min as the oracle unpacks."""
+    blk = synth.weights(synth.Q2_K, 1, 256, seed=dl + 5)
+    buf = np.zeros(112, np.uint8)
+    buf[dl:dl + 84] = blk
+    d_or, dmin_or, sc_or, m_or, q_or = O.unpack_q2_k(blk)
+
+    def word(o):
+        assert o % 4 == 0
+        return int.from_bytes(bytes(buf[o:o + 4]), "little")
+    dd = word(dl + 80)
+    assert dd & 0xFFFF == d_or and dd >> 16 == dmin_or
+    for h in range(2):
+        for cp in range(2):
+            sw = word(dl + 8 * h + 4 * cp)
+            for k in range(4):
+                g = 8 * h + 4 * cp + k
+                assert (sw >> (8 * k)) & 15 == int(sc_or[g]) and (sw >> (8 * k + 4)) & 15 == int(m_or[g])
+            qs = _realign(_words(buf, 16 * (1 + 2 * h), 12), dl, 8)
+            for jj in range(2):
+                j = 2 * cp + jj
+                for e in range(8):
+                    q2 = (qs[e] >> (2 * j)) & 0x03030303
+                    for b in range(4):
+                        p = 128 * h + 32 * j + 4 * e + b
+                        assert (q2 >> (8 * b)) & 255 == int(q_or[p])
+                        assert 8 * h + 4 * cp + 2 * jj + (e >> 2) == p // 16
