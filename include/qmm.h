@@ -264,11 +264,16 @@ QMM_API int64_t qmm_launch_count(void);
  *   QMM_DECODE_AUTO   : chosen by type and M (default).  Q4_K and Q6_K with
  *                       QMM_TENSOR_MIN_M <= M <= 8 run on the tensor-core
  *                       decode kernel (quantiser + mma.sync, two launches),
- *                       everything else on the block-per-lane dp4a kernel.
+ *                       Q4_K and Q6_K with M <= 2 on the lane-per-row dp4a
+ *                       kernel (one weight row per lane) where its copy
+ *                       sizes suit the shape, everything else on the
+ *                       block-per-lane dp4a kernel.
  *   QMM_DECODE_BLOCK  : the block-per-lane kernel wherever it fits.
  *   QMM_DECODE_TENSOR : the tensor-core kernel for every Q4_K / Q6_K product
  *                       with 2 <= M <= 8 that fits it (Q6_K: K a multiple
- *                       of 512).
+ *                       of 512); M = 1 as with QMM_DECODE_AUTO.
+ *   QMM_DECODE_ROWS   : as QMM_DECODE_AUTO, with the lane-per-row kernel
+ *                       for every Q4_K / Q6_K product with M <= 2 that fits.
  * Results of the paths agree within the accuracy bound of qmm(), not bit
  * for bit.  Returns the previous path, or QMM_EINVAL_SHAPE for an unknown
  * value (nothing changes).  Needs no GPU.
@@ -276,6 +281,7 @@ QMM_API int64_t qmm_launch_count(void);
 #define QMM_DECODE_AUTO 0
 #define QMM_DECODE_BLOCK 1
 #define QMM_DECODE_TENSOR 2
+#define QMM_DECODE_ROWS 3
 #define QMM_TENSOR_MIN_M 3
 QMM_API int qmm_set_decode_path(int path);
 

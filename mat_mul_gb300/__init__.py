@@ -243,7 +243,7 @@ def qmm_launch_count() -> int:
 
 
 # Decode kernel choice (qmm_set_decode_path in the C header).
-DECODE_AUTO, DECODE_BLOCK, DECODE_TENSOR = 0, 1, 2
+DECODE_AUTO, DECODE_BLOCK, DECODE_TENSOR, DECODE_ROWS = 0, 1, 2, 3
 
 
 def set_decode_path(path: int) -> int:

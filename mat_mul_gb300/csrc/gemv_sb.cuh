@@ -459,17 +459,17 @@ __device__ __forceinline__ float absmax(const float (&a)[N]) {
     return t[0];
 }
 
-template <int T, int TPB, int R, class F>
+template <int T, int TPB, int R, int NT, class F>
 __device__ __forceinline__ void quantize_tpb(const SbParams &P, uint8_t *smem, F &&after_loads) {
     constexpr int EPT = 32 / TPB;
     const int nb32 = P.K / 32;
     const int items = P.M * nb32 * TPB;
-    for (int base = 0; base < items; base += R * NTHREADS) {
+    for (int base = 0; base < items; base += R * NT) {
         // every load of this pass first: R items of EPT values per thread
         float a[R][EPT];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int it = base + r * NTHREADS + static_cast<int>(threadIdx.x);
+            const int it = base + r * NT + static_cast<int>(threadIdx.x);
             const bool ok = it < items;
             const int id = ok ? it / TPB : 0;
             const int m = id / nb32, b = id - m * nb32;
@@ -489,7 +489,7 @@ __device__ __forceinline__ void quantize_tpb(const SbParams &P, uint8_t *smem, F
         if (base == 0) after_loads();
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int it = base + r * NTHREADS + static_cast<int>(threadIdx.x);
+            const int it = base + r * NT + static_cast<int>(threadIdx.x);
             const bool ok = it < items;
             const int id = ok ? it / TPB : 0;
             const int part = it & (TPB - 1);
@@ -545,18 +545,19 @@ __device__ __forceinline__ void quantize_tpb(const SbParams &P, uint8_t *smem, F
     }
 }
 
-// after_loads() runs once, after the first pass's activation loads are issued
-// and before their values are used.  The split (threads per block TPB, items
-// per thread R) keeps one pass and the fewest values per thread.
-template <int T, class F>
+// Run by threads 0 .. NT-1 of the CTA.  after_loads() runs once, after the
+// first pass's activation loads are issued and before their values are used.
+// The split (threads per block TPB, items per thread R) keeps one pass and
+// the fewest values per thread.
+template <int T, int NT = NTHREADS, class F>
 __device__ __forceinline__ void quantize_to_smem(const SbParams &P, uint8_t *smem, F &&after_loads) {
     const int total = P.M * (P.K / 32);
-    if (4 * total <= NTHREADS) quantize_tpb<T, 4, 1>(P, smem, after_loads);
-    else if (2 * total <= NTHREADS) quantize_tpb<T, 2, 1>(P, smem, after_loads);
-    else if (total <= NTHREADS) quantize_tpb<T, 1, 1>(P, smem, after_loads);
-    else if (2 * total <= 2 * NTHREADS) quantize_tpb<T, 2, 2>(P, smem, after_loads);
-    else if (2 * total <= 3 * NTHREADS) quantize_tpb<T, 2, 3>(P, smem, after_loads);
-    else quantize_tpb<T, 2, 4>(P, smem, after_loads);
+    if (4 * total <= NT) quantize_tpb<T, 4, 1, NT>(P, smem, after_loads);
+    else if (2 * total <= NT) quantize_tpb<T, 2, 1, NT>(P, smem, after_loads);
+    else if (total <= NT) quantize_tpb<T, 1, 1, NT>(P, smem, after_loads);
+    else if (2 * total <= 2 * NT) quantize_tpb<T, 2, 2, NT>(P, smem, after_loads);
+    else if (2 * total <= 3 * NT) quantize_tpb<T, 2, 3, NT>(P, smem, after_loads);
+    else quantize_tpb<T, 2, 4, NT>(P, smem, after_loads);
 }
 
 // The work of CTA `cta` of one matrix (its share of the rows).  With GATEUP

@@ -234,12 +234,22 @@ int quantize_for_tensor_cores(int dev, cudaStream_t st, const float *x, int64_t 
     return QMM_OK;
 }
 
+// The decode product of this type and shape runs on the lane-per-row kernel
+// (unless the tensor-core one takes it first).
+bool decode_on_rows(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo &di) {
+    if (M < 1 || M > 2 || g_no_mma_gemv) return false;
+    const int path = g_decode_path.load();
+    if (path == QMM_DECODE_BLOCK) return false;
+    if (path != QMM_DECODE_ROWS && !qk::gemv_rows_preferred(type, N, K)) return false;
+    return qk::gemv_rows_fits(type, static_cast<int>(M), K, di.max_smem);
+}
+
 // The decode product of this type and shape runs on the tensor-core kernel.
 bool decode_on_tensor_cores(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo &di) {
     if (M < 2 || M > 8 || g_force_round_gemv) return false;
     const int path = g_decode_path.load();
     if (path == QMM_DECODE_BLOCK) return false;
-    if (path == QMM_DECODE_AUTO && (M < QMM_TENSOR_MIN_M || g_no_mma_gemv)) return false;
+    if ((path == QMM_DECODE_AUTO || path == QMM_DECODE_ROWS) && (M < QMM_TENSOR_MIN_M || g_no_mma_gemv)) return false;
     return qk::gemv_mma_fits(type, static_cast<int>(M), N, K, di.max_smem, di.num_sms);
 }
 }  // namespace
@@ -264,7 +274,7 @@ const char *qmm_last_error(void) { return g_err; }
 int64_t qmm_launch_count(void) { return g_launches.load(); }
 
 int qmm_set_decode_path(int path) {
-    if (path != QMM_DECODE_AUTO && path != QMM_DECODE_BLOCK && path != QMM_DECODE_TENSOR)
+    if (path != QMM_DECODE_AUTO && path != QMM_DECODE_BLOCK && path != QMM_DECODE_TENSOR && path != QMM_DECODE_ROWS)
         return fail(QMM_EINVAL_SHAPE, "unknown decode path %d", path);
     return g_decode_path.exchange(path);
 }
@@ -375,6 +385,13 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
         e = qk::launch_gemv_mma(type, W_blocks, N, K, ws, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
                                 di.status);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core gemv launch");
+        g_launches.fetch_add(1);
+        return QMM_OK;
+    }
+    if (decode_on_rows(type, M, N, K, di)) {
+        e = qk::launch_gemv_rows(type, W_blocks, N, K, x, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
+                                 di.status);
+        if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
         g_launches.fetch_add(1);
         return QMM_OK;
     }
@@ -515,7 +532,21 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
         DeviceInfo di;
         if (int rc = device_info(dev, di)) return rc;
-        // one launch when every entry takes the block-per-lane kernel (an
+        // one launch when every entry takes the lane-per-row kernel
+        bool rows = true;
+        for (int i = 0; i < n; ++i)
+            rows = rows && (Ns[i] == 0 || (decode_on_rows(types[i], M, Ns[i], K, di) &&
+                                           !decode_on_tensor_cores(types[i], M, Ns[i], K, di)));
+        if (rows) {
+            e = qk::launch_gemv_rows_group(n, types, Ws, Ns, K, x, static_cast<int>(M), ys,
+                                           static_cast<cudaStream_t>(stream), di.num_sms, di.max_smem, di.status);
+            if (e == cudaSuccess) {
+                g_launches.fetch_add(1);
+                return QMM_OK;
+            }
+            if (e != cudaErrorNotSupported) return cuda_fail(e, "group gemv launch");
+        }
+        // else one launch when every entry takes the block-per-lane kernel (an
         // entry for the tensor-core one makes them separate calls)
         bool fits = true;
         for (int i = 0; i < n; ++i)

@@ -78,6 +78,22 @@ cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws,
                                  const float *x, int M, float *const *ys, cudaStream_t st, int num_sms,
                                  int max_smem, int *status);
 void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t *need, int num_sms, int *g);
+
+// Lane-per-row decode kernel (gemv_rows.cu): Q4_K and Q6_K, M <= 2, K a
+// multiple of 256; quantises x itself (one launch, no workspace), launched
+// with programmatic dependent launch.  The group launch takes several
+// matrices sharing K and x (CTAs split as in group_ctas);
+// cudaErrorNotSupported when one of them does not fit the kernel's plan.
+bool gemv_rows_fits(int type, int M, int64_t K, int max_smem);
+// Whether the lane-per-row kernel is the faster choice for this matrix (by
+// its copy sizes and the matrix size); qmm_set_decode_path(QMM_DECODE_ROWS)
+// takes it wherever it fits.
+bool gemv_rows_preferred(int type, int64_t N, int64_t K);
+cudaError_t launch_gemv_rows(int type, const void *W, int64_t N, int64_t K, const float *x, int M, float *y,
+                             cudaStream_t st, int num_sms, int max_smem, int *status);
+cudaError_t launch_gemv_rows_group(int n, const int *types, const void *const *Ws, const int64_t *Ns, int64_t K,
+                                   const float *x, int M, float *const *ys, cudaStream_t st, int num_sms,
+                                   int max_smem, int *status);
 // The gate and up products of one MLP (same type and shape, M <= 2) in one
 // launch of the block-per-lane kernel: h = silu(Wg.x) * (Wu.x).
 // cudaErrorNotSupported when the pair does not fit the kernel's plan.
