@@ -86,6 +86,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, letting the thread sleep until the phase completes, for
+// at most SUSPEND_NS nanoseconds per call (a waiting warp then takes no
+// issue slots from the working ones).
+constexpr uint32_t SUSPEND_NS = 10000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(SUSPEND_NS)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, giving up after
 // WAIT_LIMIT_CYCLES; on expiry the status word `status` (device memory owned
 // by the library) records a timeout and the function returns false.
@@ -95,7 +111,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *st
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait_sleep(bar, parity)) return true;
         if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
             atomicOr(status, STATUS_TIMEOUT);
             return false;
