@@ -272,8 +272,9 @@ QMM_API int64_t qmm_launch_count(void);
  *   QMM_DECODE_TENSOR : the tensor-core kernel for every Q4_K / Q6_K product
  *                       with 2 <= M <= 8 that fits it (Q6_K: K a multiple
  *                       of 512); M = 1 as with QMM_DECODE_AUTO.
- *   QMM_DECODE_ROWS   : as QMM_DECODE_AUTO, with the lane-per-row kernel
- *                       for every Q4_K / Q6_K product with M <= 2 that fits.
+ *   QMM_DECODE_ROWS   : the lane-per-row kernel for every product it takes
+ *                       (Q4_K with M <= 8, Q6_K with M <= 2), else as
+ *                       QMM_DECODE_AUTO.
  * Results of the paths agree within the accuracy bound of qmm(), not bit
  * for bit.  Returns the previous path, or QMM_EINVAL_SHAPE for an unknown
  * value (nothing changes).  Needs no GPU.

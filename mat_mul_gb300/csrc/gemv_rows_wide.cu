@@ -1,0 +1,25 @@
+// gemv_rows_wide.cu -- the lane-per-row decode kernel (gemv_rows.cuh) for
+// 3 <= M <= 8 activation rows, Q4_K: the same stages and lanes, MT = 4 or 8
+// accumulators per lane (rows M .. MT-1 of the activations are computed on
+// and never written).  A translation unit of its own so that it compiles in
+// parallel with the M <= 2 instantiations.
+#include "gemv_rows.cuh"
+
+namespace qk {
+namespace rwk {
+
+cudaError_t launch_rows_wide(const RwParams &R, int MT, int CW, int H, int grid, int smem, cudaStream_t st) {
+    if (R.q.type != QMM_Q4_K) return cudaErrorNotSupported;
+    return MT == 4 ? launch_single<QMM_Q4_K, 4>(R, CW, H, grid, smem, st)
+                   : launch_single<QMM_Q4_K, 8>(R, CW, H, grid, smem, st);
+}
+
+cudaError_t launch_rows_wide_group(const RwGroup &G, int MT, int CW, int H, int grid, int smem, cudaStream_t st) {
+    for (int i = 0; i < G.n; ++i)
+        if (G.p[i].q.type != QMM_Q4_K) return cudaErrorNotSupported;
+    return MT == 4 ? launch_group<4, false>(G, CW, H, grid, smem, st)
+                   : launch_group<8, false>(G, CW, H, grid, smem, st);
+}
+
+}  // namespace rwk
+}  // namespace qk

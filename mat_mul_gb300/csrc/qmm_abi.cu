@@ -237,12 +237,15 @@ int quantize_for_tensor_cores(int dev, cudaStream_t st, const float *x, int64_t 
 // The decode product of this type and shape runs on the lane-per-row kernel
 // (unless the tensor-core one takes it first).
 bool decode_on_rows(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo &di) {
-    if (M < 1 || M > 2 || g_no_mma_gemv) return false;
+    if (M < 1 || M > 8 || g_no_mma_gemv) return false;
     const int path = g_decode_path.load();
     if (path == QMM_DECODE_BLOCK) return false;
-    if (path != QMM_DECODE_ROWS && !qk::gemv_rows_preferred(type, N, K)) return false;
+    if (path != QMM_DECODE_ROWS && (M > 2 || !qk::gemv_rows_preferred(type, N, K))) return false;
     return qk::gemv_rows_fits(type, static_cast<int>(M), K, di.max_smem);
 }
+
+// Under QMM_DECODE_ROWS the lane-per-row kernel goes before the tensor-core one.
+bool rows_first() { return g_decode_path.load() == QMM_DECODE_ROWS; }
 
 // The decode product of this type and shape runs on the tensor-core kernel.
 bool decode_on_tensor_cores(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo &di) {
@@ -379,7 +382,7 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     //   gemm : prefill after the quantiser: on tcgen05 (fp16 operands, fp32
     //          accumulators) when K is a multiple of 256, else on the int8
     //          mma.sync kernel
-    if (decode_on_tensor_cores(type, M, N, K, di)) {
+    if (!(rows_first() && decode_on_rows(type, M, N, K, di)) && decode_on_tensor_cores(type, M, N, K, di)) {
         void *ws = nullptr;
         if (int rc = quantize_for_tensor_cores(dev, st, x, M, K, di, &ws)) return rc;
         e = qk::launch_gemv_mma(type, W_blocks, N, K, ws, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
@@ -536,7 +539,7 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
         bool rows = true;
         for (int i = 0; i < n; ++i)
             rows = rows && (Ns[i] == 0 || (decode_on_rows(types[i], M, Ns[i], K, di) &&
-                                           !decode_on_tensor_cores(types[i], M, Ns[i], K, di)));
+                                           (rows_first() || !decode_on_tensor_cores(types[i], M, Ns[i], K, di))));
         if (rows) {
             e = qk::launch_gemv_rows_group(n, types, Ws, Ns, K, x, static_cast<int>(M), ys,
                                            static_cast<cudaStream_t>(stream), di.num_sms, di.max_smem, di.status);

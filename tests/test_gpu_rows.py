@@ -49,7 +49,15 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("qtype,N,K,M", CASES)
+# Q4_K with 3 <= M <= 8: four or eight accumulators per lane (the rows of
+# the activations past M are computed on and never written)
+CASES_WIDE = [
+    (synth.Q4_K, 1, 256, 3), (synth.Q4_K, 33, 2048, 4), (synth.Q4_K, 300, 4608, 5), (synth.Q4_K, 4865, 5120, 8),
+    (synth.Q4_K, 200, 10240, 6), (synth.Q4_K, 77, 1024, 7), (synth.Q4_K, 5, 5120, 4),
+]
+
+
+@pytest.mark.parametrize("qtype,N,K,M", CASES + CASES_WIDE)
 def test_rows_decode_matches_oracle(cuda_lib, rows_path, qtype, N, K, M):
     q = cuda_lib
     W = synth.weights(qtype, N, K, seed=3 * N + K + M)
@@ -110,3 +118,21 @@ def test_rows_and_block_paths_agree_within_the_bound(cuda_lib):
     # both take exact int32 block dots: only the fp32 order of the scaled
     # sums differs
     assert np.all(np.abs(y_rows.astype(np.float64) - y_block) <= REL * A + ABS)
+
+
+@pytest.mark.parametrize("M", [4, 8])
+def test_rows_group_one_launch_wide(cuda_lib, rows_path, M):
+    q = cuda_lib
+    K = 5120
+    items = [(synth.Q4_K, 5120), (synth.Q4_K, 1024), (synth.Q4_K, 0), (synth.Q4_K, 77)]
+    Ws = [synth.weights(t, N, K, seed=80 + i) for i, (t, N) in enumerate(items)]
+    x = synth.activations(M, K, seed=81 + M, outlier_frac=0.01)
+    before = q.qmm_launch_count()
+    ys = q.qmm_group([(t, _dev(W), N) for (t, N), W in zip(items, Ws)], K, _dev(x))
+    assert q.qmm_launch_count() - before == 1
+    assert q.qmm_device_status() == 0
+    for (t, N), W, y in zip(items, Ws, ys):
+        if N == 0:
+            continue
+        yo, A = O.qmm(t, W, N, K, x)
+        _check(y.cpu().numpy(), yo, A, f"group entry N={N} M={M}")
