@@ -7,9 +7,9 @@ namespace qk {
 using namespace rwk;
 
 bool gemv_rows_fits(int type, int M, int64_t K, int max_smem) {
-    // Q4_K for M <= 8, Q6_K for M <= 2
-    if ((type != QMM_Q4_K && type != QMM_Q6_K) || M < 1 || M > (type == QMM_Q4_K ? 8 : 2) || K < 256 ||
-        K % 256 != 0 || K > (1 << 22))
+    // Q4_K for M <= 8, Q5_K and Q6_K for M <= 2
+    if ((type != QMM_Q4_K && type != QMM_Q5_K && type != QMM_Q6_K) || M < 1 || M > (type == QMM_Q4_K ? 8 : 2) ||
+        K < 256 || K % 256 != 0 || K > (1 << 22))
         return false;
     const Shape sh = choose_shape(K / 256, block_bytes(type));
     RwParams R = {};
@@ -21,7 +21,7 @@ bool gemv_rows_preferred(int type, int64_t N, int64_t K) {
     // Q6_K rows are 2-byte aligned and read as 32-bit words: at any 16-byte
     // row pitch, 32 lanes on GR rows meet GR/8-way bank conflicts, which the
     // block-per-lane kernel (lanes on consecutive blocks) does not have
-    if (type != QMM_Q4_K) return false;
+    if (type != QMM_Q4_K && type != QMM_Q5_K) return false;
     // below full copy efficiency the block-per-lane kernel's long contiguous
     // copies win on large matrices; small ones gain from the shorter setup
     const Shape sh = choose_shape(K / 256, block_bytes(type));
@@ -49,6 +49,9 @@ cudaError_t launch_gemv_rows(int type, const void *W, int64_t N, int64_t K, cons
     if (type == QMM_Q4_K)
         return M <= 1 ? launch_single<QMM_Q4_K, 1>(R, sh.CW, sh.H, g, smem, st)
                       : launch_single<QMM_Q4_K, 2>(R, sh.CW, sh.H, g, smem, st);
+    if (type == QMM_Q5_K)
+        return M <= 1 ? launch_single<QMM_Q5_K, 1>(R, sh.CW, sh.H, g, smem, st)
+                      : launch_single<QMM_Q5_K, 2>(R, sh.CW, sh.H, g, smem, st);
     return M <= 1 ? launch_single<QMM_Q6_K, 1>(R, sh.CW, sh.H, g, smem, st)
                   : launch_single<QMM_Q6_K, 2>(R, sh.CW, sh.H, g, smem, st);
 }
@@ -62,7 +65,9 @@ cudaError_t launch_gemv_rows_group(int n, const int *types, const void *const *W
     Shape sh = {};
     for (int i = 0; i < n; ++i) {
         if (Ns[i] <= 0) continue;
-        if (!gemv_rows_fits(types[i], M, K, max_smem)) return cudaErrorNotSupported;
+        // the group launch takes Q4_K and Q6_K
+        if ((types[i] != QMM_Q4_K && types[i] != QMM_Q6_K) || !gemv_rows_fits(types[i], M, K, max_smem))
+            return cudaErrorNotSupported;
         const int64_t b = Ns[i] * (K / 256) * block_bytes(types[i]);
         if (b > most) most = b, sh = choose_shape(K / 256, block_bytes(types[i]));
     }

@@ -1,6 +1,6 @@
 // gemv_rows.cuh -- the lane-per-row decode kernel (device code, shared-memory
-// plan and launch templates), instantiated by gemv_rows.cu (M <= 2, Q4_K and
-// Q6_K) and gemv_rows_wide.cu (3 <= M <= 8, Q4_K): decode product
+// plan and launch templates), instantiated by gemv_rows.cu (M <= 2, Q4_K,
+// Q5_K and Q6_K) and gemv_rows_wide.cu (3 <= M <= 8, Q4_K): decode product
 // y[M,N] = W[N,K] . x[M,K]^T with one weight row per lane.
 //
 // Design (sm_103a):
@@ -71,6 +71,7 @@ struct RwGroup {
 template <int T, int MT>
 __device__ __forceinline__ void superblock(const XS &X, int blk, int kb, float (&v)[MT]) {
     if constexpr (T == QMM_Q4_K) sb_q4k<MT>(X, blk, kb, v);
+    else if constexpr (T == QMM_Q5_K) sb_q5k<MT>(X, blk, kb, v);
     else sb_q6k<MT>(X, blk, kb, v);
 }
 
@@ -292,7 +293,7 @@ inline bool plan_rows(int type, int M, int64_t K, int max_smem, int CW, int H, R
     const int GR = 32 / H;
     const int64_t nb = K / 256;
     const int64_t q_ld = nb * XPITCH;
-    const int64_t meta_ld = nb * (type == QMM_Q4_K ? Rec<QMM_Q4_K>::B : Rec<QMM_Q6_K>::B);
+    const int64_t meta_ld = nb * (type == QMM_Q4_K || type == QMM_Q5_K ? Rec<QMM_Q4_K>::B : Rec<QMM_Q6_K>::B);
     // a row's span: CW*H super-blocks from an offset of up to 15 bytes into
     // its first 16-byte chunk, rounded out; an odd number of chunks
     const int64_t CH = static_cast<int64_t>(CW) * H;

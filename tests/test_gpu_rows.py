@@ -1,5 +1,5 @@
-"""GPU parity of the lane-per-row decode kernel (Q4_K and Q6_K at M <= 2,
-the default decode path there) against the CPU oracle, within the library's
+"""GPU parity of the lane-per-row decode kernel (Q4_K, Q5_K and Q6_K at
+M <= 2, Q4_K up to M = 8) against the CPU oracle, within the library's
 bound |y_gpu - y_oracle| <= 2e-3 * sum_k |w_k xhat_k| + 1e-5.
 
 The shapes cover what the kernel's plan and indexing branch on: a CTA's row
@@ -46,6 +46,8 @@ CASES = [
     (synth.Q6_K, 1, 256, 1), (synth.Q6_K, 3, 512, 2), (synth.Q6_K, 77, 2048, 1), (synth.Q6_K, 33, 2560, 2),
     (synth.Q6_K, 301, 4608, 2), (synth.Q6_K, 4097, 5120, 1), (synth.Q6_K, 150, 17408, 1),
     (synth.Q6_K, 120, 17408, 2),
+    (synth.Q5_K, 1, 256, 1), (synth.Q5_K, 77, 2048, 2), (synth.Q5_K, 300, 5120, 1), (synth.Q5_K, 4097, 5120, 2),
+    (synth.Q5_K, 150, 17408, 1),
 ]
 
 
