@@ -151,6 +151,8 @@ struct TcParams {
     int M, N;
     int ksteps;   // 128-wide K steps of the whole product
     int splits;   // K ranges per tile (grid z); split z takes its share of whole super-steps
+    int tile0;    // this launch's first tile (tiles numbered token-tile-major: t = mt * nt + n-tile)
+    int nt;       // weight-row tiles
     float *y;
     int *status;
     int stop_step;  // the first CTA's token producer issues no step from this one on (failure test hook)
@@ -351,7 +353,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // stages need 1024-byte alignment for the 128-byte swizzle
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BW, m0 = blockIdx.y * BT;
+    const int tile = P.tile0 + static_cast<int>(blockIdx.x);
+    const int n0 = (tile % P.nt) * BW, m0 = (tile / P.nt) * BT;
     // this split's K steps [k_step0, k_step0 + nsteps): an even share of the
     // product's super-steps (Q6_K, Q8_0 load whole super-steps) or K steps
     constexpr int KU = C::OWN ? 2 : 1;
@@ -403,13 +406,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // a launch of the remaining tiles that follows this one on the stream
+    // (the split second part of a two-part schedule) may start as SMs free
+    pdl_trigger();
 
     if (warp == W_XLOAD) {
         // ------------------------------------------ token tile producer
         if (lane == 0) {
             // steps from `stop` on are never issued (only with the test hook:
             // the MMA issuer's bounded wait on step `stop` then expires)
-            const int stop = (blockIdx.x | blockIdx.y | blockIdx.z) == 0 ? P.stop_step : NO_STOP;
+            const int stop = P.tile0 == 0 && (blockIdx.x | blockIdx.z) == 0 ? P.stop_step : NO_STOP;
             int issued = 0;
             for (int kk = 0; kk < nsteps && kk < stop; ++kk) {
                 const int s = kk % C::X_STAGES;
@@ -997,6 +1003,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
                      : "memory");
     }
+    // The second part of a two-part schedule reads nothing the first part
+    // writes (disjoint tiles of y, the same inputs, complete before the first
+    // part started); it ends only after the first part has, so that what
+    // follows on the stream sees both.  (No-op when launched without the
+    // programmatic dependency.)
+    pdl_wait();
 }
 
 bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
@@ -1012,33 +1024,43 @@ bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
 // CTA, + 1 for the cluster's sum), with the clusters that fit at once taken
 // from the occupancy calculator (a cluster's CTAs must share one GPC).
 // Cached per kernel and cluster size.
+// Clusters of s CTAs of the kernel resident at once (cached; -1: unknown,
+// do not split this way).
+template <int T, int BT>
+int clusters_resident(int s, int num_sms) {
+    using C = TcCfg<BT, T>;
+    static int fit[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // 0: not asked yet
+    if (fit[s] == 0) {
+        int n = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, s);
+        cfg.blockDim = dim3(NTHREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<T, BT>, &cfg) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = s == 1 ? num_sms : -1;
+        }
+        fit[s] = n;
+    }
+    return fit[s];
+}
+
 template <int T, int BT>
 int choose_splits(int64_t tiles, int ksteps, int num_sms) {
     using C = TcCfg<BT, T>;
-    static int fit[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // clusters of s CTAs resident at once (0: not asked yet)
     const int kunits = C::OWN ? ksteps / 2 : ksteps;
     int best = 1;
     double best_cost = 0.0;
+    int fit[9];
     for (int s = 1; s <= 8 && s <= kunits; ++s) {
-        if (fit[s] == 0) {
-            int n = 0;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(1, 1, s);
-            cfg.blockDim = dim3(NTHREADS);
-            cfg.dynamicSmemBytes = C::SMEM_BYTES;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 1;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = s;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<T, BT>, &cfg) != cudaSuccess || n < 1) {
-                (void)cudaGetLastError();
-                n = s == 1 ? num_sms : -1;  // unknown: do not split this way
-            }
-            fit[s] = n;
-        }
+        fit[s] = clusters_resident<T, BT>(s, num_sms);
         if (fit[s] < 1) continue;
         // splitting pays only while the tiles leave SMs idle in one wave
         if (s > 1 && tiles >= fit[1]) break;
@@ -1088,7 +1110,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     cudaError_t e =
         cudaFuncSetAttribute(gemm_tc_kernel<T, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int splits = choose_splits<T, BT>(static_cast<int64_t>(nt) * mt, ksteps, num_sms);
+    const int64_t tiles = static_cast<int64_t>(nt) * mt;
     TcParams P;
     P.W = static_cast<const uint8_t *>(W);
     P.xinv = xinv;
@@ -1098,22 +1120,48 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     P.N = static_cast<int>(N);
     P.y = y;
     P.ksteps = ksteps;
-    P.splits = splits;
+    P.nt = nt;
     P.status = status;
     P.stop_step = inject_stop_stage();
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nt, mt, splits);
-    cfg.blockDim = dim3(NTHREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = splits;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T, BT>, tx, th, tq, P);
+    // tiles [tile0, tile0 + count) in clusters of `splits` along K; with
+    // `after` the launch may start while the one before it on the stream
+    // still runs (programmatic dependent launch)
+    auto launch = [&](int64_t tile0, int64_t count, int splits, bool after) {
+        P.tile0 = static_cast<int>(tile0);
+        P.splits = splits;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(count), 1, splits);
+        cfg.blockDim = dim3(NTHREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = splits;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = after ? 2 : 1;
+        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T, BT>, tx, th, tq, P);
+    };
+    // Two parts when the tiles leave the last wave partly empty: the whole
+    // waves unsplit, then the remaining tiles split along K (clusters) so
+    // that they fill the SMs the first part frees.
+    const int fit1 = clusters_resident<T, BT>(1, num_sms);
+    if (fit1 > 0 && tiles > fit1 && tiles % fit1 != 0) {
+        const int64_t full = tiles / fit1 * fit1, rest = tiles - full;
+        const int s_rest = choose_splits<T, BT>(rest, ksteps, num_sms);
+        if (s_rest > 1) {
+            cudaError_t e2 = launch(0, full, 1, false);
+            if (e2 != cudaSuccess) return e2;
+            P.stop_step = NO_STOP;
+            e2 = launch(full, rest, s_rest, true);
+            if (e2 == cudaSuccess) count_launches(1);
+            return e2;
+        }
+    }
+    return launch(0, tiles, choose_splits<T, BT>(tiles, ksteps, num_sms), false);
 }
 
 }  // namespace
