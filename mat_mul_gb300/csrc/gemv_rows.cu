@@ -1,4 +1,4 @@
-// gemv_rows.cu -- the lane-per-row decode kernel (gemv_rows.cuh has the
+// gemv_rows.cu -- the row-per-lane decode kernel (gemv_rows.cuh has the
 // design) for M <= 2, Q4_K and Q6_K, and the entry points of every M.
 #include "gemv_rows.cuh"
 

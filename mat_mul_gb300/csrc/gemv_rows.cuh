@@ -1,4 +1,4 @@
-// gemv_rows.cuh -- the lane-per-row decode kernel (device code, shared-memory
+// gemv_rows.cuh -- the row-per-lane decode kernel (device code, shared-memory
 // plan and launch templates), instantiated by gemv_rows.cu (M <= 2, Q4_K,
 // Q5_K and Q6_K) and gemv_rows_wide.cu (3 <= M <= 8, Q4_K): decode product
 // y[M,N] = W[N,K] . x[M,K]^T with one weight row per lane.

@@ -1,4 +1,4 @@
-// gemv_rows_wide.cu -- the lane-per-row decode kernel (gemv_rows.cuh) for
+// gemv_rows_wide.cu -- the row-per-lane decode kernel (gemv_rows.cuh) for
 // 3 <= M <= 8 activation rows, Q4_K: the same stages and lanes, MT = 4 or 8
 // accumulators per lane (rows M .. MT-1 of the activations are computed on
 // and never written).  A translation unit of its own so that it compiles in

@@ -234,7 +234,7 @@ int quantize_for_tensor_cores(int dev, cudaStream_t st, const float *x, int64_t 
     return QMM_OK;
 }
 
-// The decode product of this type and shape runs on the lane-per-row kernel
+// The decode product of this type and shape runs on the row-per-lane kernel
 // (unless the tensor-core one takes it first).
 bool decode_on_rows(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo &di) {
     if (M < 1 || M > 8 || g_no_mma_gemv) return false;
@@ -244,7 +244,7 @@ bool decode_on_rows(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo 
     return qk::gemv_rows_fits(type, static_cast<int>(M), K, di.max_smem);
 }
 
-// Under QMM_DECODE_ROWS the lane-per-row kernel goes before the tensor-core one.
+// Under QMM_DECODE_ROWS the row-per-lane kernel goes before the tensor-core one.
 bool rows_first() { return g_decode_path.load() == QMM_DECODE_ROWS; }
 
 // The decode product of this type and shape runs on the tensor-core kernel.
@@ -535,7 +535,7 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
         DeviceInfo di;
         if (int rc = device_info(dev, di)) return rc;
-        // one launch when every entry takes the lane-per-row kernel
+        // one launch when every entry takes the row-per-lane kernel
         bool rows = true;
         for (int i = 0; i < n; ++i)
             rows = rows && (Ns[i] == 0 || (decode_on_rows(types[i], M, Ns[i], K, di) &&

@@ -1,4 +1,4 @@
-"""GPU parity of the lane-per-row decode kernel (Q4_K, Q5_K and Q6_K at
+"""GPU parity of the row-per-lane decode kernel (Q4_K, Q5_K and Q6_K at
 M <= 2, Q4_K up to M = 8) against the CPU oracle, within the library's
 bound |y_gpu - y_oracle| <= 2e-3 * sum_k |w_k xhat_k| + 1e-5.
 
