@@ -30,7 +30,9 @@ def _rows(N, seed):
 
 # (type, N, K, M): 128-row weight tiles x 256-token tiles; tiles beyond a
 # multiple of the CTAs resident at once (one per SM) form the split part
-CASES = [(synth.Q4_K, 20000, 1024, 300), (synth.Q6_K, 20000, 2048, 300), (synth.Q4_K, 14336, 4096, 512)]
+CASES = [(synth.Q4_K, 20000, 1024, 300), (synth.Q6_K, 20000, 2048, 300), (synth.Q4_K, 14336, 4096, 512),
+         # 153 tiles: one past a full wave, the last tile split the most ways
+         (synth.Q4_K, 19584, 1024, 200), (synth.Q6_K, 19584, 2048, 100)]
 
 
 @pytest.mark.parametrize("qtype,N,K,M", CASES)
