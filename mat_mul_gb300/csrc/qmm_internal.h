@@ -137,7 +137,7 @@ cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const
 // sum_n x[h][m][n] * w[h][n][k], K a multiple of 32 up to 256.  part: the
 // workspace of qmm_t_part_bytes() bytes; count: H unsigned counters that are
 // zero before the call and are left zero by it.  One launch per 16 rows of x.
-int64_t qmm_t_chunk_rows(int64_t H, int64_t N, int num_sms);
+int64_t qmm_t_chunk_rows(int64_t H, int64_t N, int64_t K, int num_sms);
 size_t qmm_t_part_bytes(int64_t H, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_qmm_t(const void *W, int64_t H, int64_t N, int64_t K, const float *x, int64_t M, float *y,
                          float *part, unsigned *count, cudaStream_t st, int num_sms, int *status);

@@ -7,10 +7,13 @@
 // heads that share the cache head.
 //
 // Memory-bound: every weight byte is read once.  Each CTA owns a contiguous
-// range of one matrix's rows (a chunk), split evenly between its eight warps;
-// each warp streams its rows through a private ring of shared-memory stages
-// with bulk async copies (its lane 0 refills a stage as soon as the warp has
-// read it), so 8 copy streams per SM keep the bytes in flight.  A warp
+// range of one matrix's rows (a chunk), split evenly between its warps
+// (sixteen for K <= 160, eight beyond, where a lane's accumulators need more
+// than the 128 registers of a 512-thread block); each warp streams its rows
+// through a private ring of shared-memory stages of about 4 KB with bulk
+// async copies (its lane 0 refills a stage as soon as the warp has read it),
+// so 16 (8) copy streams per SM keep the bytes in flight.  The contraction is
+// issue-bound: four warps per scheduler hide its latencies better than two.  A warp
 // contracts 16 rows at a time on the tensor cores (mma.sync m16n8k16, fp16
 // operands, fp32 accumulation):
 //   A (16 x 16) = x[m][n] * 2^e for the 16 positions n (rows m >= M zero),
@@ -28,10 +31,11 @@
 // holding 2*CPG consecutive columns; for the other K the MMA j (0..3) of
 // block b covers columns 32b + 4g + j, a 4-byte group per row and block.
 // Reduction, in a fixed order so that the result is bitwise reproducible:
-// the eight warps' sums are added in warp order in shared memory and scaled
-// back, each CTA writes its chunk sum to the workspace, and the CTA that
-// finishes a matrix last (a counter per matrix, reset by that CTA) adds the
-// chunk sums in chunk order and writes y.
+// the warps' sums, scaled back, meet in shared memory (with W warps, warp
+// w + W/2 added to warp w, then the W/2 pair sums in warp order), each CTA
+// writes its chunk sum to the workspace, and the CTA that finishes a matrix
+// last (a counter per matrix, reset by that CTA) adds the chunk sums in chunk
+// order and writes y.
 //
 // Bounded waits only: a wait that expires raises the status word; the warp
 // still drains its copies and the CTA completes the reduction protocol.
@@ -42,24 +46,30 @@ namespace qk {
 
 namespace {
 
-constexpr int VT_WARPS = 8;
-constexpr int VT_THREADS = 32 * VT_WARPS;
-constexpr int VT_ROWS = 16 * VT_WARPS;                 // chunks are multiples of this
 constexpr int VT_MG = 16;                              // rows of x per launch
 constexpr int VT_RING = 192 * 1024;                    // shared-memory ring bytes of all warps (about)
 
+// warps per CTA: sixteen while a lane's NB x 16 accumulators leave room in
+// the 128 registers that 512 threads may use; eight beyond
+constexpr int vt_warps(int nb) { return nb <= 5 ? 16 : 8; }
+
 template <int NB>
 struct VtCfg {
+    static constexpr int WARPS = vt_warps(NB), HALF = WARPS / 2, THREADS = 32 * WARPS;
     static constexpr int K = 32 * NB, RB = 34 * NB;
-    static constexpr int SR = NB <= 4 ? 32 : 16;             // rows per stage
+    // rows per stage, a multiple of 16: copies of 2 to 4.4 KB (much smaller
+    // ones are limited by the copy engine's rate, not by HBM), at least two
+    // stages per warp in flight
+    static constexpr int SR = NB == 1 ? 64 : NB <= 4 ? 32 : 16;
     // a stage, + room for the 16-byte rounding of both ends
     static constexpr int SLOT = (SR * RB + 32 + 15) & ~15;
-    static constexpr int D_FIT = VT_RING / (VT_WARPS * SLOT);
+    static constexpr int D_FIT = VT_RING / (WARPS * SLOT);
     static constexpr int D = D_FIT > 8 ? 8 : D_FIT;           // ring depth per warp
-    static constexpr int RK = K + 1;                          // row pitch of the warps' sums
-    static constexpr int SMEM = VT_WARPS * D * SLOT + 8 * VT_WARPS * D + 16;
-    // after the stream the rings hold the eight warps' sums, [warp][16][RK] floats
-    static_assert(VT_WARPS * 16 * RK * 4 <= VT_WARPS * D * SLOT, "warp sums fit in the rings");
+    static constexpr int FR = 16 * K;                         // floats of one warp's sums
+    static constexpr int SMEM = WARPS * D * SLOT + 8 * WARPS * D + 16;
+    // after the stream the rings hold the pair sums, [HALF][FR] floats
+    static_assert(HALF * FR * 4 <= WARPS * D * SLOT, "warp sums fit in the rings");
+    static_assert(D >= 2, "at least two stages per warp");
 };
 
 // 2^(e - 127) as a float for a biased exponent 1 <= e <= 254, else 0
@@ -71,7 +81,7 @@ struct VtParams {
     const uint8_t *W;   // H*N rows of RB bytes
     uint64_t w_end;     // first byte past the matrices
     int64_t N;          // rows per matrix
-    int64_t R;          // rows per chunk (a multiple of VT_ROWS)
+    int64_t R;          // rows per chunk (a multiple of the warps per CTA)
     int nchunk;         // chunks per matrix
     const float *x;     // [H][M][N]
     int64_t M;
@@ -134,20 +144,21 @@ __device__ __forceinline__ uint32_t row_q4(uint32_t row, int b, int g, bool vali
 }
 
 template <int NB>
-__global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
+__global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParams P) {
     using C = VtCfg<NB>;
-    constexpr int K = C::K, RB = C::RB, SR = C::SR, SLOT = C::SLOT, D = C::D, RK = C::RK;
+    constexpr int K = C::K, RB = C::RB, SR = C::SR, SLOT = C::SLOT, D = C::D, FR = C::FR;
+    constexpr int WARPS = C::WARPS, HALF = C::HALF, THREADS = C::THREADS;
     constexpr bool CONTIG = NB == 1 || NB == 2 || NB == 4 || NB == 8;
     constexpr int CPG = 4 * NB, NW = CPG / 4;  // columns per MMA column index, their words
     extern __shared__ __align__(16) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + VT_WARPS * D * SLOT);  // [warp][D]
-    int *last = reinterpret_cast<int *>(bars + VT_WARPS * D);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * D * SLOT);  // [warp][D]
+    int *last = reinterpret_cast<int *>(bars + WARPS * D);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, c = blockIdx.x;
-    // this warp's rows: the w-th eighth of the chunk
+    // this warp's rows: the w-th sixteenth of the chunk
     const int64_t n_lo = static_cast<int64_t>(c) * P.R, n_hi = min(P.N, n_lo + P.R);
-    const int64_t rw = P.R / VT_WARPS;
+    const int64_t rw = P.R / WARPS;
     const int64_t w_lo = min(n_hi, n_lo + warp * rw), w_hi = min(n_hi, w_lo + rw);
     const int nst = static_cast<int>((w_hi - w_lo + SR - 1) / SR);
     const uint64_t mat0 = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(h) * P.N * RB;
@@ -305,38 +316,48 @@ __global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
         for (int t = issued > D ? issued - D : 0; t < issued; ++t) mbar_wait(bar0 + 8u * (t % D), (t / D) & 1, P.status);
     // back to the true scale: 1 / up = 2^(ew - 139) (exact)
     const float down = ew > 12 ? pow2_biased(ew - 12) : 0x1p-127f;
-    // every warp's ring is drained: the rings now hold the warps' sums,
-    // [warp][m][RK] (pitch K + 1); lane (g, tq) holds rows g ([0], [1]) and
-    // g + 8 ([2], [3]) of the MMA's output columns 2tq and 2tq + 1
+    // every warp's ring is drained: the rings now hold the pair sums in the
+    // MMA fragments' own order, [warp % HALF][b][j][e][lane], so that each
+    // store of a warp covers 32 consecutive words (no bank conflicts): the
+    // upper half of the warps store theirs, then the lower half add their own
     __syncthreads();
     float *sums = reinterpret_cast<float *>(smem);
-    {
-        float *r0p = sums + (warp * 16 + g) * RK, *r1p = r0p + 8 * RK;
+    for (int phase = 0; phase < 2; ++phase) {
+        if ((warp >= HALF) == (phase == 0)) {
+            float *sw = sums + (warp % HALF) * FR + lane;
 #pragma unroll
-        for (int b = 0; b < NB; ++b)
+            for (int b = 0; b < NB; ++b)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                // contiguous mapping: MMA jj = 4b + j, columns CPG*2tq + jj and CPG*(2tq+1) + jj
-                const int k0 = CONTIG ? CPG * 2 * tq + 4 * b + j : 32 * b + 8 * tq + j;
-                const int k1 = CONTIG ? k0 + CPG : k0 + 4;
-                r0p[k0] = acc[b][j][0] * down;
-                r0p[k1] = acc[b][j][1] * down;
-                r1p[k0] = acc[b][j][2] * down;
-                r1p[k1] = acc[b][j][3] * down;
-            }
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float *p = sw + ((b * 4 + j) * 4 + e) * 32;
+                        const float v = acc[b][j][e] * down;
+                        *p = phase ? v + *p : v;
+                    }
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    // the chunk sum into the workspace
+    // the chunk sum into the workspace [m][k]: fragment word i is element
+    // e = (i / 32) % 4 of lane (g, tq) = ((i % 32) / 4, i % 4) in MMA (b, j) =
+    // (i / 512, (i / 128) % 4), i.e. row g + 8 (e / 2) and, for odd e, the
+    // second of the lane's two columns: with the contiguous mapping MMA 4b + j
+    // gives the lane columns CPG*2tq + 4b + j and CPG*(2tq+1) + 4b + j, else
+    // 32b + 8tq + j and 32b + 8tq + j + 4
     float *part_hc = P.part + (static_cast<int64_t>(h) * P.nchunk + c) * 16 * K;
-    for (int i = threadIdx.x; i < P.mg * K; i += VT_THREADS) {
-        const int off = (i / K) * RK + i % K;
-        float v[VT_WARPS];
+    for (int i = threadIdx.x; i < FR; i += THREADS) {
+        const int ln = i & 31, e = (i >> 5) & 3, j = (i >> 7) & 3, b = i >> 9;
+        const int m = (ln >> 2) + 8 * (e >> 1), t = ln & 3;
+        if (m >= P.mg) continue;
+        const int k0 = CONTIG ? CPG * 2 * t + 4 * b + j : 32 * b + 8 * t + j;
+        const int k = (e & 1) ? k0 + (CONTIG ? CPG : 4) : k0;
+        float v[HALF];
 #pragma unroll
-        for (int w = 0; w < VT_WARPS; ++w) v[w] = sums[w * 16 * RK + off];
+        for (int w = 0; w < HALF; ++w) v[w] = sums[w * FR + i];
         float sum = v[0];
 #pragma unroll
-        for (int w = 1; w < VT_WARPS; ++w) sum += v[w];  // in warp order
-        part_hc[i] = sum;
+        for (int w = 1; w < HALF; ++w) sum += v[w];  // in warp order
+        part_hc[m * K + k] = sum;
     }
     __threadfence();
     __syncthreads();
@@ -350,16 +371,17 @@ __global__ void __launch_bounds__(VT_THREADS) qmm_t_kernel(const VtParams P) {
     __threadfence();
     const float *part_h = P.part + static_cast<int64_t>(h) * P.nchunk * 16 * K;
     float *yh = P.y + (static_cast<int64_t>(h) * P.M + P.m0) * K;
-    for (int i = threadIdx.x; i < P.mg * K; i += VT_THREADS) {
-        // eight chunk sums in flight at a time, added in chunk order
+    for (int i = threadIdx.x; i < P.mg * K; i += THREADS) {
+        // 24 chunk sums in flight at a time (one pass for up to 24 chunks per
+        // matrix), added in chunk order
         float sum = 0.0f;
-        for (int c0 = 0; c0 < P.nchunk; c0 += 8) {
-            float v[8];
+        for (int c0 = 0; c0 < P.nchunk; c0 += 24) {
+            float v[24];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < 24; ++u)
                 v[u] = c0 + u < P.nchunk ? __ldcg(part_h + static_cast<int64_t>(c0 + u) * 16 * K + i) : 0.0f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < 24; ++u)
                 if (c0 + u < P.nchunk) sum += v[u];
         }
         yh[i] = sum;
@@ -373,25 +395,27 @@ cudaError_t launch_nb(const VtParams &P, int64_t H, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(qmm_t_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    qmm_t_kernel<NB><<<dim3(P.nchunk, static_cast<unsigned>(H)), VT_THREADS, smem, st>>>(P);
+    qmm_t_kernel<NB><<<dim3(P.nchunk, static_cast<unsigned>(H)), VtCfg<NB>::THREADS, smem, st>>>(P);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int64_t qmm_t_chunk_rows(int64_t H, int64_t N, int num_sms) {
+int64_t qmm_t_chunk_rows(int64_t H, int64_t N, int64_t K, int num_sms) {
     // one CTA per SM over all matrices (the rings fill most of an SM's shared
-    // memory, so one CTA is resident per SM), whole stages per chunk
+    // memory, so one CTA is resident per SM), each chunk split evenly between
+    // the warps (a warp's last 16-row group may be partly empty)
     const int64_t want = static_cast<int64_t>(num_sms);
-    int64_t per = (want + H - 1) / H;  // chunks per matrix
+    const int64_t w = vt_warps(static_cast<int>(K / 32));
+    int64_t per = want / H;  // chunks per matrix: all CTAs in one wave
     if (per < 1) per = 1;
     int64_t R = (N + per - 1) / per;
-    R = (R + VT_ROWS - 1) / VT_ROWS * VT_ROWS;
-    return R < VT_ROWS ? VT_ROWS : R;
+    R = (R + w - 1) / w * w;
+    return R < w ? w : R;
 }
 
 size_t qmm_t_part_bytes(int64_t H, int64_t N, int64_t K, int num_sms) {
-    const int64_t R = qmm_t_chunk_rows(H, N, num_sms);
+    const int64_t R = qmm_t_chunk_rows(H, N, K, num_sms);
     const int64_t nchunk = (N + R - 1) / R;
     return static_cast<size_t>(H * nchunk * 16 * K) * sizeof(float);
 }
@@ -402,7 +426,7 @@ cudaError_t launch_qmm_t(const void *W, int64_t H, int64_t N, int64_t K, const f
     P.W = static_cast<const uint8_t *>(W);
     P.N = N;
     P.w_end = reinterpret_cast<uint64_t>(W) + static_cast<uint64_t>(H * N) * (K / 32) * 34;
-    P.R = qmm_t_chunk_rows(H, N, num_sms);
+    P.R = qmm_t_chunk_rows(H, N, K, num_sms);
     P.nchunk = static_cast<int>((N + P.R - 1) / P.R);
     P.x = x;
     P.M = M;

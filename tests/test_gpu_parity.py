@@ -489,7 +489,10 @@ def _run_qmm_t(q, W, H, N, K, x, stream=None):
 
 
 QMM_T_CASES = [(1, 1, 32, 1), (1, 16, 128, 5), (2, 300, 128, 5), (3, 1000, 64, 8), (1, 777, 256, 16),
-               (2, 129, 96, 17), (4, 2049, 160, 3), (1, 5000, 224, 1), (5, 64, 32, 2), (6, 12345, 128, 4)]
+               (2, 129, 96, 17), (4, 2049, 160, 3), (1, 5000, 224, 1), (5, 64, 32, 2), (6, 12345, 128, 4),
+               (2, 4000, 192, 6),
+               # 137 chunks of one matrix: the last CTA adds them over several passes
+               (1, 70000, 64, 3)]
 
 
 @pytest.mark.parametrize("H,N,K,M", QMM_T_CASES)

@@ -2,19 +2,20 @@
 any GPU run (no GPU needed):
 
 * the value-cache product (qmm_t.cu): the chunks of all CTAs and the row
-  ranges of their eight warps cover every matrix exactly once; every bulk
+  ranges of their warps cover every matrix exactly once; every bulk
   copy starts 16-byte aligned, has a 16-byte multiple size, stays inside the
   cache and its shared-memory slot; the bytes a lane reads (quant words,
-  scales) lie inside what its stage copied; the warps' sums fit in the rings
-  after the stream; shared memory stays within the per-block limit;
+  scales) lie inside what its stage copied; the warps' pair sums fit in the
+  rings after the stream; shared memory stays within the per-block limit;
 * the tcgen05 prefill's Q6_K / Q8_0 staging (gemm_tc.cu): each dequantiser
   warp's 16-byte chunk loads stay inside the matrix unless the kernel's
   "careful" test selects the word-by-word path, which it does exactly when a
   chunk would cross the matrix end; the read-back words of a super-block lie
   inside its staged chunks; the shared-memory plan fits.
 
-The constants mirror the kernels (8 warps, ~192 KB of rings, 32- or 16-row
-stages; 14 / 17 chunks per super-step, 60 / 68-word rows)."""
+The constants mirror the kernels (16 warps for K <= 160 else 8, ~192 KB of
+rings, stages of 64 / 32 / 16 rows; 14 / 17 chunks per super-step, 60 /
+68-word rows)."""
 import pytest
 
 SMEM_MAX = 232448
@@ -23,22 +24,27 @@ SMS = 152
 # --------------------------------------------------------------- qmm_t
 
 
+def vt_warps(nb):
+    return 16 if nb <= 5 else 8
+
+
 def vt_cfg(nb):
     K, RB = 32 * nb, 34 * nb
-    SR = 32 if nb <= 4 else 16
+    WARPS = vt_warps(nb)
+    SR = 64 if nb == 1 else 32 if nb <= 4 else 16
     SLOT = (SR * RB + 32 + 15) & ~15
-    D = min(8, (192 * 1024) // (8 * SLOT))
-    RK = K + 1
-    SMEM = 8 * D * SLOT + 8 * 8 * D + 16
-    return dict(K=K, RB=RB, SR=SR, SLOT=SLOT, D=D, RK=RK, SMEM=SMEM)
+    D = min(8, (192 * 1024) // (WARPS * SLOT))
+    FR = 16 * K
+    SMEM = WARPS * D * SLOT + 8 * WARPS * D + 16
+    return dict(K=K, RB=RB, SR=SR, SLOT=SLOT, D=D, FR=FR, SMEM=SMEM, WARPS=WARPS)
 
 
-def vt_chunk_rows(H, N, num_sms=SMS):
-    want = num_sms
-    per = max(1, -(-want // H))
+def vt_chunk_rows(H, N, K, num_sms=SMS):
+    w = vt_warps(K // 32)
+    per = max(1, num_sms // H)
     R = -(-N // per)
-    R = -(-R // 128) * 128
-    return max(R, 128)
+    R = -(-R // w) * w
+    return max(R, w)
 
 
 @pytest.mark.parametrize("nb", range(1, 9))
@@ -46,9 +52,13 @@ def test_qmm_t_shared_memory_plan(nb):
     C = vt_cfg(nb)
     assert C["D"] >= 2
     assert C["SMEM"] <= SMEM_MAX
-    assert C["SLOT"] % 16 == 0
-    # after the stream the rings hold the eight warps' sums [warp][16][RK]
-    assert 8 * 16 * C["RK"] * 4 <= 8 * C["D"] * C["SLOT"]
+    assert C["SLOT"] % 16 == 0 and C["SR"] % 16 == 0 and C["SR"] >= 16
+    # a stage's copy is at least 2 KB (smaller copies are copy-rate bound)
+    assert C["SR"] * C["RB"] >= 2048
+    # after the stream the rings hold the pair sums [warp % (W/2)][16 K]
+    assert (C["WARPS"] // 2) * C["FR"] * 4 <= C["WARPS"] * C["D"] * C["SLOT"]
+    # a lane's 16 NB accumulators and the rest fit 65536 / (32 W) registers
+    assert 16 * nb <= 65536 // (32 * C["WARPS"]) - 48
 
 
 @pytest.mark.parametrize("H,N,K", [(1, 1, 32), (1, 15, 64), (2, 300, 128), (8, 4096, 128), (8, 32768, 128),
@@ -58,9 +68,10 @@ def test_qmm_t_chunks_and_copies(H, N, K):
     nb = K // 32
     C = vt_cfg(nb)
     RB, SR, SLOT = C["RB"], C["SR"], C["SLOT"]
-    R = vt_chunk_rows(H, N)
-    assert R % 128 == 0
+    R = vt_chunk_rows(H, N, K)
+    assert R % C["WARPS"] == 0
     nchunk = -(-N // R)
+    assert H * nchunk <= max(SMS, H)  # one wave of CTAs (one per SM)
     assert nchunk < 2 ** 31 and H <= 65535
     base = 1 << 20  # W is 16-byte aligned
     w_end = base + H * N * RB
@@ -71,9 +82,9 @@ def test_qmm_t_chunks_and_copies(H, N, K):
         mat0 = base + h * N * RB
         for c in range(nchunk):
             n_lo, n_hi = c * R, min(N, c * R + R)
-            rw = R // 8
-            assert rw % 16 == 0
-            for w in range(8):
+            W = C["WARPS"]
+            rw = R // W
+            for w in range(W):
                 w_lo = min(n_hi, n_lo + w * rw)
                 w_hi = min(n_hi, w_lo + rw)
                 if w_lo < w_hi:
@@ -110,7 +121,7 @@ def test_qmm_t_chunks_and_copies(H, N, K):
 
 def test_qmm_t_counters_and_parts():
     for H, N, K in [(8, 32768, 128), (1, 1, 32), (65535, 16, 32)]:
-        R = vt_chunk_rows(H, N)
+        R = vt_chunk_rows(H, N, K)
         nchunk = -(-N // R)
         part = H * nchunk * 16 * K * 4
         assert part > 0 and nchunk >= 1
