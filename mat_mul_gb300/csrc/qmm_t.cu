@@ -39,6 +39,8 @@
 //
 // Bounded waits only: a wait that expires raises the status word; the warp
 // still drains its copies and the CTA completes the reduction protocol.
+#include <type_traits>
+
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 
@@ -143,6 +145,39 @@ __device__ __forceinline__ uint32_t row_q4(uint32_t row, int b, int g, bool vali
     return __funnelshift_r(lds32(base), lds32(base + 4u), (a & 3u) * 8u);
 }
 
+// This lane's accumulators times `down`, stored (ADD false) or added to what
+// is there (ADD true: own + stored) in the fragment order [b][j][lane][e < EH]
+// at sw: one EH-float vector per MMA, so a warp's access covers 32 x EH
+// consecutive words (no bank conflicts).
+template <int NB, int EH, bool ADD>
+__device__ __forceinline__ void put_sums(float *sw, int lane, const float (&acc)[NB][4][4], float down) {
+    using V = typename std::conditional<EH == 4, float4, float2>::type;
+    V *vp = reinterpret_cast<V *>(sw) + lane;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        V old[4];
+        if (ADD) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) old[j] = vp[(b * 4 + j) * 32];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = acc[b][j][e] * down;
+            V v;
+            if constexpr (EH == 4) {
+                v = make_float4(f[0], f[1], f[2], f[3]);
+                if (ADD) v = make_float4(f[0] + old[j].x, f[1] + old[j].y, f[2] + old[j].z, f[3] + old[j].w);
+            } else {
+                v = make_float2(f[0], f[1]);
+                if (ADD) v = make_float2(f[0] + old[j].x, f[1] + old[j].y);
+            }
+            vp[(b * 4 + j) * 32] = v;
+        }
+    }
+}
+
 template <int NB>
 __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParams P) {
     using C = VtCfg<NB>;
@@ -168,7 +203,16 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
     if (lane == 0) {
         for (int s = 0; s < D; ++s) mbar_init(bar0 + 8u * s, 1);
         fence_mbar_init();
+        // while the preceding grid finishes: warm L2 with this warp's first
+        // 16 KB (L2 is the point of coherence, so this is safe even if that
+        // grid writes the cache); nothing else is read, and nothing written,
+        // before the wait
+        const uint64_t a16 = (mat0 + static_cast<uint64_t>(w_lo) * RB) & ~uint64_t(15);
+        const uint64_t b16 = min((mat0 + static_cast<uint64_t>(w_hi) * RB) & ~uint64_t(15), a16 + 16384);
+        if (b16 > a16) bulk_prefetch_l2(reinterpret_cast<const void *>(a16), static_cast<uint32_t>(b16 - a16));
     }
+    pdl_trigger();
+    pdl_wait();
     __syncwarp();
     // issue stage t of this warp into slot t % D (lane 0): its rows rounded out
     // to 16 bytes (the bulk-copy rule); the matrices' last bytes, past the
@@ -317,47 +361,34 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
     // back to the true scale: 1 / up = 2^(ew - 139) (exact)
     const float down = ew > 12 ? pow2_biased(ew - 12) : 0x1p-127f;
     // every warp's ring is drained: the rings now hold the pair sums in the
-    // MMA fragments' own order, [warp % HALF][b][j][e][lane], so that each
-    // store of a warp covers 32 consecutive words (no bank conflicts): the
-    // upper half of the warps store theirs, then the lower half add their own
+    // MMA fragments' own order, [warp % HALF][b][j][lane][e < EH]: the upper
+    // half of the warps store theirs, then the lower half add their own.
+    // Elements e = 2, 3 (rows g + 8) are kept only when this launch has more
+    // than 8 rows of x.
     __syncthreads();
     float *sums = reinterpret_cast<float *>(smem);
-    for (int phase = 0; phase < 2; ++phase) {
-        if ((warp >= HALF) == (phase == 0)) {
-            float *sw = sums + (warp % HALF) * FR + lane;
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float *p = sw + ((b * 4 + j) * 4 + e) * 32;
-                        const float v = acc[b][j][e] * down;
-                        *p = phase ? v + *p : v;
-                    }
-        }
-        __syncthreads();
+    const int EH = P.mg > 8 ? 4 : 2;
+    if (warp >= HALF) {
+        if (EH == 4) put_sums<NB, 4, false>(sums + (warp - HALF) * FR, lane, acc, down);
+        else put_sums<NB, 2, false>(sums + (warp - HALF) * FR, lane, acc, down);
     }
-    // the chunk sum into the workspace [m][k]: fragment word i is element
-    // e = (i / 32) % 4 of lane (g, tq) = ((i % 32) / 4, i % 4) in MMA (b, j) =
-    // (i / 512, (i / 128) % 4), i.e. row g + 8 (e / 2) and, for odd e, the
-    // second of the lane's two columns: with the contiguous mapping MMA 4b + j
-    // gives the lane columns CPG*2tq + 4b + j and CPG*(2tq+1) + 4b + j, else
-    // 32b + 8tq + j and 32b + 8tq + j + 4
-    float *part_hc = P.part + (static_cast<int64_t>(h) * P.nchunk + c) * 16 * K;
-    for (int i = threadIdx.x; i < FR; i += THREADS) {
-        const int ln = i & 31, e = (i >> 5) & 3, j = (i >> 7) & 3, b = i >> 9;
-        const int m = (ln >> 2) + 8 * (e >> 1), t = ln & 3;
-        if (m >= P.mg) continue;
-        const int k0 = CONTIG ? CPG * 2 * t + 4 * b + j : 32 * b + 8 * t + j;
-        const int k = (e & 1) ? k0 + (CONTIG ? CPG : 4) : k0;
+    __syncthreads();
+    if (warp < HALF) {
+        if (EH == 4) put_sums<NB, 4, true>(sums + warp * FR, lane, acc, down);
+        else put_sums<NB, 2, true>(sums + warp * FR, lane, acc, down);
+    }
+    __syncthreads();
+    // the chunk sum into the workspace, in the same fragment order (coalesced)
+    const int nf = FR / 4 * EH;
+    float *part_hc = P.part + (static_cast<int64_t>(h) * P.nchunk + c) * FR;
+    for (int i = threadIdx.x; i < nf; i += THREADS) {
         float v[HALF];
 #pragma unroll
         for (int w = 0; w < HALF; ++w) v[w] = sums[w * FR + i];
         float sum = v[0];
 #pragma unroll
         for (int w = 1; w < HALF; ++w) sum += v[w];  // in warp order
-        part_hc[m * K + k] = sum;
+        part_hc[i] = sum;
     }
     __threadfence();
     __syncthreads();
@@ -367,36 +398,66 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
     }
     __syncthreads();
     if (!*last) return;
-    // the last CTA of matrix h: chunk sums in chunk order
+    // the last CTA of matrix h: chunk sums in chunk order, two fragment words
+    // per thread and 24 chunks in flight at a time; fragment word i is element
+    // e = i % EH of lane (g, tq) = (((i / EH) % 32) / 4, (i / EH) % 4) in MMA
+    // (b, j) = (i / (128 EH), (i / (32 EH)) % 4): row g + 8 (e / 2) and, for odd e, the
+    // second of the lane's two columns (with the contiguous mapping MMA 4b + j
+    // gives the lane columns CPG*2tq + 4b + j and CPG*(2tq+1) + 4b + j, else
+    // 32b + 8tq + j and 32b + 8tq + j + 4)
     __threadfence();
-    const float *part_h = P.part + static_cast<int64_t>(h) * P.nchunk * 16 * K;
+    const float *part_h = P.part + static_cast<int64_t>(h) * P.nchunk * FR;
     float *yh = P.y + (static_cast<int64_t>(h) * P.M + P.m0) * K;
-    for (int i = threadIdx.x; i < P.mg * K; i += THREADS) {
-        // 24 chunk sums in flight at a time (one pass for up to 24 chunks per
-        // matrix), added in chunk order
-        float sum = 0.0f;
+    auto put = [&](int i, float v) {
+        const int e = i % EH, ln = (i / EH) & 31, bj = i / (32 * EH), j = bj & 3, b = bj >> 2;
+        const int m = (ln >> 2) + 8 * (e >> 1), t = ln & 3;
+        const int k0 = CONTIG ? CPG * 2 * t + 4 * b + j : 32 * b + 8 * t + j;
+        if (m < P.mg) yh[m * K + ((e & 1) ? k0 + (CONTIG ? CPG : 4) : k0)] = v;
+    };
+    for (int i0 = threadIdx.x; i0 < nf; i0 += 2 * THREADS) {
+        const int i1 = i0 + THREADS;
+        const bool two = i1 < nf;
+        float s0 = 0.0f, s1 = 0.0f;
         for (int c0 = 0; c0 < P.nchunk; c0 += 24) {
-            float v[24];
+            float v0[24], v1[24];
+#pragma unroll
+            for (int u = 0; u < 24; ++u) {
+                const bool ok = c0 + u < P.nchunk;
+                const float *pc = part_h + static_cast<int64_t>(c0 + u) * FR;
+                v0[u] = ok ? __ldcg(pc + i0) : 0.0f;
+                v1[u] = ok && two ? __ldcg(pc + i1) : 0.0f;
+            }
 #pragma unroll
             for (int u = 0; u < 24; ++u)
-                v[u] = c0 + u < P.nchunk ? __ldcg(part_h + static_cast<int64_t>(c0 + u) * 16 * K + i) : 0.0f;
-#pragma unroll
-            for (int u = 0; u < 24; ++u)
-                if (c0 + u < P.nchunk) sum += v[u];
+                if (c0 + u < P.nchunk) {
+                    s0 += v0[u];
+                    s1 += v1[u];
+                }
         }
-        yh[i] = sum;
+        put(i0, s0);
+        if (two) put(i1, s1);
     }
     if (threadIdx.x == 0) P.count[h] = 0u;  // ready for the next call on this stream
 }
 
+// Programmatic dependent launch: the CTAs start (and warm L2 with their rows)
+// as SMs free up at the end of the preceding grid, then wait for it.
 template <int NB>
 cudaError_t launch_nb(const VtParams &P, int64_t H, cudaStream_t st) {
-    const size_t smem = VtCfg<NB>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(qmm_t_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    const int smem = VtCfg<NB>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(qmm_t_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    qmm_t_kernel<NB><<<dim3(P.nchunk, static_cast<unsigned>(H)), VtCfg<NB>::THREADS, smem, st>>>(P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.nchunk, static_cast<unsigned>(H));
+    cfg.blockDim = dim3(VtCfg<NB>::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qmm_t_kernel<NB>, P);
 }
 
 }  // namespace

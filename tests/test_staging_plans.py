@@ -89,6 +89,13 @@ def test_qmm_t_chunks_and_copies(H, N, K):
                 w_hi = min(n_hi, w_lo + rw)
                 if w_lo < w_hi:
                     seen.append((w_lo, w_hi))
+                # the L2 warm-up before the dependency wait: at most 16 KB of
+                # the warp's own rows, 16-byte aligned, inside the cache
+                p16 = (mat0 + w_lo * RB) & ~15
+                q16 = min((mat0 + w_hi * RB) & ~15, p16 + 16384)
+                if q16 > p16:
+                    assert p16 >= base and q16 <= w_end and (q16 - p16) % 16 == 0
+                    assert q16 <= ((mat0 + w_hi * RB) + 15) & ~15
                 nst = -(-(w_hi - w_lo) // SR)
                 for t in range(nst):
                     r0, r1 = w_lo + t * SR, min(w_hi, w_lo + t * SR + SR)
