@@ -243,18 +243,40 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
     const uint32_t qoff = 34u * bb + 2u + static_cast<uint32_t>((CPG * g) % 32);
     const float *xh = P.x + (static_cast<int64_t>(h) * P.M + P.m0) * P.N;  // row m of this launch: xh + m*N
     const int ra = 2 * tq, rb = ra + 1, rc = ra + 8, rd = ra + 9;  // this lane's four rows of a group
-    // x of this lane's four positions of the group at n0, rows g and g + 8
-    // (zero past the warp's rows or past this launch's rows of x)
-    auto load_x = [&](int64_t n0, float (&v)[2][4]) {
-#pragma unroll
-        for (int hm = 0; hm < 2; ++hm) {
-            const int m = g + 8 * hm;
-            const float *xr = xh + m * P.N + n0;
-            const bool vm = m < P.mg;
-            v[hm][0] = vm && n0 + ra < w_hi ? __ldg(xr + ra) : 0.0f;
-            v[hm][1] = vm && n0 + rb < w_hi ? __ldg(xr + rb) : 0.0f;
-            v[hm][2] = vm && n0 + rc < w_hi ? __ldg(xr + rc) : 0.0f;
-            v[hm][3] = vm && n0 + rd < w_hi ? __ldg(xr + rd) : 0.0f;
+    // positions are counted from w_lo from here on (32-bit): the warp's rows are [0, nw)
+    const int nw = static_cast<int>(w_hi - w_lo);
+    // x of rows g and g + 8 at position ra of the warp's first group; rows
+    // g + 8 exist only when this launch has more than 8 rows of x
+    const float *xp0 = xh + static_cast<int64_t>(g) * P.N + w_lo + ra;
+    const float *xp1 = xp0 + 8 * P.N;
+    const bool vm0 = g < P.mg, vm1 = g + 8 < P.mg, two = P.mg > 8;
+    // x of this lane's four positions of the group at o (ra, rb, rc, rd), rows
+    // g and g + 8 (zero past the warp's rows or past this launch's rows of x)
+    auto load_x = [&](int o, float (&v)[2][4]) {
+        const float *p0 = xp0 + o, *p1 = xp1 + o;
+        if (o + 16 <= nw) {
+            v[0][0] = vm0 ? __ldg(p0) : 0.0f;
+            v[0][1] = vm0 ? __ldg(p0 + 1) : 0.0f;
+            v[0][2] = vm0 ? __ldg(p0 + 8) : 0.0f;
+            v[0][3] = vm0 ? __ldg(p0 + 9) : 0.0f;
+            if (two) {
+                v[1][0] = vm1 ? __ldg(p1) : 0.0f;
+                v[1][1] = vm1 ? __ldg(p1 + 1) : 0.0f;
+                v[1][2] = vm1 ? __ldg(p1 + 8) : 0.0f;
+                v[1][3] = vm1 ? __ldg(p1 + 9) : 0.0f;
+            }
+        } else {
+            const int n = nw - o;  // positions left in the group
+            v[0][0] = vm0 && ra < n ? __ldg(p0) : 0.0f;
+            v[0][1] = vm0 && rb < n ? __ldg(p0 + 1) : 0.0f;
+            v[0][2] = vm0 && rc < n ? __ldg(p0 + 8) : 0.0f;
+            v[0][3] = vm0 && rd < n ? __ldg(p0 + 9) : 0.0f;
+            if (two) {
+                v[1][0] = vm1 && ra < n ? __ldg(p1) : 0.0f;
+                v[1][1] = vm1 && rb < n ? __ldg(p1 + 1) : 0.0f;
+                v[1][2] = vm1 && rc < n ? __ldg(p1 + 8) : 0.0f;
+                v[1][3] = vm1 && rd < n ? __ldg(p1 + 9) : 0.0f;
+            }
         }
     };
 
@@ -268,8 +290,49 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
     int ew = 12;           // biased exponent of the warp's running max |x| (at least 12)
     float up = 0x1p127f;   // 2^(139 - ew): that max times up lies in [2^12, 2^13)
 
-    float xn[2][4];  // x of the next group, in flight while the current one is contracted
-    load_x(w_lo, xn);
+    // one group of 16 positions whose rows start at shared address `rows`; nv
+    // of them are the warp's (16 for every group but perhaps the last)
+    auto contract = [&](const float (&xc)[2][4], uint32_t rows, int nv) {
+        const bool va = ra < nv, vb = rb < nv, vc = rc < nv, vd = rd < nv;
+        // A: x * up of positions ra, rb (a0, a1) and rc, rd (a2, a3); rows g, g + 8
+        const uint32_t a0 = pack_half2(xc[0][0] * up, xc[0][1] * up), a2 = pack_half2(xc[0][2] * up, xc[0][3] * up);
+        const uint32_t a1 = two ? pack_half2(xc[1][0] * up, xc[1][1] * up) : 0u;
+        const uint32_t a3 = two ? pack_half2(xc[1][2] * up, xc[1][3] * up) : 0u;
+        const uint32_t row_a = rows + ra * RB, row_b = rows + rb * RB, row_c = rows + rc * RB,
+                       row_dd = rows + rd * RB;
+        if constexpr (CONTIG) {
+            // CPG contiguous quant bytes of block bb per row, one d per row
+            uint32_t wa[NW], wb[NW], wc[NW], wd[NW];
+            row_words(row_a + qoff, va, wa);
+            row_words(row_b + qoff, vb, wb);
+            row_words(row_c + qoff, vc, wc);
+            row_words(row_dd + qoff, vd, wd);
+            const uint32_t dab = row_d(row_a, bb, va) | (row_d(row_b, bb, vb) << 16);
+            const uint32_t dcd = row_d(row_c, bb, vc) | (row_d(row_dd, bb, vd) << 16);
+            const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
+            const __half2 d89 = *reinterpret_cast<const __half2 *>(&dcd);
+#pragma unroll
+            for (int j = 0; j < CPG; ++j)
+                mma16816(acc[j >> 2][j & 3], a0, a1, a2, a3, b_pair(wa[j >> 2], wb[j >> 2], j & 3, d01),
+                         b_pair(wc[j >> 2], wd[j >> 2], j & 3, d89));
+        } else {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const uint32_t wa = row_q4(row_a, b, g, va), wb = row_q4(row_b, b, g, vb);
+                const uint32_t wc = row_q4(row_c, b, g, vc), wd = row_q4(row_dd, b, g, vd);
+                const uint32_t dab = row_d(row_a, b, va) | (row_d(row_b, b, vb) << 16);
+                const uint32_t dcd = row_d(row_c, b, vc) | (row_d(row_dd, b, vd) << 16);
+                const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
+                const __half2 d89 = *reinterpret_cast<const __half2 *>(&dcd);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma16816(acc[b][j], a0, a1, a2, a3, b_pair(wa, wb, j, d01), b_pair(wc, wd, j, d89));
+            }
+        }
+    };
+
+    float xn[2][4] = {};  // x of the next group, in flight while the current one is contracted
+    load_x(0, xn);
     bool ok = true;
     for (int t = 0; t < nst && ok; ++t) {
         const int s = t % D;
@@ -277,19 +340,18 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
         // reports it); the CTA still takes part in the reduction
         ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8u * s, (t / D) & 1, P.status));
         if (!ok) break;
-        const int64_t r0 = w_lo + static_cast<int64_t>(t) * SR;
-        const uint64_t a = mat0 + static_cast<uint64_t>(r0) * RB;
+        const uint64_t a = mat0 + static_cast<uint64_t>(w_lo + static_cast<int64_t>(t) * SR) * RB;
         const uint32_t stage = smem_u32(ring + s * SLOT) + static_cast<uint32_t>(a & 15);
 #pragma unroll 1
         for (int gi = 0; gi < SR / 16; ++gi) {
-            const int64_t n0 = r0 + 16 * gi;  // these 16 positions
-            if (n0 >= w_hi) break;
+            const int o = t * SR + 16 * gi;  // these 16 positions
+            if (o >= nw) break;
             float xc[2][4];
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) xc[hm][e] = xn[hm][e];
-            if (n0 + 16 < w_hi) load_x(n0 + 16, xn);
+            if (o + 16 < nw) load_x(o + 16, xn);
             // the running scale: the warp's max |x| so far
             float mloc = 0.0f;
 #pragma unroll
@@ -310,42 +372,8 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
                 up = pow2_biased(266 - ew);
             }
             const uint32_t rows = stage + static_cast<uint32_t>(16 * gi * RB);
-            const int nv = static_cast<int>(min(static_cast<int64_t>(16), w_hi - n0));
-            const bool va = ra < nv, vb = rb < nv, vc = rc < nv, vd = rd < nv;
-            // A: x * up of positions ra, rb (a0, a1) and rc, rd (a2, a3); rows g, g + 8
-            const uint32_t a0 = pack_half2(xc[0][0] * up, xc[0][1] * up), a1 = pack_half2(xc[1][0] * up, xc[1][1] * up);
-            const uint32_t a2 = pack_half2(xc[0][2] * up, xc[0][3] * up), a3 = pack_half2(xc[1][2] * up, xc[1][3] * up);
-            const uint32_t row_a = rows + ra * RB, row_b = rows + rb * RB, row_c = rows + rc * RB,
-                           row_dd = rows + rd * RB;
-            if constexpr (CONTIG) {
-                // CPG contiguous quant bytes of block bb per row, one d per row
-                uint32_t wa[NW], wb[NW], wc[NW], wd[NW];
-                row_words(row_a + qoff, va, wa);
-                row_words(row_b + qoff, vb, wb);
-                row_words(row_c + qoff, vc, wc);
-                row_words(row_dd + qoff, vd, wd);
-                const uint32_t dab = row_d(row_a, bb, va) | (row_d(row_b, bb, vb) << 16);
-                const uint32_t dcd = row_d(row_c, bb, vc) | (row_d(row_dd, bb, vd) << 16);
-                const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
-                const __half2 d89 = *reinterpret_cast<const __half2 *>(&dcd);
-#pragma unroll
-                for (int j = 0; j < CPG; ++j)
-                    mma16816(acc[j >> 2][j & 3], a0, a1, a2, a3, b_pair(wa[j >> 2], wb[j >> 2], j & 3, d01),
-                             b_pair(wc[j >> 2], wd[j >> 2], j & 3, d89));
-            } else {
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const uint32_t wa = row_q4(row_a, b, g, va), wb = row_q4(row_b, b, g, vb);
-                    const uint32_t wc = row_q4(row_c, b, g, vc), wd = row_q4(row_dd, b, g, vd);
-                    const uint32_t dab = row_d(row_a, b, va) | (row_d(row_b, b, vb) << 16);
-                    const uint32_t dcd = row_d(row_c, b, vc) | (row_d(row_dd, b, vd) << 16);
-                    const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
-                    const __half2 d89 = *reinterpret_cast<const __half2 *>(&dcd);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma16816(acc[b][j], a0, a1, a2, a3, b_pair(wa, wb, j, d01), b_pair(wc, wd, j, d89));
-                }
-            }
+            if (o + 16 <= nw) contract(xc, rows, 16);  // a full group: no per-row checks
+            else contract(xc, rows, nw - o);
         }
         __syncwarp();
         if (lane == 0 && issued < nst) {
