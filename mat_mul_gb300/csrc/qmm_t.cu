@@ -119,30 +119,38 @@ __device__ __forceinline__ uint32_t b_pair(uint32_t wa, uint32_t wb, int j, __ha
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-// The fp16 d of block b of a row at shared address `row` (2-byte aligned), as
-// raw bits; zero for a row past the matrix.
-__device__ __forceinline__ uint32_t row_d(uint32_t row, int b, bool valid) {
-    return valid ? lds16(row + 34u * b) : 0u;
+// Rows are read from the rings through plain pointers into the dynamic
+// shared memory (the compiler then folds the constant offsets into the loads
+// and schedules them freely after the stage's barrier wait, whose asm clobbers
+// memory).
+
+// The fp16 d of block b of a row (2-byte aligned), as raw bits; zero for a
+// row past the matrix.
+__device__ __forceinline__ uint32_t row_d(const uint8_t *row, int b, bool valid) {
+    return valid ? *reinterpret_cast<const uint16_t *>(row + 34 * b) : 0u;
 }
 
-// NW consecutive 32-bit words from the 2-byte-aligned shared address a;
-// zeros for a row past the matrix.
+// NW consecutive 32-bit words starting sh / 8 bytes past the 4-byte-aligned
+// q; zeros for a row past the matrix.
 template <int NW>
-__device__ __forceinline__ void row_words(uint32_t a, bool valid, uint32_t (&w)[NW]) {
-    if (valid) {
-        lds_words_u16aligned(a, w);
-    } else {
+__device__ __forceinline__ void row_words(const uint8_t *q, uint32_t sh, bool valid, uint32_t (&w)[NW]) {
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(q);
+    uint32_t prev = valid ? p[0] : 0u;
 #pragma unroll
-        for (int i = 0; i < NW; ++i) w[i] = 0u;
+    for (int i = 0; i < NW; ++i) {
+        const uint32_t next = valid ? p[i + 1] : 0u;
+        w[i] = __funnelshift_r(prev, next, sh);
+        prev = next;
     }
 }
 
-// Quant bytes 4g .. 4g+3 of block b of a row (2-byte aligned).
-__device__ __forceinline__ uint32_t row_q4(uint32_t row, int b, int g, bool valid) {
+// Quant bytes 4g .. 4g+3 of block b of a row (2-byte aligned; base is the
+// 16-byte-aligned start of the shared memory).
+__device__ __forceinline__ uint32_t row_q4(const uint8_t *base, const uint8_t *row, int b, int g, bool valid) {
     if (!valid) return 0u;
-    const uint32_t a = row + 34u * b + 2u + 4u * g;
-    const uint32_t base = a & ~3u;
-    return __funnelshift_r(lds32(base), lds32(base + 4u), (a & 3u) * 8u);
+    const uint32_t a = static_cast<uint32_t>(row - base) + 34u * b + 2u + 4u * g;
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(base + (a & ~3u));
+    return __funnelshift_r(p[0], p[1], (a & 3u) * 8u);
 }
 
 // This lane's accumulators times `down`, stored (ADD false) or added to what
@@ -290,23 +298,35 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
     int ew = 12;           // biased exponent of the warp's running max |x| (at least 12)
     float up = 0x1p127f;   // 2^(139 - ew): that max times up lies in [2^12, 2^13)
 
-    // one group of 16 positions whose rows start at shared address `rows`; nv
-    // of them are the warp's (16 for every group but perhaps the last)
-    auto contract = [&](const float (&xc)[2][4], uint32_t rows, int nv) {
+    // one group of 16 positions whose rows start at `rows` in shared memory;
+    // nv of them are the warp's (16 for every group but perhaps the last)
+    auto contract = [&](const float (&xc)[2][4], const uint8_t *rows, int nv) {
         const bool va = ra < nv, vb = rb < nv, vc = rc < nv, vd = rd < nv;
         // A: x * up of positions ra, rb (a0, a1) and rc, rd (a2, a3); rows g, g + 8
         const uint32_t a0 = pack_half2(xc[0][0] * up, xc[0][1] * up), a2 = pack_half2(xc[0][2] * up, xc[0][3] * up);
         const uint32_t a1 = two ? pack_half2(xc[1][0] * up, xc[1][1] * up) : 0u;
         const uint32_t a3 = two ? pack_half2(xc[1][2] * up, xc[1][3] * up) : 0u;
-        const uint32_t row_a = rows + ra * RB, row_b = rows + rb * RB, row_c = rows + rc * RB,
-                       row_dd = rows + rd * RB;
+        const uint8_t *row_a = rows + ra * RB, *row_b = rows + rb * RB, *row_c = rows + rc * RB,
+                      *row_dd = rows + rd * RB;
         if constexpr (CONTIG) {
-            // CPG contiguous quant bytes of block bb per row, one d per row
+            // CPG contiguous quant bytes of block bb per row, one d per row:
+            // from the 4-byte word at or below them, shifted by their offset
+            // in it (the same for every row when RB is a multiple of 4, since
+            // the stage then starts on a 4-byte boundary too)
             uint32_t wa[NW], wb[NW], wc[NW], wd[NW];
-            row_words(row_a + qoff, va, wa);
-            row_words(row_b + qoff, vb, wb);
-            row_words(row_c + qoff, vc, wc);
-            row_words(row_dd + qoff, vd, wd);
+            if constexpr (RB % 4 == 0) {
+                const uint32_t sh = (qoff & 3u) * 8u, q4 = qoff & ~3u;
+                row_words(row_a + q4, sh, va, wa);
+                row_words(row_b + q4, sh, vb, wb);
+                row_words(row_c + q4, sh, vc, wc);
+                row_words(row_dd + q4, sh, vd, wd);
+            } else {
+                auto at = [&](const uint8_t *row) { return static_cast<uint32_t>(row - smem) + qoff; };
+                row_words(smem + (at(row_a) & ~3u), (at(row_a) & 3u) * 8u, va, wa);
+                row_words(smem + (at(row_b) & ~3u), (at(row_b) & 3u) * 8u, vb, wb);
+                row_words(smem + (at(row_c) & ~3u), (at(row_c) & 3u) * 8u, vc, wc);
+                row_words(smem + (at(row_dd) & ~3u), (at(row_dd) & 3u) * 8u, vd, wd);
+            }
             const uint32_t dab = row_d(row_a, bb, va) | (row_d(row_b, bb, vb) << 16);
             const uint32_t dcd = row_d(row_c, bb, vc) | (row_d(row_dd, bb, vd) << 16);
             const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
@@ -318,8 +338,8 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
         } else {
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const uint32_t wa = row_q4(row_a, b, g, va), wb = row_q4(row_b, b, g, vb);
-                const uint32_t wc = row_q4(row_c, b, g, vc), wd = row_q4(row_dd, b, g, vd);
+                const uint32_t wa = row_q4(smem, row_a, b, g, va), wb = row_q4(smem, row_b, b, g, vb);
+                const uint32_t wc = row_q4(smem, row_c, b, g, vc), wd = row_q4(smem, row_dd, b, g, vd);
                 const uint32_t dab = row_d(row_a, b, va) | (row_d(row_b, b, vb) << 16);
                 const uint32_t dcd = row_d(row_c, b, vc) | (row_d(row_dd, b, vd) << 16);
                 const __half2 d01 = *reinterpret_cast<const __half2 *>(&dab);
@@ -341,7 +361,7 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
         ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8u * s, (t / D) & 1, P.status));
         if (!ok) break;
         const uint64_t a = mat0 + static_cast<uint64_t>(w_lo + static_cast<int64_t>(t) * SR) * RB;
-        const uint32_t stage = smem_u32(ring + s * SLOT) + static_cast<uint32_t>(a & 15);
+        const uint8_t *stage = ring + s * SLOT + (a & 15);
 #pragma unroll 1
         for (int gi = 0; gi < SR / 16; ++gi) {
             const int o = t * SR + 16 * gi;  // these 16 positions
@@ -371,7 +391,7 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
                 ew = eg;
                 up = pow2_biased(266 - ew);
             }
-            const uint32_t rows = stage + static_cast<uint32_t>(16 * gi * RB);
+            const uint8_t *rows = stage + 16 * gi * RB;
             if (o + 16 <= nw) contract(xc, rows, 16);  // a full group: no per-row checks
             else contract(xc, rows, nw - o);
         }
