@@ -33,11 +33,14 @@
 // Warp roles (11 warps), per 128-wide K step (half a super-block):
 //   0 = token producer: the step's two 64-wide token boxes (ring released
 //       by this CTA's MMA commits);
-//   10 = raw weight producer (Q4_K): the 16-byte super-block header and the
-//       64 quant bytes of each of the 128 weight rows (ring released by the
-//       dequantisers, so dequantisation runs ahead of the MMA); Q6_K and
-//       Q8_0 rows are not 16-byte multiples, so there the dequantisers load
-//       their rows' bytes themselves;
+//   10 = raw weight producer: Q4_K / Q5_K the super-block head and the 64
+//       quant bytes of each of the 128 weight rows per K step; Q8_0 (rows
+//       are 16-byte multiples) and Q6_K (when two rows are: K a multiple of
+//       1024, N even) the whole super-step of the 128 rows (ring released
+//       by the dequantisers, so dequantisation runs ahead of the MMA); the
+//       other Q6_K shapes, Q3_K and Q2_K have rows that are no 16-byte
+//       multiples, so there the dequantisers load their rows' bytes
+//       themselves;
 //   1 = MMA issuer (and TMEM owner);
 //   2..9 = dequantisers, two per TMEM lane quarter (warp w serves lanes
 //       32*(w%4).. and the K step's weights 64*((w-2)/4)..), then epilogue
@@ -85,14 +88,16 @@ struct RawTma {
     static constexpr int R_BYTES = H_BYTES + Q_BYTES;
 };
 
-// Q6_K and Q8_0: rows are not 16-byte multiples, so no tensor map describes
-// them; each dequantiser warp reads the raw bytes of its 32 rows itself with
-// 16-byte loads into registers, one super-step (two K steps, 256 weights:
-// one Q6_K super-block, eight Q8_0 blocks) ahead, and stores them into two
-// buffers of 32 rows x PITCH_W words, read back as whole 16-byte chunks (an
-// odd number of chunks per row: conflict-free).  Q6_K: the 14 chunks from
-// the 16-byte boundary at or below the super-block's start (rows are only
-// 2-byte aligned), Q8_0: the 17 chunks of its 272 bytes.
+// Q6_K (the shapes the TMA stages below do not take), Q3_K, Q2_K: rows are
+// not 16-byte multiples, so no tensor map describes them; each dequantiser
+// warp reads the raw bytes of its 32 rows itself with 16-byte loads into
+// registers, one super-step (two K steps, 256 weights: one super-block)
+// ahead, and stores them into two buffers of 32 rows x PITCH_W words, read
+// back as whole 16-byte chunks (an odd number of chunks per row:
+// conflict-free): the chunks from the 16-byte boundary at or below the
+// super-block's start (rows are only 2-byte aligned).  (The Q8_0 entry sizes
+// this path's registers when it is compiled for the TMA-staged Q8_0, where
+// it never runs.)
 template <int T>
 struct RawStep {
     static constexpr int BYTES = 0, CHUNKS = 0, PITCH_W = 0;
@@ -116,17 +121,48 @@ struct RawStep<QMM_Q2_K> {
     static constexpr int BYTES = 84, CHUNKS = 6, PITCH_W = 28;
 };
 
-template <int BT, int T>
+// Q6_K and Q8_0 raw stages by TMA (TM): one super-step of the tile's 128
+// rows per stage.
+//   Q6_K, when rows are pairs of 16-byte multiples (K a multiple of 1024,
+//     N even): the matrix seen as N/2 double rows of 2*RB bytes; two boxes of
+//     64 double rows x 240 bytes from the 16-byte boundary at or below the
+//     super-block's start in the even rows (box 0) and in the odd rows (box
+//     1).  TMEM lane n holds weight row 2*(n % 64) + n / 64, so that each
+//     dequantiser warp reads consecutive rows of one box (15 chunks apart:
+//     conflict-free).
+//   Q8_0 (rows are 16-byte multiples when K is a multiple of 256): one box of
+//     128 rows x 272 bytes (136 two-byte elements), 17 chunks apart.
+template <int T>
+struct RawTile {
+    static constexpr int ROW = 0, BOX = 0, TX = 0, R_BYTES = 1024;
+};
+template <>
+struct RawTile<QMM_Q6_K> {
+    static constexpr int ROW = 240, BOX = 64 * ROW, TX = 2 * BOX, R_BYTES = (TX + 1023) / 1024 * 1024;
+};
+template <>
+struct RawTile<QMM_Q8_0> {
+    static constexpr int ROW = 272, BOX = 128 * ROW, TX = BOX, R_BYTES = (TX + 1023) / 1024 * 1024;
+};
+
+template <int BT, int T, bool TM = false>
 struct TcCfg {
-    static constexpr bool OWN = T != QMM_Q4_K && T != QMM_Q5_K;  // the dequantisers copy their own raw bytes
-    static constexpr int R_BYTES = RawTma<T>::R_BYTES;
+    // raw bytes by super-steps (two K steps): every type but Q4_K and Q5_K
+    static constexpr bool SUPER = T != QMM_Q4_K && T != QMM_Q5_K;
+    static_assert(!TM || T == QMM_Q6_K || T == QMM_Q8_0, "raw stages by TMA: Q6_K, Q8_0");
+    static constexpr bool OWN = SUPER && !TM;  // the dequantisers copy their own raw bytes
+    static constexpr bool TMA_RAW = TM;
+    static constexpr bool PERM = TM && T == QMM_Q6_K;  // TMEM lane n holds weight row 2*(n%64) + n/64
+    static constexpr int R_BYTES = TM ? RawTile<T>::R_BYTES : RawTma<T>::R_BYTES;
     static constexpr int XBOX = BT * 128;   // one 64-wide K box of tokens (128-byte swizzle rows)
     static constexpr int X_BYTES = 2 * XBOX;
     static constexpr int RAW_Q = 32 * RawStep<T>::PITCH_W * 4;  // one super-step of a lane quarter's rows (OWN)
     static constexpr int X_FIT = (232448 - 1536 - 4 * RAW_Q) / X_BYTES;
     // (Q5_K's larger raw stages leave room for two 256-token stages)
-    static constexpr int X_STAGES =
-        OWN ? (X_FIT > 8 ? 8 : X_FIT) : (BT == 256 ? (T == QMM_Q5_K ? 2 : 3) : BT == 128 ? 5 : 8);
+    static constexpr int X_FIT_TM = (232448 - 1536 - 2 * R_BYTES) / X_BYTES;  // two raw stages at least
+    static constexpr int X_STAGES = OWN  ? (X_FIT > 8 ? 8 : X_FIT)
+                                    : TM ? (X_FIT_TM > 8 ? 8 : X_FIT_TM)
+                                         : (BT == 256 ? (T == QMM_Q5_K ? 2 : 3) : BT == 128 ? 5 : 8);
     static constexpr int OFF_R = X_STAGES * X_BYTES;
     static constexpr int R_STAGES_FIT = OWN ? 0 : (232448 - 1536 - OFF_R) / R_BYTES;
     static constexpr int R_STAGES = R_STAGES_FIT > 8 ? 8 : R_STAGES_FIT;
@@ -137,7 +173,7 @@ struct TcCfg {
     // D fp32, A and B fp16, both K-major, M = 128 weight rows, N = BT tokens
     static constexpr uint32_t IDESC = (1u << 4) | ((BT >> 3) << 17) | ((BW >> 4) << 24);
     static_assert(X_BYTES % 1024 == 0 && R_BYTES % 1024 == 0, "stage alignment");
-    static_assert(OWN || R_STAGES >= 3, "raw ring depth");
+    static_assert(OWN || R_STAGES >= (TM ? 2 : 3), "raw ring depth");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(16 * (X_STAGES + R_STAGES + A_STAGES) + 8 + 64 <= 480, "barrier area");
     static_assert(BT + A_COLS * A_STAGES <= TMEM_COLS, "tensor memory");
@@ -344,11 +380,11 @@ __device__ __forceinline__ void dequant4(uint32_t w, bool hi, uint32_t fifth, __
     out1 = *reinterpret_cast<const uint32_t *>(&w1);
 }
 
-template <int T, int BT>
+template <int T, int BT, bool TM>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
                    const __grid_constant__ CUtensorMap tmQ, const TcParams P) {
-    using C = TcCfg<BT, T>;
+    using C = TcCfg<BT, T, TM>;
     extern __shared__ uint8_t smem_raw[];
     // stages need 1024-byte alignment for the 128-byte swizzle
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -357,7 +393,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int n0 = (tile % P.nt) * BW, m0 = (tile / P.nt) * BT;
     // this split's K steps [k_step0, k_step0 + nsteps): an even share of the
     // product's super-steps (Q6_K, Q8_0 load whole super-steps) or K steps
-    constexpr int KU = C::OWN ? 2 : 1;
+    constexpr int KU = C::SUPER ? 2 : 1;
     const int ku = P.ksteps / KU;
     const int k_step0 = KU * static_cast<int>(static_cast<int64_t>(blockIdx.z) * ku / P.splits);
     const int nsteps = KU * static_cast<int>(static_cast<int64_t>(blockIdx.z + 1) * ku / P.splits) - k_step0;
@@ -439,8 +475,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     } else if (warp == W_RLOAD) {
-        // ------------------------------------------ raw weight producer (Q4_K)
-        if constexpr (!C::OWN) {
+        // ------------------------------ raw weight producer (Q4_K, Q5_K; TM)
+        if constexpr (C::TMA_RAW) {
+            if (lane == 0) {
+                const int nss = nsteps / 2, js0 = k_step0 / 2;  // this CTA's super-steps
+                int issued = 0;
+                for (int js = 0; js < nss; ++js) {
+                    const int r = js % C::R_STAGES;
+                    if (js >= C::R_STAGES &&
+                        (*abort_flag || !mbar_wait(bar_r_empty + 8 * r, ((js / C::R_STAGES) - 1) & 1, P.status))) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const int gs = js0 + js;  // global super-step
+                    const uint32_t st = sR + r * C::R_BYTES;
+                    mbar_arrive_expect_tx(bar_r_full + 8 * r, RawTile<T>::TX);
+                    if constexpr (T == QMM_Q6_K) {
+                        // boxes from the 16-byte boundary at or below the super-block
+                        // in the even (0) and the odd (1) rows of the double rows
+                        const int rb = static_cast<int>(P.RB);
+                        tma_load_2d(st, &tmH, (210 * gs) & ~15, n0 / 2, bar_r_full + 8 * r);
+                        tma_load_2d(st + RawTile<T>::BOX, &tmH, (rb + 210 * gs) & ~15, n0 / 2, bar_r_full + 8 * r);
+                    } else {
+                        tma_load_2d(st, &tmH, 136 * gs, n0, bar_r_full + 8 * r);
+                    }
+                    ++issued;
+                }
+                for (int js = issued > C::R_STAGES ? issued - C::R_STAGES : 0; js < issued; ++js)
+                    mbar_wait(bar_r_full + 8 * (js % C::R_STAGES), (js / C::R_STAGES) & 1, P.status);
+            }
+        } else if constexpr (!C::OWN) {
             if (lane == 0) {
                 int issued = 0;
                 for (int kk = 0; kk < nsteps; ++kk) {
@@ -493,7 +557,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // the TMEM lanes of quarter w % 4 (weight rows 32*(w%4)..) with weights
         // 64*cp .. 64*cp+63 of the K step, cp = (w - 2) / 4.
         const int quarter = warp & 3, cp = (warp - 2) >> 2;
-        const int n = 32 * quarter + lane;  // weight row within the tile (= TMEM lane)
+        const int n = 32 * quarter + lane;  // TMEM lane
+        const int wr = C::PERM ? 2 * (n & 63) + (n >> 6) : n;  // the weight row (within the tile) it holds
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
         const uint32_t a_col = C::A_COL0 + 32 * cp;  // + A_COLS * stage
         // this row's power of two f_n; both warps of the quarter see the same
@@ -543,7 +608,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             return true;
         };
         auto wfac = [&]() { return f == RS::UNSET ? 1.0f : pow2f(f); };
-        if constexpr (!C::OWN) {
+        if constexpr (!C::SUPER) {
             for (int kk = 0; kk < nsteps; ++kk) {
                 const int r = kk % C::R_STAGES, sa = kk % A_STAGES;
                 bool ok = !*abort_flag;
@@ -618,10 +683,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         } else {
-            // Q6_K / Q8_0: the quarter's 32 rows, one super-step at a time, in
-            // one buffer that its two warps fill (half the chunks each) and
-            // read; p_full / p_empty hand it over (each completes once per
-            // super-step, 64 lanes arriving)
+            // Q6_K, Q8_0, Q3_K, Q2_K: one super-step at a time.  TM: from the
+            // raw stages the producer fills (r_full / r_empty, the eight warps
+            // arriving).  Otherwise the quarter's 32 rows are in one buffer
+            // that its two warps fill (half the chunks each) and read; p_full /
+            // p_empty hand it over (each completes once per super-step, 64
+            // lanes arriving)
             constexpr int SSB = RawStep<T>::BYTES, PW = RawStep<T>::PITCH_W;
             uint8_t *raw = smem + C::OFF_R + quarter * C::RAW_Q;
             const uint32_t p_full = bar_p_full + 8 * quarter, p_empty = bar_p_empty + 8 * quarter;
@@ -674,25 +741,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             make_uint4(stg[4 * t], stg[4 * t + 1], stg[4 * t + 2], stg[4 * t + 3]);
                 }
             };
-            load(0);
-            store();
-            mbar_arrive(p_full);
-            if (nss > 1) load(1);
+            if constexpr (C::OWN) {
+                load(0);
+                store();
+                mbar_arrive(p_full);
+                if (nss > 1) load(1);
+            }
+            // this lane's row of the super-step's raw bytes: from the 16-byte
+            // boundary at or below the super-block (Q6_K, Q3_K, Q2_K) or the
+            // super-step's first block (Q8_0)
             const uint8_t *row = raw + lane * PW * 4;
+            auto tm_row = [&](int js) {
+                const uint8_t *st = smem + C::OFF_R + (js % max(1, C::R_STAGES)) * C::R_BYTES;
+                return C::PERM ? st + (n >> 6) * RawTile<T>::BOX + (n & 63) * RawTile<T>::ROW
+                               : st + n * RawTile<T>::ROW;
+            };
             for (int kk = 0; kk < nsteps; ++kk) {
                 const int js = kk >> 1, h = kk & 1, sa = kk % A_STAGES;
                 bool ok = !*abort_flag;
                 if (ok && kk >= A_STAGES) ok = mbar_wait(bar_a_empty + 8 * sa, ((kk / A_STAGES) - 1) & 1, P.status);
-                if (ok && h == 0) ok = mbar_wait(p_full, js & 1, P.status);
+                if (ok && h == 0) {
+                    if constexpr (C::TMA_RAW)
+                        ok = mbar_wait(bar_r_full + 8 * (js % C::R_STAGES), (js / C::R_STAGES) & 1, P.status);
+                    else
+                        ok = mbar_wait(p_full, js & 1, P.status);
+                }
                 if (__any_sync(0xffffffffu, !ok)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
+                if constexpr (C::TMA_RAW) row = tm_row(js);
                 uint32_t rr[32];
                 if constexpr (T == QMM_Q6_K) {
                     // the super-block starts at this (even) byte of its first chunk
-                    const int dl = static_cast<int>((rows0 + static_cast<uint64_t>(lane) * P.RB +
+                    const int dl = static_cast<int>((reinterpret_cast<uint64_t>(P.W) +
+                                                     static_cast<uint64_t>(n0 + wr) * P.RB +
                                                      static_cast<uint64_t>(js0 + js) * SSB) & 15);
                     // half h of the super-block: ql bytes 64h.., qh 128+32h.., scales
                     // 192+8h.., d at 208; weight 32qi + l: low bits from ql byte
@@ -751,7 +835,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 } else if constexpr (T == QMM_Q3_K) {
                     // the super-block starts at this (even) byte of its first chunk
-                    const int dl = static_cast<int>((rows0 + static_cast<uint64_t>(lane) * P.RB +
+                    const int dl = static_cast<int>((reinterpret_cast<uint64_t>(P.W) +
+                                                     static_cast<uint64_t>(n0 + wr) * P.RB +
                                                      static_cast<uint64_t>(js0 + js) * SSB) & 15);
                     // weight 128h + 32j + l, j = 2cp + jj: low bits (byte 32 + 32h + l
                     // >> 2j) & 3, high bit (mask byte l >> 4h + j) & 1, q + 4 = low |
@@ -803,7 +888,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 } else if constexpr (T == QMM_Q2_K) {
                     // the super-block starts at this (4-byte multiple) byte of its first chunk
-                    const int dl = static_cast<int>((rows0 + static_cast<uint64_t>(lane) * P.RB +
+                    const int dl = static_cast<int>((reinterpret_cast<uint64_t>(P.W) +
+                                                     static_cast<uint64_t>(n0 + wr) * P.RB +
                                                      static_cast<uint64_t>(js0 + js) * SSB) & 15);
                     // weight 128h + 32j + l, j = 2cp + jj: q = (byte 16 + 32h + l >> 2j)
                     // & 3; its group 8h + 4cp + k, k = 2jj + (l >= 16), with scale and
@@ -909,7 +995,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_a_full + 8 * sa);
-                if (h == 1) {
+                if constexpr (C::TMA_RAW) {
+                    // super-step js is read: its raw stage may be refilled
+                    if (h == 1 && lane == 0) mbar_arrive(bar_r_empty + 8 * (js % C::R_STAGES));
+                } else if (h == 1) {
                     // super-step js is read; once the other warp has read it too,
                     // the next one goes into the buffer and the one after that
                     // into the registers
@@ -930,7 +1019,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // half, into y (one split) or into this CTA's partial tile in shared
         // memory (split K: the rings are idle once the accumulator is final)
         const bool ok = mbar_wait(bar_acc, 0, P.status);
-        const int ncol = n0 + n;
+        const int ncol = n0 + wr;
         if (__all_sync(0xffffffffu, ok) && !*abort_flag) {
             tc_fence_after();
             const float rowf = f == RS::UNSET ? 1.0f : pow2f(-f);
@@ -944,7 +1033,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (P.splits > 1) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        red[(cc + i) * BW + n] = i < mrem ? v[i] * rowf * __ldg(xf + i) : 0.0f;
+                        red[(cc + i) * BW + wr] = i < mrem ? v[i] * rowf * __ldg(xf + i) : 0.0f;
                 } else if (ncol < P.N) {
                     float *yc = P.y + static_cast<int64_t>(m0 + cc) * P.N + ncol;
 #pragma unroll
@@ -1026,9 +1115,9 @@ bool tc_supported(int type, int64_t N, int64_t K, int64_t M) {
 // Cached per kernel and cluster size.
 // Clusters of s CTAs of the kernel resident at once (cached; -1: unknown,
 // do not split this way).
-template <int T, int BT>
+template <int T, int BT, bool TM>
 int clusters_resident(int s, int num_sms) {
-    using C = TcCfg<BT, T>;
+    using C = TcCfg<BT, T, TM>;
     static int fit[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};  // 0: not asked yet
     if (fit[s] == 0) {
         int n = 0;
@@ -1043,7 +1132,7 @@ int clusters_resident(int s, int num_sms) {
         attr[0].val.clusterDim.z = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<T, BT>, &cfg) != cudaSuccess || n < 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<T, BT, TM>, &cfg) != cudaSuccess || n < 1) {
             (void)cudaGetLastError();
             n = s == 1 ? num_sms : -1;
         }
@@ -1052,15 +1141,15 @@ int clusters_resident(int s, int num_sms) {
     return fit[s];
 }
 
-template <int T, int BT>
+template <int T, int BT, bool TM>
 int choose_splits(int64_t tiles, int ksteps, int num_sms) {
-    using C = TcCfg<BT, T>;
-    const int kunits = C::OWN ? ksteps / 2 : ksteps;
+    using C = TcCfg<BT, T, TM>;
+    const int kunits = C::SUPER ? ksteps / 2 : ksteps;
     int best = 1;
     double best_cost = 0.0;
     int fit[9];
     for (int s = 1; s <= 8 && s <= kunits; ++s) {
-        fit[s] = clusters_resident<T, BT>(s, num_sms);
+        fit[s] = clusters_resident<T, BT, TM>(s, num_sms);
         if (fit[s] < 1) continue;
         // splitting pays only while the tiles leave SMs idle in one wave
         if (s > 1 && tiles >= fit[1]) break;
@@ -1075,10 +1164,10 @@ int choose_splits(int64_t tiles, int ksteps, int num_sms) {
     return best;
 }
 
-template <int T, int BT>
+template <int T, int BT, bool TM>
 cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, const void *xh, const float *xinv,
                       int64_t M, float *y, cudaStream_t st, int num_sms, int *status) {
-    using C = TcCfg<BT, T>;
+    using C = TcCfg<BT, T, TM>;
     CUtensorMap tx = {}, th = {}, tq = {};
     // tokens: fp16 [M][K], boxes of 64 K x BT rows, 128-byte swizzle
     {
@@ -1094,7 +1183,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     // raw weights as bytes [N][row bytes]: 16-byte boxes (super-block header)
     // and 64-byte boxes (one K step's quants, 64-byte swizzle), 128 rows each
     const int64_t rb = (K / 256) * RawTma<T>::ROW;
-    for (int which = 0; which < 2 && !C::OWN; ++which) {
+    for (int which = 0; which < 2 && !C::SUPER; ++which) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
         const cuuint32_t box[2] = {which ? 64u : static_cast<cuuint32_t>(RawTma<T>::HB), static_cast<cuuint32_t>(BW)};
@@ -1105,10 +1194,26 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    if constexpr (TM) {
+        // Q6_K: N/2 double rows of 2*RB bytes, boxes of 240 bytes x 64 double
+        // rows; Q8_0: N rows of RB bytes as two-byte elements, boxes of 136
+        // elements (272 bytes) x 128 rows.  Out-of-range parts arrive as zeros.
+        const int64_t RB = (K / qk_weights(T)) * qk_block_bytes(T);
+        const bool q6 = T == QMM_Q6_K;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(q6 ? 2 * RB : RB / 2),
+                                    static_cast<cuuint64_t>(q6 ? N / 2 : N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(q6 ? 2 * RB : RB)};
+        const cuuint32_t box[2] = {q6 ? 240u : 136u, q6 ? 64u : 128u};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&th, q6 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W),
+                dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     const int nt = static_cast<int>((N + BW - 1) / BW), mt = static_cast<int>((M + BT - 1) / BT);
     const int ksteps = static_cast<int>(K / BK);
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<T, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(gemm_tc_kernel<T, BT, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t tiles = static_cast<int64_t>(nt) * mt;
     TcParams P;
@@ -1143,15 +1248,15 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = after ? 2 : 1;
-        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T, BT>, tx, th, tq, P);
+        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T, BT, TM>, tx, th, tq, P);
     };
     // Two parts when the tiles leave the last wave partly empty: the whole
     // waves unsplit, then the remaining tiles split along K (clusters) so
     // that they fill the SMs the first part frees.
-    const int fit1 = clusters_resident<T, BT>(1, num_sms);
+    const int fit1 = clusters_resident<T, BT, TM>(1, num_sms);
     if (fit1 > 0 && tiles > fit1 && tiles % fit1 != 0) {
         const int64_t full = tiles / fit1 * fit1, rest = tiles - full;
-        const int s_rest = choose_splits<T, BT>(rest, ksteps, num_sms);
+        const int s_rest = choose_splits<T, BT, TM>(rest, ksteps, num_sms);
         if (s_rest > 1) {
             cudaError_t e2 = launch(0, full, 1, false);
             if (e2 != cudaSuccess) return e2;
@@ -1161,7 +1266,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
             return e2;
         }
     }
-    return launch(0, tiles, choose_splits<T, BT>(tiles, ksteps, num_sms), false);
+    return launch(0, tiles, choose_splits<T, BT, TM>(tiles, ksteps, num_sms), false);
 }
 
 }  // namespace
@@ -1185,18 +1290,25 @@ cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const 
                            int64_t M, float *y, cudaStream_t st, int num_sms, int *status) {
     if (!gemm_tc_supported(type, N, K, M)) return cudaErrorNotSupported;
     EncodeTiled enc = tensor_map_encoder();
-    auto run = [&](auto t) {
+    auto run = [&](auto t, auto tm) {
         constexpr int T = decltype(t)::value;
-        if (M <= 64) return launch_bt<T, 64>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
-        if (M <= 128) return launch_bt<T, 128>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
-        return launch_bt<T, 256>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
+        constexpr bool TM = decltype(tm)::value;
+        if (M <= 64) return launch_bt<T, 64, TM>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
+        if (M <= 128) return launch_bt<T, 128, TM>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
+        return launch_bt<T, 256, TM>(enc, W, N, K, xh, xinv, M, y, st, num_sms, status);
     };
-    if (type == QMM_Q6_K) return run(std::integral_constant<int, QMM_Q6_K>{});
-    if (type == QMM_Q5_K) return run(std::integral_constant<int, QMM_Q5_K>{});
-    if (type == QMM_Q3_K) return run(std::integral_constant<int, QMM_Q3_K>{});
-    if (type == QMM_Q2_K) return run(std::integral_constant<int, QMM_Q2_K>{});
-    if (type == QMM_Q8_0) return run(std::integral_constant<int, QMM_Q8_0>{});
-    return run(std::integral_constant<int, QMM_Q4_K>{});
+    const std::false_type own;
+    const std::true_type tma;
+    // Q6_K raw stages by TMA when rows pair up into 16-byte multiples (K a
+    // multiple of 1024) and N is even; Q8_0 rows are 16-byte multiples
+    if (type == QMM_Q6_K)
+        return (K / 256) % 4 == 0 && N % 2 == 0 ? run(std::integral_constant<int, QMM_Q6_K>{}, tma)
+                                                : run(std::integral_constant<int, QMM_Q6_K>{}, own);
+    if (type == QMM_Q5_K) return run(std::integral_constant<int, QMM_Q5_K>{}, own);
+    if (type == QMM_Q3_K) return run(std::integral_constant<int, QMM_Q3_K>{}, own);
+    if (type == QMM_Q2_K) return run(std::integral_constant<int, QMM_Q2_K>{}, own);
+    if (type == QMM_Q8_0) return run(std::integral_constant<int, QMM_Q8_0>{}, tma);
+    return run(std::integral_constant<int, QMM_Q4_K>{}, own);
 }
 
 }  // namespace qk

@@ -7,11 +7,15 @@ any GPU run (no GPU needed):
   cache and its shared-memory slot; the bytes a lane reads (quant words,
   scales) lie inside what its stage copied; the warps' pair sums fit in the
   rings after the stream; shared memory stays within the per-block limit;
-* the tcgen05 prefill's Q6_K / Q8_0 staging (gemm_tc.cu): each dequantiser
-  warp's 16-byte chunk loads stay inside the matrix unless the kernel's
-  "careful" test selects the word-by-word path, which it does exactly when a
-  chunk would cross the matrix end; the read-back words of a super-block lie
-  inside its staged chunks; the shared-memory plan fits.
+* the tcgen05 prefill's staging of the super-step types (gemm_tc.cu): by
+  TMA for Q8_0, and for Q6_K when K is a multiple of 1024 and N even (the
+  boxes' coordinates meet the 16-byte rule, each row's super-block lies in
+  its box row, the TMEM lane -> weight row map is a permutation whose warps
+  read one box each); otherwise (Q6_K, Q3_K, Q2_K) each dequantiser warp's
+  16-byte chunk loads stay inside the matrix unless the kernel's "careful"
+  test selects the word-by-word path, which it does exactly when a chunk
+  would cross the matrix end; the read-back words of a super-block lie inside
+  its staged bytes; the shared-memory plans fit.
 
 The constants mirror the kernels (16 warps for K <= 160 else 8, ~192 KB of
 rings, stages of 64 / 32 / 16 rows; 14 / 17 chunks per super-step, 60 /
@@ -154,7 +158,7 @@ def tc_smem(BT, T):
     return dict(X=X, SMEM=OFF_BAR + 512 + 1024, RAW_Q=RAW_Q)
 
 
-@pytest.mark.parametrize("T", [QMM_Q6_K, QMM_Q8_0, QMM_Q3_K, QMM_Q2_K])
+@pytest.mark.parametrize("T", [QMM_Q6_K, QMM_Q3_K, QMM_Q2_K])
 @pytest.mark.parametrize("BT", [64, 128, 256])
 def test_tc_own_shared_memory_plan(T, BT):
     P = tc_smem(BT, T)
@@ -167,9 +171,14 @@ def test_tc_own_shared_memory_plan(T, BT):
     assert (PITCH_W[T] * 4 // 16) % 2 == 1
 
 
-@pytest.mark.parametrize("T,N,K", [(QMM_Q6_K, 301, 768), (QMM_Q6_K, 1000, 2048), (QMM_Q6_K, 130, 5120),
-                                   (QMM_Q6_K, 77, 256), (QMM_Q6_K, 5120, 17408), (QMM_Q6_K, 3, 4352),
-                                   (QMM_Q8_0, 301, 768), (QMM_Q8_0, 257, 4352), (QMM_Q8_0, 33, 256),
+def tc_uses_tma(T, N, K):
+    """The dispatch of gemm_tc.cu: raw stages by TMA for Q8_0, and for Q6_K
+    when rows pair up into 16-byte multiples and N is even."""
+    return T == QMM_Q8_0 or (T == QMM_Q6_K and (K // 256) % 4 == 0 and N % 2 == 0)
+
+
+@pytest.mark.parametrize("T,N,K", [(QMM_Q6_K, 301, 768), (QMM_Q6_K, 1001, 2048), (QMM_Q6_K, 130, 5376),
+                                   (QMM_Q6_K, 77, 256), (QMM_Q6_K, 5121, 17408), (QMM_Q6_K, 3, 4352),
                                    (QMM_Q3_K, 301, 768), (QMM_Q3_K, 77, 256), (QMM_Q3_K, 130, 5120),
                                    (QMM_Q3_K, 3, 4352), (QMM_Q2_K, 301, 768), (QMM_Q2_K, 77, 256),
                                    (QMM_Q2_K, 1000, 2048), (QMM_Q2_K, 3, 4352)])
@@ -178,6 +187,7 @@ def test_tc_own_chunk_loads(T, N, K):
     chunks each) stays inside [W, w_end) unless the careful path is taken, and
     the careful path is taken exactly for the matrix's final super-block
     reaching past the end."""
+    assert not tc_uses_tma(T, N, K)
     ssb, CH = SSB[T], CHUNKS[T]
     RB = (K // 32) * 34 if T == QMM_Q8_0 else (K // 256) * BLOCK_BYTES_TC[T]
     odd = T in (QMM_Q6_K, QMM_Q3_K, QMM_Q2_K)  # super-steps not 16-byte multiples
@@ -250,6 +260,88 @@ def test_tc_own_chunk_loads(T, N, K):
                     assert need or odd
     if odd and (N * RB) % 16:
         assert careful_seen >= 1
+
+
+# Q6_K / Q8_0 raw stages by TMA: Q6_K two boxes of 64 double rows x 240
+# bytes (even rows, odd rows), Q8_0 one box of 128 rows x 272 bytes
+TM_ROW = {QMM_Q6_K: 240, QMM_Q8_0: 272}
+TM_TX = {QMM_Q6_K: 2 * 64 * 240, QMM_Q8_0: 128 * 272}
+
+
+def tc_tm_smem(BT, T):
+    X_BYTES = 2 * BT * 128
+    R_BYTES = -(-TM_TX[T] // 1024) * 1024
+    X = min(8, (232448 - 1536 - 2 * R_BYTES) // X_BYTES)
+    OFF_R = X * X_BYTES
+    R = min(8, (232448 - 1536 - OFF_R) // R_BYTES)
+    return dict(X=X, R=R, R_BYTES=R_BYTES, OFF_R=OFF_R, SMEM=OFF_R + R * R_BYTES + 512 + 1024)
+
+
+@pytest.mark.parametrize("T", [QMM_Q6_K, QMM_Q8_0])
+@pytest.mark.parametrize("BT", [64, 128, 256])
+def test_tc_tma_raw_shared_memory_plan(T, BT):
+    P = tc_tm_smem(BT, T)
+    assert P["X"] >= 2 and P["R"] >= 2
+    assert P["SMEM"] <= SMEM_MAX
+    assert 16 * (P["X"] + P["R"] + 4) + 8 + 64 <= 480  # barrier area
+    assert TM_TX[T] <= P["R_BYTES"]
+    # box destinations 128-byte aligned: stages at 1024-byte multiples, Q6_K's
+    # odd-row box 64 rows x 240 bytes after the even one
+    assert P["OFF_R"] % 1024 == 0 and P["R_BYTES"] % 1024 == 0 and (64 * 240) % 128 == 0
+    # box rows an odd number of 16-byte chunks apart: conflict-free chunk reads
+    assert (TM_ROW[T] // 16) % 2 == 1
+
+
+@pytest.mark.parametrize("T,N,K", [(QMM_Q6_K, 1000, 2048), (QMM_Q6_K, 130, 5120), (QMM_Q6_K, 5120, 17408),
+                                   (QMM_Q6_K, 2, 1024), (QMM_Q6_K, 300, 3072), (QMM_Q8_0, 301, 768),
+                                   (QMM_Q8_0, 257, 4352), (QMM_Q8_0, 33, 256), (QMM_Q8_0, 14336, 4096)])
+def test_tc_tma_raw_boxes(T, N, K):
+    """The tensor map's stride is a 16-byte multiple; every box starts on a
+    16-byte boundary (x in bytes); each row's super-step lies inside its box
+    row at the offset dl the dequantiser reads from, and its read-back
+    (chunks, scale word, d) stays inside the box row; TMEM lanes map onto the
+    tile's 128 rows one to one, and a warp's 32 lanes read consecutive rows
+    of one box."""
+    assert tc_uses_tma(T, N, K)
+    W = 1 << 24
+    if T == QMM_Q6_K:
+        RB = (K // 256) * 210
+        assert (2 * RB) % 16 == 0  # the double rows' stride
+        for n0 in range(0, -(-N // 128) * 128, 128):
+            assert n0 % 2 == 0
+            rows = set()
+            for n in range(128):
+                wr = 2 * (n & 63) + (n >> 6)
+                rows.add(wr)
+                box, brow = n >> 6, n & 63
+                assert (n0 // 2 + brow) * 2 + box == n0 + wr  # the box row holds weight row n0 + wr
+                for gs in range(K // 256):
+                    start = box * RB + 210 * gs  # the super-block inside its double row
+                    x = start & ~15              # the box's first byte
+                    assert x % 16 == 0
+                    dl = (W + (n0 + wr) * RB + 210 * gs) & 15  # as the dequantiser computes it
+                    assert dl == start - x and dl % 2 == 0
+                    assert dl + 210 <= TM_ROW[T]
+                    for h in range(2):
+                        assert 16 * (4 * h + 5) <= TM_ROW[T] and 16 * (8 + 2 * h + 3) <= TM_ROW[T]
+                        assert ((dl + 192 + 8 * h + 4) & ~3) + 8 <= TM_ROW[T]
+                    assert dl + 208 + 2 <= TM_ROW[T]
+            assert rows == set(range(128))
+        # warp (quarter q) lanes: rows 32(q % 2) .. of box q // 2, consecutive
+        for q in range(4):
+            ns = [32 * q + lane for lane in range(32)]
+            assert len({n >> 6 for n in ns}) == 1
+            brows = [n & 63 for n in ns]
+            assert brows == list(range(brows[0], brows[0] + 32))
+            for i in range(0, 32, 8):  # 8 lanes per 16-byte wavefront: distinct bank groups
+                assert len({(b * TM_ROW[T] // 16) % 8 for b in brows[i:i + 8]}) == 8
+    else:
+        RB = (K // 32) * 34
+        assert RB % 16 == 0
+        for gs in range(K // 256):
+            assert (136 * gs * 2) % 16 == 0 and 136 * gs * 2 + 272 <= RB
+        for i in range(0, 128, 8):
+            assert len({(r * TM_ROW[T] // 16) % 8 for r in range(i, i + 8)}) == 8
 
 
 # ------------------------------------------- tcgen05 prefill TMA coordinates
