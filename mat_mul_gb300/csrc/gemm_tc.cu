@@ -121,15 +121,16 @@ struct RawStep<QMM_Q2_K> {
     static constexpr int BYTES = 84, CHUNKS = 6, PITCH_W = 28;
 };
 
-// Q6_K and Q8_0 raw stages by TMA (TM): one super-step of the tile's 128
-// rows per stage.
-//   Q6_K, when rows are pairs of 16-byte multiples (K a multiple of 1024,
-//     N even): the matrix seen as N/2 double rows of 2*RB bytes; two boxes of
-//     64 double rows x 240 bytes from the 16-byte boundary at or below the
-//     super-block's start in the even rows (box 0) and in the odd rows (box
-//     1).  TMEM lane n holds weight row 2*(n % 64) + n / 64, so that each
-//     dequantiser warp reads consecutive rows of one box (15 chunks apart:
-//     conflict-free).
+// Raw stages by TMA (TM): one super-step of the tile's 128 rows per stage.
+//   Q6_K, Q3_K, Q2_K, when two rows are a 16-byte multiple (K a multiple of
+//     1024; for Q2_K of 512) and N is even: the matrix seen as N/2 double
+//     rows of 2*RB bytes; two boxes of 64 double rows x ROW bytes from the
+//     16-byte boundary at or below the super-block's start in the even rows
+//     (box 0) and in the odd rows (box 1), ROW an odd number of 16-byte
+//     chunks that holds the super-block at any even offset and every chunk
+//     and word the dequantiser reads (240 / 144 / 112 bytes).  TMEM lane n
+//     holds weight row 2*(n % 64) + n / 64, so that each dequantiser warp
+//     reads consecutive rows of one box (conflict-free).
 //   Q8_0 (rows are 16-byte multiples when K is a multiple of 256): one box of
 //     128 rows x 272 bytes (136 two-byte elements), 17 chunks apart.
 template <int T>
@@ -141,6 +142,14 @@ struct RawTile<QMM_Q6_K> {
     static constexpr int ROW = 240, BOX = 64 * ROW, TX = 2 * BOX, R_BYTES = (TX + 1023) / 1024 * 1024;
 };
 template <>
+struct RawTile<QMM_Q3_K> {
+    static constexpr int ROW = 144, BOX = 64 * ROW, TX = 2 * BOX, R_BYTES = (TX + 1023) / 1024 * 1024;
+};
+template <>
+struct RawTile<QMM_Q2_K> {
+    static constexpr int ROW = 112, BOX = 64 * ROW, TX = 2 * BOX, R_BYTES = (TX + 1023) / 1024 * 1024;
+};
+template <>
 struct RawTile<QMM_Q8_0> {
     static constexpr int ROW = 272, BOX = 128 * ROW, TX = BOX, R_BYTES = (TX + 1023) / 1024 * 1024;
 };
@@ -149,10 +158,10 @@ template <int BT, int T, bool TM = false>
 struct TcCfg {
     // raw bytes by super-steps (two K steps): every type but Q4_K and Q5_K
     static constexpr bool SUPER = T != QMM_Q4_K && T != QMM_Q5_K;
-    static_assert(!TM || T == QMM_Q6_K || T == QMM_Q8_0, "raw stages by TMA: Q6_K, Q8_0");
+    static_assert(!TM || SUPER, "raw stages by TMA: the super-step types");
     static constexpr bool OWN = SUPER && !TM;  // the dequantisers copy their own raw bytes
     static constexpr bool TMA_RAW = TM;
-    static constexpr bool PERM = TM && T == QMM_Q6_K;  // TMEM lane n holds weight row 2*(n%64) + n/64
+    static constexpr bool PERM = TM && T != QMM_Q8_0;  // double rows: TMEM lane n holds weight row 2*(n%64) + n/64
     static constexpr int R_BYTES = TM ? RawTile<T>::R_BYTES : RawTma<T>::R_BYTES;
     static constexpr int XBOX = BT * 128;   // one 64-wide K box of tokens (128-byte swizzle rows)
     static constexpr int X_BYTES = 2 * XBOX;
@@ -490,12 +499,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int gs = js0 + js;  // global super-step
                     const uint32_t st = sR + r * C::R_BYTES;
                     mbar_arrive_expect_tx(bar_r_full + 8 * r, RawTile<T>::TX);
-                    if constexpr (T == QMM_Q6_K) {
+                    if constexpr (C::PERM) {
                         // boxes from the 16-byte boundary at or below the super-block
                         // in the even (0) and the odd (1) rows of the double rows
-                        const int rb = static_cast<int>(P.RB);
-                        tma_load_2d(st, &tmH, (210 * gs) & ~15, n0 / 2, bar_r_full + 8 * r);
-                        tma_load_2d(st + RawTile<T>::BOX, &tmH, (rb + 210 * gs) & ~15, n0 / 2, bar_r_full + 8 * r);
+                        const int rb = static_cast<int>(P.RB), ssb = RawStep<T>::BYTES;
+                        tma_load_2d(st, &tmH, (ssb * gs) & ~15, n0 / 2, bar_r_full + 8 * r);
+                        tma_load_2d(st + RawTile<T>::BOX, &tmH, (rb + ssb * gs) & ~15, n0 / 2, bar_r_full + 8 * r);
                     } else {
                         tma_load_2d(st, &tmH, 136 * gs, n0, bar_r_full + 8 * r);
                     }
@@ -1195,17 +1204,18 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
             return cudaErrorInvalidValue;
     }
     if constexpr (TM) {
-        // Q6_K: N/2 double rows of 2*RB bytes, boxes of 240 bytes x 64 double
-        // rows; Q8_0: N rows of RB bytes as two-byte elements, boxes of 136
-        // elements (272 bytes) x 128 rows.  Out-of-range parts arrive as zeros.
+        // Q6_K, Q3_K, Q2_K: N/2 double rows of 2*RB bytes, boxes of ROW bytes x
+        // 64 double rows; Q8_0: N rows of RB bytes as two-byte elements, boxes
+        // of 136 elements (272 bytes) x 128 rows.  Out-of-range parts arrive
+        // as zeros.
         const int64_t RB = (K / qk_weights(T)) * qk_block_bytes(T);
-        const bool q6 = T == QMM_Q6_K;
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(q6 ? 2 * RB : RB / 2),
-                                    static_cast<cuuint64_t>(q6 ? N / 2 : N)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(q6 ? 2 * RB : RB)};
-        const cuuint32_t box[2] = {q6 ? 240u : 136u, q6 ? 64u : 128u};
+        const bool dr = C::PERM;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(dr ? 2 * RB : RB / 2),
+                                    static_cast<cuuint64_t>(dr ? N / 2 : N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(dr ? 2 * RB : RB)};
+        const cuuint32_t box[2] = {dr ? static_cast<cuuint32_t>(RawTile<T>::ROW) : 136u, dr ? 64u : 128u};
         const cuuint32_t es[2] = {1, 1};
-        if (enc(&th, q6 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W),
+        if (enc(&th, dr ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(W),
                 dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
@@ -1299,14 +1309,16 @@ cudaError_t launch_gemm_tc(int type, const void *W, int64_t N, int64_t K, const 
     };
     const std::false_type own;
     const std::true_type tma;
-    // Q6_K raw stages by TMA when rows pair up into 16-byte multiples (K a
-    // multiple of 1024) and N is even; Q8_0 rows are 16-byte multiples
+    // Q6_K, Q3_K, Q2_K raw stages by TMA when two rows are a 16-byte multiple
+    // and N is even; Q8_0 rows are 16-byte multiples
+    const bool pairs = (2 * (K / 256) * qk_block_bytes(type)) % 16 == 0 && N % 2 == 0;
     if (type == QMM_Q6_K)
-        return (K / 256) % 4 == 0 && N % 2 == 0 ? run(std::integral_constant<int, QMM_Q6_K>{}, tma)
-                                                : run(std::integral_constant<int, QMM_Q6_K>{}, own);
+        return pairs ? run(std::integral_constant<int, QMM_Q6_K>{}, tma) : run(std::integral_constant<int, QMM_Q6_K>{}, own);
+    if (type == QMM_Q3_K)
+        return pairs ? run(std::integral_constant<int, QMM_Q3_K>{}, tma) : run(std::integral_constant<int, QMM_Q3_K>{}, own);
+    if (type == QMM_Q2_K)
+        return pairs ? run(std::integral_constant<int, QMM_Q2_K>{}, tma) : run(std::integral_constant<int, QMM_Q2_K>{}, own);
     if (type == QMM_Q5_K) return run(std::integral_constant<int, QMM_Q5_K>{}, own);
-    if (type == QMM_Q3_K) return run(std::integral_constant<int, QMM_Q3_K>{}, own);
-    if (type == QMM_Q2_K) return run(std::integral_constant<int, QMM_Q2_K>{}, own);
     if (type == QMM_Q8_0) return run(std::integral_constant<int, QMM_Q8_0>{}, tma);
     return run(std::integral_constant<int, QMM_Q4_K>{}, own);
 }

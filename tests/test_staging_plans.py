@@ -8,10 +8,10 @@ any GPU run (no GPU needed):
   scales) lie inside what its stage copied; the warps' pair sums fit in the
   rings after the stream; shared memory stays within the per-block limit;
 * the tcgen05 prefill's staging of the super-step types (gemm_tc.cu): by
-  TMA for Q8_0, and for Q6_K when K is a multiple of 1024 and N even (the
-  boxes' coordinates meet the 16-byte rule, each row's super-block lies in
-  its box row, the TMEM lane -> weight row map is a permutation whose warps
-  read one box each); otherwise (Q6_K, Q3_K, Q2_K) each dequantiser warp's
+  TMA for Q8_0, and for Q6_K, Q3_K and Q2_K when two rows are a 16-byte
+  multiple and N is even (the boxes' coordinates meet the 16-byte rule, each
+  row's super-block lies in its box row, the TMEM lane -> weight row map is a
+  permutation whose warps read one box each); otherwise each dequantiser warp's
   16-byte chunk loads stay inside the matrix unless the kernel's "careful"
   test selects the word-by-word path, which it does exactly when a chunk
   would cross the matrix end; the read-back words of a super-block lie inside
@@ -172,16 +172,16 @@ def test_tc_own_shared_memory_plan(T, BT):
 
 
 def tc_uses_tma(T, N, K):
-    """The dispatch of gemm_tc.cu: raw stages by TMA for Q8_0, and for Q6_K
-    when rows pair up into 16-byte multiples and N is even."""
-    return T == QMM_Q8_0 or (T == QMM_Q6_K and (K // 256) % 4 == 0 and N % 2 == 0)
+    """The dispatch of gemm_tc.cu: raw stages by TMA for Q8_0, and for Q6_K,
+    Q3_K and Q2_K when two rows are a 16-byte multiple and N is even."""
+    return T == QMM_Q8_0 or ((2 * (K // 256) * BLOCK_BYTES_TC[T]) % 16 == 0 and N % 2 == 0)
 
 
 @pytest.mark.parametrize("T,N,K", [(QMM_Q6_K, 301, 768), (QMM_Q6_K, 1001, 2048), (QMM_Q6_K, 130, 5376),
                                    (QMM_Q6_K, 77, 256), (QMM_Q6_K, 5121, 17408), (QMM_Q6_K, 3, 4352),
-                                   (QMM_Q3_K, 301, 768), (QMM_Q3_K, 77, 256), (QMM_Q3_K, 130, 5120),
-                                   (QMM_Q3_K, 3, 4352), (QMM_Q2_K, 301, 768), (QMM_Q2_K, 77, 256),
-                                   (QMM_Q2_K, 1000, 2048), (QMM_Q2_K, 3, 4352)])
+                                   (QMM_Q3_K, 301, 768), (QMM_Q3_K, 77, 256), (QMM_Q3_K, 131, 5120),
+                                   (QMM_Q3_K, 3, 4352), (QMM_Q3_K, 130, 1536), (QMM_Q2_K, 301, 768),
+                                   (QMM_Q2_K, 77, 256), (QMM_Q2_K, 1000, 768), (QMM_Q2_K, 3, 4352)])
 def test_tc_own_chunk_loads(T, N, K):
     """Every 16-byte chunk load of the staging (two warps per quarter, half the
     chunks each) stays inside [W, w_end) unless the careful path is taken, and
@@ -264,8 +264,8 @@ def test_tc_own_chunk_loads(T, N, K):
 
 # Q6_K / Q8_0 raw stages by TMA: Q6_K two boxes of 64 double rows x 240
 # bytes (even rows, odd rows), Q8_0 one box of 128 rows x 272 bytes
-TM_ROW = {QMM_Q6_K: 240, QMM_Q8_0: 272}
-TM_TX = {QMM_Q6_K: 2 * 64 * 240, QMM_Q8_0: 128 * 272}
+TM_ROW = {QMM_Q6_K: 240, QMM_Q3_K: 144, QMM_Q2_K: 112, QMM_Q8_0: 272}
+TM_TX = {QMM_Q6_K: 2 * 64 * 240, QMM_Q3_K: 2 * 64 * 144, QMM_Q2_K: 2 * 64 * 112, QMM_Q8_0: 128 * 272}
 
 
 def tc_tm_smem(BT, T):
@@ -277,7 +277,7 @@ def tc_tm_smem(BT, T):
     return dict(X=X, R=R, R_BYTES=R_BYTES, OFF_R=OFF_R, SMEM=OFF_R + R * R_BYTES + 512 + 1024)
 
 
-@pytest.mark.parametrize("T", [QMM_Q6_K, QMM_Q8_0])
+@pytest.mark.parametrize("T", [QMM_Q6_K, QMM_Q3_K, QMM_Q2_K, QMM_Q8_0])
 @pytest.mark.parametrize("BT", [64, 128, 256])
 def test_tc_tma_raw_shared_memory_plan(T, BT):
     P = tc_tm_smem(BT, T)
@@ -285,15 +285,17 @@ def test_tc_tma_raw_shared_memory_plan(T, BT):
     assert P["SMEM"] <= SMEM_MAX
     assert 16 * (P["X"] + P["R"] + 4) + 8 + 64 <= 480  # barrier area
     assert TM_TX[T] <= P["R_BYTES"]
-    # box destinations 128-byte aligned: stages at 1024-byte multiples, Q6_K's
-    # odd-row box 64 rows x 240 bytes after the even one
-    assert P["OFF_R"] % 1024 == 0 and P["R_BYTES"] % 1024 == 0 and (64 * 240) % 128 == 0
+    # box destinations 128-byte aligned: stages at 1024-byte multiples, the
+    # odd-row box 64 rows x ROW bytes after the even one
+    assert P["OFF_R"] % 1024 == 0 and P["R_BYTES"] % 1024 == 0 and (64 * TM_ROW[T]) % 128 == 0
     # box rows an odd number of 16-byte chunks apart: conflict-free chunk reads
     assert (TM_ROW[T] // 16) % 2 == 1
 
 
 @pytest.mark.parametrize("T,N,K", [(QMM_Q6_K, 1000, 2048), (QMM_Q6_K, 130, 5120), (QMM_Q6_K, 5120, 17408),
-                                   (QMM_Q6_K, 2, 1024), (QMM_Q6_K, 300, 3072), (QMM_Q8_0, 301, 768),
+                                   (QMM_Q6_K, 2, 1024), (QMM_Q6_K, 300, 3072), (QMM_Q3_K, 300, 1024),
+                                   (QMM_Q3_K, 14336, 4096), (QMM_Q3_K, 130, 5120), (QMM_Q2_K, 70, 512),
+                                   (QMM_Q2_K, 14336, 4096), (QMM_Q2_K, 2, 1536), (QMM_Q8_0, 301, 768),
                                    (QMM_Q8_0, 257, 4352), (QMM_Q8_0, 33, 256), (QMM_Q8_0, 14336, 4096)])
 def test_tc_tma_raw_boxes(T, N, K):
     """The tensor map's stride is a 16-byte multiple; every box starts on a
@@ -304,8 +306,9 @@ def test_tc_tma_raw_boxes(T, N, K):
     of one box."""
     assert tc_uses_tma(T, N, K)
     W = 1 << 24
-    if T == QMM_Q6_K:
-        RB = (K // 256) * 210
+    if T != QMM_Q8_0:
+        ssb = SSB[T]
+        RB = (K // 256) * ssb
         assert (2 * RB) % 16 == 0  # the double rows' stride
         for n0 in range(0, -(-N // 128) * 128, 128):
             assert n0 % 2 == 0
@@ -316,16 +319,31 @@ def test_tc_tma_raw_boxes(T, N, K):
                 box, brow = n >> 6, n & 63
                 assert (n0 // 2 + brow) * 2 + box == n0 + wr  # the box row holds weight row n0 + wr
                 for gs in range(K // 256):
-                    start = box * RB + 210 * gs  # the super-block inside its double row
+                    start = box * RB + ssb * gs  # the super-block inside its double row
                     x = start & ~15              # the box's first byte
                     assert x % 16 == 0
-                    dl = (W + (n0 + wr) * RB + 210 * gs) & 15  # as the dequantiser computes it
+                    dl = (W + (n0 + wr) * RB + ssb * gs) & 15  # as the dequantiser computes it
                     assert dl == start - x and dl % 2 == 0
-                    assert dl + 210 <= TM_ROW[T]
+                    assert dl + ssb <= TM_ROW[T]
+                    ROW = TM_ROW[T]
                     for h in range(2):
-                        assert 16 * (4 * h + 5) <= TM_ROW[T] and 16 * (8 + 2 * h + 3) <= TM_ROW[T]
-                        assert ((dl + 192 + 8 * h + 4) & ~3) + 8 <= TM_ROW[T]
-                    assert dl + 208 + 2 <= TM_ROW[T]
+                        if T == QMM_Q6_K:
+                            # ql 5 chunks from 4h, qh 3 from 8 + 2h, the scale word, d
+                            assert 16 * (4 * h + 5) <= ROW and 16 * (8 + 2 * h + 3) <= ROW
+                            assert ((dl + 192 + 8 * h + 4) & ~3) + 8 <= ROW
+                        elif T == QMM_Q3_K:
+                            # mask chunks 0..2, 2-bit chunks 2 + 2h .. 4 + 2h
+                            assert 16 * 3 <= ROW and 16 * (4 + 2 * h + 1) <= ROW
+                        else:
+                            # 2-bit chunks 1 + 2h .. 3 + 2h, the scale word (4-byte aligned)
+                            assert dl % 4 == 0 and 16 * (3 + 2 * h + 1) <= ROW
+                            assert dl + 8 * h + 4 + 4 <= ROW
+                    if T == QMM_Q6_K:
+                        assert dl + 208 + 2 <= ROW
+                    elif T == QMM_Q3_K:
+                        assert ((dl + 108) & ~3) + 8 <= ROW and ((dl + 104) & ~3) + 8 <= ROW
+                    else:
+                        assert dl + 80 + 4 <= ROW
             assert rows == set(range(128))
         # warp (quarter q) lanes: rows 32(q % 2) .. of box q // 2, consecutive
         for q in range(4):
