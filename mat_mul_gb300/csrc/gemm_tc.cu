@@ -395,8 +395,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                    const __grid_constant__ CUtensorMap tmQ, const TcParams P) {
     using C = TcCfg<BT, T, TM>;
     extern __shared__ uint8_t smem_raw[];
-    // stages need 1024-byte alignment for the 128-byte swizzle
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // stages need 1024-byte alignment for the 128-byte swizzle; the base is
+    // advanced by an offset from the array itself (not through an integer
+    // round trip), so that the compiler keeps every pointer derived from it
+    // in the shared state space and reads through them are shared loads
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = P.tile0 + static_cast<int>(blockIdx.x);
     const int n0 = (tile % P.nt) * BW, m0 = (tile / P.nt) * BT;
