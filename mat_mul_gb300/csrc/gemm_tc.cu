@@ -373,6 +373,23 @@ __device__ __forceinline__ void realign(const uint32_t (&w)[NIN], int o, uint32_
     for (int j = 0; j < NOUT; ++j) out[j] = __funnelshift_r(u[j], u[j + 1], (o & 2) * 8);
 }
 
+// out[j] = the 32-bit word at byte o + 4j (o even) past the 4-byte aligned
+// p, from 4-byte loads at p + (o & ~3) shifted by (o & 2) * 8: for a warp
+// whose lanes share o (the double-row TMA stages), cheaper than loading
+// whole chunks and choosing words per lane.
+template <int NOUT>
+__device__ __forceinline__ void words_at(const uint8_t *p, int o, uint32_t (&out)[NOUT]) {
+    const uint32_t *a = reinterpret_cast<const uint32_t *>(p + (o & ~3));
+    const uint32_t sh = static_cast<uint32_t>(o & 2) * 8u;
+    uint32_t prev = a[0];
+#pragma unroll
+    for (int j = 0; j < NOUT; ++j) {
+        const uint32_t next = a[j + 1];
+        out[j] = __funnelshift_r(prev, next, sh);
+        prev = next;
+    }
+}
+
 // Four fp16 weights from the four bytes of a quant word (low nibbles, or
 // high ones when hi; plus, for Q5_K, the fifth bits at bit 4 of each byte):
 // w = q*a + nb with q recovered exactly from the fp16 bit pattern
@@ -804,25 +821,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t scw = row_word(row, dl + 192 + 8 * h + 4 * cp);
                     // ql bytes 64h .. 64h+63 lie in chunks 4h .. 4h+4, qh bytes
                     // 128+32h .. 128+32h+31 in chunks 8+2h .. 10+2h
-                    uint32_t wl[20], wh[12], qh[8], ql[16];
+                    uint32_t qh[8], ql[16];
+                    if constexpr (C::PERM) {
+                        words_at(row + 64 * h, dl, ql);
+                        words_at(row + 128 + 32 * h, dl, qh);
+                    } else {
+                        uint32_t wl[20], wh[12];
 #pragma unroll
-                    for (int c = 0; c < 5; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (4 * h + c));
-                        wl[4 * c] = v.x;
-                        wl[4 * c + 1] = v.y;
-                        wl[4 * c + 2] = v.z;
-                        wl[4 * c + 3] = v.w;
-                    }
+                        for (int c = 0; c < 5; ++c) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (4 * h + c));
+                            wl[4 * c] = v.x;
+                            wl[4 * c + 1] = v.y;
+                            wl[4 * c + 2] = v.z;
+                            wl[4 * c + 3] = v.w;
+                        }
 #pragma unroll
-                    for (int c = 0; c < 3; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (8 + 2 * h + c));
-                        wh[4 * c] = v.x;
-                        wh[4 * c + 1] = v.y;
-                        wh[4 * c + 2] = v.z;
-                        wh[4 * c + 3] = v.w;
+                        for (int c = 0; c < 3; ++c) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (8 + 2 * h + c));
+                            wh[4 * c] = v.x;
+                            wh[4 * c + 1] = v.y;
+                            wh[4 * c + 2] = v.z;
+                            wh[4 * c + 3] = v.w;
+                        }
+                        realign(wl, dl, ql);
+                        realign(wh, dl, qh);
                     }
-                    realign(wl, dl, ql);
-                    realign(wh, dl, qh);
                     const __half2 k1056 = __half2half2(__ushort_as_half(0x6420));  // 1056 = 1024 + 32
 #pragma unroll
                     for (int qq = 0; qq < 2; ++qq) {
@@ -871,16 +894,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         sk[k] = __float2half2_rn(d * static_cast<float>(static_cast<int>((sc4 >> (8 * k)) & 0xFFu) - 32));
                     // mask bytes 0..31 lie in chunks 0..2, the 2-bit bytes 32 + 32h ..
                     // in chunks 2 + 2h .. 4 + 2h
-                    uint32_t wm[12], wq[12], hm[8], qs[8];
+                    uint32_t hm[8], qs[8];
+                    if constexpr (C::PERM) {
+                        words_at(row, dl, hm);
+                        words_at(row + 32 + 32 * h, dl, qs);
+                    } else {
+                        uint32_t wm[12], wq[12];
 #pragma unroll
-                    for (int c = 0; c < 3; ++c) {
-                        const uint4 vm = *reinterpret_cast<const uint4 *>(row + 16 * c);
-                        const uint4 vq = *reinterpret_cast<const uint4 *>(row + 16 * (2 + 2 * h + c));
-                        wm[4 * c] = vm.x, wm[4 * c + 1] = vm.y, wm[4 * c + 2] = vm.z, wm[4 * c + 3] = vm.w;
-                        wq[4 * c] = vq.x, wq[4 * c + 1] = vq.y, wq[4 * c + 2] = vq.z, wq[4 * c + 3] = vq.w;
+                        for (int c = 0; c < 3; ++c) {
+                            const uint4 vm = *reinterpret_cast<const uint4 *>(row + 16 * c);
+                            const uint4 vq = *reinterpret_cast<const uint4 *>(row + 16 * (2 + 2 * h + c));
+                            wm[4 * c] = vm.x, wm[4 * c + 1] = vm.y, wm[4 * c + 2] = vm.z, wm[4 * c + 3] = vm.w;
+                            wq[4 * c] = vq.x, wq[4 * c + 1] = vq.y, wq[4 * c + 2] = vq.z, wq[4 * c + 3] = vq.w;
+                        }
+                        realign(wm, dl, hm);
+                        realign(wq, dl, qs);
                     }
-                    realign(wm, dl, hm);
-                    realign(wq, dl, qs);
                     const __half2 k1028 = __half2half2(__ushort_as_half(0x6404));  // 1028 = 1024 + 4
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
@@ -923,13 +952,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         bk[k] = __float2half2_rn(-(dmin * static_cast<float>((sw >> (8 * k + 4)) & 15u)));
                     }
                     // the 2-bit bytes 16 + 32h .. lie in chunks 1 + 2h .. 3 + 2h
-                    uint32_t wq[12], qs[8];
+                    uint32_t qs[8];
+                    if constexpr (C::PERM) {
+                        words_at(row + 16 + 32 * h, dl, qs);
+                    } else {
+                        uint32_t wq[12];
 #pragma unroll
-                    for (int c = 0; c < 3; ++c) {
-                        const uint4 vq = *reinterpret_cast<const uint4 *>(row + 16 * (1 + 2 * h + c));
-                        wq[4 * c] = vq.x, wq[4 * c + 1] = vq.y, wq[4 * c + 2] = vq.z, wq[4 * c + 3] = vq.w;
+                        for (int c = 0; c < 3; ++c) {
+                            const uint4 vq = *reinterpret_cast<const uint4 *>(row + 16 * (1 + 2 * h + c));
+                            wq[4 * c] = vq.x, wq[4 * c + 1] = vq.y, wq[4 * c + 2] = vq.z, wq[4 * c + 3] = vq.w;
+                        }
+                        realign(wq, dl, qs);
                     }
-                    realign(wq, dl, qs);
                     const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
