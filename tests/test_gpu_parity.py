@@ -429,6 +429,34 @@ def test_qmm_prefill_workload_full_size(cuda_lib):
         _assert_within_bound(y[:, rows], yo, A, f"prefill {name}")
 
 
+# the prefill shapes the bench times beyond the Mistral-7B MLP, with the
+# bench's inputs: the Q6_K v and down of the Qwen3-14B layer (raw stages by
+# TMA, K split in clusters), Q8_0 and the other K-quants in the Mistral up
+# shape (raw stages by TMA), all at M = 512
+PREFILL_BENCH = [("qwen3_14b_v", 3, 2), ("qwen3_14b_down", 3, 6), ("q8_0_mistral_up", synth.Q8_0, 4100),
+                 ("q5_k_mistral_up", synth.Q5_K, 6000 + synth.Q5_K), ("q3_k_mistral_up", synth.Q3_K, 6000 + synth.Q3_K),
+                 ("q2_k_mistral_up", synth.Q2_K, 6000 + synth.Q2_K)]
+
+
+@pytest.mark.parametrize("name,a,b", PREFILL_BENCH)
+def test_qmm_prefill_bench_shapes_full_size(cuda_lib, name, a, b):
+    """Sampled rows (the first and last 64 and 96 random ones) of the
+    prefill products the bench times, against the oracle within the bound."""
+    if name.startswith("qwen3"):
+        qtype, K, N = synth.CONFIGS[a]["mats"][b][1:]
+        W = synth.config_weights(a, b)
+    else:
+        qtype, K, N = a, 4096, 14336
+        W = synth.weights(qtype, N, K, seed=b)
+    x = synth.config_activations(4, 512, K)
+    y = cuda_lib.qmm(qtype, _dev(W), N, K, _dev(x)).cpu().numpy()
+    assert cuda_lib.qmm_device_status() == 0
+    rows = _sample_rows(N, k=96, seed=N)
+    rb = synth.row_bytes(qtype, K)
+    yo, A = O.qmm(qtype, W.reshape(N, rb)[rows], len(rows), K, x)
+    _assert_within_bound(y[:, rows], yo, A, f"prefill {name}")
+
+
 # ------------------------------------------- exact integer special cases
 
 def _int_activations(rng, M, K):
