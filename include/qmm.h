@@ -263,7 +263,8 @@ QMM_API int64_t qmm_launch_count(void);
  * decode product (M <= 8), process-wide, for every later call:
  *   QMM_DECODE_AUTO   : chosen by type and M (default).  Q4_K and Q6_K with
  *                       QMM_TENSOR_MIN_M <= M <= 8 run on the tensor-core
- *                       decode kernel (quantiser + mma.sync, two launches),
+ *                       decode kernel (quantiser + mma.sync, two launches;
+ *                       not Q6_K with K <= 2048 at M <= 4),
  *                       Q4_K and Q5_K with M <= 2 on the row-per-lane dp4a
  *                       kernel (one weight row per lane) where its copy
  *                       sizes suit the shape, everything else on the

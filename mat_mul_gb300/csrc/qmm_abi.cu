@@ -253,6 +253,12 @@ bool decode_on_tensor_cores(int type, int64_t M, int64_t N, int64_t K, const Dev
     const int path = g_decode_path.load();
     if (path == QMM_DECODE_BLOCK) return false;
     if ((path == QMM_DECODE_AUTO || path == QMM_DECODE_ROWS) && (M < QMM_TENSOR_MIN_M || g_no_mma_gemv)) return false;
+    // Q6_K rows of at most 8 super-blocks at M <= 4: a tensor-core stage is a
+    // whole 16-row group, so the group-end sums come every stage; the
+    // block-per-lane kernel was faster there (the 2048 x 128256 lm_head at
+    // M = 3 / 4: 58.6 / 60.3 against 71.5 us)
+    if ((path == QMM_DECODE_AUTO || path == QMM_DECODE_ROWS) && type == QMM_Q6_K && K <= 8 * 256 && M <= 4)
+        return false;
     return qk::gemv_mma_fits(type, static_cast<int>(M), N, K, di.max_smem, di.num_sms);
 }
 }  // namespace

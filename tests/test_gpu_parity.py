@@ -188,6 +188,20 @@ def test_qmm_decode_block_path_on_request(cuda_lib, decode_path, M):
     _assert_within_bound(y, yo, A, f"block-per-lane decode N={N} K={K} M={M}")
 
 
+@pytest.mark.parametrize("M", [3, 4])
+def test_small_k_q6k_decode_on_block_per_lane(cuda_lib, M):
+    """Q6_K with K <= 2048 at M = 3, 4 takes the block-per-lane kernel (one
+    launch, x quantised inside it) by default, and matches the oracle."""
+    N, K = 3000, 2048
+    W = synth.weights(synth.Q6_K, N, K, seed=M + 11)
+    x = synth.activations(M, K, seed=M + 12)
+    before = cuda_lib.qmm_launch_count()
+    y = _run_qmm(cuda_lib, synth.Q6_K, W, N, K, x)
+    assert cuda_lib.qmm_launch_count() - before == 1
+    yo, A = O.qmm(synth.Q6_K, W, N, K, x)
+    _assert_within_bound(y, yo, A, f"Q6_K K={K} M={M}")
+
+
 @pytest.mark.parametrize("qtype,K", [(synth.Q4_K, 5120), (synth.Q6_K, 17408)])
 def test_qmm_decode_tensor_core_is_deterministic(cuda_lib, decode_path, qtype, K):
     import torch

@@ -39,8 +39,11 @@ SCALES = [1e-30, 1e-6, 1.0, 1e4, 1e30]
 # for the small one), tensor-core decode (M = 3..8) and the dp4a decode
 PREFILL = [(synth.Q4_K, 300, 1024, 64), (synth.Q4_K, 200, 2048, 300), (synth.Q6_K, 130, 1536, 64),
            (synth.Q6_K, 257, 1024, 300), (synth.Q8_0, 140, 1024, 64), (synth.Q8_0, 300, 768, 300)]
+# (Q6_K with K <= 2048 at M <= 4 runs on the block-per-lane kernel, K = 2560
+# at M = 4 on the tensor-core one)
 DECODE = [(synth.Q4_K, 300, 5120, 3), (synth.Q4_K, 77, 2048, 8), (synth.Q6_K, 301, 2048, 4),
-          (synth.Q6_K, 129, 5120, 8), (synth.Q4_K, 300, 2048, 1), (synth.Q6_K, 100, 1024, 2)]
+          (synth.Q6_K, 301, 2560, 4), (synth.Q6_K, 129, 5120, 8), (synth.Q4_K, 300, 2048, 1),
+          (synth.Q6_K, 100, 1024, 2)]
 
 
 @pytest.mark.parametrize("scale", SCALES)
