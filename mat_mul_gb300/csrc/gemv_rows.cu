@@ -1,5 +1,6 @@
 // gemv_rows.cu -- the row-per-lane decode kernel (gemv_rows.cuh has the
-// design) for M <= 2, Q4_K and Q6_K, and the entry points of every M.
+// design) for M <= 2 (Q4_K, Q5_K, Q6_K, Q3_K, Q2_K), and the entry points of
+// every M.
 #include "gemv_rows.cuh"
 
 namespace qk {
@@ -7,8 +8,9 @@ namespace qk {
 using namespace rwk;
 
 bool gemv_rows_fits(int type, int M, int64_t K, int max_smem) {
-    // Q4_K for M <= 8, Q5_K and Q6_K for M <= 2
-    if ((type != QMM_Q4_K && type != QMM_Q5_K && type != QMM_Q6_K) || M < 1 || M > (type == QMM_Q4_K ? 8 : 2) ||
+    // Q4_K for M <= 8, Q5_K, Q6_K, Q3_K and Q2_K for M <= 2
+    if ((type != QMM_Q4_K && type != QMM_Q5_K && type != QMM_Q6_K && type != QMM_Q3_K && type != QMM_Q2_K) ||
+        M < 1 || M > (type == QMM_Q4_K ? 8 : 2) ||
         K < 256 || K % 256 != 0 || K > (1 << 22))
         return false;
     const Shape sh = choose_shape(K / 256, block_bytes(type));
@@ -17,15 +19,24 @@ bool gemv_rows_fits(int type, int M, int64_t K, int max_smem) {
     return plan_rows(type, M, K, max_smem, sh.CW, sh.H, R, smem);
 }
 
-bool gemv_rows_preferred(int type, int64_t N, int64_t K) {
+bool gemv_rows_preferred(int type, int M, int64_t N, int64_t K) {
     // Q6_K rows are 2-byte aligned and read as 32-bit words: at any 16-byte
     // row pitch, 32 lanes on GR rows meet GR/8-way bank conflicts, which the
     // block-per-lane kernel (lanes on consecutive blocks) does not have
-    if (type != QMM_Q4_K && type != QMM_Q5_K) return false;
+    if (type != QMM_Q4_K && type != QMM_Q5_K && type != QMM_Q3_K && type != QMM_Q2_K) return false;
+    // at M = 2 the block-per-lane kernel's per-lane activation reads double;
+    // the row-per-lane kernel was as fast or faster on every Q5_K, Q3_K and
+    // Q2_K shape measured (5120 -> 17408, 17408 -> 5120, 2048 -> 8192)
+    if (M == 2 && type != QMM_Q4_K) return true;
+    // Q3_K and Q2_K at M = 1: faster on rows at K = 2048 and 5120, slower at
+    // K = 17408 (measured)
+    if (type == QMM_Q3_K || type == QMM_Q2_K) return K <= 8192;
     // below full copy efficiency the block-per-lane kernel's long contiguous
     // copies win on large matrices; small ones gain from the shorter setup
+    // (Q5_K at 17408 -> 5120, score 0.85, measured faster on rows)
     const Shape sh = choose_shape(K / 256, block_bytes(type));
-    return sh.score >= 0.9 || N * (K / 256) * block_bytes(type) <= (int64_t(16) << 20);
+    const double need = type == QMM_Q5_K ? 0.8 : 0.9;
+    return sh.score >= need || N * (K / 256) * block_bytes(type) <= (int64_t(16) << 20);
 }
 
 cudaError_t launch_gemv_rows(int type, const void *W, int64_t N, int64_t K, const float *x, int M, float *y,
@@ -52,6 +63,12 @@ cudaError_t launch_gemv_rows(int type, const void *W, int64_t N, int64_t K, cons
     if (type == QMM_Q5_K)
         return M <= 1 ? launch_single<QMM_Q5_K, 1>(R, sh.CW, sh.H, g, smem, st)
                       : launch_single<QMM_Q5_K, 2>(R, sh.CW, sh.H, g, smem, st);
+    if (type == QMM_Q3_K)
+        return M <= 1 ? launch_single<QMM_Q3_K, 1>(R, sh.CW, sh.H, g, smem, st)
+                      : launch_single<QMM_Q3_K, 2>(R, sh.CW, sh.H, g, smem, st);
+    if (type == QMM_Q2_K)
+        return M <= 1 ? launch_single<QMM_Q2_K, 1>(R, sh.CW, sh.H, g, smem, st)
+                      : launch_single<QMM_Q2_K, 2>(R, sh.CW, sh.H, g, smem, st);
     return M <= 1 ? launch_single<QMM_Q6_K, 1>(R, sh.CW, sh.H, g, smem, st)
                   : launch_single<QMM_Q6_K, 2>(R, sh.CW, sh.H, g, smem, st);
 }

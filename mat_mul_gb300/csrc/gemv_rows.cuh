@@ -1,6 +1,6 @@
 // gemv_rows.cuh -- the row-per-lane decode kernel (device code, shared-memory
 // plan and launch templates), instantiated by gemv_rows.cu (M <= 2, Q4_K,
-// Q5_K and Q6_K) and gemv_rows_wide.cu (3 <= M <= 8, Q4_K): decode product
+// Q5_K, Q6_K, Q3_K and Q2_K) and gemv_rows_wide.cu (3 <= M <= 8, Q4_K): decode product
 // y[M,N] = W[N,K] . x[M,K]^T with one weight row per lane.
 //
 // Design (sm_103a):
@@ -72,6 +72,8 @@ template <int T, int MT>
 __device__ __forceinline__ void superblock(const XS &X, int blk, int kb, float (&v)[MT]) {
     if constexpr (T == QMM_Q4_K) sb_q4k<MT>(X, blk, kb, v);
     else if constexpr (T == QMM_Q5_K) sb_q5k<MT>(X, blk, kb, v);
+    else if constexpr (T == QMM_Q3_K) sb_q3k<MT>(X, blk, kb, v);
+    else if constexpr (T == QMM_Q2_K) sb_q2k<MT>(X, blk, kb, v);
     else sb_q6k<MT>(X, blk, kb, v);
 }
 

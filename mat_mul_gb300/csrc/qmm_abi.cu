@@ -240,7 +240,7 @@ bool decode_on_rows(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo 
     if (M < 1 || M > 8 || g_no_mma_gemv) return false;
     const int path = g_decode_path.load();
     if (path == QMM_DECODE_BLOCK) return false;
-    if (path != QMM_DECODE_ROWS && (M > 2 || !qk::gemv_rows_preferred(type, N, K))) return false;
+    if (path != QMM_DECODE_ROWS && (M > 2 || !qk::gemv_rows_preferred(type, static_cast<int>(M), N, K))) return false;
     return qk::gemv_rows_fits(type, static_cast<int>(M), K, di.max_smem);
 }
 

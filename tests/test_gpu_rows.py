@@ -1,5 +1,5 @@
-"""GPU parity of the row-per-lane decode kernel (Q4_K, Q5_K and Q6_K at
-M <= 2, Q4_K up to M = 8) against the CPU oracle, within the library's
+"""GPU parity of the row-per-lane decode kernel (Q4_K, Q5_K, Q6_K, Q3_K and
+Q2_K at M <= 2, Q4_K up to M = 8) against the CPU oracle, within the library's
 bound |y_gpu - y_oracle| <= 2e-3 * sum_k |w_k xhat_k| + 1e-5.
 
 The shapes cover what the kernel's plan and indexing branch on: a CTA's row
@@ -45,6 +45,9 @@ CASES = [
     (synth.Q4_K, 200, 17408, 2), (synth.Q4_K, 9000, 2048, 2),
     (synth.Q6_K, 1, 256, 1), (synth.Q6_K, 3, 512, 2), (synth.Q6_K, 77, 2048, 1), (synth.Q6_K, 33, 2560, 2),
     (synth.Q6_K, 301, 4608, 2), (synth.Q6_K, 4097, 5120, 1), (synth.Q6_K, 150, 17408, 1),
+    (synth.Q3_K, 1, 256, 1), (synth.Q3_K, 77, 2048, 2), (synth.Q3_K, 301, 4608, 1), (synth.Q3_K, 4097, 5120, 2),
+    (synth.Q3_K, 150, 17408, 1), (synth.Q2_K, 3, 512, 2), (synth.Q2_K, 33, 2560, 1), (synth.Q2_K, 300, 4608, 2),
+    (synth.Q2_K, 4865, 5120, 1), (synth.Q2_K, 200, 17408, 2),
     (synth.Q6_K, 120, 17408, 2),
     (synth.Q5_K, 1, 256, 1), (synth.Q5_K, 77, 2048, 2), (synth.Q5_K, 300, 5120, 1), (synth.Q5_K, 4097, 5120, 2),
     (synth.Q5_K, 150, 17408, 1),

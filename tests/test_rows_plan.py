@@ -22,9 +22,9 @@ SMS = 152
 XPITCH = 272
 HEAD = 256
 MAX_NS = 8
-Q4_K, Q5_K, Q6_K = 1, 3, 2
-BB = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
-REC = {Q4_K: 80, Q5_K: 80, Q6_K: 112}
+Q4_K, Q5_K, Q6_K, Q3_K, Q2_K = 1, 3, 2, 4, 5
+BB = {Q4_K: 144, Q5_K: 176, Q6_K: 210, Q3_K: 110, Q2_K: 84}
+REC = {Q4_K: 80, Q5_K: 80, Q6_K: 112, Q3_K: 112, Q2_K: 112}
 
 
 def choose_shape(nb, bb):
@@ -72,7 +72,7 @@ def fits(qtype, M, K):
     return plan_rows(qtype, M, K, cw, h)
 
 
-@pytest.mark.parametrize("qtype", [Q4_K, Q5_K, Q6_K])
+@pytest.mark.parametrize("qtype", [Q4_K, Q5_K, Q6_K, Q3_K, Q2_K])
 @pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_shared_memory_plan(qtype, M):
     for K in range(256, 65536 + 1, 256):
@@ -118,6 +118,8 @@ def grid_of(N, K, qtype):
     (Q6_K, 1, 256, 1), (Q6_K, 3, 512, 2), (Q6_K, 77, 2048, 1), (Q6_K, 301, 4608, 2), (Q6_K, 150, 17408, 1),
     (Q6_K, 5120, 17408, 1), (Q6_K, 4097, 5120, 1),
     (Q5_K, 1, 256, 1), (Q5_K, 77, 2048, 2), (Q5_K, 4097, 5120, 2), (Q5_K, 150, 17408, 1),
+    (Q3_K, 1, 256, 1), (Q3_K, 77, 2048, 2), (Q3_K, 301, 4608, 1), (Q3_K, 4097, 5120, 2), (Q3_K, 150, 17408, 1),
+    (Q2_K, 3, 512, 2), (Q2_K, 33, 2560, 1), (Q2_K, 300, 4608, 2), (Q2_K, 4865, 5120, 1), (Q2_K, 200, 17408, 2),
 ])
 def test_copies_cover_each_row_span_and_reads_stay_inside(qtype, N, K, M):
     p = fits(qtype, M, K)
