@@ -265,17 +265,19 @@ QMM_API int64_t qmm_launch_count(void);
  *                       QMM_TENSOR_MIN_M <= M <= 8 run on the tensor-core
  *                       decode kernel (quantiser + mma.sync, two launches;
  *                       not Q6_K with K <= 2048 at M <= 4),
- *                       Q4_K, Q5_K, Q3_K and Q2_K with M <= 2 on the
- *                       row-per-lane dp4a kernel (one weight row per lane)
- *                       where its copy sizes suit the shape (at M = 2 always
- *                       for Q5_K, Q3_K and Q2_K), everything else on the
- *                       block-per-lane dp4a kernel.
+ *                       Q4_K with M <= 2 and Q5_K, Q3_K and Q2_K with
+ *                       M <= 8 on the row-per-lane dp4a kernel (one weight
+ *                       row per lane) where its copy sizes suit the shape
+ *                       (from M = 2 on always for Q5_K, Q3_K and Q2_K),
+ *                       everything else on the block-per-lane dp4a kernel;
+ *                       a product that no decode kernel holds (x too large
+ *                       for shared memory) on the prefill kernel.
  *   QMM_DECODE_BLOCK  : the block-per-lane kernel wherever it fits.
  *   QMM_DECODE_TENSOR : the tensor-core kernel for every Q4_K / Q6_K product
  *                       with 2 <= M <= 8 that fits it (Q6_K: K a multiple
  *                       of 512); M = 1 as with QMM_DECODE_AUTO.
  *   QMM_DECODE_ROWS   : the row-per-lane kernel for every product it takes
- *                       (Q4_K with M <= 8, Q5_K, Q6_K, Q3_K and Q2_K with
+ *                       (Q4_K, Q5_K, Q3_K and Q2_K with M <= 8, Q6_K with
  *                       M <= 2), else as QMM_DECODE_AUTO.
  * Results of the paths agree within the accuracy bound of qmm(), not bit
  * for bit.  Returns the previous path, or QMM_EINVAL_SHAPE for an unknown

@@ -1,6 +1,6 @@
 // gemv_rows.cu -- the row-per-lane decode kernel (gemv_rows.cuh has the
 // design) for M <= 2 (Q4_K, Q5_K, Q6_K, Q3_K, Q2_K), and the entry points of
-// every M.
+// every M (gemv_rows_wide.cu and gemv_rows_wide_kq.cu: 3 <= M <= 8).
 #include "gemv_rows.cuh"
 
 namespace qk {
@@ -8,9 +8,9 @@ namespace qk {
 using namespace rwk;
 
 bool gemv_rows_fits(int type, int M, int64_t K, int max_smem) {
-    // Q4_K for M <= 8, Q5_K, Q6_K, Q3_K and Q2_K for M <= 2
+    // Q4_K, Q5_K, Q3_K and Q2_K for M <= 8, Q6_K for M <= 2
     if ((type != QMM_Q4_K && type != QMM_Q5_K && type != QMM_Q6_K && type != QMM_Q3_K && type != QMM_Q2_K) ||
-        M < 1 || M > (type == QMM_Q4_K ? 8 : 2) ||
+        M < 1 || M > (type == QMM_Q6_K ? 2 : 8) ||
         K < 256 || K % 256 != 0 || K > (1 << 22))
         return false;
     const Shape sh = choose_shape(K / 256, block_bytes(type));
@@ -24,10 +24,13 @@ bool gemv_rows_preferred(int type, int M, int64_t N, int64_t K) {
     // row pitch, 32 lanes on GR rows meet GR/8-way bank conflicts, which the
     // block-per-lane kernel (lanes on consecutive blocks) does not have
     if (type != QMM_Q4_K && type != QMM_Q5_K && type != QMM_Q3_K && type != QMM_Q2_K) return false;
-    // at M = 2 the block-per-lane kernel's per-lane activation reads double;
-    // the row-per-lane kernel was as fast or faster on every Q5_K, Q3_K and
-    // Q2_K shape measured (5120 -> 17408, 17408 -> 5120, 2048 -> 8192)
-    if (M == 2 && type != QMM_Q4_K) return true;
+    // Q4_K from M = 3 on runs on the tensor cores
+    if (type == QMM_Q4_K && M > 2) return false;
+    // from M = 2 on the block-per-lane kernel's per-lane activation reads
+    // multiply; the row-per-lane kernel was as fast or faster on every Q5_K,
+    // Q3_K and Q2_K shape measured (5120 -> 17408, 17408 -> 5120, 2048 ->
+    // 8192; M = 2, 4, 8)
+    if (M >= 2 && type != QMM_Q4_K) return true;
     // Q3_K and Q2_K at M = 1: faster on rows at K = 2048 and 5120, slower at
     // K = 17408 (measured)
     if (type == QMM_Q3_K || type == QMM_Q2_K) return K <= 8192;

@@ -1,17 +1,26 @@
 // gemv_rows_wide.cu -- the row-per-lane decode kernel (gemv_rows.cuh) for
-// 3 <= M <= 8 activation rows, Q4_K: the same stages and lanes, MT = 4 or 8
-// accumulators per lane (rows M .. MT-1 of the activations are computed on
-// and never written).  A translation unit of its own so that it compiles in
-// parallel with the M <= 2 instantiations.
+// 3 <= M <= 8 activation rows, Q4_K and Q5_K (Q3_K and Q2_K in
+// gemv_rows_wide_kq.cu): the same stages and lanes, MT = 4 or 8 accumulators
+// per lane (rows M .. MT-1 of the activations are computed on and never
+// written).  Translation units of their own so that they compile in parallel
+// with the M <= 2 instantiations.
 #include "gemv_rows.cuh"
 
 namespace qk {
 namespace rwk {
 
 cudaError_t launch_rows_wide(const RwParams &R, int MT, int CW, int H, int grid, int smem, cudaStream_t st) {
-    if (R.q.type != QMM_Q4_K) return cudaErrorNotSupported;
-    return MT == 4 ? launch_single<QMM_Q4_K, 4>(R, CW, H, grid, smem, st)
-                   : launch_single<QMM_Q4_K, 8>(R, CW, H, grid, smem, st);
+    switch (R.q.type) {
+    case QMM_Q4_K:
+        return MT == 4 ? launch_single<QMM_Q4_K, 4>(R, CW, H, grid, smem, st)
+                       : launch_single<QMM_Q4_K, 8>(R, CW, H, grid, smem, st);
+    case QMM_Q5_K:
+        return MT == 4 ? launch_single<QMM_Q5_K, 4>(R, CW, H, grid, smem, st)
+                       : launch_single<QMM_Q5_K, 8>(R, CW, H, grid, smem, st);
+    case QMM_Q3_K:
+    case QMM_Q2_K: return launch_rows_wide_kq(R, MT, CW, H, grid, smem, st);
+    default: return cudaErrorNotSupported;
+    }
 }
 
 cudaError_t launch_rows_wide_group(const RwGroup &G, int MT, int CW, int H, int grid, int smem, cudaStream_t st) {

@@ -240,7 +240,7 @@ bool decode_on_rows(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo 
     if (M < 1 || M > 8 || g_no_mma_gemv) return false;
     const int path = g_decode_path.load();
     if (path == QMM_DECODE_BLOCK) return false;
-    if (path != QMM_DECODE_ROWS && (M > 2 || !qk::gemv_rows_preferred(type, static_cast<int>(M), N, K))) return false;
+    if (path != QMM_DECODE_ROWS && !qk::gemv_rows_preferred(type, static_cast<int>(M), N, K)) return false;
     return qk::gemv_rows_fits(type, static_cast<int>(M), K, di.max_smem);
 }
 
@@ -387,7 +387,9 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
     //   gemv : decode, 32 units per round, after the quantiser kernel
     //   gemm : prefill after the quantiser: on tcgen05 (fp16 operands, fp32
     //          accumulators) when K is a multiple of 256, else on the int8
-    //          mma.sync kernel
+    //          mma.sync kernel; also a decode (M <= 8) that none of the
+    //          decode kernels above can hold (their activations do not fit),
+    //          which the round-based decode would take many times longer for
     if (!(rows_first() && decode_on_rows(type, M, N, K, di)) && decode_on_tensor_cores(type, M, N, K, di)) {
         void *ws = nullptr;
         if (int rc = quantize_for_tensor_cores(dev, st, x, M, K, di, &ws)) return rc;
@@ -411,8 +413,10 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
         g_launches.fetch_add(1);
         return QMM_OK;
     }
-    // Prefill on the tcgen05 kernel: fp16 activations d*q [M][K].
-    if (M > 8 && !g_force_mma_gemm && g_prefill_path.load() == QMM_PREFILL_AUTO &&
+    // Prefill on the tcgen05 kernel: fp16 activations d*q [M][K].  (At M <= 8
+    // only when none of the decode kernels fits: e.g. Q5_K / Q3_K / Q2_K at
+    // M = 8 and K = 17408, 14x faster than the round-based decode.)
+    if ((M > 8 || !g_force_round_gemv) && !g_force_mma_gemm && g_prefill_path.load() == QMM_PREFILL_AUTO &&
         qk::gemm_tc_supported(type, N, K, M)) {
         const size_t xh_bytes = align_up(static_cast<size_t>(M * K) * 2, 256);
         const size_t xinv_bytes = align_up(static_cast<size_t>(M) * 4, 256);

@@ -79,16 +79,17 @@ cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws,
                                  int max_smem, int *status);
 void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t *need, int num_sms, int *g);
 
-// Row-per-lane decode kernel (gemv_rows.cu): Q4_K for M <= 8, Q5_K, Q6_K,
-// Q3_K and Q2_K for M <= 2, K a multiple of 256; quantises x itself (one
+// Row-per-lane decode kernel (gemv_rows.cu): Q4_K, Q5_K, Q3_K and Q2_K for
+// M <= 8, Q6_K for M <= 2, K a multiple of 256; quantises x itself (one
 // launch, no workspace), launched with programmatic dependent launch.  The
 // group launch takes several Q4_K / Q6_K matrices sharing K and x (CTAs
 // split as in group_ctas); cudaErrorNotSupported when one of them does not
 // fit the kernel's plan or is of another type.
 bool gemv_rows_fits(int type, int M, int64_t K, int max_smem);
 // Whether the row-per-lane kernel is the faster choice for this matrix (by
-// its copy sizes and the matrix size; at M = 2 always for Q5_K, Q3_K and
-// Q2_K); qmm_set_decode_path(QMM_DECODE_ROWS) takes it wherever it fits.
+// its copy sizes and the matrix size; from M = 2 on always for Q5_K, Q3_K
+// and Q2_K, never for Q4_K beyond M = 2); qmm_set_decode_path(
+// QMM_DECODE_ROWS) takes it wherever it fits.
 bool gemv_rows_preferred(int type, int M, int64_t N, int64_t K);
 cudaError_t launch_gemv_rows(int type, const void *W, int64_t N, int64_t K, const float *x, int M, float *y,
                              cudaStream_t st, int num_sms, int max_smem, int *status);

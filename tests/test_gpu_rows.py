@@ -1,5 +1,5 @@
 """GPU parity of the row-per-lane decode kernel (Q4_K, Q5_K, Q6_K, Q3_K and
-Q2_K at M <= 2, Q4_K up to M = 8) against the CPU oracle, within the library's
+Q2_K at M <= 2, all but Q6_K up to M = 8) against the CPU oracle, within the library's
 bound |y_gpu - y_oracle| <= 2e-3 * sum_k |w_k xhat_k| + 1e-5.
 
 The shapes cover what the kernel's plan and indexing branch on: a CTA's row
@@ -54,11 +54,14 @@ CASES = [
 ]
 
 
-# Q4_K with 3 <= M <= 8: four or eight accumulators per lane (the rows of
-# the activations past M are computed on and never written)
+# Q4_K, Q5_K, Q3_K and Q2_K with 3 <= M <= 8: four or eight accumulators per
+# lane (the rows of the activations past M are computed on and never written)
 CASES_WIDE = [
     (synth.Q4_K, 1, 256, 3), (synth.Q4_K, 33, 2048, 4), (synth.Q4_K, 300, 4608, 5), (synth.Q4_K, 4865, 5120, 8),
     (synth.Q4_K, 200, 10240, 6), (synth.Q4_K, 77, 1024, 7), (synth.Q4_K, 5, 5120, 4),
+    (synth.Q5_K, 33, 2048, 3), (synth.Q5_K, 300, 5120, 8), (synth.Q5_K, 150, 17408, 4),
+    (synth.Q3_K, 1, 256, 5), (synth.Q3_K, 301, 4608, 4), (synth.Q3_K, 200, 5120, 8),
+    (synth.Q2_K, 77, 1024, 7), (synth.Q2_K, 4865, 5120, 4), (synth.Q2_K, 120, 17408, 3),
 ]
 
 
@@ -141,3 +144,20 @@ def test_rows_group_one_launch_wide(cuda_lib, rows_path, M):
             continue
         yo, A = O.qmm(t, W, N, K, x)
         _check(y.cpu().numpy(), yo, A, f"group entry N={N} M={M}")
+
+
+# Q5_K, Q3_K and Q2_K at M = 8 with K = 17408: neither decode kernel holds the
+# activations in shared memory, so the product runs on the tcgen05 prefill
+# kernel (the quantiser, then the GEMM) instead of the round-based decode
+@pytest.mark.parametrize("qtype,N,M", [(synth.Q5_K, 300, 8), (synth.Q3_K, 200, 8), (synth.Q2_K, 150, 7)])
+def test_decode_too_large_for_the_decode_kernels(cuda_lib, qtype, N, M):
+    q = cuda_lib
+    K = 17408
+    W = synth.weights(qtype, N, K, seed=N + M)
+    x = synth.activations(M, K, seed=N + 2 * M, outlier_frac=0.01)
+    before = q.qmm_launch_count()
+    y = q.qmm(qtype, _dev(W), N, K, _dev(x)).cpu().numpy()
+    assert q.qmm_device_status() == 0
+    assert q.qmm_launch_count() - before == 2
+    yo, A = O.qmm(qtype, W, N, K, x)
+    _check(y, yo, A, f"type {qtype} N={N} K={K} M={M}")

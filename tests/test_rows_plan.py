@@ -66,7 +66,7 @@ def plan_rows(qtype, M, K, CW, H, max_smem=SMEM_MAX):
 
 
 def fits(qtype, M, K):
-    if qtype not in BB or M < 1 or M > (8 if qtype == Q4_K else 2) or K < 256 or K % 256:
+    if qtype not in BB or M < 1 or M > (2 if qtype == Q6_K else 8) or K < 256 or K % 256:
         return None
     cw, h, _ = choose_shape(K // 256, BB[qtype])
     return plan_rows(qtype, M, K, cw, h)
