@@ -128,13 +128,16 @@ QMM_API int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const floa
  *                W 16-byte aligned, K a multiple of every type's QK; an entry
  *                with N = 0 is skipped.
  *   K, x, M, stream : shared by all entries, as in qmm().
- * When every entry takes the block-per-lane decode kernel (M = 1, M = 2,
- * see qmm_set_decode_path) the whole group is ONE launch of it: its CTAs are
- * split between the matrices in proportion to their weight bytes and each
- * quantises x itself.  When every entry takes the tensor-core decode kernel
- * (Q4_K / Q6_K at QMM_TENSOR_MIN_M <= M <= 8) x is quantised once and each
- * matrix is one decode launch.  Otherwise the products run one after another
- * as qmm() calls.  Accuracy as qmm().
+ * When every entry takes one of the one-weight-stream decode kernels (the
+ * row-per-lane one for Q4_K and Q6_K, the block-per-lane one for Q8_0, Q4_K
+ * and Q6_K; M <= 2, see qmm_set_decode_path), and under QMM_DECODE_AUTO for
+ * two or more Q4_K / Q6_K matrices at QMM_TENSOR_MIN_M <= M <= 4, the whole
+ * group is ONE launch of that kernel: its CTAs are split between the
+ * matrices in proportion to their weight bytes and each quantises x itself.
+ * When every entry takes the tensor-core decode kernel (Q4_K / Q6_K, up to
+ * M = 8) x is quantised once and each matrix is one decode launch.
+ * Otherwise the products run one after another as qmm() calls.  Accuracy as
+ * qmm().
  * Every entry is validated before anything is launched; errors as qmm(),
  * QMM_EINVAL_SHAPE for n out of range, QMM_EINVAL_PTR for a null array.
  */
@@ -271,14 +274,16 @@ QMM_API int64_t qmm_launch_count(void);
  *                       (from M = 2 on always for Q5_K, Q3_K and Q2_K),
  *                       everything else on the block-per-lane dp4a kernel;
  *                       a product that no decode kernel holds (x too large
- *                       for shared memory) on the prefill kernel.
+ *                       for shared memory) on the prefill kernel.  A
+ *                       qmm_group of Q4_K / Q6_K matrices at
+ *                       QMM_TENSOR_MIN_M <= M <= 4: one row-per-lane launch.
  *   QMM_DECODE_BLOCK  : the block-per-lane kernel wherever it fits.
  *   QMM_DECODE_TENSOR : the tensor-core kernel for every Q4_K / Q6_K product
  *                       with 2 <= M <= 8 that fits it (Q6_K: K a multiple
  *                       of 512); M = 1 as with QMM_DECODE_AUTO.
  *   QMM_DECODE_ROWS   : the row-per-lane kernel for every product it takes
- *                       (Q4_K, Q5_K, Q3_K and Q2_K with M <= 8, Q6_K with
- *                       M <= 2), else as QMM_DECODE_AUTO.
+ *                       (Q4_K, Q5_K, Q6_K, Q3_K and Q2_K with M <= 8 when
+ *                       the activations fit), else as QMM_DECODE_AUTO.
  * Results of the paths agree within the accuracy bound of qmm(), not bit
  * for bit.  Returns the previous path, or QMM_EINVAL_SHAPE for an unknown
  * value (nothing changes).  Needs no GPU.

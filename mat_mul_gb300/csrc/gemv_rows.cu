@@ -8,9 +8,9 @@ namespace qk {
 using namespace rwk;
 
 bool gemv_rows_fits(int type, int M, int64_t K, int max_smem) {
-    // Q4_K, Q5_K, Q3_K and Q2_K for M <= 8, Q6_K for M <= 2
+    // Q4_K, Q5_K, Q6_K, Q3_K and Q2_K for M <= 8
     if ((type != QMM_Q4_K && type != QMM_Q5_K && type != QMM_Q6_K && type != QMM_Q3_K && type != QMM_Q2_K) ||
-        M < 1 || M > (type == QMM_Q6_K ? 2 : 8) ||
+        M < 1 || M > 8 ||
         K < 256 || K % 256 != 0 || K > (1 << 22))
         return false;
     const Shape sh = choose_shape(K / 256, block_bytes(type));

@@ -1,7 +1,7 @@
 // gemv_rows.cuh -- the row-per-lane decode kernel (device code, shared-memory
 // plan and launch templates), instantiated by gemv_rows.cu (M <= 2, Q4_K,
-// Q5_K, Q6_K, Q3_K and Q2_K) and gemv_rows_wide.cu / gemv_rows_wide_kq.cu
-// (3 <= M <= 8, Q4_K, Q5_K, Q3_K and Q2_K): decode product
+// Q5_K, Q6_K, Q3_K and Q2_K) and gemv_rows_wide.cu / gemv_rows_wide_kq.cu /
+// gemv_rows_wide_q6k.cu (3 <= M <= 8, every K-quant): decode product
 // y[M,N] = W[N,K] . x[M,K]^T with one weight row per lane.
 //
 // Design (sm_103a):
@@ -384,10 +384,13 @@ cudaError_t launch_group(const RwGroup &G, int CW, int H, int grid, int smem, cu
                   : launch_pdl(gemv_rows_group_kernel<MT, 10, 2, Q6K>, G, grid, 11 * 32, smem, st);
 }
 
-// The launches for 3 <= M <= 8 (Q4_K only; gemv_rows_wide.cu): MT = 4 or 8.
+// The launches for 3 <= M <= 8 (gemv_rows_wide.cu, gemv_rows_wide_kq.cu,
+// gemv_rows_wide_q6k.cu): MT = 4 or 8.
 cudaError_t launch_rows_wide(const RwParams &R, int MT, int CW, int H, int grid, int smem, cudaStream_t st);
 cudaError_t launch_rows_wide_kq(const RwParams &R, int MT, int CW, int H, int grid, int smem, cudaStream_t st);
+cudaError_t launch_rows_wide_q6k(const RwParams &R, int MT, int CW, int H, int grid, int smem, cudaStream_t st);
 cudaError_t launch_rows_wide_group(const RwGroup &G, int MT, int CW, int H, int grid, int smem, cudaStream_t st);
+cudaError_t launch_rows_wide_group_q6k(const RwGroup &G, int MT, int CW, int H, int grid, int smem, cudaStream_t st);
 
 }  // namespace rwk
 }  // namespace qk

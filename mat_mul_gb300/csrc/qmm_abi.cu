@@ -261,6 +261,26 @@ bool decode_on_tensor_cores(int type, int64_t M, int64_t N, int64_t K, const Dev
         return false;
     return qk::gemv_mma_fits(type, static_cast<int>(M), N, K, di.max_smem, di.num_sms);
 }
+
+// The entries of a qmm_group call take one launch of the row-per-lane kernel:
+// each entry would on its own, or (QMM_DECODE_AUTO, 3 <= M <= 4, two or more
+// matrices) every entry fits it.  There one row-per-lane launch beats the
+// quantiser and one tensor-core launch per matrix (the Qwen3-14B q/k/v and
+// gate/up at M = 4: measured); at M = 8 the tensor cores' faster loop wins.
+bool group_on_rows(int n, const int *types, const int64_t *Ns, int64_t K, int64_t M, const DeviceInfo &di) {
+    int live = 0;
+    for (int i = 0; i < n; ++i) live += Ns[i] > 0 ? 1 : 0;
+    const bool whole = live >= 2 && M >= QMM_TENSOR_MIN_M && M <= 4 && g_decode_path.load() == QMM_DECODE_AUTO &&
+                       !g_no_mma_gemv;
+    for (int i = 0; i < n; ++i) {
+        if (Ns[i] == 0) continue;
+        const bool ok = whole ? qk::gemv_rows_fits(types[i], static_cast<int>(M), K, di.max_smem)
+                              : decode_on_rows(types[i], M, Ns[i], K, di) &&
+                                    (rows_first() || !decode_on_tensor_cores(types[i], M, Ns[i], K, di));
+        if (!ok) return false;
+    }
+    return true;
+}
 }  // namespace
 
 extern "C" {
@@ -545,12 +565,8 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
         DeviceInfo di;
         if (int rc = device_info(dev, di)) return rc;
-        // one launch when every entry takes the row-per-lane kernel
-        bool rows = true;
-        for (int i = 0; i < n; ++i)
-            rows = rows && (Ns[i] == 0 || (decode_on_rows(types[i], M, Ns[i], K, di) &&
-                                           (rows_first() || !decode_on_tensor_cores(types[i], M, Ns[i], K, di))));
-        if (rows) {
+        // one launch when the entries take the row-per-lane kernel
+        if (group_on_rows(n, types, Ns, K, M, di)) {
             e = qk::launch_gemv_rows_group(n, types, Ws, Ns, K, x, static_cast<int>(M), ys,
                                            static_cast<cudaStream_t>(stream), di.num_sms, di.max_smem, di.status);
             if (e == cudaSuccess) {

@@ -79,8 +79,8 @@ cudaError_t launch_gemv_sb_group(int n, const int *types, const void *const *Ws,
                                  int max_smem, int *status);
 void group_ctas(int n, const int64_t *bytes, const int64_t *rows, const int64_t *need, int num_sms, int *g);
 
-// Row-per-lane decode kernel (gemv_rows.cu): Q4_K, Q5_K, Q3_K and Q2_K for
-// M <= 8, Q6_K for M <= 2, K a multiple of 256; quantises x itself (one
+// Row-per-lane decode kernel (gemv_rows.cu): Q4_K, Q5_K, Q6_K, Q3_K and Q2_K
+// for M <= 8, K a multiple of 256; quantises x itself (one
 // launch, no workspace), launched with programmatic dependent launch.  The
 // group launch takes several Q4_K / Q6_K matrices sharing K and x (CTAs
 // split as in group_ctas); cudaErrorNotSupported when one of them does not

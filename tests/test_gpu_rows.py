@@ -1,5 +1,5 @@
 """GPU parity of the row-per-lane decode kernel (Q4_K, Q5_K, Q6_K, Q3_K and
-Q2_K at M <= 2, all but Q6_K up to M = 8) against the CPU oracle, within the library's
+Q2_K up to M = 8) against the CPU oracle, within the library's
 bound |y_gpu - y_oracle| <= 2e-3 * sum_k |w_k xhat_k| + 1e-5.
 
 The shapes cover what the kernel's plan and indexing branch on: a CTA's row
@@ -54,14 +54,15 @@ CASES = [
 ]
 
 
-# Q4_K, Q5_K, Q3_K and Q2_K with 3 <= M <= 8: four or eight accumulators per
-# lane (the rows of the activations past M are computed on and never written)
+# every K-quant with 3 <= M <= 8: four or eight accumulators per lane (the
+# rows of the activations past M are computed on and never written)
 CASES_WIDE = [
     (synth.Q4_K, 1, 256, 3), (synth.Q4_K, 33, 2048, 4), (synth.Q4_K, 300, 4608, 5), (synth.Q4_K, 4865, 5120, 8),
     (synth.Q4_K, 200, 10240, 6), (synth.Q4_K, 77, 1024, 7), (synth.Q4_K, 5, 5120, 4),
     (synth.Q5_K, 33, 2048, 3), (synth.Q5_K, 300, 5120, 8), (synth.Q5_K, 150, 17408, 4),
     (synth.Q3_K, 1, 256, 5), (synth.Q3_K, 301, 4608, 4), (synth.Q3_K, 200, 5120, 8),
     (synth.Q2_K, 77, 1024, 7), (synth.Q2_K, 4865, 5120, 4), (synth.Q2_K, 120, 17408, 3),
+    (synth.Q6_K, 77, 2048, 3), (synth.Q6_K, 301, 4608, 8), (synth.Q6_K, 4097, 5120, 5), (synth.Q6_K, 150, 10240, 4),
 ]
 
 
@@ -144,6 +145,45 @@ def test_rows_group_one_launch_wide(cuda_lib, rows_path, M):
             continue
         yo, A = O.qmm(t, W, N, K, x)
         _check(y.cpu().numpy(), yo, A, f"group entry N={N} M={M}")
+
+
+# A group of several matrices at M = 3 or 4 (q/k/v with a Q6_K v, as in a
+# Q4_K_M model) takes one row-per-lane launch under the default kernel
+# choice; at M = 8 x is quantised once and each matrix is a tensor-core
+# launch.
+@pytest.mark.parametrize("M", [3, 4, 8])
+def test_group_default_choice_q_k_v(cuda_lib, M):
+    q = cuda_lib
+    K = 5120
+    items = [(synth.Q4_K, 5120), (synth.Q4_K, 1024), (synth.Q6_K, 1024), (synth.Q6_K, 0), (synth.Q6_K, 33)]
+    Ws = [synth.weights(t, N, K, seed=90 + i) for i, (t, N) in enumerate(items)]
+    x = synth.activations(M, K, seed=91 + M, outlier_frac=0.01)
+    before = q.qmm_launch_count()
+    ys = q.qmm_group([(t, _dev(W), N) for (t, N), W in zip(items, Ws)], K, _dev(x))
+    launches = q.qmm_launch_count() - before
+    assert q.qmm_device_status() == 0
+    assert launches == (1 if M <= 4 else 1 + sum(1 for _, N in items if N))
+    for (t, N), W, y in zip(items, Ws, ys):
+        if N == 0:
+            continue
+        yo, A = O.qmm(t, W, N, K, x)
+        _check(y.cpu().numpy(), yo, A, f"group entry type {t} N={N} M={M}")
+
+
+@pytest.mark.parametrize("M", [4, 8])
+def test_rows_group_one_launch_wide_with_q6k(cuda_lib, rows_path, M):
+    q = cuda_lib
+    K = 2560
+    items = [(synth.Q6_K, 2049), (synth.Q4_K, 300), (synth.Q6_K, 77)]
+    Ws = [synth.weights(t, N, K, seed=95 + i) for i, (t, N) in enumerate(items)]
+    x = synth.activations(M, K, seed=96 + M, outlier_frac=0.01)
+    before = q.qmm_launch_count()
+    ys = q.qmm_group([(t, _dev(W), N) for (t, N), W in zip(items, Ws)], K, _dev(x))
+    assert q.qmm_launch_count() - before == 1
+    assert q.qmm_device_status() == 0
+    for (t, N), W, y in zip(items, Ws, ys):
+        yo, A = O.qmm(t, W, N, K, x)
+        _check(y.cpu().numpy(), yo, A, f"group entry type {t} N={N} M={M}")
 
 
 # Q5_K, Q3_K and Q2_K at M = 8 with K = 17408: neither decode kernel holds the

@@ -66,7 +66,7 @@ def plan_rows(qtype, M, K, CW, H, max_smem=SMEM_MAX):
 
 
 def fits(qtype, M, K):
-    if qtype not in BB or M < 1 or M > (2 if qtype == Q6_K else 8) or K < 256 or K % 256:
+    if qtype not in BB or M < 1 or M > 8 or K < 256 or K % 256:
         return None
     cw, h, _ = choose_shape(K // 256, BB[qtype])
     return plan_rows(qtype, M, K, cw, h)
@@ -90,7 +90,8 @@ def test_shared_memory_plan(qtype, M):
 def test_the_shapes_the_gpu_tests_expect():
     # one launch on the row-per-lane kernel (tests/test_gpu_rows.py) ...
     for qtype, K, M in [(Q4_K, 5120, 8), (Q4_K, 10240, 6), (Q4_K, 2048, 4), (Q6_K, 17408, 2), (Q5_K, 17408, 1),
-                        (Q4_K, 17408, 2), (Q6_K, 17408, 1)]:
+                        (Q4_K, 17408, 2), (Q6_K, 17408, 1), (Q6_K, 4608, 8), (Q6_K, 10240, 4), (Q6_K, 5120, 5),
+                        (Q6_K, 2560, 8)]:
         assert fits(qtype, M, K) is not None, (qtype, K, M)
     # ... and one it does not take (the tensor-core path then runs)
     assert fits(Q4_K, 6, 14336) is None
@@ -116,7 +117,8 @@ def grid_of(N, K, qtype):
     (Q4_K, 1, 256, 1), (Q4_K, 5, 1024, 2), (Q4_K, 153, 2560, 1), (Q4_K, 300, 4608, 2), (Q4_K, 4865, 5120, 1),
     (Q4_K, 200, 17408, 2), (Q4_K, 17408, 5120, 1), (Q4_K, 77, 1024, 7),
     (Q6_K, 1, 256, 1), (Q6_K, 3, 512, 2), (Q6_K, 77, 2048, 1), (Q6_K, 301, 4608, 2), (Q6_K, 150, 17408, 1),
-    (Q6_K, 5120, 17408, 1), (Q6_K, 4097, 5120, 1),
+    (Q6_K, 5120, 17408, 1), (Q6_K, 4097, 5120, 1), (Q6_K, 77, 2048, 3), (Q6_K, 301, 4608, 8),
+    (Q6_K, 150, 10240, 4), (Q6_K, 4097, 5120, 5),
     (Q5_K, 1, 256, 1), (Q5_K, 77, 2048, 2), (Q5_K, 4097, 5120, 2), (Q5_K, 150, 17408, 1),
     (Q3_K, 1, 256, 1), (Q3_K, 77, 2048, 2), (Q3_K, 301, 4608, 1), (Q3_K, 4097, 5120, 2), (Q3_K, 150, 17408, 1),
     (Q2_K, 3, 512, 2), (Q2_K, 33, 2560, 1), (Q2_K, 300, 4608, 2), (Q2_K, 4865, 5120, 1), (Q2_K, 200, 17408, 2),
