@@ -135,7 +135,8 @@ QMM_API int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const floa
  * group is ONE launch of that kernel: its CTAs are split between the
  * matrices in proportion to their weight bytes and each quantises x itself.
  * When every entry takes the tensor-core decode kernel (Q4_K / Q6_K, up to
- * M = 8) x is quantised once and each matrix is one decode launch.
+ * M = 8) x is quantised once and the matrices share one decode launch (its
+ * CTAs split by weight bytes).
  * Otherwise the products run one after another as qmm() calls.  Accuracy as
  * qmm().
  * Every entry is validated before anything is launched; errors as qmm(),

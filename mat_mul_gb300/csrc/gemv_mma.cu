@@ -407,15 +407,14 @@ __device__ __forceinline__ void cursor_next(const MmParams &P, StageCursor &c, i
     }
 }
 
+// The work of CTA `cta` of one matrix (tmW: its Q4_K tensor map).
 template <int T, int CW>
-__global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
-    gemv_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ MmParams P) {
+__device__ __forceinline__ void mma_body(const CUtensorMap *tmW, const MmParams &P, const int cta) {
     constexpr int NTHREADS = Shape<CW>::NTHREADS, CHS = Shape<CW>::CHS;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // this CTA's rows [r0, r1): whole 8-row halves; groups of 16 from r0
-    const int cta = blockIdx.x;
     const int64_t h0 = P.halves_q * cta + min(cta, P.halves_r);
     const int nh = static_cast<int>(P.halves_q + (cta < P.halves_r ? 1 : 0));
     const int64_t r0 = 8 * h0;
@@ -499,7 +498,7 @@ __global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
                     const int boxes = r1 - row0 > 8 ? 2 : 1;
                     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(boxes * 8 * P.row_pitch));
                     for (int bx = 0; bx < boxes; ++bx)
-                        tma_load_2d_hint(dst + bx * 8 * P.row_pitch, &tmW, sb0 * SB_WORDS,
+                        tma_load_2d_hint(dst + bx * 8 * P.row_pitch, tmW, sb0 * SB_WORDS,
                                          static_cast<int>(row0 + 8 * bx), bar, pol);
                 }
             } else {
@@ -662,6 +661,33 @@ __global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
     for (int e = tid; e < ng * EDGE_FLOATS; e += CW * 32) store_y(e / EDGE_FLOATS, e % EDGE_FLOATS, table[e]);
 }
 
+template <int T, int CW>
+__global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1)
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ MmParams P) {
+    mma_body<T, CW>(&tmW, P, static_cast<int>(blockIdx.x));
+}
+
+// Several matrices that share K and the quantised x in one launch: CTAs
+// [cta_begin[i], cta_begin[i+1]) work on matrix i, each with its own
+// shared-memory plan (the launch has the largest).
+struct MmGroup {
+    CUtensorMap tm[QMM_GROUP_MAX];  // the Q4_K entries' tensor maps
+    MmParams p[QMM_GROUP_MAX];
+    int type[QMM_GROUP_MAX];
+    int cta_begin[QMM_GROUP_MAX + 1];
+    int n;
+};
+
+// Q6K: the launch holds a Q6_K matrix (else Q4_K only)
+template <int CW, bool Q6K>
+__global__ void __launch_bounds__(Shape<CW>::NTHREADS, 1) gemv_mma_group_kernel(const __grid_constant__ MmGroup G) {
+    int i = 0;
+    while (i + 1 < G.n && static_cast<int>(blockIdx.x) >= G.cta_begin[i + 1]) ++i;
+    const int cta = static_cast<int>(blockIdx.x) - G.cta_begin[i];
+    if (!Q6K || G.type[i] == QMM_Q4_K) mma_body<QMM_Q4_K, CW>(&G.tm[i], G.p[i], cta);
+    else mma_body<QMM_Q6_K, CW>(&G.tm[i], G.p[i], cta);
+}
+
 // Shared-memory plan: head | activation window [M][x_ld] | Q6_K group sums
 // window | phase table | ring of NS stages of GR rows x CW super-blocks.  The
 // fewest phases that fit with at least two stages.
@@ -737,28 +763,13 @@ bool plan_for(int type, int cw, int M, int64_t K, int64_t mg, int max_smem, Plan
     return cw == 10 ? plan_mm<QMM_Q6_K, 10>(M, K, mg, max_smem, pl) : plan_mm<QMM_Q6_K, 8>(M, K, mg, max_smem, pl);
 }
 
-}  // namespace
-
-bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_sms) {
-    if (!type_ok(type, M, K, N)) return false;
-    const int64_t mg = max_groups_of(N, num_sms, nullptr);
-    Plan pl;
-    return plan_for(type, consumer_warps(K), M, K, mg, max_smem, pl);
-}
-
-cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
-                            cudaStream_t st, int num_sms, int max_smem, int *status, const float *gate) {
-    if (!type_ok(type, M, K, N)) return cudaErrorNotSupported;
-    int64_t grid = 0;
-    const int64_t mg = max_groups_of(N, num_sms, &grid);
-    const int cw = consumer_warps(K);
-    Plan pl;
-    if (!plan_for(type, cw, M, K, mg, max_smem, pl)) return cudaErrorNotSupported;
+// The launch arguments of one matrix split over `grid` CTAs (one per 8-row
+// half at most) with the plan pl; tm receives the Q4_K tensor map.
+cudaError_t fill_mm(MmParams &P, CUtensorMap &tm, int type, const void *W, int64_t N, int64_t K, const void *xh,
+                    int M, float *y, int *status, const float *gate, int64_t grid, const Plan &pl) {
     const int nb = static_cast<int>(K / 256);
     const int bb = type == QMM_Q4_K ? Mm<QMM_Q4_K>::BB : Mm<QMM_Q6_K>::BB;
-    // a CTA's stages count in int
-    if (mg * ((nb + cw - 1) / cw + pl.nphase) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
-    MmParams P = {};
+    P = {};
     P.W = static_cast<const uint8_t *>(W);
     P.RB = static_cast<int64_t>(nb) * bb;
     P.w_end = reinterpret_cast<uint64_t>(W) + static_cast<uint64_t>(N) * P.RB;
@@ -785,35 +796,113 @@ cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const
     P.off_table = pl.off_table;
     P.off_ring = pl.off_ring;
     P.status = status;
-    P.stop_stage = inject_stop_stage();
-    CUtensorMap tmW = {};
+    P.stop_stage = NO_STOP;
+    tm = {};
     if (type == QMM_Q4_K) {
-        // the weights as 8-byte elements [N][18 * nb]: boxes of 8 super-blocks
+        // the weights as 8-byte elements [N][18 * nb]: boxes of CW super-blocks
         // and 2 elements (the next header, or zeros past the row end) x 8 rows
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nb) * SB_WORDS, static_cast<cuuint64_t>(N)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nb) * 144};
         const cuuint32_t box[2] = {static_cast<cuuint32_t>(pl.row_pitch / 8), 8u};
         const cuuint32_t es[2] = {1, 1};
-        if (tensor_map_encoder()(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), dims, strides, box,
+        if (tensor_map_encoder()(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), dims, strides, box,
                                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    auto kern = type == QMM_Q4_K ? (cw == 10 ? gemv_mma_kernel<QMM_Q4_K, 10> : gemv_mma_kernel<QMM_Q4_K, 8>)
-                                 : (cw == 10 ? gemv_mma_kernel<QMM_Q6_K, 10> : gemv_mma_kernel<QMM_Q6_K, 8>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+    return cudaSuccess;
+}
+
+template <class Kern, class... Args>
+cudaError_t launch_mm(Kern kern, int64_t grid, int cw, int smem, cudaStream_t st, const Args &...args) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3((cw + 1) * 32);
-    cfg.dynamicSmemBytes = pl.smem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmW, P);
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace
+
+bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_sms) {
+    if (!type_ok(type, M, K, N)) return false;
+    const int64_t mg = max_groups_of(N, num_sms, nullptr);
+    Plan pl;
+    return plan_for(type, consumer_warps(K), M, K, mg, max_smem, pl);
+}
+
+cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
+                            cudaStream_t st, int num_sms, int max_smem, int *status, const float *gate) {
+    if (!type_ok(type, M, K, N)) return cudaErrorNotSupported;
+    int64_t grid = 0;
+    const int64_t mg = max_groups_of(N, num_sms, &grid);
+    const int cw = consumer_warps(K);
+    Plan pl;
+    if (!plan_for(type, cw, M, K, mg, max_smem, pl)) return cudaErrorNotSupported;
+    // a CTA's stages count in int
+    if (mg * ((K / 256 + cw - 1) / cw + pl.nphase) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    MmParams P;
+    CUtensorMap tmW;
+    cudaError_t e = fill_mm(P, tmW, type, W, N, K, xh, M, y, status, gate, grid, pl);
+    if (e != cudaSuccess) return e;
+    P.stop_stage = inject_stop_stage();
+    auto kern = type == QMM_Q4_K ? (cw == 10 ? gemv_mma_kernel<QMM_Q4_K, 10> : gemv_mma_kernel<QMM_Q4_K, 8>)
+                                 : (cw == 10 ? gemv_mma_kernel<QMM_Q6_K, 10> : gemv_mma_kernel<QMM_Q6_K, 8>);
+    return launch_mm(kern, grid, cw, pl.smem, st, tmW, P);
+}
+
+cudaError_t launch_gemv_mma_group(int n, const int *types, const void *const *Ws, const int64_t *Ns, int64_t K,
+                                  const void *xh, int M, float *const *ys, cudaStream_t st, int num_sms,
+                                  int max_smem, int *status) {
+    if (n < 1 || n > QMM_GROUP_MAX) return cudaErrorInvalidValue;
+    const int cw = consumer_warps(K);
+    int idx[QMM_GROUP_MAX], m = 0;
+    int64_t bytes[QMM_GROUP_MAX], halves[QMM_GROUP_MAX], need[QMM_GROUP_MAX];
+    bool q6k = false;
+    for (int i = 0; i < n; ++i) {
+        if (Ns[i] <= 0) continue;  // an empty matrix gets no CTA
+        if (!type_ok(types[i], M, K, Ns[i])) return cudaErrorNotSupported;
+        q6k = q6k || types[i] == QMM_Q6_K;
+        bytes[m] = Ns[i] * (K / 256) * (types[i] == QMM_Q4_K ? Mm<QMM_Q4_K>::BB : Mm<QMM_Q6_K>::BB);
+        halves[m] = (Ns[i] + 7) / 8;
+        need[m] = 1;
+        idx[m++] = i;
+    }
+    if (m == 0) return cudaSuccess;
+    int g[QMM_GROUP_MAX];
+    group_ctas(m, bytes, halves, need, num_sms, g);
+    MmGroup G = {};
+    G.n = m;
+    int64_t grid = 0;
+    int smem = 0;
+    for (int j = 0; j < m; ++j) {
+        const int i = idx[j];
+        const int64_t mg = (halves[j] / g[j] + 2) / 2;
+        Plan pl;
+        if (!plan_for(types[i], cw, M, K, mg, max_smem, pl)) return cudaErrorNotSupported;
+        if (mg * ((K / 256 + cw - 1) / cw + pl.nphase) > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+        cudaError_t e = fill_mm(G.p[j], G.tm[j], types[i], Ws[i], Ns[i], K, xh, M, ys[i], status, nullptr, g[j], pl);
+        if (e != cudaSuccess) return e;
+        G.type[j] = types[i];
+        G.cta_begin[j] = static_cast<int>(grid);
+        grid += g[j];
+        if (pl.smem > smem) smem = pl.smem;
+    }
+    G.cta_begin[m] = static_cast<int>(grid);
+    G.p[0].stop_stage = inject_stop_stage();
+    if (q6k)
+        return cw == 10 ? launch_mm(gemv_mma_group_kernel<10, true>, grid, cw, smem, st, G)
+                        : launch_mm(gemv_mma_group_kernel<8, true>, grid, cw, smem, st, G);
+    return cw == 10 ? launch_mm(gemv_mma_group_kernel<10, false>, grid, cw, smem, st, G)
+                    : launch_mm(gemv_mma_group_kernel<8, false>, grid, cw, smem, st, G);
 }
 
 }  // namespace qk

@@ -592,14 +592,21 @@ int qmm_group(int n, const int *types, const void *const *Ws, const int64_t *Ns,
             if (e != cudaErrorNotSupported) return cuda_fail(e, "group gemv launch");
         }
         // every entry on the tensor-core kernel: x quantised once, then one
-        // decode launch per matrix (each later one starts as the one before
-        // it starts, so it streams its weights meanwhile)
+        // decode launch for all the matrices (CTAs split by their bytes), or
+        // one per matrix if that does not fit
         bool tensor = true;
         for (int i = 0; i < n; ++i) tensor = tensor && (Ns[i] == 0 || decode_on_tensor_cores(types[i], M, Ns[i], K, di));
         if (tensor) {
             cudaStream_t st = static_cast<cudaStream_t>(stream);
             void *ws = nullptr;
             if (int rc = quantize_for_tensor_cores(dev, st, x, M, K, di, &ws)) return rc;
+            e = qk::launch_gemv_mma_group(n, types, Ws, Ns, K, ws, static_cast<int>(M), ys, st, di.num_sms,
+                                          di.max_smem, di.status);
+            if (e == cudaSuccess) {
+                g_launches.fetch_add(1);
+                return QMM_OK;
+            }
+            if (e != cudaErrorNotSupported) return cuda_fail(e, "tensor-core group gemv launch");
             for (int i = 0; i < n; ++i) {
                 if (Ns[i] == 0) continue;
                 e = qk::launch_gemv_mma(types[i], Ws[i], Ns[i], K, ws, static_cast<int>(M), ys[i], st, di.num_sms,

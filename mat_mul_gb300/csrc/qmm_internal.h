@@ -119,6 +119,12 @@ cudaError_t launch_silu_mul(const float *g, const float *u, float *h, int64_t n,
 bool gemv_mma_fits(int type, int M, int64_t N, int64_t K, int max_smem, int num_sms);
 cudaError_t launch_gemv_mma(int type, const void *W, int64_t N, int64_t K, const void *xh, int M, float *y,
                             cudaStream_t st, int num_sms, int max_smem, int *status, const float *gate = nullptr);
+// Several Q4_K / Q6_K matrices that share K and xh in one launch (CTAs split
+// as in group_ctas, at most one per 8-row half); cudaErrorNotSupported when
+// one of them does not fit the kernel.
+cudaError_t launch_gemv_mma_group(int n, const int *types, const void *const *Ws, const int64_t *Ns, int64_t K,
+                                  const void *xh, int M, float *const *ys, cudaStream_t st, int num_sms,
+                                  int max_smem, int *status);
 
 // Prefill GEMM on tcgen05 (gemm_tc.cu): Q4_K, Q6_K or Q8_0 weights with K a
 // multiple of 256, fp16 activations xh [M][K] (d*q*2^e_m from the

@@ -44,12 +44,14 @@ def test_expired_wait_is_reported_and_the_next_call_is_right(cuda_lib, qtype, N,
     assert np.all(np.abs(y - yo) <= 2e-3 * A + 1e-5)
 
 
-def test_expired_wait_in_a_group_launch(cuda_lib):
+# the group launches: block-per-lane at M = 1, the tensor-core one at M = 6
+@pytest.mark.parametrize("M", [1, 6])
+def test_expired_wait_in_a_group_launch(cuda_lib, M):
     q = cuda_lib
     K = 5120
     items = [(synth.Q4_K, 8192), (synth.Q6_K, 1024)]
     Ws = [synth.weights(t, N, K, seed=10 + i) for i, (t, N) in enumerate(items)]
-    x = synth.activations(1, K, seed=11)
+    x = synth.activations(M, K, seed=11)
     xd = _dev(x)
     q.inject_stall(1)
     q.qmm_group([(t, _dev(W), N) for (t, N), W in zip(items, Ws)], K, xd)
