@@ -79,6 +79,11 @@
 // only after its own wait for the kernels before it, so the first weight
 // stages are issued before this kernel waits (every kernel that could write
 // the weights has completed by then) and the activations are read after.
+//
+// Groups.  Matrices that read the same quantised x (q/k/v, gate/up) can
+// share one launch: its CTAs are split between them by weight bytes, and
+// each CTA runs its own matrix (type, tensor map, shared-memory plan).
+//
 // All waits are bounded.
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
