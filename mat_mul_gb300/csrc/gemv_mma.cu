@@ -18,13 +18,16 @@
 //     one MMA per super-block, A = -dmin*m_j (fp16), B = X_j = sum_{k in j}
 //     x_k as fp16 hi + lo (about 22 bits).
 //   Q6_K (groups G of 16, int8 scale sc_G, q = 6 bits, offset 32):
-//     y = sum_G d*sc_G * (sum_{k in G} q_k x_k  -  32 * X_G)
+//     y = sum_G d*sc_G * sum_{k in G} q_k x_k  -  32 d * sum_G sc_G X_G
 //     one MMA per group; A = the six-bit values assembled from the 4-bit and
 //     2-bit fields in place (two LOP3 and one IMAD per pair; groups 8..15 of
-//     a half read the high nibbles as 16x); X_G = the fp32 sum of the group's
-//     fp16 x, subtracted in fp32 before the scaling.
-// Rounding: x to fp16 (as the tcgen05 prefill kernel) and, for Q4_K, dmin*m_j
-// to fp16; every scale is exact and every sum fp32.  Both fp16 operands are
+//     a half read the high nibbles as 16x); the offset term is two MMAs per
+//     super-block with the 16 groups as the k slots: A = sc_G (fp16
+//     subnormals, exact), B = X_G = the sum of the group's fp16 x as fp16 hi
+//     + lo (about 22 bits).
+// Rounding: x to fp16 (as the tcgen05 prefill kernel), for Q4_K dmin*m_j to
+// fp16, and the Q4_K block sums and Q6_K group sums to 22 bits; every scale
+// is exact and every other sum fp32.  Both fp16 operands are
 // scaled by powers of two into fp16's normal range first: x per token row
 // by the quantiser (its fp32 results are multiplied by the row's xinv at the
 // store), -dmin*m_j per row and super-block by 2^g with dmin*2^g in
@@ -171,7 +174,7 @@ struct MmParams {
     int64_t halves_q;   // 8-row halves per CTA: halves / gridDim.x
     int halves_r;       // halves % gridDim.x: the first halves_r CTAs take one more
     const uint8_t *xh;  // quantiser output [M][2K + K/8 bytes]: x fp16 | Q4_K block sums
-    const uint8_t *xs16;  // Q6_K group sums [K/16][8] fp32
+    const uint8_t *xs16;  // Q6_K group sums: per super-block [hi | lo][2][8 tokens][8] fp16 (x 2^-4)
     const float *xinv;    // [M] 2^-e_m: undoes the quantiser's power of two of token row m
     const float *gate;    // null, or g [M][N] from the preceding launch: y = silu(g) * (this product)
     int nphase;         // K phases
@@ -317,12 +320,24 @@ __device__ __forceinline__ void q4k_superblock(uint32_t a_sb, const uint8_t *hdr
     });
 }
 
+// The int8 scales of groups G, G+1 at p (2-byte aligned) as the fp16
+// subnormal pair (sc_G, sc_G+1) * 2^-24, exact: the bytes with their sign
+// bits flipped are sc + 128 in the low byte of each half, and 128 * 2^-24
+// is taken off.
+__device__ __forceinline__ uint32_t q6k_scale_pair(const uint8_t *p) {
+    const uint32_t v = *reinterpret_cast<const uint16_t *>(p) ^ 0x8080u;
+    const uint32_t u = __byte_perm(v, 0u, 0x4140);
+    const __half2 k128 = __half2half2(__ushort_as_half(0x0080));
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&u), k128);
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // One Q6_K super-block of the 16 rows: ra / rb = its bytes for rows g and
 // g+8 (2-byte aligned when ODD), x_sb = the lane's ldmatrix address of the
-// activations, xs_sb = the group sums [16][8 tokens].
+// activations, xg_sb = the lane's ldmatrix address of the group-sum tiles.
 template <bool ODD>
 __device__ __forceinline__ void q6k_superblock(const uint8_t *ra, const uint8_t *rb, uint32_t x_sb,
-                                               const float *xs_sb, int t, int quad, float (&c)[4], float (&c2)[4]) {
+                                               uint32_t xg_sb, int t, int quad, float (&c)[4], float (&c2)[4]) {
     // scales of groups 4t..4t+3 for rows g and g+8: d*sc * 2^24 / f, f = 16
     // for the groups read from high nibbles (groups 4..7 and 12..15: t odd)
     const float fs = (t & 1) ? 1048576.0f : 16777216.0f;
@@ -334,6 +349,24 @@ __device__ __forceinline__ void q6k_superblock(const uint8_t *ra, const uint8_t 
     for (int i = 0; i < 4; ++i) {
         Sa[i] = da * static_cast<float>(static_cast<int8_t>(sca >> (8 * i)));
         Sb[i] = db * static_cast<float>(static_cast<int8_t>(scb >> (8 * i)));
+    }
+    // the offset: -32 d sum_G sc_G X_G, one MMA per plane of the group sums
+    // (k slots = groups: A = sc * 2^-24, B = X * 2^-4 as hi and lo), so the
+    // result times -32 d 2^28
+    {
+        uint32_t xhi0, xhi1, xlo0, xlo1;
+        ldsm_x4(xg_sb, xhi0, xhi1, xlo0, xlo1);
+        const uint32_t a0 = q6k_scale_pair(ra + 192 + 2 * t), a1 = q6k_scale_pair(rb + 192 + 2 * t);
+        const uint32_t a2 = q6k_scale_pair(ra + 200 + 2 * t), a3 = q6k_scale_pair(rb + 200 + 2 * t);
+        float r[4];
+        mma_new(r, a0, a1, a2, a3, xhi0, xhi1);
+        mma_acc(r, a0, a1, a2, a3, xlo0, xlo1);
+        const float ka = __half2float(*reinterpret_cast<const __half *>(ra + 208)) * -8589934592.0f;
+        const float kb = __half2float(*reinterpret_cast<const __half *>(rb + 208)) * -8589934592.0f;
+        c[0] = fmaf(ka, r[0], c[0]);
+        c[1] = fmaf(ka, r[1], c[1]);
+        c[2] = fmaf(kb, r[2], c[2]);
+        c[3] = fmaf(kb, r[3], c[3]);
     }
     static_for<0, 2>([&](auto n_) {  // weights 128n .. 128n+127
         constexpr int n = decltype(n_)::value;
@@ -356,8 +389,6 @@ __device__ __forceinline__ void q6k_superblock(const uint8_t *ra, const uint8_t 
             constexpr uint32_t mlo = qi >= 2 ? 0x00F000F0u : 0x000F000Fu;
             constexpr uint32_t mhi = 0x00030003u << (2 * qi);
             constexpr uint32_t mul = (qi & 1) ? 4u : 16u;
-            // 32 * f * 2^-24: the offset 32 in the units of the MMA result
-            constexpr float kf = qi >= 2 ? 3.0517578125e-05f : 1.9073486328125e-06f;
             static_for<0, 2>([&](auto lh_) {
                 constexpr int lh = decltype(lh_)::value;
                 constexpr int G = 8 * n + 2 * qi + lh;
@@ -368,12 +399,6 @@ __device__ __forceinline__ void q6k_superblock(const uint8_t *ra, const uint8_t 
                 const uint32_t a3 = ((hb[lh] >> 8) & mhi) * mul + ((qlb >> 8) & mlo);
                 float d[4];
                 mma_new(d, a0, a1, a2, a3, lh ? x2 : x0, lh ? x3 : x1);
-                // minus 32 * the group sums of tokens 2t, 2t+1
-                const float2 X = *reinterpret_cast<const float2 *>(xs_sb + G * 8 + 2 * t);
-                d[0] = fmaf(-kf, X.x, d[0]);
-                d[1] = fmaf(-kf, X.y, d[1]);
-                d[2] = fmaf(-kf, X.x, d[2]);
-                d[3] = fmaf(-kf, X.y, d[3]);
                 const float sa = __shfl_sync(0xffffffffu, Sa[G & 3], quad | (G >> 2));
                 const float sb = __shfl_sync(0xffffffffu, Sb[G & 3], quad | (G >> 2));
                 float(&acc)[4] = lh ? c2 : c;
@@ -561,7 +586,8 @@ __device__ __forceinline__ void mma_body(const CUtensorMap *tmW, const MmParams 
     const uint32_t x_base = (tok_ok ? x_row : zero) + 16 * lm;
     const uint32_t xs_base = (tok_ok ? x_row + 512 * P.nbp : zero) + 16 * (lm & 1);
     const uint32_t x_step = tok_ok ? 512u : 0u, xs_step = tok_ok ? 32u : 0u;  // per super-block
-    const float *xs16 = reinterpret_cast<const float *>(smem + P.off_xs);
+    // Q6_K group-sum tiles: lane l reads row l & 7 of matrix l >> 3 (16 bytes each)
+    const uint32_t xg_base = smem_u32(smem + P.off_xs) + 16 * lane;
     const int tid = threadIdx.x;  // 0 .. 255
 
     // an element of a group's 16 x 8 result in fragment order -> y
@@ -635,9 +661,9 @@ __device__ __forceinline__ void mma_body(const CUtensorMap *tmW, const MmParams 
                         const uint8_t *ra = st + g * P.row_pitch + oa + 210 * idx;
                         const uint8_t *rb = st + (g + 8) * P.row_pitch + ob + 210 * idx;
                         if (idx & 1)
-                            q6k_superblock<true>(ra, rb, x_base + kw * x_step, xs16 + kw * 128, t, quad, acc, acc2);
+                            q6k_superblock<true>(ra, rb, x_base + kw * x_step, xg_base + 512 * kw, t, quad, acc, acc2);
                         else
-                            q6k_superblock<false>(ra, rb, x_base + kw * x_step, xs16 + kw * 128, t, quad, acc, acc2);
+                            q6k_superblock<false>(ra, rb, x_base + kw * x_step, xg_base + 512 * kw, t, quad, acc, acc2);
                     }
                 }
                 // this warp is done with the stage

@@ -38,7 +38,8 @@ struct QuantOut {
     void *xh;  // __half
     int64_t xh_ld;
     int xh_mma;
-    float *xs16;  // with xh_mma: the sums of the fp16 values per 16 elements, [K/16][8], tokens >= M zero
+    float *xs16;  // with xh_mma: the sums X of the fp16 values per 16 elements times 2^-4 as fp16 hi + lo,
+                  // per 256 elements [hi | lo][groups 0-7 | 8-15][8 tokens][8] (512 bytes), tokens >= M zero
     float *xinv;  // with xh: [M] the factor 2^-e_m that undoes row m's power of two
 };
 
@@ -108,7 +109,8 @@ cudaError_t launch_silu_mul(const float *g, const float *u, float *h, int64_t n,
 // Decode for 2 <= M <= 8 on the tensor cores (gemv_mma.cu): Q4_K or Q6_K,
 // sixteen weight rows per mma.sync.m16n8k16 (fp16 operands, fp32
 // accumulation).  xh: the quantiser's output with xh_mma, [M][2K + K/8
-// bytes] (16-byte aligned), then the group sums [K/16][8] fp32 (xs16), then
+// bytes] (16-byte aligned), then the group sums (xs16: 512 bytes per 256 of
+// K, fp16 hi/lo tiles), then
 // the row factors xinv [8] fp32; the kernel copies one K window of it at a
 // time into shared memory.
 // Launched with programmatic dependent launch right after that quantiser

@@ -209,15 +209,23 @@ __global__ void __launch_bounds__(XH_THREADS) quantize_xh_kernel(const float *__
             if (live) row[32 * b + ((l >> 4) * 2 + (l & 1)) * 8 + ((l >> 2) & 3) * 2 + ((l >> 1) & 1)] = hq[i];
             x8 += __half2float(hq[i]);
         }
-        // the sums of the two groups of 16 ([K/16][8 tokens], zeros for the
-        // tokens M..7, written with token 0) and of the block
+        // the sums of the two groups of 16 and of the block.  A group sum
+        // X_G times 2^-4 (16 values below 2^15 sum below 2^15) as fp16 hi +
+        // lo, in the B-operand tiles of the Q6_K kernel: per super-block
+        // [hi | lo][groups 0-7 | 8-15][8 tokens][8 groups], zeros for the
+        // tokens M..7 (written with token 0)
         const float x16 = x8 + __shfl_xor_sync(0xffffffffu, x8, 1);
         const float xs = x16 + __shfl_xor_sync(0xffffffffu, x16, 2);
         if (live && o.xs16 && (u & 1) == 0) {
-            float *gs = o.xs16 + (2 * b + (u >> 1)) * 8;
-            gs[m] = x16;
+            const int64_t gidx = 2 * b + (u >> 1);
+            const int G = static_cast<int>(gidx & 15);
+            __half *tile = reinterpret_cast<__half *>(o.xs16) + (gidx >> 4) * 256 + (G >> 3) * 64 + (G & 7);
+            const float v = x16 * 0.0625f;
+            const __half hi = __float2half_rn(v);
+            tile[8 * m] = hi;
+            tile[128 + 8 * m] = __float2half_rn(v - __half2float(hi));
             if (m == 0)
-                for (int64_t mm = M; mm < 8; ++mm) gs[mm] = 0.0f;
+                for (int64_t mm = M; mm < 8; ++mm) tile[8 * mm] = tile[128 + 8 * mm] = __float2half_rn(0.0f);
         }
         if (live && u == 0) {
             const float xs5 = xs * 0.03125f;

@@ -609,23 +609,53 @@ def _lane_q6k_scales(blk, t):
     return [np.float32(d * np.float32(np.int8(blk[192 + 4 * t + i]))) for i in range(4)]
 
 
-def q6k_mma_replay(rows, xh, M):
-    """y[16 rows][8 tokens] of one Q6_K super-block column, with the registers
-    built as q6k_superblock builds them: six-bit fields assembled by
-    mask/multiply/add into fp16 subnormals, one MMA per group of 16, minus
-    32 * the group sums, scaled by the shuffled group scale."""
-    zero = np.zeros(512, np.uint8)
-    tok = [_token_row(xh[m])[:512] for m in range(M)] + [zero] * (8 - M)
-    xs = np.zeros((16, 8), np.float32)   # the quantiser's group sums of the fp16 values
+def _q6k_scale_pair(blk, off):
+    """q6k_scale_pair: the int8 scales at off, off+1 as fp16 subnormals sc * 2^-24."""
+    v = (int(blk[off]) | (int(blk[off + 1]) << 8)) ^ 0x8080
+    u = (v & 0xFF) | ((v >> 8) << 16)
+    k = 128 * 2.0 ** -24
+    return _word(_f16(_h(u) - k), _f16(_h(u >> 16) - k))
+
+
+def q6k_group_tiles(xh, M):
+    """The quantiser's group-sum tiles of one super-block: X_G * 2^-4 as fp16
+    hi and lo planes, [plane][G][token] (zeros for tokens >= M)."""
+    t = np.zeros((2, 16, 8), np.float16)
     for m in range(M):
         for G in range(16):
             acc = np.float32(0)
             for v in xh[m, 16 * G:16 * G + 16]:
                 acc = np.float32(acc + np.float32(v))
-            xs[G, m] = acc
+            v = np.float32(acc * np.float32(0.0625))
+            t[0, G, m] = _f16(v)
+            t[1, G, m] = _f16(np.float32(v - np.float32(t[0, G, m])))
+    return t
+
+
+def q6k_mma_replay(rows, xh, M):
+    """y[16 rows][8 tokens] of one Q6_K super-block column, with the registers
+    built as q6k_superblock builds them: six-bit fields assembled by
+    mask/multiply/add into fp16 subnormals, one MMA per group of 16 scaled by
+    the shuffled group scale, and the offset -32 d sum_G sc_G X_G as two MMAs
+    over the group-sum tiles (ldmatrix rows = tokens)."""
+    zero = np.zeros(512, np.uint8)
+    tok = [_token_row(xh[m])[:512] for m in range(M)] + [zero] * (8 - M)
+    tiles = q6k_group_tiles(xh, M)
+    # ldmatrix x4 over [plane][half][token][8]: matrix q = (plane, half)
+    xg = [_ldmatrix([np.ascontiguousarray(tiles[q_ >> 1, 8 * (q_ & 1):8 * (q_ & 1) + 8, r]).view(np.uint8)
+                     for r in range(8)]) for q_ in range(4)]
+    c = np.zeros((16, 8))
+    a = []
+    for lane in range(32):
+        g, t = lane >> 2, lane & 3
+        a.append((_q6k_scale_pair(rows[g], 192 + 2 * t), _q6k_scale_pair(rows[g + 8], 192 + 2 * t),
+                  _q6k_scale_pair(rows[g], 200 + 2 * t), _q6k_scale_pair(rows[g + 8], 200 + 2 * t)))
+    r = _mma(a, [(xg[0][l], xg[1][l]) for l in range(32)]) + _mma(a, [(xg[2][l], xg[3][l]) for l in range(32)])
+    for row in range(16):
+        k = np.float32(np.float32(_h(_u32(rows[row], 208) & 0xFFFF)) * np.float32(-(2.0 ** 33)))
+        c[row, :] += float(k) * r[row, :]
     S = [(_lane_q6k_scales(rows[lane >> 2], lane & 3), _lane_q6k_scales(rows[(lane >> 2) + 8], lane & 3))
          for lane in range(32)]
-    c = np.zeros((16, 8))
     for n in range(2):
         for qi in range(4):
             xw = [_ldmatrix([tok[r][64 * (4 * n + qi) + 16 * q_: 64 * (4 * n + qi) + 16 * q_ + 16]
@@ -633,7 +663,6 @@ def q6k_mma_replay(rows, xh, M):
             mlo = 0x00F000F0 if qi >= 2 else 0x000F000F
             mhi = 0x00030003 << (2 * qi)
             mul = 4 if qi & 1 else 16
-            kf = 2.0 ** -15 if qi >= 2 else 2.0 ** -19
             for lh in range(2):
                 G = 8 * n + 2 * qi + lh
                 a = []
@@ -648,7 +677,6 @@ def q6k_mma_replay(rows, xh, M):
                     a.append((regs[0][0], regs[1][0], regs[0][1], regs[1][1]))
                 b = [((xw[2][l], xw[3][l]) if lh else (xw[0][l], xw[1][l])) for l in range(32)]
                 d = _mma(a, b)
-                d -= kf * xs[G][None, :]
                 for lane in range(32):
                     g, t = lane >> 2, lane & 3
                     src = (lane & ~3) | (G >> 2)
