@@ -130,10 +130,9 @@ QMM_API int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const floa
  *   K, x, M, stream : shared by all entries, as in qmm().
  * When every entry takes one of the one-weight-stream decode kernels (the
  * row-per-lane one for Q4_K and Q6_K, the block-per-lane one for Q8_0, Q4_K
- * and Q6_K; M <= 2, see qmm_set_decode_path), and under QMM_DECODE_AUTO for
- * two or more Q4_K / Q6_K matrices at QMM_TENSOR_MIN_M <= M <= 4, the whole
- * group is ONE launch of that kernel: its CTAs are split between the
- * matrices in proportion to their weight bytes and each quantises x itself.
+ * and Q6_K; M <= 2, see qmm_set_decode_path) the whole group is ONE launch of
+ * that kernel: its CTAs are split between the matrices in proportion to
+ * their weight bytes and each quantises x itself.
  * When every entry takes the tensor-core decode kernel (Q4_K / Q6_K, up to
  * M = 8) x is quantised once and the matrices share one decode launch (its
  * CTAs split by weight bytes).
@@ -275,9 +274,7 @@ QMM_API int64_t qmm_launch_count(void);
  *                       (from M = 2 on always for Q5_K, Q3_K and Q2_K),
  *                       everything else on the block-per-lane dp4a kernel;
  *                       a product that no decode kernel holds (x too large
- *                       for shared memory) on the prefill kernel.  A
- *                       qmm_group of Q4_K / Q6_K matrices at
- *                       QMM_TENSOR_MIN_M <= M <= 4: one row-per-lane launch.
+ *                       for shared memory) on the prefill kernel.
  *   QMM_DECODE_BLOCK  : the block-per-lane kernel wherever it fits.
  *   QMM_DECODE_TENSOR : the tensor-core kernel for every Q4_K / Q6_K product
  *                       with 2 <= M <= 8 that fits it (Q6_K: K a multiple

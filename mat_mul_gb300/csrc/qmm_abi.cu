@@ -263,21 +263,17 @@ bool decode_on_tensor_cores(int type, int64_t M, int64_t N, int64_t K, const Dev
 }
 
 // The entries of a qmm_group call take one launch of the row-per-lane kernel:
-// each entry would on its own, or (QMM_DECODE_AUTO, 3 <= M <= 4, two or more
-// matrices) every entry fits it.  There one row-per-lane launch beats the
-// quantiser and one tensor-core launch per matrix (the Qwen3-14B q/k/v and
-// gate/up at M = 4: measured); at M = 8 the tensor cores' faster loop wins.
+// each of them would on its own.  (At M = 3, 4 such a launch of Q4_K / Q6_K
+// matrices measured faster per call than the quantiser and the tensor-core
+// launch, q+k+v 16.9 -> 13.0 us, but slower inside a layer whose other
+// products run on the tensor cores: each switch between the two kinds of
+// launch cost 3-10 us, the Qwen3-14B layer at M = 4 106 us against 95 us.)
 bool group_on_rows(int n, const int *types, const int64_t *Ns, int64_t K, int64_t M, const DeviceInfo &di) {
-    int live = 0;
-    for (int i = 0; i < n; ++i) live += Ns[i] > 0 ? 1 : 0;
-    const bool whole = live >= 2 && M >= QMM_TENSOR_MIN_M && M <= 4 && g_decode_path.load() == QMM_DECODE_AUTO &&
-                       !g_no_mma_gemv;
     for (int i = 0; i < n; ++i) {
         if (Ns[i] == 0) continue;
-        const bool ok = whole ? qk::gemv_rows_fits(types[i], static_cast<int>(M), K, di.max_smem)
-                              : decode_on_rows(types[i], M, Ns[i], K, di) &&
-                                    (rows_first() || !decode_on_tensor_cores(types[i], M, Ns[i], K, di));
-        if (!ok) return false;
+        if (!decode_on_rows(types[i], M, Ns[i], K, di) ||
+            (!rows_first() && decode_on_tensor_cores(types[i], M, Ns[i], K, di)))
+            return false;
     }
     return true;
 }

@@ -147,10 +147,9 @@ def test_rows_group_one_launch_wide(cuda_lib, rows_path, M):
         _check(y.cpu().numpy(), yo, A, f"group entry N={N} M={M}")
 
 
-# A group of several matrices at M = 3 or 4 (q/k/v with a Q6_K v, as in a
-# Q4_K_M model) takes one row-per-lane launch under the default kernel
-# choice; at M = 8 x is quantised once and the matrices share one
-# tensor-core launch.
+# A group of several matrices from M = 3 on (q/k/v with a Q6_K v, as in a
+# Q4_K_M model) under the default kernel choice: x is quantised once and the
+# matrices share one tensor-core launch.
 @pytest.mark.parametrize("M", [3, 4, 8])
 def test_group_default_choice_q_k_v(cuda_lib, M):
     q = cuda_lib
@@ -162,7 +161,7 @@ def test_group_default_choice_q_k_v(cuda_lib, M):
     ys = q.qmm_group([(t, _dev(W), N) for (t, N), W in zip(items, Ws)], K, _dev(x))
     launches = q.qmm_launch_count() - before
     assert q.qmm_device_status() == 0
-    assert launches == (1 if M <= 4 else 2)
+    assert launches == 2
     for (t, N), W, y in zip(items, Ws, ys):
         if N == 0:
             continue
