@@ -15,6 +15,8 @@
 // seven times the bytes read -- is written fully coalesced.
 #include "qmm_device.cuh"
 
+#include <type_traits>
+
 namespace qk {
 
 // Q4_K six-bit scale and min of sub-block j from the 12 scale bytes S.
@@ -190,13 +192,18 @@ cudaError_t launch_dequant(int type, const void *blocks, int64_t n_elems, float 
     if (grid < 1) grid = 1;
     const auto *b = static_cast<const uint8_t *>(blocks);
     const unsigned gx = static_cast<unsigned>(grid);
+    auto run = [&](auto t) {
+        constexpr int T = decltype(t)::value;
+        prefer_max_shared(dequant_kernel<T>);
+        dequant_kernel<T><<<gx, 256, 0, st>>>(b, n_elems, out);
+    };
     switch (type) {
-    case QMM_Q8_0: dequant_kernel<QMM_Q8_0><<<gx, 256, 0, st>>>(b, n_elems, out); break;
-    case QMM_Q4_K: dequant_kernel<QMM_Q4_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
-    case QMM_Q5_K: dequant_kernel<QMM_Q5_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
-    case QMM_Q3_K: dequant_kernel<QMM_Q3_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
-    case QMM_Q2_K: dequant_kernel<QMM_Q2_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
-    default: dequant_kernel<QMM_Q6_K><<<gx, 256, 0, st>>>(b, n_elems, out); break;
+    case QMM_Q8_0: run(std::integral_constant<int, QMM_Q8_0>{}); break;
+    case QMM_Q4_K: run(std::integral_constant<int, QMM_Q4_K>{}); break;
+    case QMM_Q5_K: run(std::integral_constant<int, QMM_Q5_K>{}); break;
+    case QMM_Q3_K: run(std::integral_constant<int, QMM_Q3_K>{}); break;
+    case QMM_Q2_K: run(std::integral_constant<int, QMM_Q2_K>{}); break;
+    default: run(std::integral_constant<int, QMM_Q6_K>{}); break;
     }
     return cudaGetLastError();
 }

@@ -27,6 +27,8 @@ cudaError_t launch_silu_mul(const float *g, const float *u, float *h, int64_t n,
     int64_t grid = (n + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (grid > cap) grid = cap;
+    const cudaError_t e = prefer_max_shared(silu_mul_kernel);
+    if (e != cudaSuccess) return e;
     silu_mul_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(g, u, h, n);
     return cudaGetLastError();
 }

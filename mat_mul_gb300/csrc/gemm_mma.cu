@@ -357,6 +357,7 @@ cudaError_t launch_gemm_mma(int type, const void *W, int64_t N, int64_t K, const
     const auto *w = static_cast<const uint8_t *>(W);
     auto run = [&](auto t) {
         constexpr int T = decltype(t)::value;
+        prefer_max_shared(gemm_mma_kernel<T>);
         gemm_mma_kernel<T><<<grid, 128, 0, st>>>(w, N, K, xq, xd, xs, xd_ld, xs16, xs16_ld, M, y);
     };
     switch (type) {

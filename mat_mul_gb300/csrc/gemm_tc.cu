@@ -1259,8 +1259,7 @@ cudaError_t launch_bt(EncodeTiled enc, const void *W, int64_t N, int64_t K, cons
     }
     const int nt = static_cast<int>((N + BW - 1) / BW), mt = static_cast<int>((M + BT - 1) / BT);
     const int ksteps = static_cast<int>(K / BK);
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<T, BT, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e = set_smem_attrs(gemm_tc_kernel<T, BT, TM>, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int64_t tiles = static_cast<int64_t>(nt) * mt;
     TcParams P;

@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemv_kernel(const __grid_constant
 template <int T, int MT>
 cudaError_t launch_t(const GemvParams &P, int grid, int smem, cudaStream_t st) {
     auto kfn = gemv_kernel<T, MT>;
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_smem_attrs(kfn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -846,7 +846,7 @@ cudaError_t fill_mm(MmParams &P, CUtensorMap &tm, int type, const void *W, int64
 
 template <class Kern, class... Args>
 cudaError_t launch_mm(Kern kern, int64_t grid, int cw, int smem, cudaStream_t st, const Args &...args) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_smem_attrs(kern, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));

@@ -351,7 +351,7 @@ inline void fill_rows(RwParams &R, int type, const void *W, int64_t N, int64_t K
 
 template <class Kern, class Arg>
 cudaError_t launch_pdl(Kern kfn, const Arg &arg, int grid, int threads, int smem, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_smem_attrs(kfn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -134,7 +134,7 @@ void fill(SbParams &P, int type, const void *W, int64_t N, int64_t K, const floa
 template <int MT>
 cudaError_t launch_group_mt(const SbGroup &G, int grid, int smem, cudaStream_t st) {
     auto kfn = gemv_sb_group_kernel<MT>;
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_smem_attrs(kfn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

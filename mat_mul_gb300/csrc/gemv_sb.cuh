@@ -813,7 +813,7 @@ cudaError_t launch_t(const SbParams &P, int grid, int smem, cudaStream_t st) {
     auto kfn = gemv_sb_kernel<T, MT>;
     if constexpr (MT <= 2)
         if (P.W2) kfn = gemv_sb_gateup_kernel<T, MT>;
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_smem_attrs(kfn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -13,6 +13,25 @@
 namespace qk {
 
 // ---------------------------------------------------------------------------
+// Launch attributes (host).  Every kernel of the library asks for the
+// largest shared-memory carveout, whatever it uses: an SM changes its
+// carveout only when it is idle, so consecutive launches that asked for
+// different ones could not overlap on it (programmatic dependent launch).
+// ---------------------------------------------------------------------------
+template <class F>
+inline cudaError_t prefer_max_shared(F kern) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
+// The dynamic shared memory a launch of kern needs, and the carveout.
+template <class F>
+inline cudaError_t set_smem_attrs(F kern, int smem) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return e != cudaSuccess ? e : prefer_max_shared(kern);
+}
+
+// ---------------------------------------------------------------------------
 // Block formats (GGUF): bytes per block and weights per block.
 // ---------------------------------------------------------------------------
 template <int T> struct Fmt;

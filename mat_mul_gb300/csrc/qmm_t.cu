@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(VtCfg<NB>::THREADS) qmm_t_kernel(const VtParam
 template <int NB>
 cudaError_t launch_nb(const VtParams &P, int64_t H, cudaStream_t st) {
     const int smem = VtCfg<NB>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(qmm_t_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_smem_attrs(qmm_t_kernel<NB>, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P.nchunk, static_cast<unsigned>(H));

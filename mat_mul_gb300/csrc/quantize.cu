@@ -266,6 +266,8 @@ cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, const QuantOut
         cfg.blockDim = dim3(XH_THREADS);
         cfg.attrs = na ? attr : nullptr;
         cfg.numAttrs = na;
+        const cudaError_t e = prefer_max_shared(quantize_xh_kernel);
+        if (e != cudaSuccess) return e;
         return cudaLaunchKernelEx(&cfg, quantize_xh_kernel, x, M, K, o, S, trigger_dependents ? 1 : 0);
     }
     const int64_t nblk = M * (K / 32);
@@ -277,6 +279,8 @@ cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, const QuantOut
     cfg.blockDim = dim3(256);
     cfg.attrs = na ? attr : nullptr;
     cfg.numAttrs = na;
+    const cudaError_t e = prefer_max_shared(quantize_act_kernel);
+    if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, quantize_act_kernel, x, M, K, o, trigger_dependents ? 1 : 0);
 }
 
