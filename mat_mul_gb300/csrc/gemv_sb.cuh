@@ -638,10 +638,12 @@ __device__ __forceinline__ void sb_body(const SbParams &P, const int cta) {
     int issued = 0;
     if (lane == 0) {
         pol_w = policy_evict_first();
-        // Q4_K: the first stage goes into shared memory at once (measured:
-        // 3-6 % off the Q4_K launches; for the other types the copies then
-        // delay x's loads more than they gain)
-        if (T == QMM_Q4_K && nst > 0) issue(0, 0, pol_w), issued = 1;
+        // the first stage goes into shared memory at once for Q4_K (measured:
+        // 3-6 % off the Q4_K launches) and for rows of at least 4096 weights
+        // (their x takes longer to quantise: 1.5 us off the decode step); for
+        // short rows of the other types the copies delay x's loads more than
+        // they gain (the 2048 x 128256 Q6_K lm_head: 33.0 against 34.2 us)
+        if ((T == QMM_Q4_K || P.K >= 4096) && nst > 0) issue(0, 0, pol_w), issued = 1;
         for (int t = issued; t < min(P.NSW, nst); ++t) {
             const int u0 = uw0 + SU * t, u1 = min(u0 + SU, uw1);
             const int a16 = (cta_off + u0 * BB) & ~15;
