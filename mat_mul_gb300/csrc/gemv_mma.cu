@@ -239,32 +239,36 @@ __device__ __forceinline__ uint32_t word_at(const uint8_t *p) {
     return __funnelshift_r(a[0], a[1], 16);
 }
 
-// Scales of this lane's sub-blocks 2t (low nibbles) and 2t+1 (high nibbles)
-// from a Q4_K header (d, dmin, GGUF six-bit packing): s0, s1 = d*sc * 2^24
-// and d*sc * 2^20 in fp32 (exact), m01 = (-dmin*m_2t, -dmin*m_2t+1) * 2^g in
-// fp16 with |dmin|*2^g in [2^8, 2^9) (g = 0 when dmin is 0), um = 2^(5-g):
-// the factor that takes the min-term MMA (whose B operand carries 2^-5)
-// back to the scale of the other terms.
-__device__ __forceinline__ void q4k_lane_scales(uint4 h, int t, float &s0, float &s1, uint32_t &m01, float &um) {
+// Scales of this lane's sub-blocks t and t+4 from a Q4_K header (d, dmin,
+// GGUF six-bit packing: sub-blocks 0-3 in the low six bits of bytes 0-7, 4-7
+// in the nibbles of bytes 8-11 with the top bits of bytes 0-7): s0, s1 =
+// d*sc_t * fs and d*sc_(t+4) * fs in fp32 (exact), fs = 2^24, or 2^20 for
+// odd t (odd sub-blocks are read from the high nibbles in place as 16q);
+// m01 = (-dmin*m_t, -dmin*m_(t+4)) * 2^g in fp16 with |dmin|*2^g in
+// [2^8, 2^9) (g = 0 when dmin is 0), um = 2^(5-g): the factor that takes the
+// min-term MMA (whose B operand carries 2^-5) back to the scale of the
+// other terms.  sel picks byte t of a word under the bits 0x4B000000, which
+// make it the fp32 2^23 + b; one FMA then gives b * scale exactly.
+__device__ __forceinline__ void q4k_lane_scales(uint4 h, uint32_t sel, float fs, float &s0, float &s1,
+                                                uint32_t &m01, float &um) {
     const float d = half_bits_to_float(h.x);
     const float dmin0 = half_bits_to_float(h.x >> 16);
     const uint32_t mb = __float_as_uint(dmin0) & 0x7fffffffu;
     const int g = mb ? 8 - exponent_of(mb) : 0;
     const float dmin = dmin0 * pow2f(g);
     um = pow2f(5 - g);
-    uint32_t scw, mnw;  // bytes: scales (mins) of sub-blocks 0..3 or 4..7
-    if (t < 2) {
-        scw = h.y & 0x3F3F3F3Fu;
-        mnw = h.z & 0x3F3F3F3Fu;
-    } else {
-        scw = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
-        mnw = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-    }
-    const int sh = 16 * (t & 1);
-    s0 = d * static_cast<float>((scw >> sh) & 0xFF) * 16777216.0f;
-    s1 = d * static_cast<float>((scw >> (sh + 8)) & 0xFF) * 1048576.0f;
-    const __half2 m = __floats2half2_rn(-(dmin * static_cast<float>((mnw >> sh) & 0xFF)),
-                                        -(dmin * static_cast<float>((mnw >> (sh + 8)) & 0xFF)));
+    // the six-bit scales and mins of sub-blocks 0-3 and 4-7, a byte each
+    const uint32_t sc_lo = h.y & 0x3F3F3F3Fu, mn_lo = h.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+    const uint32_t mn_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+    const float ds = d * fs;
+    const float kd = -8388608.0f * ds;
+    s0 = fmaf(__uint_as_float(__byte_perm(sc_lo, 0x4B000000u, sel)), ds, kd);
+    s1 = fmaf(__uint_as_float(__byte_perm(sc_hi, 0x4B000000u, sel)), ds, kd);
+    const float km = 8388608.0f * dmin;
+    const float m0 = fmaf(__uint_as_float(__byte_perm(mn_lo, 0x4B000000u, sel)), -dmin, km);
+    const float m1 = fmaf(__uint_as_float(__byte_perm(mn_hi, 0x4B000000u, sel)), -dmin, km);
+    const __half2 m = __floats2half2_rn(m0, m1);
     m01 = *reinterpret_cast<const uint32_t *>(&m);
 }
 
@@ -273,13 +277,14 @@ __device__ __forceinline__ void q4k_lane_scales(uint4 h, int t, float &s0, float
 // x_sb = the lane's ldmatrix address of the activations, xs_sb = of the
 // block sums.
 __device__ __forceinline__ void q4k_superblock(uint32_t a_sb, const uint8_t *hdr_a, const uint8_t *hdr_b,
-                                               uint32_t x_sb, uint32_t xs_sb, int t, int quad, float (&c)[4],
-                                               float (&c2)[4]) {
+                                               uint32_t x_sb, uint32_t xs_sb, uint32_t sel, float fs, int quad,
+                                               float (&c)[4], float (&c2)[4]) {
     float sa0, sa1, sb0, sb1, ua, ub;
     uint32_t ma, mb;
-    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_a), t, sa0, sa1, ma, ua);
-    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_b), t, sb0, sb1, mb, ub);
-    // the min term: k slots 2t, 2t+1 = sub-blocks 2t, 2t+1 (sums hi), slots
+    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_a), sel, fs, sa0, sa1, ma, ua);
+    q4k_lane_scales(*reinterpret_cast<const uint4 *>(hdr_b), sel, fs, sb0, sb1, mb, ub);
+    // the min term: k slots 2t, 2t+1 = sub-blocks t, t+4 (sums hi; the
+    // quantiser stores sub-block j's sums at slot 2(j mod 4) + j/4), slots
     // 2t+8, 2t+9 = the same sub-blocks (sums lo); rows g | g+8 scaled back
     // by their own factors
     {
@@ -297,11 +302,13 @@ __device__ __forceinline__ void q4k_superblock(uint32_t a_sb, const uint8_t *hdr
         uint32_t wa0, wb0, wa1, wb1;  // rows g | g+8, halves e = 0 | 1
         ldsm_x4(a_sb + 32 * cc, wa0, wb0, wa1, wb1);
         const uint32_t wa0s = wa0 >> 8, wb0s = wb0 >> 8, wa1s = wa1 >> 8, wb1s = wb1 >> 8;
-        // scales of sub-blocks 2cc, 2cc+1 from the quad's lane cc
-        const float s_a0 = __shfl_sync(0xffffffffu, sa0, quad | cc);
-        const float s_a1 = __shfl_sync(0xffffffffu, sa1, quad | cc);
-        const float s_b0 = __shfl_sync(0xffffffffu, sb0, quad | cc);
-        const float s_b1 = __shfl_sync(0xffffffffu, sb1, quad | cc);
+        // scales of sub-blocks 2cc, 2cc+1: the first (cc < 2) or second value
+        // of the quad's lanes 2cc mod 4 and 2cc+1 mod 4
+        constexpr int l0 = (2 * cc) & 3, l1 = (2 * cc + 1) & 3;
+        const float s_a0 = __shfl_sync(0xffffffffu, cc < 2 ? sa0 : sa1, quad | l0);
+        const float s_a1 = __shfl_sync(0xffffffffu, cc < 2 ? sa0 : sa1, quad | l1);
+        const float s_b0 = __shfl_sync(0xffffffffu, cc < 2 ? sb0 : sb1, quad | l0);
+        const float s_b1 = __shfl_sync(0xffffffffu, cc < 2 ? sb0 : sb1, quad | l1);
         static_for<0, 2>([&](auto h_) {  // sub-block 2cc + h: low or high nibbles
             constexpr int h = decltype(h_)::value;
             constexpr uint32_t mk = h ? 0x00F000F0u : 0x000F000Fu;
@@ -586,6 +593,10 @@ __device__ __forceinline__ void mma_body(const CUtensorMap *tmW, const MmParams 
     const uint32_t x_base = (tok_ok ? x_row : zero) + 16 * lm;
     const uint32_t xs_base = (tok_ok ? x_row + 512 * P.nbp : zero) + 16 * (lm & 1);
     const uint32_t x_step = tok_ok ? 512u : 0u, xs_step = tok_ok ? 32u : 0u;  // per super-block
+    // Q4_K scale decode of this lane (sub-blocks t and t+4): the byte selector
+    // and the fp32 factor of its nibble half
+    const uint32_t q4k_sel = 0x7650u + static_cast<uint32_t>(t);
+    const float q4k_fs = (t & 1) ? 1048576.0f : 16777216.0f;
     // Q6_K group-sum tiles: lane l reads row l & 7 of matrix l >> 3 (16 bytes each)
     const uint32_t xg_base = smem_u32(smem + P.off_xs) + 16 * lane;
     const int tid = threadIdx.x;  // 0 .. 255
@@ -637,7 +648,7 @@ __device__ __forceinline__ void mma_body(const CUtensorMap *tmW, const MmParams 
                     if constexpr (T == QMM_Q4_K) {
                         q4k_superblock(smem_u32(st) + a_off + 144 * idx, st + g * P.row_pitch + 144 * idx,
                                        st + (g + 8) * P.row_pitch + 144 * idx, x_base + kw * x_step,
-                                       xs_base + kw * xs_step, t, quad, acc, acc2);
+                                       xs_base + kw * xs_step, q4k_sel, q4k_fs, quad, acc, acc2);
                     } else {
                         const int64_t row0 = r0 + GR * gi;
                         const uint64_t base = reinterpret_cast<uint64_t>(P.W) + static_cast<uint64_t>(210) * sb0;

@@ -24,7 +24,8 @@ namespace qk {
 //                   32b + ((l>>4)*2 + (l&1))*8 + ((l>>2)&3)*2 + ((l>>1)&1),
 //                   then after the K halves the block sums of the fp16
 //                   values times 2^-5 as hi + lo, per super-block 8 hi then
-//                   8 lo (xh_ld >= K + K/16).  When xh is set only the fp16
+//                   8 lo, sub-block j at slot 2(j mod 4) + j/4 (xh_ld >=
+//                   K + K/16).  When xh is set only the fp16
 //                   outputs (xh, xs16, xinv) are written.
 struct QuantOut {
     int8_t *q;

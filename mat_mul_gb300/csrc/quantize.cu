@@ -228,11 +228,15 @@ __global__ void __launch_bounds__(XH_THREADS) quantize_xh_kernel(const float *__
                 for (int64_t mm = M; mm < 8; ++mm) tile[8 * mm] = tile[128 + 8 * mm] = __float2half_rn(0.0f);
         }
         if (live && u == 0) {
+            // sub-block j of the super-block at slot 2(j mod 4) + j/4: the
+            // tensor-core kernel's lane t holds the mins of sub-blocks t, t+4
+            const int j = static_cast<int>(b & 7);
+            const int slot = 2 * (j & 3) + (j >> 2);
             const float xs5 = xs * 0.03125f;
             const __half hi = __float2half_rn(xs5);
             const __half lo = __float2half_rn(xs5 - __half2float(hi));
-            row[K + (b >> 3) * 16 + (b & 7)] = hi;
-            row[K + (b >> 3) * 16 + 8 + (b & 7)] = lo;
+            row[K + (b >> 3) * 16 + slot] = hi;
+            row[K + (b >> 3) * 16 + 8 + slot] = lo;
         }
     }
 }

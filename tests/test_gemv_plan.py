@@ -514,19 +514,20 @@ def _mma(a, b):
 
 
 def _lane_scales(hdr, t):
-    """(s0, s1, m01) as q4k_lane_scales: fp32 scales, fp16 pair of -dmin*m."""
+    """(s0, s1, m01) as q4k_lane_scales for sub-blocks t and t+4: fp32 scales
+    d*sc*fs (fs = 2^24, 2^20 for odd t), fp16 pair of -dmin*m (dmin kept
+    unscaled here: the power of two 2^g cancels against um)."""
     hx, hy, hz, hw = (_u32(hdr, 4 * i) for i in range(4))
     d, dmin = np.float32(_h(hx)), np.float32(_h(hx >> 16))
-    if t < 2:
-        scw, mnw = hy & 0x3F3F3F3F, hz & 0x3F3F3F3F
-    else:
-        scw = (hw & 0x0F0F0F0F) | ((hy >> 2) & 0x30303030)
-        mnw = ((hw >> 4) & 0x0F0F0F0F) | ((hz >> 2) & 0x30303030)
-    sh = 16 * (t & 1)
-    s0 = np.float32(np.float32(d * np.float32((scw >> sh) & 0xFF)) * np.float32(2.0 ** 24))
-    s1 = np.float32(np.float32(d * np.float32((scw >> (sh + 8)) & 0xFF)) * np.float32(2.0 ** 20))
-    m0 = _f16(-np.float32(dmin * np.float32((mnw >> sh) & 0xFF)))
-    m1 = _f16(-np.float32(dmin * np.float32((mnw >> (sh + 8)) & 0xFF)))
+    sc_lo, mn_lo = hy & 0x3F3F3F3F, hz & 0x3F3F3F3F
+    sc_hi = (hw & 0x0F0F0F0F) | ((hy >> 2) & 0x30303030)
+    mn_hi = ((hw >> 4) & 0x0F0F0F0F) | ((hz >> 2) & 0x30303030)
+    fs = np.float32(2.0 ** 20 if t & 1 else 2.0 ** 24)
+    byte = lambda w: np.float32((w >> (8 * t)) & 0xFF)
+    s0 = np.float32(np.float32(d * fs) * byte(sc_lo))
+    s1 = np.float32(np.float32(d * fs) * byte(sc_hi))
+    m0 = _f16(-np.float32(dmin * byte(mn_lo)))
+    m1 = _f16(-np.float32(dmin * byte(mn_hi)))
     return s0, s1, _word(m0, m1)
 
 
@@ -542,8 +543,9 @@ def _token_row(xh):
         xs = np.float32(0)
         for v in xh[32 * b:32 * b + 32]:
             xs = np.float32(xs + np.float32(v))  # any order: the values are exact in fp32 here
-        hi[b] = _f16(xs)
-        lo[b] = _f16(np.float32(xs - np.float32(hi[b])))
+        slot = 2 * (b & 3) + (b >> 2)   # the quantiser's order of the block sums
+        hi[slot] = _f16(xs)
+        lo[slot] = _f16(np.float32(xs - np.float32(hi[slot])))
     return np.concatenate([st.view(np.uint8), hi.view(np.uint8), lo.view(np.uint8)])
 
 
@@ -574,11 +576,12 @@ def mma_replay(rows, xh, M):
                      [(xw[0][l], xw[1][l]) for l in range(32)])
             d += _mma([(wa1[l] & mk, wb1[l] & mk, (wa1[l] >> 8) & mk, (wb1[l] >> 8) & mk) for l in range(32)],
                       [(xw[2][l], xw[3][l]) for l in range(32)])
+            j = 2 * cc + h              # the sub-block
             for lane in range(32):
                 g, t = lane >> 2, lane & 3
-                src = (lane & ~3) | cc  # the shuffle source in the quad
-                sa = float(ls[src][0][h])
-                sb = float(ls[src][1][h])
+                src = (lane & ~3) | (j & 3)  # the shuffle source in the quad: its first or second value
+                sa = float(ls[src][0][j >> 2])
+                sb = float(ls[src][1][j >> 2])
                 c[g, 2 * t:2 * t + 2] += sa * d[g, 2 * t:2 * t + 2]
                 c[g + 8, 2 * t:2 * t + 2] += sb * d[g + 8, 2 * t:2 * t + 2]
     return c
