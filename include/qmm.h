@@ -274,7 +274,9 @@ QMM_API int64_t qmm_launch_count(void);
  *                       (from M = 2 on always for Q5_K, Q3_K and Q2_K),
  *                       everything else on the block-per-lane dp4a kernel;
  *                       a product that no decode kernel holds (x too large
- *                       for shared memory) on the prefill kernel.
+ *                       for shared memory), and a Q8_0 product with
+ *                       QMM_TENSOR_MIN_M <= M <= 8 of at least 2^24 weights
+ *                       (3 * 2^24 at M <= 4), on the prefill kernel.
  *   QMM_DECODE_BLOCK  : the block-per-lane kernel wherever it fits.
  *   QMM_DECODE_TENSOR : the tensor-core kernel for every Q4_K / Q6_K product
  *                       with 2 <= M <= 8 that fits it (Q6_K: K a multiple

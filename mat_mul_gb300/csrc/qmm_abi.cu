@@ -244,6 +244,20 @@ bool decode_on_rows(int type, int64_t M, int64_t N, int64_t K, const DeviceInfo 
     return qk::gemv_rows_fits(type, static_cast<int>(M), K, di.max_smem);
 }
 
+// Large Q8_0 matrices from M = 3 on: the tcgen05 prefill kernel (the
+// quantiser, then one 64-token tile per weight tile) instead of the
+// block-per-lane decode, whose per-lane activation reads grow with M
+// (QMM_DECODE_AUTO only).  Measured (rotating copies): from 2^24 weights at
+// M >= 5 (4096 x 4096 at M = 8: 15.6 against 20.5 us) and from 3 * 2^24 at
+// M = 3, 4 (4096 -> 14336: 27.8 against 40.4 us; 5120 x 5120: 20.8 against
+// 18.8 us, so smaller ones stay).
+bool q8_0_decode_on_prefill(int type, int64_t M, int64_t N, int64_t K) {
+    const int64_t min_weights = (M >= 5 ? int64_t(1) : int64_t(3)) << 24;
+    return type == QMM_Q8_0 && M >= QMM_TENSOR_MIN_M && M <= 8 && N * K >= min_weights &&
+           g_decode_path.load() == QMM_DECODE_AUTO && !g_no_mma_gemv && !g_force_mma_gemm &&
+           g_prefill_path.load() == QMM_PREFILL_AUTO && qk::gemm_tc_supported(type, N, K, M);
+}
+
 // Under QMM_DECODE_ROWS the row-per-lane kernel goes before the tensor-core one.
 bool rows_first() { return g_decode_path.load() == QMM_DECODE_ROWS; }
 
@@ -422,7 +436,8 @@ int qmm(int type, const void *W_blocks, int64_t N, int64_t K, const float *x, in
         g_launches.fetch_add(1);
         return QMM_OK;
     }
-    if (M <= 8 && !g_force_round_gemv && qk::gemv_sb_fits(type, static_cast<int>(M), K, di.max_smem)) {
+    if (M <= 8 && !g_force_round_gemv && qk::gemv_sb_fits(type, static_cast<int>(M), K, di.max_smem) &&
+        !q8_0_decode_on_prefill(type, M, N, K)) {
         e = qk::launch_gemv_sb(type, W_blocks, N, K, x, static_cast<int>(M), y, st, di.num_sms, di.max_smem,
                                di.status);
         if (e != cudaSuccess) return cuda_fail(e, "gemv launch");

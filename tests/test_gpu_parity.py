@@ -620,3 +620,23 @@ def test_attention_scores_on_q8_0_key_cache(cuda_lib, N, K, M):
     got = _run_qmm(cuda_lib, synth.Q8_0, W, N, K, x)
     want, A = O.qmm(synth.Q8_0, W, N, K, x)
     _assert_within_bound(got, want, A, f"scores N={N} K={K} M={M}")
+
+
+# Large Q8_0 matrices at 3 <= M <= 8 run on the tcgen05 prefill kernel (the
+# quantiser, then the GEMM); smaller ones stay on the block-per-lane decode.
+# Sampled rows against the oracle.
+@pytest.mark.parametrize("N,K,M,launches", [(4096, 4096, 5, 2), (4096, 4096, 8, 2), (12288, 4096, 3, 2),
+                                            (4096, 4096, 4, 1), (2048, 4096, 8, 1)])
+def test_q8_0_decode_route(cuda_lib, N, K, M, launches):
+    q = cuda_lib
+    W = synth.weights(synth.Q8_0, N, K, seed=N + M)
+    x = synth.activations(M, K, seed=K + M, outlier_frac=0.01)
+    before = q.qmm_launch_count()
+    y = q.qmm(synth.Q8_0, _dev(W), N, K, _dev(x)).cpu().numpy()
+    assert q.qmm_launch_count() - before == launches
+    assert q.qmm_device_status() == 0
+    rng = np.random.default_rng(N + K + M)
+    rows = np.unique(np.concatenate([np.arange(130), np.arange(N - 130, N), rng.choice(N, 200, replace=False)]))
+    rb = synth.row_bytes(synth.Q8_0, K)
+    yo, A = O.qmm(synth.Q8_0, W.reshape(N, rb)[rows], len(rows), K, x)
+    _assert_within_bound(y[:, rows], yo, A, f"Q8_0 N={N} K={K} M={M}")
